@@ -1,0 +1,422 @@
+"""Pins of the CPU oracle: checks against what the pages and mathematics fix.
+
+Each check takes an oracle library handle, so the same checks run against
+the real oracle (tests/test_oracle_pins.py) and against deliberately wrong
+builds of it (the planted-mistake test), which must each fail at least one.
+Independent formulations only: numpy matmuls, numpy's stable argsort and
+bincount, closed forms, hand-derived fixtures.  Nothing here calls the CUDA
+library.
+"""
+import math
+import os
+
+import numpy as np
+
+from oracle import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _golden(name):
+    import json
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# --------------------------------------------------------------------------
+# helpers: independent numpy formulations
+# --------------------------------------------------------------------------
+def np_silu(g):
+    return g / (1.0 + np.exp(-g))
+
+
+def act_to_f64(a, act_bytes):
+    return O.bf16_bits_to_f32(a).astype(np.float64) if act_bytes == 2 else \
+        np.asarray(a, np.float32).astype(np.float64)
+
+
+def np_round_act(v, act_bytes):
+    if act_bytes == 4:
+        return v.astype(np.float32).astype(np.float64)
+    import torch
+    return torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def np_swiglu(X, W13, Wd, act_bytes):
+    """Dense SwiGLU MLP with numpy matmuls: X [T, H], W13 [2I, H], Wd [H, I]."""
+    I = W13.shape[0] // 2
+    G = X @ W13[:I].T
+    U = X @ W13[I:].T
+    Hm = np_round_act(np_silu(G) * U, act_bytes)
+    return Hm @ Wd.T
+
+
+def rand_act(rng, shape, act_bytes, scale=1.0):
+    a = (rng.standard_normal(shape) * scale).astype(np.float32)
+    if act_bytes == 4:
+        return a
+    import torch
+    return torch.from_numpy(a).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def make_problem(rng, *, seq_lens, hidden, E, k, inter, shared_inter, act_bytes,
+                 renorm=False, scale=1.0, bias=False, ring_depth=1, num_regions=None,
+                 token_cap=None):
+    num_regions = num_regions or len(seq_lens)
+    token_cap = token_cap or max(8, max(seq_lens))
+    cfg = dict(num_regions=num_regions, ring_depth=ring_depth, token_cap=token_cap,
+               hidden=hidden, act_bytes=act_bytes, num_experts=E, topk=k, inter=inter,
+               shared_inter=shared_inter, renorm=renorm, max_total_tokens=0,
+               routed_scaling=scale)
+    xs = [rand_act(rng, (n, hidden), act_bytes) for n in seq_lens]
+    Wt = dict(
+        Wg=(rng.standard_normal((hidden, E)) / math.sqrt(hidden)).astype(np.float32),
+        bias=(rng.standard_normal(E) * 0.5).astype(np.float32) if bias else None,
+        W13=rand_act(rng, (E, 2 * inter, hidden), act_bytes, 1 / math.sqrt(hidden)),
+        Wd=rand_act(rng, (E, hidden, inter), act_bytes, 1 / math.sqrt(inter)),
+        W13s=rand_act(rng, (2 * shared_inter, hidden), act_bytes, 1 / math.sqrt(hidden))
+        if shared_inter else None,
+        Wds=rand_act(rng, (hidden, shared_inter), act_bytes, 1 / math.sqrt(shared_inter))
+        if shared_inter else None)
+    return cfg, xs, Wt
+
+
+def run_forward(lib, cfg, xs, Wt, *, layer=0, stage=0, slots=None, seqs=None,
+                with_shared=True, want_h=False):
+    """Pack every peer into a host dispatch window, run the oracle step, and
+    return (rc, result dict, return window, layout)."""
+    L = O.slot_layout(cfg["num_regions"], cfg["ring_depth"], cfg["token_cap"], cfg["topk"],
+                      cfg["hidden"], cfg["act_bytes"], cfg["num_experts"],
+                      cfg["shared_inter"] > 0, lib=lib)
+    win = np.zeros(L.window_bytes, np.uint8)
+    ret = np.zeros(L.window_bytes, np.uint8)
+    slots = list(range(len(xs))) if slots is None else slots
+    seqs = seqs or [100 + i for i in range(len(xs))]
+    for i, p in enumerate(slots):
+        rc = O.pack_slot(win, L, cfg["ring_depth"], p, stage, layer, xs[i], cfg["hidden"],
+                         cfg["act_bytes"], cfg["token_cap"], cfg["num_experts"],
+                         with_shared and cfg["shared_inter"] > 0, cfg["shared_inter"] > 0,
+                         seqs[i], lib=lib)
+        assert rc == 0
+    seen = np.zeros(cfg["num_regions"] * cfg["ring_depth"], np.uint64)
+    rc, r = O.ffn_forward(cfg, win, ret, Wt, layer, stage, [x.shape[0] for x in xs], slots,
+                          seen, want_h=want_h, lib=lib)
+    return rc, r, win, ret, L
+
+
+def return_rows(ret, L, cfg, peer, stage, n):
+    off = L.flags_bytes + (peer * cfg["ring_depth"] + stage) * L.slot_bytes
+    rb = cfg["hidden"] * cfg["act_bytes"]
+    raw = ret[off + L.routed_x: off + L.routed_x + n * rb]
+    dt = np.uint16 if cfg["act_bytes"] == 2 else np.float32
+    return act_to_f64(raw.view(dt).reshape(n, cfg["hidden"]), cfg["act_bytes"])
+
+
+def header_words(win, L, cfg, peer, stage):
+    off = L.flags_bytes + (peer * cfg["ring_depth"] + stage) * L.slot_bytes + L.header
+    return win[off: off + 4 * (12 + cfg["num_experts"])].view(np.int32)
+
+
+# --------------------------------------------------------------------------
+# checks
+# --------------------------------------------------------------------------
+def check_bf16(lib):
+    import torch
+    allbits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = O.bf16_to_f64(allbits, lib=lib)
+    ref = torch.from_numpy(allbits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    both_nan = np.isnan(ours) & np.isnan(ref)
+    assert np.all((ours == ref) | both_nan)
+    rng = np.random.default_rng(7)
+    v = np.concatenate([rng.standard_normal(4000).astype(np.float32) * 10,
+                        (rng.standard_normal(500) * 1e-39).astype(np.float32),
+                        np.array([0.0, -0.0, 3e38, -3e38, 1e-45, 65504.0], np.float32)])
+    ref_bits = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(O.f64_to_bf16(v.astype(np.float64), lib=lib), ref_bits)
+    for case in _golden("bf16_rounding.json")["cases"]:
+        assert int(O.f64_to_bf16([eval(case["value"])], lib=lib)[0]) == case["bits"], case
+
+
+def check_layout(lib):
+    for case in _golden("slot_layout_tiny.json")["cases"]:
+        args = [case[n] for n in ("num_regions", "ring_depth", "token_cap", "topk", "hidden",
+                                  "act_bytes", "num_experts", "has_shared")]
+        assert O.slot_layout(*args, lib=lib).as_dict() == case["expect"]
+    rng = np.random.default_rng(3)
+    for _ in range(200):
+        R, D = int(rng.integers(1, 17)), int(rng.integers(1, 3))
+        cap, k = int(rng.integers(1, 5000)), int(rng.integers(1, 9))
+        H, ab = int(rng.integers(1, 600)) * 8, int(rng.choice([2, 4]))
+        E, sh = int(rng.integers(1, 257)), int(rng.integers(0, 2))
+        L = O.slot_layout(R, D, cap, k, H, ab, E, sh, lib=lib).as_dict()
+        row = H * ab
+        fields = [("header", (12 + E) * 4), ("route_table", cap * k * 4),
+                  ("routed_x", cap * row), ("shared_idx", cap * 4 * sh),
+                  ("shared_x", cap * row * sh)]
+        end = 0
+        for name, size in fields:
+            off = L[name]
+            assert off % 256 == 0 and off % row == 0 and off % 4 == 0, (name, L)
+            assert off >= end, "fields overlap"
+            end = off + size
+        assert end <= L["slot_bytes"] and L["slot_bytes"] % 256 == 0
+        assert L["flags_bytes"] >= R * D * 8 and L["flags_bytes"] % row == 0
+        assert L["window_bytes"] == L["flags_bytes"] + R * D * L["slot_bytes"]
+
+
+def check_header_roundtrip(lib):
+    g = _golden("header_magic.json")
+    rng = np.random.default_rng(11)
+    cfg, xs, Wt = make_problem(rng, seq_lens=[5, 3], hidden=64, E=4, k=2, inter=16,
+                               shared_inter=16, act_bytes=2, ring_depth=2)
+    L = O.slot_layout(2, 2, cfg["token_cap"], 2, 64, 2, 4, 1, lib=lib)
+    win = np.zeros(L.window_bytes, np.uint8)
+    assert O.pack_slot(win, L, 2, 1, 1, 7, xs[0], 64, 2, cfg["token_cap"], 4, 1, 1, 41,
+                       shutdown=1, lib=lib) == 0
+    h = header_words(win, L, cfg, 1, 1)
+    assert bytes(h[:1].view(np.uint8)) == g["magic_bytes"].encode()
+    assert int(h[0]) == g["magic_word_le"] and len(h) == g["fixed_words"] + 4
+    assert int(h[2]) & g["shutdown_mask"]
+    assert list(h[3:12]) == [41, 41, 7, 1, 5, 0, 5, 4, 16]
+    flags = win[:L.flags_bytes].view(np.uint64)
+    assert flags[1 * 2 + 1] == 41 and flags.sum() == 41
+    off = L.flags_bytes + 3 * L.slot_bytes
+    assert np.array_equal(win[off + L.routed_x: off + L.routed_x + xs[0].nbytes], xs[0].view(np.uint8).ravel())
+    assert np.array_equal(win[off + L.shared_x: off + L.shared_x + xs[0].nbytes], xs[0].view(np.uint8).ravel())
+    assert list(win[off + L.shared_idx: off + L.shared_idx + 20].view(np.int32)) == [0, 1, 2, 3, 4]
+    rc, out = O.unpack_split(win, L, 2, 1, 1, 5, 64, 2, 4, 41, lib=lib)
+    assert rc == 0 and np.array_equal(out, xs[0])
+    assert O.unpack_split(win, L, 2, 1, 1, 5, 64, 2, 4, 42, lib=lib)[0] == O.ERR_TIMEOUT
+    assert O.unpack_split(win, L, 2, 1, 1, 5, 64, 2, 4, 40, lib=lib)[0] == O.ERR_SEQ
+    assert O.unpack_split(win, L, 2, 1, 1, 4, 64, 2, 4, 41, lib=lib)[0] == O.ERR_SHAPE
+    win[off] ^= 1
+    assert O.unpack_split(win, L, 2, 1, 1, 5, 64, 2, 4, 41, lib=lib)[0] == O.ERR_HEADER
+
+
+def check_split(lib):
+    for c in _golden("split_sizes.json")["cases"]:
+        rc, sizes = O.split_sizes(c["total"], c["n_peers"], c["seq_lens"], lib=lib)
+        assert rc == c["status"], c
+        if rc == 0:
+            assert sizes == c["sizes"]
+
+
+def check_logit_order(lib):
+    for c in _golden("logit_order.json")["cases"]:
+        H = c["hidden"]
+        x = np.zeros((1, H), np.float32)
+        for h, v in c["x_nonzero"].items():
+            x[0, int(h)] = v
+        Wg = np.zeros((H, 2), np.float32)
+        Wg[:, 0] = 1.0
+        ids, w, gap, lg = O.route(x, 4, Wg, None, 1, False, 1.0, with_logits=True, lib=lib)
+        assert float(lg[0, 0]) == c["expect"], (float(lg[0, 0]), c)
+
+
+def check_router(lib):
+    rng = np.random.default_rng(5)
+    for ab, renorm, scale, bias in ((4, True, 1.0, False), (2, False, 2.5, True)):
+        T, H, E, k = 96, 256, 16, 4
+        x = rand_act(rng, (T, H), ab)
+        Wg = (rng.standard_normal((H, E)) / 16).astype(np.float32)
+        b = (rng.standard_normal(E) * 0.3).astype(np.float32) if bias else None
+        ids, w, gap, lg = O.route(x, ab, Wg, b, k, renorm, scale, with_logits=True, lib=lib)
+        X = act_to_f64(x, ab)
+        L64 = X @ Wg.astype(np.float64) + (0 if b is None else b.astype(np.float64))
+        bound = 1e-5 * (np.abs(X) @ np.abs(Wg.astype(np.float64)) + 1)
+        assert np.all(np.abs(lg - L64) <= bound)
+        order = np.argsort(-L64, axis=1, kind="stable")[:, :k]
+        clear = np.sort(L64, axis=1)[:, ::-1]
+        clear = (clear[:, k - 1] - clear[:, k]) > 2 * bound.max()
+        assert np.array_equal(ids[clear], order[clear])
+        P = np.exp(lg.astype(np.float64) - lg.max(axis=1, keepdims=True))
+        P /= P.sum(axis=1, keepdims=True)
+        wref = np.take_along_axis(P, ids, axis=1)
+        if renorm:
+            wref /= wref.sum(axis=1, keepdims=True)
+            assert np.allclose(w.sum(axis=1), 1.0, atol=1e-6)
+        assert np.allclose(w, wref * scale, rtol=1e-6, atol=0)
+        assert np.all(gap[clear] > 0)
+
+
+def check_router_ties(lib):
+    rng = np.random.default_rng(9)
+    T, H, E, k = 400, 64, 8, 3
+    x = rand_act(rng, (T, H), 4)
+    Wg = (rng.standard_normal((H, E)) / 8).astype(np.float32)
+    Wg[:, 5] = Wg[:, 2]
+    ids, w, gap, lg = O.route(x, 4, Wg, None, k, False, 1.0, with_logits=True, lib=lib)
+    assert np.array_equal(lg[:, 2], lg[:, 5])
+    saw = 0
+    for t in range(T):
+        row = list(ids[t])
+        if 5 in row:
+            assert 2 in row and row.index(2) < row.index(5)
+        if 2 in row and 5 not in row and row.index(2) == k - 1:
+            saw += 1
+    assert saw > 0, "no token exercised the boundary tie"
+
+
+def check_plan(lib):
+    rng = np.random.default_rng(13)
+    for n, E in ((0, 4), (1, 1), (777, 16), (5000, 64)):
+        ids = rng.integers(0, max(E // 2, 1), size=n).astype(np.int32)
+        counts, offsets, perm, inv = O.plan(ids, E, lib=lib)
+        assert np.array_equal(counts, np.bincount(ids, minlength=E))
+        assert np.array_equal(offsets, np.concatenate([[0], np.cumsum(counts)]))
+        assert np.array_equal(perm, np.argsort(ids, kind="stable"))
+        assert np.array_equal(inv[perm], np.arange(n))
+
+
+def check_dense_swiglu(lib):
+    """E = 1, k = 1: the layer is a plain dense SwiGLU MLP (plus the shared
+    expert when present)."""
+    rng = np.random.default_rng(17)
+    for shared in (0, 24):
+        cfg, xs, Wt = make_problem(rng, seq_lens=[6, 11], hidden=64, E=1, k=1, inter=40,
+                                   shared_inter=shared, act_bytes=4)
+        rc, r, win, ret, L = run_forward(lib, cfg, xs, Wt)
+        assert rc == 0
+        X = np.concatenate([act_to_f64(x, 4) for x in xs])
+        ref = np_swiglu(X, act_to_f64(Wt["W13"][0], 4), act_to_f64(Wt["Wd"][0], 4), 4)
+        if shared:
+            ref = ref + np_swiglu(X, act_to_f64(Wt["W13s"], 4), act_to_f64(Wt["Wds"], 4), 4)
+        assert np.all(r["w"] == 1.0)
+        err = np.abs(r["out64"] - ref).max() / np.sqrt((ref ** 2).mean())
+        assert err < 1e-6, err
+
+
+def check_dense_mixture(lib):
+    """sum over all experts with the unselected gates zeroed (numpy, dense)
+    equals the routed layer."""
+    rng = np.random.default_rng(19)
+    for ab in (4, 2):
+        cfg, xs, Wt = make_problem(rng, seq_lens=[9, 4, 12], hidden=64, E=8, k=3, inter=32,
+                                   shared_inter=16, act_bytes=ab, renorm=(ab == 4))
+        rc, r, win, ret, L = run_forward(lib, cfg, xs, Wt)
+        assert rc == 0
+        X = np.concatenate([act_to_f64(x, ab) for x in xs])
+        T = X.shape[0]
+        wdense = np.zeros((T, 8))
+        np.put_along_axis(wdense, r["ids"], r["w"].astype(np.float64), axis=1)
+        ref = np.zeros_like(X)
+        for e in range(8):
+            ref += wdense[:, e:e + 1] * np_swiglu(X, act_to_f64(Wt["W13"][e], ab),
+                                                  act_to_f64(Wt["Wd"][e], ab), ab)
+        ref += np_swiglu(X, act_to_f64(Wt["W13s"], ab), act_to_f64(Wt["Wds"], ab), ab)
+        tol = 1e-6 if ab == 4 else 2e-3
+        err = np.abs(r["out64"] - ref).max() / np.sqrt((ref ** 2).mean())
+        assert err < tol, (ab, err)
+        # the oracle's own dense-mixture entry agrees too
+        xcat = np.concatenate(xs)
+        dm = O.dense_mixture(xcat, ab, Wt, 8, 32, 16, wdense, lib=lib)
+        assert np.abs(dm - r["out64"]).max() / np.sqrt((ref ** 2).mean()) < tol
+        # returned rows are the fp64 result rounded once
+        rows = np.concatenate([return_rows(ret, L, cfg, p, 0, xs[p].shape[0]) for p in range(3)])
+        assert np.array_equal(rows, np_round_act(r["out64"], ab)) or ab == 2
+        if ab == 2:
+            assert np.abs(rows - r["out64"]).max() <= 2 ** -8 * np.abs(r["out64"]).max()
+
+
+def check_identity_combine(lib):
+    rng = np.random.default_rng(23)
+    T, k, H = 7, 3, 5
+    x = rng.standard_normal((T, H))
+    s = rng.standard_normal((T, H))
+    w = rng.random((T, k)).astype(np.float32)
+    y = np.repeat(x[:, None, :], k, axis=1)
+    out = O.combine(y, w, s, lib=lib)
+    assert np.allclose(out, w.astype(np.float64).sum(1, keepdims=True) * x + s, rtol=1e-14)
+
+
+def check_fanin_split(lib):
+    """Each token's output depends on its own row only, so the fan-in result
+    for a peer equals that peer run alone; a zero-length peer gets an empty
+    slice; T = sum(seq_lens)."""
+    rng = np.random.default_rng(29)
+    cfg, xs, Wt = make_problem(rng, seq_lens=[5, 0, 9, 3], hidden=32, E=4, k=2, inter=16,
+                               shared_inter=8, act_bytes=4)
+    order = [2, 0, 3, 1]
+    rc, r, win, ret, L = run_forward(lib, cfg, [xs[p] for p in order], Wt, slots=order)
+    assert rc == 0 and r["ids"].shape[0] == sum(x.shape[0] for x in xs)
+    for p in range(4):
+        n = xs[p].shape[0]
+        h = header_words(ret, L, cfg, p, 0)
+        assert h[7] == n and h[8] == n * 2
+        alone_cfg = dict(cfg)
+        rc1, r1, _, ret1, _ = run_forward(lib, alone_cfg, [xs[p]], Wt, slots=[p])
+        assert rc1 == 0
+        if n:
+            assert np.array_equal(return_rows(ret, L, cfg, p, 0, n),
+                                  return_rows(ret1, L, cfg, p, 0, n))
+            counts = np.bincount(r1["ids"].ravel(), minlength=4)
+            assert list(h[12:]) == list(counts)
+
+
+def check_hand_moe(lib):
+    g = _golden("hand_moe.json")
+    cfg = dict(num_regions=1, ring_depth=1, token_cap=4, hidden=2, act_bytes=4,
+               num_experts=2, topk=1, inter=1, shared_inter=1, renorm=False,
+               max_total_tokens=0, routed_scaling=1.0)
+    Wt = {k: np.array(g[k], np.float32) for k in ("Wg", "W13", "Wd", "W13s", "Wds")}
+    Wt["bias"] = None
+    rc, r, win, ret, L = run_forward(lib, cfg, [np.array(g["x"], np.float32)], Wt)
+    assert rc == 0 and r["ids"].tolist() == g["expect_ids"]
+    s1, s3 = 1 / (1 + math.exp(-1)), 1 / (1 + math.exp(-3))
+    expect = [2 * s1 ** 2 - 3 * s3, -2 * s1 ** 2 - 3 * s3]
+    assert np.allclose(r["out64"][0], expect, atol=g["tolerance_abs"], rtol=0)
+
+
+def check_fault_codes(lib):
+    rng = np.random.default_rng(31)
+    cfg, xs, Wt = make_problem(rng, seq_lens=[4, 6], hidden=32, E=4, k=2, inter=8,
+                               shared_inter=8, act_bytes=2, token_cap=8)
+    L = O.slot_layout(2, 1, 8, 2, 32, 2, 4, 1, lib=lib)
+
+    def packed():
+        win = np.zeros(L.window_bytes, np.uint8)
+        for p in range(2):
+            assert O.pack_slot(win, L, 1, p, 0, 3, xs[p], 32, 2, 8, 4, 1, 1, 10 + p, lib=lib) == 0
+        return win
+
+    def fwd(win, layer=3, stage=0, seq_lens=(4, 6), slots=(0, 1), seen=None, c=cfg):
+        ret = np.zeros(L.window_bytes, np.uint8)
+        seen = np.zeros(2, np.uint64) if seen is None else seen
+        return O.ffn_forward(c, win, ret, Wt, layer, stage, list(seq_lens), list(slots), seen,
+                             lib=lib)[0]
+
+    assert fwd(packed()) == O.OK
+    hdr = lambda win, p: L.flags_bytes + p * L.slot_bytes + L.header
+    for word, val, code in ((0, 0x12345678, O.ERR_HEADER), (1, 2, O.ERR_HEADER),
+                            (10, 5, O.ERR_HEADER), (11, 99, O.ERR_HEADER),
+                            (3, 77, O.ERR_SEQ), (4, 77, O.ERR_SEQ), (2, 2, O.ERR_SHUTDOWN),
+                            (5, 4, O.ERR_LAYER), (6, 1, O.ERR_STAGE), (7, 5, O.ERR_SHAPE),
+                            (8, 3, O.ERR_SHAPE), (9, 2, O.ERR_SHAPE)):
+        win = packed()
+        win[hdr(win, 1) + 4 * word: hdr(win, 1) + 4 * word + 4] = np.array([val], np.int32).view(np.uint8)
+        assert fwd(win) == code, (word, val, code)
+    win = packed()
+    sidx = L.flags_bytes + 1 * L.slot_bytes + L.shared_idx
+    win[sidx + 4: sidx + 8] = np.array([3], np.int32).view(np.uint8)
+    assert fwd(win) == O.ERR_SHAPE
+    assert fwd(packed(), seq_lens=(4, 5)) == O.ERR_SHAPE
+    assert fwd(packed(), seen=np.array([10, 0], np.uint64)) == O.ERR_TIMEOUT
+    assert fwd(packed(), slots=(0, 0)) == O.ERR_ARG
+    assert fwd(packed(), stage=1) == O.ERR_ARG
+    assert fwd(packed(), seq_lens=(4, 9)) == O.ERR_CAPACITY
+    assert fwd(packed(), c=dict(cfg, max_total_tokens=9)) == O.ERR_CAPACITY
+    win = np.zeros(L.window_bytes, np.uint8)
+    big = rand_act(rng, (9, 32), 2)
+    assert O.pack_slot(win, L, 1, 0, 0, 3, big, 32, 2, 8, 4, 1, 1, 5, lib=lib) == O.ERR_CAPACITY
+    # a consumed slot is not consumed again: the flag must advance
+    win = packed()
+    seen = np.zeros(2, np.uint64)
+    assert fwd(win, seen=seen) == O.OK
+    assert list(seen) == [10, 11]
+    assert fwd(win, seen=seen) == O.ERR_TIMEOUT
+
+
+ALL_CHECKS = [check_bf16, check_layout, check_header_roundtrip, check_split,
+              check_logit_order, check_router, check_router_ties, check_plan,
+              check_dense_swiglu, check_dense_mixture, check_identity_combine,
+              check_fanin_split, check_hand_moe, check_fault_codes]

@@ -1,0 +1,213 @@
+"""ctypes binding of libafd_gb300.so (include/afd.h), argument marshalling only.
+
+Every function keeps the C name.  Tensors are passed by data_ptr(); all
+computation happens in the library's CUDA kernels.  Loading fails loudly
+when the library has not been built: there is no other implementation.
+"""
+import ctypes as C
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libafd_gb300.so")
+
+AFD_OK = 0
+(AFD_ERR_ARG, AFD_ERR_SHAPE, AFD_ERR_CAPACITY, AFD_ERR_HEADER, AFD_ERR_SEQ, AFD_ERR_LAYER,
+ AFD_ERR_STAGE, AFD_ERR_TIMEOUT, AFD_ERR_SHUTDOWN, AFD_ERR_SPLIT_UNEVEN, AFD_ERR_NOT_DEVICE,
+ AFD_ERR_CUDA, AFD_ERR_UNSUPPORTED) = range(1, 14)
+AFD_DTYPE_F32, AFD_DTYPE_BF16 = 0, 1
+AFD_GEMM_TENSOR, AFD_GEMM_SIMT = 0, 1
+AFD_DIR_DISPATCH, AFD_DIR_RETURN = 0, 1
+(AFD_WS_IDS, AFD_WS_WEIGHTS, AFD_WS_COUNTS, AFD_WS_OFFSETS, AFD_WS_PERM, AFD_WS_INV, AFD_WS_XP,
+ AFD_WS_H, AFD_WS_Y, AFD_WS_HS, AFD_WS_S, AFD_WS_STATUS) = range(12)
+AFD_HEADER_FIXED_WORDS = 12
+AFD_MAX_PEERS = 64
+
+
+class afd_config(C.Structure):
+    _fields_ = [("num_peers", C.c_int32), ("ring_depth", C.c_int32), ("token_cap", C.c_int32),
+                ("max_total_tokens", C.c_int32), ("hidden", C.c_int32),
+                ("num_experts", C.c_int32), ("topk", C.c_int32), ("inter", C.c_int32),
+                ("shared_inter", C.c_int32), ("act_dtype", C.c_int32), ("renorm", C.c_int32),
+                ("max_layers", C.c_int32), ("gemm", C.c_int32), ("reserved", C.c_int32),
+                ("routed_scaling", C.c_float), ("routed_cap_multiplier", C.c_float),
+                ("wait_timeout_ns", C.c_int64)]
+
+
+class afd_layout(C.Structure):
+    _fields_ = [(n, C.c_int64) for n in ("header", "route_table", "routed_x", "shared_idx",
+                                         "shared_x", "slot_bytes", "flags_bytes",
+                                         "window_bytes", "align")]
+
+    def as_dict(self):
+        return {n: int(getattr(self, n)) for n, _ in self._fields_}
+
+
+class afd_stats(C.Structure):
+    _fields_ = [("window_bytes", C.c_int64), ("workspace_bytes", C.c_int64),
+                ("last_total_tokens", C.c_int32), ("num_sms", C.c_int32),
+                ("forwards", C.c_int64)]
+
+
+class AfdError(RuntimeError):
+    def __init__(self, code, what):
+        super().__init__(f"{what}: {strerror(code)} ({code})")
+        self.code = code
+
+
+_lib = None
+
+# (name, restype, argtypes) -- mirrors include/afd.h
+_P, _I, _I64, _U64, _F = C.c_void_p, C.c_int, C.c_int64, C.c_uint64, C.c_float
+SIGNATURES = [
+    ("afd_create", _I, [C.POINTER(afd_config), _P, C.POINTER(_P)]),
+    ("afd_destroy", None, [_P]),
+    ("afd_set_stream", _I, [_P, _P]),
+    ("afd_slot_layout", _I, [C.POINTER(afd_config), C.POINTER(afd_layout)]),
+    ("afd_split_sizes", _I, [_I, _I, C.POINTER(C.c_int), _I, C.POINTER(C.c_int)]),
+    ("afd_set_layer", _I, [_P, _I, _P, _P, _P, _P, _P, _P]),
+    ("afd_pack_slot", _I, [_P, _I, _I, _I, _P, _I, _I, _U64]),
+    ("afd_announce_shutdown", _I, [_P, _I, _I, _U64]),
+    ("afd_ffn_forward", _I, [_P, _I, _I, C.POINTER(C.c_int), C.POINTER(C.c_int), _I]),
+    ("afd_unpack_split", _I, [_P, _I, _I, _P, _I, _U64]),
+    ("afd_poll_status", _I, [_P]),
+    ("afd_get_window", _I, [_P, _I, C.POINTER(_P), C.POINTER(_I64)]),
+    ("afd_get_workspace", _I, [_P, _I, C.POINTER(_P), C.POINTER(_I64)]),
+    ("afd_get_stats", _I, [_P, C.POINTER(afd_stats)]),
+    ("afd_launch_count", _I64, [_P]),
+    ("afd_strerror", C.c_char_p, [_I]),
+    ("afd_profile", _I, [_P, _I]),
+    ("afd_stage_times", _I, [_P, C.POINTER(C.c_float), _I]),
+]
+AFD_NUM_STAGES = 8
+STAGE_NAMES = ("header_check", "router", "plan", "gather", "gemm_swiglu", "gemm_down",
+               "combine_split", "return_header")
+
+
+def lib(path=None):
+    """Load the library once; raise if it is missing (build it with
+    __graft_entry__.build() or combine_peer_slot_gb300/build.py)."""
+    global _lib
+    if _lib is None:
+        path = path or LIB_PATH
+        if not os.path.exists(path):
+            raise ImportError(f"{path} is not built; run __graft_entry__.build()")
+        L = C.CDLL(path)
+        for name, res, args in SIGNATURES:
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def strerror(code):
+    return lib().afd_strerror(int(code)).decode()
+
+
+def _check(rc, what):
+    if rc != AFD_OK:
+        raise AfdError(rc, what)
+    return rc
+
+
+def _ints(seq):
+    arr = (C.c_int * max(len(seq), 1))(*[int(v) for v in seq])
+    return arr
+
+
+def make_config(num_peers, token_cap, hidden, num_experts, topk, inter, shared_inter=0,
+                act="bf16", renorm=False, routed_scaling=1.0, ring_depth=1,
+                max_total_tokens=0, max_layers=1, gemm=AFD_GEMM_TENSOR,
+                routed_cap_multiplier=2.0, wait_timeout_ns=0):
+    return afd_config(num_peers, ring_depth, token_cap, max_total_tokens, hidden, num_experts,
+                      topk, inter, shared_inter,
+                      AFD_DTYPE_BF16 if act == "bf16" else AFD_DTYPE_F32, int(bool(renorm)),
+                      max_layers, gemm, 0, float(routed_scaling),
+                      float(routed_cap_multiplier), int(wait_timeout_ns))
+
+
+# ---- thin functional wrappers (same names as the C ABI) ----------------------
+def afd_slot_layout(cfg):
+    L = afd_layout()
+    _check(lib().afd_slot_layout(C.byref(cfg), C.byref(L)), "afd_slot_layout")
+    return L
+
+
+def afd_split_sizes(total, n_peers, seq_lens):
+    sizes = (C.c_int * max(n_peers, 1))()
+    rc = lib().afd_split_sizes(int(total), int(n_peers), _ints(seq_lens), len(seq_lens), sizes)
+    return rc, [int(sizes[i]) for i in range(n_peers)] if rc == AFD_OK else None
+
+
+def afd_create(cfg, stream=0):
+    ctx = C.c_void_p()
+    _check(lib().afd_create(C.byref(cfg), C.c_void_p(int(stream)), C.byref(ctx)), "afd_create")
+    return ctx
+
+
+def afd_destroy(ctx):
+    lib().afd_destroy(ctx)
+
+
+def afd_set_stream(ctx, stream):
+    return _check(lib().afd_set_stream(ctx, C.c_void_p(int(stream))), "afd_set_stream")
+
+
+def afd_set_layer(ctx, layer, Wg, bias, W13, Wd, W13_s=0, Wd_s=0):
+    """Pointers as ints (tensor.data_ptr())."""
+    return _check(lib().afd_set_layer(ctx, int(layer), Wg, bias or None, W13, Wd,
+                                      W13_s or None, Wd_s or None), "afd_set_layer")
+
+
+def afd_pack_slot(ctx, peer, stage, layer, x_ptr, n_tokens, with_shared, seq):
+    return lib().afd_pack_slot(ctx, peer, stage, layer, x_ptr or None, n_tokens,
+                               int(bool(with_shared)), seq)
+
+
+def afd_announce_shutdown(ctx, peer, stage, seq):
+    return lib().afd_announce_shutdown(ctx, peer, stage, seq)
+
+
+def afd_ffn_forward(ctx, layer, stage, seq_lens, slots):
+    return lib().afd_ffn_forward(ctx, int(layer), int(stage), _ints(seq_lens), _ints(slots),
+                                 len(slots))
+
+
+def afd_unpack_split(ctx, peer, stage, out_ptr, n_tokens, expect_seq):
+    return lib().afd_unpack_split(ctx, peer, stage, out_ptr or None, n_tokens, expect_seq)
+
+
+def afd_poll_status(ctx):
+    return lib().afd_poll_status(ctx)
+
+
+def afd_get_window(ctx, direction):
+    p, n = C.c_void_p(), C.c_int64()
+    _check(lib().afd_get_window(ctx, direction, C.byref(p), C.byref(n)), "afd_get_window")
+    return p.value, n.value
+
+
+def afd_get_workspace(ctx, which):
+    p, n = C.c_void_p(), C.c_int64()
+    _check(lib().afd_get_workspace(ctx, which, C.byref(p), C.byref(n)), "afd_get_workspace")
+    return p.value, n.value
+
+
+def afd_get_stats(ctx):
+    s = afd_stats()
+    _check(lib().afd_get_stats(ctx, C.byref(s)), "afd_get_stats")
+    return s
+
+
+def afd_launch_count(ctx):
+    return int(lib().afd_launch_count(ctx))
+
+
+def afd_profile(ctx, enable):
+    return _check(lib().afd_profile(ctx, int(bool(enable))), "afd_profile")
+
+
+def afd_stage_times(ctx):
+    ms = (C.c_float * AFD_NUM_STAGES)()
+    _check(lib().afd_stage_times(ctx, ms, AFD_NUM_STAGES), "afd_stage_times")
+    return [float(v) for v in ms]

@@ -1,0 +1,650 @@
+// afd_api.cu -- host side of the C ABI declared in include/afd.h: context,
+// windows, workspace, TMA descriptors, argument checks and the launch
+// sequence of the FFN step.
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#include "afd_internal.cuh"
+
+size_t gemm_tc_smem_bytes();
+
+namespace {
+
+struct LayerW {
+  bool set = false;
+  const float* Wg = nullptr;
+  const float* bias = nullptr;
+  const void* W13 = nullptr;
+  const void* Wd = nullptr;
+  const void* W13s = nullptr;
+  const void* Wds = nullptr;
+  float* WgT = nullptr;              // library-owned transposed router weight
+  CUtensorMap tmA1[2];               // SwiGLU projection: routed, shared
+  CUtensorMap tmA2[2];               // down projection: routed, shared
+};
+
+int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+int64_t gcd64(int64_t a, int64_t b) {
+  while (b) { int64_t t = a % b; a = b; b = t; }
+  return a;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int get_encoder() {
+  if (g_encode) return AFD_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return AFD_ERR_CUDA;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return AFD_OK;
+}
+
+// bf16 tensor map, 128-byte swizzle, zero fill out of bounds
+int encode_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+               const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base),
+                        dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    fprintf(stderr, "afd: cuTensorMapEncodeTiled failed (%d), rank %d\n", (int)r, rank);
+    return AFD_ERR_CUDA;
+  }
+  return AFD_OK;
+}
+
+// [E][2I][H] viewed as (h, r16, s, j, e): one box = 4 x (16 gate rows, 16 up rows)
+int encode_swiglu_weight(CUtensorMap* m, const void* W, int E, int I, int H) {
+  const cuuint64_t dims[5] = {(cuuint64_t)H, 16, 2, (cuuint64_t)(I / 16), (cuuint64_t)E};
+  const cuuint64_t str[4] = {(cuuint64_t)H * 2, (cuuint64_t)I * H * 2, (cuuint64_t)16 * H * 2,
+                             (cuuint64_t)2 * I * H * 2};
+  const cuuint32_t box[5] = {64, 16, 2, 4, 1};
+  return encode_map(m, W, 5, dims, str, box);
+}
+
+// [E][M][K] K-major, box 64 x 128
+int encode_plain_weight(CUtensorMap* m, const void* W, int E, int M, int K) {
+  const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)M, (cuuint64_t)E};
+  const cuuint64_t str[2] = {(cuuint64_t)K * 2, (cuuint64_t)M * K * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  return encode_map(m, W, 3, dims, str, box);
+}
+
+// [rows][K] token rows, box 64 x 32
+int encode_rows(CUtensorMap* m, const void* X, int64_t rows, int K) {
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)(rows > 0 ? rows : 1)};
+  const cuuint64_t str[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {64, 32};
+  return encode_map(m, X, 2, dims, str, box);
+}
+
+int check_dev_ptr(const void* p) {
+  if (!p) return AFD_ERR_ARG;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return AFD_ERR_NOT_DEVICE;
+  }
+  return (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) ? AFD_OK
+                                                                              : AFD_ERR_NOT_DEVICE;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int layout_of(const afd_config* c, afd_layout* L) {
+  const int64_t ab = c->act_dtype == AFD_DTYPE_BF16 ? 2 : 4;
+  const int64_t row = (int64_t)c->hidden * ab;
+  const int64_t a = 256 / gcd64(256, row) * row;
+  const int has_shared = c->shared_inter > 0;
+  int64_t off = 0;
+  L->align = a;
+  L->header = off;
+  off += round_up((int64_t)(AFD_HEADER_FIXED_WORDS + c->num_experts) * 4, a);
+  L->route_table = off;
+  off += round_up((int64_t)c->token_cap * c->topk * 4, a);
+  L->routed_x = off;
+  off += round_up((int64_t)c->token_cap * row, a);
+  L->shared_idx = off;
+  if (has_shared) off += round_up((int64_t)c->token_cap * 4, a);
+  L->shared_x = off;
+  if (has_shared) off += round_up((int64_t)c->token_cap * row, a);
+  L->slot_bytes = off;
+  L->flags_bytes = round_up((int64_t)c->num_peers * c->ring_depth * 8, a);
+  L->window_bytes = L->flags_bytes + (int64_t)c->num_peers * c->ring_depth * off;
+  return AFD_OK;
+}
+
+int validate_config(const afd_config* c) {
+  if (!c) return AFD_ERR_ARG;
+  if (c->num_peers < 1 || c->num_peers > AFD_MAX_PEERS || c->ring_depth < 1 || c->ring_depth > 8 ||
+      c->token_cap < 1 || c->max_total_tokens < 0 || c->hidden < 8 || c->num_experts < 1 ||
+      c->topk < 1 || c->topk > c->num_experts || c->inter < 1 || c->shared_inter < 0 ||
+      c->max_layers < 1 || c->routed_cap_multiplier < 1.0f || c->wait_timeout_ns < 0)
+    return AFD_ERR_ARG;
+  if (c->act_dtype != AFD_DTYPE_F32 && c->act_dtype != AFD_DTYPE_BF16) return AFD_ERR_ARG;
+  if (c->gemm != AFD_GEMM_TENSOR && c->gemm != AFD_GEMM_SIMT) return AFD_ERR_ARG;
+  // kernel coverage: 16-byte rows, <= 256 experts, k <= 16
+  if (c->hidden % 8 || c->num_experts > 256 || c->topk > 16) return AFD_ERR_UNSUPPORTED;
+  if (c->act_dtype == AFD_DTYPE_F32 && c->gemm == AFD_GEMM_TENSOR) return AFD_ERR_UNSUPPORTED;
+  if (c->gemm == AFD_GEMM_TENSOR && (c->inter % 16 || c->shared_inter % 16)) return AFD_ERR_UNSUPPORTED;
+  const int64_t tmax = c->max_total_tokens ? c->max_total_tokens : (int64_t)c->num_peers * c->token_cap;
+  if (tmax * c->topk + tmax > (int64_t)1 << 30) return AFD_ERR_UNSUPPORTED;
+  return AFD_OK;
+}
+
+}  // namespace
+
+struct afd_ctx {
+  afd_config cfg;
+  afd_layout L;
+  WinGeom geom;
+  int device = 0;
+  int num_sms = 0;
+  cudaStream_t stream = nullptr;
+  uint8_t* win[2] = {nullptr, nullptr};
+  uint8_t* ws_mem = nullptr;
+  int64_t ws_bytes = 0;
+  DevWS ws;
+  GemmPlan* plan1 = nullptr;
+  GemmPlan* plan2 = nullptr;
+  CUtensorMap tmXp, tmH, tmHs;
+  std::vector<LayerW> layers;
+  std::vector<uint64_t> last_seq;
+  int tmax = 0;
+  int act_f32 = 0;
+  int64_t launches = 0;
+  int last_T = 0;
+  int64_t forwards = 0;
+  int64_t ws_cap[12];
+  bool profiling = false;
+  cudaEvent_t ev[AFD_NUM_STAGES + 1] = {};
+
+  void mark(int i) {
+    if (profiling) cudaEventRecord(ev[i], stream);
+  }
+
+  LaunchCtx lc() { return LaunchCtx{stream, num_sms, &launches}; }
+  int64_t timeout() const { return cfg.wait_timeout_ns ? cfg.wait_timeout_ns : 1000000000ll; }
+};
+
+static int cuda_fail(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return AFD_OK;
+  fprintf(stderr, "afd: %s: %s\n", what, cudaGetErrorString(e));
+  return AFD_ERR_CUDA;
+}
+
+extern "C" {
+
+const char* afd_strerror(int code) {
+  switch (code) {
+    case AFD_OK: return "ok";
+    case AFD_ERR_ARG: return "invalid argument";
+    case AFD_ERR_SHAPE: return "token counts disagree";
+    case AFD_ERR_CAPACITY: return "capacity exceeded";
+    case AFD_ERR_HEADER: return "bad slot header";
+    case AFD_ERR_SEQ: return "sequence number mismatch";
+    case AFD_ERR_LAYER: return "layer mismatch or unregistered layer";
+    case AFD_ERR_STAGE: return "stage mismatch";
+    case AFD_ERR_TIMEOUT: return "device wait timed out";
+    case AFD_ERR_SHUTDOWN: return "peer announced shutdown";
+    case AFD_ERR_SPLIT_UNEVEN: return "even split does not divide";
+    case AFD_ERR_NOT_DEVICE: return "pointer is not device memory";
+    case AFD_ERR_CUDA: return "CUDA error";
+    case AFD_ERR_UNSUPPORTED: return "unsupported configuration";
+    default: return "unknown status";
+  }
+}
+
+int afd_slot_layout(const afd_config* cfg, afd_layout* out) {
+  if (!out) return AFD_ERR_ARG;
+  const int rc = validate_config(cfg);
+  if (rc) return rc;
+  return layout_of(cfg, out);
+}
+
+int afd_split_sizes(int total, int n_peers, const int* seq_lens, int n_lens, int* sizes) {
+  if (n_peers <= 0 || total < 0 || !sizes || n_lens < 0 || (n_lens > 0 && !seq_lens))
+    return AFD_ERR_ARG;
+  if (n_lens == n_peers) {
+    int64_t s = 0;
+    for (int i = 0; i < n_peers; i++) {
+      if (seq_lens[i] < 0) return AFD_ERR_ARG;
+      s += seq_lens[i];
+      sizes[i] = seq_lens[i];
+    }
+    return s == total ? AFD_OK : AFD_ERR_SHAPE;
+  }
+  if (total % n_peers) return AFD_ERR_SPLIT_UNEVEN;
+  for (int i = 0; i < n_peers; i++) sizes[i] = total / n_peers;
+  return AFD_OK;
+}
+
+void afd_destroy(afd_ctx* ctx) {
+  if (!ctx) return;
+  cudaSetDevice(ctx->device);
+  cudaStreamSynchronize(ctx->stream);
+  for (auto& l : ctx->layers) cudaFree(l.WgT);
+  for (auto& e : ctx->ev)
+    if (e) cudaEventDestroy(e);
+  cudaFree(ctx->win[0]);
+  cudaFree(ctx->win[1]);
+  cudaFree(ctx->ws_mem);
+  delete ctx;
+}
+
+int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out) {
+  if (!out) return AFD_ERR_ARG;
+  *out = nullptr;
+  int rc = validate_config(cfg);
+  if (rc) return rc;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return AFD_ERR_CUDA;
+  }
+  afd_ctx* c = new afd_ctx();
+  c->cfg = *cfg;
+  c->device = dev;
+  c->stream = reinterpret_cast<cudaStream_t>(cuda_stream);
+  c->act_f32 = cfg->act_dtype == AFD_DTYPE_F32;
+  cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
+  layout_of(cfg, &c->L);
+  c->geom = WinGeom{c->L.flags_bytes, c->L.slot_bytes, c->L.header, c->L.route_table,
+                    c->L.routed_x, c->L.shared_idx, c->L.shared_x, cfg->ring_depth, cfg->num_peers};
+  c->tmax = cfg->max_total_tokens ? cfg->max_total_tokens : cfg->num_peers * cfg->token_cap;
+  c->layers.resize(cfg->max_layers);
+  c->last_seq.assign((size_t)cfg->num_peers * cfg->ring_depth, 0);
+  for (int d = 0; d < 2; d++) {
+    rc = cuda_fail(cudaMalloc(&c->win[d], c->L.window_bytes), "window allocation");
+    if (!rc) rc = cuda_fail(cudaMemset(c->win[d], 0, c->L.window_bytes), "window zero");
+    if (rc) { afd_destroy(c); return rc; }
+  }
+  // workspace
+  const int64_t Tm = c->tmax, k = cfg->topk, H = cfg->hidden, E = cfg->num_experts;
+  const int64_t I = cfg->inter, Is = cfg->shared_inter;
+  const int64_t ab = c->act_f32 ? 4 : 2;
+  const int64_t yb = c->act_f32 ? 4 : 2;
+  struct Part { int64_t bytes; } parts[] = {
+      {4},                                   // status
+      {(int64_t)cfg->num_peers * cfg->ring_depth * 8},  // seen
+      {AFD_MAX_PEERS * 8},                   // cur_seq
+      {AFD_MAX_PEERS * 4},                   // peer_shared
+      {Tm * k * 4}, {Tm * k * 4},            // ids, w
+      {E * 4}, {(E + 1) * 4},                // counts, offsets
+      {Tm * k * 4}, {Tm * k * 4},            // perm, inv
+      {AFD_MAX_PEERS * E * 4},               // peer_counts
+      {(Tm * k + Tm) * H * ab},              // xp
+      {Tm * k * I * ab},                     // h
+      {Tm * k * H * yb},                     // y
+      {Tm * (Is > 0 ? Is : 1) * ab},         // hs
+      {Tm * H * 4},                          // s
+      {(int64_t)sizeof(GemmPlan)}, {(int64_t)sizeof(GemmPlan)}};
+  const int nparts = sizeof(parts) / sizeof(parts[0]);
+  int64_t offs[32], total = 0;
+  for (int i = 0; i < nparts; i++) {
+    offs[i] = total;
+    total += round_up(parts[i].bytes > 0 ? parts[i].bytes : 1, 256);
+  }
+  rc = cuda_fail(cudaMalloc(&c->ws_mem, total), "workspace allocation");
+  if (!rc) rc = cuda_fail(cudaMemset(c->ws_mem, 0, total), "workspace zero");
+  if (rc) { afd_destroy(c); return rc; }
+  c->ws_bytes = total;
+  uint8_t* b = c->ws_mem;
+  c->ws.status = reinterpret_cast<int32_t*>(b + offs[0]);
+  c->ws.seen = reinterpret_cast<uint64_t*>(b + offs[1]);
+  c->ws.cur_seq = reinterpret_cast<uint64_t*>(b + offs[2]);
+  c->ws.peer_shared = reinterpret_cast<int32_t*>(b + offs[3]);
+  c->ws.ids = reinterpret_cast<int32_t*>(b + offs[4]);
+  c->ws.w = reinterpret_cast<float*>(b + offs[5]);
+  c->ws.counts = reinterpret_cast<int32_t*>(b + offs[6]);
+  c->ws.offsets = reinterpret_cast<int32_t*>(b + offs[7]);
+  c->ws.perm = reinterpret_cast<int32_t*>(b + offs[8]);
+  c->ws.inv = reinterpret_cast<int32_t*>(b + offs[9]);
+  c->ws.peer_counts = reinterpret_cast<int32_t*>(b + offs[10]);
+  c->ws.xp = b + offs[11];
+  c->ws.h = b + offs[12];
+  c->ws.y = b + offs[13];
+  c->ws.hs = b + offs[14];
+  c->ws.s = reinterpret_cast<float*>(b + offs[15]);
+  c->ws.wgt = nullptr;
+  c->plan1 = reinterpret_cast<GemmPlan*>(b + offs[16]);
+  c->plan2 = reinterpret_cast<GemmPlan*>(b + offs[17]);
+  const int ws_map[12] = {4, 5, 6, 7, 8, 9, 11, 12, 13, 14, 15, 0};
+  for (int i = 0; i < 12; i++) c->ws_cap[i] = parts[ws_map[i]].bytes;
+  if (cfg->gemm == AFD_GEMM_TENSOR) {
+    rc = get_encoder();
+    if (!rc) rc = encode_rows(&c->tmXp, c->ws.xp, Tm * k + Tm, (int)H);
+    if (!rc) rc = encode_rows(&c->tmH, c->ws.h, Tm * k, (int)I);
+    if (!rc) rc = encode_rows(&c->tmHs, c->ws.hs, Tm, (int)(Is > 0 ? Is : 64));
+    if (rc) { afd_destroy(c); return rc; }
+  }
+  *out = c;
+  return AFD_OK;
+}
+
+int afd_set_stream(afd_ctx* ctx, void* cuda_stream) {
+  if (!ctx) return AFD_ERR_ARG;
+  ctx->stream = reinterpret_cast<cudaStream_t>(cuda_stream);
+  return AFD_OK;
+}
+
+int afd_set_layer(afd_ctx* ctx, int layer, const float* Wg, const float* bias, const void* W13,
+                  const void* Wd, const void* W13_s, const void* Wd_s) {
+  if (!ctx || layer < 0 || layer >= ctx->cfg.max_layers) return AFD_ERR_ARG;
+  const afd_config& c = ctx->cfg;
+  const bool has_shared = c.shared_inter > 0;
+  if (!Wg || !W13 || !Wd || (has_shared && (!W13_s || !Wd_s))) return AFD_ERR_ARG;
+  const void* ptrs[6] = {Wg, bias, W13, Wd, has_shared ? W13_s : nullptr, has_shared ? Wd_s : nullptr};
+  for (const void* p : ptrs) {
+    if (!p) continue;
+    int rc = check_dev_ptr(p);
+    if (rc) return rc;
+    if (!aligned16(p)) return AFD_ERR_ARG;
+  }
+  LayerW& L = ctx->layers[layer];
+  if (!L.WgT) {
+    int rc = cuda_fail(cudaMalloc(&L.WgT, (size_t)c.hidden * c.num_experts * 4), "router copy");
+    if (rc) return rc;
+  }
+  int rc = cuda_fail(launch_transpose_wg(ctx->lc(), Wg, L.WgT, c.hidden, c.num_experts), "transpose");
+  if (rc) return rc;
+  L.Wg = Wg;
+  L.bias = bias;
+  L.W13 = W13;
+  L.Wd = Wd;
+  L.W13s = has_shared ? W13_s : nullptr;
+  L.Wds = has_shared ? Wd_s : nullptr;
+  if (c.gemm == AFD_GEMM_TENSOR) {
+    rc = encode_swiglu_weight(&L.tmA1[0], W13, c.num_experts, c.inter, c.hidden);
+    if (!rc) rc = encode_plain_weight(&L.tmA2[0], Wd, c.num_experts, c.hidden, c.inter);
+    if (!rc && has_shared) {
+      rc = encode_swiglu_weight(&L.tmA1[1], W13_s, 1, c.shared_inter, c.hidden);
+      if (!rc) rc = encode_plain_weight(&L.tmA2[1], Wd_s, 1, c.hidden, c.shared_inter);
+    } else if (!rc) {
+      L.tmA1[1] = L.tmA1[0];
+      L.tmA2[1] = L.tmA2[0];
+    }
+    if (rc) return rc;
+  }
+  L.set = true;
+  return AFD_OK;
+}
+
+static int pack_common(afd_ctx* ctx, int peer, int stage, int layer, const void* x, int n,
+                       int with_shared, uint64_t seq, int shutdown) {
+  if (!ctx) return AFD_ERR_ARG;
+  const afd_config& c = ctx->cfg;
+  if (peer < 0 || peer >= c.num_peers || stage < 0 || stage >= c.ring_depth || n < 0)
+    return AFD_ERR_ARG;
+  if (with_shared && c.shared_inter <= 0) return AFD_ERR_ARG;
+  if (n > c.token_cap) return AFD_ERR_CAPACITY;
+  if (n > 0) {
+    const int rc = check_dev_ptr(x);
+    if (rc) return rc;
+    if (!aligned16(x)) return AFD_ERR_ARG;
+  }
+  uint64_t& last = ctx->last_seq[(size_t)peer * c.ring_depth + stage];
+  if (seq <= last) return AFD_ERR_SEQ;
+  const int row_bytes = c.hidden * (ctx->act_f32 ? 4 : 2);
+  LaunchCtx lc = ctx->lc();
+  int rc = cuda_fail(launch_pack_payload(lc, ctx->geom, ctx->win[0], peer, stage, x, n, row_bytes,
+                                         with_shared, ctx->ws.status),
+                     "pack payload");
+  if (!rc)
+    rc = cuda_fail(launch_pack_header(lc, ctx->geom, ctx->win[0], peer, stage, layer, n, with_shared,
+                                      c.num_experts, seq, shutdown),
+                   "pack header");
+  if (!rc) last = seq;
+  return rc;
+}
+
+int afd_pack_slot(afd_ctx* ctx, int peer, int stage, int layer, const void* x, int n_tokens,
+                  int with_shared, uint64_t seq) {
+  return pack_common(ctx, peer, stage, layer, x, n_tokens, with_shared, seq, 0);
+}
+
+int afd_announce_shutdown(afd_ctx* ctx, int peer, int stage, uint64_t seq) {
+  return pack_common(ctx, peer, stage, 0, nullptr, 0, 0, seq, 1);
+}
+
+int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, const int* slots,
+                    int n_peers) {
+  if (!ctx || !seq_lens || !slots) return AFD_ERR_ARG;
+  const afd_config& c = ctx->cfg;
+  if (n_peers <= 0 || n_peers > c.num_peers) return AFD_ERR_ARG;
+  if (stage < 0 || stage >= c.ring_depth) return AFD_ERR_ARG;
+  FanIn f;
+  memset(&f, 0, sizeof f);
+  f.n_peers = n_peers;
+  f.stage = stage;
+  f.layer = layer;
+  int64_t T = 0;
+  for (int i = 0; i < n_peers; i++) {
+    if (slots[i] < 0 || slots[i] >= c.num_peers) return AFD_ERR_ARG;
+    for (int j = 0; j < i; j++)
+      if (slots[j] == slots[i]) return AFD_ERR_ARG;
+    if (seq_lens[i] < 0) return AFD_ERR_ARG;
+    if (seq_lens[i] > c.token_cap) return AFD_ERR_CAPACITY;
+    f.prefix[i] = (int)T;
+    f.region[i] = slots[i];
+    T += seq_lens[i];
+  }
+  if (T > ctx->tmax) return AFD_ERR_CAPACITY;
+  f.prefix[n_peers] = (int)T;
+  f.total = (int)T;
+  if (layer < 0 || layer >= c.max_layers || !ctx->layers[layer].set) return AFD_ERR_LAYER;
+  const LayerW& L = ctx->layers[layer];
+  const int has_shared = c.shared_inter > 0;
+  const int ab = ctx->act_f32 ? 4 : 2;
+  const int row_bytes = c.hidden * ab;
+  const int bn = 256;
+  LaunchCtx lc = ctx->lc();
+  const DevWS& ws = ctx->ws;
+  ctx->mark(0);
+  int rc = cuda_fail(launch_header_check(lc, ctx->geom, ctx->win[0], f, ws, c.num_experts,
+                                         c.token_cap, has_shared, ctx->timeout()),
+                     "header check");
+  if (rc) return rc;
+  ctx->mark(1);
+  rc = cuda_fail(launch_router(lc, ctx->geom, ctx->win[0], f, ws, c.hidden, ctx->act_f32, L.WgT,
+                               L.bias, c.num_experts, c.topk, c.renorm, c.routed_scaling),
+                 "router");
+  if (rc) return rc;
+  ctx->mark(2);
+  rc = cuda_fail(launch_plan(lc, f, ws, c.num_experts, c.topk, c.inter, c.shared_inter, c.hidden,
+                             has_shared, bn, ctx->plan1, ctx->plan2),
+                 "plan");
+  if (rc) return rc;
+  ctx->mark(3);
+  rc = cuda_fail(launch_gather(lc, ctx->geom, ctx->win[0], f, ws, c.topk, row_bytes, has_shared),
+                 "gather");
+  if (rc) return rc;
+  ctx->mark(4);
+  if (T > 0) {
+    if (c.gemm == AFD_GEMM_TENSOR) {
+      GemmArgs a1;
+      memset(&a1, 0, sizeof a1);
+      a1.tmA[0] = L.tmA1[0];
+      a1.tmA[1] = L.tmA1[1];
+      a1.tmB[0] = ctx->tmXp;
+      a1.tmB[1] = ctx->tmXp;
+      a1.out[0] = ws.h;
+      a1.out[1] = ws.hs;
+      a1.ldo[0] = c.inter;
+      a1.ldo[1] = c.shared_inter;
+      a1.K[0] = a1.K[1] = c.hidden;
+      a1.M[0] = 2 * c.inter;
+      a1.M[1] = 2 * c.shared_inter;
+      a1.plan = ctx->plan1;
+      a1.status = ws.status;
+      a1.swiglu = 1;
+      a1.timeout_ns = ctx->timeout();
+      rc = cuda_fail(launch_gemm_tc(lc, a1), "gemm1");
+      if (rc) return rc;
+      ctx->mark(5);
+      GemmArgs a2;
+      memset(&a2, 0, sizeof a2);
+      a2.tmA[0] = L.tmA2[0];
+      a2.tmA[1] = L.tmA2[1];
+      a2.tmB[0] = ctx->tmH;
+      a2.tmB[1] = ctx->tmHs;
+      a2.out[0] = ws.y;
+      a2.out[1] = ws.s;
+      a2.ldo[0] = a2.ldo[1] = c.hidden;
+      a2.out_f32[0] = 0;
+      a2.out_f32[1] = 1;
+      a2.K[0] = c.inter;
+      a2.K[1] = c.shared_inter;
+      a2.M[0] = a2.M[1] = c.hidden;
+      a2.plan = ctx->plan2;
+      a2.status = ws.status;
+      a2.swiglu = 0;
+      a2.timeout_ns = ctx->timeout();
+      rc = cuda_fail(launch_gemm_tc(lc, a2), "gemm2");
+      if (rc) return rc;
+    } else {
+      SimtArgs s1;
+      memset(&s1, 0, sizeof s1);
+      s1.A[0] = L.W13;
+      s1.A[1] = L.W13s;
+      s1.B[0] = s1.B[1] = ws.xp;
+      s1.ldb[0] = s1.ldb[1] = c.hidden;
+      s1.out[0] = ws.h;
+      s1.out[1] = ws.hs;
+      s1.ldo[0] = c.inter;
+      s1.ldo[1] = c.shared_inter;
+      s1.out_f32[0] = s1.out_f32[1] = ctx->act_f32;
+      s1.K[0] = s1.K[1] = c.hidden;
+      s1.M[0] = 2 * c.inter;
+      s1.M[1] = 2 * c.shared_inter;
+      s1.act_f32 = ctx->act_f32;
+      s1.swiglu = 1;
+      s1.plan = ctx->plan1;
+      s1.status = ws.status;
+      rc = cuda_fail(launch_gemm_simt(lc, s1, c.num_experts + 1), "simt gemm1");
+      if (rc) return rc;
+      ctx->mark(5);
+      SimtArgs s2 = s1;
+      s2.A[0] = L.Wd;
+      s2.A[1] = L.Wds;
+      s2.B[0] = ws.h;
+      s2.B[1] = ws.hs;
+      s2.ldb[0] = c.inter;
+      s2.ldb[1] = c.shared_inter;
+      s2.out[0] = ws.y;
+      s2.out[1] = ws.s;
+      s2.ldo[0] = s2.ldo[1] = c.hidden;
+      s2.out_f32[0] = ctx->act_f32;
+      s2.out_f32[1] = 1;
+      s2.K[0] = c.inter;
+      s2.K[1] = c.shared_inter;
+      s2.M[0] = s2.M[1] = c.hidden;
+      s2.swiglu = 0;
+      s2.plan = ctx->plan2;
+      rc = cuda_fail(launch_gemm_simt(lc, s2, c.num_experts + 1), "simt gemm2");
+      if (rc) return rc;
+    }
+  } else {
+    ctx->mark(5);
+  }
+  ctx->mark(6);
+  rc = cuda_fail(launch_combine(lc, ctx->geom, ctx->win[1], f, ws, c.hidden, c.topk, ctx->act_f32,
+                                has_shared, ctx->act_f32),
+                 "combine");
+  if (rc) return rc;
+  ctx->mark(7);
+  rc = cuda_fail(launch_return_header(lc, ctx->geom, ctx->win[1], ctx->win[0], f, ws, c.num_experts,
+                                      c.topk),
+                 "return header");
+  if (rc) return rc;
+  ctx->mark(8);
+  ctx->last_T = (int)T;
+  ctx->forwards++;
+  return AFD_OK;
+}
+
+int afd_unpack_split(afd_ctx* ctx, int peer, int stage, void* out, int n_tokens,
+                     uint64_t expect_seq) {
+  if (!ctx) return AFD_ERR_ARG;
+  const afd_config& c = ctx->cfg;
+  if (peer < 0 || peer >= c.num_peers || stage < 0 || stage >= c.ring_depth || n_tokens < 0)
+    return AFD_ERR_ARG;
+  if (n_tokens > c.token_cap) return AFD_ERR_CAPACITY;
+  if (n_tokens > 0) {
+    const int rc = check_dev_ptr(out);
+    if (rc) return rc;
+    if (!aligned16(out)) return AFD_ERR_ARG;
+  }
+  const int row_bytes = c.hidden * (ctx->act_f32 ? 4 : 2);
+  return cuda_fail(launch_unpack(ctx->lc(), ctx->geom, ctx->win[1], peer, stage, out, n_tokens,
+                                 row_bytes, c.num_experts, expect_seq, ctx->ws.status,
+                                 ctx->timeout()),
+                   "unpack");
+}
+
+int afd_poll_status(afd_ctx* ctx) {
+  if (!ctx) return AFD_ERR_ARG;
+  if (cuda_fail(cudaStreamSynchronize(ctx->stream), "stream sync")) return AFD_ERR_CUDA;
+  int32_t st = 0;
+  if (cuda_fail(cudaMemcpy(&st, ctx->ws.status, 4, cudaMemcpyDeviceToHost), "status read"))
+    return AFD_ERR_CUDA;
+  if (st && cuda_fail(cudaMemset(ctx->ws.status, 0, 4), "status clear")) return AFD_ERR_CUDA;
+  return st;
+}
+
+int afd_get_window(afd_ctx* ctx, int direction, void** dev_ptr, int64_t* bytes) {
+  if (!ctx || (direction != AFD_DIR_DISPATCH && direction != AFD_DIR_RETURN)) return AFD_ERR_ARG;
+  if (dev_ptr) *dev_ptr = ctx->win[direction];
+  if (bytes) *bytes = ctx->L.window_bytes;
+  return AFD_OK;
+}
+
+int afd_get_workspace(afd_ctx* ctx, int which, void** dev_ptr, int64_t* bytes) {
+  if (!ctx || which < 0 || which > AFD_WS_STATUS) return AFD_ERR_ARG;
+  void* ptrs[12] = {ctx->ws.ids, ctx->ws.w, ctx->ws.counts, ctx->ws.offsets, ctx->ws.perm,
+                    ctx->ws.inv, ctx->ws.xp, ctx->ws.h, ctx->ws.y, ctx->ws.hs, ctx->ws.s,
+                    ctx->ws.status};
+  if (dev_ptr) *dev_ptr = ptrs[which];
+  if (bytes) *bytes = ctx->ws_cap[which];
+  return AFD_OK;
+}
+
+int afd_get_stats(afd_ctx* ctx, afd_stats* out) {
+  if (!ctx || !out) return AFD_ERR_ARG;
+  out->window_bytes = ctx->L.window_bytes;
+  out->workspace_bytes = ctx->ws_bytes;
+  out->last_total_tokens = ctx->last_T;
+  out->num_sms = ctx->num_sms;
+  out->forwards = ctx->forwards;
+  return AFD_OK;
+}
+
+int64_t afd_launch_count(afd_ctx* ctx) { return ctx ? ctx->launches : -1; }
+
+int afd_profile(afd_ctx* ctx, int enable) {
+  if (!ctx) return AFD_ERR_ARG;
+  if (enable && !ctx->ev[0])
+    for (auto& e : ctx->ev)
+      if (cuda_fail(cudaEventCreate(&e), "event create")) return AFD_ERR_CUDA;
+  ctx->profiling = enable != 0;
+  return AFD_OK;
+}
+
+int afd_stage_times(afd_ctx* ctx, float* ms, int n) {
+  if (!ctx || !ms || n < 0 || n > AFD_NUM_STAGES || !ctx->ev[0]) return AFD_ERR_ARG;
+  if (cuda_fail(cudaEventSynchronize(ctx->ev[AFD_NUM_STAGES]), "event sync")) return AFD_ERR_CUDA;
+  for (int i = 0; i < n; i++)
+    if (cuda_fail(cudaEventElapsedTime(&ms[i], ctx->ev[i], ctx->ev[i + 1]), "event time"))
+      return AFD_ERR_CUDA;
+  return AFD_OK;
+}
+
+}  // extern "C"

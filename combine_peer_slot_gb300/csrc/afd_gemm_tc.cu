@@ -1,0 +1,334 @@
+// afd_gemm_tc.cu -- grouped expert GEMM on the sm_103a tensor cores
+// (tcgen05.mma kind::f16, bf16 in, fp32 accumulate in TMEM), fed by TMA.
+//
+// Orientation: the weights are the M side (128 rows per tile) and the tokens
+// the N side (up to 256 per tile, any multiple of 16), D[m][n] = W[m] . X[n].
+// Ragged per-expert token counts then only round N up to 16, and the
+// decode-sized groups (a few dozen tokens) stream each weight tile once.
+//
+// Projections (Async GPU Connector, "Attention gate and FFN expert compute":
+// fused_experts = gate/up GEMM, SiLU-and-multiply, down GEMM; Async AFD for
+// Prefill on Ascend NPU, "Architecture": W1 with SwiGLU, then W2):
+//  - SwiGLU mode: a 5-D tensor map views W13[e] = [gate rows | up rows] as
+//    (h, r in 16, s in {gate, up}, j, e), so one TMA box lands 16 gate rows
+//    then the 16 matching up rows, four times: 128 rows covering 64
+//    intermediate columns.  In TMEM, warp quadrant q holds gate rows in
+//    lanes 0-15 and the matching up rows in lanes 16-31; a shuffle pairs
+//    them and h = silu(g) * u is written as bf16.
+//  - plain mode: y = h . Wd^T with Wd[e] = [hidden, inter] as a 3-D map.
+//
+// Warp roles (192 threads, one CTA per SM, persistent over the tile table
+// built on the device from the expert counts):
+//   warp 0  TMA producer (one lane), STAGES-deep smem ring
+//   warp 1  TMEM allocator and MMA issuer (one lane)
+//   warps 2-5 epilogue: TMEM -> registers -> global (quadrant = warp % 4)
+// Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile run
+// under the main loop of the next.  Every mbarrier wait is bounded.
+#include "afd_internal.cuh"
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;             // one 128-byte swizzle atom of bf16
+constexpr int BN = 256;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BOX_ROWS = 32;
+constexpr int B_BOX_BYTES = B_BOX_ROWS * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 192;
+constexpr int TMEM_COLS = 512;
+constexpr uint64_t kGemmTimeoutNs = 5000000000ull;
+
+struct SmemTail {
+  GemmPlan plan;
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int skip;
+};
+
+constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(SmemTail);
+
+// shared-memory matrix descriptor: K-major, 128-byte swizzle, rows of 128 B,
+// 8-row core groups 1024 B apart (SBO), descriptor version 1
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
+// N >> 3 at bit 17, M >> 4 at bit 24
+__device__ __forceinline__ uint32_t idesc_bf16(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(BM >> 4) << 24);
+}
+
+struct Tile {
+  int group, kind, mt, nt, rows;   // rows: valid tokens in this tile
+};
+
+__device__ __forceinline__ Tile decode_tile(const GemmPlan& p, int tile) {
+  int lo = 0, hi = p.ngroups - 1;
+  while (lo < hi) {  // last group with tile0 <= tile
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.g[mid].tile0 <= tile) lo = mid; else hi = mid - 1;
+  }
+  // skip empty groups sharing the same tile0
+  while (lo + 1 < p.ngroups && p.g[lo].m_tiles * p.g[lo].n_tiles == 0) lo++;
+  const GemmGroup& G = p.g[lo];
+  const int u = tile - G.tile0;
+  Tile t;
+  t.group = lo;
+  t.kind = G.kind;
+  t.mt = u % G.m_tiles;
+  t.nt = u / G.m_tiles;
+  t.rows = min(p.bn, G.rows - t.nt * p.bn);
+  return t;
+}
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         uint64_t deadline, int32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint32_t spins = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++spins & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() > deadline) {
+        *abort_flag = 1;
+        set_error(status, AFD_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+__global__ void __launch_bounds__(NUM_THREADS, 1) k_gemm_tc(const __grid_constant__ GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  SmemTail* tail = reinterpret_cast<SmemTail*>(smem + (size_t)STAGES * STAGE_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) tail->skip = read_status(args.status);
+  {
+    const int* src = reinterpret_cast<const int*>(args.plan);
+    int* dst = reinterpret_cast<int*>(&tail->plan);
+    for (int i = threadIdx.x; i < (int)(sizeof(GemmPlan) / 4); i += blockDim.x) dst[i] = src[i];
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; s++) {
+      mbar_init(smem_u32(&tail->full[s]), 1);
+      mbar_init(smem_u32(&tail->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; b++) {
+      mbar_init(smem_u32(&tail->tfull[b]), 1);
+      mbar_init(smem_u32(&tail->tempty[b]), 4);
+    }
+    mbar_init(smem_u32(&tail->drain), 1);
+    tail->abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (tail->skip || tail->plan.total_tiles <= (int)blockIdx.x) return;  // uniform for the CTA
+
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&tail->tmem_base)),
+                 "r"(TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tail->tmem_base;
+  const GemmPlan& plan = tail->plan;
+  const int total = plan.total_tiles;
+  const uint64_t deadline = globaltimer_ns() + kGemmTimeoutNs;
+  volatile int* abort_flag = &tail->abort_flag;
+  const uint32_t smem_base = smem_u32(smem);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------ TMA producer
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t pending = 0;  // stages with a fill issued (for the abort drain)
+      uint32_t pend_par = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const Tile t = decode_tile(plan, tile);
+        const GemmGroup& G = plan.g[t.group];
+        const int nkb = (args.K[t.kind] + BK - 1) / BK;
+        const int nb = (t.rows + B_BOX_ROWS - 1) / B_BOX_ROWS;
+        const int brow = G.b_row0 + t.nt * plan.bn;
+        const CUtensorMap* ta = &args.tmA[t.kind];
+        const CUtensorMap* tb = &args.tmB[t.kind];
+        for (int kb = 0; kb < nkb; kb++) {
+          if (!wait_bar(smem_u32(&tail->empty[s]), ph ^ 1, abort_flag, deadline, args.status)) { ok = false; break; }
+          const uint32_t full = smem_u32(&tail->full[s]);
+          const uint32_t sa = smem_base + s * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          mbar_expect_tx(full, A_BYTES + nb * B_BOX_BYTES);
+          if (args.swiglu)
+            tma_load_5d(sa, ta, kb * BK, 0, 0, t.mt * 4, G.a_idx, full);
+          else
+            tma_load_3d(sa, ta, kb * BK, t.mt * BM, G.a_idx, full);
+          for (int q = 0; q < nb; q++)
+            tma_load_2d(sb + q * B_BOX_BYTES, tb, kb * BK, brow + q * B_BOX_ROWS, full);
+          pending |= 1u << s;
+          pend_par = (pend_par & ~(1u << s)) | (ph << s);
+          if (++s == STAGES) { s = 0; ph ^= 1; }
+        }
+      }
+      if (!ok) {
+        // let every issued copy land before the CTA's shared memory goes away
+        const uint64_t dl = globaltimer_ns() + 100000000ull;
+        for (int q = 0; q < STAGES; q++)
+          if (pending & (1u << q))
+            while (!mbar_try_wait(smem_u32(&tail->full[q]), (pend_par >> q) & 1u) && globaltimer_ns() < dl) {}
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------ MMA issuer
+      int s = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t acc_ph = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const Tile t = decode_tile(plan, tile);
+        const int nkb = (args.K[t.kind] + BK - 1) / BK;
+        const int n_mma = (t.rows + 15) & ~15;
+        const uint32_t idesc = idesc_bf16(n_mma);
+        if (!wait_bar(smem_u32(&tail->tempty[acc]), acc_ph ^ 1, abort_flag, deadline, args.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < nkb; kb++) {
+          if (!wait_bar(smem_u32(&tail->full[s]), ph, abort_flag, deadline, args.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_base + s * STAGE_BYTES;
+          const uint64_t adesc = sdesc_sw128(sa);
+          const uint64_t bdesc = sdesc_sw128(sa + A_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; kk++)
+            tc_mma_f16(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
+                       (kb | kk) != 0);
+          tc_commit(smem_u32(&tail->empty[s]));
+          if (++s == STAGES) { s = 0; ph ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&tail->tfull[acc]));
+        if (++acc == 2) { acc = 0; acc_ph ^= 1; }
+      }
+      // all issued MMAs complete before TMEM is released
+      tc_commit(smem_u32(&tail->drain));
+      const uint64_t dl = globaltimer_ns() + 100000000ull;
+      while (!mbar_try_wait(smem_u32(&tail->drain), 0) && globaltimer_ns() < dl) {}
+    }
+  } else {
+    // ------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;
+    int acc = 0;
+    uint32_t acc_ph = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const Tile t = decode_tile(plan, tile);
+      const GemmGroup& G = plan.g[t.group];
+      bool ok = wait_bar(smem_u32(&tail->tfull[acc]), acc_ph, abort_flag, deadline, args.status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      const int kind = t.kind;
+      const int64_t ldo = args.ldo[kind];
+      const int out_f32 = args.out_f32[kind];
+      const int64_t row0 = (int64_t)G.out_row0 + (int64_t)t.nt * plan.bn;
+      if (args.swiglu) {
+        const int col = t.mt * 64 + q * 16 + (lane & 15);
+        const bool col_ok = col < args.M[kind] / 2;
+        const int my_par = lane >> 4;  // lanes 0-15 take even columns, 16-31 odd
+        for (int c0 = 0; c0 < t.rows; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(taddr + (uint32_t)c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; c++) {
+            const float mine = __uint_as_float(v[c]);
+            const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
+            if ((c & 1) == my_par) {
+              const float g = (lane < 16) ? mine : other;
+              const float u = (lane < 16) ? other : mine;
+              const int r = c0 + c;
+              if (r < t.rows && col_ok) {
+                const float hv = silu_f(g) * u;
+                const int64_t o = (row0 + r) * ldo + col;
+                if (out_f32) reinterpret_cast<float*>(args.out[kind])[o] = hv;
+                else reinterpret_cast<__nv_bfloat16*>(args.out[kind])[o] = __float2bfloat16_rn(hv);
+              }
+            }
+          }
+        }
+      } else {
+        const int col = t.mt * BM + q * 32 + lane;
+        const bool col_ok = col < args.M[kind];
+        for (int c0 = 0; c0 < t.rows; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(taddr + (uint32_t)c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; c++) {
+            const int r = c0 + c;
+            if (r < t.rows && col_ok) {
+              const int64_t o = (row0 + r) * ldo + col;
+              const float yv = __uint_as_float(v[c]);
+              if (out_f32) reinterpret_cast<float*>(args.out[kind])[o] = yv;
+              else reinterpret_cast<__nv_bfloat16*>(args.out[kind])[o] = __float2bfloat16_rn(yv);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&tail->tempty[acc]));
+      if (++acc == 2) { acc = 0; acc_ph ^= 1; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const LaunchCtx& lc, const GemmArgs& a) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  k_gemm_tc<<<lc.num_sms, NUM_THREADS, kSmemBytes, lc.stream>>>(a);
+  ++*lc.launches;
+  return cudaGetLastError();
+}
+
+size_t gemm_tc_smem_bytes() { return kSmemBytes; }

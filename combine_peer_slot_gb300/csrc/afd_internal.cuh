@@ -1,0 +1,263 @@
+// afd_internal.cuh -- structures shared by the host side and the kernels of
+// the AFD FFN-side library, plus thin inline-PTX wrappers for sm_103a.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/afd.h"
+
+#define AFD_MAX_GROUPS 320   // routed experts (<= 256) + one shared group
+
+// ---------------------------------------------------------------------------
+// per-forward fan-in description, passed by value.  Data on the wire, step
+// 3: the input is the concatenation of the listed peers' rows in list order.
+// ---------------------------------------------------------------------------
+struct FanIn {
+  int n_peers;
+  int stage;
+  int layer;
+  int total;                          // T = sum of seq_lens
+  int prefix[AFD_MAX_PEERS + 1];      // exclusive prefix of seq_lens
+  int region[AFD_MAX_PEERS];          // peer (window region) of list entry i
+};
+
+// window geometry (both windows share it)
+struct WinGeom {
+  int64_t flags_bytes, slot_bytes;
+  int64_t header, route_table, routed_x, shared_idx, shared_x;
+  int ring_depth;
+  int num_regions;
+};
+
+// workspace pointers
+struct DevWS {
+  int32_t* status;        // [1] sticky first error
+  uint64_t* seen;         // [regions * ring] last dispatch flag consumed
+  uint64_t* cur_seq;      // [MAX_PEERS] flag value consumed by this forward
+  int32_t* peer_shared;   // [MAX_PEERS] 1 if entry i carries shared rows
+  int32_t* ids;           // [Tmax * k]
+  float* w;               // [Tmax * k]
+  int32_t* counts;        // [E]
+  int32_t* offsets;       // [E + 1]
+  int32_t* perm;          // [Tmax * k]
+  int32_t* inv;           // [Tmax * k]
+  int32_t* peer_counts;   // [MAX_PEERS * E]
+  void* xp;               // act [Tmax * k + Tmax, H]
+  void* h;                // act [Tmax * k, I]
+  void* y;                // act [Tmax * k, H]
+  void* hs;               // act [Tmax, Is]
+  float* s;               // f32 [Tmax, H]
+  float* wgt;             // unused slot
+};
+
+// one group of the grouped GEMM: rows of the B operand (tokens) that share
+// one weight matrix (an expert, or the shared expert)
+struct GemmGroup {
+  int rows;      // tokens in the group
+  int b_row0;    // first row in the B source
+  int out_row0;  // first output row
+  int a_idx;     // expert index in the weight tensor
+  int kind;      // 0 routed, 1 shared
+  int m_tiles;   // 128-row tiles of the weight (M) dimension
+  int n_tiles;   // token tiles
+  int tile0;     // first linear tile index of the group
+};
+
+struct GemmPlan {
+  int ngroups;
+  int total_tiles;
+  int bn;        // token tile
+  int pad;
+  GemmGroup g[AFD_MAX_GROUPS];
+};
+
+// Arguments of the tensor-core grouped GEMM (one launch = one projection).
+struct GemmArgs {
+  CUtensorMap tmA[2];     // weights: [0] routed experts, [1] shared expert
+  CUtensorMap tmB[2];     // token rows: [0] routed source, [1] shared source
+  void* out[2];           // outputs per kind
+  int64_t ldo[2];         // output row pitch in elements
+  int out_f32[2];         // 1 = fp32 output, 0 = bf16
+  int K[2];               // reduction length per kind
+  int M[2];               // weight rows per kind (2I for SwiGLU, H for down)
+  const GemmPlan* plan;
+  int32_t* status;
+  int swiglu;             // 1: gate/up interleaved SwiGLU epilogue
+  int pad;
+  int64_t timeout_ns;
+};
+
+// SIMT GEMM arguments (fp32 activations, cross-check engine)
+struct SimtArgs {
+  const void* A[2];       // weights per kind: [E or 1][M][K] row-major
+  const void* B[2];       // token rows per kind: [rows][K]
+  int64_t ldb[2];
+  void* out[2];
+  int64_t ldo[2];
+  int out_f32[2];
+  int K[2];
+  int M[2];               // SwiGLU: 2I (gate rows then up rows); plain: H
+  int act_f32;
+  int swiglu;
+  const GemmPlan* plan;
+  int32_t* status;
+};
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+#ifdef __CUDACC__
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// record the first error in the sticky status word
+__device__ __forceinline__ void set_error(int32_t* status, int code) {
+  atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ int read_status(const int32_t* status) {
+  return *(volatile const int32_t*)status;
+}
+
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.acquire.sys.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.release.sys.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// mbarrier -------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// TMA ------------------------------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(tm), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
+                                            int c2, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(dst), "l"(tm), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
+                                            int c2, int c3, int c4, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+      ::"r"(dst), "l"(tm), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
+      : "memory");
+}
+
+// tcgen05 -------------------------------------------------------------------
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 in, fp32 accumulate)
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+#endif  // __CUDACC__
+
+// ---------------------------------------------------------------------------
+// launchers implemented in the kernel translation units (host side)
+// ---------------------------------------------------------------------------
+struct LaunchCtx {
+  cudaStream_t stream;
+  int num_sms;
+  int64_t* launches;
+};
+
+cudaError_t launch_pack_payload(const LaunchCtx& lc, const WinGeom& g, uint8_t* win, int region,
+                                int stage, const void* x, int n, int row_bytes, int with_shared,
+                                const int32_t* status);
+cudaError_t launch_pack_header(const LaunchCtx& lc, const WinGeom& g, uint8_t* win, int region,
+                               int stage, int layer, int n, int with_shared, int num_experts,
+                               uint64_t seq, int shutdown);
+cudaError_t launch_header_check(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
+                                const FanIn& f, const DevWS& ws, int num_experts,
+                                int token_cap, int has_shared_expert, int64_t timeout_ns);
+cudaError_t launch_router(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
+                          const FanIn& f, const DevWS& ws, int hidden, int act_f32,
+                          const float* WgT, const float* bias, int E, int k, int renorm,
+                          float scale);
+cudaError_t launch_plan(const LaunchCtx& lc, const FanIn& f, const DevWS& ws, int E, int k,
+                        int inter, int shared_inter, int hidden, int has_shared, int bn,
+                        GemmPlan* plan1, GemmPlan* plan2);
+cudaError_t launch_gather(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
+                          const FanIn& f, const DevWS& ws, int k, int row_bytes,
+                          int has_shared);
+cudaError_t launch_gemm_tc(const LaunchCtx& lc, const GemmArgs& a);
+cudaError_t launch_gemm_simt(const LaunchCtx& lc, const SimtArgs& a, int max_rows_hint);
+cudaError_t launch_combine(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret,
+                           const FanIn& f, const DevWS& ws, int hidden, int k, int act_f32,
+                           int has_shared, int y_f32);
+cudaError_t launch_return_header(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret,
+                                 const uint8_t* win, const FanIn& f, const DevWS& ws, int E,
+                                 int k);
+cudaError_t launch_unpack(const LaunchCtx& lc, const WinGeom& g, const uint8_t* ret, int region,
+                          int stage, void* out, int n, int row_bytes, int num_experts,
+                          uint64_t expect_seq, int32_t* status, int64_t timeout_ns);
+cudaError_t launch_transpose_wg(const LaunchCtx& lc, const float* Wg, float* WgT, int hidden,
+                                int E);

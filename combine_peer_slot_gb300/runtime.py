@@ -1,0 +1,128 @@
+"""Device-side plumbing around the C ABI: torch allocates the inputs and
+weights and provides the stream; every step of the FFN path runs in the
+library's kernels (combine_peer_slot_gb300/afd.py)."""
+import numpy as np
+
+from . import afd as A
+from . import workloads as W
+
+
+class DeviceBytes:
+    """Zero-copy uint8 view of a device allocation owned by the library, for
+    inspecting or editing slot bytes from torch."""
+
+    def __init__(self, ptr, nbytes):
+        self.__cuda_array_interface__ = {"shape": (int(nbytes),), "typestr": "|u1",
+                                         "data": (int(ptr), False), "version": 2}
+
+
+def device_view(ptr, nbytes):
+    import torch
+    return torch.as_tensor(DeviceBytes(ptr, nbytes), device="cuda")
+
+
+def act_tensor(a, act, device):
+    """numpy activation storage (uint16 bf16 bits / float32) -> torch tensor."""
+    import torch
+    if act == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device)
+
+
+class Runner:
+    """One library context bound to a workload: inputs on the device, the
+    layer weights registered, and helpers for pack / forward / unpack."""
+
+    def __init__(self, w: W.Workload, gemm=A.AFD_GEMM_TENSOR, layers=None, stream=None,
+                 max_total_tokens=0, wait_timeout_ns=0, device="cuda"):
+        import torch
+        self.w = w
+        self.device = device
+        self.layers = w.layers if layers is None else layers
+        self.stream = stream if stream is not None else torch.cuda.current_stream()
+        self.cfg = A.make_config(w.num_peers, w.token_cap, w.hidden, w.num_experts, w.topk,
+                                 w.inter, w.shared_inter, act=w.act, renorm=w.renorm,
+                                 routed_scaling=w.routed_scaling, max_layers=self.layers,
+                                 max_total_tokens=max_total_tokens, gemm=gemm,
+                                 wait_timeout_ns=wait_timeout_ns)
+        self.ctx = A.afd_create(self.cfg, self.stream.cuda_stream)
+        self.layout = A.afd_slot_layout(self.cfg)
+        self.host = W.host_inputs(w)
+        self.x = [act_tensor(a, w.act, device) for a in self.host["x"]]
+        self.Wg = torch.from_numpy(self.host["Wg"]).to(device)
+        self.bias = None if self.host["bias"] is None else torch.from_numpy(self.host["bias"]).to(device)
+        self.weights = []
+        for layer in range(self.layers):
+            wt = W.expert_weights(w, layer, device)
+            self.weights.append(wt)
+            A.afd_set_layer(self.ctx, layer, self.Wg.data_ptr(),
+                            self.bias.data_ptr() if self.bias is not None else 0,
+                            wt["W13"].data_ptr(), wt["Wd"].data_ptr(),
+                            wt["W13s"].data_ptr() if wt["W13s"] is not None else 0,
+                            wt["Wds"].data_ptr() if wt["Wds"] is not None else 0)
+        self.seq = 0
+        self.last_seq = {}
+        dt = torch.bfloat16 if w.act == "bf16" else torch.float32
+        self.out = [torch.empty((max(n, 1), w.hidden), dtype=dt, device=device) for n in w.seq_lens]
+
+    # -- attention side, simulated ------------------------------------------------
+    def pack_all(self, layer=0, stage=0, peers=None, with_shared=None):
+        ws = (self.w.shared_inter > 0) if with_shared is None else with_shared
+        for p in (range(self.w.num_peers) if peers is None else peers):
+            self.seq += 1
+            n = self.w.seq_lens[p]
+            rc = A.afd_pack_slot(self.ctx, p, stage, layer, self.x[p].data_ptr() if n else 0, n,
+                                 ws, self.seq)
+            if rc:
+                raise A.AfdError(rc, "afd_pack_slot")
+            self.last_seq[(p, stage)] = self.seq
+
+    def forward(self, layer=0, stage=0, slots=None):
+        slots = list(range(self.w.num_peers)) if slots is None else list(slots)
+        lens = [self.w.seq_lens[p] for p in slots]
+        return A.afd_ffn_forward(self.ctx, layer, stage, lens, slots)
+
+    def unpack_all(self, stage=0, peers=None):
+        for p in (range(self.w.num_peers) if peers is None else peers):
+            n = self.w.seq_lens[p]
+            rc = A.afd_unpack_split(self.ctx, p, stage, self.out[p].data_ptr() if n else 0, n,
+                                    self.last_seq[(p, stage)])
+            if rc:
+                raise A.AfdError(rc, "afd_unpack_split")
+        return self.out
+
+    def poll(self):
+        return A.afd_poll_status(self.ctx)
+
+    # -- inspection -----------------------------------------------------------------
+    def window(self, direction):
+        ptr, n = A.afd_get_window(self.ctx, direction)
+        return device_view(ptr, n)
+
+    def workspace(self, which, nbytes=None):
+        ptr, cap = A.afd_get_workspace(self.ctx, which)
+        return device_view(ptr, cap if nbytes is None else nbytes)
+
+    def weights_numpy(self, layer):
+        d = W.weights_to_numpy(self.weights[layer])
+        d["Wg"] = self.host["Wg"]
+        d["bias"] = self.host["bias"]
+        return d
+
+    def oracle_cfg(self):
+        w = self.w
+        return dict(num_regions=w.num_peers, ring_depth=1, token_cap=w.token_cap, hidden=w.hidden,
+                    act_bytes=w.act_bytes, num_experts=w.num_experts, topk=w.topk, inter=w.inter,
+                    shared_inter=w.shared_inter, renorm=w.renorm,
+                    max_total_tokens=self.cfg.max_total_tokens, routed_scaling=w.routed_scaling)
+
+    def close(self):
+        if self.ctx:
+            A.afd_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -165,3 +165,16 @@ def weights_to_numpy(wt):
         else:
             out[k] = v.detach().cpu().contiguous().numpy()
     return out
+
+
+def custom(name, **overrides):
+    """A named workload with some fields replaced (edge-case parity runs);
+    new seq_lens also reset num_peers and token_cap."""
+    w = get(name)
+    for key, val in overrides.items():
+        setattr(w, key, val)
+    if "seq_lens" in overrides:
+        w.num_peers = len(w.seq_lens)
+        if "token_cap" not in overrides:
+            w.token_cap = max(64, -(-max(max(w.seq_lens), 1) // 64) * 64)
+    return w

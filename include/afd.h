@@ -1,0 +1,296 @@
+/*
+ * afd.h -- C ABI of the GB300 (sm_103a) library for the FFN side of
+ * Attention-FFN Disaggregation (AFD): fan-in of per-peer slots, softmax top-k
+ * router, stable per-expert token permutation, grouped SwiGLU experts on the
+ * tensor cores (plus an optional shared expert), top-k weighted combine, and
+ * the split back into per-peer return slots.
+ *
+ * Sources (page title, section):
+ *  - "[RFC]: Async GPU Connector" (vllm-project/afd-plugin #233):
+ *    "Window and slot layout", "Capacity and ring depth", "Data flow",
+ *    "Attention gate and FFN expert compute", "FFN main loop",
+ *    "Risks and alternatives".
+ *  - "Data on the wire: tensors per layer and stage": steps 1-4 and
+ *    "What can go wrong".
+ *  - "[RFC]: Async AFD for Prefill on Ascend NPU": "Architecture",
+ *    "Asynchronous work-item contract", "Risks".
+ *
+ * One process, one GPU.  The attention peers are regions of a device
+ * "window" owned by the library (two windows: the FFN inbox that peers pack
+ * into, and the return inbox the FFN step writes).  All pointers passed in
+ * are plain device pointers unless a comment says host; no call allocates
+ * device memory except afd_create / afd_set_layer.
+ *
+ * Conventions
+ *  - Every call returns an int status: AFD_OK (0) or an AFD_ERR_* code.
+ *  - Calls that launch work are asynchronous and ordered on the context's
+ *    stream.  Errors that only the device can see (header checks, bounded
+ *    waits) are recorded in a device status word; afd_poll_status reads it.
+ *    After a device error, later steps on the same context do no work until
+ *    the status is polled (sticky first error).
+ *  - Activation element type: AFD_DTYPE_BF16 or AFD_DTYPE_F32.  Weights use
+ *    the activation type; the router weight and bias are fp32.
+ */
+#ifndef AFD_H
+#define AFD_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define AFD_OK 0
+#define AFD_ERR_ARG 1          /* invalid argument (range, duplicate peer, NULL) */
+#define AFD_ERR_SHAPE 2        /* token counts disagree (header vs seq_lens,
+                                  Data on the wire, "What can go wrong") */
+#define AFD_ERR_CAPACITY 3     /* over token_cap / max_total_tokens: raise,
+                                  never truncate (Async GPU Connector,
+                                  "Capacity and ring depth") */
+#define AFD_ERR_HEADER 4       /* magic / version / length self-check failed */
+#define AFD_ERR_SEQ 5          /* header seq or echo_seq mismatch (Async GPU
+                                  Connector, "Risks and alternatives") */
+#define AFD_ERR_LAYER 6        /* header layer != requested layer, or no
+                                  weights registered for it */
+#define AFD_ERR_STAGE 7        /* header stage != requested stage */
+#define AFD_ERR_TIMEOUT 8      /* a bounded device wait gave up */
+#define AFD_ERR_SHUTDOWN 9     /* the peer set the shutdown bit */
+#define AFD_ERR_SPLIT_UNEVEN 10 /* even-split fallback does not divide */
+#define AFD_ERR_NOT_DEVICE 11  /* a host pointer where device memory is required
+                                  (Data on the wire: CPU tensors are rejected) */
+#define AFD_ERR_CUDA 12        /* a CUDA runtime/driver call failed */
+#define AFD_ERR_UNSUPPORTED 13 /* configuration outside what the kernels cover */
+
+#define AFD_DTYPE_F32 0
+#define AFD_DTYPE_BF16 1
+
+/* GEMM engine of the expert projections.  TENSOR (default for bf16) is the
+ * tcgen05/TMEM grouped GEMM; SIMT is a plain fp32-FMA CUDA kernel that
+ * serves fp32 activations and cross-checks the tensor-core path. */
+#define AFD_GEMM_TENSOR 0
+#define AFD_GEMM_SIMT 1
+
+#define AFD_MAX_PEERS 64
+
+/* ---- configuration -------------------------------------------------------
+ * num_peers        attention peers = window regions (with one FFN rank the
+ *                  region count max(attn, ffn) is the peer count)
+ * ring_depth       slots per peer, one per stage in flight (1 without
+ *                  micro-batching; Async GPU Connector, "Capacity and ring
+ *                  depth": an invariant, not a knob)
+ * token_cap        max tokens per slot (max_num_batched_tokens)
+ * max_total_tokens max fan-in total per forward; 0 = num_peers * token_cap
+ * hidden, num_experts, topk, inter (routed SwiGLU intermediate),
+ * shared_inter     shared SwiGLU intermediate, 0 = no shared expert
+ * act_dtype        AFD_DTYPE_*; renorm: top-k weights renormalised to sum 1
+ * routed_scaling   routed_scaling_factor applied to the gate weights
+ * routed_cap_multiplier  recorded for the multi-FFN-rank dispatch (must be
+ *                  >= 1); one FFN rank receives exactly T * topk partials
+ * wait_timeout_ns  bound on every device-side wait (flag polls); 0 = 1 s
+ * gemm             AFD_GEMM_*; max_layers: size of the layer weight table
+ */
+typedef struct afd_config {
+  int32_t num_peers;
+  int32_t ring_depth;
+  int32_t token_cap;
+  int32_t max_total_tokens;
+  int32_t hidden;
+  int32_t num_experts;
+  int32_t topk;
+  int32_t inter;
+  int32_t shared_inter;
+  int32_t act_dtype;
+  int32_t renorm;
+  int32_t max_layers;
+  int32_t gemm;
+  int32_t reserved;
+  float routed_scaling;
+  float routed_cap_multiplier;
+  int64_t wait_timeout_ns;
+} afd_config;
+
+/* Byte offsets of the slot fields and window sizes.  Async GPU Connector,
+ * "Window and slot layout":
+ *   window = [ flag[num_regions * ring_depth] | slot(0,0) | slot(0,1) | ... ]
+ *   slot   = [ header | route_table | routed_x | shared_idx | shared_x ]
+ * Every field is aligned to align = lcm(256, hidden * element size), so each
+ * field is 256-byte aligned and every activation row is a whole row of the
+ * window viewed as a [rows, hidden] matrix.  Sizes: header (12 + E) int32;
+ * route_table [token_cap, topk] int32; routed_x and shared_x
+ * [token_cap, hidden]; shared_idx [token_cap] int32; the shared fields are
+ * empty without a shared expert.  Flags are uint64 sequence numbers; slot
+ * (peer p, stage s) is slot number p * ring_depth + s, as is its flag. */
+typedef struct afd_layout {
+  int64_t header, route_table, routed_x, shared_idx, shared_x;
+  int64_t slot_bytes, flags_bytes, window_bytes, align;
+} afd_layout;
+
+/* Header words (int32), Async GPU Connector, "Window and slot layout": a
+ * fixed 12 words then expert_counts[num_experts]; the page names the fields
+ * but not their order, which is this library's:
+ *   0 magic (bytes 'A','F','D','G'), 1 version (1), 2 flags (bit 1, value
+ *   2, = shutdown), 3 seq (low 32 bits of the flag), 4 echo_seq, 5 layer,
+ *   6 stage, 7 num_tokens, 8 routed_tokens, 9 shared_tokens, 10 num_experts,
+ *   11 header length in words (12 + num_experts).
+ * Dispatch: routed_x = the peer's tokens in order, routed_tokens = 0 (no
+ * partials routed by the sender: the FFN routes), shared_tokens = 0 or
+ * num_tokens with shared_idx = 0..n-1 and shared_x = the same rows.
+ * Return: routed_x = output rows, route_table = chosen expert ids [n, topk],
+ * routed_tokens = n * topk, expert_counts = this peer's per-expert partial
+ * counts, seq = echo_seq = the dispatch seq; the return flag = that seq. */
+#define AFD_HEADER_FIXED_WORDS 12
+#define AFD_HEADER_MAGIC 0x47444641
+#define AFD_HEADER_VERSION 1
+#define AFD_FLAG_SHUTDOWN 2
+
+#define AFD_DIR_DISPATCH 0  /* FFN inbox: peers pack into it */
+#define AFD_DIR_RETURN 1    /* return inbox: the FFN step writes it */
+
+/* workspace buffers exposed for inspection (afd_get_workspace) */
+#define AFD_WS_IDS 0        /* int32 [T, topk] chosen expert ids */
+#define AFD_WS_WEIGHTS 1    /* fp32 [T, topk] gate weights */
+#define AFD_WS_COUNTS 2     /* int32 [E] partials per expert */
+#define AFD_WS_OFFSETS 3    /* int32 [E + 1] exclusive prefix of counts */
+#define AFD_WS_PERM 4       /* int32 [T*topk] position -> flattened index t*k+j */
+#define AFD_WS_INV 5        /* int32 [T*topk] flattened index -> position */
+#define AFD_WS_XP 6         /* act [T*topk + T, hidden] permuted rows, then shared rows */
+#define AFD_WS_H 7          /* act [T*topk, inter] routed SwiGLU output */
+#define AFD_WS_Y 8          /* act [T*topk, hidden] routed down projection */
+#define AFD_WS_HS 9         /* act [T, shared_inter] shared SwiGLU output */
+#define AFD_WS_S 10         /* fp32 [T, hidden] shared expert output */
+#define AFD_WS_STATUS 11    /* int32 device status word */
+
+typedef struct afd_ctx afd_ctx;
+
+typedef struct afd_stats {
+  int64_t window_bytes;      /* one window */
+  int64_t workspace_bytes;
+  int32_t last_total_tokens; /* T of the last forward */
+  int32_t num_sms;
+  int64_t forwards;
+} afd_stats;
+
+/* Create a context on the current CUDA device: validates cfg, allocates the
+ * two windows (zeroed: every flag 0), the workspace sized for
+ * max_total_tokens, and the layer table.  cuda_stream is a cudaStream_t (NULL
+ * = the legacy default stream).  *out is owned by the caller; release it
+ * with afd_destroy.  Errors: AFD_ERR_ARG / AFD_ERR_UNSUPPORTED for bad cfg,
+ * AFD_ERR_CUDA when a device call fails (e.g. no GPU). */
+int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out);
+
+/* Synchronise the context's stream and free everything it owns. NULL is a
+ * no-op. */
+void afd_destroy(afd_ctx* ctx);
+
+/* Change the stream later calls are ordered on. */
+int afd_set_stream(afd_ctx* ctx, void* cuda_stream);
+
+/* Host only (no GPU needed): the slot layout for cfg. */
+int afd_slot_layout(const afd_config* cfg, afd_layout* out);
+
+/* Host only.  Data on the wire, step 4 and "What can go wrong": split
+ * `total` tokens over n_peers by the recorded lengths (seq_lens, host array
+ * of n_lens ints) in peer order; when n_lens != n_peers the split is even
+ * and AFD_ERR_SPLIT_UNEVEN is returned if it does not divide.  Lengths that
+ * do not sum to total give AFD_ERR_SHAPE.  sizes: host array [n_peers]. */
+int afd_split_sizes(int total, int n_peers, const int* seq_lens, int n_lens, int* sizes);
+
+/* Register the weights of one layer (layer-select table, Async AFD for
+ * Prefill on Ascend NPU, "Architecture": an address table for every layer).
+ *   Wg   fp32 [hidden, E] row-major (router)
+ *   bias fp32 [E] or NULL (added to the logits)
+ *   W13  act [E, 2*inter, hidden]: rows 0..inter-1 gate, inter..2*inter-1 up
+ *   Wd   act [E, hidden, inter]
+ *   W13_s act [2*shared_inter, hidden], Wd_s act [hidden, shared_inter]
+ *        (both NULL when shared_inter == 0)
+ * All device pointers, caller-owned, must stay valid while the layer is
+ * used; 16-byte aligned.  The library keeps a transposed fp32 copy of Wg
+ * (the only weight copy) and the TMA descriptors.  Errors: AFD_ERR_ARG,
+ * AFD_ERR_NOT_DEVICE, AFD_ERR_CUDA. */
+int afd_set_layer(afd_ctx* ctx, int layer, const float* Wg, const float* bias,
+                  const void* W13, const void* Wd, const void* W13_s, const void* Wd_s);
+
+/* The attention side's send, simulated (Async GPU Connector, "Window and
+ * slot layout" and "Data flow"): copy x (device, act [n_tokens, hidden],
+ * row-major) into slot (peer, stage) of the dispatch window -- routed_x, and
+ * shared_idx/shared_x when with_shared -- then write the header (layer,
+ * stage, num_tokens, seq) and, after the payload, the flag = seq.  seq must
+ * exceed the previous seq packed into that slot (monotonic, host-checked:
+ * AFD_ERR_SEQ).  n_tokens may be 0 (x may then be NULL).  Errors:
+ * AFD_ERR_ARG, AFD_ERR_CAPACITY (n_tokens > token_cap), AFD_ERR_NOT_DEVICE,
+ * AFD_ERR_SEQ. */
+int afd_pack_slot(afd_ctx* ctx, int peer, int stage, int layer, const void* x, int n_tokens,
+                  int with_shared, uint64_t seq);
+
+/* Publish an empty slot whose header carries the shutdown bit (Async GPU
+ * Connector, "FFN main loop": announce_shutdown); a forward that reads it
+ * records AFD_ERR_SHUTDOWN. */
+int afd_announce_shutdown(afd_ctx* ctx, int peer, int stage, uint64_t seq);
+
+/* The FFN step over one fan-in (the timed hot path).  seq_lens and slots
+ * are host arrays of n_peers ints: slots[i] is the peer whose slot (peer,
+ * stage) is the i-th part of the concatenation and seq_lens[i] its token
+ * count (Data on the wire, steps 2-4).  On the device, in stream order:
+ *   a0 bounded wait for each listed flag to pass the last value consumed,
+ *      then header checks (magic, version, length, seq/echo, shutdown,
+ *      layer, stage, num_tokens == seq_lens[i], shared fields);
+ *   a1 router over the virtual concatenation (fp32 logits, top-k with
+ *      lowest-index ties, softmax gate weights);
+ *   a2/a3 per-expert counts and offsets, stable permutation, gather of the
+ *      rows straight from the peer slots;
+ *   a4-a6 grouped SwiGLU GEMMs for the routed experts and the shared expert;
+ *   a7 weighted combine, split into each peer's return slot (routed_x,
+ *      route_table, header), then each return flag = the dispatch seq.
+ * Host-checked errors (returned): AFD_ERR_ARG (peer range/duplicates, stage
+ * range, n_peers), AFD_ERR_CAPACITY, AFD_ERR_LAYER (no weights).  Device
+ * errors (afd_poll_status): AFD_ERR_TIMEOUT, AFD_ERR_HEADER, AFD_ERR_SEQ,
+ * AFD_ERR_SHUTDOWN, AFD_ERR_LAYER, AFD_ERR_STAGE, AFD_ERR_SHAPE. */
+int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, const int* slots,
+                    int n_peers);
+
+/* The attention side's receive, simulated (Data on the wire, step 4: each
+ * peer receives its slice): bounded wait until the return flag of (peer,
+ * stage) equals expect_seq, check magic / version / echo_seq / num_tokens
+ * == n_tokens, then copy the n_tokens output rows into out (device, act
+ * [n_tokens, hidden]).  Device errors: AFD_ERR_TIMEOUT, AFD_ERR_SEQ (flag
+ * past expect_seq or echo mismatch), AFD_ERR_HEADER, AFD_ERR_SHAPE. */
+int afd_unpack_split(afd_ctx* ctx, int peer, int stage, void* out, int n_tokens,
+                     uint64_t expect_seq);
+
+/* Synchronise the stream, return the first device-recorded error since the
+ * last poll (AFD_OK if none) and clear it; AFD_ERR_CUDA if the stream itself
+ * failed. */
+int afd_poll_status(afd_ctx* ctx);
+
+/* Device base pointer and size of a window (AFD_DIR_*). */
+int afd_get_window(afd_ctx* ctx, int direction, void** dev_ptr, int64_t* bytes);
+
+/* Device pointer and capacity in bytes of a workspace buffer (AFD_WS_*);
+ * contents describe the last forward. */
+int afd_get_workspace(afd_ctx* ctx, int which, void** dev_ptr, int64_t* bytes);
+
+int afd_get_stats(afd_ctx* ctx, afd_stats* out);
+
+/* Kernel launches the library issued on this context since creation. */
+int64_t afd_launch_count(afd_ctx* ctx);
+
+/* Stage timing.  With enable != 0, every afd_ffn_forward records a CUDA
+ * event on the context's stream before and after each stage:
+ *   0 header check, 1 router, 2 plan, 3 gather, 4 SwiGLU GEMM (routed +
+ *   shared), 5 down GEMM (routed + shared), 6 combine + split, 7 return
+ *   headers and flags.
+ * afd_stage_times waits for the last forward's events and writes the
+ * elapsed milliseconds of the first n (<= AFD_NUM_STAGES) stages into ms
+ * (host array).  Events cost no device work; timing is off by default. */
+#define AFD_NUM_STAGES 8
+int afd_profile(afd_ctx* ctx, int enable);
+int afd_stage_times(afd_ctx* ctx, float* ms, int n);
+
+/* Static string for a status code. */
+const char* afd_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* AFD_H */

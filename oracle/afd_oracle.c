@@ -300,6 +300,9 @@ static void orc_router_logits(const float* x, int hidden, const float* Wg,
   }
 }
 
+/* Selection key of a logit: a NaN ranks below every number (as -inf). */
+static float rank_key(float v) { return isnan(v) ? -INFINITY : v; }
+
 /* Top-k on the logits with ties broken toward the lower expert index, then
  * gate weights from a softmax over all E experts ([RFC-GPU] "Attention gate
  * and FFN expert compute": softmax router; the k chosen experts carry their
@@ -318,9 +321,9 @@ static void orc_router_token(const float* x, int hidden, const float* Wg,
     int best = -1;
     for (int e = 0; e < E; e++)
 #if ORC_PLANT == 3
-      if (!taken[e] && (best < 0 || lg[e] >= lg[best])) best = e;
+      if (!taken[e] && (best < 0 || rank_key(lg[e]) >= rank_key(lg[best]))) best = e;
 #else
-      if (!taken[e] && (best < 0 || lg[e] > lg[best])) best = e;
+      if (!taken[e] && (best < 0 || rank_key(lg[e]) > rank_key(lg[best]))) best = e;
 #endif
     taken[best] = 1;
     ids[j] = best;

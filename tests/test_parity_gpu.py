@@ -1,0 +1,75 @@
+"""GPU path against the CPU oracle through the C ABI (needs an sm_103a GPU)."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from combine_peer_slot_gb300 import afd as A
+from combine_peer_slot_gb300 import runtime as R
+from combine_peer_slot_gb300 import workloads as W
+from tests import gpu_parity as G
+
+
+@pytest.fixture(autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    A.lib()
+
+
+def test_tiny_fp32():
+    run = R.Runner(W.get("tiny"), gemm=A.AFD_GEMM_SIMT)
+    e, _ = G.run_and_compare_full(run)
+    print("tiny max|err|/rms", e)
+
+
+@pytest.mark.parametrize("gemm", [A.AFD_GEMM_TENSOR, A.AFD_GEMM_SIMT], ids=["tcgen05", "simt"])
+def test_fanin_bf16(gemm):
+    run = R.Runner(W.get("fanin"), gemm=gemm)
+    e, _ = G.run_and_compare_full(run)
+    print("fanin max|err|/rms", e)
+
+
+def test_fanin_reordered_with_empty_peer():
+    w = W.custom("fanin", seq_lens=[37, 0, 91, 5])
+    run = R.Runner(w)
+    G.run_and_compare_full(run, slots=[2, 1, 3, 0])
+
+
+def test_fanin_subset_of_peers_and_repeat():
+    """Only some peers in the fan-in; then a second round on the same slots
+    (the flags must advance) gives the same answer."""
+    w = W.custom("fanin", seq_lens=[37, 91, 64])
+    run = R.Runner(w)
+    G.run_and_compare_full(run, slots=[2, 0])
+    e2, _ = G.run_and_compare_full(run, slots=[2, 0])
+
+
+def test_single_peer_ragged_tiles():
+    """One peer, token counts that leave ragged 16/32/256 tails per expert."""
+    w = W.custom("fanin", seq_lens=[301], num_experts=8, topk=2)
+    run = R.Runner(w)
+    G.run_and_compare_full(run)
+
+
+def test_v2lite_prefill_full_size():
+    w = W.get("v2lite_prefill")
+    run = R.Runner(w, max_total_tokens=w.total_tokens)
+    e = G.run_and_compare_sampled(run, per_peer=8)
+    print("v2lite max|err|/rms", e)
+
+
+def test_skewed_full_size():
+    w = W.get("skewed")
+    run = R.Runner(w, max_total_tokens=w.total_tokens)
+    e = G.run_and_compare_sampled(run, per_peer=4)
+    counts = G.ws_array(run, A.AFD_WS_COUNTS, w.num_experts, np.int32)
+    assert (counts == 0).any() and counts.max() > 5 * counts.mean()
+
+
+def test_decode_26_layers():
+    w = W.get("decode")
+    run = R.Runner(w, max_total_tokens=w.total_tokens)
+    for layer in range(w.layers):
+        G.run_and_compare_sampled(run, layer=layer, per_peer=1, check_routing=True)

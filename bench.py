@@ -1,0 +1,466 @@
+"""Benchmark of the AFD FFN-side step (fan-in -> router -> permute -> grouped
+SwiGLU experts + shared expert -> combine -> per-peer split) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload v2lite_prefill|decode|skewed|fanin]
+
+One step = afd_ffn_forward over one freshly packed fan-in (for the decode
+workload: all 26 layers, each re-packed).  Timing: CUDA events around each
+forward on the library's stream; the packs (the attention side's remote
+write) and an L2 flush run between the timed windows.  Rank 0 prints one
+JSON line.  --impl reference times the CPU oracle (the plain C reference of
+the same computation) on a bounded sample of the same workload.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FFN-side MoE tokens/s + TFLOP/s (V2-Lite shape, bf16); % of roofline, 1xGB300"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def dist_init(n_gpus):
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, ws):
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(v, ws):
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, device_index):
+        self.path = tempfile.mktemp(prefix="afd_clocks_", suffix=".csv")
+        self.proc = None
+        self.dev = device_index
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if not self.proc or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work (roofline numerators)
+# ---------------------------------------------------------------------------
+def stage_work(w, T):
+    """Algorithmic FLOPs / bytes per launch of each stage for T tokens."""
+    H, I, Is, k, E = w.hidden, w.inter, w.shared_inter, w.topk, w.num_experts
+    ab = w.act_bytes
+    return {
+        "router": {"flops": 2 * T * H * E, "bytes": T * H * ab + H * E * 4 + T * k * 8},
+        "gather": {"bytes": (T * k + T) * H * ab * 2},
+        "gemm_swiglu": {"flops": 2 * T * H * 2 * (k * I + Is)},
+        "gemm_down": {"flops": 2 * T * H * (k * I + Is)},
+        "combine_split": {"bytes": T * k * H * ab + T * H * 4 + T * H * ab + T * k * 8},
+    }
+
+
+def path_roofline(w, T, counts_nonzero, pk):
+    """Roofline time of one forward: max(FLOP / bf16 peak, bytes / HBM) with
+    bytes = weights of every expert that received a token + shared + router
+    weight + activations (x in, shared_x in, output)."""
+    H, I, Is, E = w.hidden, w.inter, w.shared_inter, w.num_experts
+    flops = T * w.flops_per_token()
+    wbytes = counts_nonzero * 3 * H * I * 2 + 3 * H * Is * 2 + H * E * 4
+    abytes = 3 * T * H * w.act_bytes
+    t_flop = flops / (pk["bf16_tflops"] * 1e12)
+    t_mem = (wbytes + abytes) / (pk["hbm_gbs"] * 1e9)
+    return flops, wbytes + abytes, max(t_flop, t_mem), ("tensor" if t_flop >= t_mem else "hbm")
+
+
+def traffic_from_profile(kernel, workload):
+    """dram bytes per launch recorded by an ncu capture under profiles/, valid
+    only while the kernel source is unchanged (sha256 recorded with it)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    src = vals.get("kernel_source")
+    if not src or "dram_bytes_per_launch" not in vals:
+        return None
+    with open(os.path.join(ROOT, src), "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != vals.get("kernel_source_sha256"):
+            return None
+    return float(vals["dram_bytes_per_launch"])
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args, ws, rank, local):
+    import numpy as np
+    import torch
+    from combine_peer_slot_gb300 import afd as A
+    from combine_peer_slot_gb300 import runtime as R
+    from combine_peer_slot_gb300 import workloads as W
+
+    w = workload_of(args)
+    T = w.total_tokens
+    run = R.Runner(w, max_total_tokens=T)
+    stream = run.stream
+    A.afd_profile(run.ctx, True)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(w.layers)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(w.layers)]
+
+    def step(timed_stats=None):
+        fwd_ms = 0.0
+        for layer in range(w.layers):
+            run.pack_all(layer)
+            flush.zero_()
+            e0[layer].record(stream)
+            rc = run.forward(layer)
+            e1[layer].record(stream)
+            if rc:
+                raise A.AfdError(rc, "afd_ffn_forward")
+            if timed_stats is not None:
+                st = A.afd_stage_times(run.ctx)
+                for i, v in enumerate(st):
+                    timed_stats[i] += v
+        torch.cuda.synchronize()
+        for layer in range(w.layers):
+            fwd_ms += e0[layer].elapsed_time(e1[layer])
+        return fwd_ms
+
+    for _ in range(args.warmup):
+        step()
+    if run.poll() != 0:
+        raise RuntimeError("device error during warm-up")
+    stage_sum = [0.0] * A.AFD_NUM_STAGES
+    dev_index = getattr(torch.cuda.get_device_properties(local), "pci_bus_id", None) or local
+    launches0 = A.afd_launch_count(run.ctx)
+    total_ms = 0.0
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(dev_index) as clk:
+        t_wall = time.perf_counter()
+        for _ in range(args.steps):
+            total_ms += step(stage_sum)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    barrier(ws)
+    launches = A.afd_launch_count(run.ctx) - launches0
+    status = run.poll()
+    if status != 0:
+        raise RuntimeError(f"device error in the timed region: {A.strerror(status)}")
+    ms_step = total_ms / args.steps
+    ms_step_max = max_over_ranks(ms_step, ws)
+    tokens_step = T * w.layers
+    value = sum_over_ranks(tokens_step, ws) / (ms_step_max / 1e3)
+
+    # roofline of the whole path and of the dominant stage
+    pk, pk_kind = peaks()
+    cnt = run.workspace(A.AFD_WS_COUNTS, 4 * w.num_experts).cpu().numpy().view(np.int32)
+    flops, nbytes, t_roof, bound = path_roofline(w, T, int((cnt > 0).sum()), pk)
+    stages = {n: stage_sum[i] / (args.steps * w.layers) for i, n in enumerate(A.STAGE_NAMES)}
+    dom = max(stages, key=stages.get)
+    work = stage_work(w, T).get(dom, {})
+    if "flops" in work and dom.startswith("gemm"):
+        ach = work["flops"] / (stages[dom] / 1e3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"],
+                "peak_source": f"{pk_kind} bf16_tflops (burst)",
+                "algorithmic_flops_per_launch": work["flops"]}
+    else:
+        ach = work.get("bytes", 0) / (stages[dom] / 1e3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "peak_source": f"{pk_kind} hbm_gbs",
+                "algorithmic_bytes_per_launch": work.get("bytes", 0)}
+    roof["avg_launch_ms"] = stages[dom]
+    roof["traffic"] = traffic_from_profile(dom, args.workload)
+
+    # end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        dt = torch.bfloat16 if w.act == "bf16" else torch.float32
+        hx = [x.cpu().pin_memory() for x in run.x]
+        hout = [torch.empty((max(n, 1), w.hidden), dtype=dt).pin_memory() for n in w.seq_lens]
+        h2d = sum(x.numel() * x.element_size() for x in hx)
+        d2h = sum(n * w.hidden * w.act_bytes for n in w.seq_lens)
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                for layer in range(w.layers):
+                    for p in range(w.num_peers):
+                        run.x[p].copy_(hx[p], non_blocking=True)
+                    run.pack_all(layer)
+                    rc = run.forward(layer)
+                    if rc:
+                        raise A.AfdError(rc, "afd_ffn_forward")
+                    run.unpack_all()
+                    for p, n in enumerate(w.seq_lens):
+                        if n:
+                            hout[p][:n].copy_(run.out[p][:n], non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(max(2, args.warmup)):
+            e2e_step()
+        n_e2e = max(5, args.steps // 4)
+        barrier(ws)
+        t = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        t = (time.perf_counter() - t) / n_e2e
+        t = max_over_ranks(t, ws)
+        if run.poll() != 0:
+            raise RuntimeError("device error in the end-to-end loop")
+        e2e = {"value": sum_over_ranks(tokens_step, ws) / t, "unit": "tokens/s",
+               "ms_per_step": t * 1e3, "h2d_bytes_per_step": h2d * w.layers,
+               "d2h_bytes_per_step": d2h * w.layers,
+               "note": "pinned host x -> device, pack, forward, unpack, device -> pinned host"}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, budget_s=args.cpu_budget)
+
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; no model weights or dataset)",
+        "config": {"workload": args.workload, "peers": w.num_peers, "seq_lens": w.seq_lens,
+                   "total_tokens": T, "hidden": w.hidden, "experts": w.num_experts,
+                   "topk": w.topk, "inter": w.inter, "shared_inter": w.shared_inter,
+                   "layers": w.layers, "parallelism": f"replicas{ws}",
+                   "l2": "flushed (256 MB write) before every timed forward"},
+        "tflops": flops * w.layers / (ms_step_max / 1e3) / 1e12,
+        "path_roofline": {"bound": bound, "roofline_ms": t_roof * 1e3 * w.layers,
+                          "frac": t_roof * 1e3 * w.layers / ms_step_max,
+                          "flops_per_layer": flops, "bytes_per_layer": nbytes,
+                          "peak_source": pk_kind},
+        "roofline": roof, "stages_ms": stages, "gpu_launches": launches,
+        "wall_s_timed": t_wall, "clocks": clk.summary(), "e2e": e2e, "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(out))
+    run.close()
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_setup(w):
+    """Pack the workload into a host dispatch window for the oracle (the
+    oracle's own pack) and return what forward_tokens needs."""
+    import numpy as np
+    from combine_peer_slot_gb300 import workloads as W
+    from oracle import oracle as O
+    host = W.host_inputs(w)
+    L = O.slot_layout(w.num_peers, 1, w.token_cap, w.topk, w.hidden, w.act_bytes, w.num_experts,
+                      w.shared_inter > 0)
+    win = np.zeros(L.window_bytes, np.uint8)
+    for p, x in enumerate(host["x"]):
+        O.pack_slot(win, L, 1, p, 0, 0, x, w.hidden, w.act_bytes, w.token_cap, w.num_experts,
+                    w.shared_inter > 0, w.shared_inter > 0, p + 1)
+    wt = W.weights_to_numpy(W.expert_weights(w, 0, "cpu"))
+    wt["Wg"], wt["bias"] = host["Wg"], host["bias"]
+    cfg = dict(num_regions=w.num_peers, ring_depth=1, token_cap=w.token_cap, hidden=w.hidden,
+               act_bytes=w.act_bytes, num_experts=w.num_experts, topk=w.topk, inter=w.inter,
+               shared_inter=w.shared_inter, renorm=w.renorm, max_total_tokens=0,
+               routed_scaling=w.routed_scaling)
+    return cfg, win, wt
+
+
+def oracle_rate(w, cfg, win, wt, n_tokens, seed=0):
+    import numpy as np
+    from oracle import oracle as O
+    rng = np.random.default_rng(seed)
+    toks = np.sort(rng.choice(w.total_tokens, size=min(n_tokens, w.total_tokens), replace=False))
+    nthreads = os.cpu_count() or 1
+    t = time.perf_counter()
+    O.forward_tokens(cfg, win, wt, 0, w.seq_lens, list(range(w.num_peers)), toks,
+                     nthreads=nthreads)
+    return len(toks), time.perf_counter() - t, nthreads
+
+
+def cpu_baseline(w, budget_s=15.0):
+    cfg, win, wt = oracle_setup(w)
+    n, dt, nth = oracle_rate(w, cfg, win, wt, 32)
+    rate = n / dt
+    n_big = int(max(32, min(w.total_tokens, rate * budget_s)))
+    n2, dt2, nth = oracle_rate(w, cfg, win, wt, n_big, seed=1)
+    return {"value": n2 / dt2 * 1.0, "unit": "tokens/s", "cores": nth, "kind": "oracle",
+            "sample": f"{n2} tokens drawn uniformly from the {w.total_tokens}-token fan-in of "
+                      f"'{w.name}' (all layer-0 experts), {dt2:.1f} s of CPU work; "
+                      f"tokens/s counts one layer per token"}
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    w = workload_of(args)
+    cfg, win, wt = oracle_setup(w)
+    n, dt, nth = oracle_rate(w, cfg, win, wt, 16)
+    rate = n / dt
+    per_step = int(max(4, min(w.total_tokens, rate * args.ref_budget / max(1, args.steps + args.warmup))))
+    for i in range(args.warmup):
+        oracle_rate(w, cfg, win, wt, per_step, seed=100 + i)
+    tot_n, tot_t = 0, 0.0
+    for i in range(args.steps):
+        n, dt, nth = oracle_rate(w, cfg, win, wt, per_step, seed=i)
+        tot_n += n
+        tot_t += dt
+    value = tot_n / tot_t
+    sample = (f"{per_step} tokens per step drawn from the {w.total_tokens}-token fan-in of "
+              f"'{w.name}' (layer 0), {args.steps} steps")
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+           "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded; no model weights or dataset)",
+           "config": {"workload": args.workload, "peers": w.num_peers,
+                      "total_tokens": w.total_tokens, "hidden": w.hidden,
+                      "experts": w.num_experts, "topk": w.topk, "inter": w.inter,
+                      "shared_inter": w.shared_inter, "layers": w.layers,
+                      "parallelism": "host cores"},
+           "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nth, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+
+
+def workload_of(args):
+    from combine_peer_slot_gb300 import workloads as W
+    if args.seq_lens:
+        return W.custom(args.workload, seq_lens=[int(v) for v in args.seq_lens.split(",")])
+    return W.get(args.workload)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="v2lite_prefill",
+                    choices=["v2lite_prefill", "decode", "skewed", "fanin"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ref-budget", type=float, default=60.0)
+    ap.add_argument("--seq-lens", default="",
+                    help="comma-separated per-peer token counts replacing the workload's "
+                         "(smaller profiling cases of the same shapes)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = dist_init(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_ours(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -22,9 +22,9 @@ def ws_array(run, which, count, dtype):
 
 
 def slot_off(run, peer, stage=0):
+    """Byte offset of slot (peer, stage); the runner uses one stage per peer."""
     L = run.layout
-    return L.flags_bytes + (peer * run.w_ring + stage) * L.slot_bytes if hasattr(run, "w_ring") else \
-        L.flags_bytes + (peer * 1 + stage) * L.slot_bytes
+    return L.flags_bytes + (peer * run.cfg.ring_depth + stage) * L.slot_bytes
 
 
 def return_rows(ret, run, peer, n):
@@ -74,7 +74,7 @@ def run_and_compare_full(run, slots=None, layer=0):
     run.pack_all(layer)
     rc = run.forward(layer, slots=slots)
     assert rc == 0, A.strerror(rc)
-    outs = run.unpack_all()
+    outs = run.unpack_all(peers=slots)
     assert run.poll() == 0
     win = run.window(A.AFD_DIR_DISPATCH).cpu().numpy()
     ret = run.window(A.AFD_DIR_RETURN).cpu().numpy()

@@ -20,6 +20,7 @@ AFD_DIR_DISPATCH, AFD_DIR_RETURN = 0, 1
 (AFD_WS_IDS, AFD_WS_WEIGHTS, AFD_WS_COUNTS, AFD_WS_OFFSETS, AFD_WS_PERM, AFD_WS_INV, AFD_WS_XP,
  AFD_WS_H, AFD_WS_Y, AFD_WS_HS, AFD_WS_S, AFD_WS_STATUS) = range(12)
 AFD_HEADER_FIXED_WORDS = 12
+AFD_NOALLOC_MAX_ROUTER_WEIGHTS = 262144
 AFD_MAX_PEERS = 64
 
 
@@ -76,6 +77,7 @@ SIGNATURES = [
     ("afd_launch_count", _I64, [_P]),
     ("afd_strerror", C.c_char_p, [_I]),
     ("afd_profile", _I, [_P, _I]),
+    ("afd_route_noalloc", _I, [_P, _I, _I, _I, _P, _P, _I, _I, _I, _F, _P, _P, _P]),
     ("afd_stage_times", _I, [_P, C.POINTER(C.c_float), _I]),
 ]
 AFD_NUM_STAGES = 8
@@ -211,3 +213,13 @@ def afd_stage_times(ctx):
     ms = (C.c_float * AFD_NUM_STAGES)()
     _check(lib().afd_stage_times(ctx, ms, AFD_NUM_STAGES), "afd_stage_times")
     return [float(v) for v in ms]
+
+
+def afd_route_noalloc(x_ptr, n_tokens, hidden, act_dtype, Wg_ptr, bias_ptr, num_experts, topk,
+                      renorm, routed_scaling, ids_ptr, weights_ptr, stream=0):
+    """Router step with no device allocation (see include/afd.h)."""
+    return lib().afd_route_noalloc(x_ptr or None, int(n_tokens), int(hidden), int(act_dtype),
+                                   Wg_ptr or None, bias_ptr or None, int(num_experts),
+                                   int(topk), int(bool(renorm)), float(routed_scaling),
+                                   ids_ptr or None, weights_ptr or None,
+                                   C.c_void_p(int(stream)))

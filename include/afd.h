@@ -287,6 +287,32 @@ int64_t afd_launch_count(afd_ctx* ctx);
 int afd_profile(afd_ctx* ctx, int enable);
 int afd_stage_times(afd_ctx* ctx, float* ms, int n);
 
+/* Router without device allocation.  The pages have no counterpart: this
+ * entry point exists for callers that cannot call cudaMalloc -- a serving
+ * process whose memory pool already holds the device's free memory, or a
+ * plugin that must not cause the device-wide synchronisation an allocation
+ * or free can bring.  It computes exactly the router step of
+ * afd_ffn_forward (same kernel, same fp32 logit order, same top-k and gate
+ * weights) for a plain activation block:
+ *   x        device, act [n_tokens, hidden] row-major, 16-byte aligned
+ *   Wg       device fp32 [hidden, num_experts]; bias device fp32 [E] or NULL
+ *   ids      device int32 [n_tokens, topk] out; weights device fp32
+ *            [n_tokens, topk] out
+ *   cuda_stream  cudaStream_t the work is ordered on (NULL = legacy stream)
+ * Its scratch (the transposed router weight and a status word) is a
+ * file-scope device array of AFD_NOALLOC_MAX_ROUTER_WEIGHTS + 64 floats
+ * (about 1 MiB) that every GPU loading this library holds until exit; the
+ * first call on a device looks up that array's device address, so make the
+ * first call on each device before any stream capture.  All calls share
+ * the array: each call rewrites it and clears the status word first, and
+ * calls that overlap on the GPU race on it.  hidden * num_experts above
+ * the maximum returns AFD_ERR_CAPACITY; bad arguments AFD_ERR_ARG; a
+ * failing CUDA call AFD_ERR_CUDA.  Asynchronous; allocates nothing. */
+#define AFD_NOALLOC_MAX_ROUTER_WEIGHTS 262144
+int afd_route_noalloc(const void* x, int n_tokens, int hidden, int act_dtype, const float* Wg,
+                      const float* bias, int num_experts, int topk, int renorm,
+                      float routed_scaling, int32_t* ids, float* weights, void* cuda_stream);
+
 /* Static string for a status code. */
 const char* afd_strerror(int code);
 

@@ -1,0 +1,107 @@
+"""The C-ABI library without a GPU: it loads, exports every function that
+include/afd.h declares, and its host-only logic (slot layout, split sizes,
+argument validation) agrees with the independent oracle and the fixtures."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+from combine_peer_slot_gb300 import afd as A
+from combine_peer_slot_gb300 import build as B
+from oracle import oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if B.needs_build():
+        B.build()
+    return A.lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "afd.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(afd_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_function(lib):
+    names = declared_functions()
+    assert len(names) >= 19
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/afd.h but not exported"
+    bound = {n for n, _, _ in A.SIGNATURES}
+    assert set(names) == bound, set(names) ^ bound
+
+
+def test_strerror(lib):
+    for code in range(0, 14):
+        assert A.strerror(code) and A.strerror(code) != "unknown status"
+    assert A.strerror(99) == "unknown status"
+
+
+def test_layout_matches_oracle(golden, lib):
+    for case in golden("slot_layout_tiny.json")["cases"]:
+        cfg = A.make_config(case["num_regions"], case["token_cap"], case["hidden"],
+                            case["num_experts"], case["topk"], 64,
+                            shared_inter=64 if case["has_shared"] else 0,
+                            act="f32" if case["act_bytes"] == 4 else "bf16",
+                            ring_depth=case["ring_depth"], gemm=A.AFD_GEMM_SIMT)
+        assert A.afd_slot_layout(cfg).as_dict() == case["expect"]
+    rng = np.random.default_rng(2)
+    for _ in range(300):
+        P, D = int(rng.integers(1, 65)), int(rng.integers(1, 9))
+        cap, k = int(rng.integers(1, 20000)), int(rng.integers(1, 17))
+        H, E = int(rng.integers(1, 1025)) * 8, int(rng.integers(k, 257))
+        act = str(rng.choice(["bf16", "f32"]))
+        Is = int(rng.choice([0, 64]))
+        cfg = A.make_config(P, cap, H, E, k, 64, shared_inter=Is, act=act, ring_depth=D,
+                            gemm=A.AFD_GEMM_SIMT)
+        ours = A.afd_slot_layout(cfg).as_dict()
+        ref = O.slot_layout(P, D, cap, k, H, 2 if act == "bf16" else 4, E, Is > 0).as_dict()
+        assert ours == ref
+
+
+def test_split_sizes(golden, lib):
+    for c in golden("split_sizes.json")["cases"]:
+        rc, sizes = A.afd_split_sizes(c["total"], c["n_peers"], c["seq_lens"])
+        assert rc == c["status"], c
+        if rc == 0:
+            assert sizes == c["sizes"]
+
+
+def test_config_validation(lib):
+    ok = A.make_config(4, 8192, 2048, 64, 6, 1408, 2816)
+    assert A.afd_slot_layout(ok).window_bytes > 0
+    bad = [dict(num_peers=0), dict(num_peers=65), dict(topk=65), dict(hidden=0),
+           dict(ring_depth=0), dict(routed_cap_multiplier=0.5), dict(act_dtype=7)]
+    for b in bad:
+        cfg = A.make_config(4, 8192, 2048, 64, 6, 1408, 2816)
+        for k, v in b.items():
+            setattr(cfg, k, v)
+        assert A.lib().afd_slot_layout(C.byref(cfg), C.byref(A.afd_layout())) == A.AFD_ERR_ARG, b
+    unsupported = [dict(hidden=2044), dict(num_experts=300, topk=2), dict(topk=17),
+                   dict(inter=1400), dict(act_dtype=A.AFD_DTYPE_F32)]
+    for b in unsupported:
+        cfg = A.make_config(4, 8192, 2048, 64, 6, 1408, 2816)
+        for k, v in b.items():
+            setattr(cfg, k, v)
+        assert A.lib().afd_slot_layout(C.byref(cfg), C.byref(A.afd_layout())) == A.AFD_ERR_UNSUPPORTED, b
+
+
+def test_noalloc_rejects_without_touching_the_device(lib):
+    assert A.afd_route_noalloc(0, 4, 4104, A.AFD_DTYPE_BF16, 0, 0, 64, 6, 0, 1.0, 0, 0) == A.AFD_ERR_CAPACITY
+    assert A.afd_route_noalloc(0, 4, 100, A.AFD_DTYPE_BF16, 0, 0, 64, 6, 0, 1.0, 0, 0) == A.AFD_ERR_ARG
+    assert A.afd_route_noalloc(0, 0, 2048, A.AFD_DTYPE_BF16, 0, 0, 64, 6, 0, 1.0, 0, 0) == A.AFD_OK
+
+
+def test_create_without_gpu_fails_cleanly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(A.AfdError) as e:
+        A.afd_create(A.make_config(2, 128, 1024, 16, 4, 512, 512))
+    assert e.value.code == A.AFD_ERR_CUDA

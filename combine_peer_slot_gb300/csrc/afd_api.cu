@@ -134,7 +134,9 @@ int validate_config(const afd_config* c) {
   // kernel coverage: 16-byte rows, <= 256 experts, k <= 16
   if (c->hidden % 8 || c->num_experts > 256 || c->topk > 16) return AFD_ERR_UNSUPPORTED;
   if (c->act_dtype == AFD_DTYPE_F32 && c->gemm == AFD_GEMM_TENSOR) return AFD_ERR_UNSUPPORTED;
-  if (c->gemm == AFD_GEMM_TENSOR && (c->inter % 16 || c->shared_inter % 16)) return AFD_ERR_UNSUPPORTED;
+  // tensor-core engine: 16-row gate/up blocks, 32-feature epilogue quadrants
+  if (c->gemm == AFD_GEMM_TENSOR && (c->inter % 16 || c->shared_inter % 16 || c->hidden % 32))
+    return AFD_ERR_UNSUPPORTED;
   const int64_t tmax = c->max_total_tokens ? c->max_total_tokens : (int64_t)c->num_peers * c->token_cap;
   if (tmax * c->topk + tmax > (int64_t)1 << 30) return AFD_ERR_UNSUPPORTED;
   return AFD_OK;

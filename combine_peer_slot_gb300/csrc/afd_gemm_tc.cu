@@ -17,11 +17,13 @@
 //    them and h = silu(g) * u is written as bf16.
 //  - plain mode: y = h . Wd^T with Wd[e] = [hidden, inter] as a 3-D map.
 //
-// Warp roles (192 threads, one CTA per SM, persistent over the tile table
+// Warp roles (320 threads, one CTA per SM, persistent over the tile table
 // built on the device from the expert counts):
 //   warp 0  TMA producer (one lane), STAGES-deep smem ring
 //   warp 1  TMEM allocator and MMA issuer (one lane)
-//   warps 2-5 epilogue: TMEM -> registers -> global (quadrant = warp % 4)
+//   warps 2-9 epilogue: TMEM -> registers -> smem transpose -> 16-byte
+//           global stores (lane quadrant = warp % 4, two warps per quadrant
+//           take alternate 32-column chunks)
 // Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile run
 // under the main loop of the next.  Every mbarrier wait is bounded.
 #include "afd_internal.cuh"
@@ -37,12 +39,19 @@ constexpr int B_BOX_ROWS = 32;
 constexpr int B_BOX_BYTES = B_BOX_ROWS * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARPS = 8;        // two per TMEM lane quadrant
+constexpr int NUM_THREADS = 64 + EPI_WARPS * 32;
 constexpr int TMEM_COLS = 512;
+// per epilogue warp: a 32-token transpose buffer for bf16 outputs, rows
+// padded so neither the column writes nor the row reads conflict on banks.
+// SwiGLU rows hold 16 values (32 B) at a 48-byte pitch, rows 16-31 shifted by
+// 32 B; down-projection rows hold 32 values (64 B) at an 80-byte pitch.
+constexpr int EPI_PITCH_SWIGLU = 48;
+constexpr int EPI_PITCH_BF16 = 80;
+constexpr int EPI_BUF_BYTES = 32 * EPI_PITCH_BF16;
 constexpr uint64_t kGemmTimeoutNs = 5000000000ull;
 
 struct SmemTail {
-  GemmPlan plan;
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
   uint64_t tfull[2];
@@ -53,7 +62,12 @@ struct SmemTail {
   int skip;
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(SmemTail);
+// layout after the 1024-aligned base: stages | barriers (SmemTail) | epilogue
+// buffers at a 128-byte boundary (16-byte vector loads read them)
+constexpr size_t kEpiOffset = ((size_t)STAGES * STAGE_BYTES + sizeof(SmemTail) + 127) / 128 * 128;
+constexpr size_t kSmemBytes = 1024 + kEpiOffset + (size_t)EPI_WARPS * EPI_BUF_BYTES;
+static_assert(kEpiOffset % 128 == 0 && EPI_BUF_BYTES % 128 == 0, "epilogue buffers must stay aligned");
+static_assert(kSmemBytes <= 232448, "over the per-CTA shared memory limit");
 
 // shared-memory matrix descriptor: K-major, 128-byte swizzle, rows of 128 B,
 // 8-row core groups 1024 B apart (SBO), descriptor version 1
@@ -114,7 +128,9 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   }
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+// silu(g) = g / (1 + e^-g); the fast divide returns 0 once the denominator
+// passes 2^126, which is silu's limit there
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1) k_gemm_tc(const __grid_constant__ GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
@@ -122,12 +138,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_gemm_tc(const __grid_constan
   SmemTail* tail = reinterpret_cast<SmemTail*>(smem + (size_t)STAGES * STAGE_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  const GemmPlan& plan = *args.plan;  // tile table, built by the plan kernel
   if (threadIdx.x == 0) tail->skip = read_status(args.status);
-  {
-    const int* src = reinterpret_cast<const int*>(args.plan);
-    int* dst = reinterpret_cast<int*>(&tail->plan);
-    for (int i = threadIdx.x; i < (int)(sizeof(GemmPlan) / 4); i += blockDim.x) dst[i] = src[i];
-  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; s++) {
       mbar_init(smem_u32(&tail->full[s]), 1);
@@ -135,14 +147,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_gemm_tc(const __grid_constan
     }
     for (int b = 0; b < 2; b++) {
       mbar_init(smem_u32(&tail->tfull[b]), 1);
-      mbar_init(smem_u32(&tail->tempty[b]), 4);
+      mbar_init(smem_u32(&tail->tempty[b]), EPI_WARPS);
     }
     mbar_init(smem_u32(&tail->drain), 1);
     tail->abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  if (tail->skip || tail->plan.total_tiles <= (int)blockIdx.x) return;  // uniform for the CTA
+  if (tail->skip || plan.total_tiles <= (int)blockIdx.x) return;  // uniform for the CTA
 
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -154,7 +166,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_gemm_tc(const __grid_constan
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = tail->tmem_base;
-  const GemmPlan& plan = tail->plan;
   const int total = plan.total_tiles;
   const uint64_t deadline = globaltimer_ns() + kGemmTimeoutNs;
   volatile int* abort_flag = &tail->abort_flag;
@@ -240,8 +251,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_gemm_tc(const __grid_constan
       while (!mbar_try_wait(smem_u32(&tail->drain), 0) && globaltimer_ns() < dl) {}
     }
   } else {
-    // ------------------------------ epilogue (warps 2..5)
+    // ------------------------------ epilogue (warps 2..9)
+    // warp -> TMEM lane quadrant q = warp % 4 and column half (even or odd
+    // 32-column chunks).  Each chunk goes TMEM -> registers -> a per-warp
+    // smem transpose -> one token row per lane -> 16-byte global stores.
     const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    uint8_t* ebuf = smem + kEpiOffset + (size_t)(warp - 2) * EPI_BUF_BYTES;
+    const bool lo = lane < 16;
     int acc = 0;
     uint32_t acc_ph = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -254,50 +271,75 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_gemm_tc(const __grid_constan
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       const int kind = t.kind;
       const int64_t ldo = args.ldo[kind];
-      const int out_f32 = args.out_f32[kind];
       const int64_t row0 = (int64_t)G.out_row0 + (int64_t)t.nt * plan.bn;
       if (args.swiglu) {
-        const int col = t.mt * 64 + q * 16 + (lane & 15);
-        const bool col_ok = col < args.M[kind] / 2;
-        const int my_par = lane >> 4;  // lanes 0-15 take even columns, 16-31 odd
-        for (int c0 = 0; c0 < t.rows; c0 += 32) {
+        // lanes 0-15 hold gate rows i = base + lane, lanes 16-31 the up rows
+        // of the same i; lane < 16 produces tokens 0-15 of the chunk, lane
+        // >= 16 tokens 16-31, after one exchange of 16 values
+        const int col0 = t.mt * 64 + q * 16;
+        const bool cols_ok = col0 + 16 <= args.M[kind] / 2;
+        for (int c0 = half * 32; c0 < t.rows; c0 += 64) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(taddr + (uint32_t)c0, v);
           tmem_ld_wait();
+          uint16_t* sb = reinterpret_cast<uint16_t*>(ebuf);
 #pragma unroll
-          for (int c = 0; c < 32; c++) {
-            const float mine = __uint_as_float(v[c]);
-            const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
-            if ((c & 1) == my_par) {
-              const float g = (lane < 16) ? mine : other;
-              const float u = (lane < 16) ? other : mine;
-              const int r = c0 + c;
-              if (r < t.rows && col_ok) {
-                const float hv = silu_f(g) * u;
-                const int64_t o = (row0 + r) * ldo + col;
-                if (out_f32) reinterpret_cast<float*>(args.out[kind])[o] = hv;
-                else reinterpret_cast<__nv_bfloat16*>(args.out[kind])[o] = __float2bfloat16_rn(hv);
-              }
-            }
+          for (int j = 0; j < 16; j++) {
+            const float a = __uint_as_float(v[j]), b = __uint_as_float(v[16 + j]);
+            const float recv = __shfl_xor_sync(0xffffffffu, lo ? b : a, 16);
+            const float g = lo ? a : recv;
+            const float u = lo ? recv : b;
+            const __nv_bfloat16 hv = __float2bfloat16_rn(silu_f(g) * u);
+            const int tok = lo ? j : 16 + j;   // row of the transpose buffer
+            sb[(tok * EPI_PITCH_SWIGLU + (lo ? 0 : 32)) / 2 + (lane & 15)] =
+                *reinterpret_cast<const uint16_t*>(&hv);
           }
+          __syncwarp();
+          const int r = c0 + lane;
+          if (r < t.rows && cols_ok) {
+            const uint4* src =
+                reinterpret_cast<const uint4*>(ebuf + lane * EPI_PITCH_SWIGLU + (lo ? 0 : 32));
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(args.out[kind]) +
+                                                  (row0 + r) * ldo + col0);
+            dst[0] = src[0];
+            dst[1] = src[1];
+          }
+          __syncwarp();
         }
       } else {
-        const int col = t.mt * BM + q * 32 + lane;
-        const bool col_ok = col < args.M[kind];
-        for (int c0 = 0; c0 < t.rows; c0 += 32) {
+        const int col0 = t.mt * BM + q * 32;
+        const bool cols_ok = col0 + 32 <= args.M[kind];
+        const int out_f32 = args.out_f32[kind];
+        for (int c0 = half * 32; c0 < t.rows; c0 += 64) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(taddr + (uint32_t)c0, v);
           tmem_ld_wait();
+          const int r = c0 + lane;
+          if (out_f32) {
+            // lane = feature: each store is 32 consecutive fp32 of one token row
+            if (cols_ok) {
+              float* dst = reinterpret_cast<float*>(args.out[kind]) + (row0 + c0) * ldo + col0 + lane;
 #pragma unroll
-          for (int c = 0; c < 32; c++) {
-            const int r = c0 + c;
-            if (r < t.rows && col_ok) {
-              const int64_t o = (row0 + r) * ldo + col;
-              const float yv = __uint_as_float(v[c]);
-              if (out_f32) reinterpret_cast<float*>(args.out[kind])[o] = yv;
-              else reinterpret_cast<__nv_bfloat16*>(args.out[kind])[o] = __float2bfloat16_rn(yv);
+              for (int c = 0; c < 32; c++)
+                if (c0 + c < t.rows) dst[(int64_t)c * ldo] = __uint_as_float(v[c]);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; c++) {
+              const __nv_bfloat16 yv = __float2bfloat16_rn(__uint_as_float(v[c]));
+              *reinterpret_cast<uint16_t*>(ebuf + c * EPI_PITCH_BF16 + lane * 2) =
+                  *reinterpret_cast<const uint16_t*>(&yv);
+            }
+            __syncwarp();
+            if (r < t.rows && cols_ok) {
+              const uint4* src = reinterpret_cast<const uint4*>(ebuf + lane * EPI_PITCH_BF16);
+              uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(args.out[kind]) +
+                                                    (row0 + r) * ldo + col0);
+#pragma unroll
+              for (int x = 0; x < 4; x++) dst[x] = src[x];
             }
           }
+          __syncwarp();
         }
       }
       tc_fence_before();

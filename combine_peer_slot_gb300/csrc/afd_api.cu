@@ -137,6 +137,9 @@ int validate_config(const afd_config* c) {
   // tensor-core engine: 16-row gate/up blocks, 32-feature epilogue quadrants
   if (c->gemm == AFD_GEMM_TENSOR && (c->inter % 16 || c->shared_inter % 16 || c->hidden % 32))
     return AFD_ERR_UNSUPPORTED;
+  // the router keeps 16 token rows and a weight ring in shared memory
+  if (router_min_smem_bytes(c->hidden, c->num_experts, c->act_dtype == AFD_DTYPE_F32) > 232448)
+    return AFD_ERR_UNSUPPORTED;
   const int64_t tmax = c->max_total_tokens ? c->max_total_tokens : (int64_t)c->num_peers * c->token_cap;
   if (tmax * c->topk + tmax > (int64_t)1 << 30) return AFD_ERR_UNSUPPORTED;
   return AFD_OK;
@@ -288,7 +291,8 @@ int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out) {
       {Tm * k * H * yb},                     // y
       {Tm * (Is > 0 ? Is : 1) * ab},         // hs
       {Tm * H * 4},                          // s
-      {(int64_t)sizeof(GemmPlan)}, {(int64_t)sizeof(GemmPlan)}};
+      {(int64_t)sizeof(GemmPlan)}, {(int64_t)sizeof(GemmPlan)},
+      {E * router_blocks((int)Tm) * 4}, {E * router_blocks((int)Tm) * 4}};  // hist, base
   const int nparts = sizeof(parts) / sizeof(parts[0]);
   int64_t offs[32], total = 0;
   for (int i = 0; i < nparts; i++) {
@@ -316,7 +320,8 @@ int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out) {
   c->ws.y = b + offs[13];
   c->ws.hs = b + offs[14];
   c->ws.s = reinterpret_cast<float*>(b + offs[15]);
-  c->ws.wgt = nullptr;
+  c->ws.hist = reinterpret_cast<int32_t*>(b + offs[18]);
+  c->ws.base = reinterpret_cast<int32_t*>(b + offs[19]);
   c->plan1 = reinterpret_cast<GemmPlan*>(b + offs[16]);
   c->plan2 = reinterpret_cast<GemmPlan*>(b + offs[17]);
   const int ws_map[12] = {4, 5, 6, 7, 8, 9, 11, 12, 13, 14, 15, 0};
@@ -457,12 +462,13 @@ int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, con
   if (rc) return rc;
   ctx->mark(1);
   rc = cuda_fail(launch_router(lc, ctx->geom, ctx->win[0], f, ws, c.hidden, ctx->act_f32, L.WgT,
-                               L.bias, c.num_experts, c.topk, c.renorm, c.routed_scaling),
+                               L.bias, c.num_experts, c.topk, c.renorm, c.routed_scaling,
+                               ws.hist),
                  "router");
   if (rc) return rc;
   ctx->mark(2);
   rc = cuda_fail(launch_plan(lc, f, ws, c.num_experts, c.topk, c.inter, c.shared_inter, c.hidden,
-                             has_shared, bn, ctx->plan1, ctx->plan2),
+                             has_shared, bn, ctx->plan1, ctx->plan2, ws.hist, ws.base),
                  "plan");
   if (rc) return rc;
   ctx->mark(3);

@@ -50,7 +50,8 @@ struct DevWS {
   void* y;                // act [Tmax * k, H]
   void* hs;               // act [Tmax, Is]
   float* s;               // f32 [Tmax, H]
-  float* wgt;             // unused slot
+  int32_t* hist;          // [E, router CTAs] per-CTA expert histograms
+  int32_t* base;          // [E, router CTAs] each CTA's first slot in each expert segment
 };
 
 // one group of the grouped GEMM: rows of the B operand (tokens) that share
@@ -238,13 +239,16 @@ cudaError_t launch_pack_header(const LaunchCtx& lc, const WinGeom& g, uint8_t* w
 cudaError_t launch_header_check(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                                 const FanIn& f, const DevWS& ws, int num_experts,
                                 int token_cap, int has_shared_expert, int64_t timeout_ns);
+// CTAs of the router for T tokens (16 tokens each); sizes the histograms
+int router_blocks(int total_tokens);
+size_t router_min_smem_bytes(int hidden, int E, int act_f32);
 cudaError_t launch_router(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                           const FanIn& f, const DevWS& ws, int hidden, int act_f32,
                           const float* WgT, const float* bias, int E, int k, int renorm,
-                          float scale);
+                          float scale, int32_t* hist);
 cudaError_t launch_plan(const LaunchCtx& lc, const FanIn& f, const DevWS& ws, int E, int k,
                         int inter, int shared_inter, int hidden, int has_shared, int bn,
-                        GemmPlan* plan1, GemmPlan* plan2);
+                        GemmPlan* plan1, GemmPlan* plan2, const int32_t* hist, int32_t* base);
 cudaError_t launch_gather(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                           const FanIn& f, const DevWS& ws, int k, int row_bytes,
                           int has_shared);

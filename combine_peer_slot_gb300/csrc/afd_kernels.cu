@@ -7,6 +7,7 @@
 namespace {
 
 constexpr int kThreads = 256;
+constexpr size_t kRouterSmemLimit = 232448;  // per-CTA opt-in shared memory
 
 __device__ __forceinline__ uint8_t* slot_ptr(uint8_t* win, const WinGeom& g, int region,
                                              int stage) {
@@ -177,89 +178,209 @@ __global__ void k_header_check(const uint8_t* win, WinGeom g, FanIn f, DevWS ws,
 // a1: router.  logits in the canonical fp32 order: lane l of a warp owns the
 // fused multiply-add chain over h = l, l+32, ... ascending (from +0), then a
 // butterfly with xor offsets 16, 8, 4, 2, 1, then + bias.  Top-k on the
-// logits (ties -> lower expert index), softmax over all E for the weights.
-// Block: 16 warps x 16 tokens; warp w owns experts [4w', 4w'+4) for
-// w' = w, w+16, ...  Wg is read transposed ([E, hidden]) so each expert's
-// column is coalesced.
+// logits (ties -> lower expert index, NaN below every number), softmax over
+// all E for the weights.
+// CTA: 16 warps x 16 tokens.  The tokens are staged transposed in smem
+// ([h][16 tokens]) straight from the peer slots, so a lane fetches its 16
+// values of one h with 16-byte loads; the transposed router weight streams
+// through a double-buffered cp.async ring of [64 experts][128 h] chunks.
+// Warp w owns experts 4w..4w+3 of the current 64-expert group.  The CTA
+// also writes its per-expert histogram (hist[e][cta]) for the plan.
 // ---------------------------------------------------------------------------
-// exp(a - b) for fp32 a >= ... b: the difference is split exactly into
-// s + err (two-sum), so exp(a - b) = expf(s) * (1 + err) to first order.
-__device__ __forceinline__ double exp_of_diff(float a, float b) {
+// Float-float helpers for the softmax: a value carried as hi + lo with the
+// rounding error of every addition kept (two-sum), so sums of E terms carry
+// no accumulated rounding and no fp64 arithmetic is needed.
+struct ffloat {
+  float hi, lo;
+};
+__device__ __forceinline__ ffloat ff_add(ffloat a, float b) {
+  const float s = __fadd_rn(a.hi, b);
+  const float bb = __fsub_rn(s, a.hi);
+  const float e = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return {s, __fadd_rn(a.lo, e)};
+}
+__device__ __forceinline__ ffloat ff_add(ffloat a, ffloat b) {
+  ffloat r = ff_add(a, b.hi);
+  r.lo = __fadd_rn(r.lo, b.lo);
+  return r;
+}
+__device__ __forceinline__ ffloat ff_shfl_xor(ffloat a, int off) {
+  return {__shfl_xor_sync(0xffffffffu, a.hi, off), __shfl_xor_sync(0xffffffffu, a.lo, off)};
+}
+// a / (d.hi + d.lo) to about one ulp
+__device__ __forceinline__ float ff_div(float a, ffloat d) {
+  const float q = __fdiv_rn(a, d.hi);
+  return __fmaf_rn(-q, __fdiv_rn(d.lo, d.hi), q);
+}
+// exp(a - b): the difference is split exactly into s + err (two-sum), so
+// exp(a - b) = expf(s) * (1 + err) to first order.
+__device__ __forceinline__ float exp_of_diff(float a, float b) {
   const float s = __fsub_rn(a, b);
   const float bb = __fsub_rn(s, a);
   const float err = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(-b, bb));
-  return (double)expf(s) * (1.0 + (double)err);
+  const float e = expf(s);
+  return __fmaf_rn(e, err, e);
 }
 
-constexpr int kRtTok = 16;
-constexpr int kRtWarps = 16;
-constexpr int kRtEpw = 4;
+constexpr int kRtTok = 16;                     // tokens per CTA
+constexpr int kRtWarps = 32;
+constexpr int kRtTpw = 8;                      // tokens per warp
+constexpr int kRtEpw = 4;                      // experts per warp
+constexpr int kRtEgroup = (kRtWarps / (kRtTok / kRtTpw)) * kRtEpw;   // 64 experts per pass
+constexpr int kRtHc = 128;                     // h per weight chunk
 
-template <bool ACT_F32>
-__global__ void __launch_bounds__(kRtWarps * 32)
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// stage weight chunk c of expert group e_base: WgT[e_base + r][c*128 .. +128)
+__device__ __forceinline__ void router_stage_w(float* dst, const float* __restrict__ WgT, int e_base,
+                                               int E, int hidden, int c) {
+  const int h0 = c * kRtHc;
+  for (int p = threadIdx.x; p < kRtEgroup * (kRtHc / 4); p += blockDim.x) {
+    const int r = p / (kRtHc / 4), q = p % (kRtHc / 4);
+    const int e = e_base + r, h = h0 + q * 4;
+    if (e < E && h < hidden) cp_async16(dst + r * kRtHc + q * 4, WgT + (int64_t)e * hidden + h);
+  }
+}
+
+// Token tile held in smem as XS (fp32, or bf16 bits when fp32 would not fit)
+// in 16-byte groups of tokens, group-major ([group][h][tokens of the group]):
+// the lane owning h reads a group with one 16-byte load, contiguous across
+// the warp's lanes (no bank conflicts).
+template <typename XS>
+__device__ __forceinline__ size_t xt_index(int h, int tt, int hidden) {
+  constexpr int per = 16 / sizeof(XS);
+  return ((size_t)(tt / per) * hidden + h) * per + (tt % per);
+}
+
+template <typename XS>
+__device__ __forceinline__ void load_tokens(const XS* xT, int h, int tt0, int hidden, float (&xv)[kRtTpw]) {
+  if constexpr (sizeof(XS) == 4) {
+#pragma unroll
+    for (int q = 0; q < kRtTpw / 4; q++) {
+      const float4 v4 = *reinterpret_cast<const float4*>(xT + xt_index<XS>(h, tt0 + 4 * q, hidden));
+      xv[4 * q] = v4.x; xv[4 * q + 1] = v4.y; xv[4 * q + 2] = v4.z; xv[4 * q + 3] = v4.w;
+    }
+  } else {
+    const uint4 v4 = *reinterpret_cast<const uint4*>(xT + xt_index<XS>(h, tt0, hidden));
+    const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+    for (int m = 0; m < 4; m++) {
+      xv[2 * m] = __uint_as_float(w4[m] << 16);
+      xv[2 * m + 1] = __uint_as_float(w4[m] & 0xffff0000u);
+    }
+  }
+}
+
+// a1 router.  logits in the canonical fp32 order: lane l of a warp owns the
+// fused multiply-add chain over h = l, l+32, ... ascending (from +0), then a
+// butterfly with xor offsets 16, 8, 4, 2, 1, then + bias.  Top-k on the
+// logits (ties -> lower expert index, NaN below every number), softmax over
+// all E for the gate weights.  CTA: 32 warps over 16 tokens; warp w owns
+// tokens 8*(w/16) .. +8 and experts 4*(w%16) .. +4 of the current 64-expert
+// pass, the transposed router weight streaming through a double-buffered
+// cp.async ring of [64 experts][128 h] chunks.  The CTA also writes its
+// per-expert histogram (hist[e][cta]) for the plan.
+template <bool ACT_F32, typename XS>
+__global__ void __launch_bounds__(kRtWarps * 32, 1)
 k_router(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int hidden,
          const float* __restrict__ WgT, const float* __restrict__ bias, int E, int k,
-         int renorm, float scale) {
+         int renorm, float scale, int32_t* __restrict__ hist, int nblocks) {
   extern __shared__ __align__(16) uint8_t rt_smem[];
   using act_t = typename std::conditional<ACT_F32, float, uint16_t>::type;
-  act_t* xs = reinterpret_cast<act_t*>(rt_smem);                       // [kRtTok][hidden]
-  float* lg = reinterpret_cast<float*>(rt_smem + (size_t)kRtTok * hidden * sizeof(act_t));  // [kRtTok][E]
+  XS* xT = reinterpret_cast<XS*>(rt_smem);                                        // [hidden][16]
+  float* wbuf = reinterpret_cast<float*>(rt_smem + (size_t)hidden * kRtTok * sizeof(XS));  // [2][64][128]
+  float* lg = wbuf + 2 * kRtEgroup * kRtHc;                                      // [16][E]
+  int* hs = reinterpret_cast<int*>(lg + kRtTok * E);                             // [E]
   if (read_status(ws.status)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.x * kRtTok;
   const int row_bytes = hidden * (int)sizeof(act_t);
-  // stage the token rows straight from the peer slots (16-byte vectors)
-  for (int tt = warp; tt < kRtTok; tt += kRtWarps) {
+  constexpr int kVecElems = 16 / sizeof(act_t);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hs[e] = 0;
+  // stage the 16 token rows straight from the peer slots, transposed
+  {
+    const int tt = threadIdx.x % kRtTok;
     const int t = t0 + tt;
-    uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)tt * hidden);
+    const int nvec = row_bytes / 16;
+    const uint4* src = nullptr;
     if (t < f.total) {
       const int i = entry_of(f, t);
-      const uint4* src = reinterpret_cast<const uint4*>(
-          slot_ptr(win, g, f.region[i], f.stage) + g.routed_x + (int64_t)(t - f.prefix[i]) * row_bytes);
-      for (int v = lane; v < row_bytes / 16; v += 32) dst[v] = src[v];
-    } else {
-      for (int v = lane; v < row_bytes / 16; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+      src = reinterpret_cast<const uint4*>(slot_ptr(win, g, f.region[i], f.stage) + g.routed_x +
+                                           (int64_t)(t - f.prefix[i]) * row_bytes);
+    }
+    for (int v = threadIdx.x / kRtTok; v < nvec; v += blockDim.x / kRtTok) {
+      const uint4 val = src ? src[v] : make_uint4(0, 0, 0, 0);
+      const act_t* e8 = reinterpret_cast<const act_t*>(&val);
+#pragma unroll
+      for (int m = 0; m < kVecElems; m++) {
+        XS xs;
+        if constexpr (sizeof(XS) == sizeof(act_t)) xs = e8[m];
+        else xs = __uint_as_float((uint32_t)e8[m] << 16);   // bf16 -> fp32, exact
+        xT[xt_index<XS>(v * kVecElems + m, tt, hidden)] = xs;
+      }
     }
   }
-  __syncthreads();
-  for (int eg = warp; eg * kRtEpw < E; eg += kRtWarps) {
-    const int e0 = eg * kRtEpw;
-    float acc[kRtTok][kRtEpw];
+  const int th = warp / (kRtWarps / 2);            // token half
+  const int eg = warp % (kRtWarps / 2);            // expert group within the pass
+  const int tt0 = th * kRtTpw;
+  const int nchunks = (hidden + kRtHc - 1) / kRtHc;
+  for (int e_base = 0; e_base < E; e_base += kRtEgroup) {
+    const int e0 = e_base + eg * kRtEpw;
+    float acc[kRtTpw][kRtEpw];
 #pragma unroll
-    for (int a = 0; a < kRtTok; a++)
+    for (int a = 0; a < kRtTpw; a++)
 #pragma unroll
       for (int b = 0; b < kRtEpw; b++) acc[a][b] = 0.0f;
-    for (int h = lane; h < hidden; h += 32) {
-      float wv[kRtEpw];
+    router_stage_w(wbuf, WgT, e_base, E, hidden, 0);
+    cp_async_commit();
+    for (int c = 0; c < nchunks; c++) {
+      if (c + 1 < nchunks) router_stage_w(wbuf + ((c + 1) & 1) * kRtEgroup * kRtHc, WgT, e_base, E, hidden, c + 1);
+      cp_async_commit();
+      cp_async_wait1();
+      __syncthreads();
+      const float* wc = wbuf + (c & 1) * kRtEgroup * kRtHc + (eg * kRtEpw) * kRtHc;
+      if (e0 < E) {
 #pragma unroll
-      for (int b = 0; b < kRtEpw; b++)
-        wv[b] = (e0 + b < E) ? __ldg(WgT + (int64_t)(e0 + b) * hidden + h) : 0.0f;
+        for (int i = 0; i < kRtHc / 32; i++) {
+          const int hl = lane + 32 * i;
+          const int h = c * kRtHc + hl;
+          if (h < hidden) {
+            float xv[kRtTpw];
+            load_tokens<XS>(xT, h, tt0, hidden, xv);
+            float wv[kRtEpw];
 #pragma unroll
-      for (int a = 0; a < kRtTok; a++) {
-        float xv;
-        if constexpr (ACT_F32) xv = xs[(size_t)a * hidden + h];
-        else xv = bf16_bits_to_f32(xs[(size_t)a * hidden + h]);
+            for (int b = 0; b < kRtEpw; b++) wv[b] = wc[b * kRtHc + hl];
 #pragma unroll
-        for (int b = 0; b < kRtEpw; b++) acc[a][b] = __fmaf_rn(xv, wv[b], acc[a][b]);
+            for (int a = 0; a < kRtTpw; a++)
+#pragma unroll
+              for (int b = 0; b < kRtEpw; b++) acc[a][b] = __fmaf_rn(xv[a], wv[b], acc[a][b]);
+          }
+        }
       }
+      __syncthreads();
     }
+    if (e0 < E) {
 #pragma unroll
-    for (int a = 0; a < kRtTok; a++)
+      for (int a = 0; a < kRtTpw; a++)
 #pragma unroll
-      for (int b = 0; b < kRtEpw; b++) {
-        float v = acc[a][b];
+        for (int b = 0; b < kRtEpw; b++) {
+          float v = acc[a][b];
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
-        acc[a][b] = v;
-      }
-    // lane a (< kRtTok) writes token a's logits
+          for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
+          acc[a][b] = v;
+        }
 #pragma unroll
-    for (int a = 0; a < kRtTok; a++)
-      if (lane == a)
+      for (int a = 0; a < kRtTpw; a++)
+        if (lane == a)
 #pragma unroll
-        for (int b = 0; b < kRtEpw; b++)
-          if (e0 + b < E)
-            lg[a * E + e0 + b] = bias ? __fadd_rn(acc[a][b], bias[e0 + b]) : acc[a][b];
+          for (int b = 0; b < kRtEpw; b++)
+            if (e0 + b < E)
+              lg[(tt0 + a) * E + e0 + b] = bias ? __fadd_rn(acc[a][b], bias[e0 + b]) : acc[a][b];
+    }
   }
   __syncthreads();
   // top-k and gate weights: one warp per token
@@ -291,109 +412,85 @@ k_router(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int hidden,
       if (j == 0) top_logit = bv;
       if (lane == j) { my_id = bi; my_logit = bv; }
     }
-    // softmax over all E relative to the maximum; the denominator and the
-    // renormalisation sum are accumulated in fp64
-    double den = 0.0;
-    for (int m = 0; m * 32 + lane < E; m++) den += exp_of_diff(l[m * 32 + lane], top_logit);
+    // softmax over all E relative to the maximum, sums carried as float-float
+    ffloat den = {0.0f, 0.0f};
+    for (int m = 0; m * 32 + lane < E; m++) den = ff_add(den, exp_of_diff(l[m * 32 + lane], top_logit));
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-    const double p = (lane < k) ? exp_of_diff(my_logit, top_logit) / den : 0.0;
-    double psum = p;
+    for (int off = 16; off >= 1; off >>= 1) den = ff_add(den, ff_shfl_xor(den, off));
+    const float p = (lane < k) ? ff_div(exp_of_diff(my_logit, top_logit), den) : 0.0f;
+    ffloat psum = {p, 0.0f};
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, off);
+    for (int off = 16; off >= 1; off >>= 1) psum = ff_add(psum, ff_shfl_xor(psum, off));
     if (lane < k) {
-      const double v = renorm ? p / psum : p;
+      const float v = renorm ? ff_div(p, psum) : p;
       ws.ids[(int64_t)t * k + lane] = my_id;
-      ws.w[(int64_t)t * k + lane] = (float)(v * (double)scale);
+      ws.w[(int64_t)t * k + lane] = __fmul_rn(v, scale);
+      atomicAdd(&hs[my_id], 1);
     }
   }
+  __syncthreads();
+  if (hist)
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(int64_t)e * nblocks + blockIdx.x] = hs[e];
 }
 
 // ---------------------------------------------------------------------------
-// a2/a3 plan: per-expert counts, exclusive offsets, the stable permutation
-// of the flattened partial index f = t*k + j (a stable counting sort by
-// expert, equal to argsort(stable=True) of the flattened ids, Async GPU
-// Connector, "Data flow" step 1), per-peer counts for the return headers,
-// and the tile tables of both grouped GEMMs.  One CTA of 32 warps: warp w
-// owns a contiguous chunk of f; per-warp histograms give each warp's base
-// per expert; within a warp, 32-element groups are ranked with match_any.
+// a2 plan, part 1 (one CTA): per-expert counts and exclusive offsets from the
+// router CTAs' histograms (bincount + cumsum, Async GPU Connector, "Data
+// flow" step 1), each router CTA's base position within each expert's
+// segment (base[e][b] = sum of hist[e][b'] for b' < b), the zeroed per-peer
+// counts, and the tile tables of both grouped GEMMs.
 // ---------------------------------------------------------------------------
-constexpr int kPlanWarps = 32;
+constexpr int kScanWarps = 32;
 
-__global__ void __launch_bounds__(kPlanWarps * 32)
-k_plan(FanIn f, DevWS ws, int E, int k, int inter, int shared_inter, int hidden, int has_shared,
-       int bn, GemmPlan* plan1, GemmPlan* plan2) {
-  extern __shared__ __align__(16) int pl_smem[];
-  int* hist = pl_smem;                          // [kPlanWarps][E]
-  int* pcnt = hist + kPlanWarps * E;            // [n_peers][E]
-  int* offs = pcnt + f.n_peers * E;             // [E + 1]
+__global__ void __launch_bounds__(kScanWarps * 32)
+k_plan_scan(FanIn f, DevWS ws, int E, int k, int inter, int shared_inter, int hidden,
+            int has_shared, int bn, const int32_t* __restrict__ hist, int32_t* __restrict__ base,
+            int nblocks, GemmPlan* plan1, GemmPlan* plan2) {
+  __shared__ int cnt[256];
+  __shared__ int offs[257];
   __shared__ int skip;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) skip = read_status(ws.status);
-  for (int i = tid; i < kPlanWarps * E + f.n_peers * E; i += blockDim.x) pl_smem[i] = 0;
   __syncthreads();
   if (skip) return;
-  const int N = f.total * k;
-  const int chunk = (N + kPlanWarps - 1) / kPlanWarps;
-  const int c0 = min(N, warp * chunk), c1 = min(N, c0 + chunk);
-  for (int fi = c0 + lane; fi < c1; fi += 32) {
-    int e = ws.ids[fi];
-    if (e < 0 || e >= E) {  // cannot come from the router; keep every index in range
-      set_error(ws.status, AFD_ERR_SHAPE);
-      e = 0;
-      ws.ids[fi] = 0;
+  for (int e = warp; e < E; e += kScanWarps) {
+    int running = 0;
+    for (int b0 = 0; b0 < nblocks; b0 += 32) {
+      const int b = b0 + lane;
+      const int v = b < nblocks ? hist[(int64_t)e * nblocks + b] : 0;
+      int incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      if (b < nblocks) base[(int64_t)e * nblocks + b] = running + incl - v;
+      running += __shfl_sync(0xffffffffu, incl, 31);
     }
-    atomicAdd(&hist[warp * E + e], 1);
-    atomicAdd(&pcnt[entry_of(f, fi / k) * E + e], 1);
+    if (lane == 0) cnt[e] = running;
   }
+  for (int i = tid; i < f.n_peers * E; i += blockDim.x) ws.peer_counts[i] = 0;
   __syncthreads();
   if (tid == 0) {
     int run = 0;
     for (int e = 0; e < E; e++) {
       offs[e] = run;
-      int c = 0;
-      for (int w = 0; w < kPlanWarps; w++) c += hist[w * E + e];
-      run += c;
+      run += cnt[e];
     }
     offs[E] = run;
   }
   __syncthreads();
-  for (int e = tid; e < E; e += blockDim.x) {
-    int base = offs[e];
-    for (int w = 0; w < kPlanWarps; w++) {
-      const int c = hist[w * E + e];
-      hist[w * E + e] = base;  // becomes warp w's cursor for expert e
-      base += c;
-    }
-    ws.counts[e] = offs[e + 1] - offs[e];
+  for (int e = tid; e <= E; e += blockDim.x) {
     ws.offsets[e] = offs[e];
-  }
-  if (tid == 0) ws.offsets[E] = offs[E];
-  for (int i = tid; i < f.n_peers * E; i += blockDim.x) ws.peer_counts[i] = pcnt[i];
-  __syncthreads();
-  const unsigned lt_mask = (1u << lane) - 1u;
-  for (int g0 = c0; g0 < c1; g0 += 32) {
-    const int fi = g0 + lane;
-    const bool ok = fi < c1;
-    const int e = ok ? ws.ids[fi] : -1 - lane;
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    const int rank = __popc(peers & lt_mask);
-    int pos = 0;
-    if (ok) pos = hist[warp * E + e] + rank;
-    __syncwarp();
-    if (ok && rank == 0) hist[warp * E + e] += __popc(peers);
-    __syncwarp();
-    if (ok) {
-      ws.perm[pos] = fi;
-      ws.inv[fi] = pos;
-    }
+    if (e < E) ws.counts[e] = cnt[e];
   }
   // tile tables
   if (tid == 0) {
+    const int N = f.total * k;
     int tiles1 = 0, tiles2 = 0, ng = 0;
     const int mt1 = (inter + 63) / 64, mt2 = (hidden + 127) / 128;
     for (int e = 0; e < E; e++, ng++) {
-      const int rows = offs[e + 1] - offs[e];
+      const int rows = cnt[e];
       const int nt = (rows + bn - 1) / bn;
       GemmGroup a{rows, offs[e], offs[e], e, 0, mt1, nt, tiles1};
       GemmGroup b{rows, offs[e], offs[e], e, 0, mt2, nt, tiles2};
@@ -420,6 +517,52 @@ k_plan(FanIn f, DevWS ws, int E, int k, int inter, int shared_inter, int hidden,
     plan2->total_tiles = tiles2;
     plan1->bn = bn;
     plan2->bn = bn;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// a3 plan, part 2: the stable permutation.  One warp per router CTA's range
+// of partials f (16 tokens x k, contiguous in f): rank among earlier
+// partials of the same expert in the range (match_any per 32-element round
+// plus running per-expert counts), position = offsets[e] + base[e][b] +
+// rank.  Equal to argsort(stable=True) of the flattened ids.  Also the
+// per-peer expert counts of the return headers.
+// ---------------------------------------------------------------------------
+constexpr int kRankWarps = 8;
+
+__global__ void __launch_bounds__(kRankWarps * 32)
+k_rank(FanIn f, DevWS ws, int E, int k, const int32_t* __restrict__ base, int nblocks) {
+  __shared__ int run_s[kRankWarps][256];
+  if (read_status(ws.status)) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.x * kRankWarps + warp;
+  if (b >= nblocks) return;
+  int* run = run_s[warp];
+  for (int e = lane; e < E; e += 32) run[e] = 0;
+  __syncwarp();
+  const int N = f.total * k;
+  const int f0 = b * kRtTok * k, f1 = min(N, f0 + kRtTok * k);
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int g0 = f0; g0 < f1; g0 += 32) {
+    const int fi = g0 + lane;
+    const bool ok = fi < f1;
+    int e = ok ? ws.ids[fi] : -1 - lane;
+    if (ok && (e < 0 || e >= E)) {  // cannot come from the router; keep every index in range
+      set_error(ws.status, AFD_ERR_SHAPE);
+      e = 0;
+    }
+    const unsigned same = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(same & lt_mask);
+    int pos = 0;
+    if (ok) pos = ws.offsets[e] + base[(int64_t)e * nblocks + b] + run[e] + rank;
+    __syncwarp();
+    if (ok && rank == 0) run[e] += __popc(same);
+    __syncwarp();
+    if (ok) {
+      ws.perm[pos] = fi;
+      ws.inv[fi] = pos;
+      atomicAdd(&ws.peer_counts[entry_of(f, fi / k) * E + e], 1);
+    }
   }
 }
 
@@ -660,6 +803,19 @@ __global__ void k_transpose_wg(const float* Wg, float* WgT, int hidden, int E) {
   }
 }
 
+}  // namespace
+
+int router_blocks(int total_tokens) { return (total_tokens + kRtTok - 1) / kRtTok; }
+
+// smallest router footprint for a configuration (bf16 token tile), checked
+// at context creation against the per-CTA shared memory limit
+size_t router_min_smem_bytes(int hidden, int E, int act_f32) {
+  return (size_t)hidden * kRtTok * (act_f32 ? 4 : 2) + (size_t)2 * 64 * 128 * 4 +
+         (size_t)kRtTok * E * 4 + (size_t)E * 4;
+}
+
+namespace {
+
 inline int grid_for(int64_t work, int per_block, int cap) {
   int64_t b = (work + per_block - 1) / per_block;
   if (b < 1) b = 1;
@@ -701,37 +857,56 @@ cudaError_t launch_header_check(const LaunchCtx& lc, const WinGeom& g, const uin
   return cudaGetLastError();
 }
 
-cudaError_t launch_router(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
-                          const FanIn& f, const DevWS& ws, int hidden, int act_f32,
-                          const float* WgT, const float* bias, int E, int k, int renorm,
-                          float scale) {
-  if (f.total == 0) return cudaSuccess;
-  const size_t smem = (size_t)kRtTok * hidden * (act_f32 ? 4 : 2) + (size_t)kRtTok * E * 4;
-  const int grid = (f.total + kRtTok - 1) / kRtTok;
-  cudaError_t err;
-  if (act_f32) {
-    err = cudaFuncSetAttribute(k_router<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    k_router<true><<<grid, kRtWarps * 32, smem, lc.stream>>>(win, g, f, ws, hidden, WgT, bias, E, k,
-                                                             renorm, scale);
-  } else {
-    err = cudaFuncSetAttribute(k_router<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    k_router<false><<<grid, kRtWarps * 32, smem, lc.stream>>>(win, g, f, ws, hidden, WgT, bias, E,
-                                                              k, renorm, scale);
-  }
+size_t router_smem_bytes(int hidden, int E, int act_f32, bool xs_f32) {
+  return (size_t)hidden * kRtTok * (xs_f32 ? 4 : 2) + (size_t)2 * kRtEgroup * kRtHc * 4 +
+         (size_t)kRtTok * E * 4 + (size_t)E * 4;
+}
+
+template <bool ACT_F32, typename XS>
+static cudaError_t launch_router_t(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
+                                   const FanIn& f, const DevWS& ws, int hidden, const float* WgT,
+                                   const float* bias, int E, int k, int renorm, float scale,
+                                   int32_t* hist, size_t smem) {
+  const int grid = router_blocks(f.total);
+  cudaError_t err = cudaFuncSetAttribute(k_router<ACT_F32, XS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  k_router<ACT_F32, XS><<<grid, kRtWarps * 32, smem, lc.stream>>>(win, g, f, ws, hidden, WgT, bias,
+                                                                  E, k, renorm, scale, hist, grid);
   ++*lc.launches;
   return cudaGetLastError();
 }
 
+// the token tile is held as fp32 when it fits next to the weight ring,
+// else as bf16 bits widened on use
+cudaError_t launch_router(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
+                          const FanIn& f, const DevWS& ws, int hidden, int act_f32,
+                          const float* WgT, const float* bias, int E, int k, int renorm,
+                          float scale, int32_t* hist) {
+  if (f.total == 0) return cudaSuccess;
+  const size_t fp32_tile = router_smem_bytes(hidden, E, act_f32, true);
+  if (act_f32)
+    return launch_router_t<true, float>(lc, g, win, f, ws, hidden, WgT, bias, E, k, renorm, scale,
+                                        hist, fp32_tile);
+  if (fp32_tile <= kRouterSmemLimit)
+    return launch_router_t<false, float>(lc, g, win, f, ws, hidden, WgT, bias, E, k, renorm, scale,
+                                         hist, fp32_tile);
+  return launch_router_t<false, uint16_t>(lc, g, win, f, ws, hidden, WgT, bias, E, k, renorm, scale,
+                                          hist, router_smem_bytes(hidden, E, act_f32, false));
+}
+
 cudaError_t launch_plan(const LaunchCtx& lc, const FanIn& f, const DevWS& ws, int E, int k,
                         int inter, int shared_inter, int hidden, int has_shared, int bn,
-                        GemmPlan* plan1, GemmPlan* plan2) {
-  const size_t smem = (size_t)(kPlanWarps * E + f.n_peers * E + E + 1) * 4;
-  cudaError_t err = cudaFuncSetAttribute(k_plan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (err != cudaSuccess) return err;
-  k_plan<<<1, kPlanWarps * 32, smem, lc.stream>>>(f, ws, E, k, inter, shared_inter, hidden,
-                                                  has_shared, bn, plan1, plan2);
+                        GemmPlan* plan1, GemmPlan* plan2, const int32_t* hist, int32_t* base) {
+  const int nblocks = router_blocks(f.total);
+  k_plan_scan<<<1, kScanWarps * 32, 0, lc.stream>>>(f, ws, E, k, inter, shared_inter, hidden,
+                                                     has_shared, bn, hist, base, nblocks, plan1,
+                                                     plan2);
+  ++*lc.launches;
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess || nblocks == 0) return err;
+  k_rank<<<(nblocks + kRankWarps - 1) / kRankWarps, kRankWarps * 32, 0, lc.stream>>>(f, ws, E, k,
+                                                                                    base, nblocks);
   ++*lc.launches;
   return cudaGetLastError();
 }

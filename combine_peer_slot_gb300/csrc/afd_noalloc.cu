@@ -95,7 +95,7 @@ extern "C" int afd_route_noalloc(const void* x, int n_tokens, int hidden, int ac
   ws.w = weights;
   if (launch_router(lc, g, static_cast<const uint8_t*>(x), f, ws, hidden,
                     act_dtype == AFD_DTYPE_F32, WgT, bias, num_experts, topk, renorm,
-                    routed_scaling) != cudaSuccess)
+                    routed_scaling, /*hist=*/nullptr) != cudaSuccess)
     return AFD_ERR_CUDA;
   return AFD_OK;
 }

@@ -55,7 +55,7 @@ def test_layout_matches_oracle(golden, lib):
     for _ in range(300):
         P, D = int(rng.integers(1, 65)), int(rng.integers(1, 9))
         cap, k = int(rng.integers(1, 20000)), int(rng.integers(1, 17))
-        H, E = int(rng.integers(1, 1025)) * 8, int(rng.integers(k, 257))
+        H, E = int(rng.integers(1, 293)) * 8, int(rng.integers(k, 257))  # router tile fits
         act = str(rng.choice(["bf16", "f32"]))
         Is = int(rng.choice([0, 64]))
         cfg = A.make_config(P, cap, H, E, k, 64, shared_inter=Is, act=act, ring_depth=D,

@@ -15,7 +15,7 @@ AFD_OK = 0
  AFD_ERR_STAGE, AFD_ERR_TIMEOUT, AFD_ERR_SHUTDOWN, AFD_ERR_SPLIT_UNEVEN, AFD_ERR_NOT_DEVICE,
  AFD_ERR_CUDA, AFD_ERR_UNSUPPORTED) = range(1, 14)
 AFD_DTYPE_F32, AFD_DTYPE_BF16 = 0, 1
-AFD_GEMM_TENSOR, AFD_GEMM_SIMT = 0, 1
+AFD_GEMM_TENSOR, AFD_GEMM_SIMT, AFD_GEMM_TENSOR_1CTA = 0, 1, 2
 AFD_DIR_DISPATCH, AFD_DIR_RETURN = 0, 1
 (AFD_WS_IDS, AFD_WS_WEIGHTS, AFD_WS_COUNTS, AFD_WS_OFFSETS, AFD_WS_PERM, AFD_WS_INV, AFD_WS_XP,
  AFD_WS_H, AFD_WS_Y, AFD_WS_HS, AFD_WS_S, AFD_WS_STATUS) = range(12)

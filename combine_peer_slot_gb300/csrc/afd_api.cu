@@ -130,12 +130,14 @@ int validate_config(const afd_config* c) {
       c->max_layers < 1 || c->routed_cap_multiplier < 1.0f || c->wait_timeout_ns < 0)
     return AFD_ERR_ARG;
   if (c->act_dtype != AFD_DTYPE_F32 && c->act_dtype != AFD_DTYPE_BF16) return AFD_ERR_ARG;
-  if (c->gemm != AFD_GEMM_TENSOR && c->gemm != AFD_GEMM_SIMT) return AFD_ERR_ARG;
+  if (c->gemm != AFD_GEMM_TENSOR && c->gemm != AFD_GEMM_SIMT && c->gemm != AFD_GEMM_TENSOR_1CTA)
+    return AFD_ERR_ARG;
+  const bool tensor = c->gemm != AFD_GEMM_SIMT;
   // kernel coverage: 16-byte rows, <= 256 experts, k <= 16
   if (c->hidden % 8 || c->num_experts > 256 || c->topk > 16) return AFD_ERR_UNSUPPORTED;
-  if (c->act_dtype == AFD_DTYPE_F32 && c->gemm == AFD_GEMM_TENSOR) return AFD_ERR_UNSUPPORTED;
+  if (c->act_dtype == AFD_DTYPE_F32 && tensor) return AFD_ERR_UNSUPPORTED;
   // tensor-core engine: 16-row gate/up blocks, 32-feature epilogue quadrants
-  if (c->gemm == AFD_GEMM_TENSOR && (c->inter % 16 || c->shared_inter % 16 || c->hidden % 32))
+  if (tensor && (c->inter % 16 || c->shared_inter % 16 || c->hidden % 32))
     return AFD_ERR_UNSUPPORTED;
   // the router keeps 16 token rows and a weight ring in shared memory
   if (router_min_smem_bytes(c->hidden, c->num_experts, c->act_dtype == AFD_DTYPE_F32) > 232448)
@@ -326,7 +328,7 @@ int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out) {
   c->plan2 = reinterpret_cast<GemmPlan*>(b + offs[17]);
   const int ws_map[12] = {4, 5, 6, 7, 8, 9, 11, 12, 13, 14, 15, 0};
   for (int i = 0; i < 12; i++) c->ws_cap[i] = parts[ws_map[i]].bytes;
-  if (cfg->gemm == AFD_GEMM_TENSOR) {
+  if (cfg->gemm != AFD_GEMM_SIMT) {
     rc = get_encoder();
     if (!rc) rc = encode_rows(&c->tmXp, c->ws.xp, Tm * k + Tm, (int)H);
     if (!rc) rc = encode_rows(&c->tmH, c->ws.h, Tm * k, (int)I);
@@ -369,7 +371,7 @@ int afd_set_layer(afd_ctx* ctx, int layer, const float* Wg, const float* bias, c
   L.Wd = Wd;
   L.W13s = has_shared ? W13_s : nullptr;
   L.Wds = has_shared ? Wd_s : nullptr;
-  if (c.gemm == AFD_GEMM_TENSOR) {
+  if (c.gemm != AFD_GEMM_SIMT) {
     rc = encode_swiglu_weight(&L.tmA1[0], W13, c.num_experts, c.inter, c.hidden);
     if (!rc) rc = encode_plain_weight(&L.tmA2[0], Wd, c.num_experts, c.hidden, c.inter);
     if (!rc && has_shared) {
@@ -477,7 +479,8 @@ int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, con
   if (rc) return rc;
   ctx->mark(4);
   if (T > 0) {
-    if (c.gemm == AFD_GEMM_TENSOR) {
+    if (c.gemm != AFD_GEMM_SIMT) {
+      auto launch = c.gemm == AFD_GEMM_TENSOR ? launch_gemm_tc2 : launch_gemm_tc;
       GemmArgs a1;
       memset(&a1, 0, sizeof a1);
       a1.tmA[0] = L.tmA1[0];
@@ -495,7 +498,7 @@ int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, con
       a1.status = ws.status;
       a1.swiglu = 1;
       a1.timeout_ns = ctx->timeout();
-      rc = cuda_fail(launch_gemm_tc(lc, a1), "gemm1");
+      rc = cuda_fail(launch(lc, a1), "gemm1");
       if (rc) return rc;
       ctx->mark(5);
       GemmArgs a2;
@@ -516,7 +519,7 @@ int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, con
       a2.status = ws.status;
       a2.swiglu = 0;
       a2.timeout_ns = ctx->timeout();
-      rc = cuda_fail(launch_gemm_tc(lc, a2), "gemm2");
+      rc = cuda_fail(launch(lc, a2), "gemm2");
       if (rc) return rc;
     } else {
       SimtArgs s1;

@@ -1,0 +1,421 @@
+// afd_gemm_tc2.cu -- the grouped expert GEMM on a pair of SMs:
+// tcgen05.mma.cta_group::2 (kind::f16, bf16 in, fp32 accumulate in TMEM).
+//
+// A cluster of two CTAs computes one unit: 256 weight rows x up to 256
+// tokens.  CTA r of the pair holds weight rows [128 r, 128 r + 128) of the
+// unit (its own 128-row m-tile) and token rows [N/2 r, N/2 (r+1)) of the
+// token tile in shared memory; the leader (r = 0) issues the MMAs, which read
+// A and B from both CTAs, and each CTA's TMEM receives its 128 weight rows x
+// all N tokens.  Per SM and 64-wide k-block the ring takes 16 KB of weights
+// and 16 KB of tokens (one CTA alone would take 16 + 32 KB for the same
+// MMA work), so six stages fit and each SM fills and reads a third less
+// shared memory.  Projections and epilogues are those of afd_gemm_tc.cu
+// (Async GPU Connector, "Attention gate and FFN expert compute": fused_experts
+// gate/up GEMM, SiLU-and-multiply, down GEMM).
+//
+// Signalling (all waits bounded):
+//   full[s]   leader only: one arrive + the bytes of both CTAs' copies (the
+//             peer's TMA signals the leader's barrier through its cluster
+//             address); the leader's MMA waits on it
+//   empty[s]  both CTAs: the leader's MMA commit, multicast to the pair
+//   tfull[a]  both CTAs: the leader's commit after a unit's last k-block
+//   tempty[a] leader only: every epilogue warp of both CTAs arrives
+// Cluster barriers after initialisation and before TMEM release keep every
+// remote arrive inside the lifetime of its target.
+#include "afd_internal.cuh"
+
+namespace {
+
+constexpr int BM = 128;            // weight rows per CTA
+constexpr int BK = 64;
+constexpr int BN_HALF = 128;       // token rows per CTA (256 per unit)
+constexpr int STAGES = 6;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BOX_ROWS = 32;
+constexpr int B_BOX_BYTES = B_BOX_ROWS * BK * 2;
+constexpr int B_BYTES = BN_HALF * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int EPI_WARPS = 8;
+constexpr int NUM_THREADS = 64 + EPI_WARPS * 32;
+constexpr int TMEM_COLS = 512;     // two accumulators of 256 columns
+constexpr int EPI_PITCH_SWIGLU = 48;
+constexpr int EPI_PITCH_BF16 = 80;
+constexpr int EPI_BUF_BYTES = 32 * EPI_PITCH_BF16;
+constexpr uint64_t kGemmTimeoutNs = 5000000000ull;
+
+struct SmemTail {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int skip;
+};
+
+constexpr size_t kEpiOffset = ((size_t)STAGES * STAGE_BYTES + sizeof(SmemTail) + 127) / 128 * 128;
+constexpr size_t kSmemBytes = 1024 + kEpiOffset + (size_t)EPI_WARPS * EPI_BUF_BYTES;
+static_assert(kEpiOffset % 128 == 0 && EPI_BUF_BYTES % 128 == 0, "epilogue buffers must stay aligned");
+static_assert(kSmemBytes <= 232448, "over the per-CTA shared memory limit");
+static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t num_clusters_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// address of this CTA's shared variable in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void tma2_load_2d(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
+                                             uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(tm), "r"(c0), "r"(c1), "r"(bar_cluster)
+      : "memory");
+}
+__device__ __forceinline__ void tma2_load_3d(uint32_t dst, const CUtensorMap* tm, int c0, int c1, int c2,
+                                             uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(dst), "l"(tm), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster)
+      : "memory");
+}
+__device__ __forceinline__ void tma2_load_5d(uint32_t dst, const CUtensorMap* tm, int c0, int c1, int c2,
+                                             int c3, int c4, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+      ::"r"(dst), "l"(tm), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar_cluster)
+      : "memory");
+}
+__device__ __forceinline__ void tc2_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p; }"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// arrive on the barrier at this offset in every CTA of the pair
+__device__ __forceinline__ void tc2_commit_pair(uint32_t bar) {
+  const uint16_t mask = 0x3;
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+      ::"r"(bar), "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ void tc2_commit_local(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// kind::f16, D fp32, A and B bf16, K-major; M = 256 across the pair
+__device__ __forceinline__ uint32_t idesc_pair(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+}
+
+struct Unit {
+  int group, kind, mpair, nt, rows, n_mma;
+};
+
+__device__ __forceinline__ Unit decode_unit(const GemmPlan& p, int unit) {
+  int lo = 0, hi = p.ngroups - 1;
+  while (lo < hi) {  // last group with unit0 <= unit (empty groups share unit0 with the next)
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.g[mid].unit0 <= unit) lo = mid; else hi = mid - 1;
+  }
+  const GemmGroup& G = p.g[lo];
+  const int m_pairs = (G.m_tiles + 1) / 2;
+  const int u = unit - G.unit0;
+  Unit t;
+  t.group = lo;
+  t.kind = G.kind;
+  t.mpair = u % m_pairs;
+  t.nt = u / m_pairs;
+  t.rows = min(p.bn, G.rows - t.nt * p.bn);
+  t.n_mma = (t.rows + 31) & ~31;    // even halves of 16-row multiples
+  return t;
+}
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         uint64_t deadline, int32_t* status) {
+  uint32_t spins = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++spins & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() > deadline) {
+        *abort_flag = 1;
+        set_error(status, AFD_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+k_gemm_tc2(const __grid_constant__ GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  SmemTail* tail = reinterpret_cast<SmemTail*>(smem + (size_t)STAGES * STAGE_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const int cid = (int)cluster_id_x();
+  const int ncl = (int)num_clusters_x();
+  const GemmPlan& plan = *args.plan;
+
+  if (threadIdx.x == 0) {
+    tail->skip = read_status(args.status);
+    for (int s = 0; s < STAGES; s++) {
+      mbar_init(smem_u32(&tail->full[s]), 1);
+      mbar_init(smem_u32(&tail->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; b++) {
+      mbar_init(smem_u32(&tail->tfull[b]), 1);
+      mbar_init(smem_u32(&tail->tempty[b]), 2 * EPI_WARPS);
+    }
+    mbar_init(smem_u32(&tail->drain), 1);
+    tail->abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const int total = plan.total_units;
+  // both CTAs of a pair take the same decision: same status, same cluster id
+  if (tail->skip || total <= cid) return;
+  cluster_sync();  // the peer's barriers are initialised before any remote signal
+
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&tail->tmem_base)),
+                 "r"(TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tail->tmem_base;
+  const uint64_t deadline = globaltimer_ns() + kGemmTimeoutNs;
+  volatile int* abort_flag = &tail->abort_flag;
+  const uint32_t smem_base = smem_u32(smem);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------ TMA producer (both CTAs)
+      int s = 0;
+      uint32_t ph = 0;
+      for (int unit = cid; unit < total; unit += ncl) {
+        const Unit t = decode_unit(plan, unit);
+        const GemmGroup& G = plan.g[t.group];
+        const int nkb = (args.K[t.kind] + BK - 1) / BK;
+        const int half = t.n_mma / 2;
+        const int nb = (half + B_BOX_ROWS - 1) / B_BOX_ROWS;
+        const int brow = G.b_row0 + t.nt * plan.bn + (int)rank * half;
+        const int mt = 2 * t.mpair + (int)rank;
+        const CUtensorMap* ta = &args.tmA[t.kind];
+        const CUtensorMap* tb = &args.tmB[t.kind];
+        bool ok = true;
+        for (int kb = 0; kb < nkb; kb++) {
+          if (!wait_bar(smem_u32(&tail->empty[s]), ph ^ 1, abort_flag, deadline, args.status)) { ok = false; break; }
+          const uint32_t full_leader = map_to_rank(smem_u32(&tail->full[s]), 0);
+          if (rank == 0) mbar_expect_tx(smem_u32(&tail->full[s]), 2 * (A_BYTES + nb * B_BOX_BYTES));
+          const uint32_t sa = smem_base + s * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          if (args.swiglu)
+            tma2_load_5d(sa, ta, kb * BK, 0, 0, mt * 4, G.a_idx, full_leader);
+          else
+            tma2_load_3d(sa, ta, kb * BK, mt * BM, G.a_idx, full_leader);
+          for (int q = 0; q < nb; q++)
+            tma2_load_2d(sb + q * B_BOX_BYTES, tb, kb * BK, brow + q * B_BOX_ROWS, full_leader);
+          if (++s == STAGES) { s = 0; ph ^= 1; }
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ------------------------------ MMA issuer (leader CTA)
+      int s = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t acc_ph = 0;
+      bool ok = true;
+      for (int unit = cid; unit < total && ok; unit += ncl) {
+        const Unit t = decode_unit(plan, unit);
+        const int nkb = (args.K[t.kind] + BK - 1) / BK;
+        const uint32_t idesc = idesc_pair(t.n_mma);
+        if (!wait_bar(smem_u32(&tail->tempty[acc]), acc_ph ^ 1, abort_flag, deadline, args.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
+        for (int kb = 0; kb < nkb; kb++) {
+          if (!wait_bar(smem_u32(&tail->full[s]), ph, abort_flag, deadline, args.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_base + s * STAGE_BYTES;
+          const uint64_t adesc = sdesc_sw128(sa);
+          const uint64_t bdesc = sdesc_sw128(sa + A_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; kk++)
+            tc2_mma_f16(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
+                        (kb | kk) != 0);
+          tc2_commit_pair(smem_u32(&tail->empty[s]));
+          if (++s == STAGES) { s = 0; ph ^= 1; }
+        }
+        if (!ok) break;
+        tc2_commit_pair(smem_u32(&tail->tfull[acc]));
+        if (++acc == 2) { acc = 0; acc_ph ^= 1; }
+      }
+      // every issued MMA completes before TMEM is released
+      tc2_commit_local(smem_u32(&tail->drain));
+      const uint64_t dl = globaltimer_ns() + 100000000ull;
+      while (!mbar_try_wait(smem_u32(&tail->drain), 0) && globaltimer_ns() < dl) {}
+    }
+  } else {
+    // ------------------------------ epilogue (warps 2..9, both CTAs)
+    const int q = warp & 3;
+    const int half_cols = (warp - 2) >> 2;
+    uint8_t* ebuf = smem + kEpiOffset + (size_t)(warp - 2) * EPI_BUF_BYTES;
+    const bool lo = lane < 16;
+    const uint32_t tempty_leader[2] = {map_to_rank(smem_u32(&tail->tempty[0]), 0),
+                                       map_to_rank(smem_u32(&tail->tempty[1]), 0)};
+    int acc = 0;
+    uint32_t acc_ph = 0;
+    for (int unit = cid; unit < total; unit += ncl) {
+      const Unit t = decode_unit(plan, unit);
+      const GemmGroup& G = plan.g[t.group];
+      bool ok = wait_bar(smem_u32(&tail->tfull[acc]), acc_ph, abort_flag, deadline, args.status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * 256);
+      const int kind = t.kind;
+      const int64_t ldo = args.ldo[kind];
+      const int64_t row0 = (int64_t)G.out_row0 + (int64_t)t.nt * plan.bn;
+      const int mt = 2 * t.mpair + (int)rank;
+      if (args.swiglu) {
+        const int col0 = mt * 64 + q * 16;
+        const bool cols_ok = col0 + 16 <= args.M[kind] / 2;
+        for (int c0 = half_cols * 32; c0 < t.rows; c0 += 64) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(taddr + (uint32_t)c0, v);
+          tmem_ld_wait();
+          uint16_t* sb = reinterpret_cast<uint16_t*>(ebuf);
+#pragma unroll
+          for (int j = 0; j < 16; j++) {
+            const float a = __uint_as_float(v[j]), b = __uint_as_float(v[16 + j]);
+            const float recv = __shfl_xor_sync(0xffffffffu, lo ? b : a, 16);
+            const float g = lo ? a : recv;
+            const float u = lo ? recv : b;
+            const __nv_bfloat16 hv = __float2bfloat16_rn(silu_f(g) * u);
+            const int tok = lo ? j : 16 + j;
+            sb[(tok * EPI_PITCH_SWIGLU + (lo ? 0 : 32)) / 2 + (lane & 15)] =
+                *reinterpret_cast<const uint16_t*>(&hv);
+          }
+          __syncwarp();
+          const int r = c0 + lane;
+          if (r < t.rows && cols_ok) {
+            const uint4* src =
+                reinterpret_cast<const uint4*>(ebuf + lane * EPI_PITCH_SWIGLU + (lo ? 0 : 32));
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(args.out[kind]) +
+                                                  (row0 + r) * ldo + col0);
+            dst[0] = src[0];
+            dst[1] = src[1];
+          }
+          __syncwarp();
+        }
+      } else {
+        const int col0 = mt * BM + q * 32;
+        const bool cols_ok = col0 + 32 <= args.M[kind];
+        const int out_f32 = args.out_f32[kind];
+        for (int c0 = half_cols * 32; c0 < t.rows; c0 += 64) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(taddr + (uint32_t)c0, v);
+          tmem_ld_wait();
+          const int r = c0 + lane;
+          if (out_f32) {
+            if (cols_ok) {
+              float* dst = reinterpret_cast<float*>(args.out[kind]) + (row0 + c0) * ldo + col0 + lane;
+#pragma unroll
+              for (int c = 0; c < 32; c++)
+                if (c0 + c < t.rows) dst[(int64_t)c * ldo] = __uint_as_float(v[c]);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; c++) {
+              const __nv_bfloat16 yv = __float2bfloat16_rn(__uint_as_float(v[c]));
+              *reinterpret_cast<uint16_t*>(ebuf + c * EPI_PITCH_BF16 + lane * 2) =
+                  *reinterpret_cast<const uint16_t*>(&yv);
+            }
+            __syncwarp();
+            if (r < t.rows && cols_ok) {
+              const uint4* src = reinterpret_cast<const uint4*>(ebuf + lane * EPI_PITCH_BF16);
+              uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(args.out[kind]) +
+                                                    (row0 + r) * ldo + col0);
+#pragma unroll
+              for (int x = 0; x < 4; x++) dst[x] = src[x];
+            }
+          }
+          __syncwarp();
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty_leader[acc]);
+      if (++acc == 2) { acc = 0; acc_ph ^= 1; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no remote arrive or MMA of the pair is outstanding past this point
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc2(const LaunchCtx& lc, const GemmArgs& a) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc2, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const int grid = (lc.num_sms / 2) * 2;  // whole pairs; persistent over the unit table
+  k_gemm_tc2<<<grid, NUM_THREADS, kSmemBytes, lc.stream>>>(a);
+  ++*lc.launches;
+  return cudaGetLastError();
+}

@@ -64,14 +64,15 @@ struct GemmGroup {
   int kind;      // 0 routed, 1 shared
   int m_tiles;   // 128-row tiles of the weight (M) dimension
   int n_tiles;   // token tiles
-  int tile0;     // first linear tile index of the group
+  int tile0;     // first linear tile index of the group (one CTA per tile)
+  int unit0;     // first pair-tile index (two CTAs, 256 weight rows per unit)
 };
 
 struct GemmPlan {
   int ngroups;
   int total_tiles;
   int bn;        // token tile
-  int pad;
+  int total_units;
   GemmGroup g[AFD_MAX_GROUPS];
 };
 
@@ -253,6 +254,7 @@ cudaError_t launch_gather(const LaunchCtx& lc, const WinGeom& g, const uint8_t* 
                           const FanIn& f, const DevWS& ws, int k, int row_bytes,
                           int has_shared);
 cudaError_t launch_gemm_tc(const LaunchCtx& lc, const GemmArgs& a);
+cudaError_t launch_gemm_tc2(const LaunchCtx& lc, const GemmArgs& a);
 cudaError_t launch_gemm_simt(const LaunchCtx& lc, const SimtArgs& a, int max_rows_hint);
 cudaError_t launch_combine(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret,
                            const FanIn& f, const DevWS& ws, int hidden, int k, int act_f32,

@@ -487,34 +487,40 @@ k_plan_scan(FanIn f, DevWS ws, int E, int k, int inter, int shared_inter, int hi
   // tile tables
   if (tid == 0) {
     const int N = f.total * k;
-    int tiles1 = 0, tiles2 = 0, ng = 0;
+    int tiles1 = 0, tiles2 = 0, units1 = 0, units2 = 0, ng = 0;
     const int mt1 = (inter + 63) / 64, mt2 = (hidden + 127) / 128;
     for (int e = 0; e < E; e++, ng++) {
       const int rows = cnt[e];
       const int nt = (rows + bn - 1) / bn;
-      GemmGroup a{rows, offs[e], offs[e], e, 0, mt1, nt, tiles1};
-      GemmGroup b{rows, offs[e], offs[e], e, 0, mt2, nt, tiles2};
+      GemmGroup a{rows, offs[e], offs[e], e, 0, mt1, nt, tiles1, units1};
+      GemmGroup b{rows, offs[e], offs[e], e, 0, mt2, nt, tiles2, units2};
       plan1->g[ng] = a;
       plan2->g[ng] = b;
       tiles1 += mt1 * nt;
       tiles2 += mt2 * nt;
+      units1 += (mt1 + 1) / 2 * nt;
+      units2 += (mt2 + 1) / 2 * nt;
     }
     if (has_shared) {
       const int rows = f.total;
       const int nt = (rows + bn - 1) / bn;
       const int mts = (shared_inter + 63) / 64;
-      GemmGroup a{rows, N, 0, 0, 1, mts, nt, tiles1};
-      GemmGroup b{rows, 0, 0, 0, 1, mt2, nt, tiles2};
+      GemmGroup a{rows, N, 0, 0, 1, mts, nt, tiles1, units1};
+      GemmGroup b{rows, 0, 0, 0, 1, mt2, nt, tiles2, units2};
       plan1->g[ng] = a;
       plan2->g[ng] = b;
       tiles1 += mts * nt;
       tiles2 += mt2 * nt;
+      units1 += (mts + 1) / 2 * nt;
+      units2 += (mt2 + 1) / 2 * nt;
       ng++;
     }
     plan1->ngroups = ng;
     plan2->ngroups = ng;
     plan1->total_tiles = tiles1;
     plan2->total_tiles = tiles2;
+    plan1->total_units = units1;
+    plan2->total_units = units2;
     plan1->bn = bn;
     plan2->bn = bn;
   }

@@ -66,10 +66,13 @@ extern "C" {
 #define AFD_DTYPE_BF16 1
 
 /* GEMM engine of the expert projections.  TENSOR (default for bf16) is the
- * tcgen05/TMEM grouped GEMM; SIMT is a plain fp32-FMA CUDA kernel that
- * serves fp32 activations and cross-checks the tensor-core path. */
+ * tcgen05/TMEM grouped GEMM on SM pairs (cta_group::2, 256 weight rows per
+ * unit); TENSOR_1CTA the same GEMM with one SM per 128-row tile; SIMT a
+ * plain fp32-FMA CUDA kernel that serves fp32 activations and cross-checks
+ * the tensor-core engines. */
 #define AFD_GEMM_TENSOR 0
 #define AFD_GEMM_SIMT 1
+#define AFD_GEMM_TENSOR_1CTA 2
 
 #define AFD_MAX_PEERS 64
 

@@ -24,7 +24,8 @@ def test_tiny_fp32():
     print("tiny max|err|/rms", e)
 
 
-@pytest.mark.parametrize("gemm", [A.AFD_GEMM_TENSOR, A.AFD_GEMM_SIMT], ids=["tcgen05", "simt"])
+@pytest.mark.parametrize("gemm", [A.AFD_GEMM_TENSOR, A.AFD_GEMM_TENSOR_1CTA, A.AFD_GEMM_SIMT],
+                         ids=["tcgen05_pair", "tcgen05_1cta", "simt"])
 def test_fanin_bf16(gemm):
     run = R.Runner(W.get("fanin"), gemm=gemm)
     e, _ = G.run_and_compare_full(run)

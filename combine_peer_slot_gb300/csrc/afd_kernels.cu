@@ -148,12 +148,24 @@ __global__ void k_header_check(const uint8_t* win, WinGeom g, FanIn f, DevWS ws,
   __syncthreads();
   // shared_idx must be 0..n-1: with one FFN rank every token is a shared
   // token (Async GPU Connector, "Data flow" step 3).
+  // (8 independent loads in flight per thread)
   for (int i = 0; i < f.n_peers; i++) {
     if (err[i] || shared_n[i] == 0) continue;
     const int32_t* sidx = reinterpret_cast<const int32_t*>(slot_ptr(win, g, f.region[i], f.stage) +
                                                            g.shared_idx);
-    for (int r = tid; r < shared_n[i]; r += blockDim.x)
-      if (sidx[r] != r) bad_sidx[i] = 1;
+    const int n = shared_n[i];
+    int bad = 0;
+    for (int r0 = tid; r0 < n; r0 += 8 * blockDim.x) {
+      int v[8];
+#pragma unroll
+      for (int u = 0; u < 8; u++) {
+        const int r = r0 + u * blockDim.x;
+        v[u] = r < n ? sidx[r] : r;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; u++) bad |= v[u] != r0 + u * (int)blockDim.x;
+    }
+    if (bad) bad_sidx[i] = 1;
   }
   __syncthreads();
   if (tid == 0) {
@@ -668,7 +680,8 @@ template <bool ACT_F32, bool Y_F32>
 __global__ void __launch_bounds__(kThreads)
 k_combine(uint8_t* ret, WinGeom g, FanIn f, DevWS ws, int hidden, int k, int has_shared) {
   if (read_status(ws.status)) return;
-  constexpr int kVec = 4;  // elements per thread step
+  // 8 features per lane step: 16-byte loads of bf16 y (two of fp32 y)
+  constexpr int kVec = 8;
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * (blockDim.x >> 5);
   for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < f.total; t += warps) {
@@ -684,39 +697,55 @@ k_combine(uint8_t* ret, WinGeom g, FanIn f, DevWS ws, int hidden, int k, int has
           ws.ids[(int64_t)t * k + lane];
     }
     for (int c = lane * kVec; c < hidden; c += 32 * kVec) {
-      float acc[kVec] = {0.f, 0.f, 0.f, 0.f};
+      float acc[kVec];
+#pragma unroll
+      for (int q = 0; q < kVec; q++) acc[q] = 0.0f;
       for (int j = 0; j < k; j++) {
         const int pos = __shfl_sync(0xffffffffu, my_pos, j);
         const float wj = __shfl_sync(0xffffffffu, my_w, j);
         float yv[kVec];
         if constexpr (Y_F32) {
-          const float4 v = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(ws.y) +
-                                                            (int64_t)pos * hidden + c);
-          yv[0] = v.x; yv[1] = v.y; yv[2] = v.z; yv[3] = v.w;
+          const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(ws.y) +
+                                                              (int64_t)pos * hidden + c);
+          const float4 a = src[0], b = src[1];
+          yv[0] = a.x; yv[1] = a.y; yv[2] = a.z; yv[3] = a.w;
+          yv[4] = b.x; yv[5] = b.y; yv[6] = b.z; yv[7] = b.w;
         } else {
-          const uint2 v = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(ws.y) +
-                                                          (int64_t)pos * hidden + c);
-          yv[0] = __uint_as_float(v.x << 16); yv[1] = __uint_as_float(v.x & 0xffff0000u);
-          yv[2] = __uint_as_float(v.y << 16); yv[3] = __uint_as_float(v.y & 0xffff0000u);
+          const uint4 v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(ws.y) +
+                                                         (int64_t)pos * hidden + c);
+          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int m = 0; m < 4; m++) {
+            yv[2 * m] = __uint_as_float(w4[m] << 16);
+            yv[2 * m + 1] = __uint_as_float(w4[m] & 0xffff0000u);
+          }
         }
 #pragma unroll
         for (int q = 0; q < kVec; q++) acc[q] = __fmaf_rn(wj, yv[q], acc[q]);
       }
       if (has_shared) {
-        const float4 sv = *reinterpret_cast<const float4*>(ws.s + (int64_t)t * hidden + c);
-        acc[0] = __fadd_rn(acc[0], sv.x); acc[1] = __fadd_rn(acc[1], sv.y);
-        acc[2] = __fadd_rn(acc[2], sv.z); acc[3] = __fadd_rn(acc[3], sv.w);
+        const float4* sp = reinterpret_cast<const float4*>(ws.s + (int64_t)t * hidden + c);
+        const float4 a = sp[0], b = sp[1];
+        acc[0] = __fadd_rn(acc[0], a.x); acc[1] = __fadd_rn(acc[1], a.y);
+        acc[2] = __fadd_rn(acc[2], a.z); acc[3] = __fadd_rn(acc[3], a.w);
+        acc[4] = __fadd_rn(acc[4], b.x); acc[5] = __fadd_rn(acc[5], b.y);
+        acc[6] = __fadd_rn(acc[6], b.z); acc[7] = __fadd_rn(acc[7], b.w);
       }
       if constexpr (ACT_F32) {
-        *reinterpret_cast<float4*>(slot + g.routed_x + ((int64_t)local * hidden + c) * 4) =
-            make_float4(acc[0], acc[1], acc[2], acc[3]);
+        float4* dst = reinterpret_cast<float4*>(slot + g.routed_x + ((int64_t)local * hidden + c) * 4);
+        dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
       } else {
+        uint4 o;
         __nv_bfloat162 p0 = __floats2bfloat162_rn(acc[0], acc[1]);
         __nv_bfloat162 p1 = __floats2bfloat162_rn(acc[2], acc[3]);
-        uint2 o;
+        __nv_bfloat162 p2 = __floats2bfloat162_rn(acc[4], acc[5]);
+        __nv_bfloat162 p3 = __floats2bfloat162_rn(acc[6], acc[7]);
         o.x = *reinterpret_cast<uint32_t*>(&p0);
         o.y = *reinterpret_cast<uint32_t*>(&p1);
-        *reinterpret_cast<uint2*>(slot + g.routed_x + ((int64_t)local * hidden + c) * 2) = o;
+        o.z = *reinterpret_cast<uint32_t*>(&p2);
+        o.w = *reinterpret_cast<uint32_t*>(&p3);
+        *reinterpret_cast<uint4*>(slot + g.routed_x + ((int64_t)local * hidden + c) * 2) = o;
       }
     }
   }
@@ -857,8 +886,8 @@ cudaError_t launch_pack_header(const LaunchCtx& lc, const WinGeom& g, uint8_t* w
 cudaError_t launch_header_check(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                                 const FanIn& f, const DevWS& ws, int num_experts, int token_cap,
                                 int has_shared_expert, int64_t timeout_ns) {
-  k_header_check<<<1, kThreads, 0, lc.stream>>>(win, g, f, ws, num_experts, token_cap,
-                                                has_shared_expert, timeout_ns);
+  k_header_check<<<1, 1024, 0, lc.stream>>>(win, g, f, ws, num_experts, token_cap,
+                                            has_shared_expert, timeout_ns);
   ++*lc.launches;
   return cudaGetLastError();
 }

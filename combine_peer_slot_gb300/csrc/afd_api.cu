@@ -78,11 +78,11 @@ int encode_plain_weight(CUtensorMap* m, const void* W, int E, int M, int K) {
   return encode_map(m, W, 3, dims, str, box);
 }
 
-// [rows][K] token rows, box 64 x 32
-int encode_rows(CUtensorMap* m, const void* X, int64_t rows, int K) {
+// [rows][K] token rows, box 64 x box_rows
+int encode_rows(CUtensorMap* m, const void* X, int64_t rows, int K, int box_rows) {
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)(rows > 0 ? rows : 1)};
   const cuuint64_t str[1] = {(cuuint64_t)K * 2};
-  const cuuint32_t box[2] = {64, 32};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   return encode_map(m, X, 2, dims, str, box);
 }
 
@@ -330,9 +330,12 @@ int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out) {
   for (int i = 0; i < 12; i++) c->ws_cap[i] = parts[ws_map[i]].bytes;
   if (cfg->gemm != AFD_GEMM_SIMT) {
     rc = get_encoder();
-    if (!rc) rc = encode_rows(&c->tmXp, c->ws.xp, Tm * k + Tm, (int)H);
-    if (!rc) rc = encode_rows(&c->tmH, c->ws.h, Tm * k, (int)I);
-    if (!rc) rc = encode_rows(&c->tmHs, c->ws.hs, Tm, (int)(Is > 0 ? Is : 64));
+    // token boxes: 32 rows for one CTA per tile, 128 rows (a CTA's half of a
+    // 256-token unit) for the SM-pair engine
+    const int box = cfg->gemm == AFD_GEMM_TENSOR ? 128 : 32;
+    if (!rc) rc = encode_rows(&c->tmXp, c->ws.xp, Tm * k + Tm, (int)H, box);
+    if (!rc) rc = encode_rows(&c->tmH, c->ws.h, Tm * k, (int)I, box);
+    if (!rc) rc = encode_rows(&c->tmHs, c->ws.hs, Tm, (int)(Is > 0 ? Is : 64), box);
     if (rc) { afd_destroy(c); return rc; }
   }
   *out = c;

@@ -31,9 +31,7 @@ constexpr int BK = 64;
 constexpr int BN_HALF = 128;       // token rows per CTA (256 per unit)
 constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BOX_ROWS = 32;
-constexpr int B_BOX_BYTES = B_BOX_ROWS * BK * 2;
-constexpr int B_BYTES = BN_HALF * BK * 2;
+constexpr int B_BYTES = BN_HALF * BK * 2;  // one [128 tokens][64 k] box
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + EPI_WARPS * 32;
@@ -238,8 +236,9 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
         const Unit t = decode_unit(plan, unit);
         const GemmGroup& G = plan.g[t.group];
         const int nkb = (args.K[t.kind] + BK - 1) / BK;
+        // one 128-row token box per CTA and k-block (rows past the half are
+        // read but not used by the MMA; past the buffer they are zero-filled)
         const int half = t.n_mma / 2;
-        const int nb = (half + B_BOX_ROWS - 1) / B_BOX_ROWS;
         const int brow = G.b_row0 + t.nt * plan.bn + (int)rank * half;
         const int mt = 2 * t.mpair + (int)rank;
         const CUtensorMap* ta = &args.tmA[t.kind];
@@ -248,15 +247,14 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
         for (int kb = 0; kb < nkb; kb++) {
           if (!wait_bar(smem_u32(&tail->empty[s]), ph ^ 1, abort_flag, deadline, args.status)) { ok = false; break; }
           const uint32_t full_leader = map_to_rank(smem_u32(&tail->full[s]), 0);
-          if (rank == 0) mbar_expect_tx(smem_u32(&tail->full[s]), 2 * (A_BYTES + nb * B_BOX_BYTES));
+          if (rank == 0) mbar_expect_tx(smem_u32(&tail->full[s]), 2 * (A_BYTES + B_BYTES));
           const uint32_t sa = smem_base + s * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
           if (args.swiglu)
             tma2_load_5d(sa, ta, kb * BK, 0, 0, mt * 4, G.a_idx, full_leader);
           else
             tma2_load_3d(sa, ta, kb * BK, mt * BM, G.a_idx, full_leader);
-          for (int q = 0; q < nb; q++)
-            tma2_load_2d(sb + q * B_BOX_BYTES, tb, kb * BK, brow + q * B_BOX_ROWS, full_leader);
+          tma2_load_2d(sb, tb, kb * BK, brow, full_leader);
           if (++s == STAGES) { s = 0; ph ^= 1; }
         }
         if (!ok) break;

@@ -80,6 +80,8 @@ struct GemmPlan {
 struct GemmArgs {
   CUtensorMap tmA[2];     // weights: [0] routed experts, [1] shared expert
   CUtensorMap tmB[2];     // token rows: [0] routed source, [1] shared source
+                          // (box 64 x 32 rows for the one-CTA engine, 64 x 128
+                          // rows for the SM-pair engine)
   void* out[2];           // outputs per kind
   int64_t ldo[2];         // output row pitch in elements
   int out_f32[2];         // 1 = fp32 output, 0 = bf16

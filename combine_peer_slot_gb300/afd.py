@@ -21,6 +21,7 @@ AFD_DIR_DISPATCH, AFD_DIR_RETURN = 0, 1
  AFD_WS_H, AFD_WS_Y, AFD_WS_HS, AFD_WS_S, AFD_WS_STATUS) = range(12)
 AFD_HEADER_FIXED_WORDS = 12
 AFD_NOALLOC_MAX_ROUTER_WEIGHTS = 262144
+AFD_NOALLOC_MAX_LOGITS = 1048576
 AFD_MAX_PEERS = 64
 
 
@@ -78,7 +79,7 @@ SIGNATURES = [
     ("afd_strerror", C.c_char_p, [_I]),
     ("afd_profile", _I, [_P, _I]),
     ("afd_route_noalloc", _I, [_P, _I, _I, _I, _P, _P, _I, _I, _I, _F, _P, _P, _P]),
-    ("afd_stage_times", _I, [_P, C.POINTER(C.c_float), _I]),
+    ("afd_stage_times", _I, [_P, C.POINTER(C.c_float), _I, C.POINTER(C.c_int64)]),
 ]
 AFD_NUM_STAGES = 8
 STAGE_NAMES = ("header_check", "router", "plan", "gather", "gemm_swiglu", "gemm_down",
@@ -210,9 +211,12 @@ def afd_profile(ctx, enable):
 
 
 def afd_stage_times(ctx):
+    """(per-stage milliseconds summed over the forwards since the previous
+    call, number of those forwards)"""
     ms = (C.c_float * AFD_NUM_STAGES)()
-    _check(lib().afd_stage_times(ctx, ms, AFD_NUM_STAGES), "afd_stage_times")
-    return [float(v) for v in ms]
+    n = C.c_int64(0)
+    _check(lib().afd_stage_times(ctx, ms, AFD_NUM_STAGES, C.byref(n)), "afd_stage_times")
+    return [float(v) for v in ms], int(n.value)
 
 
 def afd_route_noalloc(x_ptr, n_tokens, hidden, act_dtype, Wg_ptr, bias_ptr, num_experts, topk,

@@ -162,7 +162,8 @@ struct afd_ctx {
   DevWS ws;
   GemmPlan* plan1 = nullptr;
   GemmPlan* plan2 = nullptr;
-  CUtensorMap tmXp, tmH, tmHs;
+  CUtensorMap tmXp, tmH, tmHs;        // token boxes of the tensor engine
+  CUtensorMap tmXp32, tmH32, tmHs32;  // 32-row boxes (small SM-pair units)
   std::vector<LayerW> layers;
   std::vector<uint64_t> last_seq;
   int tmax = 0;
@@ -171,11 +172,43 @@ struct afd_ctx {
   int last_T = 0;
   int64_t forwards = 0;
   int64_t ws_cap[12];
+  // stage timing: one set of events per forward, in a ring, so the host
+  // reads them after many forwards instead of waiting after each one
+  static constexpr int kProfRing = 64;
   bool profiling = false;
-  cudaEvent_t ev[AFD_NUM_STAGES + 1] = {};
+  bool events_made = false;
+  cudaEvent_t ev[kProfRing][AFD_NUM_STAGES + 1] = {};
+  int prof_head = 0;     // set the next forward records into
+  int prof_pending = 0;  // recorded sets not yet folded into prof_acc
+  double prof_acc[AFD_NUM_STAGES] = {};
+  int64_t prof_acc_n = 0;
 
+  // wait for the oldest recorded set and add its stage times to prof_acc
+  int fold_oldest() {
+    const int idx = (prof_head - prof_pending + kProfRing) % kProfRing;
+    if (cudaEventSynchronize(ev[idx][AFD_NUM_STAGES]) != cudaSuccess) return AFD_ERR_CUDA;
+    for (int i = 0; i < AFD_NUM_STAGES; i++) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, ev[idx][i], ev[idx][i + 1]) != cudaSuccess) return AFD_ERR_CUDA;
+      prof_acc[i] += ms;
+    }
+    prof_acc_n++;
+    prof_pending--;
+    return AFD_OK;
+  }
   void mark(int i) {
-    if (profiling) cudaEventRecord(ev[i], stream);
+    if (!profiling) return;
+    if (i == 0 && prof_pending == kProfRing && fold_oldest()) {
+      fprintf(stderr, "afd: stage timing failed; timing switched off\n");
+      cudaGetLastError();
+      profiling = false;
+      return;
+    }
+    cudaEventRecord(ev[prof_head][i], stream);
+    if (i == AFD_NUM_STAGES) {  // a complete set: count it
+      prof_head = (prof_head + 1) % kProfRing;
+      prof_pending++;
+    }
   }
 
   LaunchCtx lc() { return LaunchCtx{stream, num_sms, &launches}; }
@@ -239,8 +272,9 @@ void afd_destroy(afd_ctx* ctx) {
   cudaSetDevice(ctx->device);
   cudaStreamSynchronize(ctx->stream);
   for (auto& l : ctx->layers) cudaFree(l.WgT);
-  for (auto& e : ctx->ev)
-    if (e) cudaEventDestroy(e);
+  for (auto& set : ctx->ev)
+    for (auto& e : set)
+      if (e) cudaEventDestroy(e);
   cudaFree(ctx->win[0]);
   cudaFree(ctx->win[1]);
   cudaFree(ctx->ws_mem);
@@ -294,7 +328,8 @@ int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out) {
       {Tm * (Is > 0 ? Is : 1) * ab},         // hs
       {Tm * H * 4},                          // s
       {(int64_t)sizeof(GemmPlan)}, {(int64_t)sizeof(GemmPlan)},
-      {E * router_blocks((int)Tm) * 4}, {E * router_blocks((int)Tm) * 4}};  // hist, base
+      {E * router_blocks((int)Tm) * 4}, {E * router_blocks((int)Tm) * 4},  // hist, base
+      {Tm * E * 4}};                         // router logits
   const int nparts = sizeof(parts) / sizeof(parts[0]);
   int64_t offs[32], total = 0;
   for (int i = 0; i < nparts; i++) {
@@ -324,6 +359,7 @@ int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out) {
   c->ws.s = reinterpret_cast<float*>(b + offs[15]);
   c->ws.hist = reinterpret_cast<int32_t*>(b + offs[18]);
   c->ws.base = reinterpret_cast<int32_t*>(b + offs[19]);
+  c->ws.logits = reinterpret_cast<float*>(b + offs[20]);
   c->plan1 = reinterpret_cast<GemmPlan*>(b + offs[16]);
   c->plan2 = reinterpret_cast<GemmPlan*>(b + offs[17]);
   const int ws_map[12] = {4, 5, 6, 7, 8, 9, 11, 12, 13, 14, 15, 0};
@@ -336,6 +372,9 @@ int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out) {
     if (!rc) rc = encode_rows(&c->tmXp, c->ws.xp, Tm * k + Tm, (int)H, box);
     if (!rc) rc = encode_rows(&c->tmH, c->ws.h, Tm * k, (int)I, box);
     if (!rc) rc = encode_rows(&c->tmHs, c->ws.hs, Tm, (int)(Is > 0 ? Is : 64), box);
+    if (!rc) rc = encode_rows(&c->tmXp32, c->ws.xp, Tm * k + Tm, (int)H, 32);
+    if (!rc) rc = encode_rows(&c->tmH32, c->ws.h, Tm * k, (int)I, 32);
+    if (!rc) rc = encode_rows(&c->tmHs32, c->ws.hs, Tm, (int)(Is > 0 ? Is : 64), 32);
     if (rc) { afd_destroy(c); return rc; }
   }
   *out = c;
@@ -468,7 +507,7 @@ int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, con
   ctx->mark(1);
   rc = cuda_fail(launch_router(lc, ctx->geom, ctx->win[0], f, ws, c.hidden, ctx->act_f32, L.WgT,
                                L.bias, c.num_experts, c.topk, c.renorm, c.routed_scaling,
-                               ws.hist),
+                               ws.logits, ws.hist),
                  "router");
   if (rc) return rc;
   ctx->mark(2);
@@ -490,6 +529,8 @@ int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, con
       a1.tmA[1] = L.tmA1[1];
       a1.tmB[0] = ctx->tmXp;
       a1.tmB[1] = ctx->tmXp;
+      a1.tmBs[0] = ctx->tmXp32;
+      a1.tmBs[1] = ctx->tmXp32;
       a1.out[0] = ws.h;
       a1.out[1] = ws.hs;
       a1.ldo[0] = c.inter;
@@ -510,6 +551,8 @@ int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, con
       a2.tmA[1] = L.tmA2[1];
       a2.tmB[0] = ctx->tmH;
       a2.tmB[1] = ctx->tmHs;
+      a2.tmBs[0] = ctx->tmH32;
+      a2.tmBs[1] = ctx->tmHs32;
       a2.out[0] = ws.y;
       a2.out[1] = ws.s;
       a2.ldo[0] = a2.ldo[1] = c.hidden;
@@ -645,19 +688,24 @@ int64_t afd_launch_count(afd_ctx* ctx) { return ctx ? ctx->launches : -1; }
 
 int afd_profile(afd_ctx* ctx, int enable) {
   if (!ctx) return AFD_ERR_ARG;
-  if (enable && !ctx->ev[0])
-    for (auto& e : ctx->ev)
-      if (cuda_fail(cudaEventCreate(&e), "event create")) return AFD_ERR_CUDA;
+  if (enable && !ctx->events_made) {
+    for (auto& set : ctx->ev)
+      for (auto& e : set)
+        if (cuda_fail(cudaEventCreate(&e), "event create")) return AFD_ERR_CUDA;
+    ctx->events_made = true;
+  }
   ctx->profiling = enable != 0;
   return AFD_OK;
 }
 
-int afd_stage_times(afd_ctx* ctx, float* ms, int n) {
-  if (!ctx || !ms || n < 0 || n > AFD_NUM_STAGES || !ctx->ev[0]) return AFD_ERR_ARG;
-  if (cuda_fail(cudaEventSynchronize(ctx->ev[AFD_NUM_STAGES]), "event sync")) return AFD_ERR_CUDA;
-  for (int i = 0; i < n; i++)
-    if (cuda_fail(cudaEventElapsedTime(&ms[i], ctx->ev[i], ctx->ev[i + 1]), "event time"))
-      return AFD_ERR_CUDA;
+int afd_stage_times(afd_ctx* ctx, float* ms, int n, int64_t* forwards) {
+  if (!ctx || !ms || n < 0 || n > AFD_NUM_STAGES || !ctx->events_made) return AFD_ERR_ARG;
+  while (ctx->prof_pending > 0)
+    if (ctx->fold_oldest()) return cuda_fail(cudaGetLastError(), "stage events");
+  for (int i = 0; i < n; i++) ms[i] = (float)ctx->prof_acc[i];
+  if (forwards) *forwards = ctx->prof_acc_n;
+  for (double& a : ctx->prof_acc) a = 0.0;
+  ctx->prof_acc_n = 0;
   return AFD_OK;
 }
 

@@ -32,6 +32,8 @@ constexpr int BN_HALF = 128;       // token rows per CTA (256 per unit)
 constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN_HALF * BK * 2;  // one [128 tokens][64 k] box
+constexpr int SMALL_BOX_ROWS = 32;
+constexpr int SMALL_BOX_BYTES = SMALL_BOX_ROWS * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + EPI_WARPS * 32;
@@ -152,13 +154,14 @@ __device__ __forceinline__ Unit decode_unit(const GemmPlan& p, int unit) {
     if (p.g[mid].unit0 <= unit) lo = mid; else hi = mid - 1;
   }
   const GemmGroup& G = p.g[lo];
-  const int m_pairs = (G.m_tiles + 1) / 2;
   const int u = unit - G.unit0;
   Unit t;
   t.group = lo;
   t.kind = G.kind;
-  t.mpair = u % m_pairs;
-  t.nt = u / m_pairs;
+  // token tiles vary fastest: units sharing a weight tile run on
+  // neighbouring clusters, so a weight tile read twice hits L2 the second time
+  t.nt = u % G.n_tiles;
+  t.mpair = u / G.n_tiles;
   t.rows = min(p.bn, G.rows - t.nt * p.bn);
   t.n_mma = (t.rows + 31) & ~31;    // even halves of 16-row multiples
   return t;
@@ -236,18 +239,21 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
         const Unit t = decode_unit(plan, unit);
         const GemmGroup& G = plan.g[t.group];
         const int nkb = (args.K[t.kind] + BK - 1) / BK;
-        // one 128-row token box per CTA and k-block (rows past the half are
-        // read but not used by the MMA; past the buffer they are zero-filled)
+        // one token box per CTA and k-block: 128 rows, or 32 rows when the
+        // unit's half fits (decode-sized groups); rows past the half are read
+        // but not used by the MMA, past the buffer they are zero-filled
         const int half = t.n_mma / 2;
         const int brow = G.b_row0 + t.nt * plan.bn + (int)rank * half;
+        const bool small_box = half <= SMALL_BOX_ROWS;
+        const uint32_t b_bytes = small_box ? SMALL_BOX_BYTES : B_BYTES;
         const int mt = 2 * t.mpair + (int)rank;
         const CUtensorMap* ta = &args.tmA[t.kind];
-        const CUtensorMap* tb = &args.tmB[t.kind];
+        const CUtensorMap* tb = small_box ? &args.tmBs[t.kind] : &args.tmB[t.kind];
         bool ok = true;
         for (int kb = 0; kb < nkb; kb++) {
           if (!wait_bar(smem_u32(&tail->empty[s]), ph ^ 1, abort_flag, deadline, args.status)) { ok = false; break; }
           const uint32_t full_leader = map_to_rank(smem_u32(&tail->full[s]), 0);
-          if (rank == 0) mbar_expect_tx(smem_u32(&tail->full[s]), 2 * (A_BYTES + B_BYTES));
+          if (rank == 0) mbar_expect_tx(smem_u32(&tail->full[s]), 2 * (A_BYTES + b_bytes));
           const uint32_t sa = smem_base + s * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
           if (args.swiglu)

@@ -52,6 +52,7 @@ struct DevWS {
   float* s;               // f32 [Tmax, H]
   int32_t* hist;          // [E, router CTAs] per-CTA expert histograms
   int32_t* base;          // [E, router CTAs] each CTA's first slot in each expert segment
+  float* logits;          // [Tmax, E] router logits
 };
 
 // one group of the grouped GEMM: rows of the B operand (tokens) that share
@@ -82,6 +83,8 @@ struct GemmArgs {
   CUtensorMap tmB[2];     // token rows: [0] routed source, [1] shared source
                           // (box 64 x 32 rows for the one-CTA engine, 64 x 128
                           // rows for the SM-pair engine)
+  CUtensorMap tmBs[2];    // the same sources with 64 x 32 boxes: the SM-pair
+                          // engine uses them for units of <= 64 tokens
   void* out[2];           // outputs per kind
   int64_t ldo[2];         // output row pitch in elements
   int out_f32[2];         // 1 = fp32 output, 0 = bf16
@@ -130,14 +133,16 @@ __device__ __forceinline__ int read_status(const int32_t* status) {
   return *(volatile const int32_t*)status;
 }
 
+// Flags are read and written with device scope: every peer of a window
+// lives on this GPU (a cross-GPU transport would need system scope).
 __device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
   uint64_t v;
-  asm volatile("ld.acquire.sys.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 
 __device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
-  asm volatile("st.release.sys.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -245,10 +250,12 @@ cudaError_t launch_header_check(const LaunchCtx& lc, const WinGeom& g, const uin
 // CTAs of the router for T tokens (16 tokens each); sizes the histograms
 int router_blocks(int total_tokens);
 size_t router_min_smem_bytes(int hidden, int E, int act_f32);
+// router: logits [T, E] fp32 (caller's scratch), then top-k / gate weights
+// into ws.ids / ws.w and, if hist is not NULL, the per-16-token histograms
 cudaError_t launch_router(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                           const FanIn& f, const DevWS& ws, int hidden, int act_f32,
                           const float* WgT, const float* bias, int E, int k, int renorm,
-                          float scale, int32_t* hist);
+                          float scale, float* logits, int32_t* hist);
 cudaError_t launch_plan(const LaunchCtx& lc, const FanIn& f, const DevWS& ws, int E, int k,
                         int inter, int shared_inter, int hidden, int has_shared, int bn,
                         GemmPlan* plan1, GemmPlan* plan2, const int32_t* hist, int32_t* base);

@@ -7,7 +7,6 @@
 namespace {
 
 constexpr int kThreads = 256;
-constexpr size_t kRouterSmemLimit = 232448;  // per-CTA opt-in shared memory
 
 __device__ __forceinline__ uint8_t* slot_ptr(uint8_t* win, const WinGeom& g, int region,
                                              int stage) {
@@ -80,7 +79,7 @@ __global__ void k_pack_header(uint8_t* win, WinGeom g, int region, int stage, in
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence_system();
+    __threadfence();
     uint64_t* flag = reinterpret_cast<uint64_t*>(win) + (int64_t)region * g.ring_depth + stage;
     st_release_u64(flag, seq);
   }
@@ -118,8 +117,18 @@ __global__ void k_header_check(const uint8_t* win, WinGeom g, FanIn f, DevWS ws,
       fl = ld_acquire_u64(flagp);
     }
     if (!e) {
-      const volatile int32_t* h =
-          reinterpret_cast<const volatile int32_t*>(slot_ptr(win, g, f.region[i], f.stage) + g.header);
+      // the 12 fixed words in three 16-byte loads, ordered after the acquire
+      int32_t h[12];
+      const int4* hp = reinterpret_cast<const int4*>(slot_ptr(win, g, f.region[i], f.stage) + g.header);
+#pragma unroll
+      for (int q = 0; q < 3; q++) {
+        int4 v;
+        asm volatile("ld.relaxed.gpu.global.v4.s32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "l"(hp + q)
+                     : "memory");
+        h[4 * q] = v.x; h[4 * q + 1] = v.y; h[4 * q + 2] = v.z; h[4 * q + 3] = v.w;
+      }
       const int n = f.prefix[i + 1] - f.prefix[i];
       if ((uint32_t)h[0] != (uint32_t)AFD_HEADER_MAGIC || h[1] != AFD_HEADER_VERSION ||
           h[10] != E || h[11] != AFD_HEADER_FIXED_WORDS + E)
@@ -147,25 +156,44 @@ __global__ void k_header_check(const uint8_t* win, WinGeom g, FanIn f, DevWS ws,
   }
   __syncthreads();
   // shared_idx must be 0..n-1: with one FFN rank every token is a shared
-  // token (Async GPU Connector, "Data flow" step 3).
-  // (8 independent loads in flight per thread)
-  for (int i = 0; i < f.n_peers; i++) {
-    if (err[i] || shared_n[i] == 0) continue;
-    const int32_t* sidx = reinterpret_cast<const int32_t*>(slot_ptr(win, g, f.region[i], f.stage) +
-                                                           g.shared_idx);
-    const int n = shared_n[i];
-    int bad = 0;
-    for (int r0 = tid; r0 < n; r0 += 8 * blockDim.x) {
-      int v[8];
+  // token (Async GPU Connector, "Data flow" step 3).  The rows of all peers
+  // form one index space, 8 independent loads in flight per thread.
+  {
+    __shared__ int sh_prefix[AFD_MAX_PEERS + 1];
+    if (tid == 0) {
+      int run = 0;
+      for (int i = 0; i < f.n_peers; i++) {
+        sh_prefix[i] = run;
+        run += err[i] ? 0 : shared_n[i];
+      }
+      sh_prefix[f.n_peers] = run;
+    }
+    __syncthreads();
+    const int total = sh_prefix[f.n_peers];
+    for (int r0 = tid; r0 < total; r0 += 8 * blockDim.x) {
+      int v[8], want[8], who[8];
 #pragma unroll
       for (int u = 0; u < 8; u++) {
         const int r = r0 + u * blockDim.x;
-        v[u] = r < n ? sidx[r] : r;
+        who[u] = -1;
+        v[u] = want[u] = 0;
+        if (r < total) {
+          int lo = 0, hi = f.n_peers - 1;
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (sh_prefix[mid] <= r) lo = mid; else hi = mid - 1;
+          }
+          const int32_t* sidx = reinterpret_cast<const int32_t*>(
+              slot_ptr(win, g, f.region[lo], f.stage) + g.shared_idx);
+          want[u] = r - sh_prefix[lo];
+          who[u] = lo;
+          v[u] = sidx[want[u]];
+        }
       }
 #pragma unroll
-      for (int u = 0; u < 8; u++) bad |= v[u] != r0 + u * (int)blockDim.x;
+      for (int u = 0; u < 8; u++)
+        if (who[u] >= 0 && v[u] != want[u]) bad_sidx[who[u]] = 1;
     }
-    if (bad) bad_sidx[i] = 1;
   }
   __syncthreads();
   if (tid == 0) {
@@ -187,17 +215,9 @@ __global__ void k_header_check(const uint8_t* win, WinGeom g, FanIn f, DevWS ws,
 }
 
 // ---------------------------------------------------------------------------
-// a1: router.  logits in the canonical fp32 order: lane l of a warp owns the
-// fused multiply-add chain over h = l, l+32, ... ascending (from +0), then a
-// butterfly with xor offsets 16, 8, 4, 2, 1, then + bias.  Top-k on the
-// logits (ties -> lower expert index, NaN below every number), softmax over
-// all E for the weights.
-// CTA: 16 warps x 16 tokens.  The tokens are staged transposed in smem
-// ([h][16 tokens]) straight from the peer slots, so a lane fetches its 16
-// values of one h with 16-byte loads; the transposed router weight streams
-// through a double-buffered cp.async ring of [64 experts][128 h] chunks.
-// Warp w owns experts 4w..4w+3 of the current 64-expert group.  The CTA
-// also writes its per-expert histogram (hist[e][cta]) for the plan.
+// a1: router (DeepSeek-V2 MoE gate: softmax over the expert affinities,
+// top-k of them).  Two kernels: k_router_logits writes the fp32 logits in
+// one fixed summation order, k_router_topk selects and weights.
 // ---------------------------------------------------------------------------
 // Float-float helpers for the softmax: a value carried as hi + lo with the
 // rounding error of every addition kept (two-sum), so sums of E terms carry
@@ -234,172 +254,155 @@ __device__ __forceinline__ float exp_of_diff(float a, float b) {
   return __fmaf_rn(e, err, e);
 }
 
-constexpr int kRtTok = 16;                     // tokens per CTA
-constexpr int kRtWarps = 32;
-constexpr int kRtTpw = 8;                      // tokens per warp
-constexpr int kRtEpw = 4;                      // experts per warp
-constexpr int kRtEgroup = (kRtWarps / (kRtTok / kRtTpw)) * kRtEpw;   // 64 experts per pass
-constexpr int kRtHc = 128;                     // h per weight chunk
+constexpr int kRtTok = 16;        // tokens per top-k CTA (and per plan histogram)
+constexpr int kLgTok = 8;         // tokens per logits warp
+constexpr int kLgEpw = 4;         // experts per logits warp
+constexpr int kLgWarps = 4;
+constexpr int kLgEblk = kLgWarps * kLgEpw;   // experts per logits CTA
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
-
-// stage weight chunk c of expert group e_base: WgT[e_base + r][c*128 .. +128)
-__device__ __forceinline__ void router_stage_w(float* dst, const float* __restrict__ WgT, int e_base,
-                                               int E, int hidden, int c) {
-  const int h0 = c * kRtHc;
-  for (int p = threadIdx.x; p < kRtEgroup * (kRtHc / 4); p += blockDim.x) {
-    const int r = p / (kRtHc / 4), q = p % (kRtHc / 4);
-    const int e = e_base + r, h = h0 + q * 4;
-    if (e < E && h < hidden) cp_async16(dst + r * kRtHc + q * 4, WgT + (int64_t)e * hidden + h);
-  }
-}
-
-// Token tile held in smem as XS (fp32, or bf16 bits when fp32 would not fit)
-// in 16-byte groups of tokens, group-major ([group][h][tokens of the group]):
-// the lane owning h reads a group with one 16-byte load, contiguous across
-// the warp's lanes (no bank conflicts).
+// Token tile of a logits CTA in smem (bf16 bits, or fp32 for fp32
+// activations), in 16-byte groups of tokens, group-major
+// ([group][h][tokens of the group]): the lane owning h reads a group with
+// one 16-byte load, contiguous across the warp's lanes (no bank conflicts).
 template <typename XS>
-__device__ __forceinline__ size_t xt_index(int h, int tt, int hidden) {
+__device__ __forceinline__ int lg_index(int h, int tt, int hidden) {
   constexpr int per = 16 / sizeof(XS);
-  return ((size_t)(tt / per) * hidden + h) * per + (tt % per);
+  return ((tt / per) * hidden + h) * per + (tt % per);
 }
 
+// a1 router, part 1: logits in the canonical fp32 order.  Lane l of a warp
+// owns the fused multiply-add chain over h = l, l+32, ... ascending (from
+// +0); a butterfly with xor offsets 16, 8, 4, 2, 1 sums the 32 chains, then
+// + bias.  CTA (8 tokens, 16 experts): warp w takes experts 4w..4w+3 for all
+// 8 tokens; the token rows are staged from the peer slots into smem, the
+// transposed router weight [E][hidden] is read from L2 with the next step's
+// values loaded ahead of the current step's multiply-adds.
 template <typename XS>
-__device__ __forceinline__ void load_tokens(const XS* xT, int h, int tt0, int hidden, float (&xv)[kRtTpw]) {
-  if constexpr (sizeof(XS) == 4) {
-#pragma unroll
-    for (int q = 0; q < kRtTpw / 4; q++) {
-      const float4 v4 = *reinterpret_cast<const float4*>(xT + xt_index<XS>(h, tt0 + 4 * q, hidden));
-      xv[4 * q] = v4.x; xv[4 * q + 1] = v4.y; xv[4 * q + 2] = v4.z; xv[4 * q + 3] = v4.w;
-    }
-  } else {
-    const uint4 v4 = *reinterpret_cast<const uint4*>(xT + xt_index<XS>(h, tt0, hidden));
-    const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
-#pragma unroll
-    for (int m = 0; m < 4; m++) {
-      xv[2 * m] = __uint_as_float(w4[m] << 16);
-      xv[2 * m + 1] = __uint_as_float(w4[m] & 0xffff0000u);
-    }
-  }
-}
-
-// a1 router.  logits in the canonical fp32 order: lane l of a warp owns the
-// fused multiply-add chain over h = l, l+32, ... ascending (from +0), then a
-// butterfly with xor offsets 16, 8, 4, 2, 1, then + bias.  Top-k on the
-// logits (ties -> lower expert index, NaN below every number), softmax over
-// all E for the gate weights.  CTA: 32 warps over 16 tokens; warp w owns
-// tokens 8*(w/16) .. +8 and experts 4*(w%16) .. +4 of the current 64-expert
-// pass, the transposed router weight streaming through a double-buffered
-// cp.async ring of [64 experts][128 h] chunks.  The CTA also writes its
-// per-expert histogram (hist[e][cta]) for the plan.
-template <bool ACT_F32, typename XS>
-__global__ void __launch_bounds__(kRtWarps * 32, 1)
-k_router(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int hidden,
-         const float* __restrict__ WgT, const float* __restrict__ bias, int E, int k,
-         int renorm, float scale, int32_t* __restrict__ hist, int nblocks) {
-  extern __shared__ __align__(16) uint8_t rt_smem[];
-  using act_t = typename std::conditional<ACT_F32, float, uint16_t>::type;
-  XS* xT = reinterpret_cast<XS*>(rt_smem);                                        // [hidden][16]
-  float* wbuf = reinterpret_cast<float*>(rt_smem + (size_t)hidden * kRtTok * sizeof(XS));  // [2][64][128]
-  float* lg = wbuf + 2 * kRtEgroup * kRtHc;                                      // [16][E]
-  int* hs = reinterpret_cast<int*>(lg + kRtTok * E);                             // [E]
+__global__ void __launch_bounds__(kLgWarps * 32)
+k_router_logits(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int hidden,
+                const float* __restrict__ WgT, const float* __restrict__ bias, int E,
+                float* __restrict__ logits) {
+  extern __shared__ __align__(16) uint8_t lg_smem[];
+  XS* xT = reinterpret_cast<XS*>(lg_smem);       // [hidden][8 tokens]
   if (read_status(ws.status)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t0 = blockIdx.x * kRtTok;
-  const int row_bytes = hidden * (int)sizeof(act_t);
-  constexpr int kVecElems = 16 / sizeof(act_t);
-  for (int e = threadIdx.x; e < E; e += blockDim.x) hs[e] = 0;
-  // stage the 16 token rows straight from the peer slots, transposed
+  const int t0 = blockIdx.x * kLgTok;
+  constexpr bool kF32 = sizeof(XS) == 4;
+  const int row_bytes = hidden * (int)sizeof(XS);
+  constexpr int kVecElems = 16 / sizeof(XS);
   {
-    const int tt = threadIdx.x % kRtTok;
+    // thread -> (token tt, vectors v = tid / 8, + 16, ...); 4 loads in flight
+    const int tt = threadIdx.x % kLgTok;
     const int t = t0 + tt;
     const int nvec = row_bytes / 16;
+    const int step = blockDim.x / kLgTok;
     const uint4* src = nullptr;
     if (t < f.total) {
       const int i = entry_of(f, t);
       src = reinterpret_cast<const uint4*>(slot_ptr(win, g, f.region[i], f.stage) + g.routed_x +
                                            (int64_t)(t - f.prefix[i]) * row_bytes);
     }
-    for (int v = threadIdx.x / kRtTok; v < nvec; v += blockDim.x / kRtTok) {
-      const uint4 val = src ? src[v] : make_uint4(0, 0, 0, 0);
-      const act_t* e8 = reinterpret_cast<const act_t*>(&val);
+    for (int v0 = threadIdx.x / kLgTok; v0 < nvec; v0 += 4 * step) {
+      uint4 val[4];
 #pragma unroll
-      for (int m = 0; m < kVecElems; m++) {
-        XS xs;
-        if constexpr (sizeof(XS) == sizeof(act_t)) xs = e8[m];
-        else xs = __uint_as_float((uint32_t)e8[m] << 16);   // bf16 -> fp32, exact
-        xT[xt_index<XS>(v * kVecElems + m, tt, hidden)] = xs;
+      for (int u = 0; u < 4; u++) {
+        const int v = v0 + u * step;
+        val[u] = (src && v < nvec) ? src[v] : make_uint4(0, 0, 0, 0);
       }
-    }
-  }
-  const int th = warp / (kRtWarps / 2);            // token half
-  const int eg = warp % (kRtWarps / 2);            // expert group within the pass
-  const int tt0 = th * kRtTpw;
-  const int nchunks = (hidden + kRtHc - 1) / kRtHc;
-  for (int e_base = 0; e_base < E; e_base += kRtEgroup) {
-    const int e0 = e_base + eg * kRtEpw;
-    float acc[kRtTpw][kRtEpw];
 #pragma unroll
-    for (int a = 0; a < kRtTpw; a++)
+      for (int u = 0; u < 4; u++) {
+        const int v = v0 + u * step;
+        if (v >= nvec) break;
+        const XS* e8 = reinterpret_cast<const XS*>(&val[u]);
 #pragma unroll
-      for (int b = 0; b < kRtEpw; b++) acc[a][b] = 0.0f;
-    router_stage_w(wbuf, WgT, e_base, E, hidden, 0);
-    cp_async_commit();
-    for (int c = 0; c < nchunks; c++) {
-      if (c + 1 < nchunks) router_stage_w(wbuf + ((c + 1) & 1) * kRtEgroup * kRtHc, WgT, e_base, E, hidden, c + 1);
-      cp_async_commit();
-      cp_async_wait1();
-      __syncthreads();
-      const float* wc = wbuf + (c & 1) * kRtEgroup * kRtHc + (eg * kRtEpw) * kRtHc;
-      if (e0 < E) {
-#pragma unroll
-        for (int i = 0; i < kRtHc / 32; i++) {
-          const int hl = lane + 32 * i;
-          const int h = c * kRtHc + hl;
-          if (h < hidden) {
-            float xv[kRtTpw];
-            load_tokens<XS>(xT, h, tt0, hidden, xv);
-            float wv[kRtEpw];
-#pragma unroll
-            for (int b = 0; b < kRtEpw; b++) wv[b] = wc[b * kRtHc + hl];
-#pragma unroll
-            for (int a = 0; a < kRtTpw; a++)
-#pragma unroll
-              for (int b = 0; b < kRtEpw; b++) acc[a][b] = __fmaf_rn(xv[a], wv[b], acc[a][b]);
-          }
-        }
+        for (int m = 0; m < kVecElems; m++) xT[lg_index<XS>(v * kVecElems + m, tt, hidden)] = e8[m];
       }
-      __syncthreads();
-    }
-    if (e0 < E) {
-#pragma unroll
-      for (int a = 0; a < kRtTpw; a++)
-#pragma unroll
-        for (int b = 0; b < kRtEpw; b++) {
-          float v = acc[a][b];
-#pragma unroll
-          for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
-          acc[a][b] = v;
-        }
-#pragma unroll
-      for (int a = 0; a < kRtTpw; a++)
-        if (lane == a)
-#pragma unroll
-          for (int b = 0; b < kRtEpw; b++)
-            if (e0 + b < E)
-              lg[(tt0 + a) * E + e0 + b] = bias ? __fadd_rn(acc[a][b], bias[e0 + b]) : acc[a][b];
     }
   }
   __syncthreads();
-  // top-k and gate weights: one warp per token
-  for (int tt = warp; tt < kRtTok; tt += kRtWarps) {
-    const int t = t0 + tt;
-    if (t >= f.total) continue;
-    const float* l = lg + tt * E;
+  const int e0 = blockIdx.y * kLgEblk + warp * kLgEpw;
+  if (e0 >= E) return;
+  const float* wrow[kLgEpw];
+#pragma unroll
+  for (int b = 0; b < kLgEpw; b++) wrow[b] = WgT + (int64_t)min(e0 + b, E - 1) * hidden;
+  float acc[kLgTok][kLgEpw];
+#pragma unroll
+  for (int a = 0; a < kLgTok; a++)
+#pragma unroll
+    for (int b = 0; b < kLgEpw; b++) acc[a][b] = 0.0f;
+  // 4 h-steps per batch: their 16 weight values are loaded together
+  const int nsteps = (hidden + 31) / 32;
+  for (int i0 = 0; i0 < nsteps; i0 += 4) {
+    float wv[4][kLgEpw];
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const int h = lane + 32 * (i0 + u);
+#pragma unroll
+      for (int b = 0; b < kLgEpw; b++) wv[u][b] = h < hidden ? __ldg(wrow[b] + h) : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const int h = lane + 32 * (i0 + u);
+      if (h < hidden) {
+        float xv[kLgTok];
+        if constexpr (kF32) {
+#pragma unroll
+          for (int q = 0; q < kLgTok / 4; q++) {
+            const float4 v4 = *reinterpret_cast<const float4*>(xT + lg_index<XS>(h, 4 * q, hidden));
+            xv[4 * q] = v4.x; xv[4 * q + 1] = v4.y; xv[4 * q + 2] = v4.z; xv[4 * q + 3] = v4.w;
+          }
+        } else {
+          const uint4 v4 = *reinterpret_cast<const uint4*>(xT + lg_index<XS>(h, 0, hidden));
+          const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+          for (int m = 0; m < 4; m++) {
+            xv[2 * m] = __uint_as_float(w4[m] << 16);
+            xv[2 * m + 1] = __uint_as_float(w4[m] & 0xffff0000u);
+          }
+        }
+#pragma unroll
+        for (int a = 0; a < kLgTok; a++)
+#pragma unroll
+          for (int b = 0; b < kLgEpw; b++) acc[a][b] = __fmaf_rn(xv[a], wv[u][b], acc[a][b]);
+      }
+    }
+  }
+#pragma unroll
+  for (int a = 0; a < kLgTok; a++)
+#pragma unroll
+    for (int b = 0; b < kLgEpw; b++) {
+      float v = acc[a][b];
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
+      acc[a][b] = v;
+    }
+#pragma unroll
+  for (int a = 0; a < kLgTok; a++)
+    if (lane == a && t0 + a < f.total)
+#pragma unroll
+      for (int b = 0; b < kLgEpw; b++)
+        if (e0 + b < E)
+          logits[(int64_t)(t0 + a) * E + e0 + b] = bias ? __fadd_rn(acc[a][b], bias[e0 + b]) : acc[a][b];
+}
+
+// a1 router, part 2: top-k on the logits (ties -> lower expert index, NaN
+// below every number) and the gate weights from a softmax over all E
+// (sums carried as float-float); one warp per token, 16 tokens per CTA,
+// whose per-expert histogram (hist[e][cta]) feeds the plan.
+__global__ void __launch_bounds__(kRtTok * 32)
+k_router_topk(FanIn f, DevWS ws, const float* __restrict__ logits, int E, int k, int renorm,
+              float scale, int32_t* __restrict__ hist, int nblocks) {
+  __shared__ int hs[256];
+  if (read_status(ws.status)) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hs[e] = 0;
+  __syncthreads();
+  const int t = blockIdx.x * kRtTok + warp;
+  if (t < f.total) {
+    const float* l = logits + (int64_t)t * E;
+    float lv[8];  // logit of expert lane + 32m
+#pragma unroll
+    for (int m = 0; m < 8; m++) lv[m] = (m * 32 + lane < E) ? l[m * 32 + lane] : -INFINITY;
     uint32_t taken = 0;  // bit m: expert lane + 32m chosen (E <= 256)
     float top_logit = 0.0f;
     int my_id = 0;       // lane j keeps the j-th choice
@@ -407,10 +410,11 @@ k_router(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int hidden,
     for (int j = 0; j < k; j++) {
       float bv = -INFINITY;
       int bi = 0x7fffffff;
-      for (int m = 0; m * 32 + lane < E; m++) {
+#pragma unroll
+      for (int m = 0; m < 8; m++) {
         const int e = m * 32 + lane;
-        if (taken & (1u << m)) continue;
-        float v = l[e];
+        if (e >= E || (taken & (1u << m))) continue;
+        float v = lv[m];
         if (v != v) v = -INFINITY;  // a NaN logit ranks below every number
         if (v > bv || (v == bv && e < bi)) { bv = v; bi = e; }
       }
@@ -424,9 +428,10 @@ k_router(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int hidden,
       if (j == 0) top_logit = bv;
       if (lane == j) { my_id = bi; my_logit = bv; }
     }
-    // softmax over all E relative to the maximum, sums carried as float-float
     ffloat den = {0.0f, 0.0f};
-    for (int m = 0; m * 32 + lane < E; m++) den = ff_add(den, exp_of_diff(l[m * 32 + lane], top_logit));
+#pragma unroll
+    for (int m = 0; m < 8; m++)
+      if (m * 32 + lane < E) den = ff_add(den, exp_of_diff(lv[m], top_logit));
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) den = ff_add(den, ff_shfl_xor(den, off));
     const float p = (lane < k) ? ff_div(exp_of_diff(my_logit, top_logit), den) : 0.0f;
@@ -452,6 +457,52 @@ k_router(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int hidden,
 // segment (base[e][b] = sum of hist[e][b'] for b' < b), the zeroed per-peer
 // counts, and the tile tables of both grouped GEMMs.
 // ---------------------------------------------------------------------------
+// Tile tables of both grouped GEMMs from the per-expert counts and offsets:
+// one group per expert (rows = its partials, in permuted order), then the
+// shared expert over all T rows; tile0 / unit0 are prefixes of the one-CTA
+// tiles and of the SM-pair units.
+__device__ void write_tile_tables(const FanIn& f, int k, int E, int inter, int shared_inter,
+                                  int hidden, int has_shared, int bn, const int* cnt,
+                                  const int* offs, GemmPlan* plan1, GemmPlan* plan2) {
+  const int N = f.total * k;
+  int tiles1 = 0, tiles2 = 0, units1 = 0, units2 = 0, ng = 0;
+  const int mt1 = (inter + 63) / 64, mt2 = (hidden + 127) / 128;
+  for (int e = 0; e < E; e++, ng++) {
+    const int rows = cnt[e];
+    const int nt = (rows + bn - 1) / bn;
+    GemmGroup a{rows, offs[e], offs[e], e, 0, mt1, nt, tiles1, units1};
+    GemmGroup b{rows, offs[e], offs[e], e, 0, mt2, nt, tiles2, units2};
+    plan1->g[ng] = a;
+    plan2->g[ng] = b;
+    tiles1 += mt1 * nt;
+    tiles2 += mt2 * nt;
+    units1 += (mt1 + 1) / 2 * nt;
+    units2 += (mt2 + 1) / 2 * nt;
+  }
+  if (has_shared) {
+    const int rows = f.total;
+    const int nt = (rows + bn - 1) / bn;
+    const int mts = (shared_inter + 63) / 64;
+    GemmGroup a{rows, N, 0, 0, 1, mts, nt, tiles1, units1};
+    GemmGroup b{rows, 0, 0, 0, 1, mt2, nt, tiles2, units2};
+    plan1->g[ng] = a;
+    plan2->g[ng] = b;
+    tiles1 += mts * nt;
+    tiles2 += mt2 * nt;
+    units1 += (mts + 1) / 2 * nt;
+    units2 += (mt2 + 1) / 2 * nt;
+    ng++;
+  }
+  plan1->ngroups = ng;
+  plan2->ngroups = ng;
+  plan1->total_tiles = tiles1;
+  plan2->total_tiles = tiles2;
+  plan1->total_units = units1;
+  plan2->total_units = units2;
+  plan1->bn = bn;
+  plan2->bn = bn;
+}
+
 constexpr int kScanWarps = 32;
 
 __global__ void __launch_bounds__(kScanWarps * 32)
@@ -496,46 +547,87 @@ k_plan_scan(FanIn f, DevWS ws, int E, int k, int inter, int shared_inter, int hi
     ws.offsets[e] = offs[e];
     if (e < E) ws.counts[e] = cnt[e];
   }
-  // tile tables
-  if (tid == 0) {
-    const int N = f.total * k;
-    int tiles1 = 0, tiles2 = 0, units1 = 0, units2 = 0, ng = 0;
-    const int mt1 = (inter + 63) / 64, mt2 = (hidden + 127) / 128;
-    for (int e = 0; e < E; e++, ng++) {
-      const int rows = cnt[e];
-      const int nt = (rows + bn - 1) / bn;
-      GemmGroup a{rows, offs[e], offs[e], e, 0, mt1, nt, tiles1, units1};
-      GemmGroup b{rows, offs[e], offs[e], e, 0, mt2, nt, tiles2, units2};
-      plan1->g[ng] = a;
-      plan2->g[ng] = b;
-      tiles1 += mt1 * nt;
-      tiles2 += mt2 * nt;
-      units1 += (mt1 + 1) / 2 * nt;
-      units2 += (mt2 + 1) / 2 * nt;
+  if (tid == 0) write_tile_tables(f, k, E, inter, shared_inter, hidden, has_shared, bn, cnt, offs, plan1, plan2);
+}
+
+// ---------------------------------------------------------------------------
+// a2/a3 plan for small fan-ins (T*k <= kPlanSmallMax, e.g. decode): one CTA
+// does the counts, offsets, per-peer counts, the stable permutation (warp w
+// owns a contiguous chunk of f; per-warp histograms give its cursor per
+// expert; 32-element rounds are ranked with match_any) and the tile tables.
+// ---------------------------------------------------------------------------
+constexpr int kPlanSmallMax = 8192;
+
+__global__ void __launch_bounds__(1024)
+k_plan_small(FanIn f, DevWS ws, int E, int k, int inter, int shared_inter, int hidden,
+             int has_shared, int bn, GemmPlan* plan1, GemmPlan* plan2) {
+  __shared__ int hist_w[32][256];
+  __shared__ int cnt[256];
+  __shared__ int offs[257];
+  __shared__ int skip;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) skip = read_status(ws.status);
+  for (int i = tid; i < 32 * 256; i += blockDim.x) (&hist_w[0][0])[i] = 0;
+  for (int i = tid; i < f.n_peers * E; i += blockDim.x) ws.peer_counts[i] = 0;
+  __syncthreads();
+  if (skip) return;
+  const int N = f.total * k;
+  const int chunk = (N + 31) / 32;
+  const int c0 = min(N, warp * chunk), c1 = min(N, c0 + chunk);
+  for (int fi = c0 + lane; fi < c1; fi += 32) {
+    int e = ws.ids[fi];
+    if (e < 0 || e >= E) {  // cannot come from the router; keep every index in range
+      set_error(ws.status, AFD_ERR_SHAPE);
+      e = 0;
+      ws.ids[fi] = 0;
     }
-    if (has_shared) {
-      const int rows = f.total;
-      const int nt = (rows + bn - 1) / bn;
-      const int mts = (shared_inter + 63) / 64;
-      GemmGroup a{rows, N, 0, 0, 1, mts, nt, tiles1, units1};
-      GemmGroup b{rows, 0, 0, 0, 1, mt2, nt, tiles2, units2};
-      plan1->g[ng] = a;
-      plan2->g[ng] = b;
-      tiles1 += mts * nt;
-      tiles2 += mt2 * nt;
-      units1 += (mts + 1) / 2 * nt;
-      units2 += (mt2 + 1) / 2 * nt;
-      ng++;
-    }
-    plan1->ngroups = ng;
-    plan2->ngroups = ng;
-    plan1->total_tiles = tiles1;
-    plan2->total_tiles = tiles2;
-    plan1->total_units = units1;
-    plan2->total_units = units2;
-    plan1->bn = bn;
-    plan2->bn = bn;
+    atomicAdd(&hist_w[warp][e], 1);
+    atomicAdd(&ws.peer_counts[entry_of(f, fi / k) * E + e], 1);
   }
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) {
+    int c = 0;
+    for (int w = 0; w < 32; w++) c += hist_w[w][e];
+    cnt[e] = c;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int run = 0;
+    for (int e = 0; e < E; e++) { offs[e] = run; run += cnt[e]; }
+    offs[E] = run;
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) {
+    int base = offs[e];
+    for (int w = 0; w < 32; w++) {
+      const int c = hist_w[w][e];
+      hist_w[w][e] = base;  // warp w's cursor for expert e
+      base += c;
+    }
+  }
+  for (int e = tid; e <= E; e += blockDim.x) {
+    ws.offsets[e] = offs[e];
+    if (e < E) ws.counts[e] = cnt[e];
+  }
+  __syncthreads();
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int g0 = c0; g0 < c1; g0 += 32) {
+    const int fi = g0 + lane;
+    const bool ok = fi < c1;
+    const int e = ok ? ws.ids[fi] : -1 - lane;
+    const unsigned same = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(same & lt_mask);
+    int pos = 0;
+    if (ok) pos = hist_w[warp][e] + rank;
+    __syncwarp();
+    if (ok && rank == 0) hist_w[warp][e] += __popc(same);
+    __syncwarp();
+    if (ok) {
+      ws.perm[pos] = fi;
+      ws.inv[fi] = pos;
+    }
+  }
+  if (tid == 0) write_tile_tables(f, k, E, inter, shared_inter, hidden, has_shared, bn, cnt, offs, plan1, plan2);
 }
 
 // ---------------------------------------------------------------------------
@@ -684,7 +776,12 @@ k_combine(uint8_t* ret, WinGeom g, FanIn f, DevWS ws, int hidden, int k, int has
   constexpr int kVec = 8;
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * (blockDim.x >> 5);
-  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < f.total; t += warps) {
+  // work item = (token, block of 256 features): a small fan-in still spreads
+  // over every SM
+  const int nfb = (hidden + 32 * kVec - 1) / (32 * kVec);
+  const int64_t items = (int64_t)f.total * nfb;
+  for (int64_t it = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items; it += warps) {
+    const int t = (int)(it / nfb), fb = (int)(it % nfb);
     const int i = entry_of(f, t);
     const int local = t - f.prefix[i];
     uint8_t* slot = slot_ptr(ret, g, f.region[i], f.stage);
@@ -693,10 +790,15 @@ k_combine(uint8_t* ret, WinGeom g, FanIn f, DevWS ws, int hidden, int k, int has
     if (lane < k) {
       my_pos = ws.inv[(int64_t)t * k + lane];
       my_w = ws.w[(int64_t)t * k + lane];
-      reinterpret_cast<int32_t*>(slot + g.route_table)[(int64_t)local * k + lane] =
-          ws.ids[(int64_t)t * k + lane];
+      if (fb == 0)
+        reinterpret_cast<int32_t*>(slot + g.route_table)[(int64_t)local * k + lane] =
+            ws.ids[(int64_t)t * k + lane];
     }
-    for (int c = lane * kVec; c < hidden; c += 32 * kVec) {
+    {
+      // every lane takes part in the shuffles; lanes past hidden skip memory
+      const int c0 = fb * 32 * kVec + lane * kVec;
+      const bool valid = c0 < hidden;
+      const int c = valid ? c0 : 0;
       float acc[kVec];
 #pragma unroll
       for (int q = 0; q < kVec; q++) acc[q] = 0.0f;
@@ -707,12 +809,14 @@ k_combine(uint8_t* ret, WinGeom g, FanIn f, DevWS ws, int hidden, int k, int has
         if constexpr (Y_F32) {
           const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(ws.y) +
                                                               (int64_t)pos * hidden + c);
-          const float4 a = src[0], b = src[1];
+          const float4 a = valid ? src[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float4 b = valid ? src[1] : make_float4(0.f, 0.f, 0.f, 0.f);
           yv[0] = a.x; yv[1] = a.y; yv[2] = a.z; yv[3] = a.w;
           yv[4] = b.x; yv[5] = b.y; yv[6] = b.z; yv[7] = b.w;
         } else {
-          const uint4 v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(ws.y) +
-                                                         (int64_t)pos * hidden + c);
+          const uint4 v = valid ? *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(ws.y) +
+                                                                 (int64_t)pos * hidden + c)
+                                : make_uint4(0, 0, 0, 0);
           const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (int m = 0; m < 4; m++) {
@@ -723,29 +827,31 @@ k_combine(uint8_t* ret, WinGeom g, FanIn f, DevWS ws, int hidden, int k, int has
 #pragma unroll
         for (int q = 0; q < kVec; q++) acc[q] = __fmaf_rn(wj, yv[q], acc[q]);
       }
-      if (has_shared) {
-        const float4* sp = reinterpret_cast<const float4*>(ws.s + (int64_t)t * hidden + c);
-        const float4 a = sp[0], b = sp[1];
-        acc[0] = __fadd_rn(acc[0], a.x); acc[1] = __fadd_rn(acc[1], a.y);
-        acc[2] = __fadd_rn(acc[2], a.z); acc[3] = __fadd_rn(acc[3], a.w);
-        acc[4] = __fadd_rn(acc[4], b.x); acc[5] = __fadd_rn(acc[5], b.y);
-        acc[6] = __fadd_rn(acc[6], b.z); acc[7] = __fadd_rn(acc[7], b.w);
-      }
-      if constexpr (ACT_F32) {
-        float4* dst = reinterpret_cast<float4*>(slot + g.routed_x + ((int64_t)local * hidden + c) * 4);
-        dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-      } else {
-        uint4 o;
-        __nv_bfloat162 p0 = __floats2bfloat162_rn(acc[0], acc[1]);
-        __nv_bfloat162 p1 = __floats2bfloat162_rn(acc[2], acc[3]);
-        __nv_bfloat162 p2 = __floats2bfloat162_rn(acc[4], acc[5]);
-        __nv_bfloat162 p3 = __floats2bfloat162_rn(acc[6], acc[7]);
-        o.x = *reinterpret_cast<uint32_t*>(&p0);
-        o.y = *reinterpret_cast<uint32_t*>(&p1);
-        o.z = *reinterpret_cast<uint32_t*>(&p2);
-        o.w = *reinterpret_cast<uint32_t*>(&p3);
-        *reinterpret_cast<uint4*>(slot + g.routed_x + ((int64_t)local * hidden + c) * 2) = o;
+      if (valid) {  // lanes past hidden write nothing
+        if (has_shared) {
+          const float4* sp = reinterpret_cast<const float4*>(ws.s + (int64_t)t * hidden + c);
+          const float4 a = sp[0], b = sp[1];
+          acc[0] = __fadd_rn(acc[0], a.x); acc[1] = __fadd_rn(acc[1], a.y);
+          acc[2] = __fadd_rn(acc[2], a.z); acc[3] = __fadd_rn(acc[3], a.w);
+          acc[4] = __fadd_rn(acc[4], b.x); acc[5] = __fadd_rn(acc[5], b.y);
+          acc[6] = __fadd_rn(acc[6], b.z); acc[7] = __fadd_rn(acc[7], b.w);
+        }
+        if constexpr (ACT_F32) {
+          float4* dst = reinterpret_cast<float4*>(slot + g.routed_x + ((int64_t)local * hidden + c) * 4);
+          dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+          dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        } else {
+          uint4 o;
+          __nv_bfloat162 p0 = __floats2bfloat162_rn(acc[0], acc[1]);
+          __nv_bfloat162 p1 = __floats2bfloat162_rn(acc[2], acc[3]);
+          __nv_bfloat162 p2 = __floats2bfloat162_rn(acc[4], acc[5]);
+          __nv_bfloat162 p3 = __floats2bfloat162_rn(acc[6], acc[7]);
+          o.x = *reinterpret_cast<uint32_t*>(&p0);
+          o.y = *reinterpret_cast<uint32_t*>(&p1);
+          o.z = *reinterpret_cast<uint32_t*>(&p2);
+          o.w = *reinterpret_cast<uint32_t*>(&p3);
+          *reinterpret_cast<uint4*>(slot + g.routed_x + ((int64_t)local * hidden + c) * 2) = o;
+        }
       }
     }
   }
@@ -780,7 +886,7 @@ __global__ void k_return_header(uint8_t* ret, WinGeom g, FanIn f, DevWS ws, int 
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence_system();
+    __threadfence();
     st_release_u64(reinterpret_cast<uint64_t*>(ret) + f.region[i] * g.ring_depth + f.stage, seq);
   }
 }
@@ -842,11 +948,10 @@ __global__ void k_transpose_wg(const float* Wg, float* WgT, int hidden, int E) {
 
 int router_blocks(int total_tokens) { return (total_tokens + kRtTok - 1) / kRtTok; }
 
-// smallest router footprint for a configuration (bf16 token tile), checked
-// at context creation against the per-CTA shared memory limit
+// shared memory of a logits CTA: 8 token rows
 size_t router_min_smem_bytes(int hidden, int E, int act_f32) {
-  return (size_t)hidden * kRtTok * (act_f32 ? 4 : 2) + (size_t)2 * 64 * 128 * 4 +
-         (size_t)kRtTok * E * 4 + (size_t)E * 4;
+  (void)E;
+  return (size_t)hidden * kLgTok * (act_f32 ? 4 : 2);
 }
 
 namespace {
@@ -892,48 +997,46 @@ cudaError_t launch_header_check(const LaunchCtx& lc, const WinGeom& g, const uin
   return cudaGetLastError();
 }
 
-size_t router_smem_bytes(int hidden, int E, int act_f32, bool xs_f32) {
-  return (size_t)hidden * kRtTok * (xs_f32 ? 4 : 2) + (size_t)2 * kRtEgroup * kRtHc * 4 +
-         (size_t)kRtTok * E * 4 + (size_t)E * 4;
-}
-
-template <bool ACT_F32, typename XS>
-static cudaError_t launch_router_t(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
+template <typename XS>
+static cudaError_t launch_logits_t(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                                    const FanIn& f, const DevWS& ws, int hidden, const float* WgT,
-                                   const float* bias, int E, int k, int renorm, float scale,
-                                   int32_t* hist, size_t smem) {
-  const int grid = router_blocks(f.total);
-  cudaError_t err = cudaFuncSetAttribute(k_router<ACT_F32, XS>,
+                                   const float* bias, int E, float* logits) {
+  const size_t smem = (size_t)hidden * kLgTok * sizeof(XS);
+  cudaError_t err = cudaFuncSetAttribute(k_router_logits<XS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  k_router<ACT_F32, XS><<<grid, kRtWarps * 32, smem, lc.stream>>>(win, g, f, ws, hidden, WgT, bias,
-                                                                  E, k, renorm, scale, hist, grid);
+  dim3 grid((f.total + kLgTok - 1) / kLgTok, (E + kLgEblk - 1) / kLgEblk);
+  k_router_logits<XS><<<grid, kLgWarps * 32, smem, lc.stream>>>(win, g, f, ws, hidden, WgT, bias, E,
+                                                                logits);
   ++*lc.launches;
   return cudaGetLastError();
 }
 
-// the token tile is held as fp32 when it fits next to the weight ring,
-// else as bf16 bits widened on use
 cudaError_t launch_router(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                           const FanIn& f, const DevWS& ws, int hidden, int act_f32,
                           const float* WgT, const float* bias, int E, int k, int renorm,
-                          float scale, int32_t* hist) {
+                          float scale, float* logits, int32_t* hist) {
   if (f.total == 0) return cudaSuccess;
-  const size_t fp32_tile = router_smem_bytes(hidden, E, act_f32, true);
-  if (act_f32)
-    return launch_router_t<true, float>(lc, g, win, f, ws, hidden, WgT, bias, E, k, renorm, scale,
-                                        hist, fp32_tile);
-  if (fp32_tile <= kRouterSmemLimit)
-    return launch_router_t<false, float>(lc, g, win, f, ws, hidden, WgT, bias, E, k, renorm, scale,
-                                         hist, fp32_tile);
-  return launch_router_t<false, uint16_t>(lc, g, win, f, ws, hidden, WgT, bias, E, k, renorm, scale,
-                                          hist, router_smem_bytes(hidden, E, act_f32, false));
+  cudaError_t err = act_f32 ? launch_logits_t<float>(lc, g, win, f, ws, hidden, WgT, bias, E, logits)
+                            : launch_logits_t<uint16_t>(lc, g, win, f, ws, hidden, WgT, bias, E, logits);
+  if (err != cudaSuccess) return err;
+  const int nblocks = router_blocks(f.total);
+  k_router_topk<<<nblocks, kRtTok * 32, 0, lc.stream>>>(f, ws, logits, E, k, renorm, scale, hist,
+                                                        nblocks);
+  ++*lc.launches;
+  return cudaGetLastError();
 }
 
 cudaError_t launch_plan(const LaunchCtx& lc, const FanIn& f, const DevWS& ws, int E, int k,
                         int inter, int shared_inter, int hidden, int has_shared, int bn,
                         GemmPlan* plan1, GemmPlan* plan2, const int32_t* hist, int32_t* base) {
   const int nblocks = router_blocks(f.total);
+  if ((int64_t)f.total * k <= kPlanSmallMax) {
+    k_plan_small<<<1, 1024, 0, lc.stream>>>(f, ws, E, k, inter, shared_inter, hidden, has_shared, bn,
+                                            plan1, plan2);
+    ++*lc.launches;
+    return cudaGetLastError();
+  }
   k_plan_scan<<<1, kScanWarps * 32, 0, lc.stream>>>(f, ws, E, k, inter, shared_inter, hidden,
                                                      has_shared, bn, hist, base, nblocks, plan1,
                                                      plan2);
@@ -967,7 +1070,8 @@ cudaError_t launch_combine(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret, 
                            const DevWS& ws, int hidden, int k, int act_f32, int has_shared,
                            int y_f32) {
   if (f.total == 0) return cudaSuccess;
-  const int grid = grid_for(f.total, kThreads / 32, lc.num_sms * 8);
+  const int64_t items = (int64_t)f.total * ((hidden + 255) / 256);
+  const int grid = grid_for(items, kThreads / 32, lc.num_sms * 8);
   if (act_f32 && y_f32)
     k_combine<true, true><<<grid, kThreads, 0, lc.stream>>>(ret, g, f, ws, hidden, k, has_shared);
   else if (!act_f32 && y_f32)

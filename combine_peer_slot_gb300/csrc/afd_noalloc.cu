@@ -5,9 +5,9 @@
 // fragments that pool), or a plugin that must not trigger the device-wide
 // synchronisation cudaMalloc/cudaFree can cause.  afd_route_noalloc serves
 // them: the caller passes inputs and outputs, and the only scratch the step
-// needs -- the transposed router weight and a status word -- lives in the
-// file-scope device array below, which every GPU that loads this library
-// holds until the process exits.
+// needs -- the transposed router weight, the router logits and a status
+// word -- lives in the file-scope device array below, which every GPU that
+// loads this library holds until the process exits.
 //
 // The array is shared by every call: a call rewrites the transposed weight
 // and clears the status word before the router runs, and calls that overlap
@@ -19,9 +19,10 @@
 
 namespace {
 
-// hidden * num_experts fp32 values of the transposed router weight, then the
-// status word; 256-byte aligned.
-static __device__ __align__(256) float g_noalloc_scratch[AFD_NOALLOC_MAX_ROUTER_WEIGHTS + 64];
+// [transposed router weight: hidden * num_experts fp32]
+// [logits: n_tokens * num_experts fp32][status word]; 256-byte aligned.
+static __device__ __align__(256) float
+    g_noalloc_scratch[AFD_NOALLOC_MAX_ROUTER_WEIGHTS + AFD_NOALLOC_MAX_LOGITS + 64];
 
 constexpr int kMaxDevices = 64;
 float* g_scratch_addr[kMaxDevices] = {};
@@ -59,14 +60,18 @@ extern "C" int afd_route_noalloc(const void* x, int n_tokens, int hidden, int ac
       topk < 1 || topk > 16 || topk > num_experts ||
       (act_dtype != AFD_DTYPE_F32 && act_dtype != AFD_DTYPE_BF16))
     return AFD_ERR_ARG;
-  if ((int64_t)hidden * num_experts > AFD_NOALLOC_MAX_ROUTER_WEIGHTS) return AFD_ERR_CAPACITY;
+  if ((int64_t)hidden * num_experts > AFD_NOALLOC_MAX_ROUTER_WEIGHTS ||
+      (int64_t)n_tokens * num_experts > AFD_NOALLOC_MAX_LOGITS)
+    return AFD_ERR_CAPACITY;
   if (n_tokens == 0) return AFD_OK;
   if (!x || !Wg || !ids || !weights || (reinterpret_cast<uintptr_t>(x) & 15)) return AFD_ERR_ARG;
   float* scratch = nullptr;
   int rc = scratch_for_current_device(&scratch);
   if (rc) return rc;
   float* WgT = scratch;
-  int32_t* status = reinterpret_cast<int32_t*>(scratch + AFD_NOALLOC_MAX_ROUTER_WEIGHTS);
+  float* logits = scratch + AFD_NOALLOC_MAX_ROUTER_WEIGHTS;
+  int32_t* status =
+      reinterpret_cast<int32_t*>(scratch + AFD_NOALLOC_MAX_ROUTER_WEIGHTS + AFD_NOALLOC_MAX_LOGITS);
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(cuda_stream);
   LaunchCtx lc{stream, 0, &g_noalloc_launches};
   int dev = 0;
@@ -95,7 +100,7 @@ extern "C" int afd_route_noalloc(const void* x, int n_tokens, int hidden, int ac
   ws.w = weights;
   if (launch_router(lc, g, static_cast<const uint8_t*>(x), f, ws, hidden,
                     act_dtype == AFD_DTYPE_F32, WgT, bias, num_experts, topk, renorm,
-                    routed_scaling, /*hist=*/nullptr) != cudaSuccess)
+                    routed_scaling, logits, /*hist=*/nullptr) != cudaSuccess)
     return AFD_ERR_CUDA;
   return AFD_OK;
 }

@@ -283,12 +283,17 @@ int64_t afd_launch_count(afd_ctx* ctx);
  *   0 header check, 1 router, 2 plan, 3 gather, 4 SwiGLU GEMM (routed +
  *   shared), 5 down GEMM (routed + shared), 6 combine + split, 7 return
  *   headers and flags.
- * afd_stage_times waits for the last forward's events and writes the
- * elapsed milliseconds of the first n (<= AFD_NUM_STAGES) stages into ms
- * (host array).  Events cost no device work; timing is off by default. */
+ * The events of up to 64 forwards are kept; a forward that would overwrite
+ * unread ones first waits for the oldest and folds it into a running sum.
+ * afd_stage_times waits for every recorded forward, writes the summed
+ * elapsed milliseconds of the first n (<= AFD_NUM_STAGES) stages over the
+ * forwards since the previous call into ms (host array), their number into
+ * *forwards (host, may be NULL), and clears the sum.  A forward that fails
+ * part-way contributes nothing.  Events cost no device work; timing is off
+ * by default. */
 #define AFD_NUM_STAGES 8
 int afd_profile(afd_ctx* ctx, int enable);
-int afd_stage_times(afd_ctx* ctx, float* ms, int n);
+int afd_stage_times(afd_ctx* ctx, float* ms, int n, int64_t* forwards);
 
 /* Router without device allocation.  The pages have no counterpart: this
  * entry point exists for callers that cannot call cudaMalloc -- a serving
@@ -302,16 +307,20 @@ int afd_stage_times(afd_ctx* ctx, float* ms, int n);
  *   ids      device int32 [n_tokens, topk] out; weights device fp32
  *            [n_tokens, topk] out
  *   cuda_stream  cudaStream_t the work is ordered on (NULL = legacy stream)
- * Its scratch (the transposed router weight and a status word) is a
- * file-scope device array of AFD_NOALLOC_MAX_ROUTER_WEIGHTS + 64 floats
- * (about 1 MiB) that every GPU loading this library holds until exit; the
+ * Its scratch (the transposed router weight, the router logits and a
+ * status word) is a file-scope device array of
+ * AFD_NOALLOC_MAX_ROUTER_WEIGHTS + AFD_NOALLOC_MAX_LOGITS + 64 floats
+ * (about 5 MiB) that every GPU loading this library holds until exit; the
  * first call on a device looks up that array's device address, so make the
  * first call on each device before any stream capture.  All calls share
  * the array: each call rewrites it and clears the status word first, and
  * calls that overlap on the GPU race on it.  hidden * num_experts above
- * the maximum returns AFD_ERR_CAPACITY; bad arguments AFD_ERR_ARG; a
- * failing CUDA call AFD_ERR_CUDA.  Asynchronous; allocates nothing. */
+ * AFD_NOALLOC_MAX_ROUTER_WEIGHTS or n_tokens * num_experts above
+ * AFD_NOALLOC_MAX_LOGITS returns AFD_ERR_CAPACITY; bad arguments
+ * AFD_ERR_ARG; a failing CUDA call AFD_ERR_CUDA.  Asynchronous; allocates
+ * nothing. */
 #define AFD_NOALLOC_MAX_ROUTER_WEIGHTS 262144
+#define AFD_NOALLOC_MAX_LOGITS 1048576
 int afd_route_noalloc(const void* x, int n_tokens, int hidden, int act_dtype, const float* Wg,
                       const float* bias, int num_experts, int topk, int renorm,
                       float routed_scaling, int32_t* ids, float* weights, void* cuda_stream);

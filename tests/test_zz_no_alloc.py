@@ -63,3 +63,7 @@ def test_noalloc_router_rejects_oversize():
     rc = A.afd_route_noalloc(dummy.data_ptr(), 4, too_wide, A.AFD_DTYPE_BF16, dummy.data_ptr(),
                              0, 64, 6, 0, 1.0, dummy.data_ptr(), dummy.data_ptr(), 0)
     assert rc == A.AFD_ERR_CAPACITY
+    too_many = A.AFD_NOALLOC_MAX_LOGITS // 64 + 1
+    rc = A.afd_route_noalloc(dummy.data_ptr(), too_many, 2048, A.AFD_DTYPE_BF16, dummy.data_ptr(),
+                             0, 64, 6, 0, 1.0, dummy.data_ptr(), dummy.data_ptr(), 0)
+    assert rc == A.AFD_ERR_CAPACITY

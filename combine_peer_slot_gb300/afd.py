@@ -16,6 +16,7 @@ AFD_OK = 0
  AFD_ERR_CUDA, AFD_ERR_UNSUPPORTED) = range(1, 14)
 AFD_DTYPE_F32, AFD_DTYPE_BF16 = 0, 1
 AFD_GEMM_TENSOR, AFD_GEMM_SIMT, AFD_GEMM_TENSOR_1CTA = 0, 1, 2
+AFD_CFG_NO_PDL = 1
 AFD_DIR_DISPATCH, AFD_DIR_RETURN = 0, 1
 (AFD_WS_IDS, AFD_WS_WEIGHTS, AFD_WS_COUNTS, AFD_WS_OFFSETS, AFD_WS_PERM, AFD_WS_INV, AFD_WS_XP,
  AFD_WS_H, AFD_WS_Y, AFD_WS_HS, AFD_WS_S, AFD_WS_STATUS) = range(12)
@@ -30,7 +31,7 @@ class afd_config(C.Structure):
                 ("max_total_tokens", C.c_int32), ("hidden", C.c_int32),
                 ("num_experts", C.c_int32), ("topk", C.c_int32), ("inter", C.c_int32),
                 ("shared_inter", C.c_int32), ("act_dtype", C.c_int32), ("renorm", C.c_int32),
-                ("max_layers", C.c_int32), ("gemm", C.c_int32), ("reserved", C.c_int32),
+                ("max_layers", C.c_int32), ("gemm", C.c_int32), ("flags", C.c_int32),
                 ("routed_scaling", C.c_float), ("routed_cap_multiplier", C.c_float),
                 ("wait_timeout_ns", C.c_int64)]
 
@@ -121,11 +122,11 @@ def _ints(seq):
 def make_config(num_peers, token_cap, hidden, num_experts, topk, inter, shared_inter=0,
                 act="bf16", renorm=False, routed_scaling=1.0, ring_depth=1,
                 max_total_tokens=0, max_layers=1, gemm=AFD_GEMM_TENSOR,
-                routed_cap_multiplier=2.0, wait_timeout_ns=0):
+                routed_cap_multiplier=2.0, wait_timeout_ns=0, flags=0):
     return afd_config(num_peers, ring_depth, token_cap, max_total_tokens, hidden, num_experts,
                       topk, inter, shared_inter,
                       AFD_DTYPE_BF16 if act == "bf16" else AFD_DTYPE_F32, int(bool(renorm)),
-                      max_layers, gemm, 0, float(routed_scaling),
+                      max_layers, gemm, int(flags), float(routed_scaling),
                       float(routed_cap_multiplier), int(wait_timeout_ns))
 
 

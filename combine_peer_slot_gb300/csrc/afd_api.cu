@@ -130,6 +130,7 @@ int validate_config(const afd_config* c) {
       c->max_layers < 1 || c->routed_cap_multiplier < 1.0f || c->wait_timeout_ns < 0)
     return AFD_ERR_ARG;
   if (c->act_dtype != AFD_DTYPE_F32 && c->act_dtype != AFD_DTYPE_BF16) return AFD_ERR_ARG;
+  if (c->flags & ~AFD_CFG_NO_PDL) return AFD_ERR_ARG;
   if (c->gemm != AFD_GEMM_TENSOR && c->gemm != AFD_GEMM_SIMT && c->gemm != AFD_GEMM_TENSOR_1CTA)
     return AFD_ERR_ARG;
   const bool tensor = c->gemm != AFD_GEMM_SIMT;
@@ -211,7 +212,7 @@ struct afd_ctx {
     }
   }
 
-  LaunchCtx lc() { return LaunchCtx{stream, num_sms, &launches}; }
+  LaunchCtx lc() { return LaunchCtx{stream, num_sms, &launches, (cfg.flags & AFD_CFG_NO_PDL) ? 0 : 1}; }
   int64_t timeout() const { return cfg.wait_timeout_ns ? cfg.wait_timeout_ns : 1000000000ll; }
 };
 
@@ -496,7 +497,11 @@ int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, con
   const int has_shared = c.shared_inter > 0;
   const int ab = ctx->act_f32 ? 4 : 2;
   const int row_bytes = c.hidden * ab;
-  const int bn = 256;
+  // token tile of the grouped GEMMs: 256 rows, or 64 on the SM-pair engine
+  // when the experts average <= 48 rows (decode-sized fan-ins), which then
+  // runs its deeper narrow ring
+  const int bn =
+      c.gemm == AFD_GEMM_TENSOR && T * c.topk <= 48 * (int64_t)c.num_experts ? 64 : 256;
   LaunchCtx lc = ctx->lc();
   const DevWS& ws = ctx->ws;
   ctx->mark(0);
@@ -541,6 +546,7 @@ int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, con
       a1.plan = ctx->plan1;
       a1.status = ws.status;
       a1.swiglu = 1;
+      a1.bn = bn;
       a1.timeout_ns = ctx->timeout();
       rc = cuda_fail(launch(lc, a1), "gemm1");
       if (rc) return rc;
@@ -564,6 +570,7 @@ int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, con
       a2.plan = ctx->plan2;
       a2.status = ws.status;
       a2.swiglu = 0;
+      a2.bn = bn;
       a2.timeout_ns = ctx->timeout();
       rc = cuda_fail(launch(lc, a2), "gemm2");
       if (rc) return rc;

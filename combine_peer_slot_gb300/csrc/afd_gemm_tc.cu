@@ -139,6 +139,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_gemm_tc(const __grid_constan
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const GemmPlan& plan = *args.plan;  // tile table, built by the plan kernel
+  grid_dep_wait();
+  grid_dep_launch();
   if (threadIdx.x == 0) tail->skip = read_status(args.status);
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; s++) {
@@ -368,9 +370,7 @@ cudaError_t launch_gemm_tc(const LaunchCtx& lc, const GemmArgs& a) {
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  k_gemm_tc<<<lc.num_sms, NUM_THREADS, kSmemBytes, lc.stream>>>(a);
-  ++*lc.launches;
-  return cudaGetLastError();
+  return launch_k(lc, k_gemm_tc, lc.num_sms, NUM_THREADS, kSmemBytes, a);
 }
 
 size_t gemm_tc_smem_bytes() { return kSmemBytes; }

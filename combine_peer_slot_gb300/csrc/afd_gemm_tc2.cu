@@ -28,13 +28,9 @@ namespace {
 
 constexpr int BM = 128;            // weight rows per CTA
 constexpr int BK = 64;
-constexpr int BN_HALF = 128;       // token rows per CTA (256 per unit)
-constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN_HALF * BK * 2;  // one [128 tokens][64 k] box
 constexpr int SMALL_BOX_ROWS = 32;
 constexpr int SMALL_BOX_BYTES = SMALL_BOX_ROWS * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + EPI_WARPS * 32;
 constexpr int TMEM_COLS = 512;     // two accumulators of 256 columns
@@ -43,22 +39,36 @@ constexpr int EPI_PITCH_BF16 = 80;
 constexpr int EPI_BUF_BYTES = 32 * EPI_PITCH_BF16;
 constexpr uint64_t kGemmTimeoutNs = 5000000000ull;
 
-struct SmemTail {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
-  uint64_t drain;
-  uint32_t tmem_base;
-  int abort_flag;
-  int skip;
+// Ring geometry of the two variants.  Wide: token tiles of up to 256 rows
+// (128 per CTA), 6 stages of one 64-wide k-block (16 KB weights + 16 KB
+// tokens).  Narrow, for token tiles of <= 64 rows (decode-sized fan-ins,
+// where the weights stream from HBM and the tensor pipe idles): 32-row token
+// boxes and two adjacent k-blocks per stage (2 x 16 KB weights + 2 x 4 KB
+// tokens, 5 stages), so every weight row is fetched 256 contiguous bytes at
+// a time, which HBM serves measurably faster than 128-byte pieces.
+template <bool kNarrow>
+struct Ring {
+  static constexpr int BN_HALF = kNarrow ? 32 : 128;   // token rows per CTA
+  static constexpr int KPS = kNarrow ? 2 : 1;          // k-blocks per stage
+  static constexpr int STAGES = kNarrow ? 5 : 6;
+  static constexpr int B_BYTES = BN_HALF * BK * 2;
+  static constexpr int STAGE_BYTES = KPS * (A_BYTES + B_BYTES);
+  struct Tail {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    int skip;
+  };
+  static constexpr size_t kEpiOffset = ((size_t)STAGES * STAGE_BYTES + sizeof(Tail) + 127) / 128 * 128;
+  static constexpr size_t kSmemBytes = 1024 + kEpiOffset + (size_t)EPI_WARPS * EPI_BUF_BYTES;
+  static_assert(kEpiOffset % 128 == 0 && EPI_BUF_BYTES % 128 == 0, "epilogue buffers must stay aligned");
+  static_assert(kSmemBytes <= 232448, "over the per-CTA shared memory limit");
+  static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
 };
-
-constexpr size_t kEpiOffset = ((size_t)STAGES * STAGE_BYTES + sizeof(SmemTail) + 127) / 128 * 128;
-constexpr size_t kSmemBytes = 1024 + kEpiOffset + (size_t)EPI_WARPS * EPI_BUF_BYTES;
-static_assert(kEpiOffset % 128 == 0 && EPI_BUF_BYTES % 128 == 0, "epilogue buffers must stay aligned");
-static_assert(kSmemBytes <= 232448, "over the per-CTA shared memory limit");
-static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -185,11 +195,15 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
+template <bool kNarrow>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 k_gemm_tc2(const __grid_constant__ GemmArgs args) {
+  using R = Ring<kNarrow>;
+  constexpr int STAGES = R::STAGES;
+  constexpr int STAGE_BYTES = R::STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  SmemTail* tail = reinterpret_cast<SmemTail*>(smem + (size_t)STAGES * STAGE_BYTES);
+  typename R::Tail* tail = reinterpret_cast<typename R::Tail*>(smem + (size_t)STAGES * STAGE_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
   const int cid = (int)cluster_id_x();
@@ -197,7 +211,6 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
   const GemmPlan& plan = *args.plan;
 
   if (threadIdx.x == 0) {
-    tail->skip = read_status(args.status);
     for (int s = 0; s < STAGES; s++) {
       mbar_init(smem_u32(&tail->full[s]), 1);
       mbar_init(smem_u32(&tail->empty[s]), 1);
@@ -209,6 +222,17 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
     mbar_init(smem_u32(&tail->drain), 1);
     tail->abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // everything above touches only this CTA's shared memory
+  grid_dep_wait();
+  grid_dep_launch();
+  if (threadIdx.x == 0) {
+    int skip = read_status(args.status);
+    if (kNarrow && plan.bn > 2 * R::BN_HALF && !skip) {  // the ring has no room for wider tiles
+      set_error(args.status, AFD_ERR_ARG);
+      skip = 1;
+    }
+    tail->skip = skip;
   }
   __syncthreads();
   const int total = plan.total_units;
@@ -244,23 +268,27 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
         // but not used by the MMA, past the buffer they are zero-filled
         const int half = t.n_mma / 2;
         const int brow = G.b_row0 + t.nt * plan.bn + (int)rank * half;
-        const bool small_box = half <= SMALL_BOX_ROWS;
-        const uint32_t b_bytes = small_box ? SMALL_BOX_BYTES : B_BYTES;
+        const bool small_box = kNarrow || half <= SMALL_BOX_ROWS;
+        const uint32_t b_bytes = small_box ? SMALL_BOX_BYTES : R::B_BYTES;
         const int mt = 2 * t.mpair + (int)rank;
         const CUtensorMap* ta = &args.tmA[t.kind];
         const CUtensorMap* tb = small_box ? &args.tmBs[t.kind] : &args.tmB[t.kind];
         bool ok = true;
-        for (int kb = 0; kb < nkb; kb++) {
+        for (int kb = 0; kb < nkb; kb += R::KPS) {
+          const int cnt = min(R::KPS, nkb - kb);
           if (!wait_bar(smem_u32(&tail->empty[s]), ph ^ 1, abort_flag, deadline, args.status)) { ok = false; break; }
           const uint32_t full_leader = map_to_rank(smem_u32(&tail->full[s]), 0);
-          if (rank == 0) mbar_expect_tx(smem_u32(&tail->full[s]), 2 * (A_BYTES + b_bytes));
+          if (rank == 0) mbar_expect_tx(smem_u32(&tail->full[s]), 2 * cnt * (A_BYTES + b_bytes));
           const uint32_t sa = smem_base + s * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
-          if (args.swiglu)
-            tma2_load_5d(sa, ta, kb * BK, 0, 0, mt * 4, G.a_idx, full_leader);
-          else
-            tma2_load_3d(sa, ta, kb * BK, mt * BM, G.a_idx, full_leader);
-          tma2_load_2d(sb, tb, kb * BK, brow, full_leader);
+          const uint32_t sb = sa + R::KPS * A_BYTES;
+          for (int j = 0; j < cnt; j++) {
+            const int kc = (kb + j) * BK;
+            if (args.swiglu)
+              tma2_load_5d(sa + j * A_BYTES, ta, kc, 0, 0, mt * 4, G.a_idx, full_leader);
+            else
+              tma2_load_3d(sa + j * A_BYTES, ta, kc, mt * BM, G.a_idx, full_leader);
+            tma2_load_2d(sb + j * R::B_BYTES, tb, kc, brow, full_leader);
+          }
           if (++s == STAGES) { s = 0; ph ^= 1; }
         }
         if (!ok) break;
@@ -281,16 +309,19 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
         if (!wait_bar(smem_u32(&tail->tempty[acc]), acc_ph ^ 1, abort_flag, deadline, args.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
-        for (int kb = 0; kb < nkb; kb++) {
+        for (int kb = 0; kb < nkb; kb += R::KPS) {
+          const int cnt = min(R::KPS, nkb - kb);
           if (!wait_bar(smem_u32(&tail->full[s]), ph, abort_flag, deadline, args.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_base + s * STAGE_BYTES;
-          const uint64_t adesc = sdesc_sw128(sa);
-          const uint64_t bdesc = sdesc_sw128(sa + A_BYTES);
+          for (int j = 0; j < cnt; j++) {
+            const uint64_t adesc = sdesc_sw128(sa + j * A_BYTES);
+            const uint64_t bdesc = sdesc_sw128(sa + R::KPS * A_BYTES + j * R::B_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; kk++)
-            tc2_mma_f16(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
-                        (kb | kk) != 0);
+            for (int kk = 0; kk < BK / 16; kk++)
+              tc2_mma_f16(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
+                          ((kb + j) | kk) != 0);
+          }
           tc2_commit_pair(smem_u32(&tail->empty[s]));
           if (++s == STAGES) { s = 0; ph ^= 1; }
         }
@@ -307,7 +338,7 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
     // ------------------------------ epilogue (warps 2..9, both CTAs)
     const int q = warp & 3;
     const int half_cols = (warp - 2) >> 2;
-    uint8_t* ebuf = smem + kEpiOffset + (size_t)(warp - 2) * EPI_BUF_BYTES;
+    uint8_t* ebuf = smem + R::kEpiOffset + (size_t)(warp - 2) * EPI_BUF_BYTES;
     const bool lo = lane < 16;
     const uint32_t tempty_leader[2] = {map_to_rank(smem_u32(&tail->tempty[0]), 0),
                                        map_to_rank(smem_u32(&tail->tempty[1]), 0)};
@@ -408,18 +439,22 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
   }
 }
 
-}  // namespace
-
-cudaError_t launch_gemm_tc2(const LaunchCtx& lc, const GemmArgs& a) {
+template <bool kNarrow>
+cudaError_t launch_variant(const LaunchCtx& lc, const GemmArgs& a) {
+  constexpr size_t smem = Ring<kNarrow>::kSmemBytes;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc2, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc2<kNarrow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   const int grid = (lc.num_sms / 2) * 2;  // whole pairs; persistent over the unit table
-  k_gemm_tc2<<<grid, NUM_THREADS, kSmemBytes, lc.stream>>>(a);
-  ++*lc.launches;
-  return cudaGetLastError();
+  return launch_k(lc, k_gemm_tc2<kNarrow>, grid, NUM_THREADS, smem, a);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc2(const LaunchCtx& lc, const GemmArgs& a) {
+  return a.bn <= 2 * Ring<true>::BN_HALF ? launch_variant<true>(lc, a) : launch_variant<false>(lc, a);
 }

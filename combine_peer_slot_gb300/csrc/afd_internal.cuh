@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <utility>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -93,7 +94,7 @@ struct GemmArgs {
   const GemmPlan* plan;
   int32_t* status;
   int swiglu;             // 1: gate/up interleaved SwiGLU epilogue
-  int pad;
+  int bn;                 // the plan's token tile (rows per unit)
   int64_t timeout_ns;
 };
 
@@ -227,6 +228,15 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Programmatic dependent launch.  Every kernel calls grid_dep_wait() before
+// it reads anything an earlier kernel of the stream wrote (a no-op when it
+// was launched without the programmatic attribute), then grid_dep_launch()
+// so the next kernel's CTAs may be scheduled and run their prologue.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 #endif  // __CUDACC__
 
 // ---------------------------------------------------------------------------
@@ -236,7 +246,29 @@ struct LaunchCtx {
   cudaStream_t stream;
   int num_sms;
   int64_t* launches;
+  int pdl = 0;  // 1: a launch may start while the previous kernel drains
 };
+
+#ifdef __CUDACC__
+// Launch with the programmatic-serialisation attribute when lc.pdl is set;
+// counts the launch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(const LaunchCtx& lc, void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                     size_t smem, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = lc.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = lc.pdl ? 1 : 0;
+  ++*lc.launches;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+#endif
 
 cudaError_t launch_pack_payload(const LaunchCtx& lc, const WinGeom& g, uint8_t* win, int region,
                                 int stage, const void* x, int n, int row_bytes, int with_shared,

@@ -38,6 +38,8 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
 __global__ void k_pack_payload(uint8_t* win, WinGeom g, int region, int stage,
                                const uint4* __restrict__ x, int n, int row_bytes,
                                int with_shared) {
+  grid_dep_wait();
+  grid_dep_launch();
   uint8_t* slot = slot_ptr(win, g, region, stage);
   uint4* rx = reinterpret_cast<uint4*>(slot + g.routed_x);
   uint4* sx = reinterpret_cast<uint4*>(slot + g.shared_x);
@@ -56,6 +58,8 @@ __global__ void k_pack_payload(uint8_t* win, WinGeom g, int region, int stage,
 
 __global__ void k_pack_header(uint8_t* win, WinGeom g, int region, int stage, int layer, int n,
                               int with_shared, int num_experts, uint64_t seq, int shutdown) {
+  grid_dep_wait();
+  grid_dep_launch();
   uint8_t* slot = slot_ptr(win, g, region, stage);
   int32_t* h = reinterpret_cast<int32_t*>(slot + g.header);
   for (int i = threadIdx.x; i < AFD_HEADER_FIXED_WORDS + num_experts; i += blockDim.x) {
@@ -92,6 +96,8 @@ __global__ void k_pack_header(uint8_t* win, WinGeom g, int region, int stage, in
 // ---------------------------------------------------------------------------
 __global__ void k_header_check(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int E,
                                int token_cap, int has_shared_expert, int64_t timeout_ns) {
+  grid_dep_wait();
+  grid_dep_launch();
   __shared__ int err[AFD_MAX_PEERS];
   __shared__ int bad_sidx[AFD_MAX_PEERS];
   __shared__ int shared_n[AFD_MAX_PEERS];
@@ -282,6 +288,8 @@ __global__ void __launch_bounds__(kLgWarps * 32)
 k_router_logits(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int hidden,
                 const float* __restrict__ WgT, const float* __restrict__ bias, int E,
                 float* __restrict__ logits) {
+  grid_dep_wait();
+  grid_dep_launch();
   extern __shared__ __align__(16) uint8_t lg_smem[];
   XS* xT = reinterpret_cast<XS*>(lg_smem);       // [hidden][8 tokens]
   if (read_status(ws.status)) return;
@@ -392,6 +400,8 @@ k_router_logits(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int hidden,
 __global__ void __launch_bounds__(kRtTok * 32)
 k_router_topk(FanIn f, DevWS ws, const float* __restrict__ logits, int E, int k, int renorm,
               float scale, int32_t* __restrict__ hist, int nblocks) {
+  grid_dep_wait();
+  grid_dep_launch();
   __shared__ int hs[256];
   if (read_status(ws.status)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -509,6 +519,8 @@ __global__ void __launch_bounds__(kScanWarps * 32)
 k_plan_scan(FanIn f, DevWS ws, int E, int k, int inter, int shared_inter, int hidden,
             int has_shared, int bn, const int32_t* __restrict__ hist, int32_t* __restrict__ base,
             int nblocks, GemmPlan* plan1, GemmPlan* plan2) {
+  grid_dep_wait();
+  grid_dep_launch();
   __shared__ int cnt[256];
   __shared__ int offs[257];
   __shared__ int skip;
@@ -561,6 +573,8 @@ constexpr int kPlanSmallMax = 8192;
 __global__ void __launch_bounds__(1024)
 k_plan_small(FanIn f, DevWS ws, int E, int k, int inter, int shared_inter, int hidden,
              int has_shared, int bn, GemmPlan* plan1, GemmPlan* plan2) {
+  grid_dep_wait();
+  grid_dep_launch();
   __shared__ int hist_w[32][256];
   __shared__ int cnt[256];
   __shared__ int offs[257];
@@ -642,6 +656,8 @@ constexpr int kRankWarps = 8;
 
 __global__ void __launch_bounds__(kRankWarps * 32)
 k_rank(FanIn f, DevWS ws, int E, int k, const int32_t* __restrict__ base, int nblocks) {
+  grid_dep_wait();
+  grid_dep_launch();
   __shared__ int run_s[kRankWarps][256];
   if (read_status(ws.status)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -684,6 +700,8 @@ k_rank(FanIn f, DevWS ws, int E, int k, const int32_t* __restrict__ base, int nb
 __global__ void __launch_bounds__(kThreads)
 k_gather(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int k, int row_bytes,
          int has_shared) {
+  grid_dep_wait();
+  grid_dep_launch();
   if (read_status(ws.status)) return;
   const int N = f.total * k;
   const int rows = N + (has_shared ? f.total : 0);
@@ -724,6 +742,8 @@ __device__ __forceinline__ float ld_act(const void* p, int64_t i, int act_f32) {
 }
 
 __global__ void __launch_bounds__(kThreads) k_gemm_simt(SimtArgs a) {
+  grid_dep_wait();
+  grid_dep_launch();
   if (read_status(a.status)) return;
   const GemmPlan* plan = a.plan;
   const int gi = blockIdx.y;
@@ -771,6 +791,8 @@ __global__ void __launch_bounds__(kThreads) k_gemm_simt(SimtArgs a) {
 template <bool ACT_F32, bool Y_F32>
 __global__ void __launch_bounds__(kThreads)
 k_combine(uint8_t* ret, WinGeom g, FanIn f, DevWS ws, int hidden, int k, int has_shared) {
+  grid_dep_wait();
+  grid_dep_launch();
   if (read_status(ws.status)) return;
   // 8 features per lane step: 16-byte loads of bf16 y (two of fp32 y)
   constexpr int kVec = 8;
@@ -859,6 +881,8 @@ k_combine(uint8_t* ret, WinGeom g, FanIn f, DevWS ws, int hidden, int k, int has
 
 // return headers, then the return flags (release) = the dispatch seq
 __global__ void k_return_header(uint8_t* ret, WinGeom g, FanIn f, DevWS ws, int E, int k) {
+  grid_dep_wait();
+  grid_dep_launch();
   if (read_status(ws.status)) return;
   const int i = blockIdx.x;
   if (i >= f.n_peers) return;
@@ -896,6 +920,8 @@ __global__ void k_return_header(uint8_t* ret, WinGeom g, FanIn f, DevWS ws, int 
 __global__ void __launch_bounds__(kThreads)
 k_unpack(const uint8_t* ret, WinGeom g, int region, int stage, uint4* out, int n, int row_bytes,
          int E, uint64_t expect_seq, int32_t* status, int64_t timeout_ns) {
+  grid_dep_wait();
+  grid_dep_launch();
   __shared__ int ok;
   if (threadIdx.x == 0) {
     int e = read_status(status) ? -1 : 0;
@@ -936,6 +962,8 @@ k_unpack(const uint8_t* ret, WinGeom g, int region, int stage, uint4* out, int n
 }
 
 __global__ void k_transpose_wg(const float* Wg, float* WgT, int hidden, int E) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int64_t n = (int64_t)hidden * E;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -973,28 +1001,23 @@ cudaError_t launch_pack_payload(const LaunchCtx& lc, const WinGeom& g, uint8_t* 
                                 const int32_t*) {
   if (n == 0) return cudaSuccess;
   const int64_t nvec = (int64_t)n * row_bytes / 16;
-  k_pack_payload<<<grid_for(nvec, kThreads * 4, lc.num_sms * 8), kThreads, 0, lc.stream>>>(
-      win, g, region, stage, reinterpret_cast<const uint4*>(x), n, row_bytes, with_shared);
-  ++*lc.launches;
-  return cudaGetLastError();
+  return launch_k(lc, k_pack_payload, grid_for(nvec, kThreads * 4, lc.num_sms * 8), kThreads, 0,
+                  win, g, region, stage, reinterpret_cast<const uint4*>(x), n, row_bytes,
+                  with_shared);
 }
 
 cudaError_t launch_pack_header(const LaunchCtx& lc, const WinGeom& g, uint8_t* win, int region,
                                int stage, int layer, int n, int with_shared, int num_experts,
                                uint64_t seq, int shutdown) {
-  k_pack_header<<<1, 128, 0, lc.stream>>>(win, g, region, stage, layer, n, with_shared,
-                                          num_experts, seq, shutdown);
-  ++*lc.launches;
-  return cudaGetLastError();
+  return launch_k(lc, k_pack_header, 1, 128, 0, win, g, region, stage, layer, n, with_shared,
+                  num_experts, seq, shutdown);
 }
 
 cudaError_t launch_header_check(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                                 const FanIn& f, const DevWS& ws, int num_experts, int token_cap,
                                 int has_shared_expert, int64_t timeout_ns) {
-  k_header_check<<<1, 1024, 0, lc.stream>>>(win, g, f, ws, num_experts, token_cap,
-                                            has_shared_expert, timeout_ns);
-  ++*lc.launches;
-  return cudaGetLastError();
+  return launch_k(lc, k_header_check, 1, 1024, 0, win, g, f, ws, num_experts, token_cap,
+                  has_shared_expert, timeout_ns);
 }
 
 template <typename XS>
@@ -1006,10 +1029,8 @@ static cudaError_t launch_logits_t(const LaunchCtx& lc, const WinGeom& g, const 
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   dim3 grid((f.total + kLgTok - 1) / kLgTok, (E + kLgEblk - 1) / kLgEblk);
-  k_router_logits<XS><<<grid, kLgWarps * 32, smem, lc.stream>>>(win, g, f, ws, hidden, WgT, bias, E,
-                                                                logits);
-  ++*lc.launches;
-  return cudaGetLastError();
+  return launch_k(lc, k_router_logits<XS>, grid, kLgWarps * 32, smem, win, g, f, ws, hidden, WgT,
+                  bias, E, logits);
 }
 
 cudaError_t launch_router(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
@@ -1021,10 +1042,8 @@ cudaError_t launch_router(const LaunchCtx& lc, const WinGeom& g, const uint8_t* 
                             : launch_logits_t<uint16_t>(lc, g, win, f, ws, hidden, WgT, bias, E, logits);
   if (err != cudaSuccess) return err;
   const int nblocks = router_blocks(f.total);
-  k_router_topk<<<nblocks, kRtTok * 32, 0, lc.stream>>>(f, ws, logits, E, k, renorm, scale, hist,
-                                                        nblocks);
-  ++*lc.launches;
-  return cudaGetLastError();
+  return launch_k(lc, k_router_topk, nblocks, kRtTok * 32, 0, f, ws, logits, E, k, renorm, scale,
+                  hist, nblocks);
 }
 
 cudaError_t launch_plan(const LaunchCtx& lc, const FanIn& f, const DevWS& ws, int E, int k,
@@ -1032,38 +1051,28 @@ cudaError_t launch_plan(const LaunchCtx& lc, const FanIn& f, const DevWS& ws, in
                         GemmPlan* plan1, GemmPlan* plan2, const int32_t* hist, int32_t* base) {
   const int nblocks = router_blocks(f.total);
   if ((int64_t)f.total * k <= kPlanSmallMax) {
-    k_plan_small<<<1, 1024, 0, lc.stream>>>(f, ws, E, k, inter, shared_inter, hidden, has_shared, bn,
-                                            plan1, plan2);
-    ++*lc.launches;
-    return cudaGetLastError();
+    return launch_k(lc, k_plan_small, 1, 1024, 0, f, ws, E, k, inter, shared_inter, hidden,
+                    has_shared, bn, plan1, plan2);
   }
-  k_plan_scan<<<1, kScanWarps * 32, 0, lc.stream>>>(f, ws, E, k, inter, shared_inter, hidden,
-                                                     has_shared, bn, hist, base, nblocks, plan1,
-                                                     plan2);
-  ++*lc.launches;
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_k(lc, k_plan_scan, 1, kScanWarps * 32, 0, f, ws, E, k, inter,
+                             shared_inter, hidden, has_shared, bn, hist, base, nblocks, plan1,
+                             plan2);
   if (err != cudaSuccess || nblocks == 0) return err;
-  k_rank<<<(nblocks + kRankWarps - 1) / kRankWarps, kRankWarps * 32, 0, lc.stream>>>(f, ws, E, k,
-                                                                                    base, nblocks);
-  ++*lc.launches;
-  return cudaGetLastError();
+  return launch_k(lc, k_rank, (nblocks + kRankWarps - 1) / kRankWarps, kRankWarps * 32, 0, f, ws,
+                  E, k, (const int32_t*)base, nblocks);
 }
 
 cudaError_t launch_gather(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                           const FanIn& f, const DevWS& ws, int k, int row_bytes, int has_shared) {
   const int64_t rows = (int64_t)f.total * k + (has_shared ? f.total : 0);
   if (rows == 0) return cudaSuccess;
-  k_gather<<<grid_for(rows, kThreads / 32, lc.num_sms * 8), kThreads, 0, lc.stream>>>(
-      win, g, f, ws, k, row_bytes, has_shared);
-  ++*lc.launches;
-  return cudaGetLastError();
+  return launch_k(lc, k_gather, grid_for(rows, kThreads / 32, lc.num_sms * 8), kThreads, 0, win, g,
+                  f, ws, k, row_bytes, has_shared);
 }
 
 cudaError_t launch_gemm_simt(const LaunchCtx& lc, const SimtArgs& a, int max_groups) {
   dim3 grid(lc.num_sms * 2, max_groups);
-  k_gemm_simt<<<grid, kThreads, 0, lc.stream>>>(a);
-  ++*lc.launches;
-  return cudaGetLastError();
+  return launch_k(lc, k_gemm_simt, grid, kThreads, 0, a);
 }
 
 cudaError_t launch_combine(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret, const FanIn& f,
@@ -1073,39 +1082,31 @@ cudaError_t launch_combine(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret, 
   const int64_t items = (int64_t)f.total * ((hidden + 255) / 256);
   const int grid = grid_for(items, kThreads / 32, lc.num_sms * 8);
   if (act_f32 && y_f32)
-    k_combine<true, true><<<grid, kThreads, 0, lc.stream>>>(ret, g, f, ws, hidden, k, has_shared);
-  else if (!act_f32 && y_f32)
-    k_combine<false, true><<<grid, kThreads, 0, lc.stream>>>(ret, g, f, ws, hidden, k, has_shared);
-  else if (!act_f32 && !y_f32)
-    k_combine<false, false><<<grid, kThreads, 0, lc.stream>>>(ret, g, f, ws, hidden, k, has_shared);
-  else
-    return cudaErrorInvalidValue;
-  ++*lc.launches;
-  return cudaGetLastError();
+    return launch_k(lc, k_combine<true, true>, grid, kThreads, 0, ret, g, f, ws, hidden, k, has_shared);
+  if (!act_f32 && y_f32)
+    return launch_k(lc, k_combine<false, true>, grid, kThreads, 0, ret, g, f, ws, hidden, k, has_shared);
+  if (!act_f32 && !y_f32)
+    return launch_k(lc, k_combine<false, false>, grid, kThreads, 0, ret, g, f, ws, hidden, k,
+                    has_shared);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_return_header(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret,
                                  const uint8_t*, const FanIn& f, const DevWS& ws, int E, int k) {
-  k_return_header<<<f.n_peers, 128, 0, lc.stream>>>(ret, g, f, ws, E, k);
-  ++*lc.launches;
-  return cudaGetLastError();
+  return launch_k(lc, k_return_header, f.n_peers, 128, 0, ret, g, f, ws, E, k);
 }
 
 cudaError_t launch_unpack(const LaunchCtx& lc, const WinGeom& g, const uint8_t* ret, int region,
                           int stage, void* out, int n, int row_bytes, int num_experts,
                           uint64_t expect_seq, int32_t* status, int64_t timeout_ns) {
   const int64_t nvec = (int64_t)n * row_bytes / 16;
-  k_unpack<<<grid_for(nvec, kThreads * 4, lc.num_sms * 4), kThreads, 0, lc.stream>>>(
-      ret, g, region, stage, reinterpret_cast<uint4*>(out), n, row_bytes, num_experts, expect_seq,
-      status, timeout_ns);
-  ++*lc.launches;
-  return cudaGetLastError();
+  return launch_k(lc, k_unpack, grid_for(nvec, kThreads * 4, lc.num_sms * 4), kThreads, 0, ret, g,
+                  region, stage, reinterpret_cast<uint4*>(out), n, row_bytes, num_experts,
+                  expect_seq, status, timeout_ns);
 }
 
 cudaError_t launch_transpose_wg(const LaunchCtx& lc, const float* Wg, float* WgT, int hidden,
                                 int E) {
-  k_transpose_wg<<<grid_for((int64_t)hidden * E, kThreads, 1024), kThreads, 0, lc.stream>>>(
-      Wg, WgT, hidden, E);
-  ++*lc.launches;
-  return cudaGetLastError();
+  return launch_k(lc, k_transpose_wg, grid_for((int64_t)hidden * E, kThreads, 1024), kThreads, 0,
+                  Wg, WgT, hidden, E);
 }

@@ -92,7 +92,12 @@ extern "C" {
  *                  >= 1); one FFN rank receives exactly T * topk partials
  * wait_timeout_ns  bound on every device-side wait (flag polls); 0 = 1 s
  * gemm             AFD_GEMM_*; max_layers: size of the layer weight table
+ * flags            AFD_CFG_* bits, 0 for the defaults
  */
+/* Launch every kernel after the previous one has fully finished, instead of
+ * letting its CTAs be scheduled (and wait on the device) while the previous
+ * kernel drains (programmatic dependent launch, the default). */
+#define AFD_CFG_NO_PDL 1
 typedef struct afd_config {
   int32_t num_peers;
   int32_t ring_depth;
@@ -107,7 +112,7 @@ typedef struct afd_config {
   int32_t renorm;
   int32_t max_layers;
   int32_t gemm;
-  int32_t reserved;
+  int32_t flags;
   float routed_scaling;
   float routed_cap_multiplier;
   int64_t wait_timeout_ns;

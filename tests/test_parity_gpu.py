@@ -32,6 +32,18 @@ def test_fanin_bf16(gemm):
     print("fanin max|err|/rms", e)
 
 
+@pytest.mark.parametrize("workload", ["fanin", "v2lite_prefill"])
+def test_serialised_launches(workload):
+    """Every kernel launched after the previous one has finished (no
+    programmatic dependent launch): the same results."""
+    w = W.get(workload)
+    run = R.Runner(w, max_total_tokens=w.total_tokens, flags=A.AFD_CFG_NO_PDL)
+    if workload == "fanin":
+        G.run_and_compare_full(run)
+    else:
+        G.run_and_compare_sampled(run, per_peer=2)
+
+
 def test_fanin_reordered_with_empty_peer():
     w = W.custom("fanin", seq_lens=[37, 0, 91, 5])
     run = R.Runner(w)

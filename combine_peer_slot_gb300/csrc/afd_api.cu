@@ -21,7 +21,7 @@ struct LayerW {
   const void* Wd = nullptr;
   const void* W13s = nullptr;
   const void* Wds = nullptr;
-  float* WgT = nullptr;              // library-owned transposed router weight
+  float* WgQ = nullptr;              // library-owned rearranged router weight
   CUtensorMap tmA1[2];               // SwiGLU projection: routed, shared
   CUtensorMap tmA2[2];               // down projection: routed, shared
 };
@@ -272,7 +272,7 @@ void afd_destroy(afd_ctx* ctx) {
   if (!ctx) return;
   cudaSetDevice(ctx->device);
   cudaStreamSynchronize(ctx->stream);
-  for (auto& l : ctx->layers) cudaFree(l.WgT);
+  for (auto& l : ctx->layers) cudaFree(l.WgQ);
   for (auto& set : ctx->ev)
     for (auto& e : set)
       if (e) cudaEventDestroy(e);
@@ -402,11 +402,12 @@ int afd_set_layer(afd_ctx* ctx, int layer, const float* Wg, const float* bias, c
     if (!aligned16(p)) return AFD_ERR_ARG;
   }
   LayerW& L = ctx->layers[layer];
-  if (!L.WgT) {
-    int rc = cuda_fail(cudaMalloc(&L.WgT, (size_t)c.hidden * c.num_experts * 4), "router copy");
+  if (!L.WgQ) {
+    int rc = cuda_fail(cudaMalloc(&L.WgQ, (size_t)wgq_groups(c.num_experts) * c.hidden * 16),
+                       "router copy");
     if (rc) return rc;
   }
-  int rc = cuda_fail(launch_transpose_wg(ctx->lc(), Wg, L.WgT, c.hidden, c.num_experts), "transpose");
+  int rc = cuda_fail(launch_arrange_wg(ctx->lc(), Wg, L.WgQ, c.hidden, c.num_experts), "router copy");
   if (rc) return rc;
   L.Wg = Wg;
   L.bias = bias;
@@ -510,7 +511,7 @@ int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, con
                      "header check");
   if (rc) return rc;
   ctx->mark(1);
-  rc = cuda_fail(launch_router(lc, ctx->geom, ctx->win[0], f, ws, c.hidden, ctx->act_f32, L.WgT,
+  rc = cuda_fail(launch_router(lc, ctx->geom, ctx->win[0], f, ws, c.hidden, ctx->act_f32, L.WgQ,
                                L.bias, c.num_experts, c.topk, c.renorm, c.routed_scaling,
                                ws.logits, ws.hist),
                  "router");

@@ -172,6 +172,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // TMA ------------------------------------------------------------------------
+// contiguous bytes global -> shared (both 16-byte aligned, size % 16 == 0)
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
                                             uint32_t bar) {
   asm volatile(
@@ -242,6 +250,9 @@ __device__ __forceinline__ void grid_dep_launch() {
 // ---------------------------------------------------------------------------
 // launchers implemented in the kernel translation units (host side)
 // ---------------------------------------------------------------------------
+// groups of 4 experts in the rearranged router weight
+__host__ __device__ inline int wgq_groups(int E) { return (E + 3) / 4; }
+
 struct LaunchCtx {
   cudaStream_t stream;
   int num_sms;
@@ -286,7 +297,7 @@ size_t router_min_smem_bytes(int hidden, int E, int act_f32);
 // into ws.ids / ws.w and, if hist is not NULL, the per-16-token histograms
 cudaError_t launch_router(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                           const FanIn& f, const DevWS& ws, int hidden, int act_f32,
-                          const float* WgT, const float* bias, int E, int k, int renorm,
+                          const float* WgQ, const float* bias, int E, int k, int renorm,
                           float scale, float* logits, int32_t* hist);
 cudaError_t launch_plan(const LaunchCtx& lc, const FanIn& f, const DevWS& ws, int E, int k,
                         int inter, int shared_inter, int hidden, int has_shared, int bn,
@@ -306,5 +317,5 @@ cudaError_t launch_return_header(const LaunchCtx& lc, const WinGeom& g, uint8_t*
 cudaError_t launch_unpack(const LaunchCtx& lc, const WinGeom& g, const uint8_t* ret, int region,
                           int stage, void* out, int n, int row_bytes, int num_experts,
                           uint64_t expect_seq, int32_t* status, int64_t timeout_ns);
-cudaError_t launch_transpose_wg(const LaunchCtx& lc, const float* Wg, float* WgT, int hidden,
+cudaError_t launch_arrange_wg(const LaunchCtx& lc, const float* Wg, float* WgQ, int hidden,
                                 int E);

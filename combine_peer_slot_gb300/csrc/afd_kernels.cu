@@ -2,6 +2,8 @@
 // step on sm_103a: slot pack / header / flag, header check with a bounded
 // flag wait, router, dispatch plan, permute-gather, combine + split, return
 // header + flag, unpack, and the SIMT GEMM used for fp32 activations.
+#include <algorithm>
+
 #include "afd_internal.cuh"
 
 namespace {
@@ -286,7 +288,7 @@ __device__ __forceinline__ int lg_index(int h, int tt, int hidden) {
 template <typename XS>
 __global__ void __launch_bounds__(kLgWarps * 32)
 k_router_logits(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int hidden,
-                const float* __restrict__ WgT, const float* __restrict__ bias, int E,
+                const float* __restrict__ WgQ, const float* __restrict__ bias, int E,
                 float* __restrict__ logits) {
   grid_dep_wait();
   grid_dep_launch();
@@ -330,9 +332,12 @@ k_router_logits(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int hidden,
   __syncthreads();
   const int e0 = blockIdx.y * kLgEblk + warp * kLgEpw;
   if (e0 >= E) return;
-  const float* wrow[kLgEpw];
+  const float* wrow[kLgEpw];  // expert e, h at wrow[b][4 h]
 #pragma unroll
-  for (int b = 0; b < kLgEpw; b++) wrow[b] = WgT + (int64_t)min(e0 + b, E - 1) * hidden;
+  for (int b = 0; b < kLgEpw; b++) {
+    const int e = min(e0 + b, E - 1);
+    wrow[b] = WgQ + (int64_t)(e >> 2) * hidden * 4 + (e & 3);
+  }
   float acc[kLgTok][kLgEpw];
 #pragma unroll
   for (int a = 0; a < kLgTok; a++)
@@ -346,7 +351,7 @@ k_router_logits(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int hidden,
     for (int u = 0; u < 4; u++) {
       const int h = lane + 32 * (i0 + u);
 #pragma unroll
-      for (int b = 0; b < kLgEpw; b++) wv[u][b] = h < hidden ? __ldg(wrow[b] + h) : 0.0f;
+      for (int b = 0; b < kLgEpw; b++) wv[u][b] = h < hidden ? __ldg(wrow[b] + 4 * h) : 0.0f;
     }
 #pragma unroll
     for (int u = 0; u < 4; u++) {
@@ -391,6 +396,479 @@ k_router_logits(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int hidden,
       for (int b = 0; b < kLgEpw; b++)
         if (e0 + b < E)
           logits[(int64_t)(t0 + a) * E + e0 + b] = bias ? __fadd_rn(acc[a][b], bias[e0 + b]) : acc[a][b];
+}
+
+// a1 router, part 1, weight-stationary form (same canonical order as
+// k_router_logits).  A CTA owns a block of 4 * EPW experts, whose rows of the
+// transposed router weight stay in shared memory for its whole life, and
+// walks the token tiles blockIdx.x, + gridDim.x, ...: each tile of 8 token
+// rows is copied from the peer slots with one bulk copy per row into a ring
+// of `ns` buffers, the copies of later tiles in flight while the four warps
+// compute (warp w: experts 4w..4w+3 of the block x the 8 tokens).
+constexpr int kWsTok = 8;
+constexpr int kWsWarps = 4;
+constexpr uint64_t kWsTimeoutNs = 1000000000ull;
+
+struct WsGeom {
+  int ns;          // x ring buffers
+  size_t w_bytes;  // weight block, 128-byte rounded
+  size_t tile_bytes;
+  size_t smem;
+};
+
+template <typename XS, int EPW>
+__global__ void __launch_bounds__(kWsWarps * 32, 1)
+k_router_logits_ws(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int hidden,
+                   const float* __restrict__ WgQ, const float* __restrict__ bias, int E,
+                   float* __restrict__ logits, WsGeom geo) {
+  grid_dep_wait();
+  grid_dep_launch();
+  extern __shared__ __align__(128) uint8_t ws_smem[];
+  constexpr int EB = EPW * kWsWarps;
+  const float* Ws = reinterpret_cast<const float*>(ws_smem);  // [EB / 4][hidden][4]
+  const uint8_t* xring = ws_smem + geo.w_bytes;                                  // [ns][8][hidden]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ws_smem + geo.w_bytes + geo.ns * geo.tile_bytes);
+  __shared__ int abort_s;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (read_status(ws.status)) return;
+  const int e_base = blockIdx.y * EB;
+  const int ne = min(EB, E - e_base);
+  const int ntiles = (f.total + kWsTok - 1) / kWsTok;
+  if ((int)blockIdx.x >= ntiles || ne <= 0) return;
+  const int my_tiles = (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1;
+  const int row_bytes = hidden * (int)sizeof(XS);
+  const uint32_t wbar = smem_u32(&bars[geo.ns]);
+  auto issue = [&](int i) {  // tile i of this CTA into buffer i % ns (thread 0)
+    const int buf = i % geo.ns;
+    const int t0 = ((int)blockIdx.x + i * (int)gridDim.x) * kWsTok;
+    const int nt = min(kWsTok, f.total - t0);
+    const uint32_t bar = smem_u32(&bars[buf]);
+    mbar_expect_tx(bar, (uint32_t)(nt * row_bytes));
+    for (int r = 0; r < nt; r++) {
+      const int t = t0 + r;
+      const int e = entry_of(f, t);
+      const uint8_t* src = slot_ptr(win, g, f.region[e], f.stage) + g.routed_x +
+                           (int64_t)(t - f.prefix[e]) * row_bytes;
+      bulk_load(smem_u32(xring + buf * geo.tile_bytes + (size_t)r * row_bytes), src,
+                (uint32_t)row_bytes, bar);
+    }
+  };
+  if (tid == 0) {
+    abort_s = 0;
+    for (int b = 0; b <= geo.ns; b++) mbar_init(smem_u32(&bars[b]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    const uint32_t wbytes = (uint32_t)(((ne + 3) / 4) * hidden * 16);
+    mbar_expect_tx(wbar, wbytes);
+    bulk_load(smem_u32(ws_smem), WgQ + (int64_t)e_base * hidden, wbytes, wbar);
+    for (int i = 0; i < min(geo.ns, my_tiles); i++) issue(i);
+  }
+  __syncthreads();
+  const uint64_t deadline = globaltimer_ns() + kWsTimeoutNs;
+  auto wait = [&](uint32_t bar, uint32_t parity) {
+    uint32_t spins = 0;
+    while (!mbar_try_wait(bar, parity)) {
+      if ((++spins & 255u) == 0 && (*(volatile int*)&abort_s || globaltimer_ns() > deadline)) {
+        abort_s = 1;
+        return false;
+      }
+    }
+    return true;
+  };
+  int done = 0;  // tiles consumed
+  // every wait is followed by a block-wide vote, so all threads leave together
+  if (!__syncthreads_or(!wait(wbar, 0))) {
+    const int el = warp * EPW;  // first local expert of this warp
+    const float* wrow[EPW];  // local expert e, h at wrow[b][4 h]
+#pragma unroll
+    for (int b = 0; b < EPW; b++) {
+      const int e = min(el + b, ne - 1);
+      wrow[b] = Ws + (size_t)(e >> 2) * hidden * 4 + (e & 3);
+    }
+    const int nfull = hidden / 32;
+    for (int i = 0; i < my_tiles; i++) {
+      const int buf = i % geo.ns;
+      if (__syncthreads_or(!wait(smem_u32(&bars[buf]), (uint32_t)((i / geo.ns) & 1)))) break;
+      const XS* xt = reinterpret_cast<const XS*>(xring + buf * geo.tile_bytes);
+      float acc[kWsTok][EPW];
+#pragma unroll
+      for (int a = 0; a < kWsTok; a++)
+#pragma unroll
+        for (int b = 0; b < EPW; b++) acc[a][b] = 0.0f;
+      auto step = [&](int h) {
+        float wv[EPW];
+#pragma unroll
+        for (int b = 0; b < EPW; b++) wv[b] = wrow[b][4 * h];
+#pragma unroll
+        for (int a = 0; a < kWsTok; a++) {
+          float xv;
+          if constexpr (sizeof(XS) == 4) xv = reinterpret_cast<const float*>(xt)[(size_t)a * hidden + h];
+          else xv = bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(xt)[(size_t)a * hidden + h]);
+#pragma unroll
+          for (int b = 0; b < EPW; b++) acc[a][b] = __fmaf_rn(xv, wv[b], acc[a][b]);
+        }
+      };
+#pragma unroll 4
+      for (int j = 0; j < nfull; j++) step(32 * j + lane);
+      if (32 * nfull + lane < hidden) step(32 * nfull + lane);
+#pragma unroll
+      for (int a = 0; a < kWsTok; a++)
+#pragma unroll
+        for (int b = 0; b < EPW; b++) {
+          float v = acc[a][b];
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
+          acc[a][b] = v;
+        }
+      const int t0 = ((int)blockIdx.x + i * (int)gridDim.x) * kWsTok;
+#pragma unroll
+      for (int a = 0; a < kWsTok; a++)
+        if (lane == a && t0 + a < f.total)
+#pragma unroll
+          for (int b = 0; b < EPW; b++)
+            if (el + b < ne) {
+              const int e = e_base + el + b;
+              logits[(int64_t)(t0 + a) * E + e] = bias ? __fadd_rn(acc[a][b], bias[e]) : acc[a][b];
+            }
+      __syncthreads();  // every warp is done with this buffer
+      done = i + 1;
+      if (tid == 0 && i + geo.ns < my_tiles && !abort_s) issue(i + geo.ns);
+    }
+  }
+  __syncthreads();
+  if (abort_s && tid == 0) {
+    set_error(ws.status, AFD_ERR_TIMEOUT);
+    // copies still in flight land in this CTA's shared memory: wait (bounded)
+    const uint64_t dl = globaltimer_ns() + 100000000ull;
+    while (!mbar_try_wait(wbar, 0) && globaltimer_ns() < dl) {}
+    const int issued = min(my_tiles, done + geo.ns);
+    for (int i = done; i < issued; i++)
+      while (!mbar_try_wait(smem_u32(&bars[i % geo.ns]), (uint32_t)((i / geo.ns) & 1)) &&
+             globaltimer_ns() < dl) {}
+  }
+}
+
+// a1 router, part 1, for bf16 activations: weight-stationary with the token
+// tile transposed in shared memory (same canonical order).  A CTA owns 16
+// experts (4 groups of the rearranged weight, 4 per warp) for its whole life
+// and walks the token tiles blockIdx.x, + gridDim.x, ...  A tile of 8 token
+// rows lands by bulk copies in a row-major staging buffer (the next tile's
+// copies overlap the current tile's arithmetic); the CTA then transposes it
+// to one 16-byte record per h holding the 8 tokens' values (a 16-byte pad
+// after every 8 records keeps both the transposing stores and the reads free
+// of bank conflicts).  Per h a lane then needs one 16-byte load of tokens
+// and one of weights for 32 multiply-adds, issued as pairs over two tokens.
+// Butterfly over the 32 lanes for 32 values at once, scattered: at offset o
+// a lane keeps the half of its values selected by its lane bit o and adds
+// the partner's copy, so lane l ends with value l summed over all lanes.
+// Each value sees exactly the additions of the all-lane butterfly with
+// offsets 16, 8, 4, 2, 1 (addition commutes), in 31 shuffles instead of 160.
+__device__ __forceinline__ float butterfly_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; i++) {
+      const float send = up ? v[i] : v[i + o];
+      const float keep = up ? v[i + o] : v[i];
+      v[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, o));
+    }
+  }
+  return v[0];
+}
+
+constexpr int kTwTok = 8;
+constexpr int kTwWarps = 4;
+constexpr int kTwExperts = 4 * kTwWarps;
+
+__host__ __device__ inline size_t tw_rec_offset(int h) { return 16 * (size_t)h + 16 * (size_t)(h >> 3); }
+
+struct TwGeom {
+  size_t w_bytes;      // weight block, 128-byte rounded
+  size_t stage_bytes;  // 8 rows, row-major
+  size_t xt_bytes;     // transposed records
+  size_t smem;
+};
+
+__global__ void __launch_bounds__(kTwWarps * 32, 1)
+k_router_logits_tw(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int hidden,
+                   const float* __restrict__ WgQ, const float* __restrict__ bias, int E,
+                   float* __restrict__ logits, TwGeom geo) {
+  grid_dep_wait();
+  grid_dep_launch();
+  extern __shared__ __align__(128) uint8_t tw_smem[];
+  const float4* Wq = reinterpret_cast<const float4*>(tw_smem);  // [4 groups][hidden]
+  uint8_t* stage = tw_smem + geo.w_bytes;                         // [8][hidden] bf16
+  uint8_t* xt = stage + geo.stage_bytes;                          // records
+  uint64_t* bars = reinterpret_cast<uint64_t*>(xt + geo.xt_bytes);  // [0] weights, [1] stage
+  __shared__ int abort_s;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (read_status(ws.status)) return;
+  const int e_base = blockIdx.y * kTwExperts;
+  const int ne = min(kTwExperts, E - e_base);
+  const int ntiles = (f.total + kTwTok - 1) / kTwTok;
+  if ((int)blockIdx.x >= ntiles || ne <= 0) return;
+  const int my_tiles = (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1;
+  const int row_bytes = hidden * 2;
+  const uint32_t wbar = smem_u32(&bars[0]), sbar = smem_u32(&bars[1]);
+  auto issue = [&](int i) {  // tile i of this CTA into the staging buffer (thread 0)
+    const int t0 = ((int)blockIdx.x + i * (int)gridDim.x) * kTwTok;
+    const int nt = min(kTwTok, f.total - t0);
+    mbar_expect_tx(sbar, (uint32_t)(nt * row_bytes));
+    for (int r = 0; r < nt; r++) {
+      const int t = t0 + r;
+      const int e = entry_of(f, t);
+      const uint8_t* src = slot_ptr(win, g, f.region[e], f.stage) + g.routed_x +
+                           (int64_t)(t - f.prefix[e]) * row_bytes;
+      bulk_load(smem_u32(stage + (size_t)r * row_bytes), src, (uint32_t)row_bytes, sbar);
+    }
+  };
+  if (tid == 0) {
+    abort_s = 0;
+    mbar_init(wbar, 1);
+    mbar_init(sbar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    const uint32_t wbytes = (uint32_t)(((ne + 3) / 4) * hidden * 16);
+    mbar_expect_tx(wbar, wbytes);
+    bulk_load(smem_u32(tw_smem), WgQ + (int64_t)e_base * hidden, wbytes, wbar);
+    issue(0);
+  }
+  __syncthreads();
+  const uint64_t deadline = globaltimer_ns() + kWsTimeoutNs;
+  auto wait = [&](uint32_t bar, uint32_t parity) {
+    uint32_t spins = 0;
+    while (!mbar_try_wait(bar, parity)) {
+      if ((++spins & 255u) == 0 && (*(volatile int*)&abort_s || globaltimer_ns() > deadline)) {
+        abort_s = 1;
+        return false;
+      }
+    }
+    return true;
+  };
+  int done = 0;  // tiles consumed
+  // every wait is followed by a block-wide vote, so all threads leave together
+  if (!__syncthreads_or(!wait(wbar, 0))) {
+    const int grp = min(warp, (ne - 1) / 4);  // a warp past the block's experts computes a copy
+    const float4* wq = Wq + (size_t)grp * hidden;
+    const int nchunks = hidden / 8;
+    for (int i = 0; i < my_tiles; i++) {
+      if (__syncthreads_or(!wait(sbar, (uint32_t)(i & 1)))) break;
+      // stage [t][h] -> records [h][t]: thread takes 8-wide h chunks; rows
+      // past the fan-in total hold stale bytes whose results are not stored
+      for (int c = tid; c < nchunks; c += blockDim.x) {
+        uint4 in[kTwTok];
+#pragma unroll
+        for (int t = 0; t < kTwTok; t++)
+          in[t] = *reinterpret_cast<const uint4*>(stage + (size_t)t * row_bytes + 16 * c);
+        const uint32_t* iw[kTwTok];
+#pragma unroll
+        for (int t = 0; t < kTwTok; t++) iw[t] = reinterpret_cast<const uint32_t*>(&in[t]);
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+          const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
+          uint4 o;
+          o.x = __byte_perm(iw[0][j >> 1], iw[1][j >> 1], sel);
+          o.y = __byte_perm(iw[2][j >> 1], iw[3][j >> 1], sel);
+          o.z = __byte_perm(iw[4][j >> 1], iw[5][j >> 1], sel);
+          o.w = __byte_perm(iw[6][j >> 1], iw[7][j >> 1], sel);
+          *reinterpret_cast<uint4*>(xt + tw_rec_offset(8 * c + j)) = o;
+        }
+      }
+      __syncthreads();  // records written, staging buffer free
+      done = i + 1;
+      if (tid == 0 && i + 1 < my_tiles) issue(i + 1);
+      float2 acc[kTwTok / 2][4];  // {token 2p, token 2p + 1} x expert b of the group
+#pragma unroll
+      for (int p = 0; p < kTwTok / 2; p++)
+#pragma unroll
+        for (int b = 0; b < 4; b++) acc[p][b] = make_float2(0.0f, 0.0f);
+      auto step = [&](int h) {
+        const uint4 xr = *reinterpret_cast<const uint4*>(xt + tw_rec_offset(h));
+        const float4 w4 = wq[h];
+        const uint32_t xw[4] = {xr.x, xr.y, xr.z, xr.w};
+        const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int p = 0; p < kTwTok / 2; p++) {
+          const float2 xp = make_float2(__uint_as_float(xw[p] << 16), __uint_as_float(xw[p] & 0xffff0000u));
+#pragma unroll
+          for (int b = 0; b < 4; b++) acc[p][b] = __ffma2_rn(xp, make_float2(wv[b], wv[b]), acc[p][b]);
+        }
+      };
+      const int nfull = hidden / 32;
+#pragma unroll 4
+      for (int j = 0; j < nfull; j++) step(32 * j + lane);
+      if (32 * nfull + lane < hidden) step(32 * nfull + lane);
+      float v[32];  // index 4 t + b
+#pragma unroll
+      for (int p = 0; p < kTwTok / 2; p++)
+#pragma unroll
+        for (int b = 0; b < 4; b++) {
+          v[8 * p + b] = acc[p][b].x;
+          v[8 * p + 4 + b] = acc[p][b].y;
+        }
+      const float sum = butterfly_scatter32(v, lane);  // token lane / 4, expert lane % 4
+      const int t = ((int)blockIdx.x + i * (int)gridDim.x) * kTwTok + (lane >> 2);
+      const int el = 4 * warp + (lane & 3);
+      if (t < f.total && el < ne) {
+        const int e = e_base + el;
+        logits[(int64_t)t * E + e] = bias ? __fadd_rn(sum, bias[e]) : sum;
+      }
+      __syncthreads();  // every warp is done with the records
+    }
+  }
+  __syncthreads();
+  if (abort_s && tid == 0) {
+    set_error(ws.status, AFD_ERR_TIMEOUT);
+    // copies still in flight land in this CTA's shared memory: wait (bounded)
+    const uint64_t dl = globaltimer_ns() + 100000000ull;
+    while (!mbar_try_wait(wbar, 0) && globaltimer_ns() < dl) {}
+    if (done < my_tiles)
+      while (!mbar_try_wait(sbar, (uint32_t)(done & 1)) && globaltimer_ns() < dl) {}
+  }
+}
+
+// The same computation with two independent tile streams per CTA (for
+// hidden <= 2048): warps 0-3 and warps 4-7 each own a transposed-record
+// buffer and take alternate token tiles, synchronising only among
+// themselves (named barriers), so one stream's transposition and barrier
+// waits overlap the other's arithmetic.  A stream's next tile is loaded from
+// the peer slots into registers while it computes the current one.
+constexpr int kTw2Chunks = 2;  // 8-element h chunks per thread and token: hidden <= 2048
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__global__ void __launch_bounds__(2 * kTwWarps * 32, 1)
+k_router_logits_tw2(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int hidden,
+                    const float* __restrict__ WgQ, const float* __restrict__ bias, int E,
+                    float* __restrict__ logits, TwGeom geo) {
+  grid_dep_wait();
+  grid_dep_launch();
+  extern __shared__ __align__(128) uint8_t tw_smem[];
+  const float4* Wq = reinterpret_cast<const float4*>(tw_smem);  // [4 groups][hidden]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int set = warp / kTwWarps, wis = warp % kTwWarps, tis = tid % (kTwWarps * 32);
+  uint8_t* xt = tw_smem + geo.w_bytes + set * geo.xt_bytes;      // this stream's records
+  uint64_t* wbar_p = reinterpret_cast<uint64_t*>(tw_smem + geo.w_bytes + 2 * geo.xt_bytes);
+  __shared__ int abort_s;
+  if (read_status(ws.status)) return;
+  const int e_base = blockIdx.y * kTwExperts;
+  const int ne = min(kTwExperts, E - e_base);
+  const int ntiles = (f.total + kTwTok - 1) / kTwTok;
+  if ((int)blockIdx.x >= ntiles || ne <= 0) return;
+  const int my_tiles = (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1;
+  const int row_bytes = hidden * 2;
+  const int nchunks = hidden / 8;
+  const uint32_t wbar = smem_u32(wbar_p);
+  if (tid == 0) {
+    abort_s = 0;
+    mbar_init(wbar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    const uint32_t wbytes = (uint32_t)(((ne + 3) / 4) * hidden * 16);
+    mbar_expect_tx(wbar, wbytes);
+    bulk_load(smem_u32(tw_smem), WgQ + (int64_t)e_base * hidden, wbytes, wbar);
+  }
+  // tiles of this stream: local index i = set, set + 2, ...
+  uint4 pre[kTw2Chunks][kTwTok];
+  auto fetch = [&](int i) {  // tile i's chunks of this thread into pre (zeros past the fan-in)
+    const int t0 = ((int)blockIdx.x + i * (int)gridDim.x) * kTwTok;
+#pragma unroll
+    for (int r = 0; r < kTwTok; r++) {
+      const int t = t0 + r;
+      const uint4* src = nullptr;
+      if (t < f.total) {
+        const int e = entry_of(f, t);
+        src = reinterpret_cast<const uint4*>(slot_ptr(win, g, f.region[e], f.stage) + g.routed_x +
+                                             (int64_t)(t - f.prefix[e]) * row_bytes);
+      }
+#pragma unroll
+      for (int cc = 0; cc < kTw2Chunks; cc++) {
+        const int c = tis + cc * kTwWarps * 32;
+        pre[cc][r] = (src && c < nchunks) ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+      }
+    }
+  };
+  if (set < my_tiles) fetch(set);
+  __syncthreads();
+  const uint64_t deadline = globaltimer_ns() + kWsTimeoutNs;
+  bool ok = true;
+  {
+    uint32_t spins = 0;
+    while (!mbar_try_wait(wbar, 0)) {
+      if ((++spins & 255u) == 0 && globaltimer_ns() > deadline) { ok = false; break; }
+    }
+  }
+  if (__syncthreads_or(!ok)) {
+    if (tid == 0) {
+      set_error(ws.status, AFD_ERR_TIMEOUT);
+      const uint64_t dl = globaltimer_ns() + 100000000ull;
+      while (!mbar_try_wait(wbar, 0) && globaltimer_ns() < dl) {}
+    }
+    return;
+  }
+  const int grp = min(wis, (ne - 1) / 4);  // a warp past the block's experts computes a copy
+  const float4* wq = Wq + (size_t)grp * hidden;
+  const int bar_id = 1 + set;
+  for (int i = set; i < my_tiles; i += 2) {
+    named_bar_sync(bar_id, kTwWarps * 32);  // this stream is done reading its records
+#pragma unroll
+    for (int cc = 0; cc < kTw2Chunks; cc++) {
+      const int c = tis + cc * kTwWarps * 32;
+      if (c < nchunks) {
+        const uint32_t* iw[kTwTok];
+#pragma unroll
+        for (int t = 0; t < kTwTok; t++) iw[t] = reinterpret_cast<const uint32_t*>(&pre[cc][t]);
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+          const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
+          uint4 o;
+          o.x = __byte_perm(iw[0][j >> 1], iw[1][j >> 1], sel);
+          o.y = __byte_perm(iw[2][j >> 1], iw[3][j >> 1], sel);
+          o.z = __byte_perm(iw[4][j >> 1], iw[5][j >> 1], sel);
+          o.w = __byte_perm(iw[6][j >> 1], iw[7][j >> 1], sel);
+          *reinterpret_cast<uint4*>(xt + tw_rec_offset(8 * c + j)) = o;
+        }
+      }
+    }
+    named_bar_sync(bar_id, kTwWarps * 32);  // records complete
+    if (i + 2 < my_tiles) fetch(i + 2);
+    float2 acc[kTwTok / 2][4];  // {token 2p, token 2p + 1} x expert b of the group
+#pragma unroll
+    for (int p = 0; p < kTwTok / 2; p++)
+#pragma unroll
+      for (int b = 0; b < 4; b++) acc[p][b] = make_float2(0.0f, 0.0f);
+    auto step = [&](int h) {
+      const uint4 xr = *reinterpret_cast<const uint4*>(xt + tw_rec_offset(h));
+      const float4 w4 = wq[h];
+      const uint32_t xw[4] = {xr.x, xr.y, xr.z, xr.w};
+      const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+      for (int p = 0; p < kTwTok / 2; p++) {
+        const float2 xp = make_float2(__uint_as_float(xw[p] << 16), __uint_as_float(xw[p] & 0xffff0000u));
+#pragma unroll
+        for (int b = 0; b < 4; b++) acc[p][b] = __ffma2_rn(xp, make_float2(wv[b], wv[b]), acc[p][b]);
+      }
+    };
+    const int nfull = hidden / 32;
+#pragma unroll 8
+    for (int j = 0; j < nfull; j++) step(32 * j + lane);
+    if (32 * nfull + lane < hidden) step(32 * nfull + lane);
+    float v[32];  // index 4 t + b
+#pragma unroll
+    for (int p = 0; p < kTwTok / 2; p++)
+#pragma unroll
+      for (int b = 0; b < 4; b++) {
+        v[8 * p + b] = acc[p][b].x;
+        v[8 * p + 4 + b] = acc[p][b].y;
+      }
+    const float sum = butterfly_scatter32(v, lane);  // token lane / 4, expert lane % 4
+    const int t = ((int)blockIdx.x + i * (int)gridDim.x) * kTwTok + (lane >> 2);
+    const int el = 4 * wis + (lane & 3);
+    if (t < f.total && el < ne) {
+      const int e = e_base + el;
+      logits[(int64_t)t * E + e] = bias ? __fadd_rn(sum, bias[e]) : sum;
+    }
+  }
 }
 
 // a1 router, part 2: top-k on the logits (ties -> lower expert index, NaN
@@ -961,14 +1439,19 @@ k_unpack(const uint8_t* ret, WinGeom g, int region, int stage, uint4* out, int n
     out[v] = src[v];
 }
 
-__global__ void k_transpose_wg(const float* Wg, float* WgT, int hidden, int E) {
+// The router weight [hidden][E] rearranged for the logits kernels as
+// WgQ[E/4 groups][hidden][4 experts] fp32 (experts past E are zero): a lane
+// reads the 4 weights of its h for a group of experts with one 16-byte load.
+__global__ void k_arrange_wg(const float* Wg, float* WgQ, int hidden, int E) {
   grid_dep_wait();
   grid_dep_launch();
-  const int64_t n = (int64_t)hidden * E;
+  const int64_t n = (int64_t)wgq_groups(E) * hidden * 4;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
-    const int e = (int)(i / hidden), h = (int)(i % hidden);
-    WgT[i] = Wg[(int64_t)h * E + e];
+    const int q = (int)(i & 3);
+    const int h = (int)((i >> 2) % hidden);
+    const int e = (int)(i / (4 * (int64_t)hidden)) * 4 + q;
+    WgQ[i] = e < E ? Wg[(int64_t)h * E + e] : 0.0f;
   }
 }
 
@@ -1022,24 +1505,114 @@ cudaError_t launch_header_check(const LaunchCtx& lc, const WinGeom& g, const uin
 
 template <typename XS>
 static cudaError_t launch_logits_t(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
-                                   const FanIn& f, const DevWS& ws, int hidden, const float* WgT,
+                                   const FanIn& f, const DevWS& ws, int hidden, const float* WgQ,
                                    const float* bias, int E, float* logits) {
   const size_t smem = (size_t)hidden * kLgTok * sizeof(XS);
   cudaError_t err = cudaFuncSetAttribute(k_router_logits<XS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   dim3 grid((f.total + kLgTok - 1) / kLgTok, (E + kLgEblk - 1) / kLgEblk);
-  return launch_k(lc, k_router_logits<XS>, grid, kLgWarps * 32, smem, win, g, f, ws, hidden, WgT,
+  return launch_k(lc, k_router_logits<XS>, grid, kLgWarps * 32, smem, win, g, f, ws, hidden, WgQ,
                   bias, E, logits);
+}
+
+// Shared memory of the weight-stationary logits kernel with 4 * epw experts
+// per CTA; the ring takes 3 buffers, or 2 when 3 do not fit.  smem = 0: it
+// does not fit at all.
+static WsGeom ws_geom(int hidden, int xs_bytes, int epw) {
+  constexpr size_t kLimit = 232448 - 1024;
+  WsGeom geo{};
+  geo.w_bytes = ((size_t)((kWsWarps * epw + 3) / 4) * hidden * 16 + 127) / 128 * 128;
+  geo.tile_bytes = (size_t)kWsTok * hidden * xs_bytes;
+  for (int ns = 3; ns >= 2; ns--) {
+    const size_t total = geo.w_bytes + ns * geo.tile_bytes + 8 * (ns + 1);
+    if (total <= kLimit) {
+      geo.ns = ns;
+      geo.smem = total;
+      return geo;
+    }
+  }
+  geo.smem = 0;
+  return geo;
+}
+
+template <typename XS, int EPW>
+static cudaError_t launch_logits_ws(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
+                                    const FanIn& f, const DevWS& ws, int hidden, const float* WgQ,
+                                    const float* bias, int E, float* logits, const WsGeom& geo) {
+  cudaError_t err = cudaFuncSetAttribute(k_router_logits_ws<XS, EPW>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.smem);
+  if (err != cudaSuccess) return err;
+  const int eblocks = (E + kWsWarps * EPW - 1) / (kWsWarps * EPW);
+  const int ntiles = (f.total + kWsTok - 1) / kWsTok;
+  // one CTA per SM (the weight block fills most of its shared memory)
+  const int gx = std::max(1, std::min(ntiles, lc.num_sms / eblocks));
+  return launch_k(lc, k_router_logits_ws<XS, EPW>, dim3(gx, eblocks), kWsWarps * 32, geo.smem, win,
+                  g, f, ws, hidden, WgQ, bias, E, logits, geo);
+}
+
+static TwGeom tw_geom(int hidden) {
+  constexpr size_t kLimit = 232448 - 1024;
+  TwGeom geo{};
+  geo.w_bytes = ((size_t)4 * hidden * 16 + 127) / 128 * 128;
+  geo.stage_bytes = (size_t)kTwTok * hidden * 2;
+  geo.xt_bytes = (tw_rec_offset(hidden) + 127) / 128 * 128;
+  const size_t total = geo.w_bytes + geo.stage_bytes + geo.xt_bytes + 16;
+  geo.smem = total <= kLimit ? total : 0;
+  return geo;
+}
+
+template <typename XS>
+static cudaError_t launch_logits(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
+                                 const FanIn& f, const DevWS& ws, int hidden, const float* WgQ,
+                                 const float* bias, int E, float* logits) {
+  if (sizeof(XS) == 2 && E >= 16 && hidden <= 8 * kTw2Chunks * kTwWarps * 32) {
+    TwGeom geo = tw_geom(hidden);
+    geo.stage_bytes = 0;  // no staging buffer; two record buffers
+    geo.smem = geo.w_bytes + 2 * geo.xt_bytes + 16;
+    if (geo.smem <= 232448 - 1024) {
+      cudaError_t err = cudaFuncSetAttribute(k_router_logits_tw2,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.smem);
+      if (err != cudaSuccess) return err;
+      const int eblocks = (E + kTwExperts - 1) / kTwExperts;
+      const int ntiles = (f.total + kTwTok - 1) / kTwTok;
+      const int gx = std::max(1, std::min(ntiles, lc.num_sms / eblocks));
+      return launch_k(lc, k_router_logits_tw2, dim3(gx, eblocks), 2 * kTwWarps * 32, geo.smem, win, g,
+                      f, ws, hidden, WgQ, bias, E, logits, geo);
+    }
+  }
+  if (sizeof(XS) == 2 && E >= 16) {
+    const TwGeom geo = tw_geom(hidden);
+    if (geo.smem) {
+      cudaError_t err = cudaFuncSetAttribute(k_router_logits_tw,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.smem);
+      if (err != cudaSuccess) return err;
+      const int eblocks = (E + kTwExperts - 1) / kTwExperts;
+      const int ntiles = (f.total + kTwTok - 1) / kTwTok;
+      const int gx = std::max(1, std::min(ntiles, lc.num_sms / eblocks));
+      return launch_k(lc, k_router_logits_tw, dim3(gx, eblocks), kTwWarps * 32, geo.smem, win, g, f,
+                      ws, hidden, WgQ, bias, E, logits, geo);
+    }
+  }
+  // experts per warp: 4 when there are >= 16 experts, fewer for small E or
+  // when the weight block and two token tiles do not fit
+  for (int epw = E >= 16 ? 4 : (E >= 8 ? 2 : 1); epw >= 1; epw >>= 1) {
+    const WsGeom geo = ws_geom(hidden, (int)sizeof(XS), epw);
+    if (!geo.smem) continue;
+    if (epw == 4) return launch_logits_ws<XS, 4>(lc, g, win, f, ws, hidden, WgQ, bias, E, logits, geo);
+    if (epw == 2) return launch_logits_ws<XS, 2>(lc, g, win, f, ws, hidden, WgQ, bias, E, logits, geo);
+    return launch_logits_ws<XS, 1>(lc, g, win, f, ws, hidden, WgQ, bias, E, logits, geo);
+  }
+  return launch_logits_t<XS>(lc, g, win, f, ws, hidden, WgQ, bias, E, logits);
 }
 
 cudaError_t launch_router(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                           const FanIn& f, const DevWS& ws, int hidden, int act_f32,
-                          const float* WgT, const float* bias, int E, int k, int renorm,
+                          const float* WgQ, const float* bias, int E, int k, int renorm,
                           float scale, float* logits, int32_t* hist) {
   if (f.total == 0) return cudaSuccess;
-  cudaError_t err = act_f32 ? launch_logits_t<float>(lc, g, win, f, ws, hidden, WgT, bias, E, logits)
-                            : launch_logits_t<uint16_t>(lc, g, win, f, ws, hidden, WgT, bias, E, logits);
+  cudaError_t err = act_f32 ? launch_logits<float>(lc, g, win, f, ws, hidden, WgQ, bias, E, logits)
+                            : launch_logits<uint16_t>(lc, g, win, f, ws, hidden, WgQ, bias, E, logits);
   if (err != cudaSuccess) return err;
   const int nblocks = router_blocks(f.total);
   return launch_k(lc, k_router_topk, nblocks, kRtTok * 32, 0, f, ws, logits, E, k, renorm, scale,
@@ -1105,8 +1678,8 @@ cudaError_t launch_unpack(const LaunchCtx& lc, const WinGeom& g, const uint8_t* 
                   expect_seq, status, timeout_ns);
 }
 
-cudaError_t launch_transpose_wg(const LaunchCtx& lc, const float* Wg, float* WgT, int hidden,
-                                int E) {
-  return launch_k(lc, k_transpose_wg, grid_for((int64_t)hidden * E, kThreads, 1024), kThreads, 0,
-                  Wg, WgT, hidden, E);
+cudaError_t launch_arrange_wg(const LaunchCtx& lc, const float* Wg, float* WgQ, int hidden,
+                              int E) {
+  return launch_k(lc, k_arrange_wg, grid_for((int64_t)wgq_groups(E) * hidden * 4, kThreads, 1024),
+                  kThreads, 0, Wg, WgQ, hidden, E);
 }

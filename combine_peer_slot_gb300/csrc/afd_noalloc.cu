@@ -5,11 +5,11 @@
 // fragments that pool), or a plugin that must not trigger the device-wide
 // synchronisation cudaMalloc/cudaFree can cause.  afd_route_noalloc serves
 // them: the caller passes inputs and outputs, and the only scratch the step
-// needs -- the transposed router weight, the router logits and a status
+// needs -- the rearranged router weight, the router logits and a status
 // word -- lives in the file-scope device array below, which every GPU that
 // loads this library holds until the process exits.
 //
-// The array is shared by every call: a call rewrites the transposed weight
+// The array is shared by every call: a call rewrites the router weight
 // and clears the status word before the router runs, and calls that overlap
 // on the GPU (different streams, no ordering between them) race on it.
 #include <cstdio>
@@ -19,7 +19,7 @@
 
 namespace {
 
-// [transposed router weight: hidden * num_experts fp32]
+// [rearranged router weight: 4 * ceil(num_experts / 4) * hidden fp32]
 // [logits: n_tokens * num_experts fp32][status word]; 256-byte aligned.
 static __device__ __align__(256) float
     g_noalloc_scratch[AFD_NOALLOC_MAX_ROUTER_WEIGHTS + AFD_NOALLOC_MAX_LOGITS + 64];
@@ -60,7 +60,7 @@ extern "C" int afd_route_noalloc(const void* x, int n_tokens, int hidden, int ac
       topk < 1 || topk > 16 || topk > num_experts ||
       (act_dtype != AFD_DTYPE_F32 && act_dtype != AFD_DTYPE_BF16))
     return AFD_ERR_ARG;
-  if ((int64_t)hidden * num_experts > AFD_NOALLOC_MAX_ROUTER_WEIGHTS ||
+  if ((int64_t)hidden * 4 * wgq_groups(num_experts) > AFD_NOALLOC_MAX_ROUTER_WEIGHTS ||
       (int64_t)n_tokens * num_experts > AFD_NOALLOC_MAX_LOGITS)
     return AFD_ERR_CAPACITY;
   if (n_tokens == 0) return AFD_OK;
@@ -68,7 +68,7 @@ extern "C" int afd_route_noalloc(const void* x, int n_tokens, int hidden, int ac
   float* scratch = nullptr;
   int rc = scratch_for_current_device(&scratch);
   if (rc) return rc;
-  float* WgT = scratch;
+  float* WgQ = scratch;
   float* logits = scratch + AFD_NOALLOC_MAX_ROUTER_WEIGHTS;
   int32_t* status =
       reinterpret_cast<int32_t*>(scratch + AFD_NOALLOC_MAX_ROUTER_WEIGHTS + AFD_NOALLOC_MAX_LOGITS);
@@ -81,7 +81,7 @@ extern "C" int afd_route_noalloc(const void* x, int n_tokens, int hidden, int ac
     cudaGetLastError();
     return AFD_ERR_CUDA;
   }
-  if (launch_transpose_wg(lc, Wg, WgT, hidden, num_experts) != cudaSuccess) return AFD_ERR_CUDA;
+  if (launch_arrange_wg(lc, Wg, WgQ, hidden, num_experts) != cudaSuccess) return AFD_ERR_CUDA;
   // the activations are one contiguous [n_tokens, hidden] block: a single
   // "peer" whose rows start at x
   FanIn f;
@@ -99,7 +99,7 @@ extern "C" int afd_route_noalloc(const void* x, int n_tokens, int hidden, int ac
   ws.ids = ids;
   ws.w = weights;
   if (launch_router(lc, g, static_cast<const uint8_t*>(x), f, ws, hidden,
-                    act_dtype == AFD_DTYPE_F32, WgT, bias, num_experts, topk, renorm,
+                    act_dtype == AFD_DTYPE_F32, WgQ, bias, num_experts, topk, renorm,
                     routed_scaling, logits, /*hist=*/nullptr) != cudaSuccess)
     return AFD_ERR_CUDA;
   return AFD_OK;

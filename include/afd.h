@@ -213,8 +213,9 @@ int afd_split_sizes(int total, int n_peers, const int* seq_lens, int n_lens, int
  *   W13_s act [2*shared_inter, hidden], Wd_s act [hidden, shared_inter]
  *        (both NULL when shared_inter == 0)
  * All device pointers, caller-owned, must stay valid while the layer is
- * used; 16-byte aligned.  The library keeps a transposed fp32 copy of Wg
- * (the only weight copy) and the TMA descriptors.  Errors: AFD_ERR_ARG,
+ * used; 16-byte aligned.  The library keeps an fp32 copy of Wg rearranged
+ * as [ceil(E / 4)][hidden][4 experts] (the only weight copy) and the TMA
+ * descriptors.  Errors: AFD_ERR_ARG,
  * AFD_ERR_NOT_DEVICE, AFD_ERR_CUDA. */
 int afd_set_layer(afd_ctx* ctx, int layer, const float* Wg, const float* bias,
                   const void* W13, const void* Wd, const void* W13_s, const void* Wd_s);
@@ -312,14 +313,14 @@ int afd_stage_times(afd_ctx* ctx, float* ms, int n, int64_t* forwards);
  *   ids      device int32 [n_tokens, topk] out; weights device fp32
  *            [n_tokens, topk] out
  *   cuda_stream  cudaStream_t the work is ordered on (NULL = legacy stream)
- * Its scratch (the transposed router weight, the router logits and a
- * status word) is a file-scope device array of
+ * Its scratch (the router weight rearranged as [ceil(E / 4)][hidden][4],
+ * the router logits and a status word) is a file-scope device array of
  * AFD_NOALLOC_MAX_ROUTER_WEIGHTS + AFD_NOALLOC_MAX_LOGITS + 64 floats
  * (about 5 MiB) that every GPU loading this library holds until exit; the
- * first call on a device looks up that array's device address, so make the
- * first call on each device before any stream capture.  All calls share
- * the array: each call rewrites it and clears the status word first, and
- * calls that overlap on the GPU race on it.  hidden * num_experts above
+ * first call on a device looks up that array's device address.  All calls
+ * share the array: each call rewrites it and clears the status word first,
+ * and calls that overlap on the GPU race on it.
+ * 4 * ceil(num_experts / 4) * hidden above
  * AFD_NOALLOC_MAX_ROUTER_WEIGHTS or n_tokens * num_experts above
  * AFD_NOALLOC_MAX_LOGITS returns AFD_ERR_CAPACITY; bad arguments
  * AFD_ERR_ARG; a failing CUDA call AFD_ERR_CUDA.  Asynchronous; allocates

@@ -1007,18 +1007,28 @@ k_plan_scan(FanIn f, DevWS ws, int E, int k, int inter, int shared_inter, int hi
   __syncthreads();
   if (skip) return;
   for (int e = warp; e < E; e += kScanWarps) {
+    const int32_t* hrow = hist + (int64_t)e * nblocks;
+    int32_t* brow = base + (int64_t)e * nblocks;
     int running = 0;
-    for (int b0 = 0; b0 < nblocks; b0 += 32) {
-      const int b = b0 + lane;
-      const int v = b < nblocks ? hist[(int64_t)e * nblocks + b] : 0;
-      int incl = v;
+    for (int b0 = 0; b0 < nblocks; b0 += 32 * 8) {
+      int v[8];  // 8 loads in flight before the scans
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
+      for (int u = 0; u < 8; u++) {
+        const int b = b0 + 32 * u + lane;
+        v[u] = b < nblocks ? hrow[b] : 0;
       }
-      if (b < nblocks) base[(int64_t)e * nblocks + b] = running + incl - v;
-      running += __shfl_sync(0xffffffffu, incl, 31);
+#pragma unroll
+      for (int u = 0; u < 8; u++) {
+        int incl = v[u];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int o = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += o;
+        }
+        const int b = b0 + 32 * u + lane;
+        if (b < nblocks) brow[b] = running + incl - v[u];
+        running += __shfl_sync(0xffffffffu, incl, 31);
+      }
     }
     if (lane == 0) cnt[e] = running;
   }

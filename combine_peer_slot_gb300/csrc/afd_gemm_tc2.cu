@@ -94,6 +94,11 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+__device__ __forceinline__ int ld_cluster_s32(uint32_t cluster_addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
@@ -236,9 +241,11 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
   }
   __syncthreads();
   const int total = plan.total_units;
-  // both CTAs of a pair take the same decision: same status, same cluster id
-  if (tail->skip || total <= cid) return;
-  cluster_sync();  // the peer's barriers are initialised before any remote signal
+  cluster_sync();  // the peer's barriers and skip flag are initialised before any remote access
+  // both CTAs of a pair take the same decision: each ORs its own flag with the peer's
+  const int peer_skip = ld_cluster_s32(map_to_rank(smem_u32(&tail->skip), rank ^ 1u));
+  cluster_sync();  // both flags read before either CTA may leave
+  if (tail->skip || peer_skip || total <= cid) return;
 
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(

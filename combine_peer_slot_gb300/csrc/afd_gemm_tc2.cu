@@ -162,6 +162,7 @@ struct Unit {
   int group, kind, mpair, nt, rows, n_mma;
 };
 
+template <bool kNarrow>
 __device__ __forceinline__ Unit decode_unit(const GemmPlan& p, int unit) {
   int lo = 0, hi = p.ngroups - 1;
   while (lo < hi) {  // last group with unit0 <= unit (empty groups share unit0 with the next)
@@ -173,10 +174,19 @@ __device__ __forceinline__ Unit decode_unit(const GemmPlan& p, int unit) {
   Unit t;
   t.group = lo;
   t.kind = G.kind;
-  // token tiles vary fastest: units sharing a weight tile run on
-  // neighbouring clusters, so a weight tile read twice hits L2 the second time
-  t.nt = u % G.n_tiles;
-  t.mpair = u / G.n_tiles;
+  if (kNarrow) {
+    // decode-sized groups stream their weights from HBM: token tiles vary
+    // fastest, so the units sharing a weight tile run on neighbouring
+    // clusters and the second read of the tile hits L2
+    t.nt = u % G.n_tiles;
+    t.mpair = u / G.n_tiles;
+  } else {
+    // prefill: weight row pairs vary fastest, so the clusters running at
+    // once share one token tile (read from HBM once, then from L2)
+    const int m_pairs = (G.m_tiles + 1) / 2;
+    t.mpair = u % m_pairs;
+    t.nt = u / m_pairs;
+  }
   t.rows = min(p.bn, G.rows - t.nt * p.bn);
   t.n_mma = (t.rows + 31) & ~31;    // even halves of 16-row multiples
   return t;
@@ -267,7 +277,7 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
       int s = 0;
       uint32_t ph = 0;
       for (int unit = cid; unit < total; unit += ncl) {
-        const Unit t = decode_unit(plan, unit);
+        const Unit t = decode_unit<kNarrow>(plan, unit);
         const GemmGroup& G = plan.g[t.group];
         const int nkb = (args.K[t.kind] + BK - 1) / BK;
         // one token box per CTA and k-block: 128 rows, or 32 rows when the
@@ -310,7 +320,7 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
       uint32_t acc_ph = 0;
       bool ok = true;
       for (int unit = cid; unit < total && ok; unit += ncl) {
-        const Unit t = decode_unit(plan, unit);
+        const Unit t = decode_unit<kNarrow>(plan, unit);
         const int nkb = (args.K[t.kind] + BK - 1) / BK;
         const uint32_t idesc = idesc_pair(t.n_mma);
         if (!wait_bar(smem_u32(&tail->tempty[acc]), acc_ph ^ 1, abort_flag, deadline, args.status)) { ok = false; break; }
@@ -352,7 +362,7 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
     int acc = 0;
     uint32_t acc_ph = 0;
     for (int unit = cid; unit < total; unit += ncl) {
-      const Unit t = decode_unit(plan, unit);
+      const Unit t = decode_unit<kNarrow>(plan, unit);
       const GemmGroup& G = plan.g[t.group];
       bool ok = wait_bar(smem_u32(&tail->tfull[acc]), acc_ph, abort_flag, deadline, args.status);
       ok = __all_sync(0xffffffffu, ok);

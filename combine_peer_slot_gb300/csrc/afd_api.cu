@@ -7,6 +7,8 @@
 #include <cstring>
 #include <vector>
 
+#include <algorithm>
+
 #include "afd_internal.cuh"
 
 size_t gemm_tc_smem_bytes();
@@ -157,6 +159,8 @@ struct afd_ctx {
   int device = 0;
   int num_sms = 0;
   cudaStream_t stream = nullptr;
+  cudaStream_t side = nullptr;       // L2 weight prefetch beside the small kernels
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   uint8_t* win[2] = {nullptr, nullptr};
   uint8_t* ws_mem = nullptr;
   int64_t ws_bytes = 0;
@@ -272,6 +276,12 @@ void afd_destroy(afd_ctx* ctx) {
   if (!ctx) return;
   cudaSetDevice(ctx->device);
   cudaStreamSynchronize(ctx->stream);
+  if (ctx->side) {
+    cudaStreamSynchronize(ctx->side);
+    cudaStreamDestroy(ctx->side);
+  }
+  if (ctx->ev_fork) cudaEventDestroy(ctx->ev_fork);
+  if (ctx->ev_join) cudaEventDestroy(ctx->ev_join);
   for (auto& l : ctx->layers) cudaFree(l.WgQ);
   for (auto& set : ctx->ev)
     for (auto& e : set)
@@ -303,6 +313,12 @@ int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out) {
                     c->L.routed_x, c->L.shared_idx, c->L.shared_x, cfg->ring_depth, cfg->num_peers};
   c->tmax = cfg->max_total_tokens ? cfg->max_total_tokens : cfg->num_peers * cfg->token_cap;
   c->layers.resize(cfg->max_layers);
+  if (cfg->gemm == AFD_GEMM_TENSOR) {
+    rc = cuda_fail(cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking), "side stream");
+    if (!rc) rc = cuda_fail(cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming), "event");
+    if (!rc) rc = cuda_fail(cudaEventCreateWithFlags(&c->ev_join, cudaEventDisableTiming), "event");
+    if (rc) { afd_destroy(c); return rc; }
+  }
   c->last_seq.assign((size_t)cfg->num_peers * cfg->ring_depth, 0);
   for (int d = 0; d < 2; d++) {
     rc = cuda_fail(cudaMalloc(&c->win[d], c->L.window_bytes), "window allocation");
@@ -505,8 +521,21 @@ int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, con
       c.gemm == AFD_GEMM_TENSOR && T * c.topk <= 48 * (int64_t)c.num_experts ? 64 : 256;
   LaunchCtx lc = ctx->lc();
   const DevWS& ws = ctx->ws;
+  // decode-sized fan-ins: the SwiGLU GEMM streams its weights from HBM while
+  // the small kernels before it leave HBM idle, so a side stream prefetches
+  // the weights of the GEMM's first wave of units (experts in order, one
+  // 256-row unit per SM pair) into L2 meanwhile; joined at the end
+  const bool prefetch = c.gemm == AFD_GEMM_TENSOR && bn == 64 && T > 0;
+  int rc = AFD_OK;
+  struct Join {  // the main stream waits for the side stream on every way out
+    afd_ctx* ctx;
+    bool armed = false;
+    ~Join() {
+      if (armed) cudaStreamWaitEvent(ctx->stream, ctx->ev_join, 0);
+    }
+  } join{ctx};
   ctx->mark(0);
-  int rc = cuda_fail(launch_header_check(lc, ctx->geom, ctx->win[0], f, ws, c.num_experts,
+  rc = cuda_fail(launch_header_check(lc, ctx->geom, ctx->win[0], f, ws, c.num_experts,
                                          c.token_cap, has_shared, ctx->timeout()),
                      "header check");
   if (rc) return rc;
@@ -516,6 +545,19 @@ int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, con
                                ws.logits, ws.hist),
                  "router");
   if (rc) return rc;
+  if (prefetch) {
+    const int64_t first_wave = (int64_t)(ctx->num_sms / 2) * 256 * c.hidden * 2;
+    const int64_t w13 = (int64_t)c.num_experts * 2 * c.inter * c.hidden * 2;
+    LaunchCtx side = lc;
+    side.stream = ctx->side;
+    side.pdl = 0;
+    rc = cuda_fail(cudaEventRecord(ctx->ev_fork, ctx->stream), "fork");
+    if (!rc) rc = cuda_fail(cudaStreamWaitEvent(ctx->side, ctx->ev_fork, 0), "fork");
+    if (!rc) rc = cuda_fail(launch_prefetch_l2(side, L.W13, std::min(first_wave, w13)), "prefetch");
+    if (!rc) rc = cuda_fail(cudaEventRecord(ctx->ev_join, ctx->side), "join");
+    if (rc) return rc;
+    join.armed = true;
+  }
   ctx->mark(2);
   rc = cuda_fail(launch_plan(lc, f, ws, c.num_experts, c.topk, c.inter, c.shared_inter, c.hidden,
                              has_shared, bn, ctx->plan1, ctx->plan2, ws.hist, ws.base),

@@ -317,5 +317,7 @@ cudaError_t launch_return_header(const LaunchCtx& lc, const WinGeom& g, uint8_t*
 cudaError_t launch_unpack(const LaunchCtx& lc, const WinGeom& g, const uint8_t* ret, int region,
                           int stage, void* out, int n, int row_bytes, int num_experts,
                           uint64_t expect_seq, int32_t* status, int64_t timeout_ns);
+// bytes: a multiple of 16 from a 16-byte aligned base
+cudaError_t launch_prefetch_l2(const LaunchCtx& lc, const void* base, int64_t bytes);
 cudaError_t launch_arrange_wg(const LaunchCtx& lc, const float* Wg, float* WgQ, int hidden,
                                 int E);

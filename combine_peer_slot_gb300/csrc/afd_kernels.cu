@@ -1449,6 +1449,20 @@ k_unpack(const uint8_t* ret, WinGeom g, int region, int stage, uint4* out, int n
     out[v] = src[v];
 }
 
+// L2 prefetch of a contiguous byte range (weights the next GEMM reads first):
+// 64 KB bulk prefetches spread over the grid; returns as soon as they are issued.
+__global__ void k_prefetch_l2(const uint8_t* base, int64_t bytes) {
+  grid_dep_wait();
+  grid_dep_launch();
+  constexpr int64_t kChunk = 65536;
+  const int64_t n = (bytes + kChunk - 1) / kChunk;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t len = min(kChunk, bytes - i * kChunk);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + i * kChunk), "r"((uint32_t)len)
+                 : "memory");
+  }
+}
+
 // The router weight [hidden][E] rearranged for the logits kernels as
 // WgQ[E/4 groups][hidden][4 experts] fp32 (experts past E are zero): a lane
 // reads the 4 weights of its h for a group of experts with one 16-byte load.
@@ -1686,6 +1700,11 @@ cudaError_t launch_unpack(const LaunchCtx& lc, const WinGeom& g, const uint8_t* 
   return launch_k(lc, k_unpack, grid_for(nvec, kThreads * 4, lc.num_sms * 4), kThreads, 0, ret, g,
                   region, stage, reinterpret_cast<uint4*>(out), n, row_bytes, num_experts,
                   expect_seq, status, timeout_ns);
+}
+
+cudaError_t launch_prefetch_l2(const LaunchCtx& lc, const void* base, int64_t bytes) {
+  if (bytes <= 0) return cudaSuccess;
+  return launch_k(lc, k_prefetch_l2, lc.num_sms, 32, 0, static_cast<const uint8_t*>(base), bytes);
 }
 
 cudaError_t launch_arrange_wg(const LaunchCtx& lc, const float* Wg, float* WgQ, int hidden,

@@ -1276,7 +1276,7 @@ __global__ void __launch_bounds__(kThreads) k_gemm_simt(SimtArgs a) {
 // its local row; the route_table row gets the chosen ids.  Deterministic:
 // each output element is reduced by one thread in a fixed order.
 // ---------------------------------------------------------------------------
-template <bool ACT_F32, bool Y_F32>
+template <bool ACT_F32, bool Y_F32, int kBatch>
 __global__ void __launch_bounds__(kThreads)
 k_combine(uint8_t* ret, WinGeom g, FanIn f, DevWS ws, int hidden, int k, int has_shared) {
   grid_dep_wait();
@@ -1312,30 +1312,78 @@ k_combine(uint8_t* ret, WinGeom g, FanIn f, DevWS ws, int hidden, int k, int has
       float acc[kVec];
 #pragma unroll
       for (int q = 0; q < kVec; q++) acc[q] = 0.0f;
-      for (int j = 0; j < k; j++) {
-        const int pos = __shfl_sync(0xffffffffu, my_pos, j);
-        const float wj = __shfl_sync(0xffffffffu, my_w, j);
-        float yv[kVec];
-        if constexpr (Y_F32) {
-          const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(ws.y) +
-                                                              (int64_t)pos * hidden + c);
-          const float4 a = valid ? src[0] : make_float4(0.f, 0.f, 0.f, 0.f);
-          const float4 b = valid ? src[1] : make_float4(0.f, 0.f, 0.f, 0.f);
-          yv[0] = a.x; yv[1] = a.y; yv[2] = a.z; yv[3] = a.w;
-          yv[4] = b.x; yv[5] = b.y; yv[6] = b.z; yv[7] = b.w;
-        } else {
-          const uint4 v = valid ? *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(ws.y) +
-                                                                 (int64_t)pos * hidden + c)
-                                : make_uint4(0, 0, 0, 0);
-          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+      if constexpr (kBatch == 1) {
+        for (int j = 0; j < k; j++) {
+          const int pos = __shfl_sync(0xffffffffu, my_pos, j);
+          const float wj = __shfl_sync(0xffffffffu, my_w, j);
+          float yv[kVec];
+          if constexpr (Y_F32) {
+            const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(ws.y) +
+                                                                (int64_t)pos * hidden + c);
+            const float4 a = valid ? src[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 b = valid ? src[1] : make_float4(0.f, 0.f, 0.f, 0.f);
+            yv[0] = a.x; yv[1] = a.y; yv[2] = a.z; yv[3] = a.w;
+            yv[4] = b.x; yv[5] = b.y; yv[6] = b.z; yv[7] = b.w;
+          } else {
+            const uint4 v = valid ? *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(ws.y) +
+                                                                   (int64_t)pos * hidden + c)
+                                  : make_uint4(0, 0, 0, 0);
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int m = 0; m < 4; m++) {
-            yv[2 * m] = __uint_as_float(w4[m] << 16);
-            yv[2 * m + 1] = __uint_as_float(w4[m] & 0xffff0000u);
+            for (int m = 0; m < 4; m++) {
+              yv[2 * m] = __uint_as_float(w4[m] << 16);
+              yv[2 * m + 1] = __uint_as_float(w4[m] & 0xffff0000u);
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < kVec; q++) acc[q] = __fmaf_rn(wj, yv[q], acc[q]);
+        }
+      } else {
+        // rounds of up to kBatch partials: their rows are all loaded before the
+        // multiply-adds, which still run in ascending j (kBatch > 1 for small
+        // fan-ins, where few warps must keep many loads in flight; 1 keeps the
+        // registers low and the SM full for large ones)
+        for (int j0 = 0; j0 < k; j0 += kBatch) {
+          uint4 raw[kBatch][Y_F32 ? 2 : 1];
+          float wj[kBatch];
+  #pragma unroll
+          for (int u = 0; u < kBatch; u++) {
+            const int j = j0 + u;
+            const int pos = __shfl_sync(0xffffffffu, my_pos, j & 31);
+            wj[u] = __shfl_sync(0xffffffffu, my_w, j & 31);
+            const bool ld = valid && j < k;
+            if constexpr (Y_F32) {
+              const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const float*>(ws.y) +
+                                                                (int64_t)pos * hidden + c);
+              raw[u][0] = ld ? src[0] : make_uint4(0, 0, 0, 0);
+              raw[u][1] = ld ? src[1] : make_uint4(0, 0, 0, 0);
+            } else {
+              raw[u][0] = ld ? *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(ws.y) +
+                                                               (int64_t)pos * hidden + c)
+                             : make_uint4(0, 0, 0, 0);
+            }
+          }
+  #pragma unroll
+          for (int u = 0; u < kBatch; u++) {
+            if (j0 + u >= k) break;
+            float yv[kVec];
+            if constexpr (Y_F32) {
+              yv[0] = __uint_as_float(raw[u][0].x); yv[1] = __uint_as_float(raw[u][0].y);
+              yv[2] = __uint_as_float(raw[u][0].z); yv[3] = __uint_as_float(raw[u][0].w);
+              yv[4] = __uint_as_float(raw[u][1].x); yv[5] = __uint_as_float(raw[u][1].y);
+              yv[6] = __uint_as_float(raw[u][1].z); yv[7] = __uint_as_float(raw[u][1].w);
+            } else {
+              const uint32_t w4[4] = {raw[u][0].x, raw[u][0].y, raw[u][0].z, raw[u][0].w};
+  #pragma unroll
+              for (int m = 0; m < 4; m++) {
+                yv[2 * m] = __uint_as_float(w4[m] << 16);
+                yv[2 * m + 1] = __uint_as_float(w4[m] & 0xffff0000u);
+              }
+            }
+  #pragma unroll
+            for (int q = 0; q < kVec; q++) acc[q] = __fmaf_rn(wj[u], yv[q], acc[q]);
           }
         }
-#pragma unroll
-        for (int q = 0; q < kVec; q++) acc[q] = __fmaf_rn(wj, yv[q], acc[q]);
       }
       if (valid) {  // lanes past hidden write nothing
         if (has_shared) {
@@ -1678,13 +1726,16 @@ cudaError_t launch_combine(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret, 
   if (f.total == 0) return cudaSuccess;
   const int64_t items = (int64_t)f.total * ((hidden + 255) / 256);
   const int grid = grid_for(items, kThreads / 32, lc.num_sms * 8);
+  const bool small = items < (int64_t)lc.num_sms * 64;
   if (act_f32 && y_f32)
-    return launch_k(lc, k_combine<true, true>, grid, kThreads, 0, ret, g, f, ws, hidden, k, has_shared);
+    return launch_k(lc, k_combine<true, true, 1>, grid, kThreads, 0, ret, g, f, ws, hidden, k, has_shared);
   if (!act_f32 && y_f32)
-    return launch_k(lc, k_combine<false, true>, grid, kThreads, 0, ret, g, f, ws, hidden, k, has_shared);
+    return launch_k(lc, k_combine<false, true, 1>, grid, kThreads, 0, ret, g, f, ws, hidden, k, has_shared);
   if (!act_f32 && !y_f32)
-    return launch_k(lc, k_combine<false, false>, grid, kThreads, 0, ret, g, f, ws, hidden, k,
-                    has_shared);
+    return small ? launch_k(lc, k_combine<false, false, 8>, grid, kThreads, 0, ret, g, f, ws, hidden, k,
+                            has_shared)
+                 : launch_k(lc, k_combine<false, false, 1>, grid, kThreads, 0, ret, g, f, ws, hidden, k,
+                            has_shared);
   return cudaErrorInvalidValue;
 }
 

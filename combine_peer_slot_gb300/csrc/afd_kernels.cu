@@ -874,7 +874,7 @@ k_router_logits_tw2(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int hidden
 // a1 router, part 2: top-k on the logits (ties -> lower expert index, NaN
 // below every number) and the gate weights from a softmax over all E
 // (sums carried as float-float); one warp per token, 16 tokens per CTA,
-// whose per-expert histogram (hist[e][cta]) feeds the plan.
+// whose per-expert histogram (hist[cta][e]) feeds the plan.
 __global__ void __launch_bounds__(kRtTok * 32)
 k_router_topk(FanIn f, DevWS ws, const float* __restrict__ logits, int E, int k, int renorm,
               float scale, int32_t* __restrict__ hist, int nblocks) {
@@ -934,15 +934,15 @@ k_router_topk(FanIn f, DevWS ws, const float* __restrict__ logits, int E, int k,
     }
   }
   __syncthreads();
-  if (hist)
-    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(int64_t)e * nblocks + blockIdx.x] = hs[e];
+  if (hist)  // block-major: hist[cta][e]
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(int64_t)blockIdx.x * E + e] = hs[e];
 }
 
 // ---------------------------------------------------------------------------
 // a2 plan, part 1 (one CTA): per-expert counts and exclusive offsets from the
 // router CTAs' histograms (bincount + cumsum, Async GPU Connector, "Data
 // flow" step 1), each router CTA's base position within each expert's
-// segment (base[e][b] = sum of hist[e][b'] for b' < b), the zeroed per-peer
+// segment (base[b][e] = sum of hist[b'][e] for b' < b), the zeroed per-peer
 // counts, and the tile tables of both grouped GEMMs.
 // ---------------------------------------------------------------------------
 // Tile tables of both grouped GEMMs from the per-expert counts and offsets:
@@ -992,6 +992,7 @@ __device__ void write_tile_tables(const FanIn& f, int k, int E, int inter, int s
 }
 
 constexpr int kScanWarps = 32;
+constexpr int kScanSegs = kScanWarps * 32 / 64;  // 16 segments x 64 experts per pass
 
 __global__ void __launch_bounds__(kScanWarps * 32)
 k_plan_scan(FanIn f, DevWS ws, int E, int k, int inter, int shared_inter, int hidden,
@@ -1006,31 +1007,39 @@ k_plan_scan(FanIn f, DevWS ws, int E, int k, int inter, int shared_inter, int hi
   if (tid == 0) skip = read_status(ws.status);
   __syncthreads();
   if (skip) return;
-  for (int e = warp; e < E; e += kScanWarps) {
-    const int32_t* hrow = hist + (int64_t)e * nblocks;
-    int32_t* brow = base + (int64_t)e * nblocks;
-    int running = 0;
-    for (int b0 = 0; b0 < nblocks; b0 += 32 * 8) {
-      int v[8];  // 8 loads in flight before the scans
+  // 64 experts per pass; thread = (segment sg of the router CTAs, expert),
+  // so a warp's loads of one CTA's histogram row are contiguous
+  __shared__ int seg_sum[kScanSegs][64];
+  const int sg = tid / 64, el = tid % 64;
+  const int L = (nblocks + kScanSegs - 1) / kScanSegs;
+  const int b_lo = min(nblocks, sg * L), b_hi = min(nblocks, b_lo + L);
+  for (int e0 = 0; e0 < E; e0 += 64) {
+    const int e = e0 + el;
+    int sum = 0;
+    if (e < E) {
+      int b = b_lo;
+      for (; b + 8 <= b_hi; b += 8) {  // 8 loads in flight
+        int v[8];
 #pragma unroll
-      for (int u = 0; u < 8; u++) {
-        const int b = b0 + 32 * u + lane;
-        v[u] = b < nblocks ? hrow[b] : 0;
+        for (int u = 0; u < 8; u++) v[u] = hist[(int64_t)(b + u) * E + e];
+#pragma unroll
+        for (int u = 0; u < 8; u++) sum += v[u];
       }
-#pragma unroll
-      for (int u = 0; u < 8; u++) {
-        int incl = v[u];
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const int o = __shfl_up_sync(0xffffffffu, incl, off);
-          if (lane >= off) incl += o;
-        }
-        const int b = b0 + 32 * u + lane;
-        if (b < nblocks) brow[b] = running + incl - v[u];
-        running += __shfl_sync(0xffffffffu, incl, 31);
-      }
+      for (; b < b_hi; b++) sum += hist[(int64_t)b * E + e];
     }
-    if (lane == 0) cnt[e] = running;
+    seg_sum[sg][el] = sum;
+    __syncthreads();
+    int run = 0;
+    for (int q = 0; q < sg; q++) run += seg_sum[q][el];
+    if (e < E) {
+      for (int b = b_lo; b < b_hi; b++) {
+        const int v = hist[(int64_t)b * E + e];
+        base[(int64_t)b * E + e] = run;
+        run += v;
+      }
+      if (sg == kScanSegs - 1) cnt[e] = run;
+    }
+    __syncthreads();
   }
   for (int i = tid; i < f.n_peers * E; i += blockDim.x) ws.peer_counts[i] = 0;
   __syncthreads();
@@ -1136,7 +1145,7 @@ k_plan_small(FanIn f, DevWS ws, int E, int k, int inter, int shared_inter, int h
 // a3 plan, part 2: the stable permutation.  One warp per router CTA's range
 // of partials f (16 tokens x k, contiguous in f): rank among earlier
 // partials of the same expert in the range (match_any per 32-element round
-// plus running per-expert counts), position = offsets[e] + base[e][b] +
+// plus running per-expert counts), position = offsets[e] + base[b][e] +
 // rank.  Equal to argsort(stable=True) of the flattened ids.  Also the
 // per-peer expert counts of the return headers.
 // ---------------------------------------------------------------------------
@@ -1151,8 +1160,9 @@ k_rank(FanIn f, DevWS ws, int E, int k, const int32_t* __restrict__ base, int nb
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.x * kRankWarps + warp;
   if (b >= nblocks) return;
+  // run[e]: next position for expert e in this block = offsets[e] + base[b][e]
   int* run = run_s[warp];
-  for (int e = lane; e < E; e += 32) run[e] = 0;
+  for (int e = lane; e < E; e += 32) run[e] = ws.offsets[e] + base[(int64_t)b * E + e];
   __syncwarp();
   const int N = f.total * k;
   const int f0 = b * kRtTok * k, f1 = min(N, f0 + kRtTok * k);
@@ -1168,7 +1178,7 @@ k_rank(FanIn f, DevWS ws, int E, int k, const int32_t* __restrict__ base, int nb
     const unsigned same = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(same & lt_mask);
     int pos = 0;
-    if (ok) pos = ws.offsets[e] + base[(int64_t)e * nblocks + b] + run[e] + rank;
+    if (ok) pos = run[e] + rank;
     __syncwarp();
     if (ok && rank == 0) run[e] += __popc(same);
     __syncwarp();

@@ -2,7 +2,9 @@
  * afd_oracle.c -- plain, slow CPU oracle for the FFN side of Attention-FFN
  * Disaggregation (AFD): fan-in of peer slots, softmax top-k router, stable
  * per-expert permutation, routed + shared SwiGLU experts, top-k weighted
- * combine and the per-peer split back into return slots.
+ * combine and the per-peer split back into return slots; and the grouped
+ * form, where the Attention side has routed and the FFN runs each received
+ * row through its expert (top-1, unit weight).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may call, link or
  * load this file.  Only tests/, __graft_entry__.smoke() and bench.py's CPU
@@ -793,6 +795,198 @@ void orc_combine(const double* y, const float* w, const double* s, int T, int k,
       if (s) a += s[(int64_t)t * hidden + f];
       out[(int64_t)t * hidden + f] = a;
     }
+}
+
+/* ------------------------------------------------------------------------ */
+/* the Attention-side gate: routed rows arrive already grouped by expert      */
+/* ------------------------------------------------------------------------ */
+
+/* Dispatch slot of the grouped form ([RFC-GPU] "Data flow" steps 1-3: the
+ * Attention side routes, sorts the flattened top-k ids stably and sends the
+ * routed rows grouped by expert, with the per-expert row counts (group_list)
+ * in the header; the shared rows travel as in the token form).  routed_x =
+ * the R rows in group order, expert_counts = group_list (sum R),
+ * routed_tokens = R, num_tokens = the peer's n tokens, shared_x = the n token
+ * rows with shared_idx = 0..n-1 when with_shared.  Payload, then header, then
+ * the flag.  Parity: the round trip and the combine identity below. */
+int orc_pack_grouped(uint8_t* win, const orc_layout* L, int ring_depth, int region,
+                     int stage, int layer, const void* rows, int R, const int* group_list,
+                     const void* x, int n_tokens, int hidden, int act_bytes, int token_cap,
+                     int num_experts, int with_shared, int has_shared, uint64_t seq) {
+  if (n_tokens < 0 || n_tokens > token_cap || R < 0 || R > token_cap) return ORC_ERR_CAPACITY;
+  if (with_shared && !has_shared) return ORC_ERR_ARG;
+  int64_t sum = 0;
+  for (int e = 0; e < num_experts; e++) {
+    if (group_list[e] < 0) return ORC_ERR_ARG;
+    sum += group_list[e];
+  }
+  if (sum != R) return ORC_ERR_SHAPE;
+  uint8_t* s = orc_slot(win, L, region, stage, ring_depth);
+  int64_t row = (int64_t)hidden * act_bytes;
+  if (R) memcpy(s + L->routed_x, rows, (size_t)(R * row));
+  if (with_shared) {
+    int32_t* sidx = (int32_t*)(s + L->shared_idx);
+    for (int i = 0; i < n_tokens; i++) sidx[i] = i;
+    if (n_tokens) memcpy(s + L->shared_x, x, (size_t)(n_tokens * row));
+  }
+  int32_t* h = (int32_t*)(s + L->header);
+  memset(h, 0, (size_t)(H_FIXED_WORDS + num_experts) * 4);
+  h[H_MAGIC] = (int32_t)ORC_MAGIC;
+  h[H_VERSION] = ORC_VERSION;
+  h[H_SEQ] = (int32_t)(uint32_t)seq;
+  h[H_ECHO_SEQ] = (int32_t)(uint32_t)seq;
+  h[H_LAYER] = layer;
+  h[H_STAGE] = stage;
+  h[H_NUM_TOKENS] = n_tokens;
+  h[H_ROUTED_TOKENS] = R;
+  h[H_SHARED_TOKENS] = with_shared ? n_tokens : 0;
+  h[H_NUM_EXPERTS] = num_experts;
+  h[H_LEN] = H_FIXED_WORDS + num_experts;
+  for (int e = 0; e < num_experts; e++) h[H_FIXED_WORDS + e] = group_list[e];
+  *orc_flag(win, region, stage, ring_depth) = seq;
+  return ORC_OK;
+}
+
+/* Header check of a grouped dispatch slot: the common fields in the order of
+ * orc_check_slot, then num_tokens == n, routed_tokens == R (both within the
+ * slot's token_cap rows), expert_counts summing to R, shared rows 0 or n with
+ * shared_idx = 0..n-1. */
+static int orc_check_grouped(const orc_cfg* c, uint8_t* win, const orc_layout* L, int region,
+                             int stage, int layer, int R, int n, uint64_t seen) {
+  uint64_t f = *orc_flag(win, region, stage, c->ring_depth);
+  if (f <= seen) return ORC_ERR_TIMEOUT;
+  const uint8_t* s = orc_slot(win, L, region, stage, c->ring_depth);
+  const int32_t* h = (const int32_t*)(s + L->header);
+  if ((uint32_t)h[H_MAGIC] != ORC_MAGIC || h[H_VERSION] != ORC_VERSION ||
+      h[H_NUM_EXPERTS] != c->num_experts || h[H_LEN] != H_FIXED_WORDS + c->num_experts)
+    return ORC_ERR_HEADER;
+  if ((uint32_t)h[H_SEQ] != (uint32_t)f || h[H_ECHO_SEQ] != h[H_SEQ]) return ORC_ERR_SEQ;
+  if (h[H_FLAGS] & ORC_FLAG_SHUTDOWN) return ORC_ERR_SHUTDOWN;
+  if (h[H_LAYER] != layer) return ORC_ERR_LAYER;
+  if (h[H_STAGE] != stage) return ORC_ERR_STAGE;
+  if (h[H_NUM_TOKENS] != n) return ORC_ERR_SHAPE;
+  if (h[H_NUM_TOKENS] > c->token_cap) return ORC_ERR_CAPACITY;
+  if (h[H_ROUTED_TOKENS] != R) return ORC_ERR_SHAPE;
+  if (h[H_ROUTED_TOKENS] > c->token_cap) return ORC_ERR_CAPACITY;
+  int64_t sum = 0;
+  for (int e = 0; e < c->num_experts; e++) {
+    if (h[H_FIXED_WORDS + e] < 0) return ORC_ERR_SHAPE;
+    sum += h[H_FIXED_WORDS + e];
+  }
+  if (sum != R) return ORC_ERR_SHAPE;
+  int st = h[H_SHARED_TOKENS];
+  if (st != 0 && (st != n || c->shared_inter <= 0)) return ORC_ERR_SHAPE;
+  if (st) {
+    const int32_t* sidx = (const int32_t*)(s + L->shared_idx);
+    for (int i = 0; i < st; i++) if (sidx[i] != i) return ORC_ERR_SHAPE;
+  }
+  return ORC_OK;
+}
+
+/* The FFN step of the grouped form ([RFC-GPU] "Attention gate and FFN expert
+ * compute": what arrives is already routed and grouped, so the FFN must not
+ * route again; every row gets the expert id expanded from group_list and a
+ * unit weight, i.e. a top-1 problem; the shared rows go through the shared
+ * expert as their own batch; [RFC-GPU] "Data flow" step 4: the gate weights
+ * stay on the Attention side, which weights and combines).  For each listed
+ * peer i: y_r = expert(e_r)(row r) for its R_i rows and s_t = shared(x_t) for
+ * its shared rows, in fp64, rounded once into the return slot (routed_x = the
+ * y rows in arrival order, shared_x = the s rows); header echoing seq, with
+ * routed_tokens = R_i, shared_tokens and expert_counts as received; then the
+ * return flag = seq.  The argument rules follow orc_check_args with rows
+ * (at most token_cap per peer) in place of tokens; the totals are bounded by
+ * max_total_tokens * topk rows and max_total_tokens tokens.  Optional
+ * outputs: y64 [sum R, hidden], s64 [sum n, hidden] (rows of the shared
+ * branch of peers without shared rows are zero).  Parity: pinned by the
+ * dense identity (E = 1) and by the combine identity with orc_ffn_forward. */
+int orc_grouped_forward(const orc_cfg* c, uint8_t* in_win, uint8_t* ret_win,
+                        const orc_weights* W, int layer, int stage, const int* rows,
+                        const int* seq_lens, const int* slots, int n_peers, uint64_t* seen,
+                        double* y64, double* s64, int nthreads) {
+  orc_layout L;
+  int rc = orc_slot_layout(c->num_regions, c->ring_depth, c->token_cap, c->topk,
+                           c->hidden, c->act_bytes, c->num_experts, c->shared_inter > 0, &L);
+  if (rc) return rc;
+  rc = orc_check_args(c, stage, seq_lens, slots, n_peers);
+  if (rc) return rc;
+  int64_t Rtot = 0;
+  for (int i = 0; i < n_peers; i++) {
+    if (rows[i] < 0) return ORC_ERR_ARG;
+    if (rows[i] > c->token_cap) return ORC_ERR_CAPACITY;
+    Rtot += rows[i];
+  }
+  int cap = c->max_total_tokens > 0 ? c->max_total_tokens : c->num_regions * c->token_cap;
+  if (Rtot > (int64_t)cap * c->topk) return ORC_ERR_CAPACITY;
+  for (int i = 0; i < n_peers; i++) {
+    rc = orc_check_grouped(c, in_win, &L, slots[i], stage, layer, rows[i], seq_lens[i],
+                           seen[(int64_t)slots[i] * c->ring_depth + stage]);
+    if (rc) return rc;
+  }
+  const int H = c->hidden, E = c->num_experts, ab = c->act_bytes;
+  int64_t e13 = (int64_t)2 * c->inter * H, ed = (int64_t)H * c->inter;
+  int64_t rbase = 0, tbase = 0;
+  for (int i = 0; i < n_peers; i++) {
+    int p = slots[i], R = rows[i], n = seq_lens[i];
+    const uint8_t* sin = orc_slot(in_win, &L, p, stage, c->ring_depth);
+    const int32_t* hin = (const int32_t*)(sin + L.header);
+    uint8_t* sout = orc_slot(ret_win, &L, p, stage, c->ring_depth);
+    const int shared = hin[H_SHARED_TOKENS] > 0;
+    /* expert of row r: the group of group_list holding it */
+    int* expert = (int*)malloc(sizeof(int) * (R + 1));
+    for (int e = 0, r = 0; e < E; e++)
+      for (int q = 0; q < hin[H_FIXED_WORDS + e]; q++) expert[r++] = e;
+    int nrows = R + (shared ? n : 0);
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int q = 0; q < nrows; q++) {
+      const int routed = q < R;
+      const int r = routed ? q : q - R;
+      const uint8_t* src = sin + (routed ? L.routed_x : L.shared_x);
+      double* x = (double*)malloc(sizeof(double) * H);
+      double* y = (double*)calloc((size_t)H, sizeof(double));
+      for (int h = 0; h < H; h++) x[h] = orc_ld(src, ab, (int64_t)r * H + h);
+      if (routed) {
+        int e = expert[r];
+        orc_swiglu_row(x, H, c->inter, (const char*)W->W13 + (int64_t)e * e13 * ab,
+                       (const char*)W->Wd + (int64_t)e * ed * ab, ab, 1.0, y, NULL);
+      } else {
+        orc_swiglu_row(x, H, c->shared_inter, W->W13s, W->Wds, ab, 1.0, y, NULL);
+      }
+      uint8_t* dst = sout + (routed ? L.routed_x : L.shared_x);
+      for (int h = 0; h < H; h++) {
+        if (ab == 2) ((uint16_t*)dst)[(int64_t)r * H + h] = orc_f64_to_bf16(y[h]);
+        else ((float*)dst)[(int64_t)r * H + h] = (float)y[h];
+      }
+      if (routed && y64) memcpy(y64 + (rbase + r) * H, y, sizeof(double) * H);
+      if (!routed && s64) memcpy(s64 + (tbase + r) * H, y, sizeof(double) * H);
+      free(x);
+      free(y);
+    }
+    if (s64 && !shared) memset(s64 + tbase * H, 0, sizeof(double) * (size_t)n * H);
+    free(expert);
+    uint64_t seq = *orc_flag(in_win, p, stage, c->ring_depth);
+    int32_t* h = (int32_t*)(sout + L.header);
+    memset(h, 0, (size_t)(H_FIXED_WORDS + E) * 4);
+    h[H_MAGIC] = (int32_t)ORC_MAGIC;
+    h[H_VERSION] = ORC_VERSION;
+    h[H_SEQ] = (int32_t)(uint32_t)seq;
+    h[H_ECHO_SEQ] = (int32_t)(uint32_t)seq;
+    h[H_LAYER] = layer;
+    h[H_STAGE] = stage;
+    h[H_NUM_TOKENS] = n;
+    h[H_ROUTED_TOKENS] = R;
+    h[H_SHARED_TOKENS] = hin[H_SHARED_TOKENS];
+    h[H_NUM_EXPERTS] = E;
+    h[H_LEN] = H_FIXED_WORDS + E;
+    for (int e = 0; e < E; e++) h[H_FIXED_WORDS + e] = hin[H_FIXED_WORDS + e];
+    *orc_flag(ret_win, p, stage, c->ring_depth) = seq;
+    seen[(int64_t)p * c->ring_depth + stage] = seq;
+    rbase += R;
+    tbase += n;
+  }
+  return ORC_OK;
 }
 
 int orc_num_threads(void) {

@@ -66,6 +66,8 @@ def load(path=None):
         "orc_ffn_forward": (I, [P, P, P, P, I, I, P, P, I, P, P, P, P, P, P, P, P, P, P, I]),
         "orc_forward_tokens": (I, [P, P, P, I, P, P, I, P, I, P, P, P, I]),
         "orc_combine": (V, [P, P, P, I, I, I, P]),
+        "orc_pack_grouped": (I, [P, P, I, I, I, I, P, I, P, P, I, I, I, I, I, I, I, U64]),
+        "orc_grouped_forward": (I, [P, P, P, P, I, I, P, P, P, I, P, P, P, I]),
         "orc_num_threads": (I, []),
     }
     for name, (res, args) in sig.items():
@@ -248,6 +250,40 @@ def ffn_forward(c, in_win, ret_win, Wdict, layer, stage, seq_lens, slots, seen,
     if want_h:
         r["h"] = h[:T]
     return rc, r
+
+
+def pack_grouped(win, L, ring_depth, region, stage, layer, rows, group_list, x, hidden,
+                 act_bytes, token_cap, num_experts, with_shared, has_shared, seq, lib=None):
+    """Grouped (Attention-side gate) dispatch: rows [R, hidden] grouped by
+    expert with group_list [E] rows per expert; x [n, hidden] the peer's
+    tokens (the shared rows)."""
+    lib = lib or load()
+    rows = np.ascontiguousarray(rows)
+    x = np.ascontiguousarray(x)
+    gl = np.ascontiguousarray(group_list, np.int32)
+    return lib.orc_pack_grouped(_p(win), C.byref(L), ring_depth, region, stage, layer,
+                                _p(rows), int(rows.shape[0]), _p(gl), _p(x), int(x.shape[0]),
+                                hidden, act_bytes, token_cap, num_experts, int(with_shared),
+                                int(has_shared), seq)
+
+
+def grouped_forward(c, in_win, ret_win, Wdict, layer, stage, rows, seq_lens, slots, seen,
+                    nthreads=0, lib=None):
+    """FFN step of the grouped form on host windows; returns (rc, y64 [sum R, H],
+    s64 [sum n, H])."""
+    lib = lib or load()
+    cfg = make_cfg(c)
+    W, keep = _weights(Wdict)
+    rw = np.ascontiguousarray(rows, np.int32)
+    sl = np.ascontiguousarray(seq_lens, np.int32)
+    sp = np.ascontiguousarray(slots, np.int32)
+    H = c["hidden"]
+    y = np.zeros((max(int(rw.sum()), 1), H), np.float64)
+    s = np.zeros((max(int(sl.sum()), 1), H), np.float64)
+    rc = lib.orc_grouped_forward(C.byref(cfg), _p(in_win), _p(ret_win), C.byref(W), layer, stage,
+                                 _p(rw), _p(sl), _p(sp), int(sl.size), _p(seen), _p(y), _p(s),
+                                 nthreads)
+    return rc, y[:int(rw.sum())], s[:int(sl.sum())]
 
 
 def forward_tokens(c, in_win, Wdict, stage, seq_lens, slots, tokens, nthreads=0,

@@ -416,7 +416,117 @@ def check_fault_codes(lib):
     assert fwd(win, seen=seen) == O.ERR_TIMEOUT
 
 
+def grouped_dispatch(ids, x, k, E):
+    """The Attention side's grouped send for one peer: the flattened top-k
+    ids sorted stably (numpy), the token rows in that order, bincount as the
+    group list.  Returns (rows, group_list, order) with order[r] = t*k + j."""
+    order = np.argsort(ids.reshape(-1), kind="stable")
+    rows = np.ascontiguousarray(x[order // k])
+    return rows, np.bincount(ids.reshape(-1), minlength=E).astype(np.int32), order
+
+
+def run_grouped(lib, cfg, xs, Wt, ids_per_peer, *, layer=0, stage=0, seqs=None,
+                with_shared=True):
+    L = O.slot_layout(cfg["num_regions"], cfg["ring_depth"], cfg["token_cap"], cfg["topk"],
+                      cfg["hidden"], cfg["act_bytes"], cfg["num_experts"],
+                      cfg["shared_inter"] > 0, lib=lib)
+    win = np.zeros(L.window_bytes, np.uint8)
+    ret = np.zeros(L.window_bytes, np.uint8)
+    seqs = seqs or [200 + i for i in range(len(xs))]
+    orders, R = [], []
+    for p, x in enumerate(xs):
+        rows, gl, order = grouped_dispatch(ids_per_peer[p], x, cfg["topk"], cfg["num_experts"])
+        rc = O.pack_grouped(win, L, cfg["ring_depth"], p, stage, layer, rows, gl, x,
+                            cfg["hidden"], cfg["act_bytes"], cfg["token_cap"],
+                            cfg["num_experts"], with_shared and cfg["shared_inter"] > 0,
+                            cfg["shared_inter"] > 0, seqs[p], lib=lib)
+        assert rc == 0, rc
+        orders.append(order)
+        R.append(rows.shape[0])
+    seen = np.zeros(cfg["num_regions"] * cfg["ring_depth"], np.uint64)
+    rc, y, sh = O.grouped_forward(cfg, win, ret, Wt, layer, stage, R, [x.shape[0] for x in xs],
+                                  list(range(len(xs))), seen, lib=lib)
+    return rc, y, sh, orders, R, win, ret, L
+
+
+def check_grouped_dense(lib):
+    """Grouped form, E = 1: every row goes through the one expert (a dense
+    SwiGLU MLP, numpy) and the shared rows through the shared MLP."""
+    rng = np.random.default_rng(23)
+    cfg, xs, Wt = make_problem(rng, seq_lens=[5, 9], hidden=64, E=1, k=1, inter=40,
+                               shared_inter=24, act_bytes=4)
+    ids = [np.zeros((x.shape[0], 1), np.int32) for x in xs]
+    rc, y, sh, orders, R, win, ret, L = run_grouped(lib, cfg, xs, Wt, ids)
+    assert rc == 0
+    X = np.concatenate([act_to_f64(x, 4) for x in xs])
+    ref = np_swiglu(X, act_to_f64(Wt["W13"][0], 4), act_to_f64(Wt["Wd"][0], 4), 4)
+    refs = np_swiglu(X, act_to_f64(Wt["W13s"], 4), act_to_f64(Wt["Wds"], 4), 4)
+    for got, want in ((y, ref), (sh, refs)):
+        err = np.abs(got - want).max() / np.sqrt((want ** 2).mean())
+        assert err < 1e-6, err
+    # the return slot carries the rows rounded once, and the group list echoed
+    for p, x in enumerate(xs):
+        n = x.shape[0]
+        start = sum(r.shape[0] for r in xs[:p])
+        assert np.array_equal(return_rows(ret, L, cfg, p, 0, n), np_round_act(y[start:start + n], 4))
+        hw = header_words(ret, L, cfg, p, 0)
+        assert hw[8] == n and hw[12] == n and hw[9] == n
+
+
+def check_grouped_combine(lib):
+    """The Attention side's combine of the grouped outputs (sum over j
+    ascending of w[t,j] * y[row of (t,j)], then + s[t], fp64) equals the FFN-side
+    routed layer on the same tokens and ids, exactly."""
+    rng = np.random.default_rng(29)
+    for ab in (4, 2):
+        cfg, xs, Wt = make_problem(rng, seq_lens=[7, 0, 12], hidden=64, E=8, k=3, inter=32,
+                                   shared_inter=16, act_bytes=ab, token_cap=48)
+        rc, r, win0, ret0, L0 = run_forward(lib, cfg, xs, Wt)
+        assert rc == 0
+        k = cfg["topk"]
+        prefix = np.cumsum([0] + [x.shape[0] for x in xs])
+        ids_pp = [r["ids"][prefix[p]:prefix[p + 1]] for p in range(len(xs))]
+        rc, y, sh, orders, R, win, ret, L = run_grouped(lib, cfg, xs, Wt, ids_pp)
+        assert rc == 0
+        rbase = np.cumsum([0] + R)
+        for p in range(len(xs)):
+            pos = np.empty(R[p], np.int64)
+            pos[orders[p]] = np.arange(R[p])   # row of (t, j) for this peer
+            for tl in range(xs[p].shape[0]):
+                t = prefix[p] + tl
+                acc = np.zeros(cfg["hidden"])
+                for j in range(k):
+                    acc = acc + np.float64(r["w"][t, j]) * y[rbase[p] + pos[tl * k + j]]
+                acc = acc + sh[t]
+                assert np.array_equal(acc, r["out64"][t]), (ab, p, tl)
+
+
+def check_grouped_faults(lib):
+    """Grouped form: a group list that does not sum to the row count, a row
+    count other than the call's, too many rows."""
+    rng = np.random.default_rng(31)
+    cfg, xs, Wt = make_problem(rng, seq_lens=[6], hidden=32, E=4, k=2, inter=16,
+                               shared_inter=0, act_bytes=4, token_cap=16)
+    ids = [rng.integers(0, 4, size=(6, 2)).astype(np.int32)]
+    rc, y, sh, orders, R, win, ret, L = run_grouped(lib, cfg, xs, Wt, ids)
+    assert rc == 0
+    def fwd(w, rows=None):
+        seen = np.zeros(1, np.uint64)
+        out = np.zeros_like(w)
+        return O.grouped_forward(cfg, w, out, Wt, 0, 0, rows or R, [6], [0], seen, lib=lib)[0]
+    assert fwd(win, rows=[R[0] - 1]) == O.ERR_SHAPE
+    bad = win.copy()
+    off = L.flags_bytes + L.header
+    bad[off + 4 * 12: off + 4 * 13] = np.array([R[0] + 1], np.int32).view(np.uint8)
+    assert fwd(bad) == O.ERR_SHAPE
+    assert fwd(win, rows=[17]) == O.ERR_CAPACITY
+    rows, gl, _ = grouped_dispatch(ids[0], xs[0], 2, 4)
+    assert O.pack_grouped(win, L, 1, 0, 0, 0, rows, gl + np.array([1, 0, 0, 0], np.int32), xs[0],
+                          32, 4, 16, 4, 0, 0, 301, lib=lib) == O.ERR_SHAPE
+
+
 ALL_CHECKS = [check_bf16, check_layout, check_header_roundtrip, check_split,
               check_logit_order, check_router, check_router_ties, check_plan,
               check_dense_swiglu, check_dense_mixture, check_identity_combine,
-              check_fanin_split, check_hand_moe, check_fault_codes]
+              check_fanin_split, check_hand_moe, check_fault_codes, check_grouped_dense,
+              check_grouped_combine, check_grouped_faults]

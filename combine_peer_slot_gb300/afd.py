@@ -72,6 +72,10 @@ SIGNATURES = [
     ("afd_announce_shutdown", _I, [_P, _I, _I, _U64]),
     ("afd_ffn_forward", _I, [_P, _I, _I, C.POINTER(C.c_int), C.POINTER(C.c_int), _I]),
     ("afd_unpack_split", _I, [_P, _I, _I, _P, _I, _U64]),
+    ("afd_pack_grouped", _I, [_P, _I, _I, _I, _P, _I, C.POINTER(C.c_int), _P, _I, _I, _U64]),
+    ("afd_ffn_forward_grouped", _I, [_P, _I, _I, C.POINTER(C.c_int), C.POINTER(C.c_int),
+                                     C.POINTER(C.c_int), _I]),
+    ("afd_unpack_grouped", _I, [_P, _I, _I, _P, _I, _P, _I, _U64]),
     ("afd_poll_status", _I, [_P]),
     ("afd_get_window", _I, [_P, _I, C.POINTER(_P), C.POINTER(_I64)]),
     ("afd_get_workspace", _I, [_P, _I, C.POINTER(_P), C.POINTER(_I64)]),
@@ -179,6 +183,23 @@ def afd_ffn_forward(ctx, layer, stage, seq_lens, slots):
 
 def afd_unpack_split(ctx, peer, stage, out_ptr, n_tokens, expect_seq):
     return lib().afd_unpack_split(ctx, peer, stage, out_ptr or None, n_tokens, expect_seq)
+
+
+def afd_pack_grouped(ctx, peer, stage, layer, rows_ptr, n_rows, group_list, x_ptr, n_tokens,
+                     with_shared, seq):
+    return lib().afd_pack_grouped(ctx, peer, stage, layer, rows_ptr or None, n_rows,
+                                  _ints(group_list), x_ptr or None, n_tokens,
+                                  int(bool(with_shared)), seq)
+
+
+def afd_ffn_forward_grouped(ctx, layer, stage, n_rows, seq_lens, slots):
+    return lib().afd_ffn_forward_grouped(ctx, int(layer), int(stage), _ints(n_rows),
+                                         _ints(seq_lens), _ints(slots), len(slots))
+
+
+def afd_unpack_grouped(ctx, peer, stage, y_ptr, n_rows, s_ptr, n_tokens, expect_seq):
+    return lib().afd_unpack_grouped(ctx, peer, stage, y_ptr or None, n_rows, s_ptr or None,
+                                    n_tokens, expect_seq)
 
 
 def afd_poll_status(ctx):

@@ -8,6 +8,7 @@
 #include <vector>
 
 #include <algorithm>
+#include <utility>
 
 #include "afd_internal.cuh"
 
@@ -346,7 +347,8 @@ int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out) {
       {Tm * H * 4},                          // s
       {(int64_t)sizeof(GemmPlan)}, {(int64_t)sizeof(GemmPlan)},
       {E * router_blocks((int)Tm) * 4}, {E * router_blocks((int)Tm) * 4},  // hist, base
-      {Tm * E * 4}};                         // router logits
+      {Tm * E * 4},                          // router logits
+      {2 * AFD_MAX_PEERS * E * 4}};          // grouped-form bases and group-list prefixes
   const int nparts = sizeof(parts) / sizeof(parts[0]);
   int64_t offs[32], total = 0;
   for (int i = 0; i < nparts; i++) {
@@ -377,6 +379,7 @@ int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out) {
   c->ws.hist = reinterpret_cast<int32_t*>(b + offs[18]);
   c->ws.base = reinterpret_cast<int32_t*>(b + offs[19]);
   c->ws.logits = reinterpret_cast<float*>(b + offs[20]);
+  c->ws.gbase = reinterpret_cast<int32_t*>(b + offs[21]);
   c->plan1 = reinterpret_cast<GemmPlan*>(b + offs[16]);
   c->plan2 = reinterpret_cast<GemmPlan*>(b + offs[17]);
   const int ws_map[12] = {4, 5, 6, 7, 8, 9, 11, 12, 13, 14, 15, 0};
@@ -464,12 +467,54 @@ static int pack_common(afd_ctx* ctx, int peer, int stage, int layer, const void*
   if (seq <= last) return AFD_ERR_SEQ;
   const int row_bytes = c.hidden * (ctx->act_f32 ? 4 : 2);
   LaunchCtx lc = ctx->lc();
-  int rc = cuda_fail(launch_pack_payload(lc, ctx->geom, ctx->win[0], peer, stage, x, n, row_bytes,
-                                         with_shared, ctx->ws.status),
+  GroupList gl;
+  memset(&gl, 0, sizeof gl);
+  int rc = cuda_fail(launch_pack_payload(lc, ctx->geom, ctx->win[0], peer, stage, x, n,
+                                         with_shared ? x : nullptr, n, row_bytes),
                      "pack payload");
   if (!rc)
     rc = cuda_fail(launch_pack_header(lc, ctx->geom, ctx->win[0], peer, stage, layer, n, with_shared,
-                                      c.num_experts, seq, shutdown),
+                                      c.num_experts, seq, shutdown, 0, gl),
+                   "pack header");
+  if (!rc) last = seq;
+  return rc;
+}
+
+int afd_pack_grouped(afd_ctx* ctx, int peer, int stage, int layer, const void* rows, int n_rows,
+                     const int* group_list, const void* x, int n_tokens, int with_shared,
+                     uint64_t seq) {
+  if (!ctx || !group_list) return AFD_ERR_ARG;
+  const afd_config& c = ctx->cfg;
+  if (peer < 0 || peer >= c.num_peers || stage < 0 || stage >= c.ring_depth || n_tokens < 0 ||
+      n_rows < 0)
+    return AFD_ERR_ARG;
+  if (with_shared && c.shared_inter <= 0) return AFD_ERR_ARG;
+  if (n_tokens > c.token_cap || n_rows > c.token_cap) return AFD_ERR_CAPACITY;
+  GroupList gl;
+  memset(&gl, 0, sizeof gl);
+  int64_t sum = 0;
+  for (int e = 0; e < c.num_experts; e++) {
+    if (group_list[e] < 0) return AFD_ERR_ARG;
+    gl.n[e] = group_list[e];
+    sum += group_list[e];
+  }
+  if (sum != n_rows) return AFD_ERR_SHAPE;
+  for (const auto& pr : {std::make_pair(rows, n_rows), std::make_pair(x, with_shared ? n_tokens : 0)}) {
+    if (pr.second <= 0) continue;
+    const int rc = check_dev_ptr(pr.first);
+    if (rc) return rc;
+    if (!aligned16(pr.first)) return AFD_ERR_ARG;
+  }
+  uint64_t& last = ctx->last_seq[(size_t)peer * c.ring_depth + stage];
+  if (seq <= last) return AFD_ERR_SEQ;
+  const int row_bytes = c.hidden * (ctx->act_f32 ? 4 : 2);
+  LaunchCtx lc = ctx->lc();
+  int rc = cuda_fail(launch_pack_payload(lc, ctx->geom, ctx->win[0], peer, stage, rows, n_rows,
+                                         with_shared ? x : nullptr, n_tokens, row_bytes),
+                     "pack payload");
+  if (!rc)
+    rc = cuda_fail(launch_pack_header(lc, ctx->geom, ctx->win[0], peer, stage, layer, n_tokens,
+                                      with_shared, c.num_experts, seq, 0, n_rows, gl),
                    "pack header");
   if (!rc) last = seq;
   return rc;
@@ -484,17 +529,17 @@ int afd_announce_shutdown(afd_ctx* ctx, int peer, int stage, uint64_t seq) {
   return pack_common(ctx, peer, stage, 0, nullptr, 0, 0, seq, 1);
 }
 
-int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, const int* slots,
-                    int n_peers) {
+// Arguments of a forward: the list entries (slots, each once and in range),
+// their token counts (<= token_cap each, total <= the context's capacity)
+static int fanin_of(afd_ctx* ctx, int stage, const int* seq_lens, const int* slots, int n_peers,
+                    FanIn& f) {
   if (!ctx || !seq_lens || !slots) return AFD_ERR_ARG;
   const afd_config& c = ctx->cfg;
   if (n_peers <= 0 || n_peers > c.num_peers) return AFD_ERR_ARG;
   if (stage < 0 || stage >= c.ring_depth) return AFD_ERR_ARG;
-  FanIn f;
   memset(&f, 0, sizeof f);
   f.n_peers = n_peers;
   f.stage = stage;
-  f.layer = layer;
   int64_t T = 0;
   for (int i = 0; i < n_peers; i++) {
     if (slots[i] < 0 || slots[i] >= c.num_peers) return AFD_ERR_ARG;
@@ -509,6 +554,46 @@ int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, con
   if (T > ctx->tmax) return AFD_ERR_CAPACITY;
   f.prefix[n_peers] = (int)T;
   f.total = (int)T;
+  return AFD_OK;
+}
+
+static int forward_impl(afd_ctx* ctx, int layer, FanIn& f);
+
+int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, const int* slots,
+                    int n_peers) {
+  FanIn f;
+  const int rc = fanin_of(ctx, stage, seq_lens, slots, n_peers, f);
+  if (rc) return rc;
+  return forward_impl(ctx, layer, f);
+}
+
+int afd_ffn_forward_grouped(afd_ctx* ctx, int layer, int stage, const int* n_rows,
+                            const int* seq_lens, const int* slots, int n_peers) {
+  FanIn f;
+  int rc = fanin_of(ctx, stage, seq_lens, slots, n_peers, f);
+  if (rc) return rc;
+  if (!n_rows) return AFD_ERR_ARG;
+  int64_t R = 0;
+  for (int i = 0; i < n_peers; i++) {
+    if (n_rows[i] < 0) return AFD_ERR_ARG;
+    if (n_rows[i] > ctx->cfg.token_cap) return AFD_ERR_CAPACITY;
+    f.rprefix[i] = (int)R;
+    R += n_rows[i];
+  }
+  if (R > (int64_t)ctx->tmax * ctx->cfg.topk) return AFD_ERR_CAPACITY;
+  f.rprefix[n_peers] = (int)R;
+  f.rtotal = (int)R;
+  f.grouped = 1;
+  return forward_impl(ctx, layer, f);
+}
+
+static int forward_impl(afd_ctx* ctx, int layer, FanIn& f) {
+  const afd_config& c = ctx->cfg;
+  f.layer = layer;
+  const int64_t T = f.total;
+  const bool grouped = f.grouped != 0;
+  // routed rows: T * k partials, or the rows the peers sent already grouped
+  const int64_t N = grouped ? f.rtotal : T * c.topk;
   if (layer < 0 || layer >= c.max_layers || !ctx->layers[layer].set) return AFD_ERR_LAYER;
   const LayerW& L = ctx->layers[layer];
   const int has_shared = c.shared_inter > 0;
@@ -517,15 +602,14 @@ int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, con
   // token tile of the grouped GEMMs: 256 rows, or 64 on the SM-pair engine
   // when the experts average <= 48 rows (decode-sized fan-ins), which then
   // runs its deeper narrow ring
-  const int bn =
-      c.gemm == AFD_GEMM_TENSOR && T * c.topk <= 48 * (int64_t)c.num_experts ? 64 : 256;
+  const int bn = c.gemm == AFD_GEMM_TENSOR && N <= 48 * (int64_t)c.num_experts ? 64 : 256;
   LaunchCtx lc = ctx->lc();
   const DevWS& ws = ctx->ws;
   // decode-sized fan-ins: the SwiGLU GEMM streams its weights from HBM while
   // the small kernels before it leave HBM idle, so a side stream prefetches
   // the weights of the GEMM's first wave of units (experts in order, one
   // 256-row unit per SM pair) into L2 meanwhile; joined at the end
-  const bool prefetch = c.gemm == AFD_GEMM_TENSOR && bn == 64 && T > 0;
+  const bool prefetch = c.gemm == AFD_GEMM_TENSOR && bn == 64 && N > 0;
   int rc = AFD_OK;
   struct Join {  // the main stream waits for the side stream on every way out
     afd_ctx* ctx;
@@ -540,11 +624,13 @@ int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, con
                      "header check");
   if (rc) return rc;
   ctx->mark(1);
-  rc = cuda_fail(launch_router(lc, ctx->geom, ctx->win[0], f, ws, c.hidden, ctx->act_f32, L.WgQ,
-                               L.bias, c.num_experts, c.topk, c.renorm, c.routed_scaling,
-                               ws.logits, ws.hist),
-                 "router");
-  if (rc) return rc;
+  if (!grouped) {  // the grouped form arrives routed
+    rc = cuda_fail(launch_router(lc, ctx->geom, ctx->win[0], f, ws, c.hidden, ctx->act_f32, L.WgQ,
+                                 L.bias, c.num_experts, c.topk, c.renorm, c.routed_scaling,
+                                 ws.logits, ws.hist),
+                   "router");
+    if (rc) return rc;
+  }
   if (prefetch) {
     const int64_t first_wave = (int64_t)(ctx->num_sms / 2) * 256 * c.hidden * 2;
     const int64_t w13 = (int64_t)c.num_experts * 2 * c.inter * c.hidden * 2;
@@ -559,8 +645,11 @@ int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, con
     join.armed = true;
   }
   ctx->mark(2);
-  rc = cuda_fail(launch_plan(lc, f, ws, c.num_experts, c.topk, c.inter, c.shared_inter, c.hidden,
-                             has_shared, bn, ctx->plan1, ctx->plan2, ws.hist, ws.base),
+  rc = cuda_fail(grouped ? launch_plan_grouped(lc, f, ws, c.num_experts, c.inter, c.shared_inter,
+                                                c.hidden, has_shared, bn, ctx->plan1, ctx->plan2)
+                         : launch_plan(lc, f, ws, c.num_experts, c.topk, c.inter, c.shared_inter,
+                                       c.hidden, has_shared, bn, ctx->plan1, ctx->plan2, ws.hist,
+                                       ws.base),
                  "plan");
   if (rc) return rc;
   ctx->mark(3);
@@ -568,7 +657,7 @@ int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, con
                  "gather");
   if (rc) return rc;
   ctx->mark(4);
-  if (T > 0) {
+  if (N + T > 0) {
     if (c.gemm != AFD_GEMM_SIMT) {
       auto launch = c.gemm == AFD_GEMM_TENSOR ? launch_gemm_tc2 : launch_gemm_tc;
       GemmArgs a1;
@@ -663,9 +752,13 @@ int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, con
     ctx->mark(5);
   }
   ctx->mark(6);
-  rc = cuda_fail(launch_combine(lc, ctx->geom, ctx->win[1], f, ws, c.hidden, c.topk, ctx->act_f32,
-                                has_shared, ctx->act_f32),
-                 "combine");
+  // the grouped form returns the expert outputs row by row (the Attention
+  // side weights and combines); the token form combines here
+  rc = cuda_fail(grouped ? launch_scatter_grouped(lc, ctx->geom, ctx->win[1], f, ws, c.hidden,
+                                                  ctx->act_f32, has_shared)
+                         : launch_combine(lc, ctx->geom, ctx->win[1], f, ws, c.hidden, c.topk,
+                                          ctx->act_f32, has_shared, ctx->act_f32),
+                 grouped ? "scatter" : "combine");
   if (rc) return rc;
   ctx->mark(7);
   rc = cuda_fail(launch_return_header(lc, ctx->geom, ctx->win[1], ctx->win[0], f, ws, c.num_experts,
@@ -693,8 +786,36 @@ int afd_unpack_split(afd_ctx* ctx, int peer, int stage, void* out, int n_tokens,
   const int row_bytes = c.hidden * (ctx->act_f32 ? 4 : 2);
   return cuda_fail(launch_unpack(ctx->lc(), ctx->geom, ctx->win[1], peer, stage, out, n_tokens,
                                  row_bytes, c.num_experts, expect_seq, ctx->ws.status,
-                                 ctx->timeout()),
+                                 ctx->timeout(), ctx->geom.routed_x, n_tokens, -1),
                    "unpack");
+}
+
+int afd_unpack_grouped(afd_ctx* ctx, int peer, int stage, void* y_out, int n_rows, void* s_out,
+                       int n_tokens, uint64_t expect_seq) {
+  if (!ctx) return AFD_ERR_ARG;
+  const afd_config& c = ctx->cfg;
+  if (peer < 0 || peer >= c.num_peers || stage < 0 || stage >= c.ring_depth || n_rows < 0 ||
+      n_tokens < 0)
+    return AFD_ERR_ARG;
+  if (n_rows > c.token_cap || n_tokens > c.token_cap) return AFD_ERR_CAPACITY;
+  for (const void* p : {y_out, s_out}) {
+    if (!p) continue;
+    const int rc = check_dev_ptr(p);
+    if (rc) return rc;
+    if (!aligned16(p)) return AFD_ERR_ARG;
+  }
+  if ((n_rows && !y_out) || (s_out && c.shared_inter <= 0)) return AFD_ERR_ARG;
+  const int row_bytes = c.hidden * (ctx->act_f32 ? 4 : 2);
+  int rc = cuda_fail(launch_unpack(ctx->lc(), ctx->geom, ctx->win[1], peer, stage, y_out, n_rows,
+                                   row_bytes, c.num_experts, expect_seq, ctx->ws.status,
+                                   ctx->timeout(), ctx->geom.routed_x, n_tokens, n_rows),
+                     "unpack");
+  if (!rc && s_out)
+    rc = cuda_fail(launch_unpack(ctx->lc(), ctx->geom, ctx->win[1], peer, stage, s_out, n_tokens,
+                                 row_bytes, c.num_experts, expect_seq, ctx->ws.status,
+                                 ctx->timeout(), ctx->geom.shared_x, n_tokens, n_rows),
+                   "unpack");
+  return rc;
 }
 
 int afd_poll_status(afd_ctx* ctx) {

@@ -23,6 +23,16 @@ struct FanIn {
   int total;                          // T = sum of seq_lens
   int prefix[AFD_MAX_PEERS + 1];      // exclusive prefix of seq_lens
   int region[AFD_MAX_PEERS];          // peer (window region) of list entry i
+  // grouped form (the Attention side routed): the routed rows of entry i
+  // are rows [rprefix[i], rprefix[i + 1]) of their concatenation
+  int grouped;
+  int rtotal;
+  int rprefix[AFD_MAX_PEERS + 1];
+};
+
+// group list carried by value into the header-writing kernel
+struct GroupList {
+  int32_t n[256];
 };
 
 // window geometry (both windows share it)
@@ -45,7 +55,8 @@ struct DevWS {
   int32_t* offsets;       // [E + 1]
   int32_t* perm;          // [Tmax * k]
   int32_t* inv;           // [Tmax * k]
-  int32_t* peer_counts;   // [MAX_PEERS * E]
+  int32_t* peer_counts;   // [MAX_PEERS * E] (grouped form: the received group lists)
+  int32_t* gbase;         // [2 * MAX_PEERS * E] grouped form: row bases, group-list prefixes
   void* xp;               // act [Tmax * k + Tmax, H]
   void* h;                // act [Tmax * k, I]
   void* y;                // act [Tmax * k, H]
@@ -281,12 +292,16 @@ cudaError_t launch_k(const LaunchCtx& lc, void (*kernel)(KArgs...), dim3 grid, d
 }
 #endif
 
+// routed_x <- rows (n_rows rows); shared_x <- xs and shared_idx = 0..n_shared-1
+// when xs is not null
 cudaError_t launch_pack_payload(const LaunchCtx& lc, const WinGeom& g, uint8_t* win, int region,
-                                int stage, const void* x, int n, int row_bytes, int with_shared,
-                                const int32_t* status);
+                                int stage, const void* rows, int n_rows, const void* xs, int n_shared,
+                                int row_bytes);
+// header + flag; routed_tokens and the group list are those of the grouped form
+// (0 and all zero for the token form)
 cudaError_t launch_pack_header(const LaunchCtx& lc, const WinGeom& g, uint8_t* win, int region,
                                int stage, int layer, int n, int with_shared, int num_experts,
-                               uint64_t seq, int shutdown);
+                               uint64_t seq, int shutdown, int routed_tokens, const GroupList& gl);
 cudaError_t launch_header_check(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                                 const FanIn& f, const DevWS& ws, int num_experts,
                                 int token_cap, int has_shared_expert, int64_t timeout_ns);
@@ -314,9 +329,19 @@ cudaError_t launch_combine(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret,
 cudaError_t launch_return_header(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret,
                                  const uint8_t* win, const FanIn& f, const DevWS& ws, int E,
                                  int k);
+// n rows of the return slot's field; the header must carry expect_tokens
+// tokens (and expect_routed routed rows unless it is -1)
 cudaError_t launch_unpack(const LaunchCtx& lc, const WinGeom& g, const uint8_t* ret, int region,
                           int stage, void* out, int n, int row_bytes, int num_experts,
-                          uint64_t expect_seq, int32_t* status, int64_t timeout_ns);
+                          uint64_t expect_seq, int32_t* status, int64_t timeout_ns, int64_t field,
+                          int expect_tokens, int expect_routed);
+// grouped form: plan from the received group lists; outputs back to the peers
+cudaError_t launch_plan_grouped(const LaunchCtx& lc, const FanIn& f, const DevWS& ws, int E,
+                                int inter, int shared_inter, int hidden, int has_shared, int bn,
+                                GemmPlan* plan1, GemmPlan* plan2);
+cudaError_t launch_scatter_grouped(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret,
+                                   const FanIn& f, const DevWS& ws, int hidden, int act_f32,
+                                   int has_shared);
 // bytes: a multiple of 16 from a 16-byte aligned base
 cudaError_t launch_prefetch_l2(const LaunchCtx& lc, const void* base, int64_t bytes);
 cudaError_t launch_arrange_wg(const LaunchCtx& lc, const float* Wg, float* WgQ, int hidden,

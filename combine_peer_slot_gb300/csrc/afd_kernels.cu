@@ -29,6 +29,16 @@ __device__ __forceinline__ int entry_of(const FanIn& f, int t) {
   return lo;
 }
 
+// grouped form: list entry i holding routed row r of the concatenation
+__device__ __forceinline__ int entry_of_rows(const FanIn& f, int r) {
+  int lo = 0, hi = f.n_peers - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (f.rprefix[mid] <= r) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
   return __uint_as_float((uint32_t)b << 16);
 }
@@ -38,28 +48,28 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
 // layout": the flag is written after the payload, on the same stream)
 // ---------------------------------------------------------------------------
 __global__ void k_pack_payload(uint8_t* win, WinGeom g, int region, int stage,
-                               const uint4* __restrict__ x, int n, int row_bytes,
-                               int with_shared) {
+                               const uint4* __restrict__ rows, int n_rows,
+                               const uint4* __restrict__ xs, int n_shared, int row_bytes) {
   grid_dep_wait();
   grid_dep_launch();
   uint8_t* slot = slot_ptr(win, g, region, stage);
   uint4* rx = reinterpret_cast<uint4*>(slot + g.routed_x);
   uint4* sx = reinterpret_cast<uint4*>(slot + g.shared_x);
   int32_t* sidx = reinterpret_cast<int32_t*>(slot + g.shared_idx);
-  const int64_t nvec = (int64_t)n * row_bytes / 16;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
-    uint4 v = x[i];
-    rx[i] = v;
-    if (with_shared) sx[i] = v;
+  const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t nvec = (int64_t)n_rows * row_bytes / 16;
+  for (int64_t i = i0; i < nvec; i += stride) rx[i] = rows[i];
+  if (xs) {
+    const int64_t svec = (int64_t)n_shared * row_bytes / 16;
+    for (int64_t i = i0; i < svec; i += stride) sx[i] = xs[i];
+    for (int64_t i = i0; i < n_shared; i += stride) sidx[i] = (int32_t)i;
   }
-  if (with_shared)
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
-      sidx[i] = (int32_t)i;
 }
 
 __global__ void k_pack_header(uint8_t* win, WinGeom g, int region, int stage, int layer, int n,
-                              int with_shared, int num_experts, uint64_t seq, int shutdown) {
+                              int with_shared, int num_experts, uint64_t seq, int shutdown,
+                              int routed_tokens, GroupList gl) {
   grid_dep_wait();
   grid_dep_launch();
   uint8_t* slot = slot_ptr(win, g, region, stage);
@@ -75,11 +85,11 @@ __global__ void k_pack_header(uint8_t* win, WinGeom g, int region, int stage, in
       case 5: v = layer; break;
       case 6: v = stage; break;
       case 7: v = n; break;
-      case 8: v = 0; break;
+      case 8: v = routed_tokens; break;
       case 9: v = with_shared ? n : 0; break;
       case 10: v = num_experts; break;
       case 11: v = AFD_HEADER_FIXED_WORDS + num_experts; break;
-      default: v = 0;
+      default: v = gl.n[i - AFD_HEADER_FIXED_WORDS];
     }
     h[i] = v;
   }
@@ -153,9 +163,26 @@ __global__ void k_header_check(const uint8_t* win, WinGeom g, FanIn f, DevWS ws,
         e = AFD_ERR_SHAPE;
       else if (h[7] > token_cap)
         e = AFD_ERR_CAPACITY;
-      else if (h[8] != 0)
+      else if (h[8] != (f.grouped ? f.rprefix[i + 1] - f.rprefix[i] : 0))
         e = AFD_ERR_SHAPE;
-      else if (h[9] != 0 && (h[9] != n || !has_shared_expert))
+      else if (h[8] > token_cap)
+        e = AFD_ERR_CAPACITY;
+      if (!e && f.grouped) {
+        // the group list: rows per expert, each >= 0, summing to the rows;
+        // kept for the plan and the return header
+        const int32_t* gl = reinterpret_cast<const int32_t*>(hp) + AFD_HEADER_FIXED_WORDS;
+        int64_t sum = 0;
+        int neg = 0;
+        for (int x = 0; x < E; x++) {
+          int32_t v;
+          asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(gl + x) : "memory");
+          neg |= v < 0;
+          sum += v;
+          ws.peer_counts[i * E + x] = v;
+        }
+        if (neg || sum != h[8]) e = AFD_ERR_SHAPE;
+      }
+      if (!e && h[9] != 0 && (h[9] != n || !has_shared_expert))
         e = AFD_ERR_SHAPE;
       if (!e) shared_n[i] = h[9];
     }
@@ -952,7 +979,7 @@ k_router_topk(FanIn f, DevWS ws, const float* __restrict__ logits, int E, int k,
 __device__ void write_tile_tables(const FanIn& f, int k, int E, int inter, int shared_inter,
                                   int hidden, int has_shared, int bn, const int* cnt,
                                   const int* offs, GemmPlan* plan1, GemmPlan* plan2) {
-  const int N = f.total * k;
+  const int N = f.grouped ? f.rtotal : f.total * k;  // routed rows; the shared rows follow
   int tiles1 = 0, tiles2 = 0, units1 = 0, units2 = 0, ng = 0;
   const int mt1 = (inter + 63) / 64, mt2 = (hidden + 127) / 128;
   for (int e = 0; e < E; e++, ng++) {
@@ -1142,6 +1169,75 @@ k_plan_small(FanIn f, DevWS ws, int E, int k, int inter, int shared_inter, int h
 }
 
 // ---------------------------------------------------------------------------
+// Plan of the grouped form (the Attention side routed; [RFC]: Async GPU
+// Connector, "Data flow" steps 1-3): the entries' group lists (from their
+// headers) give the per-expert counts and offsets; entry i's rows of expert e
+// go, in arrival order, after the same expert's rows of the entries before
+// it (stable in list order).  One CTA.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024)
+k_plan_grouped(FanIn f, DevWS ws, int E, int inter, int shared_inter, int hidden, int has_shared,
+               int bn, GemmPlan* plan1, GemmPlan* plan2) {
+  grid_dep_wait();
+  grid_dep_launch();
+  __shared__ int cnt[256];
+  __shared__ int offs[257];
+  __shared__ int skip;
+  const int tid = threadIdx.x;
+  if (tid == 0) skip = read_status(ws.status);
+  __syncthreads();
+  if (skip) return;
+  const int P = f.n_peers;
+  int* base = ws.gbase;                       // [P][E] first position of entry i's expert-e rows
+  int* gpre = ws.gbase + AFD_MAX_PEERS * E;   // [P][E] first row of expert e within entry i
+  for (int e = tid; e < E; e += blockDim.x) {
+    int c = 0;
+    for (int i = 0; i < P; i++) c += ws.peer_counts[i * E + e];
+    cnt[e] = c;
+  }
+  for (int i = tid; i < P; i += blockDim.x) {
+    int r = 0;
+    for (int e = 0; e < E; e++) {
+      gpre[i * E + e] = r;
+      r += ws.peer_counts[i * E + e];
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int run = 0;
+    for (int e = 0; e < E; e++) { offs[e] = run; run += cnt[e]; }
+    offs[E] = run;
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) {
+    int b = offs[e];
+    for (int i = 0; i < P; i++) {
+      base[i * E + e] = b;
+      b += ws.peer_counts[i * E + e];
+    }
+  }
+  for (int e = tid; e <= E; e += blockDim.x) {
+    ws.offsets[e] = offs[e];
+    if (e < E) ws.counts[e] = cnt[e];
+  }
+  __syncthreads();
+  for (int r = tid; r < f.rtotal; r += blockDim.x) {
+    const int i = entry_of_rows(f, r);
+    const int lr = r - f.rprefix[i];
+    const int* gp = gpre + i * E;
+    int lo = 0, hi = E - 1;  // the last expert whose first row is <= lr (that one is not empty)
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (gp[mid] <= lr) lo = mid; else hi = mid - 1;
+    }
+    const int pos = base[i * E + lo] + (lr - gp[lo]);
+    ws.perm[pos] = r;
+    ws.inv[r] = pos;
+  }
+  if (tid == 0) write_tile_tables(f, 1, E, inter, shared_inter, hidden, has_shared, bn, cnt, offs, plan1, plan2);
+}
+
+// ---------------------------------------------------------------------------
 // a3 plan, part 2: the stable permutation.  One warp per router CTA's range
 // of partials f (16 tokens x k, contiguous in f): rank among earlier
 // partials of the same expert in the range (match_any per 32-element round
@@ -1201,29 +1297,32 @@ k_gather(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int k, int row_bytes,
   grid_dep_wait();
   grid_dep_launch();
   if (read_status(ws.status)) return;
-  const int N = f.total * k;
+  const int N = f.grouped ? f.rtotal : f.total * k;
   const int rows = N + (has_shared ? f.total : 0);
   const int nvec = row_bytes / 16;
   const int warps = gridDim.x * (blockDim.x >> 5);
   for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
     uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(ws.xp) + (int64_t)r * row_bytes);
-    int t;
+    int i, local;
     int64_t field;
-    if (r < N) {
-      t = ws.perm[r] / k;
+    if (r < N && f.grouped) {  // routed row perm[r] of the concatenation of the entries' rows
+      const int gr = ws.perm[r];
+      i = entry_of_rows(f, gr);
+      local = gr - f.rprefix[i];
       field = g.routed_x;
     } else {
-      t = r - N;
-      field = g.shared_x;
+      const int t = r < N ? ws.perm[r] / k : r - N;
+      i = entry_of(f, t);
+      local = t - f.prefix[i];
+      field = r < N ? g.routed_x : g.shared_x;
     }
-    const int i = entry_of(f, t);
     const int lane = threadIdx.x & 31;
     if (r >= N && !ws.peer_shared[i]) {
       for (int v = lane; v < nvec; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
       continue;
     }
     const uint4* src = reinterpret_cast<const uint4*>(slot_ptr(win, g, f.region[i], f.stage) + field +
-                                                      (int64_t)(t - f.prefix[i]) * row_bytes);
+                                                      (int64_t)local * row_bytes);
     for (int v = lane; v < nvec; v += 32) dst[v] = __ldg(src + v);
   }
 }
@@ -1425,6 +1524,58 @@ k_combine(uint8_t* ret, WinGeom g, FanIn f, DevWS ws, int hidden, int k, int has
   }
 }
 
+// Grouped form, the way back ([RFC]: Async GPU Connector, "Data flow" step 4:
+// the Attention side weights and combines): the expert output of every
+// received row into its peer's return slot in arrival order (routed_x), and
+// the shared expert's outputs (shared_x, rounded to the activation type).
+// One warp per row.
+template <bool ACT_F32>
+__global__ void __launch_bounds__(kThreads)
+k_scatter_grouped(uint8_t* ret, WinGeom g, FanIn f, DevWS ws, int hidden, int has_shared) {
+  grid_dep_wait();
+  grid_dep_launch();
+  if (read_status(ws.status)) return;
+  constexpr int kEl = ACT_F32 ? 4 : 2;
+  const int row_bytes = hidden * kEl;
+  const int rows = f.rtotal + (has_shared ? f.total : 0);
+  const int lane = threadIdx.x & 31;
+  const int warps = gridDim.x * (blockDim.x >> 5);
+  for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
+    if (r < f.rtotal) {
+      const int i = entry_of_rows(f, r);
+      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(ws.y) +
+                                                        (int64_t)ws.inv[r] * row_bytes);
+      uint4* dst = reinterpret_cast<uint4*>(slot_ptr(ret, g, f.region[i], f.stage) + g.routed_x +
+                                            (int64_t)(r - f.rprefix[i]) * row_bytes);
+      for (int v = lane; v < row_bytes / 16; v += 32) dst[v] = src[v];
+    } else {
+      const int t = r - f.rtotal;
+      const int i = entry_of(f, t);
+      if (!ws.peer_shared[i]) continue;
+      const float* src = ws.s + (int64_t)t * hidden;
+      uint8_t* dst = slot_ptr(ret, g, f.region[i], f.stage) + g.shared_x +
+                     (int64_t)(t - f.prefix[i]) * row_bytes;
+      for (int c = lane * 8; c < hidden; c += 32 * 8) {
+        const float4 a = *reinterpret_cast<const float4*>(src + c);
+        const float4 b = *reinterpret_cast<const float4*>(src + c + 4);
+        if constexpr (ACT_F32) {
+          reinterpret_cast<float4*>(dst + (int64_t)c * 4)[0] = a;
+          reinterpret_cast<float4*>(dst + (int64_t)c * 4)[1] = b;
+        } else {
+          __nv_bfloat162 p0 = __floats2bfloat162_rn(a.x, a.y), p1 = __floats2bfloat162_rn(a.z, a.w);
+          __nv_bfloat162 p2 = __floats2bfloat162_rn(b.x, b.y), p3 = __floats2bfloat162_rn(b.z, b.w);
+          uint4 o;
+          o.x = *reinterpret_cast<uint32_t*>(&p0);
+          o.y = *reinterpret_cast<uint32_t*>(&p1);
+          o.z = *reinterpret_cast<uint32_t*>(&p2);
+          o.w = *reinterpret_cast<uint32_t*>(&p3);
+          *reinterpret_cast<uint4*>(dst + (int64_t)c * 2) = o;
+        }
+      }
+    }
+  }
+}
+
 // return headers, then the return flags (release) = the dispatch seq
 __global__ void k_return_header(uint8_t* ret, WinGeom g, FanIn f, DevWS ws, int E, int k) {
   grid_dep_wait();
@@ -1446,7 +1597,7 @@ __global__ void k_return_header(uint8_t* ret, WinGeom g, FanIn f, DevWS ws, int 
       case 5: v = f.layer; break;
       case 6: v = f.stage; break;
       case 7: v = n; break;
-      case 8: v = n * k; break;
+      case 8: v = f.grouped ? f.rprefix[i + 1] - f.rprefix[i] : n * k; break;
       case 9: v = ws.peer_shared[i] ? n : 0; break;
       case 10: v = E; break;
       case 11: v = AFD_HEADER_FIXED_WORDS + E; break;
@@ -1465,7 +1616,8 @@ __global__ void k_return_header(uint8_t* ret, WinGeom g, FanIn f, DevWS ws, int 
 // thread 0, then the block copies its share of the rows.
 __global__ void __launch_bounds__(kThreads)
 k_unpack(const uint8_t* ret, WinGeom g, int region, int stage, uint4* out, int n, int row_bytes,
-         int E, uint64_t expect_seq, int32_t* status, int64_t timeout_ns) {
+         int E, uint64_t expect_seq, int32_t* status, int64_t timeout_ns, int64_t field,
+         int expect_tokens, int expect_routed) {
   grid_dep_wait();
   grid_dep_launch();
   __shared__ int ok;
@@ -1491,7 +1643,7 @@ k_unpack(const uint8_t* ret, WinGeom g, int region, int stage, uint4* out, int n
           e = AFD_ERR_HEADER;
         else if ((uint32_t)h[4] != (uint32_t)expect_seq)
           e = AFD_ERR_SEQ;
-        else if (h[7] != n)
+        else if (h[7] != expect_tokens || (expect_routed >= 0 && h[8] != expect_routed))
           e = AFD_ERR_SHAPE;
       }
       if (e > 0) set_error(status, e);
@@ -1500,7 +1652,7 @@ k_unpack(const uint8_t* ret, WinGeom g, int region, int stage, uint4* out, int n
   }
   __syncthreads();
   if (!ok) return;
-  const uint4* src = reinterpret_cast<const uint4*>(slot_ptr(ret, g, region, stage) + g.routed_x);
+  const uint4* src = reinterpret_cast<const uint4*>(slot_ptr(ret, g, region, stage) + field);
   const int64_t nvec = (int64_t)n * row_bytes / 16;
   for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec;
        v += (int64_t)gridDim.x * blockDim.x)
@@ -1562,20 +1714,20 @@ inline int grid_for(int64_t work, int per_block, int cap) {
 // launchers
 // ---------------------------------------------------------------------------
 cudaError_t launch_pack_payload(const LaunchCtx& lc, const WinGeom& g, uint8_t* win, int region,
-                                int stage, const void* x, int n, int row_bytes, int with_shared,
-                                const int32_t*) {
-  if (n == 0) return cudaSuccess;
-  const int64_t nvec = (int64_t)n * row_bytes / 16;
-  return launch_k(lc, k_pack_payload, grid_for(nvec, kThreads * 4, lc.num_sms * 8), kThreads, 0,
-                  win, g, region, stage, reinterpret_cast<const uint4*>(x), n, row_bytes,
-                  with_shared);
+                                int stage, const void* rows, int n_rows, const void* xs, int n_shared,
+                                int row_bytes) {
+  const int64_t work = (int64_t)std::max(n_rows, xs ? n_shared : 0) * row_bytes / 16;
+  if (work == 0) return cudaSuccess;
+  return launch_k(lc, k_pack_payload, grid_for(work, kThreads * 4, lc.num_sms * 8), kThreads, 0,
+                  win, g, region, stage, reinterpret_cast<const uint4*>(rows), n_rows,
+                  reinterpret_cast<const uint4*>(xs), n_shared, row_bytes);
 }
 
 cudaError_t launch_pack_header(const LaunchCtx& lc, const WinGeom& g, uint8_t* win, int region,
                                int stage, int layer, int n, int with_shared, int num_experts,
-                               uint64_t seq, int shutdown) {
+                               uint64_t seq, int shutdown, int routed_tokens, const GroupList& gl) {
   return launch_k(lc, k_pack_header, 1, 128, 0, win, g, region, stage, layer, n, with_shared,
-                  num_experts, seq, shutdown);
+                  num_experts, seq, shutdown, routed_tokens, gl);
 }
 
 cudaError_t launch_header_check(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
@@ -1756,11 +1908,30 @@ cudaError_t launch_return_header(const LaunchCtx& lc, const WinGeom& g, uint8_t*
 
 cudaError_t launch_unpack(const LaunchCtx& lc, const WinGeom& g, const uint8_t* ret, int region,
                           int stage, void* out, int n, int row_bytes, int num_experts,
-                          uint64_t expect_seq, int32_t* status, int64_t timeout_ns) {
+                          uint64_t expect_seq, int32_t* status, int64_t timeout_ns, int64_t field,
+                          int expect_tokens, int expect_routed) {
   const int64_t nvec = (int64_t)n * row_bytes / 16;
   return launch_k(lc, k_unpack, grid_for(nvec, kThreads * 4, lc.num_sms * 4), kThreads, 0, ret, g,
                   region, stage, reinterpret_cast<uint4*>(out), n, row_bytes, num_experts,
-                  expect_seq, status, timeout_ns);
+                  expect_seq, status, timeout_ns, field, expect_tokens, expect_routed);
+}
+
+cudaError_t launch_plan_grouped(const LaunchCtx& lc, const FanIn& f, const DevWS& ws, int E,
+                                int inter, int shared_inter, int hidden, int has_shared, int bn,
+                                GemmPlan* plan1, GemmPlan* plan2) {
+  return launch_k(lc, k_plan_grouped, 1, 1024, 0, f, ws, E, inter, shared_inter, hidden, has_shared,
+                  bn, plan1, plan2);
+}
+
+cudaError_t launch_scatter_grouped(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret,
+                                   const FanIn& f, const DevWS& ws, int hidden, int act_f32,
+                                   int has_shared) {
+  const int64_t rows = (int64_t)f.rtotal + (has_shared ? f.total : 0);
+  if (rows == 0) return cudaSuccess;
+  const int grid = grid_for(rows, kThreads / 32, lc.num_sms * 8);
+  if (act_f32)
+    return launch_k(lc, k_scatter_grouped<true>, grid, kThreads, 0, ret, g, f, ws, hidden, has_shared);
+  return launch_k(lc, k_scatter_grouped<false>, grid, kThreads, 0, ret, g, f, ws, hidden, has_shared);
 }
 
 cudaError_t launch_prefetch_l2(const LaunchCtx& lc, const void* base, int64_t bytes) {

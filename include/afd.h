@@ -267,6 +267,52 @@ int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, con
 int afd_unpack_split(afd_ctx* ctx, int peer, int stage, void* out, int n_tokens,
                      uint64_t expect_seq);
 
+/* ---- grouped form: the Attention side routes ------------------------------
+ * [RFC]: Async GPU Connector, "Data flow" steps 1-4 and "Attention gate and
+ * FFN expert compute": the Attention side computes the gate, sorts the
+ * flattened top-k ids stably and sends each FFN rank its routed rows grouped
+ * by expert, with the rows per expert (group_list) in the header; the FFN
+ * must not route again and runs every row through its expert with a unit
+ * weight (a top-1 problem), the shared rows through the shared expert as
+ * their own batch; the gate weights never travel, and the Attention side
+ * weights and combines what comes back.
+ *
+ * afd_pack_grouped -- the Attention side's send of this form, simulated:
+ *   rows        device act [n_rows, hidden], grouped by expert (ascending e)
+ *   group_list  host int32 [num_experts], rows per expert, summing to n_rows
+ *   x           device act [n_tokens, hidden], the peer's tokens: the shared
+ *               rows (shared_idx = 0..n_tokens-1) when with_shared
+ * Writes routed_x, shared rows, then the header (routed_tokens = n_rows,
+ * num_tokens = n_tokens, expert_counts = group_list) and the flag = seq.
+ * Errors: AFD_ERR_ARG, AFD_ERR_CAPACITY (n_rows or n_tokens > token_cap),
+ * AFD_ERR_SHAPE (group_list does not sum to n_rows), AFD_ERR_SEQ,
+ * AFD_ERR_NOT_DEVICE. */
+int afd_pack_grouped(afd_ctx* ctx, int peer, int stage, int layer, const void* rows, int n_rows,
+                     const int* group_list, const void* x, int n_tokens, int with_shared,
+                     uint64_t seq);
+
+/* afd_ffn_forward_grouped -- the FFN-side step of the grouped form over the
+ * listed slots: n_rows[i] / seq_lens[i] (host) are the routed rows and the
+ * tokens of list entry i.  Header checks as afd_ffn_forward plus
+ * routed_tokens == n_rows[i] and the group list summing to it; the rows of
+ * all entries grouped by expert (entry order within an expert); the routed
+ * and shared SwiGLU GEMMs; then each entry's return slot gets routed_x = the
+ * expert output of each of its rows in arrival order, shared_x = its shared
+ * outputs, the header (routed_tokens, shared_tokens and expert_counts as
+ * received) and the flag = the dispatch seq.  Capacity: n_rows[i] <=
+ * token_cap, sum n_rows <= max_total_tokens * topk.  Errors as
+ * afd_ffn_forward. */
+int afd_ffn_forward_grouped(afd_ctx* ctx, int layer, int stage, const int* n_rows,
+                            const int* seq_lens, const int* slots, int n_peers);
+
+/* afd_unpack_grouped -- the Attention side's receive of the grouped form,
+ * simulated: bounded wait for the return flag == expect_seq, header checks
+ * (num_tokens == n_tokens, routed_tokens == n_rows), then the n_rows expert
+ * outputs into y_out (device act [n_rows, hidden]) and, when s_out is not
+ * NULL, the n_tokens shared outputs into s_out.  Errors as afd_unpack_split. */
+int afd_unpack_grouped(afd_ctx* ctx, int peer, int stage, void* y_out, int n_rows, void* s_out,
+                       int n_tokens, uint64_t expect_seq);
+
 /* Synchronise the stream, return the first device-recorded error since the
  * last poll (AFD_OK if none) and clear it; AFD_ERR_CUDA if the stream itself
  * failed. */

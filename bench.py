@@ -157,6 +157,32 @@ def stage_work(w, T):
     }
 
 
+def stage_work_grouped(w, T, Rr):
+    """Algorithmic work per stage of the grouped form: Rr routed rows arrive
+    grouped (no router, no combine: the rows' outputs go back)."""
+    H, I, Is = w.hidden, w.inter, w.shared_inter
+    ab = w.act_bytes
+    return {
+        "gather": {"bytes": (Rr + T) * H * ab * 2},
+        "gemm_swiglu": {"flops": 2 * H * 2 * (Rr * I + T * Is)},
+        "gemm_down": {"flops": 2 * H * (Rr * I + T * Is)},
+        "combine_split": {"bytes": Rr * H * ab * 2 + T * H * (4 + ab)},
+    }
+
+
+def path_roofline_grouped(w, T, Rr, counts_nonzero, pk):
+    """Roofline of one grouped forward: FLOP = 6 H (Rr I + T I_s); bytes =
+    weights of every expert with rows + shared + rows and shared rows in +
+    their outputs."""
+    H, I, Is = w.hidden, w.inter, w.shared_inter
+    flops = 6 * H * (Rr * I + T * Is)
+    wbytes = counts_nonzero * 3 * H * I * 2 + 3 * H * Is * 2
+    abytes = 2 * (Rr + T) * H * w.act_bytes
+    t_flop = flops / (pk["bf16_tflops"] * 1e12)
+    t_mem = (wbytes + abytes) / (pk["hbm_gbs"] * 1e9)
+    return flops, wbytes + abytes, max(t_flop, t_mem), ("tensor" if t_flop >= t_mem else "hbm")
+
+
 def path_roofline(w, T, counts_nonzero, pk):
     """Roofline time of one forward: max(FLOP / bf16 peak, bytes / HBM) with
     bytes = weights of every expert that received a token + shared + router
@@ -203,7 +229,12 @@ def run_ours(args, ws, rank, local):
 
     w = workload_of(args)
     T = w.total_tokens
+    grouped = args.form == "grouped"
     run = R.Runner(w, max_total_tokens=T)
+    if grouped:  # the Attention side routes: grouped rows, no router or combine here
+        run.prepare_grouped(seed=w.seed)
+    pack = run.pack_grouped_all if grouped else run.pack_all
+    fwd = run.forward_grouped if grouped else run.forward
     stream = run.stream
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
     e0 = [torch.cuda.Event(enable_timing=True) for _ in range(w.layers)]
@@ -212,10 +243,10 @@ def run_ours(args, ws, rank, local):
     def step(timed_stats=None):
         fwd_ms = 0.0
         for layer in range(w.layers):
-            run.pack_all(layer)
+            pack(layer)
             flush.zero_()
             e0[layer].record(stream)
-            rc = run.forward(layer)
+            rc = fwd(layer)
             e1[layer].record(stream)
             if rc:
                 raise A.AfdError(rc, "afd_ffn_forward")
@@ -267,10 +298,14 @@ def run_ours(args, ws, rank, local):
     # roofline of the whole path and of the dominant stage
     pk, pk_kind = peaks()
     cnt = run.workspace(A.AFD_WS_COUNTS, 4 * w.num_experts).cpu().numpy().view(np.int32)
-    flops, nbytes, t_roof, bound = path_roofline(w, T, int((cnt > 0).sum()), pk)
+    if grouped:
+        Rr = int(sum(run.g_n))
+        flops, nbytes, t_roof, bound = path_roofline_grouped(w, T, Rr, int((cnt > 0).sum()), pk)
+    else:
+        flops, nbytes, t_roof, bound = path_roofline(w, T, int((cnt > 0).sum()), pk)
     stages = {n: stage_sum[i] / (args.steps * w.layers) for i, n in enumerate(A.STAGE_NAMES)}
     dom = max(stages, key=stages.get)
-    work = stage_work(w, T).get(dom, {})
+    work = (stage_work_grouped(w, T, Rr) if grouped else stage_work(w, T)).get(dom, {})
     if "flops" in work and dom.startswith("gemm"):
         ach = work["flops"] / (stages[dom] / 1e3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
@@ -283,7 +318,7 @@ def run_ours(args, ws, rank, local):
                 "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "peak_source": f"{pk_kind} hbm_gbs",
                 "algorithmic_bytes_per_launch": work.get("bytes", 0)}
     roof["avg_launch_ms"] = stages[dom]
-    roof["traffic"] = traffic_from_profile(dom, args.workload)
+    roof["traffic"] = None if grouped else traffic_from_profile(dom, args.workload)
 
     # end to end through the C ABI with host buffers
     e2e = None
@@ -293,20 +328,32 @@ def run_ours(args, ws, rank, local):
         hout = [torch.empty((max(n, 1), w.hidden), dtype=dt).pin_memory() for n in w.seq_lens]
         h2d = sum(x.numel() * x.element_size() for x in hx)
         d2h = sum(n * w.hidden * w.act_bytes for n in w.seq_lens)
+        if grouped:  # also the routed rows in and their expert outputs back
+            hrows = [r.cpu().pin_memory() if r is not None else None for r in run.g_rows]
+            hy = [torch.empty_like(y, device="cpu").pin_memory() for y in run.g_y]
+            h2d += sum(r.numel() * r.element_size() for r in hrows if r is not None)
+            d2h += sum(n * w.hidden * w.act_bytes for n in run.g_n)
 
         def e2e_step():
             with torch.cuda.stream(stream):
                 for layer in range(w.layers):
                     for p in range(w.num_peers):
                         run.x[p].copy_(hx[p], non_blocking=True)
-                    run.pack_all(layer)
-                    rc = run.forward(layer)
+                        if grouped and hrows[p] is not None:
+                            run.g_rows[p].copy_(hrows[p], non_blocking=True)
+                    pack(layer)
+                    rc = fwd(layer)
                     if rc:
                         raise A.AfdError(rc, "afd_ffn_forward")
-                    run.unpack_all()
+                    if grouped:
+                        run.unpack_grouped_all()
+                    else:
+                        run.unpack_all()
                     for p, n in enumerate(w.seq_lens):
                         if n:
                             hout[p][:n].copy_(run.out[p][:n], non_blocking=True)
+                        if grouped and run.g_n[p]:
+                            hy[p][:run.g_n[p]].copy_(run.g_y[p][:run.g_n[p]], non_blocking=True)
             stream.synchronize()
 
         for _ in range(max(2, args.warmup)):
@@ -326,7 +373,7 @@ def run_ours(args, ws, rank, local):
                "note": "pinned host x -> device, pack, forward, unpack, device -> pinned host"}
 
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and not grouped:
         cpu = cpu_baseline(w, budget_s=args.cpu_budget)
 
     out = {
@@ -334,14 +381,19 @@ def run_ours(args, ws, rank, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; no model weights or dataset)",
-        "config": {"workload": args.workload, "peers": w.num_peers, "seq_lens": w.seq_lens,
+        "config": {"workload": args.workload + ("_grouped" if grouped else ""),
+                   "peers": w.num_peers, "seq_lens": w.seq_lens,
                    "total_tokens": T, "hidden": w.hidden, "experts": w.num_experts,
                    "topk": w.topk, "inter": w.inter, "shared_inter": w.shared_inter,
                    "layers": w.layers, "parallelism": f"replicas{ws}",
                    "l2": "flushed (256 MB write) before every timed forward",
                    "stage_timing": "per-stage events on the launching stream in a second "
                                    "pass of the same K steps; the timed pass records only "
-                                   "the events around each forward"},
+                                   "the events around each forward",
+                   **({"form": "grouped: the Attention side routed (seeded distinct top-k "
+                               "per token); rows grouped by expert arrive, their expert "
+                               "outputs go back", "routed_rows": int(sum(run.g_n))}
+                      if grouped else {})},
         "tflops": flops * w.layers / (ms_step_max / 1e3) / 1e12,
         "path_roofline": {"bound": bound, "roofline_ms": t_roof * 1e3 * w.layers,
                           "frac": t_roof * 1e3 * w.layers / ms_step_max,
@@ -443,6 +495,10 @@ def run_reference(args, ws, rank):
 def workload_of(args):
     from combine_peer_slot_gb300 import workloads as W
     over = {}
+    if getattr(args, "form", "tokens") == "grouped":  # a slot holds a peer's n * k routed rows
+        w0 = W.get(args.workload)
+        lens = [int(v) for v in args.seq_lens.split(",")] if args.seq_lens else w0.seq_lens
+        over["token_cap"] = -(-max(lens) * w0.topk // 64) * 64
     if args.seq_lens:
         over["seq_lens"] = [int(v) for v in args.seq_lens.split(",")]
     if args.layers:
@@ -465,6 +521,8 @@ def main():
     ap.add_argument("--seq-lens", default="",
                     help="comma-separated per-peer token counts replacing the workload's "
                          "(smaller profiling cases of the same shapes)")
+    ap.add_argument("--form", choices=["tokens", "grouped"], default="tokens",
+                    help="grouped: the Attention side routes and sends rows grouped by expert")
     ap.add_argument("--layers", type=int, default=0,
                     help="number of layers replacing the workload's (smaller profiling cases)")
     args = ap.parse_args()

@@ -91,6 +91,51 @@ class Runner:
                 raise A.AfdError(rc, "afd_unpack_split")
         return self.out
 
+    # -- grouped form: the Attention side routes ---------------------------------
+    def prepare_grouped(self, seed=0):
+        """Draw the Attention side's routing (distinct top-k experts per token,
+        seeded) and build each peer's routed rows grouped by expert (stable
+        sort of the flattened ids) and its group list, on the device."""
+        import torch
+        w = self.w
+        rng = np.random.default_rng(seed)
+        self.g_rows, self.g_list, self.g_n = [], [], []
+        for p, n in enumerate(w.seq_lens):
+            ids = np.argsort(rng.random((n, w.num_experts)), axis=1)[:, :w.topk]
+            order = np.argsort(ids.reshape(-1), kind="stable")
+            rows = np.ascontiguousarray(self.host["x"][p][order // w.topk])
+            self.g_rows.append(act_tensor(rows, w.act, self.device) if rows.shape[0] else None)
+            self.g_list.append(np.bincount(ids.reshape(-1), minlength=w.num_experts))
+            self.g_n.append(int(rows.shape[0]))
+        dt = torch.bfloat16 if w.act == "bf16" else torch.float32
+        self.g_y = [torch.empty((max(r, 1), w.hidden), dtype=dt, device=self.device) for r in self.g_n]
+
+    def pack_grouped_all(self, layer=0, stage=0, with_shared=None):
+        ws = (self.w.shared_inter > 0) if with_shared is None else with_shared
+        for p, n in enumerate(self.w.seq_lens):
+            self.seq += 1
+            rows = self.g_rows[p]
+            rc = A.afd_pack_grouped(self.ctx, p, stage, layer, rows.data_ptr() if rows is not None else 0,
+                                    self.g_n[p], self.g_list[p], self.x[p].data_ptr() if n else 0, n,
+                                    ws, self.seq)
+            if rc:
+                raise A.AfdError(rc, "afd_pack_grouped")
+            self.last_seq[(p, stage)] = self.seq
+
+    def forward_grouped(self, layer=0, stage=0):
+        slots = list(range(self.w.num_peers))
+        return A.afd_ffn_forward_grouped(self.ctx, layer, stage, self.g_n, list(self.w.seq_lens), slots)
+
+    def unpack_grouped_all(self, stage=0, with_shared=None):
+        ws = (self.w.shared_inter > 0) if with_shared is None else with_shared
+        for p, n in enumerate(self.w.seq_lens):
+            rc = A.afd_unpack_grouped(self.ctx, p, stage, self.g_y[p].data_ptr() if self.g_n[p] else 0,
+                                      self.g_n[p], self.out[p].data_ptr() if (ws and n) else 0, n,
+                                      self.last_seq[(p, stage)])
+            if rc:
+                raise A.AfdError(rc, "afd_unpack_grouped")
+        return self.g_y, self.out
+
     def poll(self):
         return A.afd_poll_status(self.ctx)
 

@@ -170,6 +170,7 @@ struct afd_ctx {
   GemmPlan* plan2 = nullptr;
   CUtensorMap tmXp, tmH, tmHs;        // token boxes of the tensor engine
   CUtensorMap tmXp32, tmH32, tmHs32;  // 32-row boxes (small SM-pair units)
+  CUtensorMap tmWin, tmWin32;         // dispatch window as [rows, hidden] (grouped form in place)
   std::vector<LayerW> layers;
   std::vector<uint64_t> last_seq;
   int tmax = 0;
@@ -395,6 +396,9 @@ int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out) {
     if (!rc) rc = encode_rows(&c->tmXp32, c->ws.xp, Tm * k + Tm, (int)H, 32);
     if (!rc) rc = encode_rows(&c->tmH32, c->ws.h, Tm * k, (int)I, 32);
     if (!rc) rc = encode_rows(&c->tmHs32, c->ws.hs, Tm, (int)(Is > 0 ? Is : 64), 32);
+    const int64_t win_rows = c->L.window_bytes / (H * ab);
+    if (!rc) rc = encode_rows(&c->tmWin, c->win[0], win_rows, (int)H, box);
+    if (!rc) rc = encode_rows(&c->tmWin32, c->win[0], win_rows, (int)H, 32);
     if (rc) { afd_destroy(c); return rc; }
   }
   *out = c;
@@ -584,6 +588,7 @@ int afd_ffn_forward_grouped(afd_ctx* ctx, int layer, int stage, const int* n_row
   f.rprefix[n_peers] = (int)R;
   f.rtotal = (int)R;
   f.grouped = 1;
+  f.num_experts = ctx->cfg.num_experts;
   return forward_impl(ctx, layer, f);
 }
 
@@ -592,6 +597,13 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f) {
   f.layer = layer;
   const int64_t T = f.total;
   const bool grouped = f.grouped != 0;
+  // grouped form from a single peer on a tensor engine: its rows are already
+  // grouped by expert in its slot, so the GEMMs read them there and write the
+  // outputs into its return slot (no gather, no scatter).  With several peers
+  // the per-(peer, expert) groups would be small and each expert's weights
+  // read once per peer (measured slower than gathering the peers' rows into
+  // one group per expert), so those take the gather and the scatter.
+  const bool in_place = grouped && c.gemm != AFD_GEMM_SIMT && f.n_peers == 1;
   // routed rows: T * k partials, or the rows the peers sent already grouped
   const int64_t N = grouped ? f.rtotal : T * c.topk;
   if (layer < 0 || layer >= c.max_layers || !ctx->layers[layer].set) return AFD_ERR_LAYER;
@@ -646,16 +658,19 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f) {
   }
   ctx->mark(2);
   rc = cuda_fail(grouped ? launch_plan_grouped(lc, f, ws, c.num_experts, c.inter, c.shared_inter,
-                                                c.hidden, has_shared, bn, ctx->plan1, ctx->plan2)
+                                                c.hidden, has_shared, bn, ctx->plan1, ctx->plan2,
+                                                ctx->geom, row_bytes, in_place)
                          : launch_plan(lc, f, ws, c.num_experts, c.topk, c.inter, c.shared_inter,
                                        c.hidden, has_shared, bn, ctx->plan1, ctx->plan2, ws.hist,
                                        ws.base),
                  "plan");
   if (rc) return rc;
   ctx->mark(3);
-  rc = cuda_fail(launch_gather(lc, ctx->geom, ctx->win[0], f, ws, c.topk, row_bytes, has_shared),
-                 "gather");
-  if (rc) return rc;
+  if (!in_place) {
+    rc = cuda_fail(launch_gather(lc, ctx->geom, ctx->win[0], f, ws, c.topk, row_bytes, has_shared),
+                   "gather");
+    if (rc) return rc;
+  }
   ctx->mark(4);
   if (N + T > 0) {
     if (c.gemm != AFD_GEMM_SIMT) {
@@ -664,10 +679,10 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f) {
       memset(&a1, 0, sizeof a1);
       a1.tmA[0] = L.tmA1[0];
       a1.tmA[1] = L.tmA1[1];
-      a1.tmB[0] = ctx->tmXp;
-      a1.tmB[1] = ctx->tmXp;
-      a1.tmBs[0] = ctx->tmXp32;
-      a1.tmBs[1] = ctx->tmXp32;
+      const CUtensorMap& tb = in_place ? ctx->tmWin : ctx->tmXp;
+      const CUtensorMap& tbs = in_place ? ctx->tmWin32 : ctx->tmXp32;
+      a1.tmB[0] = a1.tmB[1] = tb;
+      a1.tmBs[0] = a1.tmBs[1] = tbs;
       a1.out[0] = ws.h;
       a1.out[1] = ws.hs;
       a1.ldo[0] = c.inter;
@@ -696,6 +711,10 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f) {
       a2.ldo[0] = a2.ldo[1] = c.hidden;
       a2.out_f32[0] = 0;
       a2.out_f32[1] = 1;
+      if (in_place) {  // outputs straight into the return slots (rows = window rows)
+        a2.out[0] = a2.out[1] = ctx->win[1];
+        a2.out_f32[1] = 0;
+      }
       a2.K[0] = c.inter;
       a2.K[1] = c.shared_inter;
       a2.M[0] = a2.M[1] = c.hidden;
@@ -754,8 +773,9 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f) {
   ctx->mark(6);
   // the grouped form returns the expert outputs row by row (the Attention
   // side weights and combines); the token form combines here
-  rc = cuda_fail(grouped ? launch_scatter_grouped(lc, ctx->geom, ctx->win[1], f, ws, c.hidden,
-                                                  ctx->act_f32, has_shared)
+  rc = cuda_fail(grouped ? (in_place ? cudaSuccess
+                                     : launch_scatter_grouped(lc, ctx->geom, ctx->win[1], f, ws,
+                                                              c.hidden, ctx->act_f32, has_shared))
                          : launch_combine(lc, ctx->geom, ctx->win[1], f, ws, c.hidden, c.topk,
                                           ctx->act_f32, has_shared, ctx->act_f32),
                  grouped ? "scatter" : "combine");

@@ -26,6 +26,7 @@ struct FanIn {
   // grouped form (the Attention side routed): the routed rows of entry i
   // are rows [rprefix[i], rprefix[i + 1]) of their concatenation
   int grouped;
+  int num_experts;                    // grouped form: E (row placement in the gather)
   int rtotal;
   int rprefix[AFD_MAX_PEERS + 1];
 };
@@ -336,9 +337,14 @@ cudaError_t launch_unpack(const LaunchCtx& lc, const WinGeom& g, const uint8_t* 
                           uint64_t expect_seq, int32_t* status, int64_t timeout_ns, int64_t field,
                           int expect_tokens, int expect_routed);
 // grouped form: plan from the received group lists; outputs back to the peers
+// in_place: one GEMM group per (entry, expert) and per entry's shared rows,
+// B rows read from the dispatch window, down-GEMM outputs written into the
+// return window (rows given as window rows); else per-expert groups over
+// the gathered Xp with a scatter afterwards
 cudaError_t launch_plan_grouped(const LaunchCtx& lc, const FanIn& f, const DevWS& ws, int E,
                                 int inter, int shared_inter, int hidden, int has_shared, int bn,
-                                GemmPlan* plan1, GemmPlan* plan2);
+                                GemmPlan* plan1, GemmPlan* plan2, const WinGeom& g, int row_bytes,
+                                int in_place);
 cudaError_t launch_scatter_grouped(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret,
                                    const FanIn& f, const DevWS& ws, int hidden, int act_f32,
                                    int has_shared);

@@ -29,6 +29,14 @@ __device__ __forceinline__ int entry_of(const FanIn& f, int t) {
   return lo;
 }
 
+// row r of a slot field as a row of the window seen as a [rows, hidden]
+// matrix (every field starts on a whole row)
+__device__ __forceinline__ int32_t window_row(const WinGeom& g, int region, int stage, int64_t field,
+                                              int r, int row_bytes) {
+  return (int32_t)((g.flags_bytes + ((int64_t)region * g.ring_depth + stage) * g.slot_bytes + field) /
+                   row_bytes) + r;
+}
+
 // grouped form: list entry i holding routed row r of the concatenation
 __device__ __forceinline__ int entry_of_rows(const FanIn& f, int r) {
   int lo = 0, hi = f.n_peers - 1;
@@ -170,12 +178,12 @@ __global__ void k_header_check(const uint8_t* win, WinGeom g, FanIn f, DevWS ws,
       if (!e && f.grouped) {
         // the group list: rows per expert, each >= 0, summing to the rows;
         // kept for the plan and the return header
+        // (ordered after the flag's acquire by the asm memory clobbers above)
         const int32_t* gl = reinterpret_cast<const int32_t*>(hp) + AFD_HEADER_FIXED_WORDS;
         int64_t sum = 0;
         int neg = 0;
         for (int x = 0; x < E; x++) {
-          int32_t v;
-          asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(gl + x) : "memory");
+          const int32_t v = gl[x];
           neg |= v < 0;
           sum += v;
           ws.peer_counts[i * E + x] = v;
@@ -1177,7 +1185,7 @@ k_plan_small(FanIn f, DevWS ws, int E, int k, int inter, int shared_inter, int h
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024)
 k_plan_grouped(FanIn f, DevWS ws, int E, int inter, int shared_inter, int hidden, int has_shared,
-               int bn, GemmPlan* plan1, GemmPlan* plan2) {
+               int bn, GemmPlan* plan1, GemmPlan* plan2, WinGeom g, int row_bytes, int in_place) {
   grid_dep_wait();
   grid_dep_launch();
   __shared__ int cnt[256];
@@ -1221,20 +1229,65 @@ k_plan_grouped(FanIn f, DevWS ws, int E, int inter, int shared_inter, int hidden
     if (e < E) ws.counts[e] = cnt[e];
   }
   __syncthreads();
-  for (int r = tid; r < f.rtotal; r += blockDim.x) {
-    const int i = entry_of_rows(f, r);
-    const int lr = r - f.rprefix[i];
-    const int* gp = gpre + i * E;
-    int lo = 0, hi = E - 1;  // the last expert whose first row is <= lr (that one is not empty)
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (gp[mid] <= lr) lo = mid; else hi = mid - 1;
-    }
-    const int pos = base[i * E + lo] + (lr - gp[lo]);
-    ws.perm[pos] = r;
-    ws.inv[r] = pos;
+  if (!in_place) {  // the gather places each row (and records perm / inv)
+    if (tid == 0) write_tile_tables(f, 1, E, inter, shared_inter, hidden, has_shared, bn, cnt, offs, plan1, plan2);
+    return;
   }
-  if (tid == 0) write_tile_tables(f, 1, E, inter, shared_inter, hidden, has_shared, bn, cnt, offs, plan1, plan2);
+  // the entries' group lists in shared memory for the one-thread table walk
+  // (in place: n_peers * E <= AFD_MAX_GROUPS)
+  __shared__ int gl_s[AFD_MAX_GROUPS];
+  for (int x = tid; x < f.n_peers * E && x < AFD_MAX_GROUPS; x += blockDim.x) gl_s[x] = ws.peer_counts[x];
+  __syncthreads();
+  if (tid != 0) return;
+  // In place: one group per (entry, expert) with rows, whose rows are
+  // contiguous in the entry's dispatch slot (the SwiGLU GEMM reads them
+  // there, the down GEMM writes their outputs straight into the entry's
+  // return slot), then one shared group per entry with shared rows (read
+  // from its shared_x, outputs into its return shared_x).  h / hs rows
+  // follow the groups' order.
+  int tiles1 = 0, tiles2 = 0, units1 = 0, units2 = 0, ng = 0, hrow = 0;
+  const int mt1 = (inter + 63) / 64, mt2 = (hidden + 127) / 128;
+  for (int i = 0; i < f.n_peers; i++)
+    for (int e = 0, lr0 = 0; e < E; lr0 += gl_s[i * E + e], e++) {
+      const int rows = gl_s[i * E + e];
+      if (!rows) continue;
+      const int nt = (rows + bn - 1) / bn;
+      GemmGroup a{rows, window_row(g, f.region[i], f.stage, g.routed_x, lr0, row_bytes), hrow, e, 0,
+                  mt1, nt, tiles1, units1};
+      GemmGroup b{rows, hrow, window_row(g, f.region[i], f.stage, g.routed_x, lr0, row_bytes), e, 0,
+                  mt2, nt, tiles2, units2};
+      plan1->g[ng] = a;
+      plan2->g[ng] = b;
+      tiles1 += mt1 * nt;
+      tiles2 += mt2 * nt;
+      units1 += (mt1 + 1) / 2 * nt;
+      units2 += (mt2 + 1) / 2 * nt;
+      hrow += rows;
+      ng++;
+    }
+  if (has_shared)
+    for (int i = 0; i < f.n_peers; i++) {
+      const int rows = ws.peer_shared[i] ? f.prefix[i + 1] - f.prefix[i] : 0;
+      if (!rows) continue;
+      const int nt = (rows + bn - 1) / bn;
+      const int mts = (shared_inter + 63) / 64;
+      const int wr = window_row(g, f.region[i], f.stage, g.shared_x, 0, row_bytes);
+      GemmGroup a{rows, wr, f.prefix[i], 0, 1, mts, nt, tiles1, units1};
+      GemmGroup b{rows, f.prefix[i], wr, 0, 1, mt2, nt, tiles2, units2};
+      plan1->g[ng] = a;
+      plan2->g[ng] = b;
+      tiles1 += mts * nt;
+      tiles2 += mt2 * nt;
+      units1 += (mts + 1) / 2 * nt;
+      units2 += (mt2 + 1) / 2 * nt;
+      ng++;
+    }
+  plan1->ngroups = plan2->ngroups = ng;
+  plan1->total_tiles = tiles1;
+  plan2->total_tiles = tiles2;
+  plan1->total_units = units1;
+  plan2->total_units = units2;
+  plan1->bn = plan2->bn = bn;
 }
 
 // ---------------------------------------------------------------------------
@@ -1305,11 +1358,25 @@ k_gather(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int k, int row_bytes,
     uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(ws.xp) + (int64_t)r * row_bytes);
     int i, local;
     int64_t field;
-    if (r < N && f.grouped) {  // routed row perm[r] of the concatenation of the entries' rows
-      const int gr = ws.perm[r];
-      i = entry_of_rows(f, gr);
-      local = gr - f.rprefix[i];
+    if (r < N && f.grouped) {
+      // source row r of the entries' concatenation goes to position
+      // base[i][e] + (its row within the entry's expert-e group)
+      i = entry_of_rows(f, r);
+      local = r - f.rprefix[i];
       field = g.routed_x;
+      const int E = f.num_experts;
+      const int* gp = ws.gbase + AFD_MAX_PEERS * E + i * E;
+      int lo = 0, hi = E - 1;  // the last expert whose first row is <= local (not empty)
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (gp[mid] <= local) lo = mid; else hi = mid - 1;
+      }
+      const int pos = ws.gbase[i * E + lo] + (local - gp[lo]);
+      dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(ws.xp) + (int64_t)pos * row_bytes);
+      if ((threadIdx.x & 31) == 0) {
+        ws.perm[pos] = r;
+        ws.inv[r] = pos;
+      }
     } else {
       const int t = r < N ? ws.perm[r] / k : r - N;
       i = entry_of(f, t);
@@ -1918,9 +1985,10 @@ cudaError_t launch_unpack(const LaunchCtx& lc, const WinGeom& g, const uint8_t* 
 
 cudaError_t launch_plan_grouped(const LaunchCtx& lc, const FanIn& f, const DevWS& ws, int E,
                                 int inter, int shared_inter, int hidden, int has_shared, int bn,
-                                GemmPlan* plan1, GemmPlan* plan2) {
+                                GemmPlan* plan1, GemmPlan* plan2, const WinGeom& g, int row_bytes,
+                                int in_place) {
   return launch_k(lc, k_plan_grouped, 1, 1024, 0, f, ws, E, inter, shared_inter, hidden, has_shared,
-                  bn, plan1, plan2);
+                  bn, plan1, plan2, g, row_bytes, in_place);
 }
 
 cudaError_t launch_scatter_grouped(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret,

@@ -156,3 +156,12 @@ def test_grouped_bad_group_list_is_a_device_error():
     assert run.poll() == A.AFD_ERR_SHAPE
     ret = run.window(A.AFD_DIR_RETURN).cpu().numpy()
     assert ret[:8].view(np.uint64)[0] == 0
+
+
+@pytest.mark.parametrize("gemm", [A.AFD_GEMM_TENSOR, A.AFD_GEMM_TENSOR_1CTA])
+@pytest.mark.parametrize("with_shared", [True, False])
+def test_grouped_single_peer_in_place(gemm, with_shared):
+    """One peer: the GEMMs read its grouped rows in its dispatch slot and write
+    the outputs into its return slot (no gather, no scatter)."""
+    w = W.custom("fanin", seq_lens=[91], token_cap=384)
+    compare(w, *run_grouped(w, seed=9, gemm=gemm, with_shared=with_shared))

@@ -34,7 +34,7 @@ class Runner:
     layer weights registered, and helpers for pack / forward / unpack."""
 
     def __init__(self, w: W.Workload, gemm=A.AFD_GEMM_TENSOR, layers=None, stream=None,
-                 max_total_tokens=0, wait_timeout_ns=0, device="cuda", flags=0):
+                 max_total_tokens=0, wait_timeout_ns=0, device="cuda", flags=0, ring_depth=1):
         import torch
         self.w = w
         self.device = device
@@ -44,7 +44,8 @@ class Runner:
                                  w.inter, w.shared_inter, act=w.act, renorm=w.renorm,
                                  routed_scaling=w.routed_scaling, max_layers=self.layers,
                                  max_total_tokens=max_total_tokens, gemm=gemm,
-                                 wait_timeout_ns=wait_timeout_ns, flags=flags)
+                                 wait_timeout_ns=wait_timeout_ns, flags=flags,
+                                 ring_depth=ring_depth)
         self.ctx = A.afd_create(self.cfg, self.stream.cuda_stream)
         self.layout = A.afd_slot_layout(self.cfg)
         self.host = W.host_inputs(w)
@@ -156,7 +157,8 @@ class Runner:
 
     def oracle_cfg(self):
         w = self.w
-        return dict(num_regions=w.num_peers, ring_depth=1, token_cap=w.token_cap, hidden=w.hidden,
+        return dict(num_regions=w.num_peers, ring_depth=self.cfg.ring_depth, token_cap=w.token_cap,
+                    hidden=w.hidden,
                     act_bytes=w.act_bytes, num_experts=w.num_experts, topk=w.topk, inter=w.inter,
                     shared_inter=w.shared_inter, renorm=w.renorm,
                     max_total_tokens=self.cfg.max_total_tokens, routed_scaling=w.routed_scaling)

@@ -24,6 +24,7 @@ AFD_HEADER_FIXED_WORDS = 12
 AFD_NOALLOC_MAX_ROUTER_WEIGHTS = 262144
 AFD_NOALLOC_MAX_LOGITS = 1048576
 AFD_MAX_PEERS = 64
+AFD_FORM_TOKENS, AFD_FORM_GROUPED = 0, 1
 
 
 class afd_config(C.Structure):
@@ -85,6 +86,13 @@ SIGNATURES = [
     ("afd_profile", _I, [_P, _I]),
     ("afd_route_noalloc", _I, [_P, _I, _I, _I, _P, _P, _I, _I, _I, _F, _P, _P, _P]),
     ("afd_stage_times", _I, [_P, C.POINTER(C.c_float), _I, C.POINTER(C.c_int64)]),
+    ("afd_ffn_serve", _I, [_P, C.POINTER(C.c_int), _I, _I, _I]),
+    ("afd_serve_graph_create", _I, [_P, C.POINTER(C.c_int), _I, _I, _I, C.POINTER(_P),
+                                    C.POINTER(_I64)]),
+    ("afd_serve_graph_launch", _I, [_P]),
+    ("afd_serve_graph_destroy", None, [_P]),
+    ("afd_serve_log", _I, [_P, C.POINTER(C.c_int32), _I, C.POINTER(C.c_int),
+                           C.POINTER(_I64)]),
 ]
 AFD_NUM_STAGES = 8
 STAGE_NAMES = ("header_check", "router", "plan", "gather", "gemm_swiglu", "gemm_down",
@@ -249,3 +257,33 @@ def afd_route_noalloc(x_ptr, n_tokens, hidden, act_dtype, Wg_ptr, bias_ptr, num_
                                    int(topk), int(bool(renorm)), float(routed_scaling),
                                    ids_ptr or None, weights_ptr or None,
                                    C.c_void_p(int(stream)))
+
+
+def afd_ffn_serve(ctx, slots, n_items, form=AFD_FORM_TOKENS):
+    """n_items steps of the device-resident work-item loop over the peers in slots."""
+    return lib().afd_ffn_serve(ctx, _ints(slots), len(slots), int(n_items), int(form))
+
+
+def afd_serve_graph_create(ctx, slots, n_items, form=AFD_FORM_TOKENS):
+    """(status, graph handle, kernels in the graph)"""
+    g, k = C.c_void_p(), C.c_int64(0)
+    rc = lib().afd_serve_graph_create(ctx, _ints(slots), len(slots), int(n_items), int(form),
+                                      C.byref(g), C.byref(k))
+    return rc, g, int(k.value)
+
+
+def afd_serve_graph_launch(graph):
+    return lib().afd_serve_graph_launch(graph)
+
+
+def afd_serve_graph_destroy(graph):
+    lib().afd_serve_graph_destroy(graph)
+
+
+def afd_serve_log(ctx, max_records=64):
+    """(records [(stage, layer, tokens, rows)] oldest first, items served)"""
+    recs = (C.c_int32 * (4 * max(max_records, 1)))()
+    n, served = C.c_int(0), C.c_int64(0)
+    _check(lib().afd_serve_log(ctx, recs, int(max_records), C.byref(n), C.byref(served)),
+           "afd_serve_log")
+    return [tuple(recs[4 * j:4 * j + 4]) for j in range(n.value)], int(served.value)

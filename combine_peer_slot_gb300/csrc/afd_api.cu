@@ -168,6 +168,7 @@ struct afd_ctx {
   DevWS ws;
   GemmPlan* plan1 = nullptr;
   GemmPlan* plan2 = nullptr;
+  DevLayer* dlayers = nullptr;       // device copy of every layer's weights (work-item loop)
   CUtensorMap tmXp, tmH, tmHs;        // token boxes of the tensor engine
   CUtensorMap tmXp32, tmH32, tmHs32;  // 32-row boxes (small SM-pair units)
   CUtensorMap tmWin, tmWin32;         // dispatch window as [rows, hidden] (grouped form in place)
@@ -349,7 +350,10 @@ int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out) {
       {(int64_t)sizeof(GemmPlan)}, {(int64_t)sizeof(GemmPlan)},
       {E * router_blocks((int)Tm) * 4}, {E * router_blocks((int)Tm) * 4},  // hist, base
       {Tm * E * 4},                          // router logits
-      {2 * AFD_MAX_PEERS * E * 4}};          // grouped-form bases and group-list prefixes
+      {2 * AFD_MAX_PEERS * E * 4},           // grouped-form bases and group-list prefixes
+      {(int64_t)sizeof(FanIn)},              // the fan-in of the step in flight
+      {AFD_LOOP_WORDS * 4},                  // work-item loop state and log
+      {(int64_t)cfg->max_layers * (int64_t)sizeof(DevLayer)}};  // per-layer weight table
   const int nparts = sizeof(parts) / sizeof(parts[0]);
   int64_t offs[32], total = 0;
   for (int i = 0; i < nparts; i++) {
@@ -381,6 +385,10 @@ int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out) {
   c->ws.base = reinterpret_cast<int32_t*>(b + offs[19]);
   c->ws.logits = reinterpret_cast<float*>(b + offs[20]);
   c->ws.gbase = reinterpret_cast<int32_t*>(b + offs[21]);
+  c->ws.item = reinterpret_cast<FanIn*>(b + offs[22]);
+  c->ws.loop = reinterpret_cast<int32_t*>(b + offs[23]);
+  c->dlayers = reinterpret_cast<DevLayer*>(b + offs[24]);
+  c->ws.layers = c->dlayers;
   c->plan1 = reinterpret_cast<GemmPlan*>(b + offs[16]);
   c->plan2 = reinterpret_cast<GemmPlan*>(b + offs[17]);
   const int ws_map[12] = {4, 5, 6, 7, 8, 9, 11, 12, 13, 14, 15, 0};
@@ -450,6 +458,25 @@ int afd_set_layer(afd_ctx* ctx, int layer, const float* Wg, const float* bias, c
     }
     if (rc) return rc;
   }
+  // the device table entry, for steps whose layer the device chooses (a
+  // pageable source: the copy is staged before the call returns)
+  DevLayer d;
+  memset(&d, 0, sizeof d);
+  d.tmA1[0] = L.tmA1[0];
+  d.tmA1[1] = L.tmA1[1];
+  d.tmA2[0] = L.tmA2[0];
+  d.tmA2[1] = L.tmA2[1];
+  d.WgQ = L.WgQ;
+  d.bias = L.bias;
+  d.W13 = L.W13;
+  d.W13s = L.W13s;
+  d.Wd = L.Wd;
+  d.Wds = L.Wds;
+  d.set = 1;
+  rc = cuda_fail(cudaMemcpyAsync(ctx->dlayers + layer, &d, sizeof d, cudaMemcpyHostToDevice,
+                                 ctx->stream),
+                 "layer table");
+  if (rc) return rc;
   L.set = true;
   return AFD_OK;
 }
@@ -561,14 +588,14 @@ static int fanin_of(afd_ctx* ctx, int stage, const int* seq_lens, const int* slo
   return AFD_OK;
 }
 
-static int forward_impl(afd_ctx* ctx, int layer, FanIn& f);
+static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev);
 
 int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, const int* slots,
                     int n_peers) {
   FanIn f;
   const int rc = fanin_of(ctx, stage, seq_lens, slots, n_peers, f);
   if (rc) return rc;
-  return forward_impl(ctx, layer, f);
+  return forward_impl(ctx, layer, f, nullptr);
 }
 
 int afd_ffn_forward_grouped(afd_ctx* ctx, int layer, int stage, const int* n_rows,
@@ -589,10 +616,151 @@ int afd_ffn_forward_grouped(afd_ctx* ctx, int layer, int stage, const int* n_row
   f.rtotal = (int)R;
   f.grouped = 1;
   f.num_experts = ctx->cfg.num_experts;
-  return forward_impl(ctx, layer, f);
+  return forward_impl(ctx, layer, f, nullptr);
 }
 
-static int forward_impl(afd_ctx* ctx, int layer, FanIn& f) {
+// Launch shapes of a work-item loop step over the listed peers: the most
+// tokens (and grouped rows) a step may carry; the device fills in the rest.
+static int serve_shape(afd_ctx* ctx, const int* slots, int n_peers, int form, PeerList& pl,
+                       FanIn& fs) {
+  if (!ctx || !slots || (form != AFD_FORM_TOKENS && form != AFD_FORM_GROUPED)) return AFD_ERR_ARG;
+  const afd_config& c = ctx->cfg;
+  if (n_peers <= 0 || n_peers > c.num_peers) return AFD_ERR_ARG;
+  memset(&pl, 0, sizeof pl);
+  memset(&fs, 0, sizeof fs);
+  pl.n = n_peers;
+  for (int i = 0; i < n_peers; i++) {
+    if (slots[i] < 0 || slots[i] >= c.num_peers) return AFD_ERR_ARG;
+    for (int j = 0; j < i; j++)
+      if (slots[j] == slots[i]) return AFD_ERR_ARG;
+    pl.slot[i] = slots[i];
+    fs.region[i] = slots[i];
+  }
+  fs.n_peers = n_peers;
+  fs.dev = 1;  // the kernels take the step's values from ws.item
+  const int64_t cap = (int64_t)n_peers * c.token_cap;
+  fs.total = (int)std::min<int64_t>(ctx->tmax, cap);
+  fs.prefix[n_peers] = fs.total;
+  if (form == AFD_FORM_GROUPED) {
+    fs.grouped = 1;
+    fs.num_experts = c.num_experts;
+    fs.rtotal = (int)std::min<int64_t>((int64_t)ctx->tmax * c.topk, cap);
+    fs.rprefix[n_peers] = fs.rtotal;
+  }
+  return AFD_OK;
+}
+
+int afd_ffn_serve(afd_ctx* ctx, const int* slots, int n_peers, int n_items, int form) {
+  PeerList pl;
+  FanIn fs;
+  int rc = serve_shape(ctx, slots, n_peers, form, pl, fs);
+  if (rc) return rc;
+  if (n_items < 0) return AFD_ERR_ARG;
+  for (int it = 0; it < n_items && !rc; it++) {
+    FanIn f = fs;
+    rc = forward_impl(ctx, -1, f, &pl);
+  }
+  return rc;
+}
+
+struct afd_serve_graph {
+  afd_ctx* ctx = nullptr;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  int n_items = 0;
+};
+
+int afd_serve_graph_create(afd_ctx* ctx, const int* slots, int n_peers, int n_items, int form,
+                           afd_serve_graph** out, int64_t* kernels) {
+  if (!out) return AFD_ERR_ARG;
+  *out = nullptr;
+  PeerList pl;
+  FanIn fs;
+  int rc = serve_shape(ctx, slots, n_peers, form, pl, fs);
+  if (rc) return rc;
+  if (n_items <= 0) return AFD_ERR_ARG;
+  // captured on a stream of its own (the caller's may be the legacy
+  // stream, which cannot be captured); replayed on the context's stream
+  cudaStream_t cap = nullptr;
+  rc = cuda_fail(cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking), "capture stream");
+  if (rc) return rc;
+  cudaStream_t user = ctx->stream;
+  const bool prof = ctx->profiling;
+  ctx->stream = cap;
+  ctx->profiling = false;
+  const int64_t before = ctx->launches;
+  const int64_t fwd = ctx->forwards;
+  cudaGraph_t graph = nullptr;
+  rc = cuda_fail(cudaStreamBeginCapture(cap, cudaStreamCaptureModeRelaxed), "begin capture");
+  if (!rc) {
+    int frc = AFD_OK;
+    for (int it = 0; it < n_items && !frc; it++) {
+      FanIn f = fs;
+      frc = forward_impl(ctx, -1, f, &pl);
+    }
+    rc = cuda_fail(cudaStreamEndCapture(cap, &graph), "end capture");
+    if (!rc) rc = frc;
+  }
+  ctx->stream = user;
+  ctx->profiling = prof;
+  ctx->forwards = fwd;
+  const int64_t captured = ctx->launches - before;
+  ctx->launches = before;
+  cudaStreamDestroy(cap);
+  cudaGraphExec_t exec = nullptr;
+  if (!rc) rc = cuda_fail(cudaGraphInstantiate(&exec, graph, 0), "graph instantiate");
+  if (rc) {
+    if (graph) cudaGraphDestroy(graph);
+    return rc;
+  }
+  afd_serve_graph* g = new afd_serve_graph();
+  g->ctx = ctx;
+  g->graph = graph;
+  g->exec = exec;
+  g->n_items = n_items;
+  if (kernels) *kernels = captured;
+  *out = g;
+  return AFD_OK;
+}
+
+int afd_serve_graph_launch(afd_serve_graph* g) {
+  if (!g || !g->ctx) return AFD_ERR_ARG;
+  const int rc = cuda_fail(cudaGraphLaunch(g->exec, g->ctx->stream), "graph launch");
+  if (!rc) g->ctx->forwards += g->n_items;
+  return rc;
+}
+
+void afd_serve_graph_destroy(afd_serve_graph* g) {
+  if (!g) return;
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  if (g->graph) cudaGraphDestroy(g->graph);
+  delete g;
+}
+
+int afd_serve_log(afd_ctx* ctx, int32_t* records, int max_records, int* n_records,
+                  int64_t* n_served) {
+  if (!ctx || !n_records || max_records < 0 || (max_records > 0 && !records)) return AFD_ERR_ARG;
+  if (cuda_fail(cudaStreamSynchronize(ctx->stream), "stream sync")) return AFD_ERR_CUDA;
+  int32_t w[AFD_LOOP_WORDS];
+  if (cuda_fail(cudaMemcpy(w, ctx->ws.loop, sizeof w, cudaMemcpyDeviceToHost), "loop log read"))
+    return AFD_ERR_CUDA;
+  const int count = w[AFD_LOOP_COUNT];
+  if (n_served) *n_served = count;
+  const int n = std::min(std::min(max_records, count), AFD_LOOP_LOG_N);
+  for (int j = 0; j < n; j++) {  // the last n items, oldest first
+    const int idx = (count - n + j) % AFD_LOOP_LOG_N;
+    for (int q = 0; q < 4; q++) records[4 * j + q] = w[AFD_LOOP_LOG + 4 * idx + q];
+  }
+  *n_records = n;
+  return AFD_OK;
+}
+
+// One FFN step.  dev == nullptr: the host describes it (f, layer).  Else a
+// step of the work-item loop over the peers in *dev: the device chooses the
+// stage and takes the layer and the counts from the headers; f then holds
+// only the launch shapes (the most tokens and rows a step may carry), and
+// the weights come from the device layer table.
+static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) {
   const afd_config& c = ctx->cfg;
   f.layer = layer;
   const int64_t T = f.total;
@@ -606,8 +774,8 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f) {
   const bool in_place = grouped && c.gemm != AFD_GEMM_SIMT && f.n_peers == 1;
   // routed rows: T * k partials, or the rows the peers sent already grouped
   const int64_t N = grouped ? f.rtotal : T * c.topk;
-  if (layer < 0 || layer >= c.max_layers || !ctx->layers[layer].set) return AFD_ERR_LAYER;
-  const LayerW& L = ctx->layers[layer];
+  if (!dev && (layer < 0 || layer >= c.max_layers || !ctx->layers[layer].set)) return AFD_ERR_LAYER;
+  const LayerW* L = dev ? nullptr : &ctx->layers[layer];
   const int has_shared = c.shared_inter > 0;
   const int ab = ctx->act_f32 ? 4 : 2;
   const int row_bytes = c.hidden * ab;
@@ -630,15 +798,22 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f) {
       if (armed) cudaStreamWaitEvent(ctx->stream, ctx->ev_join, 0);
     }
   } join{ctx};
-  ctx->mark(0);
-  rc = cuda_fail(launch_header_check(lc, ctx->geom, ctx->win[0], f, ws, c.num_experts,
-                                         c.token_cap, has_shared, ctx->timeout()),
-                     "header check");
+  // stage timing marks only for host-described steps
+  auto mark = [&](int i) {
+    if (!dev) ctx->mark(i);
+  };
+  mark(0);
+  rc = cuda_fail(dev ? launch_item_head(lc, ctx->geom, ctx->win[0], *dev, ws, c.num_experts,
+                                        c.token_cap, has_shared, grouped, ctx->tmax,
+                                        ctx->tmax * c.topk, c.max_layers, ctx->timeout())
+                     : launch_header_check(lc, ctx->geom, ctx->win[0], f, ws, c.num_experts,
+                                           c.token_cap, has_shared, ctx->timeout()),
+                 "header check");
   if (rc) return rc;
-  ctx->mark(1);
+  mark(1);
   if (!grouped) {  // the grouped form arrives routed
-    rc = cuda_fail(launch_router(lc, ctx->geom, ctx->win[0], f, ws, c.hidden, ctx->act_f32, L.WgQ,
-                                 L.bias, c.num_experts, c.topk, c.renorm, c.routed_scaling,
+    rc = cuda_fail(launch_router(lc, ctx->geom, ctx->win[0], f, ws, c.hidden, ctx->act_f32,
+                                 L ? L->WgQ : nullptr, L ? L->bias : nullptr, c.num_experts, c.topk, c.renorm, c.routed_scaling,
                                  ws.logits, ws.hist),
                    "router");
     if (rc) return rc;
@@ -651,12 +826,13 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f) {
     side.pdl = 0;
     rc = cuda_fail(cudaEventRecord(ctx->ev_fork, ctx->stream), "fork");
     if (!rc) rc = cuda_fail(cudaStreamWaitEvent(ctx->side, ctx->ev_fork, 0), "fork");
-    if (!rc) rc = cuda_fail(launch_prefetch_l2(side, L.W13, std::min(first_wave, w13)), "prefetch");
+    if (!rc) rc = cuda_fail(launch_prefetch_l2(side, L ? L->W13 : nullptr, std::min(first_wave, w13), ws),
+                              "prefetch");
     if (!rc) rc = cuda_fail(cudaEventRecord(ctx->ev_join, ctx->side), "join");
     if (rc) return rc;
     join.armed = true;
   }
-  ctx->mark(2);
+  mark(2);
   rc = cuda_fail(grouped ? launch_plan_grouped(lc, f, ws, c.num_experts, c.inter, c.shared_inter,
                                                 c.hidden, has_shared, bn, ctx->plan1, ctx->plan2,
                                                 ctx->geom, row_bytes, in_place)
@@ -665,20 +841,26 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f) {
                                        ws.base),
                  "plan");
   if (rc) return rc;
-  ctx->mark(3);
+  mark(3);
   if (!in_place) {
     rc = cuda_fail(launch_gather(lc, ctx->geom, ctx->win[0], f, ws, c.topk, row_bytes, has_shared),
                    "gather");
     if (rc) return rc;
   }
-  ctx->mark(4);
+  mark(4);
   if (N + T > 0) {
     if (c.gemm != AFD_GEMM_SIMT) {
       auto launch = c.gemm == AFD_GEMM_TENSOR ? launch_gemm_tc2 : launch_gemm_tc;
       GemmArgs a1;
       memset(&a1, 0, sizeof a1);
-      a1.tmA[0] = L.tmA1[0];
-      a1.tmA[1] = L.tmA1[1];
+      if (L) {
+        a1.tmA[0] = L->tmA1[0];
+        a1.tmA[1] = L->tmA1[1];
+      } else {
+        a1.layers = ws.layers;
+        a1.item = ws.item;
+        a1.wsel = 1;
+      }
       const CUtensorMap& tb = in_place ? ctx->tmWin : ctx->tmXp;
       const CUtensorMap& tbs = in_place ? ctx->tmWin32 : ctx->tmXp32;
       a1.tmB[0] = a1.tmB[1] = tb;
@@ -697,11 +879,17 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f) {
       a1.timeout_ns = ctx->timeout();
       rc = cuda_fail(launch(lc, a1), "gemm1");
       if (rc) return rc;
-      ctx->mark(5);
+      mark(5);
       GemmArgs a2;
       memset(&a2, 0, sizeof a2);
-      a2.tmA[0] = L.tmA2[0];
-      a2.tmA[1] = L.tmA2[1];
+      if (L) {
+        a2.tmA[0] = L->tmA2[0];
+        a2.tmA[1] = L->tmA2[1];
+      } else {
+        a2.layers = ws.layers;
+        a2.item = ws.item;
+        a2.wsel = 2;
+      }
       a2.tmB[0] = ctx->tmH;
       a2.tmB[1] = ctx->tmHs;
       a2.tmBs[0] = ctx->tmH32;
@@ -728,8 +916,14 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f) {
     } else {
       SimtArgs s1;
       memset(&s1, 0, sizeof s1);
-      s1.A[0] = L.W13;
-      s1.A[1] = L.W13s;
+      if (L) {
+        s1.A[0] = L->W13;
+        s1.A[1] = L->W13s;
+      } else {
+        s1.layers = ws.layers;
+        s1.item = ws.item;
+        s1.wsel = 1;
+      }
       s1.B[0] = s1.B[1] = ws.xp;
       s1.ldb[0] = s1.ldb[1] = c.hidden;
       s1.out[0] = ws.h;
@@ -746,10 +940,14 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f) {
       s1.status = ws.status;
       rc = cuda_fail(launch_gemm_simt(lc, s1, c.num_experts + 1), "simt gemm1");
       if (rc) return rc;
-      ctx->mark(5);
+      mark(5);
       SimtArgs s2 = s1;
-      s2.A[0] = L.Wd;
-      s2.A[1] = L.Wds;
+      if (L) {
+        s2.A[0] = L->Wd;
+        s2.A[1] = L->Wds;
+      } else {
+        s2.wsel = 2;
+      }
       s2.B[0] = ws.h;
       s2.B[1] = ws.hs;
       s2.ldb[0] = c.inter;
@@ -768,9 +966,9 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f) {
       if (rc) return rc;
     }
   } else {
-    ctx->mark(5);
+    mark(5);
   }
-  ctx->mark(6);
+  mark(6);
   // the grouped form returns the expert outputs row by row (the Attention
   // side weights and combines); the token form combines here
   rc = cuda_fail(grouped ? (in_place ? cudaSuccess
@@ -780,13 +978,13 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f) {
                                           ctx->act_f32, has_shared, ctx->act_f32),
                  grouped ? "scatter" : "combine");
   if (rc) return rc;
-  ctx->mark(7);
+  mark(7);
   rc = cuda_fail(launch_return_header(lc, ctx->geom, ctx->win[1], ctx->win[0], f, ws, c.num_experts,
                                       c.topk),
                  "return header");
   if (rc) return rc;
-  ctx->mark(8);
-  ctx->last_T = (int)T;
+  mark(8);
+  ctx->last_T = dev ? -1 : (int)T;
   ctx->forwards++;
   return AFD_OK;
 }

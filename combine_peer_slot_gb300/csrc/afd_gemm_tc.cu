@@ -158,6 +158,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_gemm_tc(const __grid_constan
   __syncthreads();
   if (tail->skip || plan.total_tiles <= (int)blockIdx.x) return;  // uniform for the CTA
 
+  // weight maps: the kernel's own, or the device table's entry for the layer
+  // the device chose for this step (host-written before any launch)
+  const CUtensorMap* tmA = args.tmA;
+  if (args.layers) {
+    const DevLayer& Ld = args.layers[args.item->layer];
+    tmA = args.wsel == 1 ? Ld.tmA1 : Ld.tmA2;
+  }
+
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&tail->tmem_base)),
@@ -187,7 +195,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_gemm_tc(const __grid_constan
         const int nkb = (args.K[t.kind] + BK - 1) / BK;
         const int nb = (t.rows + B_BOX_ROWS - 1) / B_BOX_ROWS;
         const int brow = G.b_row0 + t.nt * plan.bn;
-        const CUtensorMap* ta = &args.tmA[t.kind];
+        const CUtensorMap* ta = tmA + t.kind;
         const CUtensorMap* tb = &args.tmB[t.kind];
         for (int kb = 0; kb < nkb; kb++) {
           if (!wait_bar(smem_u32(&tail->empty[s]), ph ^ 1, abort_flag, deadline, args.status)) { ok = false; break; }

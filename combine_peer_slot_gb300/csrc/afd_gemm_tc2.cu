@@ -257,6 +257,14 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
   cluster_sync();  // both flags read before either CTA may leave
   if (tail->skip || peer_skip || total <= cid) return;
 
+  // weight maps: the kernel's own, or the device table's entry for the layer
+  // the device chose for this step (host-written before any launch)
+  const CUtensorMap* tmA = args.tmA;
+  if (args.layers) {
+    const DevLayer& Ld = args.layers[args.item->layer];
+    tmA = args.wsel == 1 ? Ld.tmA1 : Ld.tmA2;
+  }
+
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&tail->tmem_base)),
@@ -288,7 +296,7 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
         const bool small_box = kNarrow || half <= SMALL_BOX_ROWS;
         const uint32_t b_bytes = small_box ? SMALL_BOX_BYTES : R::B_BYTES;
         const int mt = 2 * t.mpair + (int)rank;
-        const CUtensorMap* ta = &args.tmA[t.kind];
+        const CUtensorMap* ta = tmA + t.kind;
         const CUtensorMap* tb = small_box ? &args.tmBs[t.kind] : &args.tmB[t.kind];
         bool ok = true;
         for (int kb = 0; kb < nkb; kb += R::KPS) {

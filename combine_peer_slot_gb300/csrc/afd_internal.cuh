@@ -13,8 +13,12 @@
 #define AFD_MAX_GROUPS 320   // routed experts (<= 256) + one shared group
 
 // ---------------------------------------------------------------------------
-// per-forward fan-in description, passed by value.  Data on the wire, step
-// 3: the input is the concatenation of the listed peers' rows in list order.
+// per-forward fan-in description (Data on the wire, step 3: the input is the
+// concatenation of the listed peers' rows in list order).  The host
+// describes it for afd_ffn_forward and passes it by value to every kernel of
+// the step.  In the work-item loop (dev set) the head kernel builds it from
+// the slot headers into the workspace (ws.item) and the kernels read it
+// there; the host's copy then gives only the launch shapes.
 // ---------------------------------------------------------------------------
 struct FanIn {
   int n_peers;
@@ -29,7 +33,37 @@ struct FanIn {
   int num_experts;                    // grouped form: E (row placement in the gather)
   int rtotal;
   int rprefix[AFD_MAX_PEERS + 1];
+  int dev;                            // 1: the step's values are in ws.item
 };
+
+// the listed peers of a work-item loop (the peers of one Attention replica)
+struct PeerList {
+  int n;
+  int slot[AFD_MAX_PEERS];
+};
+
+// per-layer weights as the kernels see them when the layer of a step is
+// chosen on the device: the TMA maps and plain pointers of every layer,
+// one entry per layer in device memory ("layer-select" operators of the
+// Async AFD RFC: the address table of every layer plus a device-side index)
+struct DevLayer {  // aligned as its tensor maps
+  CUtensorMap tmA1[2];    // SwiGLU GEMM weights: routed experts, shared expert
+  CUtensorMap tmA2[2];    // down GEMM weights
+  const float* WgQ;       // router weight, rearranged
+  const float* bias;
+  const void* W13;
+  const void* W13s;
+  const void* Wd;
+  const void* Wds;
+  int set;
+};
+
+// workspace words of the work-item loop
+#define AFD_LOOP_ROT 0        // stage the next scan starts at
+#define AFD_LOOP_COUNT 1      // items served so far
+#define AFD_LOOP_LOG 2        // AFD_LOOP_LOG_N records of 4 words: stage, layer, T, rows
+#define AFD_LOOP_LOG_N 64
+#define AFD_LOOP_WORDS (AFD_LOOP_LOG + 4 * AFD_LOOP_LOG_N)
 
 // group list carried by value into the header-writing kernel
 struct GroupList {
@@ -66,6 +100,9 @@ struct DevWS {
   int32_t* hist;          // [E, router CTAs] per-CTA expert histograms
   int32_t* base;          // [E, router CTAs] each CTA's first slot in each expert segment
   float* logits;          // [Tmax, E] router logits
+  FanIn* item;            // the fan-in of the step in flight
+  const DevLayer* layers; // [max_layers] per-layer weights
+  int32_t* loop;          // [AFD_LOOP_WORDS] work-item loop state and log
 };
 
 // one group of the grouped GEMM: rows of the B operand (tokens) that share
@@ -108,6 +145,11 @@ struct GemmArgs {
   int swiglu;             // 1: gate/up interleaved SwiGLU epilogue
   int bn;                 // the plan's token tile (rows per unit)
   int64_t timeout_ns;
+  // layer chosen on the device: tmA is ignored and the weight maps are
+  // layers[item->layer].tmA1 (wsel 1) or .tmA2 (wsel 2)
+  const DevLayer* layers;
+  const FanIn* item;
+  int wsel;
 };
 
 // SIMT GEMM arguments (fp32 activations, cross-check engine)
@@ -124,6 +166,11 @@ struct SimtArgs {
   int swiglu;
   const GemmPlan* plan;
   int32_t* status;
+  // layer chosen on the device: A is ignored; wsel 1 takes the layer's
+  // W13 / W13s, wsel 2 its Wd / Wds
+  const DevLayer* layers;
+  const FanIn* item;
+  int wsel;
 };
 
 // ---------------------------------------------------------------------------
@@ -303,9 +350,19 @@ cudaError_t launch_pack_payload(const LaunchCtx& lc, const WinGeom& g, uint8_t* 
 cudaError_t launch_pack_header(const LaunchCtx& lc, const WinGeom& g, uint8_t* win, int region,
                                int stage, int layer, int n, int with_shared, int num_experts,
                                uint64_t seq, int shutdown, int routed_tokens, const GroupList& gl);
+// host-described step: bounded flag waits and header checks of the listed
+// entries, then f is written to ws.item
 cudaError_t launch_header_check(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                                 const FanIn& f, const DevWS& ws, int num_experts,
                                 int token_cap, int has_shared_expert, int64_t timeout_ns);
+// device-chosen step: bounded wait for any stage whose listed peers have all
+// published, the fan-in built from their headers (token form, or the grouped
+// form when grouped is set), the same checks, then ws.item.  tmax / rmax: the
+// most tokens / grouped rows a step may carry; max_layers: the layer table's size.
+cudaError_t launch_item_head(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
+                             const PeerList& pl, const DevWS& ws, int num_experts, int token_cap,
+                             int has_shared_expert, int grouped, int tmax, int rmax,
+                             int max_layers, int64_t timeout_ns);
 // CTAs of the router for T tokens (16 tokens each); sizes the histograms
 int router_blocks(int total_tokens);
 size_t router_min_smem_bytes(int hidden, int E, int act_f32);
@@ -348,7 +405,9 @@ cudaError_t launch_plan_grouped(const LaunchCtx& lc, const FanIn& f, const DevWS
 cudaError_t launch_scatter_grouped(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret,
                                    const FanIn& f, const DevWS& ws, int hidden, int act_f32,
                                    int has_shared);
-// bytes: a multiple of 16 from a 16-byte aligned base
-cudaError_t launch_prefetch_l2(const LaunchCtx& lc, const void* base, int64_t bytes);
+// bytes: a multiple of 16 from a 16-byte aligned base; base NULL: the W13
+// of the layer in ws.item (nothing when the step has no routed rows)
+cudaError_t launch_prefetch_l2(const LaunchCtx& lc, const void* base, int64_t bytes,
+                               const DevWS& ws);
 cudaError_t launch_arrange_wg(const LaunchCtx& lc, const float* Wg, float* WgQ, int hidden,
                                 int E);

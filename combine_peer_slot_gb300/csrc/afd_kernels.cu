@@ -47,6 +47,24 @@ __device__ __forceinline__ int entry_of_rows(const FanIn& f, int r) {
   return lo;
 }
 
+// The fan-in of the step: the kernel argument for a host-described step
+// (kDev false), else the one the work-item head built in the workspace,
+// copied into shared memory by the whole CTA (every thread must call this,
+// before any early return) so that the per-row peer lookups stay on chip.
+template <bool kDev>
+__device__ __forceinline__ const FanIn& step_item(const FanIn& fp, const FanIn* g) {
+  if constexpr (kDev) {
+    __shared__ FanIn s;
+    constexpr int kWords = (int)(sizeof(FanIn) / 4);
+    for (int i = threadIdx.x; i < kWords; i += blockDim.x)
+      reinterpret_cast<int32_t*>(&s)[i] = reinterpret_cast<const int32_t*>(g)[i];
+    __syncthreads();
+    return s;
+  } else {
+    return fp;
+  }
+}
+
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
   return __uint_as_float((uint32_t)b << 16);
 }
@@ -112,21 +130,22 @@ __global__ void k_pack_header(uint8_t* win, WinGeom g, int region, int stage, in
 // ---------------------------------------------------------------------------
 // a0: bounded wait for each listed flag, then header checks.  The order of
 // the checks fixes which error is reported: the first failing check of the
-// first failing list entry.
+// first failing list entry, then item_err (a fault of the step as a whole).
+// kFromHeaders: f was built from these headers (work-item loop), so the
+// token and row counts are checked against the slot capacity instead of a
+// count the host gave.  Returns true (block-uniform) when every check passed;
+// the consumed flags are then recorded in ws.seen.
 // ---------------------------------------------------------------------------
-__global__ void k_header_check(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int E,
-                               int token_cap, int has_shared_expert, int64_t timeout_ns) {
-  grid_dep_wait();
-  grid_dep_launch();
+template <bool kFromHeaders>
+__device__ bool check_entries(const uint8_t* win, const WinGeom& g, const FanIn& f, const DevWS& ws,
+                              int E, int token_cap, int has_shared_expert, int64_t timeout_ns,
+                              int item_err) {
   __shared__ int err[AFD_MAX_PEERS];
   __shared__ int bad_sidx[AFD_MAX_PEERS];
   __shared__ int shared_n[AFD_MAX_PEERS];
-  __shared__ int skip;
   const int tid = threadIdx.x;
-  if (tid == 0) skip = read_status(ws.status);
   if (tid < AFD_MAX_PEERS) { err[tid] = 0; bad_sidx[tid] = 0; shared_n[tid] = 0; }
   __syncthreads();
-  if (skip) return;
   if (tid < f.n_peers) {
     const int i = tid;
     const int slotno = f.region[i] * g.ring_depth + f.stage;
@@ -167,11 +186,12 @@ __global__ void k_header_check(const uint8_t* win, WinGeom g, FanIn f, DevWS ws,
         e = AFD_ERR_LAYER;
       else if (h[6] != f.stage)
         e = AFD_ERR_STAGE;
-      else if (h[7] != n)
+      else if (kFromHeaders ? h[7] < 0 : h[7] != n)
         e = AFD_ERR_SHAPE;
       else if (h[7] > token_cap)
         e = AFD_ERR_CAPACITY;
-      else if (h[8] != (f.grouped ? f.rprefix[i + 1] - f.rprefix[i] : 0))
+      else if (kFromHeaders ? (h[8] < 0 || (!f.grouped && h[8] != 0))
+                            : h[8] != (f.grouped ? f.rprefix[i + 1] - f.rprefix[i] : 0))
         e = AFD_ERR_SHAPE;
       else if (h[8] > token_cap)
         e = AFD_ERR_CAPACITY;
@@ -239,6 +259,7 @@ __global__ void k_header_check(const uint8_t* win, WinGeom g, FanIn f, DevWS ws,
     }
   }
   __syncthreads();
+  __shared__ int ok_s;
   if (tid == 0) {
     int first = 0;
     for (int i = 0; i < f.n_peers && !first; i++) {
@@ -246,6 +267,7 @@ __global__ void k_header_check(const uint8_t* win, WinGeom g, FanIn f, DevWS ws,
       if (!e && bad_sidx[i]) e = AFD_ERR_SHAPE;
       first = e;
     }
+    if (!first) first = item_err;
     if (first) {
       set_error(ws.status, first);
     } else {
@@ -254,6 +276,133 @@ __global__ void k_header_check(const uint8_t* win, WinGeom g, FanIn f, DevWS ws,
         ws.peer_shared[i] = shared_n[i] > 0;
       }
     }
+    ok_s = !first;
+  }
+  __syncthreads();
+  return ok_s != 0;
+}
+
+// host-described step: f comes from the host, and so it does for the
+// kernels after this one
+__global__ void __launch_bounds__(1024)
+k_header_check(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn f, DevWS ws, int E,
+               int token_cap, int has_shared_expert, int64_t timeout_ns) {
+  grid_dep_wait();
+  grid_dep_launch();
+  __shared__ int skip;
+  const int tid = threadIdx.x;
+  if (tid == 0) skip = read_status(ws.status);
+  __syncthreads();
+  if (skip) return;
+  check_entries<false>(win, g, f, ws, E, token_cap, has_shared_expert, timeout_ns, 0);
+}
+
+// ---------------------------------------------------------------------------
+// Head of a step of the device-resident work-item loop ([RFC]: Async AFD
+// for Prefill on Ascend NPU, "Asynchronous work-item contract" and "FFN
+// execution modes"; [RFC]: Async GPU Connector, the wait_any kernel named
+// under "Risks and alternatives").  A stage of the ring is a work item; it
+// is ready once every listed peer has published a flag newer than the one
+// last consumed from its slot.  The scan starts after the stage served
+// last, so a ready stage waits for at most ring_depth - 1 others.  The wait
+// is bounded (AFD_ERR_TIMEOUT).  The layer and the token / row counts are
+// then taken from the headers, never read back by the host: the fan-in is
+// built here, checked like a host-described one, written to ws.item, and
+// the item is appended to the loop's log.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024)
+k_item_head(const uint8_t* win, WinGeom g, PeerList pl, DevWS ws, int E, int token_cap,
+            int has_shared_expert, int grouped, int tmax, int rmax, int max_layers,
+            int64_t timeout_ns) {
+  grid_dep_wait();
+  grid_dep_launch();
+  __shared__ FanIn fs;
+  __shared__ int hl[AFD_MAX_PEERS], hn[AFD_MAX_PEERS], hr[AFD_MAX_PEERS];
+  __shared__ int skip, rot, item_err;
+  const int tid = threadIdx.x;
+  const int R = g.ring_depth;
+  const uint64_t* flags = reinterpret_cast<const uint64_t*>(win);
+  if (tid == 0) {
+    skip = read_status(ws.status);
+    rot = ws.loop[AFD_LOOP_ROT];
+  }
+  __syncthreads();
+  if (skip) return;
+  // wait_any: block-uniform scan of the stages from rot
+  const uint64_t t0 = globaltimer_ns();
+  unsigned backoff = 32;
+  int chosen = -1;
+  for (;;) {
+    for (int s = 0; s < R && chosen < 0; s++) {
+      const int r = (rot + s) % R;
+      bool ready = true;
+      if (tid < pl.n) {
+        const int slotno = pl.slot[tid] * R + r;
+        ready = ld_acquire_u64(flags + slotno) > ws.seen[slotno];
+      }
+      if (__syncthreads_and(ready)) chosen = r;
+    }
+    if (chosen >= 0) break;
+    if (__syncthreads_or(tid == 0 && globaltimer_ns() - t0 > (uint64_t)timeout_ns)) break;
+    __nanosleep(backoff);
+    if (backoff < 1024) backoff <<= 1;
+  }
+  if (chosen < 0) {
+    if (tid == 0) set_error(ws.status, AFD_ERR_TIMEOUT);
+    return;
+  }
+  // layer and counts of every entry, ordered after its flag
+  if (tid < pl.n) {
+    (void)ld_acquire_u64(flags + pl.slot[tid] * R + chosen);
+    const int32_t* hp = reinterpret_cast<const int32_t*>(slot_ptr(win, g, pl.slot[tid], chosen) + g.header);
+    int32_t w5, w7, w8;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(w5) : "l"(hp + 5) : "memory");
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(w7) : "l"(hp + 7) : "memory");
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(w8) : "l"(hp + 8) : "memory");
+    hl[tid] = w5;
+    hn[tid] = w7;
+    hr[tid] = w8;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    fs.n_peers = pl.n;
+    fs.stage = chosen;
+    fs.layer = hl[0];
+    fs.grouped = grouped;
+    fs.num_experts = E;
+    int64_t T = 0, Rr = 0;
+    for (int i = 0; i < pl.n; i++) {
+      fs.region[i] = pl.slot[i];
+      fs.prefix[i] = (int)T;
+      fs.rprefix[i] = (int)Rr;
+      // out-of-range counts count as 0 here; the checks report them
+      T += (hn[i] >= 0 && hn[i] <= token_cap) ? hn[i] : 0;
+      Rr += (grouped && hr[i] >= 0 && hr[i] <= token_cap) ? hr[i] : 0;
+    }
+    fs.prefix[pl.n] = fs.total = (int)T;
+    fs.rprefix[pl.n] = fs.rtotal = (int)Rr;
+    const int L = fs.layer;
+    item_err = (L < 0 || L >= max_layers || !ws.layers[L].set) ? AFD_ERR_LAYER
+               : (T > tmax || Rr > rmax)                        ? AFD_ERR_CAPACITY
+                                                                : 0;
+  }
+  __syncthreads();
+  if (!check_entries<true>(win, g, fs, ws, E, token_cap, has_shared_expert, timeout_ns, item_err))
+    return;
+  {
+    const int32_t* src = reinterpret_cast<const int32_t*>(&fs);
+    int32_t* dst = reinterpret_cast<int32_t*>(ws.item);
+    for (int i = tid; i < (int)(sizeof(FanIn) / 4); i += blockDim.x) dst[i] = src[i];
+  }
+  if (tid == 0) {
+    ws.loop[AFD_LOOP_ROT] = (chosen + 1) % R;
+    const int c = ws.loop[AFD_LOOP_COUNT];
+    int32_t* rec = ws.loop + AFD_LOOP_LOG + 4 * (c % AFD_LOOP_LOG_N);
+    rec[0] = chosen;
+    rec[1] = fs.layer;
+    rec[2] = fs.total;
+    rec[3] = fs.rtotal;
+    ws.loop[AFD_LOOP_COUNT] = c + 1;
   }
 }
 
@@ -320,13 +469,18 @@ __device__ __forceinline__ int lg_index(int h, int tt, int hidden) {
 // 8 tokens; the token rows are staged from the peer slots into smem, the
 // transposed router weight [E][hidden] is read from L2 with the next step's
 // values loaded ahead of the current step's multiply-adds.
-template <typename XS>
+template <typename XS, bool kDev>
 __global__ void __launch_bounds__(kLgWarps * 32)
-k_router_logits(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int hidden,
+k_router_logits(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn fp, DevWS ws, int hidden,
                 const float* __restrict__ WgQ, const float* __restrict__ bias, int E,
                 float* __restrict__ logits) {
   grid_dep_wait();
   grid_dep_launch();
+  const FanIn& f = step_item<kDev>(fp, ws.item);
+  if (!WgQ) {  // the layer of the step was chosen on the device
+    WgQ = ws.layers[f.layer].WgQ;
+    bias = ws.layers[f.layer].bias;
+  }
   extern __shared__ __align__(16) uint8_t lg_smem[];
   XS* xT = reinterpret_cast<XS*>(lg_smem);       // [hidden][8 tokens]
   if (read_status(ws.status)) return;
@@ -451,13 +605,18 @@ struct WsGeom {
   size_t smem;
 };
 
-template <typename XS, int EPW>
+template <typename XS, int EPW, bool kDev>
 __global__ void __launch_bounds__(kWsWarps * 32, 1)
-k_router_logits_ws(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int hidden,
+k_router_logits_ws(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn fp, DevWS ws, int hidden,
                    const float* __restrict__ WgQ, const float* __restrict__ bias, int E,
                    float* __restrict__ logits, WsGeom geo) {
   grid_dep_wait();
   grid_dep_launch();
+  const FanIn& f = step_item<kDev>(fp, ws.item);
+  if (!WgQ) {  // the layer of the step was chosen on the device
+    WgQ = ws.layers[f.layer].WgQ;
+    bias = ws.layers[f.layer].bias;
+  }
   extern __shared__ __align__(128) uint8_t ws_smem[];
   constexpr int EB = EPW * kWsWarps;
   const float* Ws = reinterpret_cast<const float*>(ws_smem);  // [EB / 4][hidden][4]
@@ -624,12 +783,18 @@ struct TwGeom {
   size_t smem;
 };
 
+template <bool kDev>
 __global__ void __launch_bounds__(kTwWarps * 32, 1)
-k_router_logits_tw(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int hidden,
+k_router_logits_tw(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn fp, DevWS ws, int hidden,
                    const float* __restrict__ WgQ, const float* __restrict__ bias, int E,
                    float* __restrict__ logits, TwGeom geo) {
   grid_dep_wait();
   grid_dep_launch();
+  const FanIn& f = step_item<kDev>(fp, ws.item);
+  if (!WgQ) {  // the layer of the step was chosen on the device
+    WgQ = ws.layers[f.layer].WgQ;
+    bias = ws.layers[f.layer].bias;
+  }
   extern __shared__ __align__(128) uint8_t tw_smem[];
   const float4* Wq = reinterpret_cast<const float4*>(tw_smem);  // [4 groups][hidden]
   uint8_t* stage = tw_smem + geo.w_bytes;                         // [8][hidden] bf16
@@ -773,19 +938,24 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+template <bool kDev>
 __global__ void __launch_bounds__(2 * kTwWarps * 32, 1)
-k_router_logits_tw2(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int hidden,
+k_router_logits_tw2(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn fp, DevWS ws, int hidden,
                     const float* __restrict__ WgQ, const float* __restrict__ bias, int E,
                     float* __restrict__ logits, TwGeom geo) {
   grid_dep_wait();
   grid_dep_launch();
+  const FanIn& f = step_item<kDev>(fp, ws.item);
+  if (!WgQ) {  // the layer of the step was chosen on the device
+    WgQ = ws.layers[f.layer].WgQ;
+    bias = ws.layers[f.layer].bias;
+  }
   extern __shared__ __align__(128) uint8_t tw_smem[];
   const float4* Wq = reinterpret_cast<const float4*>(tw_smem);  // [4 groups][hidden]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int set = warp / kTwWarps, wis = warp % kTwWarps, tis = tid % (kTwWarps * 32);
   uint8_t* xt = tw_smem + geo.w_bytes + set * geo.xt_bytes;      // this stream's records
   uint64_t* wbar_p = reinterpret_cast<uint64_t*>(tw_smem + geo.w_bytes + 2 * geo.xt_bytes);
-  __shared__ int abort_s;
   if (read_status(ws.status)) return;
   const int e_base = blockIdx.y * kTwExperts;
   const int ne = min(kTwExperts, E - e_base);
@@ -796,7 +966,6 @@ k_router_logits_tw2(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int hidden
   const int nchunks = hidden / 8;
   const uint32_t wbar = smem_u32(wbar_p);
   if (tid == 0) {
-    abort_s = 0;
     mbar_init(wbar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     const uint32_t wbytes = (uint32_t)(((ne + 3) / 4) * hidden * 16);
@@ -910,11 +1079,13 @@ k_router_logits_tw2(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int hidden
 // below every number) and the gate weights from a softmax over all E
 // (sums carried as float-float); one warp per token, 16 tokens per CTA,
 // whose per-expert histogram (hist[cta][e]) feeds the plan.
+template <bool kDev>
 __global__ void __launch_bounds__(kRtTok * 32)
-k_router_topk(FanIn f, DevWS ws, const float* __restrict__ logits, int E, int k, int renorm,
+k_router_topk(const __grid_constant__ FanIn fp, DevWS ws, const float* __restrict__ logits, int E, int k, int renorm,
               float scale, int32_t* __restrict__ hist, int nblocks) {
   grid_dep_wait();
   grid_dep_launch();
+  const FanIn& f = step_item<kDev>(fp, ws.item);
   __shared__ int hs[256];
   if (read_status(ws.status)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1029,16 +1200,18 @@ __device__ void write_tile_tables(const FanIn& f, int k, int E, int inter, int s
 constexpr int kScanWarps = 32;
 constexpr int kScanSegs = kScanWarps * 32 / 64;  // 16 segments x 64 experts per pass
 
+template <bool kDev>
 __global__ void __launch_bounds__(kScanWarps * 32)
-k_plan_scan(FanIn f, DevWS ws, int E, int k, int inter, int shared_inter, int hidden,
+k_plan_scan(const __grid_constant__ FanIn fp, DevWS ws, int E, int k, int inter, int shared_inter, int hidden,
             int has_shared, int bn, const int32_t* __restrict__ hist, int32_t* __restrict__ base,
-            int nblocks, GemmPlan* plan1, GemmPlan* plan2) {
+            GemmPlan* plan1, GemmPlan* plan2) {
   grid_dep_wait();
   grid_dep_launch();
+  const FanIn& f = step_item<kDev>(fp, ws.item);
   __shared__ int cnt[256];
   __shared__ int offs[257];
   __shared__ int skip;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x;
   if (tid == 0) skip = read_status(ws.status);
   __syncthreads();
   if (skip) return;
@@ -1046,6 +1219,7 @@ k_plan_scan(FanIn f, DevWS ws, int E, int k, int inter, int shared_inter, int hi
   // so a warp's loads of one CTA's histogram row are contiguous
   __shared__ int seg_sum[kScanSegs][64];
   const int sg = tid / 64, el = tid % 64;
+  const int nblocks = (f.total + kRtTok - 1) / kRtTok;  // router CTAs of this step
   const int L = (nblocks + kScanSegs - 1) / kScanSegs;
   const int b_lo = min(nblocks, sg * L), b_hi = min(nblocks, b_lo + L);
   for (int e0 = 0; e0 < E; e0 += 64) {
@@ -1102,11 +1276,13 @@ k_plan_scan(FanIn f, DevWS ws, int E, int k, int inter, int shared_inter, int hi
 // ---------------------------------------------------------------------------
 constexpr int kPlanSmallMax = 8192;
 
+template <bool kDev>
 __global__ void __launch_bounds__(1024)
-k_plan_small(FanIn f, DevWS ws, int E, int k, int inter, int shared_inter, int hidden,
+k_plan_small(const __grid_constant__ FanIn fp, DevWS ws, int E, int k, int inter, int shared_inter, int hidden,
              int has_shared, int bn, GemmPlan* plan1, GemmPlan* plan2) {
   grid_dep_wait();
   grid_dep_launch();
+  const FanIn& f = step_item<kDev>(fp, ws.item);
   __shared__ int hist_w[32][256];
   __shared__ int cnt[256];
   __shared__ int offs[257];
@@ -1183,11 +1359,13 @@ k_plan_small(FanIn f, DevWS ws, int E, int k, int inter, int shared_inter, int h
 // go, in arrival order, after the same expert's rows of the entries before
 // it (stable in list order).  One CTA.
 // ---------------------------------------------------------------------------
+template <bool kDev>
 __global__ void __launch_bounds__(1024)
-k_plan_grouped(FanIn f, DevWS ws, int E, int inter, int shared_inter, int hidden, int has_shared,
+k_plan_grouped(const __grid_constant__ FanIn fp, DevWS ws, int E, int inter, int shared_inter, int hidden, int has_shared,
                int bn, GemmPlan* plan1, GemmPlan* plan2, WinGeom g, int row_bytes, int in_place) {
   grid_dep_wait();
   grid_dep_launch();
+  const FanIn& f = step_item<kDev>(fp, ws.item);
   __shared__ int cnt[256];
   __shared__ int offs[257];
   __shared__ int skip;
@@ -1300,15 +1478,17 @@ k_plan_grouped(FanIn f, DevWS ws, int E, int inter, int shared_inter, int hidden
 // ---------------------------------------------------------------------------
 constexpr int kRankWarps = 8;
 
+template <bool kDev>
 __global__ void __launch_bounds__(kRankWarps * 32)
-k_rank(FanIn f, DevWS ws, int E, int k, const int32_t* __restrict__ base, int nblocks) {
+k_rank(const __grid_constant__ FanIn fp, DevWS ws, int E, int k, const int32_t* __restrict__ base) {
   grid_dep_wait();
   grid_dep_launch();
+  const FanIn& f = step_item<kDev>(fp, ws.item);
   __shared__ int run_s[kRankWarps][256];
   if (read_status(ws.status)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.x * kRankWarps + warp;
-  if (b >= nblocks) return;
+  if (b >= (f.total + kRtTok - 1) / kRtTok) return;  // past this step's router CTAs
   // run[e]: next position for expert e in this block = offsets[e] + base[b][e]
   int* run = run_s[warp];
   for (int e = lane; e < E; e += 32) run[e] = ws.offsets[e] + base[(int64_t)b * E + e];
@@ -1344,11 +1524,13 @@ k_rank(FanIn f, DevWS ws, int E, int k, const int32_t* __restrict__ base, int nb
 // peer slot (the fan-in concatenation is never materialised), then the
 // shared rows in concatenation order.  One warp per row, 16-byte vectors.
 // ---------------------------------------------------------------------------
+template <bool kDev>
 __global__ void __launch_bounds__(kThreads)
-k_gather(const uint8_t* win, WinGeom g, FanIn f, DevWS ws, int k, int row_bytes,
+k_gather(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn fp, DevWS ws, int k, int row_bytes,
          int has_shared) {
   grid_dep_wait();
   grid_dep_launch();
+  const FanIn& f = step_item<kDev>(fp, ws.item);
   if (read_status(ws.status)) return;
   const int N = f.grouped ? f.rtotal : f.total * k;
   const int rows = N + (has_shared ? f.total : 0);
@@ -1418,6 +1600,10 @@ __global__ void __launch_bounds__(kThreads) k_gemm_simt(SimtArgs a) {
   const int cols = a.swiglu ? a.M[kind] / 2 : a.M[kind];
   const int64_t total = (int64_t)G.rows * cols;
   const void* A = a.A[kind];
+  if (a.layers) {  // the layer of the step was chosen on the device
+    const DevLayer& L = a.layers[a.item->layer];
+    A = a.wsel == 1 ? (kind ? L.W13s : L.W13) : (kind ? L.Wds : L.Wd);
+  }
   const int64_t a_off = (int64_t)G.a_idx * a.M[kind] * K;
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {
@@ -1452,11 +1638,12 @@ __global__ void __launch_bounds__(kThreads) k_gemm_simt(SimtArgs a) {
 // its local row; the route_table row gets the chosen ids.  Deterministic:
 // each output element is reduced by one thread in a fixed order.
 // ---------------------------------------------------------------------------
-template <bool ACT_F32, bool Y_F32, int kBatch>
+template <bool ACT_F32, bool Y_F32, int kBatch, bool kDev>
 __global__ void __launch_bounds__(kThreads)
-k_combine(uint8_t* ret, WinGeom g, FanIn f, DevWS ws, int hidden, int k, int has_shared) {
+k_combine(uint8_t* ret, WinGeom g, const __grid_constant__ FanIn fp, DevWS ws, int hidden, int k, int has_shared) {
   grid_dep_wait();
   grid_dep_launch();
+  const FanIn& f = step_item<kDev>(fp, ws.item);
   if (read_status(ws.status)) return;
   // 8 features per lane step: 16-byte loads of bf16 y (two of fp32 y)
   constexpr int kVec = 8;
@@ -1596,11 +1783,12 @@ k_combine(uint8_t* ret, WinGeom g, FanIn f, DevWS ws, int hidden, int k, int has
 // received row into its peer's return slot in arrival order (routed_x), and
 // the shared expert's outputs (shared_x, rounded to the activation type).
 // One warp per row.
-template <bool ACT_F32>
+template <bool ACT_F32, bool kDev>
 __global__ void __launch_bounds__(kThreads)
-k_scatter_grouped(uint8_t* ret, WinGeom g, FanIn f, DevWS ws, int hidden, int has_shared) {
+k_scatter_grouped(uint8_t* ret, WinGeom g, const __grid_constant__ FanIn fp, DevWS ws, int hidden, int has_shared) {
   grid_dep_wait();
   grid_dep_launch();
+  const FanIn& f = step_item<kDev>(fp, ws.item);
   if (read_status(ws.status)) return;
   constexpr int kEl = ACT_F32 ? 4 : 2;
   const int row_bytes = hidden * kEl;
@@ -1644,9 +1832,11 @@ k_scatter_grouped(uint8_t* ret, WinGeom g, FanIn f, DevWS ws, int hidden, int ha
 }
 
 // return headers, then the return flags (release) = the dispatch seq
-__global__ void k_return_header(uint8_t* ret, WinGeom g, FanIn f, DevWS ws, int E, int k) {
+template <bool kDev>
+__global__ void k_return_header(uint8_t* ret, WinGeom g, const __grid_constant__ FanIn fp, DevWS ws, int E, int k) {
   grid_dep_wait();
   grid_dep_launch();
+  const FanIn& f = step_item<kDev>(fp, ws.item);
   if (read_status(ws.status)) return;
   const int i = blockIdx.x;
   if (i >= f.n_peers) return;
@@ -1728,9 +1918,16 @@ k_unpack(const uint8_t* ret, WinGeom g, int region, int stage, uint4* out, int n
 
 // L2 prefetch of a contiguous byte range (weights the next GEMM reads first):
 // 64 KB bulk prefetches spread over the grid; returns as soon as they are issued.
-__global__ void k_prefetch_l2(const uint8_t* base, int64_t bytes) {
+__global__ void k_prefetch_l2(const uint8_t* base, int64_t bytes, DevWS ws) {
   grid_dep_wait();
   grid_dep_launch();
+  if (!base) {  // the W13 of the layer the device chose for the step in flight
+    if (read_status(ws.status)) return;
+    const FanIn& f = *ws.item;
+    if ((f.grouped ? f.rtotal : f.total) == 0) return;
+    base = static_cast<const uint8_t*>(ws.layers[f.layer].W13);
+    if (!base) return;
+  }
   constexpr int64_t kChunk = 65536;
   const int64_t n = (bytes + kChunk - 1) / kChunk;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
@@ -1804,22 +2001,23 @@ cudaError_t launch_header_check(const LaunchCtx& lc, const WinGeom& g, const uin
                   has_shared_expert, timeout_ns);
 }
 
-template <typename XS>
+template <typename XS, bool kDev>
 static cudaError_t launch_logits_t(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                                    const FanIn& f, const DevWS& ws, int hidden, const float* WgQ,
                                    const float* bias, int E, float* logits) {
   const size_t smem = (size_t)hidden * kLgTok * sizeof(XS);
-  cudaError_t err = cudaFuncSetAttribute(k_router_logits<XS>,
+  cudaError_t err = cudaFuncSetAttribute(k_router_logits<XS, kDev>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   dim3 grid((f.total + kLgTok - 1) / kLgTok, (E + kLgEblk - 1) / kLgEblk);
-  return launch_k(lc, k_router_logits<XS>, grid, kLgWarps * 32, smem, win, g, f, ws, hidden, WgQ,
-                  bias, E, logits);
+  return launch_k(lc, k_router_logits<XS, kDev>, grid, kLgWarps * 32, smem, win, g, f, ws, hidden,
+                  WgQ, bias, E, logits);
 }
 
 // Shared memory of the weight-stationary logits kernel with 4 * epw experts
 // per CTA; the ring takes 3 buffers, or 2 when 3 do not fit.  smem = 0: it
-// does not fit at all.
+// does not fit at all.  (The 1024 bytes held back cover the kernels' static
+// shared memory, the step's fan-in included.)
 static WsGeom ws_geom(int hidden, int xs_bytes, int epw) {
   constexpr size_t kLimit = 232448 - 1024;
   WsGeom geo{};
@@ -1836,20 +2034,21 @@ static WsGeom ws_geom(int hidden, int xs_bytes, int epw) {
   geo.smem = 0;
   return geo;
 }
+static_assert(sizeof(FanIn) + 64 <= 1024, "static shared memory of the router kernels");
 
-template <typename XS, int EPW>
+template <typename XS, int EPW, bool kDev>
 static cudaError_t launch_logits_ws(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                                     const FanIn& f, const DevWS& ws, int hidden, const float* WgQ,
                                     const float* bias, int E, float* logits, const WsGeom& geo) {
-  cudaError_t err = cudaFuncSetAttribute(k_router_logits_ws<XS, EPW>,
+  cudaError_t err = cudaFuncSetAttribute(k_router_logits_ws<XS, EPW, kDev>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.smem);
   if (err != cudaSuccess) return err;
   const int eblocks = (E + kWsWarps * EPW - 1) / (kWsWarps * EPW);
   const int ntiles = (f.total + kWsTok - 1) / kWsTok;
   // one CTA per SM (the weight block fills most of its shared memory)
   const int gx = std::max(1, std::min(ntiles, lc.num_sms / eblocks));
-  return launch_k(lc, k_router_logits_ws<XS, EPW>, dim3(gx, eblocks), kWsWarps * 32, geo.smem, win,
-                  g, f, ws, hidden, WgQ, bias, E, logits, geo);
+  return launch_k(lc, k_router_logits_ws<XS, EPW, kDev>, dim3(gx, eblocks), kWsWarps * 32, geo.smem,
+                  win, g, f, ws, hidden, WgQ, bias, E, logits, geo);
 }
 
 static TwGeom tw_geom(int hidden) {
@@ -1863,7 +2062,7 @@ static TwGeom tw_geom(int hidden) {
   return geo;
 }
 
-template <typename XS>
+template <typename XS, bool kDev>
 static cudaError_t launch_logits(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                                  const FanIn& f, const DevWS& ws, int hidden, const float* WgQ,
                                  const float* bias, int E, float* logits) {
@@ -1872,27 +2071,27 @@ static cudaError_t launch_logits(const LaunchCtx& lc, const WinGeom& g, const ui
     geo.stage_bytes = 0;  // no staging buffer; two record buffers
     geo.smem = geo.w_bytes + 2 * geo.xt_bytes + 16;
     if (geo.smem <= 232448 - 1024) {
-      cudaError_t err = cudaFuncSetAttribute(k_router_logits_tw2,
+      cudaError_t err = cudaFuncSetAttribute(k_router_logits_tw2<kDev>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.smem);
       if (err != cudaSuccess) return err;
       const int eblocks = (E + kTwExperts - 1) / kTwExperts;
       const int ntiles = (f.total + kTwTok - 1) / kTwTok;
       const int gx = std::max(1, std::min(ntiles, lc.num_sms / eblocks));
-      return launch_k(lc, k_router_logits_tw2, dim3(gx, eblocks), 2 * kTwWarps * 32, geo.smem, win, g,
-                      f, ws, hidden, WgQ, bias, E, logits, geo);
+      return launch_k(lc, k_router_logits_tw2<kDev>, dim3(gx, eblocks), 2 * kTwWarps * 32, geo.smem,
+                      win, g, f, ws, hidden, WgQ, bias, E, logits, geo);
     }
   }
   if (sizeof(XS) == 2 && E >= 16) {
     const TwGeom geo = tw_geom(hidden);
     if (geo.smem) {
-      cudaError_t err = cudaFuncSetAttribute(k_router_logits_tw,
+      cudaError_t err = cudaFuncSetAttribute(k_router_logits_tw<kDev>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.smem);
       if (err != cudaSuccess) return err;
       const int eblocks = (E + kTwExperts - 1) / kTwExperts;
       const int ntiles = (f.total + kTwTok - 1) / kTwTok;
       const int gx = std::max(1, std::min(ntiles, lc.num_sms / eblocks));
-      return launch_k(lc, k_router_logits_tw, dim3(gx, eblocks), kTwWarps * 32, geo.smem, win, g, f,
-                      ws, hidden, WgQ, bias, E, logits, geo);
+      return launch_k(lc, k_router_logits_tw<kDev>, dim3(gx, eblocks), kTwWarps * 32, geo.smem, win,
+                      g, f, ws, hidden, WgQ, bias, E, logits, geo);
     }
   }
   // experts per warp: 4 when there are >= 16 experts, fewer for small E or
@@ -1900,11 +2099,27 @@ static cudaError_t launch_logits(const LaunchCtx& lc, const WinGeom& g, const ui
   for (int epw = E >= 16 ? 4 : (E >= 8 ? 2 : 1); epw >= 1; epw >>= 1) {
     const WsGeom geo = ws_geom(hidden, (int)sizeof(XS), epw);
     if (!geo.smem) continue;
-    if (epw == 4) return launch_logits_ws<XS, 4>(lc, g, win, f, ws, hidden, WgQ, bias, E, logits, geo);
-    if (epw == 2) return launch_logits_ws<XS, 2>(lc, g, win, f, ws, hidden, WgQ, bias, E, logits, geo);
-    return launch_logits_ws<XS, 1>(lc, g, win, f, ws, hidden, WgQ, bias, E, logits, geo);
+    if (epw == 4)
+      return launch_logits_ws<XS, 4, kDev>(lc, g, win, f, ws, hidden, WgQ, bias, E, logits, geo);
+    if (epw == 2)
+      return launch_logits_ws<XS, 2, kDev>(lc, g, win, f, ws, hidden, WgQ, bias, E, logits, geo);
+    return launch_logits_ws<XS, 1, kDev>(lc, g, win, f, ws, hidden, WgQ, bias, E, logits, geo);
   }
-  return launch_logits_t<XS>(lc, g, win, f, ws, hidden, WgQ, bias, E, logits);
+  return launch_logits_t<XS, kDev>(lc, g, win, f, ws, hidden, WgQ, bias, E, logits);
+}
+
+template <bool kDev>
+static cudaError_t launch_router_t(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
+                                   const FanIn& f, const DevWS& ws, int hidden, int act_f32,
+                                   const float* WgQ, const float* bias, int E, int k, int renorm,
+                                   float scale, float* logits, int32_t* hist) {
+  cudaError_t err =
+      act_f32 ? launch_logits<float, kDev>(lc, g, win, f, ws, hidden, WgQ, bias, E, logits)
+              : launch_logits<uint16_t, kDev>(lc, g, win, f, ws, hidden, WgQ, bias, E, logits);
+  if (err != cudaSuccess) return err;
+  const int nblocks = router_blocks(f.total);
+  return launch_k(lc, k_router_topk<kDev>, nblocks, kRtTok * 32, 0, f, ws, logits, E, k, renorm,
+                  scale, hist, nblocks);
 }
 
 cudaError_t launch_router(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
@@ -1912,36 +2127,45 @@ cudaError_t launch_router(const LaunchCtx& lc, const WinGeom& g, const uint8_t* 
                           const float* WgQ, const float* bias, int E, int k, int renorm,
                           float scale, float* logits, int32_t* hist) {
   if (f.total == 0) return cudaSuccess;
-  cudaError_t err = act_f32 ? launch_logits<float>(lc, g, win, f, ws, hidden, WgQ, bias, E, logits)
-                            : launch_logits<uint16_t>(lc, g, win, f, ws, hidden, WgQ, bias, E, logits);
-  if (err != cudaSuccess) return err;
+  return f.dev ? launch_router_t<true>(lc, g, win, f, ws, hidden, act_f32, WgQ, bias, E, k, renorm,
+                                       scale, logits, hist)
+               : launch_router_t<false>(lc, g, win, f, ws, hidden, act_f32, WgQ, bias, E, k,
+                                        renorm, scale, logits, hist);
+}
+
+template <bool kDev>
+static cudaError_t launch_plan_t(const LaunchCtx& lc, const FanIn& f, const DevWS& ws, int E,
+                                 int k, int inter, int shared_inter, int hidden, int has_shared,
+                                 int bn, GemmPlan* plan1, GemmPlan* plan2, const int32_t* hist,
+                                 int32_t* base) {
   const int nblocks = router_blocks(f.total);
-  return launch_k(lc, k_router_topk, nblocks, kRtTok * 32, 0, f, ws, logits, E, k, renorm, scale,
-                  hist, nblocks);
+  if ((int64_t)f.total * k <= kPlanSmallMax) {
+    return launch_k(lc, k_plan_small<kDev>, 1, 1024, 0, f, ws, E, k, inter, shared_inter, hidden,
+                    has_shared, bn, plan1, plan2);
+  }
+  cudaError_t err = launch_k(lc, k_plan_scan<kDev>, 1, kScanWarps * 32, 0, f, ws, E, k, inter,
+                             shared_inter, hidden, has_shared, bn, hist, base, plan1, plan2);
+  if (err != cudaSuccess || nblocks == 0) return err;
+  return launch_k(lc, k_rank<kDev>, (nblocks + kRankWarps - 1) / kRankWarps, kRankWarps * 32, 0, f,
+                  ws, E, k, (const int32_t*)base);
 }
 
 cudaError_t launch_plan(const LaunchCtx& lc, const FanIn& f, const DevWS& ws, int E, int k,
                         int inter, int shared_inter, int hidden, int has_shared, int bn,
                         GemmPlan* plan1, GemmPlan* plan2, const int32_t* hist, int32_t* base) {
-  const int nblocks = router_blocks(f.total);
-  if ((int64_t)f.total * k <= kPlanSmallMax) {
-    return launch_k(lc, k_plan_small, 1, 1024, 0, f, ws, E, k, inter, shared_inter, hidden,
-                    has_shared, bn, plan1, plan2);
-  }
-  cudaError_t err = launch_k(lc, k_plan_scan, 1, kScanWarps * 32, 0, f, ws, E, k, inter,
-                             shared_inter, hidden, has_shared, bn, hist, base, nblocks, plan1,
-                             plan2);
-  if (err != cudaSuccess || nblocks == 0) return err;
-  return launch_k(lc, k_rank, (nblocks + kRankWarps - 1) / kRankWarps, kRankWarps * 32, 0, f, ws,
-                  E, k, (const int32_t*)base, nblocks);
+  return f.dev ? launch_plan_t<true>(lc, f, ws, E, k, inter, shared_inter, hidden, has_shared, bn,
+                                     plan1, plan2, hist, base)
+               : launch_plan_t<false>(lc, f, ws, E, k, inter, shared_inter, hidden, has_shared, bn,
+                                      plan1, plan2, hist, base);
 }
 
 cudaError_t launch_gather(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                           const FanIn& f, const DevWS& ws, int k, int row_bytes, int has_shared) {
   const int64_t rows = (int64_t)f.total * k + (has_shared ? f.total : 0);
   if (rows == 0) return cudaSuccess;
-  return launch_k(lc, k_gather, grid_for(rows, kThreads / 32, lc.num_sms * 8), kThreads, 0, win, g,
-                  f, ws, k, row_bytes, has_shared);
+  return launch_k(lc, f.dev ? k_gather<true> : k_gather<false>,
+                  grid_for(rows, kThreads / 32, lc.num_sms * 8), kThreads, 0, win, g, f, ws, k,
+                  row_bytes, has_shared);
 }
 
 cudaError_t launch_gemm_simt(const LaunchCtx& lc, const SimtArgs& a, int max_groups) {
@@ -1956,21 +2180,23 @@ cudaError_t launch_combine(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret, 
   const int64_t items = (int64_t)f.total * ((hidden + 255) / 256);
   const int grid = grid_for(items, kThreads / 32, lc.num_sms * 8);
   const bool small = items < (int64_t)lc.num_sms * 64;
+  const bool d = f.dev != 0;
+  decltype(&k_combine<true, true, 1, false>) kern = nullptr;
   if (act_f32 && y_f32)
-    return launch_k(lc, k_combine<true, true, 1>, grid, kThreads, 0, ret, g, f, ws, hidden, k, has_shared);
-  if (!act_f32 && y_f32)
-    return launch_k(lc, k_combine<false, true, 1>, grid, kThreads, 0, ret, g, f, ws, hidden, k, has_shared);
-  if (!act_f32 && !y_f32)
-    return small ? launch_k(lc, k_combine<false, false, 8>, grid, kThreads, 0, ret, g, f, ws, hidden, k,
-                            has_shared)
-                 : launch_k(lc, k_combine<false, false, 1>, grid, kThreads, 0, ret, g, f, ws, hidden, k,
-                            has_shared);
-  return cudaErrorInvalidValue;
+    kern = d ? k_combine<true, true, 1, true> : k_combine<true, true, 1, false>;
+  else if (!act_f32 && y_f32)
+    kern = d ? k_combine<false, true, 1, true> : k_combine<false, true, 1, false>;
+  else if (!act_f32 && !y_f32)
+    kern = small ? (d ? k_combine<false, false, 8, true> : k_combine<false, false, 8, false>)
+                 : (d ? k_combine<false, false, 1, true> : k_combine<false, false, 1, false>);
+  if (!kern) return cudaErrorInvalidValue;
+  return launch_k(lc, kern, grid, kThreads, 0, ret, g, f, ws, hidden, k, has_shared);
 }
 
 cudaError_t launch_return_header(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret,
                                  const uint8_t*, const FanIn& f, const DevWS& ws, int E, int k) {
-  return launch_k(lc, k_return_header, f.n_peers, 128, 0, ret, g, f, ws, E, k);
+  return launch_k(lc, f.dev ? k_return_header<true> : k_return_header<false>, f.n_peers, 128, 0,
+                  ret, g, f, ws, E, k);
 }
 
 cudaError_t launch_unpack(const LaunchCtx& lc, const WinGeom& g, const uint8_t* ret, int region,
@@ -1987,7 +2213,8 @@ cudaError_t launch_plan_grouped(const LaunchCtx& lc, const FanIn& f, const DevWS
                                 int inter, int shared_inter, int hidden, int has_shared, int bn,
                                 GemmPlan* plan1, GemmPlan* plan2, const WinGeom& g, int row_bytes,
                                 int in_place) {
-  return launch_k(lc, k_plan_grouped, 1, 1024, 0, f, ws, E, inter, shared_inter, hidden, has_shared,
+  return launch_k(lc, f.dev ? k_plan_grouped<true> : k_plan_grouped<false>, 1, 1024, 0, f, ws, E,
+                  inter, shared_inter, hidden, has_shared,
                   bn, plan1, plan2, g, row_bytes, in_place);
 }
 
@@ -1997,14 +2224,25 @@ cudaError_t launch_scatter_grouped(const LaunchCtx& lc, const WinGeom& g, uint8_
   const int64_t rows = (int64_t)f.rtotal + (has_shared ? f.total : 0);
   if (rows == 0) return cudaSuccess;
   const int grid = grid_for(rows, kThreads / 32, lc.num_sms * 8);
-  if (act_f32)
-    return launch_k(lc, k_scatter_grouped<true>, grid, kThreads, 0, ret, g, f, ws, hidden, has_shared);
-  return launch_k(lc, k_scatter_grouped<false>, grid, kThreads, 0, ret, g, f, ws, hidden, has_shared);
+  const bool d = f.dev != 0;
+  auto kern = act_f32 ? (d ? k_scatter_grouped<true, true> : k_scatter_grouped<true, false>)
+                      : (d ? k_scatter_grouped<false, true> : k_scatter_grouped<false, false>);
+  return launch_k(lc, kern, grid, kThreads, 0, ret, g, f, ws, hidden, has_shared);
 }
 
-cudaError_t launch_prefetch_l2(const LaunchCtx& lc, const void* base, int64_t bytes) {
+cudaError_t launch_prefetch_l2(const LaunchCtx& lc, const void* base, int64_t bytes,
+                               const DevWS& ws) {
   if (bytes <= 0) return cudaSuccess;
-  return launch_k(lc, k_prefetch_l2, lc.num_sms, 32, 0, static_cast<const uint8_t*>(base), bytes);
+  return launch_k(lc, k_prefetch_l2, lc.num_sms, 32, 0, static_cast<const uint8_t*>(base), bytes,
+                  ws);
+}
+
+cudaError_t launch_item_head(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
+                             const PeerList& pl, const DevWS& ws, int num_experts, int token_cap,
+                             int has_shared_expert, int grouped, int tmax, int rmax,
+                             int max_layers, int64_t timeout_ns) {
+  return launch_k(lc, k_item_head, 1, 1024, 0, win, g, pl, ws, num_experts, token_cap,
+                  has_shared_expert, grouped, tmax, rmax, max_layers, timeout_ns);
 }
 
 cudaError_t launch_arrange_wg(const LaunchCtx& lc, const float* Wg, float* WgQ, int hidden,

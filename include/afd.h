@@ -313,6 +313,61 @@ int afd_ffn_forward_grouped(afd_ctx* ctx, int layer, int stage, const int* n_row
 int afd_unpack_grouped(afd_ctx* ctx, int peer, int stage, void* y_out, int n_rows, void* s_out,
                        int n_tokens, uint64_t expect_seq);
 
+/* ---- device-resident work-item loop ---------------------------------------
+ * [RFC]: Async AFD for Prefill on Ascend NPU, "Asynchronous work-item
+ * contract" and "FFN execution modes"; [RFC]: Async GPU Connector, "FFN main
+ * loop" and the device-side wait_any named under "Risks and alternatives".
+ * A work item is one stage of the ring over the listed peers (one Attention
+ * replica).  It is ready once every listed peer has published a flag newer
+ * than the one last consumed from its (peer, stage) slot.  Each step of the
+ * loop, on the device and in stream order:
+ *   - waits (bounded by wait_timeout_ns) for any ready stage; the scan
+ *     starts after the stage served last, so a ready stage waits for at most
+ *     ring_depth - 1 others;
+ *   - takes the layer (header word layer_idx, which must agree across the
+ *     listed peers) and the token / routed-row counts from the headers;
+ *   - runs the same FFN step as afd_ffn_forward (form AFD_FORM_TOKENS) or
+ *     afd_ffn_forward_grouped (AFD_FORM_GROUPED) with that layer's weights,
+ *     which come from a device copy of the table afd_set_layer fills.
+ * The host reads nothing back to drive a step, and every launch has a fixed
+ * shape: the most tokens a step may carry (min(max_total_tokens, n_peers *
+ * token_cap); grouped rows: min(max_total_tokens * topk, n_peers *
+ * token_cap)), with the kernels bounded by the counts on the device.
+ * Device errors (afd_poll_status) as afd_ffn_forward, plus AFD_ERR_TIMEOUT
+ * when no stage gets ready, AFD_ERR_LAYER for a layer outside the table or
+ * without weights, AFD_ERR_CAPACITY for a step over the shape above.  The
+ * first error ends the loop: later steps do no work until it is polled. */
+#define AFD_FORM_TOKENS 0
+#define AFD_FORM_GROUPED 1
+
+/* Enqueue n_items steps of the loop over the peers slots[0..n_peers-1]
+ * (host ints) on the context's stream (eager mode).  Host-checked errors:
+ * AFD_ERR_ARG (form, peer range or duplicates, n_peers, n_items < 0). */
+int afd_ffn_serve(afd_ctx* ctx, const int* slots, int n_peers, int n_items, int form);
+
+/* The same n_items steps captured once into a CUDA graph (graph mode: the
+ * loop runs a fixed number of items and is replayed without host
+ * orchestration).  Captured on a stream of the library's own; *kernels (may
+ * be NULL) receives the kernel launches the graph holds.  The graph refers to
+ * the context's window, workspace and layer table, not to the weights: a
+ * later afd_set_layer takes effect in the next replay.  Errors: as
+ * afd_ffn_serve, n_items == 0 is AFD_ERR_ARG, AFD_ERR_CUDA if the capture or
+ * the instantiation fails. */
+typedef struct afd_serve_graph afd_serve_graph;
+int afd_serve_graph_create(afd_ctx* ctx, const int* slots, int n_peers, int n_items, int form,
+                           afd_serve_graph** out, int64_t* kernels);
+/* Replay on the context's current stream. */
+int afd_serve_graph_launch(afd_serve_graph* g);
+void afd_serve_graph_destroy(afd_serve_graph* g);
+
+/* Synchronise the stream and copy out the loop's record of the items it
+ * served, oldest first: records (host int32 [max_records][4]) gets (stage,
+ * layer, tokens, routed rows) of the last min(max_records, served, 64)
+ * items and *n_records how many that is; *n_served (may be NULL) the items
+ * served since creation.  Errors: AFD_ERR_ARG, AFD_ERR_CUDA. */
+int afd_serve_log(afd_ctx* ctx, int32_t* records, int max_records, int* n_records,
+                  int64_t* n_served);
+
 /* Synchronise the stream, return the first device-recorded error since the
  * last poll (AFD_OK if none) and clear it; AFD_ERR_CUDA if the stream itself
  * failed. */

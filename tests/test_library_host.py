@@ -105,3 +105,14 @@ def test_create_without_gpu_fails_cleanly(lib):
     with pytest.raises(A.AfdError) as e:
         A.afd_create(A.make_config(2, 128, 1024, 16, 4, 512, 512))
     assert e.value.code == A.AFD_ERR_CUDA
+
+
+def test_serve_rejects_bad_arguments_without_a_context(lib):
+    """The work-item loop's host checks come before any device work."""
+    assert A.afd_ffn_serve(None, [0], 1) == A.AFD_ERR_ARG
+    rc, g, _ = A.afd_serve_graph_create(None, [0], 1)
+    assert rc == A.AFD_ERR_ARG and not g.value
+    assert A.afd_serve_graph_launch(None) == A.AFD_ERR_ARG
+    A.afd_serve_graph_destroy(None)
+    with pytest.raises(A.AfdError):
+        A.afd_serve_log(None)

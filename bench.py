@@ -408,6 +408,120 @@ def run_ours(args, ws, rank, local):
     run.close()
 
 
+def run_serve(args, ws, rank, local):
+    """The device-resident work-item loop measured: every layer's item packed
+    into a stage of its own (ring_depth = layers) before the timed region,
+    then one step = the whole set served back to back, by the host-described
+    step per item ("host"), by the loop's eager steps ("eager") or by one
+    replay of the captured loop ("graph").  All three modes run in the same
+    process on the same packs; --serve names the one reported as value."""
+    import numpy as np
+    import torch
+    from combine_peer_slot_gb300 import afd as A
+    from combine_peer_slot_gb300 import runtime as R
+
+    w = workload_of(args)
+    T, L = w.total_tokens, w.layers
+    grouped = args.form == "grouped"
+    run = R.Runner(w, max_total_tokens=T, ring_depth=L)
+    if grouped:
+        run.prepare_grouped(seed=w.seed)
+    slots = list(range(w.num_peers))
+    form = A.AFD_FORM_GROUPED if grouped else A.AFD_FORM_TOKENS
+    rc, graph, graph_kernels = A.afd_serve_graph_create(run.ctx, slots, L, form)
+    if rc:
+        raise A.AfdError(rc, "afd_serve_graph_create")
+    stream = run.stream
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def step(mode):
+        for layer in range(L):
+            if grouped:
+                run.pack_grouped_all(layer, stage=layer)
+            else:
+                run.pack_all(layer, stage=layer)
+        flush.zero_()
+        e0.record(stream)
+        if mode == "host":
+            for layer in range(L):
+                rc = (run.forward_grouped if grouped else run.forward)(layer, stage=layer)
+                if rc:
+                    raise A.AfdError(rc, "host-described step")
+        elif mode == "eager":
+            rc = A.afd_ffn_serve(run.ctx, slots, L, form)
+            if rc:
+                raise A.AfdError(rc, "afd_ffn_serve")
+        else:
+            rc = A.afd_serve_graph_launch(graph)
+            if rc:
+                raise A.AfdError(rc, "afd_serve_graph_launch")
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    modes = ["host", "eager", "graph"]
+    for _ in range(args.warmup):
+        for m in modes:
+            step(m)
+    if run.poll() != 0:
+        raise RuntimeError("device error during warm-up")
+    dev_index = getattr(torch.cuda.get_device_properties(local), "pci_bus_id", None) or local
+    ms = {m: 0.0 for m in modes}
+    launches = {m: 0 for m in modes}
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(dev_index) as clk:
+        for _ in range(args.steps):
+            for m in modes:  # interleaved, so the three see the same clocks
+                l0 = A.afd_launch_count(run.ctx)
+                ms[m] += step(m)
+                launches[m] += A.afd_launch_count(run.ctx) - l0
+    barrier(ws)
+    status = run.poll()
+    if status != 0:
+        raise RuntimeError(f"device error in the timed region: {A.strerror(status)}")
+    log, served = A.afd_serve_log(run.ctx, 64)
+    assert [r[1] for r in log[-L:]] == list(range(L)), "items served out of layer order"
+    # the pack kernels are the Attention side's, not the step's
+    pack_launches = L * w.num_peers * 2
+    launches = {m: v - pack_launches * args.steps for m, v in launches.items()}
+    launches["graph"] = graph_kernels * args.steps
+    per = {m: max_over_ranks(v / args.steps, ws) for m, v in ms.items()}
+    tokens_step = T * L
+    value = sum_over_ranks(tokens_step, ws) / (per[args.serve] / 1e3)
+    pk, pk_kind = peaks()
+    cnt = run.workspace(A.AFD_WS_COUNTS, 4 * w.num_experts).cpu().numpy().view(np.int32)
+    if grouped:
+        flops, nbytes, t_roof, bound = path_roofline_grouped(w, T, int(sum(run.g_n)),
+                                                             int((cnt > 0).sum()), pk)
+    else:
+        flops, nbytes, t_roof, bound = path_roofline(w, T, int((cnt > 0).sum()), pk)
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per[args.serve],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; no model weights or dataset)",
+        "config": {"workload": args.workload + ("_grouped" if grouped else "") + "_serve",
+                   "serve": args.serve, "items_per_step": L, "ring_depth": L,
+                   "peers": w.num_peers, "seq_lens": w.seq_lens, "total_tokens": T,
+                   "layers": L, "parallelism": f"replicas{ws}",
+                   "l2": "flushed (256 MB write) before every timed step",
+                   "timing": "one event pair around the whole set of items; every item "
+                             "packed into its own stage before the first event"},
+        "serve_ms_per_step": per, "graph_kernels": graph_kernels,
+        "gpu_launches": launches[args.serve], "gpu_launches_by_mode": launches,
+        "path_roofline": {"bound": bound, "roofline_ms": t_roof * 1e3 * L,
+                          "frac": t_roof * 1e3 * L / per[args.serve], "peak_source": pk_kind},
+        "roofline": None, "clocks": clk.summary(), "e2e": None, "cpu_baseline": None,
+        "items_served": served,
+    }
+    if rank == 0:
+        print(json.dumps(out))
+    A.afd_serve_graph_destroy(graph)
+    run.close()
+
+
 # ---------------------------------------------------------------------------
 # the CPU oracle (baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
@@ -525,12 +639,18 @@ def main():
                     help="grouped: the Attention side routes and sends rows grouped by expert")
     ap.add_argument("--layers", type=int, default=0,
                     help="number of layers replacing the workload's (smaller profiling cases)")
+    ap.add_argument("--serve", choices=["host", "eager", "graph"], default=None,
+                    help="measure the device-resident work-item loop: all layers' items "
+                         "packed into stages, served by host-described steps, the loop's "
+                         "eager steps or a replay of its captured graph (value = this mode)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     ws, rank, local = dist_init(args.gpus)
     if args.impl == "reference":
         run_reference(args, ws, rank)
+    elif args.serve:
+        run_serve(args, ws, rank, local)
     else:
         run_ours(args, ws, rank, local)
     if ws > 1:

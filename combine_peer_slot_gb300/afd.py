@@ -24,6 +24,7 @@ AFD_HEADER_FIXED_WORDS = 12
 AFD_NOALLOC_MAX_ROUTER_WEIGHTS = 262144
 AFD_NOALLOC_MAX_LOGITS = 1048576
 AFD_MAX_PEERS = 64
+AFD_MAX_RING = 64
 AFD_FORM_TOKENS, AFD_FORM_GROUPED = 0, 1
 
 

@@ -127,7 +127,7 @@ int layout_of(const afd_config* c, afd_layout* L) {
 
 int validate_config(const afd_config* c) {
   if (!c) return AFD_ERR_ARG;
-  if (c->num_peers < 1 || c->num_peers > AFD_MAX_PEERS || c->ring_depth < 1 || c->ring_depth > 8 ||
+  if (c->num_peers < 1 || c->num_peers > AFD_MAX_PEERS || c->ring_depth < 1 || c->ring_depth > AFD_MAX_RING ||
       c->token_cap < 1 || c->max_total_tokens < 0 || c->hidden < 8 || c->num_experts < 1 ||
       c->topk < 1 || c->topk > c->num_experts || c->inter < 1 || c->shared_inter < 0 ||
       c->max_layers < 1 || c->routed_cap_multiplier < 1.0f || c->wait_timeout_ns < 0)

@@ -75,13 +75,14 @@ extern "C" {
 #define AFD_GEMM_TENSOR_1CTA 2
 
 #define AFD_MAX_PEERS 64
+#define AFD_MAX_RING 64    /* most stages in flight per peer (ring_depth) */
 
 /* ---- configuration -------------------------------------------------------
  * num_peers        attention peers = window regions (with one FFN rank the
  *                  region count max(attn, ffn) is the peer count)
  * ring_depth       slots per peer, one per stage in flight (1 without
  *                  micro-batching; Async GPU Connector, "Capacity and ring
- *                  depth": an invariant, not a knob)
+ *                  depth": an invariant, not a knob); 1..AFD_MAX_RING
  * token_cap        max tokens per slot (max_num_batched_tokens)
  * max_total_tokens max fan-in total per forward; 0 = num_peers * token_cap
  * hidden, num_experts, topk, inter (routed SwiGLU intermediate),

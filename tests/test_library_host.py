@@ -77,7 +77,7 @@ def test_config_validation(lib):
     ok = A.make_config(4, 8192, 2048, 64, 6, 1408, 2816)
     assert A.afd_slot_layout(ok).window_bytes > 0
     bad = [dict(num_peers=0), dict(num_peers=65), dict(topk=65), dict(hidden=0),
-           dict(ring_depth=0), dict(routed_cap_multiplier=0.5), dict(act_dtype=7)]
+           dict(ring_depth=0), dict(ring_depth=A.AFD_MAX_RING + 1), dict(routed_cap_multiplier=0.5), dict(act_dtype=7)]
     for b in bad:
         cfg = A.make_config(4, 8192, 2048, 64, 6, 1408, 2816)
         for k, v in b.items():

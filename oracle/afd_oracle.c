@@ -147,22 +147,32 @@ static int64_t orc_round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; 
  * 64-bit sequence numbers.  Slot (region r, ring s) is slot number
  * r * ring_depth + s.  Parity: pinned by the disjoint / in-bounds / aligned
  * checks the page lists under "Existing verification". */
-int orc_slot_layout(int num_regions, int ring_depth, int token_cap, int topk,
-                    int hidden, int act_bytes, int num_experts, int has_shared,
-                    orc_layout* L) {
+/* Slot of an FFN rank among several ([RFC-GPU] "Capacity and ring depth":
+ * the routed fields hold routed_cap partial rows, the token fields
+ * token_cap tokens): routed_x holds max(token_cap, routed_cap) rows and
+ * route_table max(token_cap * topk, routed_cap) int32 (a token's k chosen
+ * ids in the return direction of the token form; the sender's partial
+ * index of each routed row in the dispatch direction of the multi-rank
+ * form).  routed_cap = 0: one FFN rank, the plain layout above. */
+int orc_slot_layout_ranks(int num_regions, int ring_depth, int token_cap, int topk,
+                          int hidden, int act_bytes, int num_experts, int has_shared,
+                          int64_t routed_cap, orc_layout* L) {
   if (num_regions <= 0 || ring_depth <= 0 || token_cap <= 0 || topk <= 0 ||
-      hidden <= 0 || (act_bytes != 2 && act_bytes != 4) || num_experts <= 0)
+      hidden <= 0 || (act_bytes != 2 && act_bytes != 4) || num_experts <= 0 || routed_cap < 0)
     return ORC_ERR_ARG;
   int64_t row = (int64_t)hidden * act_bytes;
   int64_t a = 256 / orc_gcd(256, row) * row;
+  int64_t rows = routed_cap > token_cap ? routed_cap : token_cap;
+  int64_t table = (int64_t)token_cap * topk;
+  if (routed_cap > table) table = routed_cap;
   int64_t off = 0;
   L->align = a;
   L->header = off;
   off += orc_round_up((int64_t)(H_FIXED_WORDS + num_experts) * 4, a);
   L->route_table = off;
-  off += orc_round_up((int64_t)token_cap * topk * 4, a);
+  off += orc_round_up(table * 4, a);
   L->routed_x = off;
-  off += orc_round_up((int64_t)token_cap * row, a);
+  off += orc_round_up(rows * row, a);
   L->shared_idx = off;
   if (has_shared) off += orc_round_up((int64_t)token_cap * 4, a);
   L->shared_x = off;
@@ -172,6 +182,37 @@ int orc_slot_layout(int num_regions, int ring_depth, int token_cap, int topk,
   L->window_bytes = L->flags_bytes + (int64_t)num_regions * ring_depth * off;
   return ORC_OK;
 }
+
+int orc_slot_layout(int num_regions, int ring_depth, int token_cap, int topk,
+                    int hidden, int act_bytes, int num_experts, int has_shared,
+                    orc_layout* L) {
+  return orc_slot_layout_ranks(num_regions, ring_depth, token_cap, topk, hidden, act_bytes,
+                               num_experts, has_shared, 0, L);
+}
+
+/* ------------------------------------------------------------------------ */
+/* several FFN ranks ([RFC-GPU] "Capacity and ring depth", "Data flow")       */
+/* ------------------------------------------------------------------------ */
+
+/* Experts of FFN rank r among F: a contiguous block; the pages fix no
+ * placement, and this build reads it as the balanced linear one -- the
+ * first E mod F ranks hold one expert more than the others. */
+void orc_expert_range(int E, int F, int r, int* first, int* count) {
+  int base = E / F, rem = E % F;
+  *count = base + (r < rem ? 1 : 0);
+  *first = r * base + (r < rem ? r : rem);
+}
+
+/* routed_cap = ceil(max_num_batched_tokens * topk / ffn_size) *
+ * routed_cap_multiplier, read as ceil(ceil(token_cap * topk / F) * mult). */
+int64_t orc_routed_cap(int token_cap, int topk, int F, double multiplier) {
+  int64_t even = ((int64_t)token_cap * topk + F - 1) / F;
+  return (int64_t)ceil((double)even * multiplier);
+}
+
+/* Shared rows of FFN rank r: tokens arange(r, n, F) ([RFC-GPU] "Data flow"
+ * step 3), i.e. how many of r, r + F, r + 2F, ... are below n. */
+int orc_rr_rows(int n, int r, int F) { return n > r ? (n - r + F - 1) / F : 0; }
 
 static uint8_t* orc_slot(uint8_t* win, const orc_layout* L, int region, int ring,
                          int ring_depth) {
@@ -546,6 +587,11 @@ typedef struct orc_cfg {
   int num_regions, ring_depth, token_cap, hidden, act_bytes, num_experts, topk;
   int inter, shared_inter, renorm, max_total_tokens;
   float routed_scaling;
+  /* this FFN rank among ffn_size (num_experts is then the rank's own count;
+   * ffn_size 0 or 1: one rank); routed_cap > 0: the rank receives token-level
+   * dispatch and its slots hold routed_cap routed rows (0: token_cap) */
+  int ffn_rank, ffn_size;
+  int64_t routed_cap;
 } orc_cfg;
 
 /* Header check of one dispatch slot ([RFC-GPU] "Window and slot layout":
@@ -847,10 +893,18 @@ int orc_pack_grouped(uint8_t* win, const orc_layout* L, int ring_depth, int regi
   return ORC_OK;
 }
 
+/* Routed rows a grouped slot may carry: routed_cap when the rank receives
+ * token-level dispatch ([RFC-GPU] "Capacity and ring depth"; routed_cap > 0
+ * in the configuration, with any number of ranks), else token_cap. */
+static int64_t orc_rows_cap(const orc_cfg* c) {
+  return c->routed_cap > 0 ? c->routed_cap : c->token_cap;
+}
+
 /* Header check of a grouped dispatch slot: the common fields in the order of
- * orc_check_slot, then num_tokens == n, routed_tokens == R (both within the
- * slot's token_cap rows), expert_counts summing to R, shared rows 0 or n with
- * shared_idx = 0..n-1. */
+ * orc_check_slot, then num_tokens == n (within token_cap), routed_tokens ==
+ * R (within the routed-row capacity), expert_counts summing to R, shared
+ * rows 0 or the rank's round-robin share of the n tokens with shared_idx =
+ * r, r + F, ... ([RFC-GPU] "Data flow" step 3; with one rank 0..n-1). */
 static int orc_check_grouped(const orc_cfg* c, uint8_t* win, const orc_layout* L, int region,
                              int stage, int layer, int R, int n, uint64_t seen) {
   uint64_t f = *orc_flag(win, region, stage, c->ring_depth);
@@ -867,18 +921,19 @@ static int orc_check_grouped(const orc_cfg* c, uint8_t* win, const orc_layout* L
   if (h[H_NUM_TOKENS] != n) return ORC_ERR_SHAPE;
   if (h[H_NUM_TOKENS] > c->token_cap) return ORC_ERR_CAPACITY;
   if (h[H_ROUTED_TOKENS] != R) return ORC_ERR_SHAPE;
-  if (h[H_ROUTED_TOKENS] > c->token_cap) return ORC_ERR_CAPACITY;
+  if (h[H_ROUTED_TOKENS] > orc_rows_cap(c)) return ORC_ERR_CAPACITY;
   int64_t sum = 0;
   for (int e = 0; e < c->num_experts; e++) {
     if (h[H_FIXED_WORDS + e] < 0) return ORC_ERR_SHAPE;
     sum += h[H_FIXED_WORDS + e];
   }
   if (sum != R) return ORC_ERR_SHAPE;
+  const int F = c->ffn_size > 1 ? c->ffn_size : 1, rank = F > 1 ? c->ffn_rank : 0;
   int st = h[H_SHARED_TOKENS];
-  if (st != 0 && (st != n || c->shared_inter <= 0)) return ORC_ERR_SHAPE;
+  if (st != 0 && (st != orc_rr_rows(n, rank, F) || c->shared_inter <= 0)) return ORC_ERR_SHAPE;
   if (st) {
     const int32_t* sidx = (const int32_t*)(s + L->shared_idx);
-    for (int i = 0; i < st; i++) if (sidx[i] != i) return ORC_ERR_SHAPE;
+    for (int i = 0; i < st; i++) if (sidx[i] != rank + i * F) return ORC_ERR_SHAPE;
   }
   return ORC_OK;
 }
@@ -894,9 +949,10 @@ static int orc_check_grouped(const orc_cfg* c, uint8_t* win, const orc_layout* L
  * y rows in arrival order, shared_x = the s rows); header echoing seq, with
  * routed_tokens = R_i, shared_tokens and expert_counts as received; then the
  * return flag = seq.  The argument rules follow orc_check_args with rows
- * (at most token_cap per peer) in place of tokens; the totals are bounded by
+ * (at most the routed-row capacity per peer) in place of tokens; the totals are bounded by
  * max_total_tokens * topk rows and max_total_tokens tokens.  Optional
- * outputs: y64 [sum R, hidden], s64 [sum n, hidden] (rows of the shared
+ * outputs: y64 [sum R, hidden], s64 [sum of each peer's shared-row count
+ * (n with one FFN rank, its round-robin share with several), hidden] (rows of the shared
  * branch of peers without shared rows are zero).  Parity: pinned by the
  * dense identity (E = 1) and by the combine identity with orc_ffn_forward. */
 int orc_grouped_forward(const orc_cfg* c, uint8_t* in_win, uint8_t* ret_win,
@@ -904,15 +960,17 @@ int orc_grouped_forward(const orc_cfg* c, uint8_t* in_win, uint8_t* ret_win,
                         const int* seq_lens, const int* slots, int n_peers, uint64_t* seen,
                         double* y64, double* s64, int nthreads) {
   orc_layout L;
-  int rc = orc_slot_layout(c->num_regions, c->ring_depth, c->token_cap, c->topk,
-                           c->hidden, c->act_bytes, c->num_experts, c->shared_inter > 0, &L);
+  int rc = orc_slot_layout_ranks(c->num_regions, c->ring_depth, c->token_cap, c->topk,
+                                 c->hidden, c->act_bytes, c->num_experts, c->shared_inter > 0,
+                                 c->routed_cap, &L);
   if (rc) return rc;
   rc = orc_check_args(c, stage, seq_lens, slots, n_peers);
   if (rc) return rc;
+  const int F = c->ffn_size > 1 ? c->ffn_size : 1, rank = F > 1 ? c->ffn_rank : 0;
   int64_t Rtot = 0;
   for (int i = 0; i < n_peers; i++) {
     if (rows[i] < 0) return ORC_ERR_ARG;
-    if (rows[i] > c->token_cap) return ORC_ERR_CAPACITY;
+    if (rows[i] > orc_rows_cap(c)) return ORC_ERR_CAPACITY;
     Rtot += rows[i];
   }
   int cap = c->max_total_tokens > 0 ? c->max_total_tokens : c->num_regions * c->token_cap;
@@ -931,11 +989,12 @@ int orc_grouped_forward(const orc_cfg* c, uint8_t* in_win, uint8_t* ret_win,
     const int32_t* hin = (const int32_t*)(sin + L.header);
     uint8_t* sout = orc_slot(ret_win, &L, p, stage, c->ring_depth);
     const int shared = hin[H_SHARED_TOKENS] > 0;
+    const int ns = orc_rr_rows(n, rank, F);   /* this rank's shared rows of the peer */
     /* expert of row r: the group of group_list holding it */
     int* expert = (int*)malloc(sizeof(int) * (R + 1));
     for (int e = 0, r = 0; e < E; e++)
       for (int q = 0; q < hin[H_FIXED_WORDS + e]; q++) expert[r++] = e;
-    int nrows = R + (shared ? n : 0);
+    int nrows = R + (shared ? ns : 0);
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
 #pragma omp parallel for schedule(dynamic, 1)
@@ -964,7 +1023,7 @@ int orc_grouped_forward(const orc_cfg* c, uint8_t* in_win, uint8_t* ret_win,
       free(x);
       free(y);
     }
-    if (s64 && !shared) memset(s64 + tbase * H, 0, sizeof(double) * (size_t)n * H);
+    if (s64 && !shared) memset(s64 + tbase * H, 0, sizeof(double) * (size_t)ns * H);
     free(expert);
     uint64_t seq = *orc_flag(in_win, p, stage, c->ring_depth);
     int32_t* h = (int32_t*)(sout + L.header);
@@ -984,8 +1043,156 @@ int orc_grouped_forward(const orc_cfg* c, uint8_t* in_win, uint8_t* ret_win,
     *orc_flag(ret_win, p, stage, c->ring_depth) = seq;
     seen[(int64_t)p * c->ring_depth + stage] = seq;
     rbase += R;
-    tbase += n;
+    tbase += ns;
   }
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* token-level dispatch to several FFN ranks and the Attention-side combine   */
+/* ------------------------------------------------------------------------ */
+
+/* One Attention peer's send to F FFN ranks ([RFC-GPU] "Data flow" steps 1-3
+ * and "Capacity and ring depth").  ids: the peer's top-k expert ids [n, k]
+ * (global, 0..E-1).  Step 1: the flattened ids are sorted stably; since every
+ * rank owns a contiguous block of experts (orc_expert_range), the sorted
+ * order is segmented by destination rank and grouped by local expert within
+ * each segment; the bincount gives each rank's group list.  A segment longer
+ * than routed_cap raises (AFD_ERR_CAPACITY) before anything is written.
+ * Step 3: rank r's slot (region = this peer, ring = stage) gets routed_x =
+ * the rows x[f / k] of its segment in order, route_table = their flattened
+ * indices f, shared rows = the tokens arange(r, n, F) with shared_idx = those
+ * token indices (when with_shared), and the header (num_tokens = n,
+ * routed_tokens = the segment's length, shared_tokens, num_experts = the
+ * rank's count, expert_counts = its group list), then the flag = seq.  Every
+ * rank gets its message, empty ones included.  Outputs for the combine:
+ * dst[f] = rank of partial f, pos[f] = its row in that rank's segment,
+ * rows_out[r] = segment lengths.  wins[r] / Ls[r]: rank r's dispatch window
+ * and slot layout.  Parity: pinned by the page's unit-test list (every
+ * partial routed exactly once, segments grouped by local expert, E not
+ * divisible by F, an empty destination) and by the round trip below. */
+int orc_dispatch_ranks(uint8_t** wins, const orc_layout* Ls, int F, int ring_depth, int region,
+                       int stage, int layer, const void* x, int n, const int* ids, int k, int E,
+                       int hidden, int act_bytes, int token_cap, int64_t routed_cap,
+                       int with_shared, int has_shared, uint64_t seq, int* dst, int* pos,
+                       int* rows_out) {
+  if (F < 1 || n < 0 || k < 1 || E < F) return ORC_ERR_ARG;
+  if (n > token_cap) return ORC_ERR_CAPACITY;
+  if (with_shared && !has_shared) return ORC_ERR_ARG;
+  const int N = n * k;
+  for (int f = 0; f < N; f++) if (ids[f] < 0 || ids[f] >= E) return ORC_ERR_ARG;
+  /* stable sort of the flattened ids (insertion sort: plain and stable) */
+  int* order = (int*)malloc(sizeof(int) * (N + 1));
+  for (int f = 0; f < N; f++) {
+    int q = f;
+    while (q > 0 && ids[order[q - 1]] > ids[f]) { order[q] = order[q - 1]; q--; }
+    order[q] = f;
+  }
+  int* counts = (int*)calloc((size_t)E, sizeof(int));
+  for (int f = 0; f < N; f++) counts[ids[f]]++;
+  int64_t seg = 0;
+  int rc = ORC_OK;
+  for (int r = 0; r < F && !rc; r++) {
+    int first, cnt;
+    orc_expert_range(E, F, r, &first, &cnt);
+    int R = 0;
+    for (int e = first; e < first + cnt; e++) R += counts[e];
+    rows_out[r] = R;
+    if (R > routed_cap) rc = ORC_ERR_CAPACITY;
+  }
+  if (rc) { free(order); free(counts); return rc; }
+  const int64_t row = (int64_t)hidden * act_bytes;
+  for (int r = 0; r < F; r++) {
+    int first, cnt;
+    orc_expert_range(E, F, r, &first, &cnt);
+    const int R = rows_out[r];
+    uint8_t* s = orc_slot(wins[r], &Ls[r], region, stage, ring_depth);
+    int32_t* table = (int32_t*)(s + Ls[r].route_table);
+    for (int q = 0; q < R; q++) {
+      const int f = order[seg + q];
+      memcpy(s + Ls[r].routed_x + (int64_t)q * row, (const char*)x + (int64_t)(f / k) * row,
+             (size_t)row);
+      table[q] = f;
+      dst[f] = r;
+      pos[f] = q;
+    }
+    seg += R;
+    const int ns = with_shared ? orc_rr_rows(n, r, F) : 0;
+    int32_t* sidx = (int32_t*)(s + Ls[r].shared_idx);
+    for (int i = 0; i < ns; i++) {
+      const int t = r + i * F;
+      sidx[i] = t;
+      memcpy(s + Ls[r].shared_x + (int64_t)i * row, (const char*)x + (int64_t)t * row, (size_t)row);
+    }
+    int32_t* h = (int32_t*)(s + Ls[r].header);
+    memset(h, 0, (size_t)(H_FIXED_WORDS + cnt) * 4);
+    h[H_MAGIC] = (int32_t)ORC_MAGIC;
+    h[H_VERSION] = ORC_VERSION;
+    h[H_SEQ] = (int32_t)(uint32_t)seq;
+    h[H_ECHO_SEQ] = (int32_t)(uint32_t)seq;
+    h[H_LAYER] = layer;
+    h[H_STAGE] = stage;
+    h[H_NUM_TOKENS] = n;
+    h[H_ROUTED_TOKENS] = R;
+    h[H_SHARED_TOKENS] = ns;
+    h[H_NUM_EXPERTS] = cnt;
+    h[H_LEN] = H_FIXED_WORDS + cnt;
+    for (int e = 0; e < cnt; e++) h[H_FIXED_WORDS + e] = counts[first + e];
+    *orc_flag(wins[r], region, stage, ring_depth) = seq;
+  }
+  free(order);
+  free(counts);
+  return ORC_OK;
+}
+
+/* The Attention side's receive of a multi-rank step ([RFC-GPU] "Data flow":
+ * recv_ffn_output waits only on the ranks that received data at dispatch --
+ * an empty message never creates a wait -- and accumulates each arrival in
+ * fp32 with the weighted scatter; the shared branch is added by shared_idx).
+ * For every rank r with rows_out[r] routed rows or shared rows: its return
+ * flag must equal expect_seq and its header echo it, with routed_tokens =
+ * rows_out[r] and shared_tokens = its round-robin share (or 0 without
+ * shared rows).  Then, in fp64, out[t] = sum over j ascending of w[t, j] *
+ * y(dst[t k + j], pos[t k + j]) + s(t mod F, t div F) -- y and s as the ranks
+ * returned them -- rounded once to the activation type into out_act (when
+ * not NULL); out64 keeps the unrounded sums.  Parity: the round trip with F
+ * ranks equals the one with a single rank exactly (pinned in the tests). */
+int orc_attn_combine(uint8_t** rets, const orc_layout* Ls, int F, int ring_depth, int region,
+                     int stage, int n, int k, const int* dst, const int* pos, const float* w,
+                     const int* rows_out, int with_shared, int hidden, int act_bytes,
+                     uint64_t expect_seq, double* out64, void* out_act) {
+  for (int r = 0; r < F; r++) {
+    const int ns = with_shared ? orc_rr_rows(n, r, F) : 0;
+    if (rows_out[r] == 0 && ns == 0) continue;  /* an empty message: no wait */
+    uint64_t fl = *orc_flag(rets[r], region, stage, ring_depth);
+    if (fl < expect_seq) return ORC_ERR_TIMEOUT;
+    if (fl > expect_seq) return ORC_ERR_SEQ;
+    const int32_t* h = (const int32_t*)(orc_slot(rets[r], &Ls[r], region, stage, ring_depth) +
+                                        Ls[r].header);
+    if ((uint32_t)h[H_MAGIC] != ORC_MAGIC || h[H_VERSION] != ORC_VERSION) return ORC_ERR_HEADER;
+    if ((uint32_t)h[H_ECHO_SEQ] != (uint32_t)expect_seq) return ORC_ERR_SEQ;
+    if (h[H_NUM_TOKENS] != n || h[H_ROUTED_TOKENS] != rows_out[r] || h[H_SHARED_TOKENS] != ns)
+      return ORC_ERR_SHAPE;
+  }
+  for (int t = 0; t < n; t++)
+    for (int c = 0; c < hidden; c++) {
+      double a = 0.0;
+      for (int j = 0; j < k; j++) {
+        const int f = t * k + j, r = dst[f];
+        const uint8_t* s = orc_slot(rets[r], &Ls[r], region, stage, ring_depth);
+        a += (double)w[f] * orc_ld(s + Ls[r].routed_x, act_bytes, (int64_t)pos[f] * hidden + c);
+      }
+      if (with_shared) {
+        const int r = t % F;
+        const uint8_t* s = orc_slot(rets[r], &Ls[r], region, stage, ring_depth);
+        a += orc_ld(s + Ls[r].shared_x, act_bytes, (int64_t)(t / F) * hidden + c);
+      }
+      if (out64) out64[(int64_t)t * hidden + c] = a;
+      if (out_act) {
+        if (act_bytes == 2) ((uint16_t*)out_act)[(int64_t)t * hidden + c] = orc_f64_to_bf16(a);
+        else ((float*)out_act)[(int64_t)t * hidden + c] = (float)a;
+      }
+    }
   return ORC_OK;
 }
 

@@ -38,7 +38,8 @@ class Cfg(C.Structure):
                 ("act_bytes", C.c_int), ("num_experts", C.c_int),
                 ("topk", C.c_int), ("inter", C.c_int), ("shared_inter", C.c_int),
                 ("renorm", C.c_int), ("max_total_tokens", C.c_int),
-                ("routed_scaling", C.c_float)]
+                ("routed_scaling", C.c_float), ("ffn_rank", C.c_int), ("ffn_size", C.c_int),
+                ("routed_cap", C.c_int64)]
 
 
 _LIBS = {}
@@ -69,6 +70,13 @@ def load(path=None):
         "orc_pack_grouped": (I, [P, P, I, I, I, I, P, I, P, P, I, I, I, I, I, I, I, U64]),
         "orc_grouped_forward": (I, [P, P, P, P, I, I, P, P, P, I, P, P, P, I]),
         "orc_num_threads": (I, []),
+        "orc_slot_layout_ranks": (I, [I, I, I, I, I, I, I, I, I64, P]),
+        "orc_expert_range": (V, [I, I, I, P, P]),
+        "orc_routed_cap": (I64, [I, I, I, C.c_double]),
+        "orc_rr_rows": (I, [I, I, I]),
+        "orc_dispatch_ranks": (I, [P, P, I, I, I, I, I, P, I, P, I, I, I, I, I, I64, I, I, U64,
+                                   P, P, P]),
+        "orc_attn_combine": (I, [P, P, I, I, I, I, I, I, P, P, P, P, I, I, I, U64, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -218,11 +226,13 @@ def combine(y, w, s=None, lib=None):
 def make_cfg(c):
     """c: dict with num_regions, ring_depth, token_cap, hidden, act_bytes,
     num_experts, topk, inter, shared_inter, renorm, max_total_tokens,
-    routed_scaling."""
+    routed_scaling; for one FFN rank among several also ffn_rank, ffn_size
+    and routed_cap (num_experts is then the rank's own count)."""
     return Cfg(c["num_regions"], c["ring_depth"], c["token_cap"], c["hidden"],
                c["act_bytes"], c["num_experts"], c["topk"], c["inter"],
                c["shared_inter"], int(c["renorm"]), c.get("max_total_tokens", 0),
-               float(c.get("routed_scaling", 1.0)))
+               float(c.get("routed_scaling", 1.0)), int(c.get("ffn_rank", 0)),
+               int(c.get("ffn_size", 1)), int(c.get("routed_cap", 0)))
 
 
 def ffn_forward(c, in_win, ret_win, Wdict, layer, stage, seq_lens, slots, seen,
@@ -278,12 +288,14 @@ def grouped_forward(c, in_win, ret_win, Wdict, layer, stage, rows, seq_lens, slo
     sl = np.ascontiguousarray(seq_lens, np.int32)
     sp = np.ascontiguousarray(slots, np.int32)
     H = c["hidden"]
+    F, r = int(c.get("ffn_size", 1)), int(c.get("ffn_rank", 0))
+    ns = sum(rr_rows(int(n), r, F, lib) for n in sl) if F > 1 else int(sl.sum())
     y = np.zeros((max(int(rw.sum()), 1), H), np.float64)
-    s = np.zeros((max(int(sl.sum()), 1), H), np.float64)
+    s = np.zeros((max(ns, 1), H), np.float64)
     rc = lib.orc_grouped_forward(C.byref(cfg), _p(in_win), _p(ret_win), C.byref(W), layer, stage,
                                  _p(rw), _p(sl), _p(sp), int(sl.size), _p(seen), _p(y), _p(s),
                                  nthreads)
-    return rc, y[:int(rw.sum())], s[:int(sl.sum())]
+    return rc, y[:int(rw.sum())], s[:ns]
 
 
 def forward_tokens(c, in_win, Wdict, stage, seq_lens, slots, tokens, nthreads=0,
@@ -304,6 +316,78 @@ def forward_tokens(c, in_win, Wdict, stage, seq_lens, slots, tokens, nthreads=0,
     if rc:
         raise ValueError(f"orc_forward_tokens rc={rc}")
     return ids, w, out
+
+
+# --------------------------------------------------------------------------
+# several FFN ranks: expert placement, capacity, dispatch, combine
+# --------------------------------------------------------------------------
+def slot_layout_ranks(num_regions, ring_depth, token_cap, topk, hidden, act_bytes, num_experts,
+                      has_shared, routed_cap, lib=None):
+    lib = lib or load()
+    L = Layout()
+    rc = lib.orc_slot_layout_ranks(num_regions, ring_depth, token_cap, topk, hidden, act_bytes,
+                                   num_experts, int(bool(has_shared)), int(routed_cap), C.byref(L))
+    if rc:
+        raise ValueError(f"orc_slot_layout_ranks rc={rc}")
+    return L
+
+
+def expert_range(E, F, r, lib=None):
+    """(first expert, count) of FFN rank r among F"""
+    lib = lib or load()
+    first, count = C.c_int(0), C.c_int(0)
+    lib.orc_expert_range(E, F, r, C.byref(first), C.byref(count))
+    return first.value, count.value
+
+
+def routed_cap(token_cap, topk, F, multiplier, lib=None):
+    return int((lib or load()).orc_routed_cap(token_cap, topk, F, float(multiplier)))
+
+
+def rr_rows(n, r, F, lib=None):
+    return int((lib or load()).orc_rr_rows(int(n), int(r), int(F)))
+
+
+def dispatch_ranks(wins, layouts, ring_depth, region, stage, layer, x, ids, E, hidden, act_bytes,
+                   token_cap, rcap, with_shared, has_shared, seq, lib=None):
+    """One peer's send to len(wins) FFN ranks; returns (rc, dst [n*k], pos [n*k],
+    rows per rank [F])."""
+    lib = lib or load()
+    F = len(wins)
+    x = np.ascontiguousarray(x)
+    ids = np.ascontiguousarray(ids, np.int32)
+    n, k = ids.shape
+    wp = (C.c_void_p * F)(*[w.ctypes.data for w in wins])
+    Ls = (Layout * F)(*layouts)
+    dst = np.full(max(n * k, 1), -1, np.int32)
+    pos = np.full(max(n * k, 1), -1, np.int32)
+    rows = np.zeros(F, np.int32)
+    rc = lib.orc_dispatch_ranks(C.cast(wp, C.c_void_p), C.cast(Ls, C.c_void_p), F, ring_depth,
+                                region, stage, layer, _p(x), n, _p(ids), k, E, hidden, act_bytes,
+                                token_cap, int(rcap), int(bool(with_shared)),
+                                int(bool(has_shared)), seq, _p(dst), _p(pos), _p(rows))
+    return rc, dst[:n * k], pos[:n * k], rows
+
+
+def attn_combine(rets, layouts, ring_depth, region, stage, n, k, dst, pos, w, rows, with_shared,
+                 hidden, act_bytes, expect_seq, lib=None):
+    """The Attention side's combine of F ranks' returns; (rc, out64 [n, H],
+    out in the activation type (uint16 bf16 bits or float32))."""
+    lib = lib or load()
+    F = len(rets)
+    rp = (C.c_void_p * F)(*[r.ctypes.data for r in rets])
+    Ls = (Layout * F)(*layouts)
+    dst = np.ascontiguousarray(dst, np.int32)
+    pos = np.ascontiguousarray(pos, np.int32)
+    w = np.ascontiguousarray(w, np.float32)
+    rows = np.ascontiguousarray(rows, np.int32)
+    out64 = np.zeros((max(n, 1), hidden), np.float64)
+    out = np.zeros((max(n, 1), hidden), np.uint16 if act_bytes == 2 else np.float32)
+    rc = lib.orc_attn_combine(C.cast(rp, C.c_void_p), C.cast(Ls, C.c_void_p), F, ring_depth,
+                              region, stage, n, k, _p(dst), _p(pos), _p(w), _p(rows),
+                              int(bool(with_shared)), hidden, act_bytes, expect_seq, _p(out64),
+                              _p(out))
+    return rc, out64[:n], out[:n]
 
 
 def num_threads(lib=None):

@@ -525,8 +525,235 @@ def check_grouped_faults(lib):
                           32, 4, 16, 4, 0, 0, 301, lib=lib) == O.ERR_SHAPE
 
 
+# --------------------------------------------------------------------------
+# several FFN ranks
+# --------------------------------------------------------------------------
+def check_expert_range(lib):
+    """Experts of FFN rank r among F (a reading: contiguous blocks, the first
+    E mod F ranks one expert more): the blocks tile 0..E-1 in rank order,
+    every rank holds at least one, and sizes differ by at most one, larger
+    first."""
+    for E in range(1, 41):
+        for F in range(1, E + 1):
+            got = [O.expert_range(E, F, r, lib=lib) for r in range(F)]
+            nxt = 0
+            for first, cnt in got:
+                assert first == nxt and cnt >= 1, (E, F, got)
+                nxt += cnt
+            assert nxt == E
+            sizes = [c for _, c in got]
+            assert max(sizes) - min(sizes) <= 1 and sizes == sorted(sizes, reverse=True)
+
+
+def check_routed_cap(lib):
+    """routed_cap against hand-computed values of the page's formula
+    (tests/golden/routed_cap.json)."""
+    for c in _golden("routed_cap.json")["cases"]:
+        got = O.routed_cap(c["token_cap"], c["topk"], c["ffn_size"], c["multiplier"], lib=lib)
+        assert got == c["routed_cap"], (c, got)
+    # the round-robin share: arange(r, n, F)
+    for n in range(0, 30):
+        for F in range(1, 7):
+            for r in range(F):
+                assert O.rr_rows(n, r, F, lib=lib) == len(range(r, n, F))
+
+
+def ranks_setup(F, E, k, hidden, ab, token_cap, mult, has_shared, lib, num_regions=2,
+                ring_depth=1):
+    rcap = O.routed_cap(token_cap, k, F, mult, lib=lib)
+    Ls, wins, rets = [], [], []
+    for r in range(F):
+        _, cnt = O.expert_range(E, F, r, lib=lib)
+        L = O.slot_layout_ranks(num_regions, ring_depth, token_cap, k, hidden, ab, cnt, has_shared,
+                                rcap, lib=lib)
+        Ls.append(L)
+        wins.append(np.zeros(L.window_bytes, np.uint8))
+        rets.append(np.zeros(L.window_bytes, np.uint8))
+    return rcap, Ls, wins, rets
+
+
+def slot_field(win, L, region, stage, ring_depth, field, nbytes):
+    off = L.flags_bytes + (region * ring_depth + stage) * L.slot_bytes + getattr(L, field)
+    return win[off: off + nbytes]
+
+
+def distinct_topk(rng, n, E, k):
+    return np.argsort(rng.random((n, E)), axis=1)[:, :k].astype(np.int32)
+
+
+def check_dispatch_ranks(lib):
+    """One peer's send to F ranks, against the page's unit-test list: every
+    partial routed exactly once, each destination's segment grouped by local
+    expert (stable: numpy's stable argsort restricted to the rank's
+    experts), E not divisible by F, the shared rows round-robin, an empty
+    destination (a header with no rows, its flag still written), and a
+    segment over routed_cap raising before anything is written."""
+    rng = np.random.default_rng(41)
+    H, ab, E, F, k, n, cap = 32, 4, 10, 4, 3, 11, 16
+    rcap, Ls, wins, _ = ranks_setup(F, E, k, H, ab, cap, 2.0, True, lib)
+    x = rand_act(rng, (n, H), ab)
+    ids = distinct_topk(rng, n, E, k)
+    rc, dst, pos, rows = O.dispatch_ranks(wins, Ls, 1, 1, 0, 3, x, ids, E, H, ab, cap, rcap, True,
+                                          True, 77, lib=lib)
+    assert rc == 0
+    flat = ids.reshape(-1)
+    order = np.argsort(flat, kind="stable")
+    seen = []
+    for r in range(F):
+        first, cnt = O.expert_range(E, F, r, lib=lib)
+        mine = order[(flat[order] >= first) & (flat[order] < first + cnt)]
+        assert rows[r] == mine.size
+        table = slot_field(wins[r], Ls[r], 1, 0, 1, "route_table", 4 * mine.size).view(np.int32)
+        assert np.array_equal(table, mine)          # grouped by local expert, stable
+        seen.extend(table.tolist())
+        assert np.array_equal(dst[mine], np.full(mine.size, r)) and np.array_equal(pos[mine], np.arange(mine.size))
+        got = slot_field(wins[r], Ls[r], 1, 0, 1, "routed_x", mine.size * H * 4).view(np.float32)
+        assert np.array_equal(got.reshape(-1, H), x[mine // k])
+        h = slot_field(wins[r], Ls[r], 1, 0, 1, "header", 4 * (12 + cnt)).view(np.int32)
+        share = np.arange(r, n, F)
+        assert h[5] == 3 and h[7] == n and h[8] == mine.size and h[9] == share.size and h[10] == cnt
+        assert np.array_equal(h[12:], np.bincount(flat - first, minlength=E)[:cnt]
+                              if False else np.bincount(flat, minlength=E)[first:first + cnt])
+        sidx = slot_field(wins[r], Ls[r], 1, 0, 1, "shared_idx", 4 * share.size).view(np.int32)
+        assert np.array_equal(sidx, share)
+        sx = slot_field(wins[r], Ls[r], 1, 0, 1, "shared_x", share.size * H * 4).view(np.float32)
+        assert np.array_equal(sx.reshape(-1, H), x[share])
+        assert wins[r][:Ls[r].flags_bytes].view(np.uint64)[1] == 77
+    assert sorted(seen) == list(range(n * k))     # every partial exactly once
+    # an empty destination: two tokens (ranks 2 and 3 get no shared row), all
+    # ids among rank 0's experts
+    rcap, Ls, wins, _ = ranks_setup(F, E, k, H, ab, cap, 2.0, True, lib)
+    x2 = rand_act(rng, (2, H), ab)
+    ids2 = np.array([[0, 1, 2], [2, 1, 0]], np.int32)
+    rc, dst, pos, rows = O.dispatch_ranks(wins, Ls, 1, 0, 0, 0, x2, ids2, E, H, ab, cap, rcap, True,
+                                          True, 5, lib=lib)
+    assert rc == 0 and list(rows) == [6, 0, 0, 0]
+    for r in (2, 3):
+        _, cnt = O.expert_range(E, F, r, lib=lib)
+        h = slot_field(wins[r], Ls[r], 0, 0, 1, "header", 4 * (12 + cnt)).view(np.int32)
+        assert h[8] == 0 and h[9] == 0 and not h[12:].any()
+        assert wins[r][:8].view(np.uint64)[0] == 5
+    # overflow: every partial on rank 0 with the multiplier at 1.0 (even share
+    # ceil(16 * 3 / 4) = 12 < 33 partials): raise, write nothing
+    rcap, Ls, wins, _ = ranks_setup(F, E, k, H, ab, cap, 1.0, True, lib)
+    ids3 = np.tile(np.array([0, 1, 2], np.int32), (n, 1))
+    rc, _, _, _ = O.dispatch_ranks(wins, Ls, 1, 0, 0, 0, x, ids3, E, H, ab, cap, rcap, True, True, 9,
+                                   lib=lib)
+    assert rc == O.ERR_CAPACITY
+    assert all(not w.any() for w in wins)
+
+
+def ranks_round_trip(lib, F, E, ab, xs, Wt, ids, ws, with_shared, k, H, inter, shared_inter, cap):
+    """Dispatch every peer to F ranks, run each rank's grouped step (its own
+    expert slice of the weights), combine on the Attention side; returns the
+    per-peer fp64 outputs."""
+    P = len(xs)
+    rcap, Ls, wins, rets = ranks_setup(F, E, k, H, ab, cap, 2.0, shared_inter > 0, lib,
+                                       num_regions=P)
+    plans = []
+    for p in range(P):
+        rc, dst, pos, rows = O.dispatch_ranks(wins, Ls, 1, p, 0, 0, xs[p], ids[p], E, H, ab, cap,
+                                              rcap, with_shared, shared_inter > 0, 500 + p,
+                                              lib=lib)
+        assert rc == 0, rc
+        plans.append((dst, pos, rows))
+    for r in range(F):
+        first, cnt = O.expert_range(E, F, r, lib=lib)
+        cfg = dict(num_regions=P, ring_depth=1, token_cap=cap, hidden=H, act_bytes=ab,
+                   num_experts=cnt, topk=k, inter=inter, shared_inter=shared_inter, renorm=False,
+                   max_total_tokens=0, routed_scaling=1.0, ffn_rank=r, ffn_size=F,
+                   routed_cap=rcap)
+        Wr = dict(Wt)
+        Wr["W13"] = np.ascontiguousarray(Wt["W13"][first:first + cnt])
+        Wr["Wd"] = np.ascontiguousarray(Wt["Wd"][first:first + cnt])
+        seen = np.zeros(P, np.uint64)
+        rc, _, _ = O.grouped_forward(cfg, wins[r], rets[r], Wr, 0, 0,
+                                     [int(plans[p][2][r]) for p in range(P)],
+                                     [x.shape[0] for x in xs], list(range(P)), seen, lib=lib)
+        assert rc == 0, (r, rc)
+    outs = []
+    for p in range(P):
+        dst, pos, rows = plans[p]
+        rc, out64, _ = O.attn_combine(rets, Ls, 1, p, 0, xs[p].shape[0], k, dst, pos, ws[p], rows,
+                                      with_shared, H, ab, 500 + p, lib=lib)
+        assert rc == 0, rc
+        outs.append(out64)
+    return outs
+
+
+def check_ranks_round_trip(lib):
+    """Token-level dispatch to F ranks, each rank's grouped step on its own
+    experts and round-robin shared rows, then the Attention side's combine,
+    equals the same step with one FFN rank, exactly (the same expert
+    arithmetic on the same rows, the same summation order); for E divisible
+    by F and not, with and without the shared expert, fp32 and bf16."""
+    rng = np.random.default_rng(43)
+    H, k, inter, Is = 64, 3, 32, 16
+    for ab in (4, 2):
+        for E, F, with_shared in ((8, 2, True), (10, 4, True), (6, 3, False), (9, 2, True)):
+            cfg, xs, Wt = make_problem(rng, seq_lens=[7, 12], hidden=H, E=E, k=k, inter=inter,
+                                       shared_inter=Is, act_bytes=ab, token_cap=48)
+            ids = [distinct_topk(rng, x.shape[0], E, k) for x in xs]
+            ws = [rng.random((x.shape[0], k)).astype(np.float32) for x in xs]
+            one = ranks_round_trip(lib, 1, E, ab, xs, Wt, ids, ws, with_shared, k, H, inter, Is, 12)
+            many = ranks_round_trip(lib, F, E, ab, xs, Wt, ids, ws, with_shared, k, H, inter, Is, 12)
+            for p in range(len(xs)):
+                assert np.array_equal(one[p], many[p]), (ab, E, F, p)
+            # and the single rank is the grouped form of the FFN-side layer:
+            # dense mixture with these ids and weights (numpy, tolerance)
+            for p, x in enumerate(xs):
+                X = act_to_f64(x, ab)
+                ref = np.zeros_like(one[p])
+                for t in range(X.shape[0]):
+                    for j in range(k):
+                        e = ids[p][t, j]
+                        y = np_swiglu(X[t:t + 1], act_to_f64(Wt["W13"][e], ab),
+                                      act_to_f64(Wt["Wd"][e], ab), ab)[0]
+                        ref[t] += np.float64(ws[p][t, j]) * np_round_act(y, ab)
+                if with_shared:
+                    ref += np_round_act(np_swiglu(X, act_to_f64(Wt["W13s"], ab),
+                                                  act_to_f64(Wt["Wds"], ab), ab), ab)
+                err = np.abs(one[p] - ref).max() / np.sqrt((ref ** 2).mean())
+                assert err < (1e-2 if ab == 2 else 1e-5), (ab, E, F, p, err)
+
+
+def check_ranks_faults(lib):
+    """An FFN rank's header checks: shared rows other than its round-robin
+    share, or shared_idx not r, r + F, ...: AFD_ERR_SHAPE; more routed rows
+    than routed_cap: AFD_ERR_CAPACITY."""
+    rng = np.random.default_rng(47)
+    H, ab, E, F, k, n, cap, inter = 32, 4, 6, 2, 2, 9, 16, 16
+    cfg0, xs, Wt = make_problem(rng, seq_lens=[n], hidden=H, E=E, k=k, inter=inter,
+                                shared_inter=16, act_bytes=ab, token_cap=cap)
+    rcap, Ls, wins, rets = ranks_setup(F, E, k, H, ab, cap, 2.0, True, lib, num_regions=1)
+    ids = distinct_topk(rng, n, E, k)
+    rc, dst, pos, rows = O.dispatch_ranks(wins, Ls, 1, 0, 0, 0, xs[0], ids, E, H, ab, cap, rcap, True,
+                                          True, 11, lib=lib)
+    assert rc == 0
+    r = 1
+    first, cnt = O.expert_range(E, F, r, lib=lib)
+    cfg = dict(cfg0, num_regions=1, num_experts=cnt, ffn_rank=r, ffn_size=F, routed_cap=rcap)
+    Wr = dict(Wt, W13=np.ascontiguousarray(Wt["W13"][first:first + cnt]),
+              Wd=np.ascontiguousarray(Wt["Wd"][first:first + cnt]))
+
+    def fwd(w, R=None):
+        return O.grouped_forward(cfg, w, np.zeros_like(w), Wr, 0, 0, [int(rows[r]) if R is None else R],
+                                 [n], [0], np.zeros(1, np.uint64), lib=lib)[0]
+    assert fwd(wins[r]) == 0
+    hoff = Ls[r].flags_bytes + Ls[r].header
+    bad = wins[r].copy()
+    bad[hoff + 4 * 9: hoff + 4 * 10] = np.array([n], np.int32).view(np.uint8)   # all n tokens
+    assert fwd(bad) == O.ERR_SHAPE
+    bad = wins[r].copy()
+    soff = Ls[r].flags_bytes + Ls[r].shared_idx
+    bad[soff: soff + 4] = np.array([0], np.int32).view(np.uint8)   # rank 0's first token
+    assert fwd(bad) == O.ERR_SHAPE
+    assert fwd(wins[r], R=rcap + 1) == O.ERR_CAPACITY
+
+
 ALL_CHECKS = [check_bf16, check_layout, check_header_roundtrip, check_split,
               check_logit_order, check_router, check_router_ties, check_plan,
               check_dense_swiglu, check_dense_mixture, check_identity_combine,
               check_fanin_split, check_hand_moe, check_fault_codes, check_grouped_dense,
-              check_grouped_combine, check_grouped_faults]
+              check_grouped_combine, check_grouped_faults, check_expert_range, check_routed_cap,
+              check_dispatch_ranks, check_ranks_round_trip, check_ranks_faults]

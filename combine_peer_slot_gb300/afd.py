@@ -26,6 +26,7 @@ AFD_NOALLOC_MAX_LOGITS = 1048576
 AFD_MAX_PEERS = 64
 AFD_MAX_RING = 64
 AFD_FORM_TOKENS, AFD_FORM_GROUPED = 0, 1
+AFD_MAX_FFN_RANKS = 16
 
 
 class afd_config(C.Structure):
@@ -35,7 +36,7 @@ class afd_config(C.Structure):
                 ("shared_inter", C.c_int32), ("act_dtype", C.c_int32), ("renorm", C.c_int32),
                 ("max_layers", C.c_int32), ("gemm", C.c_int32), ("flags", C.c_int32),
                 ("routed_scaling", C.c_float), ("routed_cap_multiplier", C.c_float),
-                ("wait_timeout_ns", C.c_int64)]
+                ("wait_timeout_ns", C.c_int64), ("ffn_rank", C.c_int32), ("ffn_size", C.c_int32)]
 
 
 class afd_layout(C.Structure):
@@ -94,6 +95,15 @@ SIGNATURES = [
     ("afd_serve_graph_destroy", None, [_P]),
     ("afd_serve_log", _I, [_P, C.POINTER(C.c_int32), _I, C.POINTER(C.c_int),
                            C.POINTER(_I64)]),
+    ("afd_get_config", _I, [_P, C.POINTER(afd_config)]),
+    ("afd_expert_range", _I, [_I, _I, _I, C.POINTER(C.c_int), C.POINTER(C.c_int)]),
+    ("afd_attn_create", _I, [C.POINTER(_P), _I, _I, _I, _P, C.POINTER(_P)]),
+    ("afd_attn_destroy", None, [_P]),
+    ("afd_attn_dispatch", _I, [_P, _I, _I, _P, _I, _P, _I, _U64]),
+    ("afd_attn_combine", _I, [_P, _I, _P, _P, _I, _U64]),
+    ("afd_attn_rows", _I, [_P, _I, C.POINTER(C.c_int)]),
+    ("afd_attn_poll_status", _I, [_P]),
+    ("afd_attn_launch_count", _I64, [_P]),
 ]
 AFD_NUM_STAGES = 8
 STAGE_NAMES = ("header_check", "router", "plan", "gather", "gemm_swiglu", "gemm_down",
@@ -135,12 +145,13 @@ def _ints(seq):
 def make_config(num_peers, token_cap, hidden, num_experts, topk, inter, shared_inter=0,
                 act="bf16", renorm=False, routed_scaling=1.0, ring_depth=1,
                 max_total_tokens=0, max_layers=1, gemm=AFD_GEMM_TENSOR,
-                routed_cap_multiplier=2.0, wait_timeout_ns=0, flags=0):
+                routed_cap_multiplier=2.0, wait_timeout_ns=0, flags=0, ffn_rank=0, ffn_size=0):
     return afd_config(num_peers, ring_depth, token_cap, max_total_tokens, hidden, num_experts,
                       topk, inter, shared_inter,
                       AFD_DTYPE_BF16 if act == "bf16" else AFD_DTYPE_F32, int(bool(renorm)),
                       max_layers, gemm, int(flags), float(routed_scaling),
-                      float(routed_cap_multiplier), int(wait_timeout_ns))
+                      float(routed_cap_multiplier), int(wait_timeout_ns), int(ffn_rank),
+                      int(ffn_size))
 
 
 # ---- thin functional wrappers (same names as the C ABI) ----------------------
@@ -288,3 +299,55 @@ def afd_serve_log(ctx, max_records=64):
     _check(lib().afd_serve_log(ctx, recs, int(max_records), C.byref(n), C.byref(served)),
            "afd_serve_log")
     return [tuple(recs[4 * j:4 * j + 4]) for j in range(n.value)], int(served.value)
+
+
+def afd_get_config(ctx):
+    c = afd_config()
+    _check(lib().afd_get_config(ctx, C.byref(c)), "afd_get_config")
+    return c
+
+
+def afd_expert_range(num_experts, ffn_size, ffn_rank):
+    """(first expert, count) of FFN rank ffn_rank among ffn_size"""
+    first, count = C.c_int(0), C.c_int(0)
+    _check(lib().afd_expert_range(int(num_experts), int(ffn_size), int(ffn_rank),
+                                  C.byref(first), C.byref(count)), "afd_expert_range")
+    return first.value, count.value
+
+
+def afd_attn_create(ranks, peer, num_experts, stream=0):
+    """One Attention peer over the FFN-rank contexts ranks (rank order)."""
+    arr = (C.c_void_p * max(len(ranks), 1))(*[r.value if isinstance(r, C.c_void_p) else r
+                                                for r in ranks])
+    a = C.c_void_p()
+    _check(lib().afd_attn_create(arr, len(ranks), int(peer), int(num_experts),
+                                 C.c_void_p(int(stream)), C.byref(a)), "afd_attn_create")
+    return a
+
+
+def afd_attn_destroy(a):
+    lib().afd_attn_destroy(a)
+
+
+def afd_attn_dispatch(a, stage, layer, x_ptr, n_tokens, ids_ptr, with_shared, seq):
+    return lib().afd_attn_dispatch(a, int(stage), int(layer), x_ptr or None, int(n_tokens),
+                                   ids_ptr or None, int(bool(with_shared)), seq)
+
+
+def afd_attn_combine(a, stage, w_ptr, out_ptr, n_tokens, expect_seq):
+    return lib().afd_attn_combine(a, int(stage), w_ptr or None, out_ptr or None, int(n_tokens),
+                                  expect_seq)
+
+
+def afd_attn_rows(a, stage, ffn_size):
+    rows = (C.c_int * ffn_size)()
+    _check(lib().afd_attn_rows(a, int(stage), rows), "afd_attn_rows")
+    return list(rows)
+
+
+def afd_attn_poll_status(a):
+    return lib().afd_attn_poll_status(a)
+
+
+def afd_attn_launch_count(a):
+    return int(lib().afd_attn_launch_count(a))

@@ -16,7 +16,8 @@ NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
-SOURCES = ["afd_api.cu", "afd_kernels.cu", "afd_gemm_tc.cu", "afd_gemm_tc2.cu", "afd_noalloc.cu"]
+SOURCES = ["afd_api.cu", "afd_kernels.cu", "afd_gemm_tc.cu", "afd_gemm_tc2.cu", "afd_noalloc.cu",
+           "afd_attn.cu"]
 
 
 def _compile(src, verbose):

@@ -8,6 +8,7 @@
 #include <vector>
 
 #include <algorithm>
+#include <cmath>
 #include <utility>
 
 #include "afd_internal.cuh"
@@ -102,19 +103,30 @@ int check_dev_ptr(const void* p) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// routed rows a slot may carry: routed_cap under token-level dispatch
+// (ceil(ceil(token_cap * topk / ffn_size) * multiplier)), else token_cap
+int64_t routed_cap_of(const afd_config* c) {
+  if (c->ffn_size < 1) return c->token_cap;
+  const int64_t even = ((int64_t)c->token_cap * c->topk + c->ffn_size - 1) / c->ffn_size;
+  return (int64_t)std::ceil((double)even * (double)c->routed_cap_multiplier);
+}
+
 int layout_of(const afd_config* c, afd_layout* L) {
   const int64_t ab = c->act_dtype == AFD_DTYPE_BF16 ? 2 : 4;
   const int64_t row = (int64_t)c->hidden * ab;
   const int64_t a = 256 / gcd64(256, row) * row;
   const int has_shared = c->shared_inter > 0;
+  const int64_t rcap = routed_cap_of(c);
+  const int64_t rows = std::max<int64_t>(c->token_cap, rcap);
+  const int64_t table = std::max<int64_t>((int64_t)c->token_cap * c->topk, c->ffn_size >= 1 ? rcap : 0);
   int64_t off = 0;
   L->align = a;
   L->header = off;
   off += round_up((int64_t)(AFD_HEADER_FIXED_WORDS + c->num_experts) * 4, a);
   L->route_table = off;
-  off += round_up((int64_t)c->token_cap * c->topk * 4, a);
+  off += round_up(table * 4, a);
   L->routed_x = off;
-  off += round_up((int64_t)c->token_cap * row, a);
+  off += round_up(rows * row, a);
   L->shared_idx = off;
   if (has_shared) off += round_up((int64_t)c->token_cap * 4, a);
   L->shared_x = off;
@@ -129,11 +141,15 @@ int validate_config(const afd_config* c) {
   if (!c) return AFD_ERR_ARG;
   if (c->num_peers < 1 || c->num_peers > AFD_MAX_PEERS || c->ring_depth < 1 || c->ring_depth > AFD_MAX_RING ||
       c->token_cap < 1 || c->max_total_tokens < 0 || c->hidden < 8 || c->num_experts < 1 ||
-      c->topk < 1 || c->topk > c->num_experts || c->inter < 1 || c->shared_inter < 0 ||
+      c->topk < 1 || (c->ffn_size < 1 && c->topk > c->num_experts) || c->inter < 1 ||
+      c->shared_inter < 0 ||
       c->max_layers < 1 || c->routed_cap_multiplier < 1.0f || c->wait_timeout_ns < 0)
     return AFD_ERR_ARG;
   if (c->act_dtype != AFD_DTYPE_F32 && c->act_dtype != AFD_DTYPE_BF16) return AFD_ERR_ARG;
   if (c->flags & ~AFD_CFG_NO_PDL) return AFD_ERR_ARG;
+  if (c->ffn_size < 0 || c->ffn_size > AFD_MAX_FFN_RANKS || c->ffn_rank < 0 ||
+      c->ffn_rank >= std::max(1, c->ffn_size))
+    return AFD_ERR_ARG;
   if (c->gemm != AFD_GEMM_TENSOR && c->gemm != AFD_GEMM_SIMT && c->gemm != AFD_GEMM_TENSOR_1CTA)
     return AFD_ERR_ARG;
   const bool tensor = c->gemm != AFD_GEMM_SIMT;
@@ -424,7 +440,9 @@ int afd_set_layer(afd_ctx* ctx, int layer, const float* Wg, const float* bias, c
   if (!ctx || layer < 0 || layer >= ctx->cfg.max_layers) return AFD_ERR_ARG;
   const afd_config& c = ctx->cfg;
   const bool has_shared = c.shared_inter > 0;
-  if (!Wg || !W13 || !Wd || (has_shared && (!W13_s || !Wd_s))) return AFD_ERR_ARG;
+  // an FFN rank under token-level dispatch never routes: no router weight needed
+  if ((!Wg && c.ffn_size < 1) || !W13 || !Wd || (has_shared && (!W13_s || !Wd_s)))
+    return AFD_ERR_ARG;
   const void* ptrs[6] = {Wg, bias, W13, Wd, has_shared ? W13_s : nullptr, has_shared ? Wd_s : nullptr};
   for (const void* p : ptrs) {
     if (!p) continue;
@@ -433,13 +451,16 @@ int afd_set_layer(afd_ctx* ctx, int layer, const float* Wg, const float* bias, c
     if (!aligned16(p)) return AFD_ERR_ARG;
   }
   LayerW& L = ctx->layers[layer];
-  if (!L.WgQ) {
-    int rc = cuda_fail(cudaMalloc(&L.WgQ, (size_t)wgq_groups(c.num_experts) * c.hidden * 16),
-                       "router copy");
+  int rc = AFD_OK;
+  if (Wg) {
+    if (!L.WgQ) {
+      rc = cuda_fail(cudaMalloc(&L.WgQ, (size_t)wgq_groups(c.num_experts) * c.hidden * 16),
+                     "router copy");
+      if (rc) return rc;
+    }
+    rc = cuda_fail(launch_arrange_wg(ctx->lc(), Wg, L.WgQ, c.hidden, c.num_experts), "router copy");
     if (rc) return rc;
   }
-  int rc = cuda_fail(launch_arrange_wg(ctx->lc(), Wg, L.WgQ, c.hidden, c.num_experts), "router copy");
-  if (rc) return rc;
   L.Wg = Wg;
   L.bias = bias;
   L.W13 = W13;
@@ -485,6 +506,7 @@ static int pack_common(afd_ctx* ctx, int peer, int stage, int layer, const void*
                        int with_shared, uint64_t seq, int shutdown) {
   if (!ctx) return AFD_ERR_ARG;
   const afd_config& c = ctx->cfg;
+  if (c.ffn_size >= 1 && !shutdown) return AFD_ERR_ARG;  // ranks receive afd_attn_dispatch
   if (peer < 0 || peer >= c.num_peers || stage < 0 || stage >= c.ring_depth || n < 0)
     return AFD_ERR_ARG;
   if (with_shared && c.shared_inter <= 0) return AFD_ERR_ARG;
@@ -520,7 +542,10 @@ int afd_pack_grouped(afd_ctx* ctx, int peer, int stage, int layer, const void* r
       n_rows < 0)
     return AFD_ERR_ARG;
   if (with_shared && c.shared_inter <= 0) return AFD_ERR_ARG;
-  if (n_tokens > c.token_cap || n_rows > c.token_cap) return AFD_ERR_CAPACITY;
+  // with several ranks a peer's shared rows are its round-robin share:
+  // afd_attn_dispatch sends those
+  if (with_shared && c.ffn_size > 1) return AFD_ERR_ARG;
+  if (n_tokens > c.token_cap || n_rows > routed_cap_of(&c)) return AFD_ERR_CAPACITY;
   GroupList gl;
   memset(&gl, 0, sizeof gl);
   int64_t sum = 0;
@@ -560,6 +585,20 @@ int afd_announce_shutdown(afd_ctx* ctx, int peer, int stage, uint64_t seq) {
   return pack_common(ctx, peer, stage, 0, nullptr, 0, 0, seq, 1);
 }
 
+// Shared rows of each list entry: its tokens with one FFN rank, its
+// round-robin share (tokens ffn_rank, ffn_rank + ffn_size, ...) with several
+static void set_shared_rows(FanIn& f, const afd_config& c) {
+  f.ffn_size = std::max(1, c.ffn_size);
+  f.ffn_rank = c.ffn_size >= 1 ? c.ffn_rank : 0;
+  int run = 0;
+  for (int i = 0; i < f.n_peers; i++) {
+    f.sprefix[i] = run;
+    run += rr_rows(f.prefix[i + 1] - f.prefix[i], f.ffn_rank, f.ffn_size);
+  }
+  f.sprefix[f.n_peers] = run;
+  f.stotal = run;
+}
+
 // Arguments of a forward: the list entries (slots, each once and in range),
 // their token counts (<= token_cap each, total <= the context's capacity)
 static int fanin_of(afd_ctx* ctx, int stage, const int* seq_lens, const int* slots, int n_peers,
@@ -585,6 +624,7 @@ static int fanin_of(afd_ctx* ctx, int stage, const int* seq_lens, const int* slo
   if (T > ctx->tmax) return AFD_ERR_CAPACITY;
   f.prefix[n_peers] = (int)T;
   f.total = (int)T;
+  set_shared_rows(f, c);
   return AFD_OK;
 }
 
@@ -592,6 +632,7 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev);
 
 int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, const int* slots,
                     int n_peers) {
+  if (ctx && ctx->cfg.ffn_size >= 1) return AFD_ERR_ARG;  // a rank receives grouped rows
   FanIn f;
   const int rc = fanin_of(ctx, stage, seq_lens, slots, n_peers, f);
   if (rc) return rc;
@@ -605,9 +646,10 @@ int afd_ffn_forward_grouped(afd_ctx* ctx, int layer, int stage, const int* n_row
   if (rc) return rc;
   if (!n_rows) return AFD_ERR_ARG;
   int64_t R = 0;
+  const int64_t rows_cap = routed_cap_of(&ctx->cfg);
   for (int i = 0; i < n_peers; i++) {
     if (n_rows[i] < 0) return AFD_ERR_ARG;
-    if (n_rows[i] > ctx->cfg.token_cap) return AFD_ERR_CAPACITY;
+    if (n_rows[i] > rows_cap) return AFD_ERR_CAPACITY;
     f.rprefix[i] = (int)R;
     R += n_rows[i];
   }
@@ -625,6 +667,7 @@ static int serve_shape(afd_ctx* ctx, const int* slots, int n_peers, int form, Pe
                        FanIn& fs) {
   if (!ctx || !slots || (form != AFD_FORM_TOKENS && form != AFD_FORM_GROUPED)) return AFD_ERR_ARG;
   const afd_config& c = ctx->cfg;
+  if (form == AFD_FORM_TOKENS && c.ffn_size >= 1) return AFD_ERR_ARG;
   if (n_peers <= 0 || n_peers > c.num_peers) return AFD_ERR_ARG;
   memset(&pl, 0, sizeof pl);
   memset(&fs, 0, sizeof fs);
@@ -638,6 +681,8 @@ static int serve_shape(afd_ctx* ctx, const int* slots, int n_peers, int form, Pe
   }
   fs.n_peers = n_peers;
   fs.dev = 1;  // the kernels take the step's values from ws.item
+  fs.ffn_size = std::max(1, c.ffn_size);
+  fs.ffn_rank = c.ffn_size >= 1 ? c.ffn_rank : 0;
   const int64_t cap = (int64_t)n_peers * c.token_cap;
   fs.total = (int)std::min<int64_t>(ctx->tmax, cap);
   fs.prefix[n_peers] = fs.total;
@@ -803,11 +848,13 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
     if (!dev) ctx->mark(i);
   };
   mark(0);
+  const int rows_cap = (int)routed_cap_of(&c);
   rc = cuda_fail(dev ? launch_item_head(lc, ctx->geom, ctx->win[0], *dev, ws, c.num_experts,
-                                        c.token_cap, has_shared, grouped, ctx->tmax,
-                                        ctx->tmax * c.topk, c.max_layers, ctx->timeout())
+                                        c.token_cap, rows_cap, f.ffn_rank, f.ffn_size, has_shared,
+                                        grouped, ctx->tmax, ctx->tmax * c.topk, c.max_layers,
+                                        ctx->timeout())
                      : launch_header_check(lc, ctx->geom, ctx->win[0], f, ws, c.num_experts,
-                                           c.token_cap, has_shared, ctx->timeout()),
+                                           c.token_cap, rows_cap, has_shared, ctx->timeout()),
                  "header check");
   if (rc) return rc;
   mark(1);
@@ -1015,7 +1062,7 @@ int afd_unpack_grouped(afd_ctx* ctx, int peer, int stage, void* y_out, int n_row
   if (peer < 0 || peer >= c.num_peers || stage < 0 || stage >= c.ring_depth || n_rows < 0 ||
       n_tokens < 0)
     return AFD_ERR_ARG;
-  if (n_rows > c.token_cap || n_tokens > c.token_cap) return AFD_ERR_CAPACITY;
+  if (n_rows > routed_cap_of(&c) || n_tokens > c.token_cap) return AFD_ERR_CAPACITY;
   for (const void* p : {y_out, s_out}) {
     if (!p) continue;
     const int rc = check_dev_ptr(p);
@@ -1024,12 +1071,14 @@ int afd_unpack_grouped(afd_ctx* ctx, int peer, int stage, void* y_out, int n_row
   }
   if ((n_rows && !y_out) || (s_out && c.shared_inter <= 0)) return AFD_ERR_ARG;
   const int row_bytes = c.hidden * (ctx->act_f32 ? 4 : 2);
+  // the peer's shared rows at this rank: all its tokens, or its round-robin share
+  const int n_shared = rr_rows(n_tokens, c.ffn_size >= 1 ? c.ffn_rank : 0, std::max(1, c.ffn_size));
   int rc = cuda_fail(launch_unpack(ctx->lc(), ctx->geom, ctx->win[1], peer, stage, y_out, n_rows,
                                    row_bytes, c.num_experts, expect_seq, ctx->ws.status,
                                    ctx->timeout(), ctx->geom.routed_x, n_tokens, n_rows),
                      "unpack");
   if (!rc && s_out)
-    rc = cuda_fail(launch_unpack(ctx->lc(), ctx->geom, ctx->win[1], peer, stage, s_out, n_tokens,
+    rc = cuda_fail(launch_unpack(ctx->lc(), ctx->geom, ctx->win[1], peer, stage, s_out, n_shared,
                                  row_bytes, c.num_experts, expect_seq, ctx->ws.status,
                                  ctx->timeout(), ctx->geom.shared_x, n_tokens, n_rows),
                    "unpack");
@@ -1044,6 +1093,12 @@ int afd_poll_status(afd_ctx* ctx) {
     return AFD_ERR_CUDA;
   if (st && cuda_fail(cudaMemset(ctx->ws.status, 0, 4), "status clear")) return AFD_ERR_CUDA;
   return st;
+}
+
+int afd_get_config(afd_ctx* ctx, afd_config* out) {
+  if (!ctx || !out) return AFD_ERR_ARG;
+  *out = ctx->cfg;
+  return AFD_OK;
 }
 
 int afd_get_window(afd_ctx* ctx, int direction, void** dev_ptr, int64_t* bytes) {

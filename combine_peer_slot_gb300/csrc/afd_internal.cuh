@@ -34,7 +34,18 @@ struct FanIn {
   int rtotal;
   int rprefix[AFD_MAX_PEERS + 1];
   int dev;                            // 1: the step's values are in ws.item
+  // shared rows: entry i's are rows [sprefix[i], sprefix[i + 1]) of their
+  // concatenation -- its tokens with one FFN rank, its round-robin share
+  // (tokens ffn_rank, ffn_rank + ffn_size, ...) with several
+  int ffn_rank, ffn_size;
+  int stotal;
+  int sprefix[AFD_MAX_PEERS + 1];
 };
+
+// how many of the tokens r, r + F, r + 2F, ... are below n
+__host__ __device__ inline int rr_rows(int n, int r, int F) {
+  return n > r ? (n - r + F - 1) / F : 0;
+}
 
 // the listed peers of a work-item loop (the peers of one Attention replica)
 struct PeerList {
@@ -352,17 +363,21 @@ cudaError_t launch_pack_header(const LaunchCtx& lc, const WinGeom& g, uint8_t* w
                                uint64_t seq, int shutdown, int routed_tokens, const GroupList& gl);
 // host-described step: bounded flag waits and header checks of the listed
 // entries, then f is written to ws.item
+// rows_cap: routed rows a slot may carry (token_cap, or routed_cap under
+// token-level dispatch)
 cudaError_t launch_header_check(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                                 const FanIn& f, const DevWS& ws, int num_experts,
-                                int token_cap, int has_shared_expert, int64_t timeout_ns);
+                                int token_cap, int rows_cap, int has_shared_expert,
+                                int64_t timeout_ns);
 // device-chosen step: bounded wait for any stage whose listed peers have all
 // published, the fan-in built from their headers (token form, or the grouped
 // form when grouped is set), the same checks, then ws.item.  tmax / rmax: the
 // most tokens / grouped rows a step may carry; max_layers: the layer table's size.
 cudaError_t launch_item_head(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                              const PeerList& pl, const DevWS& ws, int num_experts, int token_cap,
-                             int has_shared_expert, int grouped, int tmax, int rmax,
-                             int max_layers, int64_t timeout_ns);
+                             int rows_cap, int ffn_rank, int ffn_size, int has_shared_expert,
+                             int grouped, int tmax, int rmax, int max_layers,
+                             int64_t timeout_ns);
 // CTAs of the router for T tokens (16 tokens each); sizes the histograms
 int router_blocks(int total_tokens);
 size_t router_min_smem_bytes(int hidden, int E, int act_f32);

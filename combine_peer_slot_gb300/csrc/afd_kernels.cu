@@ -37,6 +37,17 @@ __device__ __forceinline__ int32_t window_row(const WinGeom& g, int region, int 
                    row_bytes) + r;
 }
 
+// list entry i holding shared row r of the concatenation of the entries'
+// shared rows
+__device__ __forceinline__ int entry_of_shared(const FanIn& f, int r) {
+  int lo = 0, hi = f.n_peers - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (f.sprefix[mid] <= r) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 // grouped form: list entry i holding routed row r of the concatenation
 __device__ __forceinline__ int entry_of_rows(const FanIn& f, int r) {
   int lo = 0, hi = f.n_peers - 1;
@@ -138,8 +149,8 @@ __global__ void k_pack_header(uint8_t* win, WinGeom g, int region, int stage, in
 // ---------------------------------------------------------------------------
 template <bool kFromHeaders>
 __device__ bool check_entries(const uint8_t* win, const WinGeom& g, const FanIn& f, const DevWS& ws,
-                              int E, int token_cap, int has_shared_expert, int64_t timeout_ns,
-                              int item_err) {
+                              int E, int token_cap, int rows_cap, int has_shared_expert,
+                              int64_t timeout_ns, int item_err) {
   __shared__ int err[AFD_MAX_PEERS];
   __shared__ int bad_sidx[AFD_MAX_PEERS];
   __shared__ int shared_n[AFD_MAX_PEERS];
@@ -193,7 +204,7 @@ __device__ bool check_entries(const uint8_t* win, const WinGeom& g, const FanIn&
       else if (kFromHeaders ? (h[8] < 0 || (!f.grouped && h[8] != 0))
                             : h[8] != (f.grouped ? f.rprefix[i + 1] - f.rprefix[i] : 0))
         e = AFD_ERR_SHAPE;
-      else if (h[8] > token_cap)
+      else if (h[8] > rows_cap)
         e = AFD_ERR_CAPACITY;
       if (!e && f.grouped) {
         // the group list: rows per expert, each >= 0, summing to the rows;
@@ -210,7 +221,9 @@ __device__ bool check_entries(const uint8_t* win, const WinGeom& g, const FanIn&
         }
         if (neg || sum != h[8]) e = AFD_ERR_SHAPE;
       }
-      if (!e && h[9] != 0 && (h[9] != n || !has_shared_expert))
+      // shared rows: none, or the entry's share (all n tokens with one FFN
+      // rank, tokens ffn_rank, ffn_rank + ffn_size, ... with several)
+      if (!e && h[9] != 0 && (h[9] != f.sprefix[i + 1] - f.sprefix[i] || !has_shared_expert))
         e = AFD_ERR_SHAPE;
       if (!e) shared_n[i] = h[9];
     }
@@ -218,9 +231,11 @@ __device__ bool check_entries(const uint8_t* win, const WinGeom& g, const FanIn&
     ws.cur_seq[i] = fl;
   }
   __syncthreads();
-  // shared_idx must be 0..n-1: with one FFN rank every token is a shared
-  // token (Async GPU Connector, "Data flow" step 3).  The rows of all peers
-  // form one index space, 8 independent loads in flight per thread.
+  // shared_idx must list the entry's shared tokens: row j is token
+  // ffn_rank + j * ffn_size (0..n-1 with one FFN rank: every token is a
+  // shared token; Async GPU Connector, "Data flow" step 3, arange(ffn_rank,
+  // n, ffn_size)).  The rows of all peers form one index space, 8
+  // independent loads in flight per thread.
   {
     __shared__ int sh_prefix[AFD_MAX_PEERS + 1];
     if (tid == 0) {
@@ -248,9 +263,10 @@ __device__ bool check_entries(const uint8_t* win, const WinGeom& g, const FanIn&
           }
           const int32_t* sidx = reinterpret_cast<const int32_t*>(
               slot_ptr(win, g, f.region[lo], f.stage) + g.shared_idx);
-          want[u] = r - sh_prefix[lo];
+          const int j = r - sh_prefix[lo];
+          want[u] = f.ffn_rank + j * f.ffn_size;
           who[u] = lo;
-          v[u] = sidx[want[u]];
+          v[u] = sidx[j];
         }
       }
 #pragma unroll
@@ -286,7 +302,7 @@ __device__ bool check_entries(const uint8_t* win, const WinGeom& g, const FanIn&
 // kernels after this one
 __global__ void __launch_bounds__(1024)
 k_header_check(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn f, DevWS ws, int E,
-               int token_cap, int has_shared_expert, int64_t timeout_ns) {
+               int token_cap, int rows_cap, int has_shared_expert, int64_t timeout_ns) {
   grid_dep_wait();
   grid_dep_launch();
   __shared__ int skip;
@@ -294,7 +310,7 @@ k_header_check(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn f, D
   if (tid == 0) skip = read_status(ws.status);
   __syncthreads();
   if (skip) return;
-  check_entries<false>(win, g, f, ws, E, token_cap, has_shared_expert, timeout_ns, 0);
+  check_entries<false>(win, g, f, ws, E, token_cap, rows_cap, has_shared_expert, timeout_ns, 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -312,8 +328,8 @@ k_header_check(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn f, D
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024)
 k_item_head(const uint8_t* win, WinGeom g, PeerList pl, DevWS ws, int E, int token_cap,
-            int has_shared_expert, int grouped, int tmax, int rmax, int max_layers,
-            int64_t timeout_ns) {
+            int rows_cap, int ffn_rank, int ffn_size, int has_shared_expert, int grouped, int tmax,
+            int rmax, int max_layers, int64_t timeout_ns) {
   grid_dep_wait();
   grid_dep_launch();
   __shared__ FanIn fs;
@@ -370,24 +386,31 @@ k_item_head(const uint8_t* win, WinGeom g, PeerList pl, DevWS ws, int E, int tok
     fs.layer = hl[0];
     fs.grouped = grouped;
     fs.num_experts = E;
-    int64_t T = 0, Rr = 0;
+    fs.ffn_rank = ffn_rank;
+    fs.ffn_size = ffn_size;
+    int64_t T = 0, Rr = 0, S = 0;
     for (int i = 0; i < pl.n; i++) {
       fs.region[i] = pl.slot[i];
       fs.prefix[i] = (int)T;
       fs.rprefix[i] = (int)Rr;
+      fs.sprefix[i] = (int)S;
       // out-of-range counts count as 0 here; the checks report them
-      T += (hn[i] >= 0 && hn[i] <= token_cap) ? hn[i] : 0;
-      Rr += (grouped && hr[i] >= 0 && hr[i] <= token_cap) ? hr[i] : 0;
+      const int n = (hn[i] >= 0 && hn[i] <= token_cap) ? hn[i] : 0;
+      T += n;
+      S += rr_rows(n, ffn_rank, ffn_size);
+      Rr += (grouped && hr[i] >= 0 && hr[i] <= rows_cap) ? hr[i] : 0;
     }
     fs.prefix[pl.n] = fs.total = (int)T;
     fs.rprefix[pl.n] = fs.rtotal = (int)Rr;
+    fs.sprefix[pl.n] = fs.stotal = (int)S;
     const int L = fs.layer;
     item_err = (L < 0 || L >= max_layers || !ws.layers[L].set) ? AFD_ERR_LAYER
                : (T > tmax || Rr > rmax)                        ? AFD_ERR_CAPACITY
                                                                 : 0;
   }
   __syncthreads();
-  if (!check_entries<true>(win, g, fs, ws, E, token_cap, has_shared_expert, timeout_ns, item_err))
+  if (!check_entries<true>(win, g, fs, ws, E, token_cap, rows_cap, has_shared_expert, timeout_ns,
+                           item_err))
     return;
   {
     const int32_t* src = reinterpret_cast<const int32_t*>(&fs);
@@ -1174,7 +1197,7 @@ __device__ void write_tile_tables(const FanIn& f, int k, int E, int inter, int s
     units2 += (mt2 + 1) / 2 * nt;
   }
   if (has_shared) {
-    const int rows = f.total;
+    const int rows = f.stotal;
     const int nt = (rows + bn - 1) / bn;
     const int mts = (shared_inter + 63) / 64;
     GemmGroup a{rows, N, 0, 0, 1, mts, nt, tiles1, units1};
@@ -1445,13 +1468,13 @@ k_plan_grouped(const __grid_constant__ FanIn fp, DevWS ws, int E, int inter, int
     }
   if (has_shared)
     for (int i = 0; i < f.n_peers; i++) {
-      const int rows = ws.peer_shared[i] ? f.prefix[i + 1] - f.prefix[i] : 0;
+      const int rows = ws.peer_shared[i] ? f.sprefix[i + 1] - f.sprefix[i] : 0;
       if (!rows) continue;
       const int nt = (rows + bn - 1) / bn;
       const int mts = (shared_inter + 63) / 64;
       const int wr = window_row(g, f.region[i], f.stage, g.shared_x, 0, row_bytes);
-      GemmGroup a{rows, wr, f.prefix[i], 0, 1, mts, nt, tiles1, units1};
-      GemmGroup b{rows, f.prefix[i], wr, 0, 1, mt2, nt, tiles2, units2};
+      GemmGroup a{rows, wr, f.sprefix[i], 0, 1, mts, nt, tiles1, units1};
+      GemmGroup b{rows, f.sprefix[i], wr, 0, 1, mt2, nt, tiles2, units2};
       plan1->g[ng] = a;
       plan2->g[ng] = b;
       tiles1 += mts * nt;
@@ -1533,7 +1556,7 @@ k_gather(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn fp, DevWS 
   const FanIn& f = step_item<kDev>(fp, ws.item);
   if (read_status(ws.status)) return;
   const int N = f.grouped ? f.rtotal : f.total * k;
-  const int rows = N + (has_shared ? f.total : 0);
+  const int rows = N + (has_shared ? f.stotal : 0);
   const int nvec = row_bytes / 16;
   const int warps = gridDim.x * (blockDim.x >> 5);
   for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
@@ -1559,11 +1582,16 @@ k_gather(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn fp, DevWS 
         ws.perm[pos] = r;
         ws.inv[r] = pos;
       }
-    } else {
-      const int t = r < N ? ws.perm[r] / k : r - N;
+    } else if (r < N) {
+      const int t = ws.perm[r] / k;
       i = entry_of(f, t);
       local = t - f.prefix[i];
-      field = r < N ? g.routed_x : g.shared_x;
+      field = g.routed_x;
+    } else {  // shared rows, entry after entry
+      const int t = r - N;
+      i = entry_of_shared(f, t);
+      local = t - f.sprefix[i];
+      field = g.shared_x;
     }
     const int lane = threadIdx.x & 31;
     if (r >= N && !ws.peer_shared[i]) {
@@ -1792,7 +1820,7 @@ k_scatter_grouped(uint8_t* ret, WinGeom g, const __grid_constant__ FanIn fp, Dev
   if (read_status(ws.status)) return;
   constexpr int kEl = ACT_F32 ? 4 : 2;
   const int row_bytes = hidden * kEl;
-  const int rows = f.rtotal + (has_shared ? f.total : 0);
+  const int rows = f.rtotal + (has_shared ? f.stotal : 0);
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * (blockDim.x >> 5);
   for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
@@ -1805,11 +1833,11 @@ k_scatter_grouped(uint8_t* ret, WinGeom g, const __grid_constant__ FanIn fp, Dev
       for (int v = lane; v < row_bytes / 16; v += 32) dst[v] = src[v];
     } else {
       const int t = r - f.rtotal;
-      const int i = entry_of(f, t);
+      const int i = entry_of_shared(f, t);
       if (!ws.peer_shared[i]) continue;
       const float* src = ws.s + (int64_t)t * hidden;
       uint8_t* dst = slot_ptr(ret, g, f.region[i], f.stage) + g.shared_x +
-                     (int64_t)(t - f.prefix[i]) * row_bytes;
+                     (int64_t)(t - f.sprefix[i]) * row_bytes;
       for (int c = lane * 8; c < hidden; c += 32 * 8) {
         const float4 a = *reinterpret_cast<const float4*>(src + c);
         const float4 b = *reinterpret_cast<const float4*>(src + c + 4);
@@ -1855,7 +1883,7 @@ __global__ void k_return_header(uint8_t* ret, WinGeom g, const __grid_constant__
       case 6: v = f.stage; break;
       case 7: v = n; break;
       case 8: v = f.grouped ? f.rprefix[i + 1] - f.rprefix[i] : n * k; break;
-      case 9: v = ws.peer_shared[i] ? n : 0; break;
+      case 9: v = ws.peer_shared[i] ? f.sprefix[i + 1] - f.sprefix[i] : 0; break;
       case 10: v = E; break;
       case 11: v = AFD_HEADER_FIXED_WORDS + E; break;
       default: v = ws.peer_counts[i * E + (w - AFD_HEADER_FIXED_WORDS)];
@@ -1996,8 +2024,8 @@ cudaError_t launch_pack_header(const LaunchCtx& lc, const WinGeom& g, uint8_t* w
 
 cudaError_t launch_header_check(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                                 const FanIn& f, const DevWS& ws, int num_experts, int token_cap,
-                                int has_shared_expert, int64_t timeout_ns) {
-  return launch_k(lc, k_header_check, 1, 1024, 0, win, g, f, ws, num_experts, token_cap,
+                                int rows_cap, int has_shared_expert, int64_t timeout_ns) {
+  return launch_k(lc, k_header_check, 1, 1024, 0, win, g, f, ws, num_experts, token_cap, rows_cap,
                   has_shared_expert, timeout_ns);
 }
 
@@ -2016,10 +2044,10 @@ static cudaError_t launch_logits_t(const LaunchCtx& lc, const WinGeom& g, const 
 
 // Shared memory of the weight-stationary logits kernel with 4 * epw experts
 // per CTA; the ring takes 3 buffers, or 2 when 3 do not fit.  smem = 0: it
-// does not fit at all.  (The 1024 bytes held back cover the kernels' static
+// does not fit at all.  (The 2048 bytes held back cover the kernels' static
 // shared memory, the step's fan-in included.)
 static WsGeom ws_geom(int hidden, int xs_bytes, int epw) {
-  constexpr size_t kLimit = 232448 - 1024;
+  constexpr size_t kLimit = 232448 - 2048;
   WsGeom geo{};
   geo.w_bytes = ((size_t)((kWsWarps * epw + 3) / 4) * hidden * 16 + 127) / 128 * 128;
   geo.tile_bytes = (size_t)kWsTok * hidden * xs_bytes;
@@ -2034,7 +2062,7 @@ static WsGeom ws_geom(int hidden, int xs_bytes, int epw) {
   geo.smem = 0;
   return geo;
 }
-static_assert(sizeof(FanIn) + 64 <= 1024, "static shared memory of the router kernels");
+static_assert(sizeof(FanIn) + 64 <= 2048, "static shared memory of the router kernels");
 
 template <typename XS, int EPW, bool kDev>
 static cudaError_t launch_logits_ws(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
@@ -2052,7 +2080,7 @@ static cudaError_t launch_logits_ws(const LaunchCtx& lc, const WinGeom& g, const
 }
 
 static TwGeom tw_geom(int hidden) {
-  constexpr size_t kLimit = 232448 - 1024;
+  constexpr size_t kLimit = 232448 - 2048;
   TwGeom geo{};
   geo.w_bytes = ((size_t)4 * hidden * 16 + 127) / 128 * 128;
   geo.stage_bytes = (size_t)kTwTok * hidden * 2;
@@ -2070,7 +2098,7 @@ static cudaError_t launch_logits(const LaunchCtx& lc, const WinGeom& g, const ui
     TwGeom geo = tw_geom(hidden);
     geo.stage_bytes = 0;  // no staging buffer; two record buffers
     geo.smem = geo.w_bytes + 2 * geo.xt_bytes + 16;
-    if (geo.smem <= 232448 - 1024) {
+    if (geo.smem <= 232448 - 2048) {
       cudaError_t err = cudaFuncSetAttribute(k_router_logits_tw2<kDev>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.smem);
       if (err != cudaSuccess) return err;
@@ -2239,10 +2267,12 @@ cudaError_t launch_prefetch_l2(const LaunchCtx& lc, const void* base, int64_t by
 
 cudaError_t launch_item_head(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                              const PeerList& pl, const DevWS& ws, int num_experts, int token_cap,
-                             int has_shared_expert, int grouped, int tmax, int rmax,
-                             int max_layers, int64_t timeout_ns) {
-  return launch_k(lc, k_item_head, 1, 1024, 0, win, g, pl, ws, num_experts, token_cap,
-                  has_shared_expert, grouped, tmax, rmax, max_layers, timeout_ns);
+                             int rows_cap, int ffn_rank, int ffn_size, int has_shared_expert,
+                             int grouped, int tmax, int rmax, int max_layers,
+                             int64_t timeout_ns) {
+  return launch_k(lc, k_item_head, 1, 1024, 0, win, g, pl, ws, num_experts, token_cap, rows_cap,
+                  ffn_rank, ffn_size, has_shared_expert, grouped, tmax, rmax, max_layers,
+                  timeout_ns);
 }
 
 cudaError_t launch_arrange_wg(const LaunchCtx& lc, const float* Wg, float* WgQ, int hidden,

@@ -173,3 +173,121 @@ class Runner:
             self.close()
         except Exception:
             pass
+
+
+class RankSet:
+    """Token-level dispatch on one GPU: ffn_size FFN-rank contexts, each with
+    its block of the experts (a view into the layer's expert weights, no
+    copy) and the shared expert, and one Attention-peer object per peer that
+    sends to all of them.  The Attention side's gate is the library's router
+    (afd_route_noalloc) on each peer's tokens.  Torch plumbing only."""
+
+    def __init__(self, w: W.Workload, ffn_size, ring_depth=1, gemm=A.AFD_GEMM_TENSOR, layers=None,
+                 multiplier=2.0, wait_timeout_ns=0, max_total_tokens=0, device="cuda"):
+        import torch
+        self.w, self.F, self.device = w, ffn_size, device
+        self.layers = w.layers if layers is None else layers
+        self.stream = torch.cuda.current_stream()
+        self.host = W.host_inputs(w)
+        self.x = [act_tensor(a, w.act, device) for a in self.host["x"]]
+        self.Wg = torch.from_numpy(self.host["Wg"]).to(device)
+        self.bias = None if self.host["bias"] is None else torch.from_numpy(self.host["bias"]).to(device)
+        self.weights = [W.expert_weights(w, layer, device) for layer in range(self.layers)]
+        self.ranks, self.experts, self.cfgs = [], [], []
+        for r in range(ffn_size):
+            first, cnt = A.afd_expert_range(w.num_experts, ffn_size, r)
+            cfg = A.make_config(w.num_peers, w.token_cap, w.hidden, cnt, w.topk, w.inter,
+                                w.shared_inter, act=w.act, renorm=w.renorm,
+                                routed_scaling=w.routed_scaling, ring_depth=ring_depth,
+                                max_total_tokens=max_total_tokens or w.total_tokens,
+                                max_layers=self.layers, gemm=gemm,
+                                routed_cap_multiplier=multiplier,
+                                wait_timeout_ns=wait_timeout_ns, ffn_rank=r, ffn_size=ffn_size)
+            ctx = A.afd_create(cfg, self.stream.cuda_stream)
+            for layer, wt in enumerate(self.weights):
+                W13, Wd = wt["W13"], wt["Wd"]
+                A.afd_set_layer(ctx, layer, 0, 0, W13[first].data_ptr(), Wd[first].data_ptr(),
+                                wt["W13s"].data_ptr() if wt["W13s"] is not None else 0,
+                                wt["Wds"].data_ptr() if wt["Wds"] is not None else 0)
+            self.ranks.append(ctx)
+            self.experts.append((first, cnt))
+            self.cfgs.append(cfg)
+        self.attn = [A.afd_attn_create(self.ranks, p, w.num_experts, self.stream.cuda_stream)
+                     for p in range(w.num_peers)]
+        dt = torch.bfloat16 if w.act == "bf16" else torch.float32
+        self.out = [torch.empty((max(n, 1), w.hidden), dtype=dt, device=device) for n in w.seq_lens]
+        self.ids = [torch.zeros((max(n, 1), w.topk), dtype=torch.int32, device=device)
+                    for n in w.seq_lens]
+        self.wts = [torch.zeros((max(n, 1), w.topk), dtype=torch.float32, device=device)
+                    for n in w.seq_lens]
+        self.seq = 0
+        self.last_seq = {}
+
+    def route(self):
+        """The Attention side's gate on every peer's tokens."""
+        w = self.w
+        for p, n in enumerate(w.seq_lens):
+            if not n:
+                continue
+            rc = A.afd_route_noalloc(self.x[p].data_ptr(), n, w.hidden,
+                                     A.AFD_DTYPE_BF16 if w.act == "bf16" else A.AFD_DTYPE_F32,
+                                     self.Wg.data_ptr(),
+                                     self.bias.data_ptr() if self.bias is not None else 0,
+                                     w.num_experts, w.topk, w.renorm, w.routed_scaling,
+                                     self.ids[p].data_ptr(), self.wts[p].data_ptr(),
+                                     self.stream.cuda_stream)
+            if rc:
+                raise A.AfdError(rc, "afd_route_noalloc")
+
+    def dispatch_all(self, stage=0, layer=0, with_shared=None):
+        ws = (self.w.shared_inter > 0) if with_shared is None else with_shared
+        for p, n in enumerate(self.w.seq_lens):
+            self.seq += 1
+            rc = A.afd_attn_dispatch(self.attn[p], stage, layer, self.x[p].data_ptr() if n else 0,
+                                     n, self.ids[p].data_ptr() if n else 0, ws, self.seq)
+            if rc:
+                raise A.AfdError(rc, "afd_attn_dispatch")
+            self.last_seq[(p, stage)] = self.seq
+
+    def serve_all(self, n_items=1, ranks=None):
+        slots = list(range(self.w.num_peers))
+        for r in (range(self.F) if ranks is None else ranks):
+            rc = A.afd_ffn_serve(self.ranks[r], slots, n_items, A.AFD_FORM_GROUPED)
+            if rc:
+                raise A.AfdError(rc, "afd_ffn_serve")
+
+    def combine_all(self, stage=0):
+        for p, n in enumerate(self.w.seq_lens):
+            rc = A.afd_attn_combine(self.attn[p], stage, self.wts[p].data_ptr() if n else 0,
+                                    self.out[p].data_ptr() if n else 0, n,
+                                    self.last_seq[(p, stage)])
+            if rc:
+                raise A.AfdError(rc, "afd_attn_combine")
+        return self.out
+
+    def poll(self):
+        """(first status of the ranks, of the peers)"""
+        fr = next((s for s in (A.afd_poll_status(c) for c in self.ranks) if s), 0)
+        fa = next((s for s in (A.afd_attn_poll_status(a) for a in self.attn) if s), 0)
+        return fr, fa
+
+    def window(self, r, direction):
+        ptr, n = A.afd_get_window(self.ranks[r], direction)
+        return device_view(ptr, n)
+
+    def rank_weights_numpy(self, r, layer=0):
+        first, cnt = self.experts[r]
+        d = W.weights_to_numpy(self.weights[layer])
+        d["W13"] = np.ascontiguousarray(d["W13"][first:first + cnt])
+        d["Wd"] = np.ascontiguousarray(d["Wd"][first:first + cnt])
+        d["Wg"] = None
+        d["bias"] = None
+        return d
+
+    def close(self):
+        for a in self.attn:
+            A.afd_attn_destroy(a)
+        self.attn = []
+        for c in self.ranks:
+            A.afd_destroy(c)
+        self.ranks = []

@@ -89,12 +89,25 @@ extern "C" {
  * shared_inter     shared SwiGLU intermediate, 0 = no shared expert
  * act_dtype        AFD_DTYPE_*; renorm: top-k weights renormalised to sum 1
  * routed_scaling   routed_scaling_factor applied to the gate weights
- * routed_cap_multiplier  recorded for the multi-FFN-rank dispatch (must be
- *                  >= 1); one FFN rank receives exactly T * topk partials
+ * routed_cap_multiplier  sizes the routed rows of a rank's slot under
+ *                  token-level dispatch (>= 1; see ffn_size)
  * wait_timeout_ns  bound on every device-side wait (flag polls); 0 = 1 s
  * gemm             AFD_GEMM_*; max_layers: size of the layer weight table
  * flags            AFD_CFG_* bits, 0 for the defaults
+ * ffn_rank, ffn_size  0 (default): this context routes itself (token form)
+ *                  or receives grouped rows of at most token_cap per slot.
+ *                  ffn_size >= 1: the context is FFN rank ffn_rank of
+ *                  ffn_size (<= AFD_MAX_FFN_RANKS) receiving token-level
+ *                  dispatch (Async GPU Connector, "Data flow" and "Capacity
+ *                  and ring depth"): num_experts is the rank's own expert
+ *                  count (afd_expert_range), only the grouped calls apply,
+ *                  a peer's shared rows are its tokens ffn_rank, ffn_rank +
+ *                  ffn_size, ... and a slot holds
+ *                  routed_cap = ceil(ceil(token_cap * topk / ffn_size)
+ *                  * routed_cap_multiplier) routed rows (AFD_ERR_CAPACITY
+ *                  above it, never truncation).
  */
+#define AFD_MAX_FFN_RANKS 16
 /* Launch every kernel after the previous one has fully finished, instead of
  * letting its CTAs be scheduled (and wait on the device) while the previous
  * kernel drains (programmatic dependent launch, the default). */
@@ -117,6 +130,8 @@ typedef struct afd_config {
   float routed_scaling;
   float routed_cap_multiplier;
   int64_t wait_timeout_ns;
+  int32_t ffn_rank;
+  int32_t ffn_size;
 } afd_config;
 
 /* Byte offsets of the slot fields and window sizes.  Async GPU Connector,
@@ -128,7 +143,10 @@ typedef struct afd_config {
  * window viewed as a [rows, hidden] matrix.  Sizes: header (12 + E) int32;
  * route_table [token_cap, topk] int32; routed_x and shared_x
  * [token_cap, hidden]; shared_idx [token_cap] int32; the shared fields are
- * empty without a shared expert.  Flags are uint64 sequence numbers; slot
+ * empty without a shared expert.  Under token-level dispatch (ffn_size >= 1)
+ * routed_x holds max(token_cap, routed_cap) rows and route_table
+ * max(token_cap * topk, routed_cap) int32 (the sender's partial index
+ * t * topk + j of each routed row).  Flags are uint64 sequence numbers; slot
  * (peer p, stage s) is slot number p * ring_depth + s, as is its flag. */
 typedef struct afd_layout {
   int64_t header, route_table, routed_x, shared_idx, shared_x;
@@ -207,7 +225,8 @@ int afd_split_sizes(int total, int n_peers, const int* seq_lens, int n_lens, int
 
 /* Register the weights of one layer (layer-select table, Async AFD for
  * Prefill on Ascend NPU, "Architecture": an address table for every layer).
- *   Wg   fp32 [hidden, E] row-major (router)
+ *   Wg   fp32 [hidden, E] row-major (router); NULL on an FFN rank under
+ *        token-level dispatch (ffn_size >= 1), which never routes
  *   bias fp32 [E] or NULL (added to the logits)
  *   W13  act [E, 2*inter, hidden]: rows 0..inter-1 gate, inter..2*inter-1 up
  *   Wd   act [E, hidden, inter]
@@ -313,6 +332,9 @@ int afd_ffn_forward_grouped(afd_ctx* ctx, int layer, int stage, const int* n_row
  * NULL, the n_tokens shared outputs into s_out.  Errors as afd_unpack_split. */
 int afd_unpack_grouped(afd_ctx* ctx, int peer, int stage, void* y_out, int n_rows, void* s_out,
                        int n_tokens, uint64_t expect_seq);
+/* (On an FFN rank among several, s_out receives the peer's round-robin
+ * share of shared outputs, tokens ffn_rank, ffn_rank + ffn_size, ...; n_rows
+ * may be up to routed_cap.) */
 
 /* ---- device-resident work-item loop ---------------------------------------
  * [RFC]: Async AFD for Prefill on Ascend NPU, "Asynchronous work-item
@@ -373,6 +395,77 @@ int afd_serve_log(afd_ctx* ctx, int32_t* records, int max_records, int* n_record
  * last poll (AFD_OK if none) and clear it; AFD_ERR_CUDA if the stream itself
  * failed. */
 int afd_poll_status(afd_ctx* ctx);
+
+/* The context's configuration (host copy). */
+int afd_get_config(afd_ctx* ctx, afd_config* out);
+
+/* ---- token-level dispatch to several FFN ranks ------------------------------
+ * [RFC]: Async GPU Connector, "Data flow" steps 1-4 and "Capacity and ring
+ * depth".  The experts are split over ffn_size FFN ranks, each an afd_ctx
+ * created with ffn_rank / ffn_size and num_experts = its own count; an
+ * Attention peer sends every rank the routed rows of its experts (grouped
+ * by local expert, with the group list in the header) and its round-robin
+ * share of the shared rows, and combines what the ranks return.  On one GPU
+ * every rank's window is local memory.
+ *
+ * afd_expert_range -- experts of rank ffn_rank among ffn_size for
+ * num_experts experts in all: a contiguous block, the first
+ * num_experts % ffn_size ranks one expert more (the pages fix no placement;
+ * balanced contiguous blocks are this library's reading).  AFD_ERR_ARG for
+ * ffn_size < 1, num_experts < ffn_size or a rank out of range. */
+int afd_expert_range(int num_experts, int ffn_size, int ffn_rank, int* first, int* count);
+
+/* afd_attn_create -- one Attention peer's side over the FFN ranks
+ * ranks[0..ffn_size-1] (ranks[r] must be rank r, all with the same peers,
+ * stages, token_cap, hidden, topk, activation type, shared expert and
+ * routed_cap_multiplier, and num_experts = afd_expert_range's count of
+ * num_experts in all, at most 256).  Allocates its per-stage plan buffers
+ * (2 * token_cap * topk int32 per stage).  Work is ordered on cuda_stream;
+ * it must be ordered before the ranks' steps that consume it (the same
+ * stream, or events).  Errors: AFD_ERR_ARG, AFD_ERR_CUDA. */
+typedef struct afd_attn afd_attn;
+int afd_attn_create(afd_ctx* const* ranks, int ffn_size, int peer, int num_experts,
+                    void* cuda_stream, afd_attn** out);
+void afd_attn_destroy(afd_attn* a);
+
+/* afd_attn_dispatch -- the peer's send of one stage (steps 1-3):
+ *   x          device act [n_tokens, hidden], 16-byte aligned
+ *   topk_ids   device int32 [n_tokens, topk], expert ids 0..num_experts-1
+ * On the device: a stable sort of the flattened ids (one pass gives the
+ * segments by rank and the local-expert groups within them), then every
+ * rank's slot (peer, stage) gets routed_x = the rows x[f / topk] of its
+ * segment, route_table = their partial indices f, shared rows = tokens
+ * ffn_rank, ffn_rank + ffn_size, ... (shared_idx = those indices) when
+ * with_shared, the header (num_tokens, routed_tokens, shared_tokens,
+ * num_experts = the rank's count, expert_counts = its group list) and the
+ * flag = seq.  Every rank gets its message, empty ones included.  A segment
+ * over routed_cap is a device error AFD_ERR_CAPACITY (nothing is written to
+ * any rank); an id out of range AFD_ERR_ARG (afd_attn_poll_status).  Host
+ * errors: AFD_ERR_ARG, AFD_ERR_CAPACITY (n_tokens > token_cap),
+ * AFD_ERR_NOT_DEVICE. */
+int afd_attn_dispatch(afd_attn* a, int stage, int layer, const void* x, int n_tokens,
+                      const int32_t* topk_ids, int with_shared, uint64_t seq);
+
+/* afd_attn_combine -- the peer's receive of that stage (step 4): a bounded
+ * wait for the return flag == expect_seq of every rank that got rows (an
+ * empty message creates no wait), header checks (magic, version, echoed
+ * seq, num_tokens, routed and shared rows as sent), then out[t] = sum over
+ * j ascending of topk_weights[t, j] * (rank output of partial t * topk + j)
+ * + (shared output of token t, from rank t mod ffn_size), in fp32, rounded
+ * once to the activation type.
+ *   topk_weights  device fp32 [n_tokens, topk]   out  device act [n_tokens, hidden]
+ * n_tokens must be that of the stage's last dispatch (else AFD_ERR_SHAPE).
+ * Device errors: AFD_ERR_TIMEOUT, AFD_ERR_SEQ, AFD_ERR_HEADER, AFD_ERR_SHAPE. */
+int afd_attn_combine(afd_attn* a, int stage, const float* topk_weights, void* out, int n_tokens,
+                     uint64_t expect_seq);
+
+/* Synchronise the peer's stream and copy out the routed rows its last
+ * dispatch of the stage sent to each rank (host int [ffn_size]). */
+int afd_attn_rows(afd_attn* a, int stage, int* rows);
+/* Synchronise the peer's stream; return and clear its first device error. */
+int afd_attn_poll_status(afd_attn* a);
+/* Kernel launches issued by this peer's calls. */
+int64_t afd_attn_launch_count(afd_attn* a);
 
 /* Device base pointer and size of a window (AFD_DIR_*). */
 int afd_get_window(afd_ctx* ctx, int direction, void** dev_ptr, int64_t* bytes);

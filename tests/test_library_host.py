@@ -116,3 +116,51 @@ def test_serve_rejects_bad_arguments_without_a_context(lib):
     A.afd_serve_graph_destroy(None)
     with pytest.raises(A.AfdError):
         A.afd_serve_log(None)
+
+
+def test_rank_layout_and_experts_match_oracle(lib):
+    """An FFN rank's slot layout under token-level dispatch (routed fields
+    sized by routed_cap) and the expert placement, against the oracle."""
+    rng = np.random.default_rng(5)
+    for _ in range(200):
+        F = int(rng.integers(1, A.AFD_MAX_FFN_RANKS + 1))
+        E = int(rng.integers(F, 257))
+        r = int(rng.integers(0, F))
+        first, cnt = A.afd_expert_range(E, F, r)
+        assert (first, cnt) == O.expert_range(E, F, r)
+        cap, k = int(rng.integers(1, 5000)), int(rng.integers(1, 17))
+        H = int(rng.integers(1, 129)) * 8
+        mult = float(rng.choice([1.0, 1.5, 2.0, 3.0]))
+        act = str(rng.choice(["bf16", "f32"]))
+        Is = int(rng.choice([0, 64]))
+        cfg = A.make_config(int(rng.integers(1, 9)), cap, H, cnt, min(k, cnt), 64,
+                            shared_inter=Is, act=act, ring_depth=int(rng.integers(1, 4)),
+                            gemm=A.AFD_GEMM_SIMT, routed_cap_multiplier=mult, ffn_rank=r,
+                            ffn_size=F)
+        ours = A.afd_slot_layout(cfg).as_dict()
+        rcap = O.routed_cap(cap, min(k, cnt), F, mult)
+        ref = O.slot_layout_ranks(cfg.num_peers, cfg.ring_depth, cap, min(k, cnt), H,
+                                  2 if act == "bf16" else 4, cnt, Is > 0, rcap).as_dict()
+        assert ours == ref
+    assert lib.afd_expert_range(4, 5, 0, None, None) == A.AFD_ERR_ARG
+
+
+def test_rank_config_validation(lib):
+    base = dict(num_peers=2, token_cap=64, hidden=256, num_experts=8, topk=2, inter=64)
+    for bad in (dict(ffn_size=A.AFD_MAX_FFN_RANKS + 1), dict(ffn_size=2, ffn_rank=2),
+                dict(ffn_size=-1), dict(ffn_size=0, ffn_rank=1)):
+        cfg = A.make_config(**{**base, **bad})
+        with pytest.raises(A.AfdError) as e:
+            A.afd_slot_layout(cfg)
+        assert e.value.code == A.AFD_ERR_ARG, bad
+    assert A.afd_slot_layout(A.make_config(**base, ffn_size=4, ffn_rank=3)).window_bytes > 0
+
+
+def test_attn_rejects_bad_arguments_without_a_context(lib):
+    import ctypes as C
+    a = C.c_void_p()
+    assert lib.afd_attn_create(None, 2, 0, 16, None, C.byref(a)) == A.AFD_ERR_ARG
+    assert A.afd_attn_dispatch(None, 0, 0, 0, 0, 0, False, 1) == A.AFD_ERR_ARG
+    assert A.afd_attn_combine(None, 0, 0, 0, 0, 1) == A.AFD_ERR_ARG
+    assert A.afd_attn_poll_status(None) == A.AFD_ERR_ARG
+    A.afd_attn_destroy(None)

@@ -522,6 +522,106 @@ def run_serve(args, ws, rank, local):
     run.close()
 
 
+def run_ranks(args, ws, rank, local):
+    """Token-level dispatch to --ffn-ranks FFN ranks on this one GPU: per
+    step, every peer's send (afd_attn_dispatch), every rank's grouped step
+    over the peers (the work-item loop, counts taken on the device), every
+    peer's combine (afd_attn_combine), each part between its own event pair
+    on the one stream, after an L2 flush.  The ranks run one after another
+    here; on ffn_size GPUs they would run side by side (rank_ms lists each)."""
+    import numpy as np
+    import torch
+    from combine_peer_slot_gb300 import afd as A
+    from combine_peer_slot_gb300 import runtime as R
+
+    w = workload_of(args)
+    T, F = w.total_tokens, args.ffn_ranks
+    rs = R.RankSet(w, F, layers=1)
+    stream = rs.stream
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(F + 3)]
+    slots = list(range(w.num_peers))
+
+    def step():
+        rs.route()                  # the Attention side's gate: not timed
+        flush.zero_()
+        ev[0].record(stream)
+        rs.dispatch_all()
+        ev[1].record(stream)
+        for r in range(F):
+            rc = A.afd_ffn_serve(rs.ranks[r], slots, 1, A.AFD_FORM_GROUPED)
+            if rc:
+                raise A.AfdError(rc, "afd_ffn_serve")
+            ev[2 + r].record(stream)
+        rs.combine_all()
+        ev[F + 2].record(stream)
+        torch.cuda.synchronize()
+        return [ev[i].elapsed_time(ev[i + 1]) for i in range(F + 2)]
+
+    for _ in range(args.warmup):
+        step()
+    if rs.poll() != (0, 0):
+        raise RuntimeError("device error during warm-up")
+    dev_index = getattr(torch.cuda.get_device_properties(local), "pci_bus_id", None) or local
+    acc = np.zeros(F + 2)
+    l0 = sum(A.afd_launch_count(c) for c in rs.ranks) + sum(A.afd_attn_launch_count(a) for a in rs.attn)
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(dev_index) as clk:
+        for _ in range(args.steps):
+            acc += np.array(step())
+    barrier(ws)
+    launches = (sum(A.afd_launch_count(c) for c in rs.ranks) +
+                sum(A.afd_attn_launch_count(a) for a in rs.attn) - l0)
+    st = rs.poll()
+    if st != (0, 0):
+        raise RuntimeError(f"device error in the timed region: {st}")
+    per = acc / args.steps
+    dispatch_ms, rank_ms, combine_ms = per[0], list(per[1:F + 1]), per[F + 1]
+    ms_step = max_over_ranks(float(per.sum()), ws)
+    value = sum_over_ranks(T, ws) / (ms_step / 1e3)
+    rows = [[int(v) for v in A.afd_attn_rows(a, 0, F)] for a in rs.attn]
+    rows_per_rank = [sum(r[q] for r in rows) for q in range(F)]
+    pk, pk_kind = peaks()
+    eb = w.act_bytes
+    # algorithmic bytes: the send reads every token row once and writes the
+    # T*k routed rows and the T shared rows; the combine reads those rows
+    # back and writes the T outputs
+    moved = (T * w.topk + T) * w.hidden * eb
+    send_bytes = T * w.hidden * eb + moved
+    recv_bytes = moved + T * w.hidden * eb
+    def hbm(nbytes, ms):
+        a = nbytes / (ms / 1e3) / 1e9
+        return {"bound": "hbm", "achieved": a, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": a / pk["hbm_gbs"], "peak_source": f"{pk_kind} hbm_gbs",
+                "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": ms, "traffic": None}
+    flops_rank = [6 * w.hidden * (rows_per_rank[q] * w.inter +
+                                  sum(len(range(q, n, F)) for n in w.seq_lens) * w.shared_inter)
+                  for q in range(F)]
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; no model weights or dataset)",
+        "config": {"workload": f"{args.workload}_ranks{F}", "ffn_size": F, "peers": w.num_peers,
+                   "seq_lens": w.seq_lens, "total_tokens": T, "experts": w.num_experts,
+                   "topk": w.topk, "routed_cap_multiplier": 2.0,
+                   "parallelism": f"replicas{ws}; {F} FFN ranks served one after another",
+                   "l2": "flushed (256 MB write) before every timed send",
+                   "gate": "the library's router on each peer's tokens, before the timed region"},
+        "dispatch_ms": dispatch_ms, "rank_ms": rank_ms, "combine_ms": combine_ms,
+        "rows_per_rank": rows_per_rank,
+        "rank_tflops": [flops_rank[q] / (rank_ms[q] / 1e3) / 1e12 for q in range(F)],
+        "roofline": hbm(send_bytes, dispatch_ms), "combine_roofline": hbm(recv_bytes, combine_ms),
+        "gpu_launches": launches, "clocks": clk.summary(), "e2e": None, "cpu_baseline": None,
+    }
+    out["roofline"]["kernel"] = "attn_dispatch"
+    out["combine_roofline"]["kernel"] = "attn_combine"
+    if rank == 0:
+        print(json.dumps(out))
+    rs.close()
+
+
 # ---------------------------------------------------------------------------
 # the CPU oracle (baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
@@ -639,6 +739,9 @@ def main():
                     help="grouped: the Attention side routes and sends rows grouped by expert")
     ap.add_argument("--layers", type=int, default=0,
                     help="number of layers replacing the workload's (smaller profiling cases)")
+    ap.add_argument("--ffn-ranks", type=int, default=0,
+                    help="token-level dispatch to this many FFN ranks on this GPU: the peers' "
+                         "send, every rank's grouped step, the peers' combine")
     ap.add_argument("--serve", choices=["host", "eager", "graph"], default=None,
                     help="measure the device-resident work-item loop: all layers' items "
                          "packed into stages, served by host-described steps, the loop's "
@@ -649,6 +752,8 @@ def main():
     ws, rank, local = dist_init(args.gpus)
     if args.impl == "reference":
         run_reference(args, ws, rank)
+    elif args.ffn_ranks:
+        run_ranks(args, ws, rank, local)
     elif args.serve:
         run_serve(args, ws, rank, local)
     else:

@@ -6,8 +6,8 @@
 //            of every routed row and every round-robin shared row into the
 //            destination ranks' dispatch slots, then each rank's header and
 //            flag (every rank gets its message, empty ones included);
-//   recv  -- a bounded wait on the ranks that received rows (an empty message
-//            never creates a wait), then the weighted combine of the routed
+//   recv  -- a bounded wait on the ranks that received rows (a rank sent
+//            nothing is not waited for), then the weighted combine of the routed
 //            outputs they returned plus the shared outputs, straight from
 //            their return slots.
 // The gate weights never leave the peer: the combine takes them from the

@@ -447,8 +447,8 @@ int afd_attn_dispatch(afd_attn* a, int stage, int layer, const void* x, int n_to
                       const int32_t* topk_ids, int with_shared, uint64_t seq);
 
 /* afd_attn_combine -- the peer's receive of that stage (step 4): a bounded
- * wait for the return flag == expect_seq of every rank that got rows (an
- * empty message creates no wait), header checks (magic, version, echoed
+ * wait for the return flag == expect_seq of every rank that got rows (a
+ * rank sent no rows is not waited for), header checks (magic, version, echoed
  * seq, num_tokens, routed and shared rows as sent), then out[t] = sum over
  * j ascending of topk_weights[t, j] * (rank output of partial t * topk + j)
  * + (shared output of token t, from rank t mod ffn_size), in fp32, rounded

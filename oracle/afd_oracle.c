@@ -1147,7 +1147,7 @@ int orc_dispatch_ranks(uint8_t** wins, const orc_layout* Ls, int F, int ring_dep
 
 /* The Attention side's receive of a multi-rank step ([RFC-GPU] "Data flow":
  * recv_ffn_output waits only on the ranks that received data at dispatch --
- * an empty message never creates a wait -- and accumulates each arrival in
+ * a rank that was sent no rows is not waited for -- and accumulates each arrival in
  * fp32 with the weighted scatter; the shared branch is added by shared_idx).
  * For every rank r with rows_out[r] routed rows or shared rows: its return
  * flag must equal expect_seq and its header echo it, with routed_tokens =
@@ -1163,7 +1163,7 @@ int orc_attn_combine(uint8_t** rets, const orc_layout* Ls, int F, int ring_depth
                      uint64_t expect_seq, double* out64, void* out_act) {
   for (int r = 0; r < F; r++) {
     const int ns = with_shared ? orc_rr_rows(n, r, F) : 0;
-    if (rows_out[r] == 0 && ns == 0) continue;  /* an empty message: no wait */
+    if (rows_out[r] == 0 && ns == 0) continue;  /* nothing sent there: no wait */
     uint64_t fl = *orc_flag(rets[r], region, stage, ring_depth);
     if (fl < expect_seq) return ORC_ERR_TIMEOUT;
     if (fl > expect_seq) return ORC_ERR_SEQ;

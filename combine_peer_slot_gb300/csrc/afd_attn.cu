@@ -24,7 +24,6 @@
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kPlanThreads = 1024;
 
 struct AttnDst {        // one destination FFN rank
   uint8_t* win;         // its dispatch window
@@ -45,6 +44,7 @@ struct AttnPlan {
   int32_t* pos;     // [token_cap * k] its row in the rank's segment
   int32_t* rows;    // [F] segment lengths
   int32_t* counts;  // [E] partials per (global) expert
+  int32_t* seg;     // [F] first position of each rank's segment in the sorted order
 };
 
 __device__ __forceinline__ uint8_t* slot_of(uint8_t* win, const WinGeom& g, int region, int stage) {
@@ -56,93 +56,152 @@ __device__ __forceinline__ const uint8_t* slot_of(const uint8_t* win, const WinG
 }
 
 // ---------------------------------------------------------------------------
-// send, step 1 (one CTA): bincount of the flattened ids, exclusive offsets
-// (global expert order = destination order, then local expert order), the
-// stable rank of every partial among the earlier partials of its expert
-// (warp w owns a contiguous chunk of the partials; per-warp histograms give
-// its cursors; 32-element rounds ranked with match_any), each rank's
-// segment length.  A segment over routed_cap raises AFD_ERR_CAPACITY, an id
-// outside 0..E-1 AFD_ERR_ARG; the later kernels then write nothing.
+// send, step 1: one stable sort of the flattened ids, in three kernels over
+// blocks of 16 tokens (16 * k consecutive partials).  k_attn_hist: a warp
+// per block counts its partials per expert (hist[b][e]) and checks the ids.
+// k_attn_scan (one CTA): per-expert totals and exclusive offsets (global
+// expert order = destination order, then local expert order), each block's
+// first position within each expert's run (base[b][e]), each rank's segment
+// length; a segment over routed_cap raises AFD_ERR_CAPACITY, an id outside
+// 0..E-1 AFD_ERR_ARG, and the later kernels write nothing.  k_attn_rank: a
+// warp per block ranks its partials among the earlier ones of their expert
+// (match_any over 32-element rounds, cursors from base) and records each
+// partial's rank and row within that rank's segment.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kPlanThreads)
-k_attn_plan(const int32_t* __restrict__ ids, int n, int k, int E, AttnDsts ds, AttnPlan pl,
-            int64_t routed_cap, int32_t* status) {
+constexpr int kBlkTok = 16;
+constexpr int kPlanWarps = 8;
+
+__global__ void __launch_bounds__(kPlanWarps * 32)
+k_attn_hist(const int32_t* __restrict__ ids, int n, int k, int E, int32_t* __restrict__ hist,
+            int32_t* status) {
   grid_dep_wait();
   grid_dep_launch();
-  __shared__ int hist_w[32][256];
-  __shared__ int cnt[256];
-  __shared__ int offs[257];
-  __shared__ int rank_of[256];
-  __shared__ int bad;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  for (int i = tid; i < 32 * 256; i += blockDim.x) (&hist_w[0][0])[i] = 0;
-  if (tid == 0) bad = read_status(status);
-  for (int r = 0; r < ds.F; r++)
-    for (int e = ds.d[r].first + tid; e < ds.d[r].first + ds.d[r].count; e += blockDim.x)
-      rank_of[e] = r;
-  __syncthreads();
-  if (bad) return;
-  const int N = n * k;
-  const int chunk = (N + 31) / 32;
-  const int c0 = min(N, warp * chunk), c1 = min(N, c0 + chunk);
-  for (int fi = c0 + lane; fi < c1; fi += 32) {
+  __shared__ int hw[kPlanWarps][256];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.x * kPlanWarps + warp;
+  const int nb = (n + kBlkTok - 1) / kBlkTok;
+  for (int e = lane; e < E; e += 32) hw[warp][e] = 0;
+  __syncwarp();
+  if (b >= nb || read_status(status)) return;
+  const int f0 = b * kBlkTok * k, f1 = min(n * k, f0 + kBlkTok * k);
+  bool bad = false;
+  for (int fi = f0 + lane; fi < f1; fi += 32) {
     const int e = ids[fi];
     if (e < 0 || e >= E) {
-      bad = 1;
+      bad = true;
       continue;
     }
-    atomicAdd(&hist_w[warp][e], 1);
+    atomicAdd(&hw[warp][e], 1);
   }
+  if (bad) set_error(status, AFD_ERR_ARG);
+  __syncwarp();
+  for (int e = lane; e < E; e += 32) hist[(int64_t)b * E + e] = hw[warp][e];
+}
+
+constexpr int kScanSegs = 16;  // 16 segments of blocks x 64 experts per pass of 1024 threads
+
+__global__ void __launch_bounds__(1024)
+k_attn_scan(int n, int E, AttnDsts ds, AttnPlan pl, const int32_t* __restrict__ hist,
+            int32_t* __restrict__ base, int64_t routed_cap, int32_t* status) {
+  grid_dep_wait();
+  grid_dep_launch();
+  __shared__ int cnt[256];
+  __shared__ int offs[257];
+  __shared__ int seg_sum[kScanSegs][64];
+  __shared__ int skip;
+  const int tid = threadIdx.x;
+  if (tid == 0) skip = read_status(status);
   __syncthreads();
-  if (bad) {
-    if (tid == 0) set_error(status, AFD_ERR_ARG);
-    return;
+  if (skip) return;
+  const int nb = (n + kBlkTok - 1) / kBlkTok;
+  const int sg = tid / 64, el = tid % 64;
+  const int L = (nb + kScanSegs - 1) / kScanSegs;
+  const int b_lo = min(nb, sg * L), b_hi = min(nb, b_lo + L);
+  for (int e0 = 0; e0 < E; e0 += 64) {
+    const int e = e0 + el;
+    int sum = 0;
+    if (e < E)
+      for (int b = b_lo; b < b_hi; b++) sum += hist[(int64_t)b * E + e];
+    seg_sum[sg][el] = sum;
+    __syncthreads();
+    if (sg == 0 && e < E) {
+      int tot = 0;
+      for (int q = 0; q < kScanSegs; q++) tot += seg_sum[q][el];
+      cnt[e] = tot;
+    }
+    __syncthreads();
   }
-  for (int e = tid; e < E; e += blockDim.x) {
-    int c = 0;
-    for (int w = 0; w < 32; w++) c += hist_w[w][e];
-    cnt[e] = c;
-  }
-  __syncthreads();
   if (tid == 0) {
     int run = 0;
     for (int e = 0; e < E; e++) { offs[e] = run; run += cnt[e]; }
     offs[E] = run;
+    int over = 0;
     for (int r = 0; r < ds.F; r++) {
       const int R = offs[ds.d[r].first + ds.d[r].count] - offs[ds.d[r].first];
       pl.rows[r] = R;
-      if (R > routed_cap) bad = 1;
+      pl.seg[r] = offs[ds.d[r].first];
+      over |= R > routed_cap;
     }
-    if (bad) set_error(status, AFD_ERR_CAPACITY);
+    if (over) set_error(status, AFD_ERR_CAPACITY);
   }
   __syncthreads();
-  if (bad) return;
-  for (int e = tid; e < E; e += blockDim.x) {
-    pl.counts[e] = cnt[e];
-    int base = offs[e];
-    for (int w = 0; w < 32; w++) {
-      const int c = hist_w[w][e];
-      hist_w[w][e] = base;  // warp w's cursor for expert e
-      base += c;
+  for (int e = tid; e < E; e += blockDim.x) pl.counts[e] = cnt[e];
+  // each block's first position within each expert's run
+  for (int e0 = 0; e0 < E; e0 += 64) {
+    const int e = e0 + el;
+    int sum = 0;
+    if (e < E)
+      for (int b = b_lo; b < b_hi; b++) sum += hist[(int64_t)b * E + e];
+    seg_sum[sg][el] = sum;
+    __syncthreads();
+    if (e < E) {
+      int run = offs[e];
+      for (int q = 0; q < sg; q++) run += seg_sum[q][el];
+      for (int b = b_lo; b < b_hi; b++) {
+        base[(int64_t)b * E + e] = run;
+        run += hist[(int64_t)b * E + e];
+      }
     }
+    __syncthreads();
   }
+}
+
+__global__ void __launch_bounds__(kPlanWarps * 32)
+k_attn_rank(const int32_t* __restrict__ ids, int n, int k, int E, AttnDsts ds, AttnPlan pl,
+            const int32_t* __restrict__ base, const int32_t* status) {
+  grid_dep_wait();
+  grid_dep_launch();
+  __shared__ int run_s[kPlanWarps][256];
+  __shared__ int rank_of[256], seg_s[AFD_MAX_FFN_RANKS];
+  for (int r = 0; r < ds.F; r++)
+    for (int e = ds.d[r].first + threadIdx.x; e < ds.d[r].first + ds.d[r].count; e += blockDim.x)
+      rank_of[e] = r;
+  if (threadIdx.x < ds.F) seg_s[threadIdx.x] = pl.seg[threadIdx.x];
   __syncthreads();
+  if (read_status(status)) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.x * kPlanWarps + warp;
+  if (b >= (n + kBlkTok - 1) / kBlkTok) return;
+  int* run = run_s[warp];
+  for (int e = lane; e < E; e += 32) run[e] = base[(int64_t)b * E + e];
+  __syncwarp();
+  const int f0 = b * kBlkTok * k, f1 = min(n * k, f0 + kBlkTok * k);
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int g0 = c0; g0 < c1; g0 += 32) {
+  for (int g0 = f0; g0 < f1; g0 += 32) {
     const int fi = g0 + lane;
-    const bool ok = fi < c1;
+    const bool ok = fi < f1;
     const int e = ok ? ids[fi] : -1 - lane;
     const unsigned same = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(same & lt_mask);
     int p = 0;
-    if (ok) p = hist_w[warp][e] + rank;
+    if (ok) p = run[e] + rank;
     __syncwarp();
-    if (ok && rank == 0) hist_w[warp][e] += __popc(same);
+    if (ok && rank == 0) run[e] += __popc(same);
     __syncwarp();
     if (ok) {
       const int r = rank_of[e];
       pl.dst[fi] = r;
-      pl.pos[fi] = p - offs[ds.d[r].first];
+      pl.pos[fi] = p - seg_s[r];
     }
   }
 }
@@ -285,8 +344,12 @@ __global__ void k_attn_wait(AttnDsts ds, AttnPlan pl, int region, int stage, int
 
 // recv, combine: work item = (token, block of 256 features), a warp per item;
 // out[t] = sum over j ascending of w[t, j] * y(rank dst, row pos) + s(row
-// t / F of rank t mod F), fp32, rounded once to the activation type.
-template <bool ACT_F32>
+// t / F of rank t mod F), fp32, rounded once to the activation type.  Lane
+// j < k finds its partial's row once per item; the rows are then read in
+// rounds of kBatch (all loads of a round before its multiply-adds, which
+// stay in ascending j): 1 keeps the registers low and the SM full for
+// large fan-ins, 8 keeps loads in flight when few warps have work.
+template <bool ACT_F32, int kBatch>
 __global__ void __launch_bounds__(kThreads)
 k_attn_combine(AttnDsts ds, AttnPlan pl, int region, int stage, int n, int k, int hidden,
                const float* __restrict__ wts, uint8_t* out, int with_shared, const int32_t* status) {
@@ -295,6 +358,7 @@ k_attn_combine(AttnDsts ds, AttnPlan pl, int region, int stage, int n, int k, in
   if (read_status(status)) return;
   constexpr int kVec = 8;  // features per lane step
   constexpr int kEl = ACT_F32 ? 4 : 2;
+  constexpr int kWords = ACT_F32 ? 2 : 1;  // 16-byte loads per lane and row
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * (blockDim.x >> 5);
   const int nfb = (hidden + 32 * kVec - 1) / (32 * kVec);
@@ -302,62 +366,79 @@ k_attn_combine(AttnDsts ds, AttnPlan pl, int region, int stage, int n, int k, in
   const int64_t row_bytes = (int64_t)hidden * kEl;
   for (int64_t it = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items; it += warps) {
     const int t = (int)(it / nfb), fb = (int)(it % nfb);
-    const int c = fb * 32 * kVec + lane * kVec;
-    int my_d = 0, my_q = 0;
+    const int c0 = fb * 32 * kVec + lane * kVec;
+    const bool valid = c0 < hidden;
+    const int64_t cb = (int64_t)(valid ? c0 : 0) * kEl;
+    const uint8_t* my_row = nullptr;
     float my_w = 0.0f;
     if (lane < k) {
-      my_d = pl.dst[(int64_t)t * k + lane];
-      my_q = pl.pos[(int64_t)t * k + lane];
+      const int d = pl.dst[(int64_t)t * k + lane];
+      my_row = slot_of(ds.d[d].ret, ds.d[d].g, region, stage) + ds.d[d].g.routed_x +
+               (int64_t)pl.pos[(int64_t)t * k + lane] * row_bytes;
       my_w = wts[(int64_t)t * k + lane];
     }
     float acc[kVec];
 #pragma unroll
     for (int v = 0; v < kVec; v++) acc[v] = 0.0f;
-    for (int j = 0; j < k; j++) {
-      const int d = __shfl_sync(0xffffffffu, my_d, j);
-      const int q = __shfl_sync(0xffffffffu, my_q, j);
-      const float wj = __shfl_sync(0xffffffffu, my_w, j);
-      if (c >= hidden) continue;
-      const uint8_t* row = slot_of(ds.d[d].ret, ds.d[d].g, region, stage) + ds.d[d].g.routed_x +
-                           (int64_t)q * row_bytes + (int64_t)c * kEl;
-      if constexpr (ACT_F32) {
-        const float4 a = *reinterpret_cast<const float4*>(row);
-        const float4 b = *reinterpret_cast<const float4*>(row + 16);
-        const float y[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    for (int j0 = 0; j0 < k; j0 += kBatch) {
+      uint4 raw[kBatch][kWords];
+      float wj[kBatch];
 #pragma unroll
-        for (int v = 0; v < kVec; v++) acc[v] = __fmaf_rn(wj, y[v], acc[v]);
-      } else {
-        const uint4 u = *reinterpret_cast<const uint4*>(row);
-        const uint32_t p[4] = {u.x, u.y, u.z, u.w};
+      for (int u = 0; u < kBatch; u++) {
+        const int j = (j0 + u) & 31;
+        const uint8_t* row = reinterpret_cast<const uint8_t*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(my_row), j));
+        wj[u] = __shfl_sync(0xffffffffu, my_w, j);
+        const bool ld = valid && j0 + u < k;
 #pragma unroll
-        for (int v = 0; v < 4; v++) {
-          acc[2 * v] = __fmaf_rn(wj, __uint_as_float(p[v] << 16), acc[2 * v]);
-          acc[2 * v + 1] = __fmaf_rn(wj, __uint_as_float(p[v] & 0xffff0000u), acc[2 * v + 1]);
+        for (int q = 0; q < kWords; q++)
+          raw[u][q] = ld ? reinterpret_cast<const uint4*>(row + cb)[q] : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; u++) {
+        if (j0 + u >= k) break;
+        float y[kVec];
+        if constexpr (ACT_F32) {
+          y[0] = __uint_as_float(raw[u][0].x); y[1] = __uint_as_float(raw[u][0].y);
+          y[2] = __uint_as_float(raw[u][0].z); y[3] = __uint_as_float(raw[u][0].w);
+          y[4] = __uint_as_float(raw[u][kWords - 1].x); y[5] = __uint_as_float(raw[u][kWords - 1].y);
+          y[6] = __uint_as_float(raw[u][kWords - 1].z); y[7] = __uint_as_float(raw[u][kWords - 1].w);
+        } else {
+          const uint32_t p[4] = {raw[u][0].x, raw[u][0].y, raw[u][0].z, raw[u][0].w};
+#pragma unroll
+          for (int v = 0; v < 4; v++) {
+            y[2 * v] = __uint_as_float(p[v] << 16);
+            y[2 * v + 1] = __uint_as_float(p[v] & 0xffff0000u);
+          }
         }
+#pragma unroll
+        for (int v = 0; v < kVec; v++) acc[v] = __fmaf_rn(wj[u], y[v], acc[v]);
       }
     }
-    if (c >= hidden) continue;
+    if (!valid) continue;
     if (with_shared) {
       const int d = t % ds.F;
       const uint8_t* row = slot_of(ds.d[d].ret, ds.d[d].g, region, stage) + ds.d[d].g.shared_x +
-                           (int64_t)(t / ds.F) * row_bytes + (int64_t)c * kEl;
+                           (int64_t)(t / ds.F) * row_bytes + cb;
+      float y[kVec];
       if constexpr (ACT_F32) {
         const float4 a = *reinterpret_cast<const float4*>(row);
         const float4 b = *reinterpret_cast<const float4*>(row + 16);
-        const float y[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int v = 0; v < kVec; v++) acc[v] = __fadd_rn(acc[v], y[v]);
+        y[0] = a.x; y[1] = a.y; y[2] = a.z; y[3] = a.w;
+        y[4] = b.x; y[5] = b.y; y[6] = b.z; y[7] = b.w;
       } else {
         const uint4 u = *reinterpret_cast<const uint4*>(row);
         const uint32_t p[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int v = 0; v < 4; v++) {
-          acc[2 * v] = __fadd_rn(acc[2 * v], __uint_as_float(p[v] << 16));
-          acc[2 * v + 1] = __fadd_rn(acc[2 * v + 1], __uint_as_float(p[v] & 0xffff0000u));
+          y[2 * v] = __uint_as_float(p[v] << 16);
+          y[2 * v + 1] = __uint_as_float(p[v] & 0xffff0000u);
         }
       }
+#pragma unroll
+      for (int v = 0; v < kVec; v++) acc[v] = __fadd_rn(acc[v], y[v]);
     }
-    uint8_t* o = out + (int64_t)t * row_bytes + (int64_t)c * kEl;
+    uint8_t* o = out + (int64_t)t * row_bytes + cb;
     if constexpr (ACT_F32) {
       reinterpret_cast<float4*>(o)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
       reinterpret_cast<float4*>(o)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
@@ -392,6 +473,8 @@ struct afd_attn {
   AttnDsts ds;
   uint8_t* mem = nullptr;
   int32_t* status = nullptr;
+  int32_t* hist = nullptr;   // [token_cap / 16][E] per-block expert counts of a send
+  int32_t* base = nullptr;   // [token_cap / 16][E] their first positions
   std::vector<AttnPlan> plans;   // one per stage
   std::vector<int> last_n;       // tokens of each stage's last send
   std::vector<int> last_shared;  // whether it carried shared rows
@@ -487,10 +570,13 @@ int afd_attn_create(afd_ctx* const* ranks, int ffn_size, int peer, int num_exper
     const int64_t even = ((int64_t)c0.token_cap * c0.topk + ffn_size - 1) / ffn_size;
     a->routed_cap = (int64_t)std::ceil((double)even * (double)c0.routed_cap_multiplier);
   }
-  // scratch: status, then per stage dst / pos [token_cap * k], rows [F], counts [E]
+  // scratch: status, the sort's per-block histograms and bases, then per
+  // stage dst / pos [token_cap * k], rows [F], counts [E], segment starts [F]
   const int64_t nk = (int64_t)a->token_cap * a->k;
-  const int64_t per_stage = (2 * nk + AFD_MAX_FFN_RANKS + 256) * 4;
-  const int64_t total = 256 + per_stage * a->ring;
+  const int64_t nb = (a->token_cap + kBlkTok - 1) / kBlkTok;
+  const int64_t hist_bytes = ((nb * num_experts * 4 + 255) / 256) * 256;
+  const int64_t per_stage = (2 * nk + 2 * AFD_MAX_FFN_RANKS + 256) * 4;
+  const int64_t total = 256 + 2 * hist_bytes + per_stage * a->ring;
   if (attn_fail(cudaMalloc(&a->mem, total), "attention-side scratch") ||
       attn_fail(cudaMemset(a->mem, 0, total), "attention-side scratch")) {
     cudaFree(a->mem);
@@ -498,9 +584,12 @@ int afd_attn_create(afd_ctx* const* ranks, int ffn_size, int peer, int num_exper
     return AFD_ERR_CUDA;
   }
   a->status = reinterpret_cast<int32_t*>(a->mem);
+  a->hist = reinterpret_cast<int32_t*>(a->mem + 256);
+  a->base = reinterpret_cast<int32_t*>(a->mem + 256 + hist_bytes);
   for (int s = 0; s < a->ring; s++) {
-    int32_t* b = reinterpret_cast<int32_t*>(a->mem + 256 + per_stage * s);
-    a->plans.push_back(AttnPlan{b, b + nk, b + 2 * nk, b + 2 * nk + AFD_MAX_FFN_RANKS});
+    int32_t* b = reinterpret_cast<int32_t*>(a->mem + 256 + 2 * hist_bytes + per_stage * s);
+    a->plans.push_back(AttnPlan{b, b + nk, b + 2 * nk, b + 2 * nk + AFD_MAX_FFN_RANKS,
+                                b + 2 * nk + AFD_MAX_FFN_RANKS + 256});
   }
   a->last_n.assign(a->ring, -1);
   a->last_shared.assign(a->ring, 0);
@@ -527,9 +616,22 @@ int afd_attn_dispatch(afd_attn* a, int stage, int layer, const void* x, int n_to
   const AttnPlan& pl = a->plans[stage];
   LaunchCtx lc = a->lc();
   const int row_bytes = a->hidden * (a->act_f32 ? 4 : 2);
-  int rc = attn_fail(launch_k(lc, k_attn_plan, 1, kPlanThreads, 0, topk_ids, n_tokens, a->k, a->E,
-                              a->ds, pl, a->routed_cap, a->status),
-                     "dispatch plan");
+  const int nb = (n_tokens + kBlkTok - 1) / kBlkTok;
+  const int plan_grid = (nb + kPlanWarps - 1) / kPlanWarps;
+  int rc = AFD_OK;
+  if (nb)
+    rc = attn_fail(launch_k(lc, k_attn_hist, plan_grid, kPlanWarps * 32, 0, topk_ids, n_tokens,
+                            a->k, a->E, a->hist, a->status),
+                   "dispatch histograms");
+  if (!rc)
+    rc = attn_fail(launch_k(lc, k_attn_scan, 1, 1024, 0, n_tokens, a->E, a->ds, pl,
+                            (const int32_t*)a->hist, a->base, a->routed_cap, a->status),
+                   "dispatch scan");
+  if (!rc && nb)
+    rc = attn_fail(launch_k(lc, k_attn_rank, plan_grid, kPlanWarps * 32, 0, topk_ids, n_tokens,
+                            a->k, a->E, a->ds, pl, (const int32_t*)a->base,
+                            (const int32_t*)a->status),
+                   "dispatch rank");
   const int64_t rows = (int64_t)n_tokens * a->k + (with_shared ? n_tokens : 0);
   if (!rc && rows > 0)
     rc = attn_fail(launch_k(lc, k_attn_copy, grid_rows(rows, kThreads / 32, a->num_sms * 8), kThreads,
@@ -565,7 +667,9 @@ int afd_attn_combine(afd_attn* a, int stage, const float* topk_weights, void* ou
   if (rc || n_tokens == 0) return rc;
   const int64_t items = (int64_t)n_tokens * ((a->hidden + 255) / 256);
   const int grid = grid_rows(items, kThreads / 32, a->num_sms * 8);
-  auto kern = a->act_f32 ? k_attn_combine<true> : k_attn_combine<false>;
+  const bool small = items < (int64_t)a->num_sms * 64;
+  auto kern = a->act_f32 ? (small ? k_attn_combine<true, 8> : k_attn_combine<true, 1>)
+                         : (small ? k_attn_combine<false, 8> : k_attn_combine<false, 1>);
   return attn_fail(launch_k(lc, kern, grid, kThreads, 0, a->ds, pl, a->peer, stage, n_tokens, a->k,
                             a->hidden, topk_weights, static_cast<uint8_t*>(out), ws,
                             (const int32_t*)a->status),

@@ -112,7 +112,9 @@ def run_round_trip(rs, with_shared=True):
                 off = L.flags_bytes + p * c.ring_depth * L.slot_bytes + getattr(L, field)
                 nb = n_p * w.hidden * w.act_bytes
                 if n_p and (field == "routed_x" or with_shared):
-                    a = O.bf16_bits_to_f32(got[off: off + nb].view(np.uint16)).reshape(n_p, -1)
+                    raw = got[off: off + nb]
+                    a = (O.bf16_bits_to_f32(raw.view(np.uint16)) if w.act == "bf16"
+                         else raw.view(np.float32)).reshape(n_p, -1)
                     errs.append(G.rel_err(a.astype(np.float64), ref[base: base + n_p]))
                 base += n_p
         assert errs and max(errs) <= G.tol_for(w), (r, errs)
@@ -148,6 +150,17 @@ def test_round_trip_other_engines_routed_only(gemm):
     """The routed-only protocol (no shared rows travel) on the other engines."""
     w = W.custom("fanin", seq_lens=[37, 91], num_experts=12)
     rs = R.RankSet(w, 3, gemm=gemm)
+    try:
+        run_round_trip(rs, with_shared=False)
+    finally:
+        rs.close()
+
+
+def test_round_trip_fp32_simt():
+    """fp32 activations (the tiny configuration: renormalised top-2 of 8,
+    no shared expert) over 2 ranks on the SIMT engine."""
+    w = W.get("tiny")
+    rs = R.RankSet(w, 2, gemm=A.AFD_GEMM_SIMT)
     try:
         run_round_trip(rs, with_shared=False)
     finally:

@@ -187,7 +187,8 @@ struct afd_ctx {
   DevLayer* dlayers = nullptr;       // device copy of every layer's weights (work-item loop)
   CUtensorMap tmXp, tmH, tmHs;        // token boxes of the tensor engine
   CUtensorMap tmXp32, tmH32, tmHs32;  // 32-row boxes (small SM-pair units)
-  CUtensorMap tmWin, tmWin32;         // dispatch window as [rows, hidden] (grouped form in place)
+  CUtensorMap tmWin, tmWin32;         // dispatch window as [rows, hidden] (shared rows, and
+                                      // the grouped form's rows from one peer, read in place)
   std::vector<LayerW> layers;
   std::vector<uint64_t> last_seq;
   int tmax = 0;
@@ -358,7 +359,7 @@ int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out) {
       {E * 4}, {(E + 1) * 4},                // counts, offsets
       {Tm * k * 4}, {Tm * k * 4},            // perm, inv
       {AFD_MAX_PEERS * E * 4},               // peer_counts
-      {(Tm * k + Tm) * H * ab},              // xp
+      {(Tm * k + Tm) * H * ab},              // xp (routed rows, then shared rows when gathered)
       {Tm * k * I * ab},                     // h
       {Tm * k * H * yb},                     // y
       {Tm * (Is > 0 ? Is : 1) * ab},         // hs
@@ -828,6 +829,17 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
   // when the experts average <= 48 rows (decode-sized fan-ins), which then
   // runs its deeper narrow ring
   const int bn = c.gemm == AFD_GEMM_TENSOR && N <= 48 * (int64_t)c.num_experts ? 64 : 256;
+  // the shared expert reads its rows in place from the slots' shared_x (one
+  // group per peer, no copy) when that takes no more GEMM units than the
+  // gathered rows: large peers (prefill); with many small peers (decode)
+  // each group would stream the shared weights once more, so those rows are
+  // gathered.  Steps of the work-item loop (counts unknown here) gather.
+  int sh_in_place = 0;
+  if (has_shared && !dev && !in_place) {
+    int64_t units_ip = 0;
+    for (int i = 0; i < f.n_peers; i++) units_ip += (f.sprefix[i + 1] - f.sprefix[i] + bn - 1) / bn;
+    sh_in_place = units_ip <= ((int64_t)f.stotal + bn - 1) / bn + 1;
+  }
   LaunchCtx lc = ctx->lc();
   const DevWS& ws = ctx->ws;
   // decode-sized fan-ins: the SwiGLU GEMM streams its weights from HBM while
@@ -882,15 +894,16 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
   mark(2);
   rc = cuda_fail(grouped ? launch_plan_grouped(lc, f, ws, c.num_experts, c.inter, c.shared_inter,
                                                 c.hidden, has_shared, bn, ctx->plan1, ctx->plan2,
-                                                ctx->geom, row_bytes, in_place)
+                                                ctx->geom, row_bytes, in_place, sh_in_place)
                          : launch_plan(lc, f, ws, c.num_experts, c.topk, c.inter, c.shared_inter,
                                        c.hidden, has_shared, bn, ctx->plan1, ctx->plan2, ws.hist,
-                                       ws.base),
+                                       ws.base, ctx->geom, row_bytes, sh_in_place),
                  "plan");
   if (rc) return rc;
   mark(3);
   if (!in_place) {
-    rc = cuda_fail(launch_gather(lc, ctx->geom, ctx->win[0], f, ws, c.topk, row_bytes, has_shared),
+    rc = cuda_fail(launch_gather(lc, ctx->geom, ctx->win[0], f, ws, c.topk, row_bytes, c.hidden,
+                                 has_shared, sh_in_place),
                    "gather");
     if (rc) return rc;
   }
@@ -908,10 +921,13 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
         a1.item = ws.item;
         a1.wsel = 1;
       }
-      const CUtensorMap& tb = in_place ? ctx->tmWin : ctx->tmXp;
-      const CUtensorMap& tbs = in_place ? ctx->tmWin32 : ctx->tmXp32;
-      a1.tmB[0] = a1.tmB[1] = tb;
-      a1.tmBs[0] = a1.tmBs[1] = tbs;
+      // routed rows: gathered into Xp, or in their slots (grouped form, one
+      // peer); shared rows: gathered after them, or in the slots' shared_x
+      const bool sh_win = in_place || sh_in_place;
+      a1.tmB[0] = in_place ? ctx->tmWin : ctx->tmXp;
+      a1.tmBs[0] = in_place ? ctx->tmWin32 : ctx->tmXp32;
+      a1.tmB[1] = sh_win ? ctx->tmWin : ctx->tmXp;
+      a1.tmBs[1] = sh_win ? ctx->tmWin32 : ctx->tmXp32;
       a1.out[0] = ws.h;
       a1.out[1] = ws.hs;
       a1.ldo[0] = c.inter;
@@ -971,7 +987,8 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
         s1.item = ws.item;
         s1.wsel = 1;
       }
-      s1.B[0] = s1.B[1] = ws.xp;
+      s1.B[0] = ws.xp;
+      s1.B[1] = sh_in_place ? (const void*)ctx->win[0] : ws.xp;  // window rows, or gathered
       s1.ldb[0] = s1.ldb[1] = c.hidden;
       s1.out[0] = ws.h;
       s1.out[1] = ws.hs;
@@ -985,7 +1002,7 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
       s1.swiglu = 1;
       s1.plan = ctx->plan1;
       s1.status = ws.status;
-      rc = cuda_fail(launch_gemm_simt(lc, s1, c.num_experts + 1), "simt gemm1");
+      rc = cuda_fail(launch_gemm_simt(lc, s1, c.num_experts + f.n_peers), "simt gemm1");
       if (rc) return rc;
       mark(5);
       SimtArgs s2 = s1;
@@ -1009,7 +1026,7 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
       s2.M[0] = s2.M[1] = c.hidden;
       s2.swiglu = 0;
       s2.plan = ctx->plan2;
-      rc = cuda_fail(launch_gemm_simt(lc, s2, c.num_experts + 1), "simt gemm2");
+      rc = cuda_fail(launch_gemm_simt(lc, s2, c.num_experts + f.n_peers), "simt gemm2");
       if (rc) return rc;
     }
   } else {

@@ -387,15 +387,19 @@ cudaError_t launch_router(const LaunchCtx& lc, const WinGeom& g, const uint8_t* 
                           const FanIn& f, const DevWS& ws, int hidden, int act_f32,
                           const float* WgQ, const float* bias, int E, int k, int renorm,
                           float scale, float* logits, int32_t* hist);
+// sh_in_place: the shared expert reads its rows in place from the slots'
+// shared_x (one group per peer; g, row_bytes give the window rows) instead of
+// from the gathered rows after the routed ones
 cudaError_t launch_plan(const LaunchCtx& lc, const FanIn& f, const DevWS& ws, int E, int k,
                         int inter, int shared_inter, int hidden, int has_shared, int bn,
-                        GemmPlan* plan1, GemmPlan* plan2, const int32_t* hist, int32_t* base);
+                        GemmPlan* plan1, GemmPlan* plan2, const int32_t* hist, int32_t* base,
+                        const WinGeom& g, int row_bytes, int sh_in_place);
 cudaError_t launch_gather(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
-                          const FanIn& f, const DevWS& ws, int k, int row_bytes,
-                          int has_shared);
+                          const FanIn& f, const DevWS& ws, int k, int row_bytes, int hidden,
+                          int has_shared, int sh_in_place);
 cudaError_t launch_gemm_tc(const LaunchCtx& lc, const GemmArgs& a);
 cudaError_t launch_gemm_tc2(const LaunchCtx& lc, const GemmArgs& a);
-cudaError_t launch_gemm_simt(const LaunchCtx& lc, const SimtArgs& a, int max_rows_hint);
+cudaError_t launch_gemm_simt(const LaunchCtx& lc, const SimtArgs& a, int max_groups);
 cudaError_t launch_combine(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret,
                            const FanIn& f, const DevWS& ws, int hidden, int k, int act_f32,
                            int has_shared, int y_f32);
@@ -416,7 +420,7 @@ cudaError_t launch_unpack(const LaunchCtx& lc, const WinGeom& g, const uint8_t* 
 cudaError_t launch_plan_grouped(const LaunchCtx& lc, const FanIn& f, const DevWS& ws, int E,
                                 int inter, int shared_inter, int hidden, int has_shared, int bn,
                                 GemmPlan* plan1, GemmPlan* plan2, const WinGeom& g, int row_bytes,
-                                int in_place);
+                                int in_place, int sh_in_place);
 cudaError_t launch_scatter_grouped(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret,
                                    const FanIn& f, const DevWS& ws, int hidden, int act_f32,
                                    int has_shared);

@@ -1178,10 +1178,11 @@ k_router_topk(const __grid_constant__ FanIn fp, DevWS ws, const float* __restric
 // one group per expert (rows = its partials, in permuted order), then the
 // shared expert over all T rows; tile0 / unit0 are prefixes of the one-CTA
 // tiles and of the SM-pair units.
-__device__ void write_tile_tables(const FanIn& f, int k, int E, int inter, int shared_inter,
-                                  int hidden, int has_shared, int bn, const int* cnt,
+__device__ void write_tile_tables(const FanIn& f, const DevWS& ws, const WinGeom& g, int row_bytes,
+                                  int k, int E, int inter, int shared_inter, int hidden,
+                                  int has_shared, int sh_in_place, int bn, const int* cnt,
                                   const int* offs, GemmPlan* plan1, GemmPlan* plan2) {
-  const int N = f.grouped ? f.rtotal : f.total * k;  // routed rows; the shared rows follow
+  const int N = f.grouped ? f.rtotal : f.total * k;  // routed rows (Xp rows 0..N-1)
   int tiles1 = 0, tiles2 = 0, units1 = 0, units2 = 0, ng = 0;
   const int mt1 = (inter + 63) / 64, mt2 = (hidden + 127) / 128;
   for (int e = 0; e < E; e++, ng++) {
@@ -1196,7 +1197,10 @@ __device__ void write_tile_tables(const FanIn& f, int k, int E, int inter, int s
     units1 += (mt1 + 1) / 2 * nt;
     units2 += (mt2 + 1) / 2 * nt;
   }
-  if (has_shared) {
+  // the shared expert: one group over the gathered shared rows (Xp rows
+  // N..), or one group per entry that sent shared rows, read in place from
+  // its slot's shared_x (window rows); outputs at the shared-row offsets
+  if (has_shared && !sh_in_place) {
     const int rows = f.stotal;
     const int nt = (rows + bn - 1) / bn;
     const int mts = (shared_inter + 63) / 64;
@@ -1209,6 +1213,27 @@ __device__ void write_tile_tables(const FanIn& f, int k, int E, int inter, int s
     units1 += (mts + 1) / 2 * nt;
     units2 += (mt2 + 1) / 2 * nt;
     ng++;
+  }
+  if (has_shared && sh_in_place) {
+    int srows[AFD_MAX_PEERS];  // all loads before the table's stores
+    for (int i = 0; i < f.n_peers; i++)
+      srows[i] = ws.peer_shared[i] ? f.sprefix[i + 1] - f.sprefix[i] : 0;
+    for (int i = 0; i < f.n_peers; i++) {
+      const int rows = srows[i];
+      if (!rows) continue;
+      const int nt = (rows + bn - 1) / bn;
+      const int mts = (shared_inter + 63) / 64;
+      const int wr = window_row(g, f.region[i], f.stage, g.shared_x, 0, row_bytes);
+      GemmGroup a{rows, wr, f.sprefix[i], 0, 1, mts, nt, tiles1, units1};
+      GemmGroup b{rows, f.sprefix[i], f.sprefix[i], 0, 1, mt2, nt, tiles2, units2};
+      plan1->g[ng] = a;
+      plan2->g[ng] = b;
+      tiles1 += mts * nt;
+      tiles2 += mt2 * nt;
+      units1 += (mts + 1) / 2 * nt;
+      units2 += (mt2 + 1) / 2 * nt;
+      ng++;
+    }
   }
   plan1->ngroups = ng;
   plan2->ngroups = ng;
@@ -1227,7 +1252,7 @@ template <bool kDev>
 __global__ void __launch_bounds__(kScanWarps * 32)
 k_plan_scan(const __grid_constant__ FanIn fp, DevWS ws, int E, int k, int inter, int shared_inter, int hidden,
             int has_shared, int bn, const int32_t* __restrict__ hist, int32_t* __restrict__ base,
-            GemmPlan* plan1, GemmPlan* plan2) {
+            GemmPlan* plan1, GemmPlan* plan2, WinGeom g, int row_bytes, int sh_in_place) {
   grid_dep_wait();
   grid_dep_launch();
   const FanIn& f = step_item<kDev>(fp, ws.item);
@@ -1288,7 +1313,9 @@ k_plan_scan(const __grid_constant__ FanIn fp, DevWS ws, int E, int k, int inter,
     ws.offsets[e] = offs[e];
     if (e < E) ws.counts[e] = cnt[e];
   }
-  if (tid == 0) write_tile_tables(f, k, E, inter, shared_inter, hidden, has_shared, bn, cnt, offs, plan1, plan2);
+  if (tid == 0)
+    write_tile_tables(f, ws, g, row_bytes, k, E, inter, shared_inter, hidden, has_shared,
+                      sh_in_place, bn, cnt, offs, plan1, plan2);
 }
 
 // ---------------------------------------------------------------------------
@@ -1302,7 +1329,8 @@ constexpr int kPlanSmallMax = 8192;
 template <bool kDev>
 __global__ void __launch_bounds__(1024)
 k_plan_small(const __grid_constant__ FanIn fp, DevWS ws, int E, int k, int inter, int shared_inter, int hidden,
-             int has_shared, int bn, GemmPlan* plan1, GemmPlan* plan2) {
+             int has_shared, int bn, GemmPlan* plan1, GemmPlan* plan2, WinGeom g, int row_bytes,
+             int sh_in_place) {
   grid_dep_wait();
   grid_dep_launch();
   const FanIn& f = step_item<kDev>(fp, ws.item);
@@ -1372,7 +1400,9 @@ k_plan_small(const __grid_constant__ FanIn fp, DevWS ws, int E, int k, int inter
       ws.inv[fi] = pos;
     }
   }
-  if (tid == 0) write_tile_tables(f, k, E, inter, shared_inter, hidden, has_shared, bn, cnt, offs, plan1, plan2);
+  if (tid == 0)
+    write_tile_tables(f, ws, g, row_bytes, k, E, inter, shared_inter, hidden, has_shared,
+                      sh_in_place, bn, cnt, offs, plan1, plan2);
 }
 
 // ---------------------------------------------------------------------------
@@ -1385,7 +1415,8 @@ k_plan_small(const __grid_constant__ FanIn fp, DevWS ws, int E, int k, int inter
 template <bool kDev>
 __global__ void __launch_bounds__(1024)
 k_plan_grouped(const __grid_constant__ FanIn fp, DevWS ws, int E, int inter, int shared_inter, int hidden, int has_shared,
-               int bn, GemmPlan* plan1, GemmPlan* plan2, WinGeom g, int row_bytes, int in_place) {
+               int bn, GemmPlan* plan1, GemmPlan* plan2, WinGeom g, int row_bytes, int in_place,
+               int sh_in_place) {
   grid_dep_wait();
   grid_dep_launch();
   const FanIn& f = step_item<kDev>(fp, ws.item);
@@ -1431,7 +1462,9 @@ k_plan_grouped(const __grid_constant__ FanIn fp, DevWS ws, int E, int inter, int
   }
   __syncthreads();
   if (!in_place) {  // the gather places each row (and records perm / inv)
-    if (tid == 0) write_tile_tables(f, 1, E, inter, shared_inter, hidden, has_shared, bn, cnt, offs, plan1, plan2);
+    if (tid == 0)
+      write_tile_tables(f, ws, g, row_bytes, 1, E, inter, shared_inter, hidden, has_shared,
+                        sh_in_place, bn, cnt, offs, plan1, plan2);
     return;
   }
   // the entries' group lists in shared memory for the one-thread table walk
@@ -1545,17 +1578,21 @@ k_rank(const __grid_constant__ FanIn fp, DevWS ws, int E, int k, const int32_t* 
 // ---------------------------------------------------------------------------
 // a3 gather: Xp[pos] = the row of token perm[pos] / k, read straight from its
 // peer slot (the fan-in concatenation is never materialised), then the
-// shared rows in concatenation order.  One warp per row, 16-byte vectors.
+// shared rows in concatenation order -- unless the shared expert reads them
+// in place from the slots' shared_x.  One warp per row, 16-byte vectors.
 // ---------------------------------------------------------------------------
 template <bool kDev>
 __global__ void __launch_bounds__(kThreads)
 k_gather(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn fp, DevWS ws, int k, int row_bytes,
-         int has_shared) {
+         int hidden, int has_shared, int sh_in_place) {
   grid_dep_wait();
   grid_dep_launch();
   const FanIn& f = step_item<kDev>(fp, ws.item);
   if (read_status(ws.status)) return;
   const int N = f.grouped ? f.rtotal : f.total * k;
+  // then the shared rows; when the shared expert reads them in place, only
+  // the rows of s of peers that sent none are zeroed here (the combine adds
+  // s for every token)
   const int rows = N + (has_shared ? f.stotal : 0);
   const int nvec = row_bytes / 16;
   const int warps = gridDim.x * (blockDim.x >> 5);
@@ -1592,6 +1629,14 @@ k_gather(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn fp, DevWS 
       i = entry_of_shared(f, t);
       local = t - f.sprefix[i];
       field = g.shared_x;
+      if (sh_in_place) {
+        if (!ws.peer_shared[i]) {
+          float4* srow = reinterpret_cast<float4*>(ws.s + (int64_t)t * hidden);
+          for (int v = threadIdx.x & 31; v < hidden / 4; v += 32)
+            srow[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        continue;
+      }
     }
     const int lane = threadIdx.x & 31;
     if (r >= N && !ws.peer_shared[i]) {
@@ -1777,7 +1822,7 @@ k_combine(uint8_t* ret, WinGeom g, const __grid_constant__ FanIn fp, DevWS ws, i
         }
       }
       if (valid) {  // lanes past hidden write nothing
-        if (has_shared) {
+        if (has_shared) {  // zero rows for peers that sent no shared rows
           const float4* sp = reinterpret_cast<const float4*>(ws.s + (int64_t)t * hidden + c);
           const float4 a = sp[0], b = sp[1];
           acc[0] = __fadd_rn(acc[0], a.x); acc[1] = __fadd_rn(acc[1], a.y);
@@ -2165,14 +2210,15 @@ template <bool kDev>
 static cudaError_t launch_plan_t(const LaunchCtx& lc, const FanIn& f, const DevWS& ws, int E,
                                  int k, int inter, int shared_inter, int hidden, int has_shared,
                                  int bn, GemmPlan* plan1, GemmPlan* plan2, const int32_t* hist,
-                                 int32_t* base) {
+                                 int32_t* base, const WinGeom& g, int row_bytes, int sh_in_place) {
   const int nblocks = router_blocks(f.total);
   if ((int64_t)f.total * k <= kPlanSmallMax) {
     return launch_k(lc, k_plan_small<kDev>, 1, 1024, 0, f, ws, E, k, inter, shared_inter, hidden,
-                    has_shared, bn, plan1, plan2);
+                    has_shared, bn, plan1, plan2, g, row_bytes, sh_in_place);
   }
   cudaError_t err = launch_k(lc, k_plan_scan<kDev>, 1, kScanWarps * 32, 0, f, ws, E, k, inter,
-                             shared_inter, hidden, has_shared, bn, hist, base, plan1, plan2);
+                             shared_inter, hidden, has_shared, bn, hist, base, plan1, plan2, g,
+                             row_bytes, sh_in_place);
   if (err != cudaSuccess || nblocks == 0) return err;
   return launch_k(lc, k_rank<kDev>, (nblocks + kRankWarps - 1) / kRankWarps, kRankWarps * 32, 0, f,
                   ws, E, k, (const int32_t*)base);
@@ -2180,20 +2226,22 @@ static cudaError_t launch_plan_t(const LaunchCtx& lc, const FanIn& f, const DevW
 
 cudaError_t launch_plan(const LaunchCtx& lc, const FanIn& f, const DevWS& ws, int E, int k,
                         int inter, int shared_inter, int hidden, int has_shared, int bn,
-                        GemmPlan* plan1, GemmPlan* plan2, const int32_t* hist, int32_t* base) {
+                        GemmPlan* plan1, GemmPlan* plan2, const int32_t* hist, int32_t* base,
+                        const WinGeom& g, int row_bytes, int sh_in_place) {
   return f.dev ? launch_plan_t<true>(lc, f, ws, E, k, inter, shared_inter, hidden, has_shared, bn,
-                                     plan1, plan2, hist, base)
+                                     plan1, plan2, hist, base, g, row_bytes, sh_in_place)
                : launch_plan_t<false>(lc, f, ws, E, k, inter, shared_inter, hidden, has_shared, bn,
-                                      plan1, plan2, hist, base);
+                                      plan1, plan2, hist, base, g, row_bytes, sh_in_place);
 }
 
 cudaError_t launch_gather(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
-                          const FanIn& f, const DevWS& ws, int k, int row_bytes, int has_shared) {
+                          const FanIn& f, const DevWS& ws, int k, int row_bytes, int hidden,
+                          int has_shared, int sh_in_place) {
   const int64_t rows = (int64_t)f.total * k + (has_shared ? f.total : 0);
   if (rows == 0) return cudaSuccess;
   return launch_k(lc, f.dev ? k_gather<true> : k_gather<false>,
                   grid_for(rows, kThreads / 32, lc.num_sms * 8), kThreads, 0, win, g, f, ws, k,
-                  row_bytes, has_shared);
+                  row_bytes, hidden, has_shared, sh_in_place);
 }
 
 cudaError_t launch_gemm_simt(const LaunchCtx& lc, const SimtArgs& a, int max_groups) {
@@ -2240,10 +2288,10 @@ cudaError_t launch_unpack(const LaunchCtx& lc, const WinGeom& g, const uint8_t* 
 cudaError_t launch_plan_grouped(const LaunchCtx& lc, const FanIn& f, const DevWS& ws, int E,
                                 int inter, int shared_inter, int hidden, int has_shared, int bn,
                                 GemmPlan* plan1, GemmPlan* plan2, const WinGeom& g, int row_bytes,
-                                int in_place) {
+                                int in_place, int sh_in_place) {
   return launch_k(lc, f.dev ? k_plan_grouped<true> : k_plan_grouped<false>, 1, 1024, 0, f, ws, E,
                   inter, shared_inter, hidden, has_shared,
-                  bn, plan1, plan2, g, row_bytes, in_place);
+                  bn, plan1, plan2, g, row_bytes, in_place, sh_in_place);
 }
 
 cudaError_t launch_scatter_grouped(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret,

@@ -181,7 +181,7 @@ typedef struct afd_layout {
 #define AFD_WS_OFFSETS 3    /* int32 [E + 1] exclusive prefix of counts */
 #define AFD_WS_PERM 4       /* int32 [T*topk] position -> flattened index t*k+j */
 #define AFD_WS_INV 5        /* int32 [T*topk] flattened index -> position */
-#define AFD_WS_XP 6         /* act [T*topk + T, hidden] permuted rows, then shared rows */
+#define AFD_WS_XP 6         /* act [T*topk, hidden] permuted routed rows (shared rows stay in the slots) */
 #define AFD_WS_H 7          /* act [T*topk, inter] routed SwiGLU output */
 #define AFD_WS_Y 8          /* act [T*topk, hidden] routed down projection */
 #define AFD_WS_HS 9         /* act [T, shared_inter] shared SwiGLU output */

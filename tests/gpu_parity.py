@@ -67,11 +67,13 @@ def check_plan_exact(run, T, ids_ref):
     return ids
 
 
-def run_and_compare_full(run, slots=None, layer=0):
-    """Whole-fan-in comparison (sizes the oracle finishes in seconds)."""
+def run_and_compare_full(run, slots=None, layer=0, pack=True):
+    """Whole-fan-in comparison (sizes the oracle finishes in seconds); with
+    pack=False the caller has packed the slots."""
     w = run.w
     slots = list(range(w.num_peers)) if slots is None else slots
-    run.pack_all(layer)
+    if pack:
+        run.pack_all(layer)
     rc = run.forward(layer, slots=slots)
     assert rc == 0, A.strerror(rc)
     outs = run.unpack_all(peers=slots)

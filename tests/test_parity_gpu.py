@@ -86,3 +86,16 @@ def test_decode_26_layers():
     run = R.Runner(w, max_total_tokens=w.total_tokens)
     for layer in range(w.layers):
         G.run_and_compare_sampled(run, layer=layer, per_peer=1, check_routing=True)
+
+
+@pytest.mark.parametrize("gemm", [A.AFD_GEMM_TENSOR, A.AFD_GEMM_SIMT])
+def test_fanin_peer_without_shared_rows(gemm):
+    """A peer that sends no shared rows (shared_tokens = 0) beside peers that
+    do: its tokens get no shared-expert term, while the shared expert reads
+    the other peers' rows in place from their slots."""
+    w = W.custom("fanin", seq_lens=[37, 20, 91])
+    run = R.Runner(w, max_total_tokens=w.total_tokens, gemm=gemm)
+    run.pack_all(peers=[0, 2])
+    run.pack_all(peers=[1], with_shared=False)
+    e, _ = G.run_and_compare_full(run, pack=False)
+    print("max|err|/rms", e)

@@ -262,3 +262,37 @@ def test_serve_grouped_form(peers):
             for field, n in ((L.header, 4 * (12 + w.num_experts)), (L.routed_x, dev.g_n[p] * rb),
                              (L.shared_x, w.seq_lens[p] * rb)):
                 assert np.array_equal(rd[off + field: off + field + n], rh[off + field: off + field + n])
+
+
+@pytest.mark.parametrize("workload", ["v2lite_prefill", "decode"])
+def test_serve_full_size_matches_host_step(workload):
+    """At full size (the bench's launch shapes): the same packed bytes served
+    by the loop and by the host-described step on one context give
+    bit-identical return windows (the device-described kernels against the
+    host-described ones; the host step is checked against the oracle in
+    test_parity_gpu.py)."""
+    w = W.get(workload)
+    run = R.Runner(w, layers=1, max_total_tokens=w.total_tokens)
+    ret = []
+    for mode in ("host", "serve"):
+        run.pack_all(0)
+        if mode == "host":
+            assert run.forward(0) == 0
+        else:
+            assert A.afd_ffn_serve(run.ctx, list(range(w.num_peers)), 1) == 0
+        assert run.poll() == 0
+        win = run.window(A.AFD_DIR_RETURN)
+        L = run.layout
+        # payload of every return slot (the flags and echoed seqs differ)
+        rb = w.hidden * w.act_bytes
+        got = []
+        for p, n in enumerate(w.seq_lens):
+            off = L.flags_bytes + p * run.cfg.ring_depth * L.slot_bytes
+            got.append(win[off + L.routed_x: off + L.routed_x + n * rb].cpu().numpy().copy())
+            got.append(win[off + L.route_table: off + L.route_table + n * w.topk * 4].cpu().numpy().copy())
+            hdr = win[off + L.header: off + L.header + 4 * (12 + w.num_experts)].cpu().numpy().copy()
+            got.append(np.delete(hdr.view(np.int32), [3, 4]))   # all but seq / echo_seq
+        ret.append(got)
+    for a, b in zip(*ret):
+        assert np.array_equal(a, b)
+    run.close()

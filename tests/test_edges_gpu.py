@@ -1,0 +1,70 @@
+"""Edge cases of the FFN step against the CPU oracle: an empty fan-in, the
+largest expert count and top-k the kernels cover, the most peers, top-k
+equal to the expert count, hidden sizes that take the router's other
+kernels.  Needs an sm_103a GPU."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from combine_peer_slot_gb300 import afd as A
+from combine_peer_slot_gb300 import runtime as R
+from combine_peer_slot_gb300 import workloads as W
+from oracle import oracle as O
+from tests import gpu_parity as G
+
+
+@pytest.fixture(autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    A.lib()
+
+
+def test_all_peers_empty():
+    """Every listed peer sends no tokens: no expert work, and each return
+    slot still gets its header (num_tokens 0, no counts) and its flag."""
+    w = W.custom("fanin", seq_lens=[0, 0, 0], token_cap=64)
+    run = R.Runner(w, max_total_tokens=64)
+    run.pack_all(0)
+    assert run.forward(0) == 0
+    assert run.poll() == 0
+    ret = run.window(A.AFD_DIR_RETURN).cpu().numpy()
+    for p in range(3):
+        h = G.header(ret, run, p)
+        assert h[0] == 0x47444641 and h[7] == 0 and h[8] == 0 and not h[12:].any()
+        assert ret[:run.layout.flags_bytes].view(np.uint64)[p] == run.last_seq[(p, 0)]
+
+
+@pytest.mark.parametrize("shape", [
+    dict(num_experts=256, topk=16, hidden=512, inter=64, shared_inter=64, seq_lens=[40, 7]),
+    # every shape carries a shared expert: alone, a token's routed sum can
+    # cancel to a small rms against which the bf16 rounding of each
+    # expert's output (up to 2^-9 of it) exceeds 2e-2 (up to 2.9e-2 seen)
+    dict(num_experts=8, topk=8, hidden=256, inter=96, shared_inter=96, seq_lens=[19, 1, 33]),
+    dict(num_experts=16, topk=2, hidden=4096, inter=128, shared_inter=64, seq_lens=[33, 20]),
+    dict(num_experts=64, topk=6, hidden=3072, inter=64, shared_inter=64, seq_lens=[25]),
+], ids=["E256_k16", "k_equals_E", "hidden4096", "hidden3072"])
+def test_shapes_at_the_edges(shape):
+    """Routing, plan and outputs against the oracle at the shapes' edges:
+    256 experts with top-16 (the largest the router covers), top-k equal to
+    the expert count, hidden above 2048 (the router's fallback kernels)."""
+    w = W.custom("fanin", **shape)
+    run = R.Runner(w, max_total_tokens=w.total_tokens)
+    e, _ = G.run_and_compare_full(run)
+    print(shape, "max|err|/rms", e)
+    run.close()
+
+
+def test_sixty_four_peers():
+    """The most peers a window holds, with ragged and empty slots, listed in
+    a shuffled order."""
+    rng = np.random.default_rng(64)
+    lens = [int(v) for v in rng.integers(0, 9, size=A.AFD_MAX_PEERS)]
+    w = W.custom("fanin", seq_lens=lens, token_cap=16)
+    run = R.Runner(w, max_total_tokens=w.total_tokens)
+    slots = [int(v) for v in rng.permutation(A.AFD_MAX_PEERS)]
+    e, _ = G.run_and_compare_full(run, slots=slots)
+    print("64 peers, T =", sum(lens), "max|err|/rms", e)
+    run.close()

@@ -1776,9 +1776,10 @@ k_combine(uint8_t* ret, WinGeom g, const __grid_constant__ FanIn fp, DevWS ws, i
         }
       } else {
         // rounds of up to kBatch partials: their rows are all loaded before the
-        // multiply-adds, which still run in ascending j (kBatch > 1 for small
-        // fan-ins, where few warps must keep many loads in flight; 1 keeps the
-        // registers low and the SM full for large ones)
+        // multiply-adds, which still run in ascending j (8 for small fan-ins,
+        // where few warps must keep many loads in flight; 4 for large ones,
+        // measured faster than 1, 2, 3, 6 and 8, which trade loads in flight
+        // against registers and resident warps)
         for (int j0 = 0; j0 < k; j0 += kBatch) {
           uint4 raw[kBatch][Y_F32 ? 2 : 1];
           float wj[kBatch];
@@ -2264,7 +2265,7 @@ cudaError_t launch_combine(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret, 
     kern = d ? k_combine<false, true, 1, true> : k_combine<false, true, 1, false>;
   else if (!act_f32 && !y_f32)
     kern = small ? (d ? k_combine<false, false, 8, true> : k_combine<false, false, 8, false>)
-                 : (d ? k_combine<false, false, 1, true> : k_combine<false, false, 1, false>);
+                 : (d ? k_combine<false, false, 4, true> : k_combine<false, false, 4, false>);
   if (!kern) return cudaErrorInvalidValue;
   return launch_k(lc, kern, grid, kThreads, 0, ret, g, f, ws, hidden, k, has_shared);
 }

@@ -66,7 +66,9 @@ struct Ring {
   static constexpr size_t kEpiOffset = ((size_t)STAGES * STAGE_BYTES + sizeof(Tail) + 127) / 128 * 128;
   static constexpr size_t kSmemBytes = 1024 + kEpiOffset + (size_t)EPI_WARPS * EPI_BUF_BYTES;
   static_assert(kEpiOffset % 128 == 0 && EPI_BUF_BYTES % 128 == 0, "epilogue buffers must stay aligned");
-  static_assert(kSmemBytes <= 232448, "over the per-CTA shared memory limit");
+  // (plus the static table of the groups' first units)
+  static_assert(kSmemBytes + AFD_MAX_GROUPS * sizeof(int) <= 232448,
+                "over the per-CTA shared memory limit");
   static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
 };
 
@@ -163,11 +165,14 @@ struct Unit {
 };
 
 template <bool kNarrow>
-__device__ __forceinline__ Unit decode_unit(const GemmPlan& p, int unit) {
-  int lo = 0, hi = p.ngroups - 1;
+// unit0_s: the groups' first unit indices, staged in shared memory (the
+// search would otherwise chain one global load per step at every unit)
+__device__ __forceinline__ Unit decode_unit(const GemmPlan& p, const int* unit0_s, int ngroups,
+                                            int unit) {
+  int lo = 0, hi = ngroups - 1;
   while (lo < hi) {  // last group with unit0 <= unit (empty groups share unit0 with the next)
     const int mid = (lo + hi + 1) >> 1;
-    if (p.g[mid].unit0 <= unit) lo = mid; else hi = mid - 1;
+    if (unit0_s[mid] <= unit) lo = mid; else hi = mid - 1;
   }
   const GemmGroup& G = p.g[lo];
   const int u = unit - G.unit0;
@@ -241,6 +246,9 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
   // everything above touches only this CTA's shared memory
   grid_dep_wait();
   grid_dep_launch();
+  __shared__ int unit0_s[AFD_MAX_GROUPS];
+  const int ngroups = min(plan.ngroups, AFD_MAX_GROUPS);
+  for (int i = threadIdx.x; i < ngroups; i += blockDim.x) unit0_s[i] = plan.g[i].unit0;
   if (threadIdx.x == 0) {
     int skip = read_status(args.status);
     if (kNarrow && plan.bn > 2 * R::BN_HALF && !skip) {  // the ring has no room for wider tiles
@@ -285,7 +293,7 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
       int s = 0;
       uint32_t ph = 0;
       for (int unit = cid; unit < total; unit += ncl) {
-        const Unit t = decode_unit<kNarrow>(plan, unit);
+        const Unit t = decode_unit<kNarrow>(plan, unit0_s, ngroups, unit);
         const GemmGroup& G = plan.g[t.group];
         const int nkb = (args.K[t.kind] + BK - 1) / BK;
         // one token box per CTA and k-block: 128 rows, or 32 rows when the
@@ -328,7 +336,7 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
       uint32_t acc_ph = 0;
       bool ok = true;
       for (int unit = cid; unit < total && ok; unit += ncl) {
-        const Unit t = decode_unit<kNarrow>(plan, unit);
+        const Unit t = decode_unit<kNarrow>(plan, unit0_s, ngroups, unit);
         const int nkb = (args.K[t.kind] + BK - 1) / BK;
         const uint32_t idesc = idesc_pair(t.n_mma);
         if (!wait_bar(smem_u32(&tail->tempty[acc]), acc_ph ^ 1, abort_flag, deadline, args.status)) { ok = false; break; }
@@ -370,7 +378,7 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
     int acc = 0;
     uint32_t acc_ph = 0;
     for (int unit = cid; unit < total; unit += ncl) {
-      const Unit t = decode_unit<kNarrow>(plan, unit);
+      const Unit t = decode_unit<kNarrow>(plan, unit0_s, ngroups, unit);
       const GemmGroup& G = plan.g[t.group];
       bool ok = wait_bar(smem_u32(&tail->tfull[acc]), acc_ph, abort_flag, deadline, args.status);
       ok = __all_sync(0xffffffffu, ok);

@@ -45,11 +45,16 @@ def test_all_peers_empty():
     dict(num_experts=8, topk=8, hidden=256, inter=96, shared_inter=96, seq_lens=[19, 1, 33]),
     dict(num_experts=16, topk=2, hidden=4096, inter=128, shared_inter=64, seq_lens=[33, 20]),
     dict(num_experts=64, topk=6, hidden=3072, inter=64, shared_inter=64, seq_lens=[25]),
-], ids=["E256_k16", "k_equals_E", "hidden4096", "hidden3072"])
+    # ~128 rows per expert take the 256-row tiles; hidden 320 and inter 176
+    # give odd k-block counts (5 and 3, the last one partial), so the pair
+    # GEMM's last stage carries a single k-block
+    dict(num_experts=8, topk=2, hidden=320, inter=176, shared_inter=80, seq_lens=[300, 212]),
+], ids=["E256_k16", "k_equals_E", "hidden4096", "hidden3072", "wide_odd_k"])
 def test_shapes_at_the_edges(shape):
     """Routing, plan and outputs against the oracle at the shapes' edges:
     256 experts with top-16 (the largest the router covers), top-k equal to
-    the expert count, hidden above 2048 (the router's fallback kernels)."""
+    the expert count, hidden above 2048 (the router's fallback kernels),
+    wide token tiles over odd and partial k-block counts."""
     w = W.custom("fanin", **shape)
     run = R.Runner(w, max_total_tokens=w.total_tokens)
     e, _ = G.run_and_compare_full(run)

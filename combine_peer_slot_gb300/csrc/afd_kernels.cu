@@ -150,20 +150,27 @@ __global__ void k_pack_header(uint8_t* win, WinGeom g, int region, int stage, in
 template <bool kFromHeaders>
 __device__ bool check_entries(const uint8_t* win, const WinGeom& g, const FanIn& f, const DevWS& ws,
                               int E, int token_cap, int rows_cap, int has_shared_expert,
-                              int64_t timeout_ns, int item_err) {
+                              int64_t timeout_ns, int item_err, bool check_status) {
   __shared__ int err[AFD_MAX_PEERS];
   __shared__ int bad_sidx[AFD_MAX_PEERS];
   __shared__ int shared_n[AFD_MAX_PEERS];
+  __shared__ int skip;
   const int tid = threadIdx.x;
+  // each entry's first flag poll is issued with the status word's load
+  const int slotno = tid < f.n_peers ? f.region[tid] * g.ring_depth + f.stage : 0;
+  const uint64_t* flagp = reinterpret_cast<const uint64_t*>(win) + slotno;
+  uint64_t seen = 0, fl = 0;
+  if (tid < f.n_peers) {
+    seen = ws.seen[slotno];
+    fl = ld_acquire_u64(flagp);
+  }
+  if (tid == 0) skip = check_status ? read_status(ws.status) : 0;
   if (tid < AFD_MAX_PEERS) { err[tid] = 0; bad_sidx[tid] = 0; shared_n[tid] = 0; }
   __syncthreads();
+  if (skip) return false;
   if (tid < f.n_peers) {
     const int i = tid;
-    const int slotno = f.region[i] * g.ring_depth + f.stage;
-    const uint64_t* flagp = reinterpret_cast<const uint64_t*>(win) + slotno;
-    const uint64_t seen = ws.seen[slotno];
     const uint64_t t0 = globaltimer_ns();
-    uint64_t fl = ld_acquire_u64(flagp);
     unsigned backoff = 32;
     int e = 0;
     while (fl <= seen) {
@@ -305,12 +312,7 @@ k_header_check(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn f, D
                int token_cap, int rows_cap, int has_shared_expert, int64_t timeout_ns) {
   grid_dep_wait();
   grid_dep_launch();
-  __shared__ int skip;
-  const int tid = threadIdx.x;
-  if (tid == 0) skip = read_status(ws.status);
-  __syncthreads();
-  if (skip) return;
-  check_entries<false>(win, g, f, ws, E, token_cap, rows_cap, has_shared_expert, timeout_ns, 0);
+  check_entries<false>(win, g, f, ws, E, token_cap, rows_cap, has_shared_expert, timeout_ns, 0, true);
 }
 
 // ---------------------------------------------------------------------------
@@ -410,7 +412,7 @@ k_item_head(const uint8_t* win, WinGeom g, PeerList pl, DevWS ws, int E, int tok
   }
   __syncthreads();
   if (!check_entries<true>(win, g, fs, ws, E, token_cap, rows_cap, has_shared_expert, timeout_ns,
-                           item_err))
+                           item_err, false))
     return;
   {
     const int32_t* src = reinterpret_cast<const int32_t*>(&fs);
@@ -1110,16 +1112,21 @@ k_router_topk(const __grid_constant__ FanIn fp, DevWS ws, const float* __restric
   grid_dep_launch();
   const FanIn& f = step_item<kDev>(fp, ws.item);
   __shared__ int hs[256];
-  if (read_status(ws.status)) return;
+  __shared__ int skip;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kRtTok + warp;
+  // the token's logits are loaded with the status word (in bounds either way)
+  float lv[8];  // logit of expert lane + 32m
+  {
+    const float* l = logits + (int64_t)min(t, f.total - 1) * E;
+#pragma unroll
+    for (int m = 0; m < 8; m++) lv[m] = (t < f.total && m * 32 + lane < E) ? l[m * 32 + lane] : -INFINITY;
+  }
+  if (threadIdx.x == 0) skip = read_status(ws.status);
   for (int e = threadIdx.x; e < E; e += blockDim.x) hs[e] = 0;
   __syncthreads();
-  const int t = blockIdx.x * kRtTok + warp;
+  if (skip) return;
   if (t < f.total) {
-    const float* l = logits + (int64_t)t * E;
-    float lv[8];  // logit of expert lane + 32m
-#pragma unroll
-    for (int m = 0; m < 8; m++) lv[m] = (m * 32 + lane < E) ? l[m * 32 + lane] : -INFINITY;
     uint32_t taken = 0;  // bit m: expert lane + 32m chosen (E <= 256)
     float top_logit = 0.0f;
     int my_id = 0;       // lane j keeps the j-th choice
@@ -1174,75 +1181,99 @@ k_router_topk(const __grid_constant__ FanIn fp, DevWS ws, const float* __restric
 // segment (base[b][e] = sum of hist[b'][e] for b' < b), the zeroed per-peer
 // counts, and the tile tables of both grouped GEMMs.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ int warp_incl_scan(int v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
 // Tile tables of both grouped GEMMs from the per-expert counts and offsets:
 // one group per expert (rows = its partials, in permuted order), then the
 // shared expert over all T rows; tile0 / unit0 are prefixes of the one-CTA
 // tiles and of the SM-pair units.
+// Called by one whole warp: lane l takes a contiguous run of at most
+// ceil(E / 32) experts (<= 8), and every group's first tile and unit are
+// warp prefix sums, so the tables equal those of a walk in group order.
 __device__ void write_tile_tables(const FanIn& f, const DevWS& ws, const WinGeom& g, int row_bytes,
                                   int k, int E, int inter, int shared_inter, int hidden,
                                   int has_shared, int sh_in_place, int bn, const int* cnt,
                                   const int* offs, GemmPlan* plan1, GemmPlan* plan2) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lt_mask = (1u << lane) - 1u;
   const int N = f.grouped ? f.rtotal : f.total * k;  // routed rows (Xp rows 0..N-1)
-  int tiles1 = 0, tiles2 = 0, units1 = 0, units2 = 0, ng = 0;
   const int mt1 = (inter + 63) / 64, mt2 = (hidden + 127) / 128;
-  for (int e = 0; e < E; e++, ng++) {
+  const int u1_per = (mt1 + 1) / 2, u2_per = (mt2 + 1) / 2;
+  const int epl = (E + 31) / 32;
+  const int e0 = min(E, lane * epl), e1 = min(E, e0 + epl);
+  int nts = 0;  // token tiles of this lane's experts
+  for (int e = e0; e < e1; e++) nts += (cnt[e] + bn - 1) / bn;
+  const int nts_incl = warp_incl_scan(nts, lane);
+  int nt_run = nts_incl - nts;  // token tiles of the experts before this lane's
+  for (int e = e0; e < e1; e++) {
     const int rows = cnt[e];
     const int nt = (rows + bn - 1) / bn;
-    GemmGroup a{rows, offs[e], offs[e], e, 0, mt1, nt, tiles1, units1};
-    GemmGroup b{rows, offs[e], offs[e], e, 0, mt2, nt, tiles2, units2};
-    plan1->g[ng] = a;
-    plan2->g[ng] = b;
-    tiles1 += mt1 * nt;
-    tiles2 += mt2 * nt;
-    units1 += (mt1 + 1) / 2 * nt;
-    units2 += (mt2 + 1) / 2 * nt;
+    plan1->g[e] = GemmGroup{rows, offs[e], offs[e], e, 0, mt1, nt, mt1 * nt_run, u1_per * nt_run};
+    plan2->g[e] = GemmGroup{rows, offs[e], offs[e], e, 0, mt2, nt, mt2 * nt_run, u2_per * nt_run};
+    nt_run += nt;
   }
+  const int nt_all = __shfl_sync(0xffffffffu, nts_incl, 31);
+  int tiles1 = mt1 * nt_all, tiles2 = mt2 * nt_all, units1 = u1_per * nt_all, units2 = u2_per * nt_all;
+  int ng = E;
   // the shared expert: one group over the gathered shared rows (Xp rows
   // N..), or one group per entry that sent shared rows, read in place from
   // its slot's shared_x (window rows); outputs at the shared-row offsets
+  const int mts = (shared_inter + 63) / 64;
+  const int us_per = (mts + 1) / 2;
   if (has_shared && !sh_in_place) {
     const int rows = f.stotal;
     const int nt = (rows + bn - 1) / bn;
-    const int mts = (shared_inter + 63) / 64;
-    GemmGroup a{rows, N, 0, 0, 1, mts, nt, tiles1, units1};
-    GemmGroup b{rows, 0, 0, 0, 1, mt2, nt, tiles2, units2};
-    plan1->g[ng] = a;
-    plan2->g[ng] = b;
+    if (lane == 0) {
+      plan1->g[ng] = GemmGroup{rows, N, 0, 0, 1, mts, nt, tiles1, units1};
+      plan2->g[ng] = GemmGroup{rows, 0, 0, 0, 1, mt2, nt, tiles2, units2};
+    }
     tiles1 += mts * nt;
     tiles2 += mt2 * nt;
-    units1 += (mts + 1) / 2 * nt;
-    units2 += (mt2 + 1) / 2 * nt;
+    units1 += us_per * nt;
+    units2 += u2_per * nt;
     ng++;
   }
   if (has_shared && sh_in_place) {
-    int srows[AFD_MAX_PEERS];  // all loads before the table's stores
-    for (int i = 0; i < f.n_peers; i++)
-      srows[i] = ws.peer_shared[i] ? f.sprefix[i + 1] - f.sprefix[i] : 0;
-    for (int i = 0; i < f.n_peers; i++) {
-      const int rows = srows[i];
-      if (!rows) continue;
+    for (int r0 = 0; r0 < f.n_peers; r0 += 32) {  // entries in rounds of 32, in list order
+      const int i = r0 + lane;
+      const int rows = (i < f.n_peers && ws.peer_shared[i]) ? f.sprefix[i + 1] - f.sprefix[i] : 0;
+      const unsigned has = __ballot_sync(0xffffffffu, rows > 0);
       const int nt = (rows + bn - 1) / bn;
-      const int mts = (shared_inter + 63) / 64;
-      const int wr = window_row(g, f.region[i], f.stage, g.shared_x, 0, row_bytes);
-      GemmGroup a{rows, wr, f.sprefix[i], 0, 1, mts, nt, tiles1, units1};
-      GemmGroup b{rows, f.sprefix[i], f.sprefix[i], 0, 1, mt2, nt, tiles2, units2};
-      plan1->g[ng] = a;
-      plan2->g[ng] = b;
-      tiles1 += mts * nt;
-      tiles2 += mt2 * nt;
-      units1 += (mts + 1) / 2 * nt;
-      units2 += (mt2 + 1) / 2 * nt;
-      ng++;
+      const int nt_incl = warp_incl_scan(nt, lane);
+      const int nt_before = nt_incl - nt;
+      if (rows > 0) {
+        const int gi = ng + __popc(has & lt_mask);
+        const int wr = window_row(g, f.region[i], f.stage, g.shared_x, 0, row_bytes);
+        plan1->g[gi] = GemmGroup{rows, wr, f.sprefix[i], 0, 1, mts, nt, tiles1 + mts * nt_before,
+                                 units1 + us_per * nt_before};
+        plan2->g[gi] = GemmGroup{rows, f.sprefix[i], f.sprefix[i], 0, 1, mt2, nt,
+                                 tiles2 + mt2 * nt_before, units2 + u2_per * nt_before};
+      }
+      const int nt_round = __shfl_sync(0xffffffffu, nt_incl, 31);
+      tiles1 += mts * nt_round;
+      tiles2 += mt2 * nt_round;
+      units1 += us_per * nt_round;
+      units2 += u2_per * nt_round;
+      ng += __popc(has);
     }
   }
-  plan1->ngroups = ng;
-  plan2->ngroups = ng;
-  plan1->total_tiles = tiles1;
-  plan2->total_tiles = tiles2;
-  plan1->total_units = units1;
-  plan2->total_units = units2;
-  plan1->bn = bn;
-  plan2->bn = bn;
+  if (lane == 0) {
+    plan1->ngroups = ng;
+    plan2->ngroups = ng;
+    plan1->total_tiles = tiles1;
+    plan2->total_tiles = tiles2;
+    plan1->total_units = units1;
+    plan2->total_units = units2;
+    plan1->bn = bn;
+    plan2->bn = bn;
+  }
 }
 
 constexpr int kScanWarps = 32;
@@ -1313,7 +1344,7 @@ k_plan_scan(const __grid_constant__ FanIn fp, DevWS ws, int E, int k, int inter,
     ws.offsets[e] = offs[e];
     if (e < E) ws.counts[e] = cnt[e];
   }
-  if (tid == 0)
+  if (tid < 32)
     write_tile_tables(f, ws, g, row_bytes, k, E, inter, shared_inter, hidden, has_shared,
                       sh_in_place, bn, cnt, offs, plan1, plan2);
 }
@@ -1325,6 +1356,7 @@ k_plan_scan(const __grid_constant__ FanIn fp, DevWS ws, int E, int k, int inter,
 // expert; 32-element rounds are ranked with match_any) and the tile tables.
 // ---------------------------------------------------------------------------
 constexpr int kPlanSmallMax = 8192;
+constexpr int kPlanPerLane = kPlanSmallMax / 1024;  // ids per lane: a warp's chunk is <= 256
 
 template <bool kDev>
 __global__ void __launch_bounds__(1024)
@@ -1339,23 +1371,35 @@ k_plan_small(const __grid_constant__ FanIn fp, DevWS ws, int E, int k, int inter
   __shared__ int offs[257];
   __shared__ int skip;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int N = f.total * k;
+  const int chunk = (N + 31) / 32;
+  const int c0 = min(N, warp * chunk), c1 = min(N, c0 + chunk);
+  const int nr = (c1 - c0 + 31) / 32;  // 32-entry rounds of this warp (<= kPlanPerLane)
+  // the warp's expert ids, loaded once (one round trip, the status word's
+  // load alongside) and kept in registers for both passes
+  int ev[kPlanPerLane];
+#pragma unroll
+  for (int j = 0; j < kPlanPerLane; j++) {
+    const int fi = c0 + 32 * j + lane;
+    ev[j] = fi < c1 ? ws.ids[fi] : 0;
+  }
   if (tid == 0) skip = read_status(ws.status);
   for (int i = tid; i < 32 * 256; i += blockDim.x) (&hist_w[0][0])[i] = 0;
   for (int i = tid; i < f.n_peers * E; i += blockDim.x) ws.peer_counts[i] = 0;
   __syncthreads();
   if (skip) return;
-  const int N = f.total * k;
-  const int chunk = (N + 31) / 32;
-  const int c0 = min(N, warp * chunk), c1 = min(N, c0 + chunk);
-  for (int fi = c0 + lane; fi < c1; fi += 32) {
-    int e = ws.ids[fi];
-    if (e < 0 || e >= E) {  // cannot come from the router; keep every index in range
-      set_error(ws.status, AFD_ERR_SHAPE);
-      e = 0;
-      ws.ids[fi] = 0;
+#pragma unroll
+  for (int j = 0; j < kPlanPerLane; j++) {
+    const int fi = c0 + 32 * j + lane;
+    if (fi < c1) {
+      if (ev[j] < 0 || ev[j] >= E) {  // cannot come from the router; keep every index in range
+        set_error(ws.status, AFD_ERR_SHAPE);
+        ev[j] = 0;
+        ws.ids[fi] = 0;
+      }
+      atomicAdd(&hist_w[warp][ev[j]], 1);
+      atomicAdd(&ws.peer_counts[entry_of(f, fi / k) * E + ev[j]], 1);
     }
-    atomicAdd(&hist_w[warp][e], 1);
-    atomicAdd(&ws.peer_counts[entry_of(f, fi / k) * E + e], 1);
   }
   __syncthreads();
   for (int e = tid; e < E; e += blockDim.x) {
@@ -1364,10 +1408,15 @@ k_plan_small(const __grid_constant__ FanIn fp, DevWS ws, int E, int k, int inter
     cnt[e] = c;
   }
   __syncthreads();
-  if (tid == 0) {
-    int run = 0;
-    for (int e = 0; e < E; e++) { offs[e] = run; run += cnt[e]; }
-    offs[E] = run;
+  if (warp == 0) {  // exclusive offsets: lane l scans a run of <= 8 experts
+    const int epl = (E + 31) / 32;
+    const int e0 = min(E, lane * epl), e1 = min(E, e0 + epl);
+    int sum = 0;
+    for (int e = e0; e < e1; e++) sum += cnt[e];
+    const int incl = warp_incl_scan(sum, lane);
+    int run = incl - sum;
+    for (int e = e0; e < e1; e++) { offs[e] = run; run += cnt[e]; }
+    if (lane == 31) offs[E] = incl;
   }
   __syncthreads();
   for (int e = tid; e < E; e += blockDim.x) {
@@ -1383,24 +1432,29 @@ k_plan_small(const __grid_constant__ FanIn fp, DevWS ws, int E, int k, int inter
     if (e < E) ws.counts[e] = cnt[e];
   }
   __syncthreads();
+  // stable ranks: rounds of 32 entries in order, ties within a round ranked
+  // by lane (match_any)
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int g0 = c0; g0 < c1; g0 += 32) {
-    const int fi = g0 + lane;
-    const bool ok = fi < c1;
-    const int e = ok ? ws.ids[fi] : -1 - lane;
-    const unsigned same = __match_any_sync(0xffffffffu, e);
-    const int rank = __popc(same & lt_mask);
-    int pos = 0;
-    if (ok) pos = hist_w[warp][e] + rank;
-    __syncwarp();
-    if (ok && rank == 0) hist_w[warp][e] += __popc(same);
-    __syncwarp();
-    if (ok) {
-      ws.perm[pos] = fi;
-      ws.inv[fi] = pos;
+#pragma unroll
+  for (int j = 0; j < kPlanPerLane; j++) {
+    if (j < nr) {
+      const int fi = c0 + 32 * j + lane;
+      const bool ok = fi < c1;
+      const int e = ok ? ev[j] : -1 - lane;
+      const unsigned same = __match_any_sync(0xffffffffu, e);
+      const int rank = __popc(same & lt_mask);
+      int pos = 0;
+      if (ok) pos = hist_w[warp][e] + rank;
+      __syncwarp();
+      if (ok && rank == 0) hist_w[warp][e] += __popc(same);
+      __syncwarp();
+      if (ok) {
+        ws.perm[pos] = fi;
+        ws.inv[fi] = pos;
+      }
     }
   }
-  if (tid == 0)
+  if (tid < 32)
     write_tile_tables(f, ws, g, row_bytes, k, E, inter, shared_inter, hidden, has_shared,
                       sh_in_place, bn, cnt, offs, plan1, plan2);
 }
@@ -1462,7 +1516,7 @@ k_plan_grouped(const __grid_constant__ FanIn fp, DevWS ws, int E, int inter, int
   }
   __syncthreads();
   if (!in_place) {  // the gather places each row (and records perm / inv)
-    if (tid == 0)
+    if (tid < 32)
       write_tile_tables(f, ws, g, row_bytes, 1, E, inter, shared_inter, hidden, has_shared,
                         sh_in_place, bn, cnt, offs, plan1, plan2);
     return;

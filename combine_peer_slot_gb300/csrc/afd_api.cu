@@ -26,6 +26,9 @@ struct LayerW {
   const void* W13s = nullptr;
   const void* Wds = nullptr;
   float* WgQ = nullptr;              // library-owned rearranged router weight
+  // library-owned tiled copies for the tensor engines: W13, Wd, W13_s, Wd_s
+  void* T[4] = {nullptr, nullptr, nullptr, nullptr};
+  size_t T_bytes[4] = {0, 0, 0, 0};
   CUtensorMap tmA1[2];               // SwiGLU projection: routed, shared
   CUtensorMap tmA2[2];               // down projection: routed, shared
 };
@@ -65,21 +68,15 @@ int encode_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dim
   return AFD_OK;
 }
 
-// [E][2I][H] viewed as (h, r16, s, j, e): one box = 4 x (16 gate rows, 16 up rows)
-int encode_swiglu_weight(CUtensorMap* m, const void* W, int E, int I, int H) {
-  const cuuint64_t dims[5] = {(cuuint64_t)H, 16, 2, (cuuint64_t)(I / 16), (cuuint64_t)E};
-  const cuuint64_t str[4] = {(cuuint64_t)H * 2, (cuuint64_t)I * H * 2, (cuuint64_t)16 * H * 2,
-                             (cuuint64_t)2 * I * H * 2};
-  const cuuint32_t box[5] = {64, 16, 2, 4, 1};
-  return encode_map(m, W, 5, dims, str, box);
-}
-
-// [E][M][K] K-major, box 64 x 128
-int encode_plain_weight(CUtensorMap* m, const void* W, int E, int M, int K) {
-  const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)M, (cuuint64_t)E};
-  const cuuint64_t str[2] = {(cuuint64_t)K * 2, (cuuint64_t)M * K * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
-  return encode_map(m, W, 3, dims, str, box);
+// A tiled weight copy [E][tiles][k-blocks][128 rows][64 columns] as a 5-D
+// map (column, row, k-block, tile, expert); one box = one 16 KB block, so a
+// load's coordinates are (0, 0, k-block, 128-row tile, expert)
+int encode_tiled_weight(CUtensorMap* m, const void* T, int E, int tiles, int K) {
+  const cuuint64_t nkb = (cuuint64_t)((K + 63) / 64);
+  const cuuint64_t dims[5] = {64, 128, nkb, (cuuint64_t)tiles, (cuuint64_t)E};
+  const cuuint64_t str[4] = {128, 128 * 128, nkb * 16384, (cuuint64_t)tiles * nkb * 16384};
+  const cuuint32_t box[5] = {64, 128, 1, 1, 1};
+  return encode_map(m, T, 5, dims, str, box);
 }
 
 // [rows][K] token rows, box 64 x box_rows
@@ -302,7 +299,10 @@ void afd_destroy(afd_ctx* ctx) {
   }
   if (ctx->ev_fork) cudaEventDestroy(ctx->ev_fork);
   if (ctx->ev_join) cudaEventDestroy(ctx->ev_join);
-  for (auto& l : ctx->layers) cudaFree(l.WgQ);
+  for (auto& l : ctx->layers) {
+    cudaFree(l.WgQ);
+    for (void* t : l.T) cudaFree(t);
+  }
   for (auto& set : ctx->ev)
     for (auto& e : set)
       if (e) cudaEventDestroy(e);
@@ -453,13 +453,17 @@ int afd_set_layer(afd_ctx* ctx, int layer, const float* Wg, const float* bias, c
   }
   LayerW& L = ctx->layers[layer];
   int rc = AFD_OK;
+  // the copies below replace what a forward still in flight may read: no
+  // overlap with earlier work on the stream
+  LaunchCtx lc = ctx->lc();
+  lc.pdl = 0;
   if (Wg) {
     if (!L.WgQ) {
       rc = cuda_fail(cudaMalloc(&L.WgQ, (size_t)wgq_groups(c.num_experts) * c.hidden * 16),
                      "router copy");
       if (rc) return rc;
     }
-    rc = cuda_fail(launch_arrange_wg(ctx->lc(), Wg, L.WgQ, c.hidden, c.num_experts), "router copy");
+    rc = cuda_fail(launch_arrange_wg(lc, Wg, L.WgQ, c.hidden, c.num_experts), "router copy");
     if (rc) return rc;
   }
   L.Wg = Wg;
@@ -469,16 +473,40 @@ int afd_set_layer(afd_ctx* ctx, int layer, const float* Wg, const float* bias, c
   L.W13s = has_shared ? W13_s : nullptr;
   L.Wds = has_shared ? Wd_s : nullptr;
   if (c.gemm != AFD_GEMM_SIMT) {
-    rc = encode_swiglu_weight(&L.tmA1[0], W13, c.num_experts, c.inter, c.hidden);
-    if (!rc) rc = encode_plain_weight(&L.tmA2[0], Wd, c.num_experts, c.hidden, c.inter);
-    if (!rc && has_shared) {
-      rc = encode_swiglu_weight(&L.tmA1[1], W13_s, 1, c.shared_inter, c.hidden);
-      if (!rc) rc = encode_plain_weight(&L.tmA2[1], Wd_s, 1, c.hidden, c.shared_inter);
-    } else if (!rc) {
+    // the tensor engines read tiled copies (one contiguous 16 KB block per
+    // TMA box); the caller's buffers are not read after this call returns
+    struct Src { const void* W; int E, M, K, swiglu, I; };
+    const Src src[4] = {{W13, c.num_experts, 2 * c.inter, c.hidden, 1, c.inter},
+                        {Wd, c.num_experts, c.hidden, c.inter, 0, 0},
+                        {W13_s, 1, 2 * c.shared_inter, c.hidden, 1, c.shared_inter},
+                        {Wd_s, 1, c.hidden, c.shared_inter, 0, 0}};
+    CUtensorMap* maps[4] = {&L.tmA1[0], &L.tmA2[0], &L.tmA1[1], &L.tmA2[1]};
+    for (int w = 0; w < (has_shared ? 4 : 2) && !rc; w++) {
+      const Src& q = src[w];
+      const int tiles = tiled_weight_tiles(q.M, q.swiglu, q.I);
+      const size_t bytes = (size_t)q.E * tiles * ((q.K + 63) / 64) * 16384;
+      if (L.T_bytes[w] != bytes) {
+        cudaFree(L.T[w]);
+        L.T[w] = nullptr;
+        L.T_bytes[w] = 0;
+        rc = cuda_fail(cudaMalloc(&L.T[w], bytes), "weight copy");
+        if (rc) break;
+        L.T_bytes[w] = bytes;
+      }
+      rc = cuda_fail(launch_tile_weight(lc, q.W, L.T[w], q.E, q.M, q.K, q.swiglu, q.I), "weight copy");
+      if (!rc) rc = encode_tiled_weight(maps[w], L.T[w], q.E, tiles, q.K);
+    }
+    if (!rc && !has_shared) {
       L.tmA1[1] = L.tmA1[0];
       L.tmA2[1] = L.tmA2[0];
     }
+    if (!rc) rc = cuda_fail(cudaStreamSynchronize(ctx->stream), "weight copy");
     if (rc) return rc;
+    // what the engines (and the decode L2 prefetch) read
+    L.W13 = L.T[0];
+    L.Wd = L.T[1];
+    L.W13s = has_shared ? L.T[2] : nullptr;
+    L.Wds = has_shared ? L.T[3] : nullptr;
   }
   // the device table entry, for steps whose layer the device chooses (a
   // pageable source: the copy is staged before the call returns)

@@ -9,13 +9,16 @@
 // Projections (Async GPU Connector, "Attention gate and FFN expert compute":
 // fused_experts = gate/up GEMM, SiLU-and-multiply, down GEMM; Async AFD for
 // Prefill on Ascend NPU, "Architecture": W1 with SwiGLU, then W2):
-//  - SwiGLU mode: a 5-D tensor map views W13[e] = [gate rows | up rows] as
-//    (h, r in 16, s in {gate, up}, j, e), so one TMA box lands 16 gate rows
+// The weights are read from the library's tiled copies: every 128-row x
+// 64-column TMA box is one contiguous 16 KB block, addressed by a 5-D map as
+// (0, 0, k-block, 128-row tile, expert).
+//  - SwiGLU mode: a tile of W13[e] = [gate rows | up rows] holds 16 gate rows
 //    then the 16 matching up rows, four times: 128 rows covering 64
 //    intermediate columns.  In TMEM, warp quadrant q holds gate rows in
 //    lanes 0-15 and the matching up rows in lanes 16-31; a shuffle pairs
 //    them and h = silu(g) * u is written as bf16.
-//  - plain mode: y = h . Wd^T with Wd[e] = [hidden, inter] as a 3-D map.
+//  - plain mode: y = h . Wd^T with Wd[e] = [hidden, inter], tiles of 128
+//    hidden rows in order.
 //
 // Warp roles (320 threads, one CTA per SM, persistent over the tile table
 // built on the device from the expert counts):
@@ -203,10 +206,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_gemm_tc(const __grid_constan
           const uint32_t sa = smem_base + s * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
           mbar_expect_tx(full, A_BYTES + nb * B_BOX_BYTES);
-          if (args.swiglu)
-            tma_load_5d(sa, ta, kb * BK, 0, 0, t.mt * 4, G.a_idx, full);
-          else
-            tma_load_3d(sa, ta, kb * BK, t.mt * BM, G.a_idx, full);
+          // weights: the tiled copy's 16 KB block (k-block, 128-row tile, expert)
+          tma_load_5d(sa, ta, 0, 0, kb, t.mt, G.a_idx, full);
           for (int q = 0; q < nb; q++)
             tma_load_2d(sb + q * B_BOX_BYTES, tb, kb * BK, brow + q * B_BOX_ROWS, full);
           pending |= 1u << s;

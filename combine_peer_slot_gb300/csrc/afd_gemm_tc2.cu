@@ -9,9 +9,10 @@
 // all N tokens.  Per SM and 64-wide k-block the ring takes 16 KB of weights
 // and 16 KB of tokens (one CTA alone would take 16 + 32 KB for the same
 // MMA work), so six k-blocks fit in flight and each SM fills and reads a
-// third less shared memory.  Projections and epilogues are those of afd_gemm_tc.cu
-// (Async GPU Connector, "Attention gate and FFN expert compute": fused_experts
-// gate/up GEMM, SiLU-and-multiply, down GEMM).
+// third less shared memory.  Weights come from the library's tiled copies
+// (one contiguous 16 KB block per 128 x 64 box).  Projections and epilogues
+// are those of afd_gemm_tc.cu (Async GPU Connector, "Attention gate and FFN
+// expert compute": fused_experts gate/up GEMM, SiLU-and-multiply, down GEMM).
 //
 // Signalling (all waits bounded):
 //   full[s]   leader only: one arrive + the bytes of both CTAs' copies (the
@@ -113,13 +114,6 @@ __device__ __forceinline__ void tma2_load_2d(uint32_t dst, const CUtensorMap* tm
   asm volatile(
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
       ::"r"(dst), "l"(tm), "r"(c0), "r"(c1), "r"(bar_cluster)
-      : "memory");
-}
-__device__ __forceinline__ void tma2_load_3d(uint32_t dst, const CUtensorMap* tm, int c0, int c1, int c2,
-                                             uint32_t bar_cluster) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
-      ::"r"(dst), "l"(tm), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster)
       : "memory");
 }
 __device__ __forceinline__ void tma2_load_5d(uint32_t dst, const CUtensorMap* tm, int c0, int c1, int c2,
@@ -320,10 +314,8 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
           const uint32_t sb = sa + R::KPS * A_BYTES;
           for (int j = 0; j < cnt; j++) {
             const int kc = (kb + j) * BK;
-            if (args.swiglu)
-              tma2_load_5d(sa + j * A_BYTES, ta, kc, 0, 0, mt * 4, G.a_idx, full_leader);
-            else
-              tma2_load_3d(sa + j * A_BYTES, ta, kc, mt * BM, G.a_idx, full_leader);
+            // weights: the tiled copy's 16 KB block (k-block, 128-row tile, expert)
+            tma2_load_5d(sa + j * A_BYTES, ta, 0, 0, kb + j, mt, G.a_idx, full_leader);
             tma2_load_2d(sb + j * R::B_BYTES, tb, kc, brow, full_leader);
           }
           if (++s == STAGES) { s = 0; ph ^= 1; }

@@ -257,13 +257,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
       ::"r"(dst), "l"(tm), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
 }
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
-                                            int c2, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
-      ::"r"(dst), "l"(tm), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-      : "memory");
-}
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
                                             int c2, int c3, int c4, uint32_t bar) {
   asm volatile(
@@ -428,5 +421,10 @@ cudaError_t launch_scatter_grouped(const LaunchCtx& lc, const WinGeom& g, uint8_
 // of the layer in ws.item (nothing when the step has no routed rows)
 cudaError_t launch_prefetch_l2(const LaunchCtx& lc, const void* base, int64_t bytes,
                                const DevWS& ws);
+// 128-row weight tiles of a tensor-engine weight copy, and the copy itself
+// ([E][tiles][k-blocks] blocks of 128 x 64 bf16; see k_tile_weight)
+int tiled_weight_tiles(int M, int swiglu, int I);
+cudaError_t launch_tile_weight(const LaunchCtx& lc, const void* W, void* T, int E, int M, int K, int swiglu,
+                               int I);
 cudaError_t launch_arrange_wg(const LaunchCtx& lc, const float* Wg, float* WgQ, int hidden,
                                 int E);

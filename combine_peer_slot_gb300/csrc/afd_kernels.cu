@@ -2065,6 +2065,50 @@ __global__ void k_prefetch_l2(const uint8_t* base, int64_t bytes, DevWS ws) {
   }
 }
 
+// Expert weights re-laid for the tensor engines: each 128-row x 64-column
+// block (one TMA box, one k-block of one 128-row weight tile) becomes 16
+// contiguous KB, ordered [expert][row tile][k-block], so a tile's k-blocks
+// stream from HBM as one contiguous run.  Row r of a tile of the gate/up
+// weight [E][2I][K] (swiglu) holds inter column 64 t + 16 (r / 32) + r % 16
+// of the gate (r / 16 even) or up (odd) rows, the order in which the
+// epilogue pairs them; the down weight [E][M][K] keeps its row order (row
+// 128 t + r).  Rows and columns past the weight are zero (what the TMA's
+// out-of-bounds fill gave on the plain layout).
+__global__ void k_tile_weight(const uint16_t* __restrict__ src, uint4* __restrict__ dst, int E, int M, int K,
+                              int swiglu, int I, int mtiles) {
+  const int nkb = (K + 63) / 64;
+  const int64_t total = (int64_t)E * mtiles * nkb * 128 * 8;  // 16-byte pieces
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int piece = (int)(i % 8);
+    int64_t r = i / 8;
+    const int row = (int)(r % 128);
+    r /= 128;
+    const int kb = (int)(r % nkb);
+    r /= nkb;
+    const int t = (int)(r % mtiles);
+    const int e = (int)(r / mtiles);
+    int srow;
+    bool ok;
+    if (swiglu) {
+      const int j = 4 * t + row / 32;  // 16-column group of the inter dimension
+      ok = j < I / 16;
+      srow = ((row / 16) & 1) * I + 16 * j + row % 16;
+    } else {
+      srow = 128 * t + row;
+      ok = srow < M;
+    }
+    uint16_t v[8];
+#pragma unroll
+    for (int q = 0; q < 8; q++) {
+      const int k = 64 * kb + 8 * piece + q;
+      v[q] = (ok && k < K) ? src[((int64_t)e * M + srow) * K + k] : (uint16_t)0;
+    }
+    dst[i] = make_uint4(v[0] | ((uint32_t)v[1] << 16), v[2] | ((uint32_t)v[3] << 16),
+                        v[4] | ((uint32_t)v[5] << 16), v[6] | ((uint32_t)v[7] << 16));
+  }
+}
+
 // The router weight [hidden][E] rearranged for the logits kernels as
 // WgQ[E/4 groups][hidden][4 experts] fp32 (experts past E are zero): a lane
 // reads the 4 weights of its h for a group of experts with one 16-byte load.
@@ -2376,6 +2420,16 @@ cudaError_t launch_item_head(const LaunchCtx& lc, const WinGeom& g, const uint8_
   return launch_k(lc, k_item_head, 1, 1024, 0, win, g, pl, ws, num_experts, token_cap, rows_cap,
                   ffn_rank, ffn_size, has_shared_expert, grouped, tmax, rmax, max_layers,
                   timeout_ns);
+}
+
+int tiled_weight_tiles(int M, int swiglu, int I) { return swiglu ? (I / 16 + 3) / 4 : (M + 127) / 128; }
+
+cudaError_t launch_tile_weight(const LaunchCtx& lc, const void* W, void* T, int E, int M, int K, int swiglu,
+                               int I) {
+  const int mtiles = tiled_weight_tiles(M, swiglu, I);
+  const int64_t pieces = (int64_t)E * mtiles * ((K + 63) / 64) * 128 * 8;
+  return launch_k(lc, k_tile_weight, grid_for(pieces, kThreads, 4096), kThreads, 0,
+                  static_cast<const uint16_t*>(W), static_cast<uint4*>(T), E, M, K, swiglu, I, mtiles);
 }
 
 cudaError_t launch_arrange_wg(const LaunchCtx& lc, const float* Wg, float* WgQ, int hidden,

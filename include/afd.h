@@ -232,11 +232,18 @@ int afd_split_sizes(int total, int n_peers, const int* seq_lens, int n_lens, int
  *   Wd   act [E, hidden, inter]
  *   W13_s act [2*shared_inter, hidden], Wd_s act [hidden, shared_inter]
  *        (both NULL when shared_inter == 0)
- * All device pointers, caller-owned, must stay valid while the layer is
- * used; 16-byte aligned.  The library keeps an fp32 copy of Wg rearranged
- * as [ceil(E / 4)][hidden][4 experts] (the only weight copy) and the TMA
- * descriptors.  Errors: AFD_ERR_ARG,
- * AFD_ERR_NOT_DEVICE, AFD_ERR_CUDA. */
+ * All device pointers, caller-owned, 16-byte aligned.  The library keeps an
+ * fp32 copy of Wg rearranged as [ceil(E / 4)][hidden][4 experts] and, for
+ * the tensor engines (cfg.gemm != AFD_GEMM_SIMT), copies of W13, Wd, W13_s
+ * and Wd_s re-laid as [E][128-row tiles][64-column k-blocks] blocks of
+ * 128 x 64 (16 contiguous KB, the unit one TMA load reads; zero past the
+ * weight's edges; within a W13 tile, 16 gate rows then the 16 matching up
+ * rows, four times).  The call returns once the copies are complete, so
+ * with a tensor engine the caller's expert weights may then be freed;
+ * with AFD_GEMM_SIMT they are read in place and must stay valid while the
+ * layer is used (Wg need not: it is copied in both cases).  Registering a
+ * layer again replaces its copies in place, ordered after the forwards
+ * already enqueued.  Errors: AFD_ERR_ARG, AFD_ERR_NOT_DEVICE, AFD_ERR_CUDA. */
 int afd_set_layer(afd_ctx* ctx, int layer, const float* Wg, const float* bias,
                   const void* W13, const void* Wd, const void* W13_s, const void* Wd_s);
 

@@ -32,6 +32,38 @@ def test_fanin_bf16(gemm):
     print("fanin max|err|/rms", e)
 
 
+@pytest.mark.parametrize("gemm", [A.AFD_GEMM_TENSOR, A.AFD_GEMM_TENSOR_1CTA],
+                         ids=["tcgen05_pair", "tcgen05_1cta"])
+def test_weights_copied_at_registration(gemm):
+    """The tensor engines read the library's tiled weight copies: the
+    caller's expert weights overwritten with NaN once afd_set_layer has
+    returned leave every result as the oracle gives it on the original
+    weights; a second registration of the same layer (same sizes, copies
+    reused) then takes the new values."""
+    w = W.get("fanin")
+    run = R.Runner(w, gemm=gemm)
+    snap = run.weights_numpy(0)
+    for key in ("W13", "Wd", "W13s", "Wds"):
+        if run.weights[0][key] is not None:
+            run.weights[0][key].fill_(float("nan"))
+    torch.cuda.synchronize()
+    run.weights_numpy = lambda layer: snap
+    e, _ = G.run_and_compare_full(run)
+    print("weights overwritten after registration: max|err|/rms", e)
+    # register the NaN weights: every output row becomes NaN
+    wt = run.weights[0]
+    assert A.afd_set_layer(run.ctx, 0, run.Wg.data_ptr(), run.bias.data_ptr() if run.bias is not None else 0,
+                           wt["W13"].data_ptr(), wt["Wd"].data_ptr(),
+                           wt["W13s"].data_ptr() if wt["W13s"] is not None else 0,
+                           wt["Wds"].data_ptr() if wt["Wds"] is not None else 0) == 0
+    run.pack_all(0)
+    assert run.forward(0) == 0
+    outs = run.unpack_all()
+    assert run.poll() == 0
+    assert all(torch.isnan(o[:n].float()).all() for o, n in zip(outs, w.seq_lens) if n)
+    run.close()
+
+
 @pytest.mark.parametrize("workload", ["fanin", "v2lite_prefill"])
 def test_serialised_launches(workload):
     """Every kernel launched after the previous one has finished (no

@@ -193,6 +193,7 @@ struct afd_ctx {
   int64_t launches = 0;
   int last_T = 0;
   int64_t forwards = 0;
+  uint32_t go_seq = 0;               // tokens for ws.go, one per host-described routed step
   int64_t ws_cap[12];
   // stage timing: one set of events per forward, in a ring, so the host
   // reads them after many forwards instead of waiting after each one
@@ -370,7 +371,8 @@ int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out) {
       {2 * AFD_MAX_PEERS * E * 4},           // grouped-form bases and group-list prefixes
       {(int64_t)sizeof(FanIn)},              // the fan-in of the step in flight
       {AFD_LOOP_WORDS * 4},                  // work-item loop state and log
-      {(int64_t)cfg->max_layers * (int64_t)sizeof(DevLayer)}};  // per-layer weight table
+      {(int64_t)cfg->max_layers * (int64_t)sizeof(DevLayer)},  // per-layer weight table
+      {4}};                                  // go word (header check -> router)
   const int nparts = sizeof(parts) / sizeof(parts[0]);
   int64_t offs[32], total = 0;
   for (int i = 0; i < nparts; i++) {
@@ -406,6 +408,7 @@ int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out) {
   c->ws.loop = reinterpret_cast<int32_t*>(b + offs[23]);
   c->dlayers = reinterpret_cast<DevLayer*>(b + offs[24]);
   c->ws.layers = c->dlayers;
+  c->ws.go = reinterpret_cast<uint32_t*>(b + offs[25]);
   c->plan1 = reinterpret_cast<GemmPlan*>(b + offs[16]);
   c->plan2 = reinterpret_cast<GemmPlan*>(b + offs[17]);
   const int ws_map[12] = {4, 5, 6, 7, 8, 9, 11, 12, 13, 14, 15, 0};
@@ -894,12 +897,19 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
   };
   mark(0);
   const int rows_cap = (int)routed_cap_of(&c);
+  // host-described routed steps: the router starts once the check has the
+  // flags (ws.go), not when the check ends
+  uint32_t go = 0;
+  if (!dev && !grouped) {
+    ctx->go_seq = ctx->go_seq % 0x7ffffffeu + 1u;
+    go = ctx->go_seq;
+  }
   rc = cuda_fail(dev ? launch_item_head(lc, ctx->geom, ctx->win[0], *dev, ws, c.num_experts,
                                         c.token_cap, rows_cap, f.ffn_rank, f.ffn_size, has_shared,
                                         grouped, ctx->tmax, ctx->tmax * c.topk, c.max_layers,
                                         ctx->timeout())
                      : launch_header_check(lc, ctx->geom, ctx->win[0], f, ws, c.num_experts,
-                                           c.token_cap, rows_cap, has_shared, ctx->timeout()),
+                                           c.token_cap, rows_cap, has_shared, ctx->timeout(), go),
                  "header check");
   if (rc) return rc;
   mark(1);
@@ -920,7 +930,7 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
   if (!grouped) {  // the grouped form arrives routed
     rc = cuda_fail(launch_router(lc, ctx->geom, ctx->win[0], f, ws, c.hidden, ctx->act_f32,
                                  L ? L->WgQ : nullptr, L ? L->bias : nullptr, c.num_experts, c.topk, c.renorm, c.routed_scaling,
-                                 ws.logits, ws.hist),
+                                 ws.logits, ws.hist, go, ctx->timeout()),
                    "router");
     if (rc) return rc;
   }

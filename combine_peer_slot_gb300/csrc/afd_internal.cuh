@@ -114,7 +114,16 @@ struct DevWS {
   FanIn* item;            // the fan-in of the step in flight
   const DevLayer* layers; // [max_layers] per-layer weights
   int32_t* loop;          // [AFD_LOOP_WORDS] work-item loop state and log
+  uint32_t* go;           // [1] the header check's word for the router (AFD_GO_ABORT)
 };
+
+// The header check of a host-described step publishes, once every listed
+// flag is acquired, the step's go token in ws.go (release); the router's
+// CTAs start under programmatic dependent launch, load their gate weights,
+// and read the fan-in's rows once they see it (acquire).  Token | ABORT:
+// the check found an earlier error or a flag wait ran out; the router then
+// does no work (the check reports the error).
+#define AFD_GO_ABORT 0x80000000u
 
 // one group of the grouped GEMM: rows of the B operand (tokens) that share
 // one weight matrix (an expert, or the shared expert)
@@ -214,6 +223,14 @@ __device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
 
 __device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -358,10 +375,11 @@ cudaError_t launch_pack_header(const LaunchCtx& lc, const WinGeom& g, uint8_t* w
 // entries, then f is written to ws.item
 // rows_cap: routed rows a slot may carry (token_cap, or routed_cap under
 // token-level dispatch)
+// go_token: 0, or the step's token (1 .. 2^31 - 1) for ws.go
 cudaError_t launch_header_check(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                                 const FanIn& f, const DevWS& ws, int num_experts,
                                 int token_cap, int rows_cap, int has_shared_expert,
-                                int64_t timeout_ns);
+                                int64_t timeout_ns, uint32_t go_token);
 // device-chosen step: bounded wait for any stage whose listed peers have all
 // published, the fan-in built from their headers (token form, or the grouped
 // form when grouped is set), the same checks, then ws.item.  tmax / rmax: the
@@ -379,7 +397,8 @@ size_t router_min_smem_bytes(int hidden, int E, int act_f32);
 cudaError_t launch_router(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                           const FanIn& f, const DevWS& ws, int hidden, int act_f32,
                           const float* WgQ, const float* bias, int E, int k, int renorm,
-                          float scale, float* logits, int32_t* hist);
+                          float scale, float* logits, int32_t* hist, uint32_t go_token = 0,
+                          int64_t timeout_ns = 0);
 // sh_in_place: the shared expert reads its rows in place from the slots'
 // shared_x (one group per peer; g, row_bytes give the window rows) instead of
 // from the gathered rows after the routed ones

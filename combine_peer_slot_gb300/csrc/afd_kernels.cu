@@ -150,7 +150,8 @@ __global__ void k_pack_header(uint8_t* win, WinGeom g, int region, int stage, in
 template <bool kFromHeaders>
 __device__ bool check_entries(const uint8_t* win, const WinGeom& g, const FanIn& f, const DevWS& ws,
                               int E, int token_cap, int rows_cap, int has_shared_expert,
-                              int64_t timeout_ns, int item_err, bool check_status) {
+                              int64_t timeout_ns, int item_err, bool check_status,
+                              uint32_t go_token) {
   __shared__ int err[AFD_MAX_PEERS];
   __shared__ int bad_sidx[AFD_MAX_PEERS];
   __shared__ int shared_n[AFD_MAX_PEERS];
@@ -167,18 +168,27 @@ __device__ bool check_entries(const uint8_t* win, const WinGeom& g, const FanIn&
   if (tid == 0) skip = check_status ? read_status(ws.status) : 0;
   if (tid < AFD_MAX_PEERS) { err[tid] = 0; bad_sidx[tid] = 0; shared_n[tid] = 0; }
   __syncthreads();
-  if (skip) return false;
+  if (skip) {
+    if (tid == 0 && go_token) st_release_u32(ws.go, go_token | AFD_GO_ABORT);
+    return false;
+  }
+  int e = 0;
   if (tid < f.n_peers) {
-    const int i = tid;
     const uint64_t t0 = globaltimer_ns();
     unsigned backoff = 32;
-    int e = 0;
     while (fl <= seen) {
       if (globaltimer_ns() - t0 > (uint64_t)timeout_ns) { e = AFD_ERR_TIMEOUT; break; }
       __nanosleep(backoff);
       if (backoff < 1024) backoff <<= 1;
       fl = ld_acquire_u64(flagp);
     }
+  }
+  if (go_token) {  // every listed flag acquired: the router may read the rows
+    const bool late = __syncthreads_or(e != 0);
+    if (tid == 0) st_release_u32(ws.go, late ? (go_token | AFD_GO_ABORT) : go_token);
+  }
+  if (tid < f.n_peers) {
+    const int i = tid;
     if (!e) {
       // the 12 fixed words in three 16-byte loads, ordered after the acquire
       int32_t h[12];
@@ -309,10 +319,12 @@ __device__ bool check_entries(const uint8_t* win, const WinGeom& g, const FanIn&
 // kernels after this one
 __global__ void __launch_bounds__(1024)
 k_header_check(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn f, DevWS ws, int E,
-               int token_cap, int rows_cap, int has_shared_expert, int64_t timeout_ns) {
+               int token_cap, int rows_cap, int has_shared_expert, int64_t timeout_ns,
+               uint32_t go_token) {
   grid_dep_wait();
   grid_dep_launch();
-  check_entries<false>(win, g, f, ws, E, token_cap, rows_cap, has_shared_expert, timeout_ns, 0, true);
+  check_entries<false>(win, g, f, ws, E, token_cap, rows_cap, has_shared_expert, timeout_ns, 0, true,
+                       go_token);
 }
 
 // ---------------------------------------------------------------------------
@@ -412,7 +424,7 @@ k_item_head(const uint8_t* win, WinGeom g, PeerList pl, DevWS ws, int E, int tok
   }
   __syncthreads();
   if (!check_entries<true>(win, g, fs, ws, E, token_cap, rows_cap, has_shared_expert, timeout_ns,
-                           item_err, false))
+                           item_err, false, 0))
     return;
   {
     const int32_t* src = reinterpret_cast<const int32_t*>(&fs);
@@ -967,8 +979,18 @@ template <bool kDev>
 __global__ void __launch_bounds__(2 * kTwWarps * 32, 1)
 k_router_logits_tw2(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn fp, DevWS ws, int hidden,
                     const float* __restrict__ WgQ, const float* __restrict__ bias, int E,
-                    float* __restrict__ logits, TwGeom geo) {
-  grid_dep_wait();
+                    float* __restrict__ logits, TwGeom geo, uint32_t go_token, int64_t go_timeout_ns) {
+  // go_token != 0 (host-described steps): started before the header check
+  // ends; the gate weights load at once, the fan-in's rows once ws.go holds
+  // the token, and the wait on the check moves to every exit, so the end of
+  // this grid still implies the check's
+  struct ExitWait {
+    bool on;
+    __device__ ~ExitWait() {
+      if (on) grid_dep_wait();
+    }
+  } exit_wait{go_token != 0};
+  if (!go_token) grid_dep_wait();
   grid_dep_launch();
   const FanIn& f = step_item<kDev>(fp, ws.item);
   if (!WgQ) {  // the layer of the step was chosen on the device
@@ -981,7 +1003,7 @@ k_router_logits_tw2(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn
   const int set = warp / kTwWarps, wis = warp % kTwWarps, tis = tid % (kTwWarps * 32);
   uint8_t* xt = tw_smem + geo.w_bytes + set * geo.xt_bytes;      // this stream's records
   uint64_t* wbar_p = reinterpret_cast<uint64_t*>(tw_smem + geo.w_bytes + 2 * geo.xt_bytes);
-  if (read_status(ws.status)) return;
+  if (!go_token && read_status(ws.status)) return;
   const int e_base = blockIdx.y * kTwExperts;
   const int ne = min(kTwExperts, E - e_base);
   const int ntiles = (f.total + kTwTok - 1) / kTwTok;
@@ -996,6 +1018,32 @@ k_router_logits_tw2(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn
     const uint32_t wbytes = (uint32_t)(((ne + 3) / 4) * hidden * 16);
     mbar_expect_tx(wbar, wbytes);
     bulk_load(smem_u32(tw_smem), WgQ + (int64_t)e_base * hidden, wbytes, wbar);
+  }
+  if (go_token) {
+    __shared__ int go_ok;
+    if (tid == 0) {
+      const uint64_t t0 = globaltimer_ns();
+      int r = 0;
+      for (;;) {
+        const uint32_t v = ld_acquire_u32(ws.go);
+        if (v == go_token) { r = 1; break; }
+        if (v == (go_token | AFD_GO_ABORT)) break;  // the check reports the error
+        if (globaltimer_ns() - t0 > (uint64_t)go_timeout_ns) {
+          set_error(ws.status, AFD_ERR_TIMEOUT);
+          break;
+        }
+        __nanosleep(64);
+      }
+      go_ok = r && !read_status(ws.status);
+    }
+    __syncthreads();
+    if (!go_ok) {
+      if (tid == 0) {  // the weight copy lands in this CTA's shared memory: wait (bounded)
+        const uint64_t dl = globaltimer_ns() + 100000000ull;
+        while (!mbar_try_wait(wbar, 0) && globaltimer_ns() < dl) {}
+      }
+      return;
+    }
   }
   // tiles of this stream: local index i = set, set + 2, ...
   uint4 pre[kTw2Chunks][kTwTok];
@@ -2174,9 +2222,10 @@ cudaError_t launch_pack_header(const LaunchCtx& lc, const WinGeom& g, uint8_t* w
 
 cudaError_t launch_header_check(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                                 const FanIn& f, const DevWS& ws, int num_experts, int token_cap,
-                                int rows_cap, int has_shared_expert, int64_t timeout_ns) {
+                                int rows_cap, int has_shared_expert, int64_t timeout_ns,
+                                uint32_t go_token) {
   return launch_k(lc, k_header_check, 1, 1024, 0, win, g, f, ws, num_experts, token_cap, rows_cap,
-                  has_shared_expert, timeout_ns);
+                  has_shared_expert, timeout_ns, go_token);
 }
 
 template <typename XS, bool kDev>
@@ -2243,7 +2292,8 @@ static TwGeom tw_geom(int hidden) {
 template <typename XS, bool kDev>
 static cudaError_t launch_logits(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                                  const FanIn& f, const DevWS& ws, int hidden, const float* WgQ,
-                                 const float* bias, int E, float* logits) {
+                                 const float* bias, int E, float* logits, uint32_t go_token,
+                                 int64_t go_timeout_ns) {
   if (sizeof(XS) == 2 && E >= 16 && hidden <= 8 * kTw2Chunks * kTwWarps * 32) {
     TwGeom geo = tw_geom(hidden);
     geo.stage_bytes = 0;  // no staging buffer; two record buffers
@@ -2256,7 +2306,8 @@ static cudaError_t launch_logits(const LaunchCtx& lc, const WinGeom& g, const ui
       const int ntiles = (f.total + kTwTok - 1) / kTwTok;
       const int gx = std::max(1, std::min(ntiles, lc.num_sms / eblocks));
       return launch_k(lc, k_router_logits_tw2<kDev>, dim3(gx, eblocks), 2 * kTwWarps * 32, geo.smem,
-                      win, g, f, ws, hidden, WgQ, bias, E, logits, geo);
+                      win, g, f, ws, hidden, WgQ, bias, E, logits, geo, kDev ? 0u : go_token,
+                      go_timeout_ns);
     }
   }
   if (sizeof(XS) == 2 && E >= 16) {
@@ -2290,10 +2341,13 @@ template <bool kDev>
 static cudaError_t launch_router_t(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                                    const FanIn& f, const DevWS& ws, int hidden, int act_f32,
                                    const float* WgQ, const float* bias, int E, int k, int renorm,
-                                   float scale, float* logits, int32_t* hist) {
+                                   float scale, float* logits, int32_t* hist, uint32_t go_token,
+                                   int64_t go_timeout_ns) {
   cudaError_t err =
-      act_f32 ? launch_logits<float, kDev>(lc, g, win, f, ws, hidden, WgQ, bias, E, logits)
-              : launch_logits<uint16_t, kDev>(lc, g, win, f, ws, hidden, WgQ, bias, E, logits);
+      act_f32 ? launch_logits<float, kDev>(lc, g, win, f, ws, hidden, WgQ, bias, E, logits, go_token,
+                                           go_timeout_ns)
+              : launch_logits<uint16_t, kDev>(lc, g, win, f, ws, hidden, WgQ, bias, E, logits, go_token,
+                                              go_timeout_ns);
   if (err != cudaSuccess) return err;
   const int nblocks = router_blocks(f.total);
   return launch_k(lc, k_router_topk<kDev>, nblocks, kRtTok * 32, 0, f, ws, logits, E, k, renorm,
@@ -2303,12 +2357,15 @@ static cudaError_t launch_router_t(const LaunchCtx& lc, const WinGeom& g, const 
 cudaError_t launch_router(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                           const FanIn& f, const DevWS& ws, int hidden, int act_f32,
                           const float* WgQ, const float* bias, int E, int k, int renorm,
-                          float scale, float* logits, int32_t* hist) {
+                          float scale, float* logits, int32_t* hist, uint32_t go_token,
+                          int64_t timeout_ns) {
   if (f.total == 0) return cudaSuccess;
+  // the router's own bound on ws.go: the check's flag waits plus a margin
+  const int64_t go_timeout_ns = timeout_ns + 100000000;
   return f.dev ? launch_router_t<true>(lc, g, win, f, ws, hidden, act_f32, WgQ, bias, E, k, renorm,
-                                       scale, logits, hist)
+                                       scale, logits, hist, 0, 0)
                : launch_router_t<false>(lc, g, win, f, ws, hidden, act_f32, WgQ, bias, E, k,
-                                        renorm, scale, logits, hist);
+                                        renorm, scale, logits, hist, go_token, go_timeout_ns);
 }
 
 template <bool kDev>

@@ -876,12 +876,15 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
   // decode-sized fan-ins: the SwiGLU GEMM streams its weights from HBM while
   // the small kernels before it leave HBM idle, so a side stream prefetches
   // the weights of the GEMM's first units (experts in order, 256 rows per
-  // unit) into L2 meanwhile, forked once the header check is issued; joined
-  // at the end.  Its traffic must have drained when the GEMM starts (the
-  // GEMM's own first loads queue behind it): 3/8 of a wave (57 units on 152
-  // SMs, 60 MB) measured best (26-layer decode 6.82 -> 6.71 ms against a
-  // full wave forked after the router; 1/4 and 1/2 wave, or forking before
-  // the header check or after the plan, were slower)
+  // unit) into L2 meanwhile; joined at the end of the step.  The fork's event
+  // ends the programmatic overlap of the two launches it falls between, and
+  // the prefetch's DRAM traffic slows the small kernels' own loads.  Host-
+  // described steps fork before the header check (no launch of the step is
+  // split) and issue from a few SMs, num_sms / 8, whose copy engines pace the
+  // traffic over the small kernels: 95 units (100 MB) from 19 SMs measured
+  // 6.33 ms per 26 layers against 6.39 ms for 57 units from every SM forked
+  // after the header check (sweep of 57-152 units x 10-152 SMs).  Steps the
+  // device describes fork after the item head, whose fan-in they read.
   const bool prefetch = c.gemm == AFD_GEMM_TENSOR && bn == 64 && N > 0;
   int rc = AFD_OK;
   struct Join {  // the main stream waits for the side stream on every way out
@@ -891,10 +894,28 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
       if (armed) cudaStreamWaitEvent(ctx->stream, ctx->ev_join, 0);
     }
   } join{ctx};
+  auto fork_prefetch = [&](int units, int sms) -> int {
+    const int64_t bytes = (int64_t)units * 256 * c.hidden * 2;
+    const int64_t w13 = (int64_t)c.num_experts * 2 * c.inter * c.hidden * 2;
+    LaunchCtx side = lc;
+    side.stream = ctx->side;
+    side.pdl = 0;
+    int r = cuda_fail(cudaEventRecord(ctx->ev_fork, ctx->stream), "fork");
+    if (!r) r = cuda_fail(cudaStreamWaitEvent(ctx->side, ctx->ev_fork, 0), "fork");
+    if (!r) r = cuda_fail(launch_prefetch_l2(side, L ? L->W13 : nullptr, std::min(bytes, w13), ws, sms),
+                          "prefetch");
+    if (!r) r = cuda_fail(cudaEventRecord(ctx->ev_join, ctx->side), "join");
+    if (!r) join.armed = true;
+    return r;
+  };
   // stage timing marks only for host-described steps
   auto mark = [&](int i) {
     if (!dev) ctx->mark(i);
   };
+  if (prefetch && !dev) {
+    rc = fork_prefetch(ctx->num_sms * 5 / 8, std::max(1, ctx->num_sms / 8));
+    if (rc) return rc;
+  }
   mark(0);
   const int rows_cap = (int)routed_cap_of(&c);
   // host-described routed steps: the router starts once the check has the
@@ -913,19 +934,9 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
                  "header check");
   if (rc) return rc;
   mark(1);
-  if (prefetch) {
-    const int64_t first_wave = (int64_t)(ctx->num_sms * 3 / 8) * 256 * c.hidden * 2;
-    const int64_t w13 = (int64_t)c.num_experts * 2 * c.inter * c.hidden * 2;
-    LaunchCtx side = lc;
-    side.stream = ctx->side;
-    side.pdl = 0;
-    rc = cuda_fail(cudaEventRecord(ctx->ev_fork, ctx->stream), "fork");
-    if (!rc) rc = cuda_fail(cudaStreamWaitEvent(ctx->side, ctx->ev_fork, 0), "fork");
-    if (!rc) rc = cuda_fail(launch_prefetch_l2(side, L ? L->W13 : nullptr, std::min(first_wave, w13), ws),
-                              "prefetch");
-    if (!rc) rc = cuda_fail(cudaEventRecord(ctx->ev_join, ctx->side), "join");
+  if (prefetch && dev) {
+    rc = fork_prefetch(ctx->num_sms * 3 / 8, ctx->num_sms);
     if (rc) return rc;
-    join.armed = true;
   }
   if (!grouped) {  // the grouped form arrives routed
     rc = cuda_fail(launch_router(lc, ctx->geom, ctx->win[0], f, ws, c.hidden, ctx->act_f32,

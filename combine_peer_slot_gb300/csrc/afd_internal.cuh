@@ -437,9 +437,10 @@ cudaError_t launch_scatter_grouped(const LaunchCtx& lc, const WinGeom& g, uint8_
                                    const FanIn& f, const DevWS& ws, int hidden, int act_f32,
                                    int has_shared);
 // bytes: a multiple of 16 from a 16-byte aligned base; base NULL: the W13
-// of the layer in ws.item (nothing when the step has no routed rows)
+// of the layer in ws.item (nothing when the step has no routed rows); sms:
+// the CTAs (one per SM) that issue the 64 KB prefetches, which paces them
 cudaError_t launch_prefetch_l2(const LaunchCtx& lc, const void* base, int64_t bytes,
-                               const DevWS& ws);
+                               const DevWS& ws, int sms);
 // 128-row weight tiles of a tensor-engine weight copy, and the copy itself
 // ([E][tiles][k-blocks] blocks of 128 x 64 bf16; see k_tile_weight)
 int tiled_weight_tiles(int M, int swiglu, int I);

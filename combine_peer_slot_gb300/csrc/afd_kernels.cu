@@ -2469,10 +2469,9 @@ cudaError_t launch_scatter_grouped(const LaunchCtx& lc, const WinGeom& g, uint8_
 }
 
 cudaError_t launch_prefetch_l2(const LaunchCtx& lc, const void* base, int64_t bytes,
-                               const DevWS& ws) {
+                               const DevWS& ws, int sms) {
   if (bytes <= 0) return cudaSuccess;
-  return launch_k(lc, k_prefetch_l2, lc.num_sms, 32, 0, static_cast<const uint8_t*>(base), bytes,
-                  ws);
+  return launch_k(lc, k_prefetch_l2, sms, 32, 0, static_cast<const uint8_t*>(base), bytes, ws);
 }
 
 cudaError_t launch_item_head(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,

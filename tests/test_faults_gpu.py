@@ -80,6 +80,27 @@ def test_flag_never_set_times_out():
     assert run.forward(0) == 0 and run.poll() == 0
 
 
+def test_forward_queued_behind_a_failed_one():
+    """A forward enqueued behind one that failed finds the sticky status: its
+    header check skips and hands the router the abort token, so nothing
+    waits out a timeout; the first error is the one reported, and the
+    context works again afterwards."""
+    import time
+    w = W.custom("fanin", seq_lens=[5, 9], token_cap=64)
+    run = R.Runner(w, layers=2, wait_timeout_ns=2_000_000_000)  # a router left waiting: > 2 s
+    run.pack_all(0)
+    assert run.forward(0) == 0 and run.poll() == 0   # warm (module loads, first launches)
+    run.pack_all(0)
+    assert run.forward(1) == 0                 # wrong layer: recorded on the device
+    run.pack_all(0)
+    t0 = time.time()
+    assert run.forward(0) == 0                 # queued behind it
+    assert run.poll() == A.AFD_ERR_LAYER
+    assert time.time() - t0 < 1.0
+    run.pack_all(0)
+    assert run.forward(0) == 0 and run.poll() == 0
+
+
 def test_shutdown_announced():
     run = make_run()
     run.pack_all(0, peers=[0])

@@ -144,28 +144,40 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # algorithmic work (roofline numerators)
 # ---------------------------------------------------------------------------
-def stage_work(w, T):
-    """Algorithmic FLOPs / bytes per launch of each stage for T tokens."""
+def stage_work(w, T, nz=None):
+    """Algorithmic FLOPs / bytes per launch of each stage for T tokens (nz:
+    experts with rows, whose weights the GEMMs read; all E by default)."""
     H, I, Is, k, E = w.hidden, w.inter, w.shared_inter, w.topk, w.num_experts
+    nz = E if nz is None else nz
     ab = w.act_bytes
     return {
         "router": {"flops": 2 * T * H * E, "bytes": T * H * ab + H * E * 4 + T * k * 8},
         "gather": {"bytes": (T * k + T) * H * ab * 2},
-        "gemm_swiglu": {"flops": 2 * T * H * 2 * (k * I + Is)},
-        "gemm_down": {"flops": 2 * T * H * (k * I + Is)},
+        # weights of the experts with rows + the shared expert, rows in, outputs
+        "gemm_swiglu": {"flops": 2 * T * H * 2 * (k * I + Is),
+                        "bytes": (nz * 2 * I + 2 * Is) * H * 2 + (T * k + T) * H * ab
+                        + (T * k * I + T * Is) * ab},
+        "gemm_down": {"flops": 2 * T * H * (k * I + Is),
+                      "bytes": (nz * I + Is) * H * 2 + (T * k * I + T * Is) * ab
+                      + T * k * H * ab + T * H * 4},
         "combine_split": {"bytes": T * k * H * ab + T * H * 4 + T * H * ab + T * k * 8},
     }
 
 
-def stage_work_grouped(w, T, Rr):
+def stage_work_grouped(w, T, Rr, nz=None):
     """Algorithmic work per stage of the grouped form: Rr routed rows arrive
     grouped (no router, no combine: the rows' outputs go back)."""
     H, I, Is = w.hidden, w.inter, w.shared_inter
+    nz = w.num_experts if nz is None else nz
     ab = w.act_bytes
     return {
         "gather": {"bytes": (Rr + T) * H * ab * 2},
-        "gemm_swiglu": {"flops": 2 * H * 2 * (Rr * I + T * Is)},
-        "gemm_down": {"flops": 2 * H * (Rr * I + T * Is)},
+        "gemm_swiglu": {"flops": 2 * H * 2 * (Rr * I + T * Is),
+                        "bytes": (nz * 2 * I + 2 * Is) * H * 2 + (Rr + T) * H * ab
+                        + (Rr * I + T * Is) * ab},
+        "gemm_down": {"flops": 2 * H * (Rr * I + T * Is),
+                      "bytes": (nz * I + Is) * H * 2 + (Rr * I + T * Is) * ab + Rr * H * ab
+                      + T * H * 4},
         "combine_split": {"bytes": Rr * H * ab * 2 + T * H * (4 + ab)},
     }
 
@@ -305,8 +317,14 @@ def run_ours(args, ws, rank, local):
         flops, nbytes, t_roof, bound = path_roofline(w, T, int((cnt > 0).sum()), pk)
     stages = {n: stage_sum[i] / (args.steps * w.layers) for i, n in enumerate(A.STAGE_NAMES)}
     dom = max(stages, key=stages.get)
-    work = (stage_work_grouped(w, T, Rr) if grouped else stage_work(w, T)).get(dom, {})
-    if "flops" in work and dom.startswith("gemm"):
+    nz = int((cnt > 0).sum())
+    work = (stage_work_grouped(w, T, Rr, nz) if grouped else stage_work(w, T, nz)).get(dom, {})
+    # a GEMM below the ridge point (peak FLOP/s / peak bytes/s) streams its
+    # weights from HBM (decode-sized fan-ins): measured against HBM then
+    gemm_tensor = dom.startswith("gemm") and "flops" in work and (
+        "bytes" not in work
+        or work["flops"] / (pk["bf16_tflops"] * 1e12) >= work["bytes"] / (pk["hbm_gbs"] * 1e9))
+    if gemm_tensor:
         ach = work["flops"] / (stages[dom] / 1e3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"],

@@ -66,7 +66,8 @@ struct Ring {
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
-    int skip;
+    int skip;       // this CTA's decision
+    int peer_skip;  // the peer's, stored here by the peer
   };
   static constexpr size_t kEpiOffset = ((size_t)STAGES * STAGE_BYTES + sizeof(Tail) + 127) / 128 * 128;
   static constexpr size_t kSmemBytes = 1024 + kEpiOffset + (size_t)EPI_WARPS * EPI_BUF_BYTES;
@@ -100,11 +101,6 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
 }
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ int ld_cluster_s32(uint32_t cluster_addr) {
-  int v;
-  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
-  return v;
 }
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
@@ -253,7 +249,19 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
     tail->abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  // everything above touches only this CTA's shared memory
+  // TMEM before the dependency wait: a GEMM CTA of an earlier launch never
+  // shares this SM (each takes over half its shared memory), so the columns
+  // are free; everything up to the wait touches only this CTA's resources
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&tail->tmem_base)),
+                 "r"(TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+  }
+  // "this CTA has started": its peer may store into its shared memory once
+  // the matching wait below returns (usually at once: both arrived before
+  // their dependency waits)
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   grid_dep_wait();
   grid_dep_launch();
   __shared__ int unit0_s[AFD_MAX_GROUPS];
@@ -267,13 +275,26 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
     }
     tail->skip = skip;
   }
-  __syncthreads();
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // the peer has started
+  if (threadIdx.x == 0) {
+    // the decision goes into the peer's shared memory too, so after the
+    // barrier each CTA reads only its own and may leave at once
+    asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(map_to_rank(smem_u32(&tail->peer_skip), rank ^ 1u)),
+                 "r"(tail->skip)
+                 : "memory");
+  }
+  tc_fence_before();
+  cluster_sync();  // both CTAs' barriers, skip decisions and TMEM columns are in place
+  tc_fence_after();
   const int total = plan.total_units;
-  cluster_sync();  // the peer's barriers and skip flag are initialised before any remote access
-  // both CTAs of a pair take the same decision: each ORs its own flag with the peer's
-  const int peer_skip = ld_cluster_s32(map_to_rank(smem_u32(&tail->skip), rank ^ 1u));
-  cluster_sync();  // both flags read before either CTA may leave
-  if (tail->skip || peer_skip || total <= cid) return;
+  if (tail->skip || tail->peer_skip || total <= cid) {  // the same decision in both CTAs
+    if (warp == 1) {
+      __syncwarp();
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tail->tmem_base),
+                   "r"(TMEM_COLS));
+    }
+    return;
+  }
 
   // weight maps: the kernel's own, or the device table's entry for the layer
   // the device chose for this step (host-written before any launch)
@@ -282,16 +303,6 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
     const DevLayer& Ld = args.layers[args.item->layer];
     tmA = args.wsel == 1 ? Ld.tmA1 : Ld.tmA2;
   }
-
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(&tail->tmem_base)),
-                 "r"(TMEM_COLS));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
   const uint32_t tmem_base = tail->tmem_base;
   const uint64_t deadline = globaltimer_ns() + kGemmTimeoutNs;
   volatile int* abort_flag = &tail->abort_flag;

@@ -1,0 +1,58 @@
+"""The bench's algorithmic work per stage and the bound it measures each GEMM
+against (host only: no GPU)."""
+import bench
+from combine_peer_slot_gb300 import workloads as W
+
+PEAKS = {"bf16_tflops": 1940.7, "hbm_gbs": 6794.1}
+
+
+def bound(work):
+    t_flop = work["flops"] / (PEAKS["bf16_tflops"] * 1e12)
+    t_mem = work["bytes"] / (PEAKS["hbm_gbs"] * 1e9)
+    return "tensor" if t_flop >= t_mem else "hbm"
+
+
+def test_gemm_work_counted_by_hand():
+    """V2-Lite prefill, every expert with rows: the SwiGLU GEMM reads the
+    64 experts' gate/up weights and the shared expert's, the routed and
+    shared rows, and writes the SwiGLU outputs; FLOPs are 2 per MAC."""
+    w = W.get("v2lite_prefill")
+    T, H, I, Is, k, E = w.total_tokens, w.hidden, w.inter, w.shared_inter, w.topk, w.num_experts
+    sw = bench.stage_work(w, T, E)["gemm_swiglu"]
+    assert sw["flops"] == 2 * H * (T * k * 2 * I + T * 2 * Is)
+    weights = (E * 2 * I * H + 2 * Is * H) * 2
+    rows_in = (T * k + T) * H * 2
+    rows_out = (T * k * I + T * Is) * 2
+    assert sw["bytes"] == weights + rows_in + rows_out
+    dn = bench.stage_work(w, T, E)["gemm_down"]
+    assert dn["flops"] == 2 * H * (T * k * I + T * Is)
+    # routed partials in bf16, the shared expert's output in fp32
+    assert dn["bytes"] == (E * I * H + Is * H) * 2 + (T * k * I + T * Is) * 2 + T * k * H * 2 + T * H * 4
+
+
+def test_only_experts_with_rows_count():
+    w = W.get("decode")
+    T = w.total_tokens
+    full = bench.stage_work(w, T, w.num_experts)["gemm_down"]["bytes"]
+    fewer = bench.stage_work(w, T, w.num_experts - 10)["gemm_down"]["bytes"]
+    assert full - fewer == 10 * w.inter * w.hidden * 2
+
+
+def test_prefill_gemms_tensor_bound_decode_gemms_hbm_bound():
+    for name, want in (("v2lite_prefill", "tensor"), ("decode", "hbm")):
+        w = W.get(name)
+        sw = bench.stage_work(w, w.total_tokens, w.num_experts)
+        assert bound(sw["gemm_swiglu"]) == want, name
+        assert bound(sw["gemm_down"]) == want, name
+
+
+def test_grouped_form_matches_token_form_when_rows_agree():
+    """The grouped form with Rr = T k routed rows does the GEMM work of the
+    token form."""
+    w = W.get("v2lite_prefill")
+    T = w.total_tokens
+    a = bench.stage_work(w, T, w.num_experts)
+    b = bench.stage_work_grouped(w, T, T * w.topk, w.num_experts)
+    for s in ("gemm_swiglu", "gemm_down"):
+        assert a[s]["flops"] == b[s]["flops"]
+        assert a[s]["bytes"] == b[s]["bytes"]

@@ -183,9 +183,40 @@ __device__ bool check_entries(const uint8_t* win, const WinGeom& g, const FanIn&
       fl = ld_acquire_u64(flagp);
     }
   }
-  if (go_token) {  // every listed flag acquired: the router may read the rows
-    const bool late = __syncthreads_or(e != 0);
-    if (tid == 0) st_release_u32(ws.go, late ? (go_token | AFD_GO_ABORT) : go_token);
+  // every listed flag acquired (or given up on): the router may read the
+  // rows, and this block reads the headers and shared_idx fields at once
+  const bool late = __syncthreads_or(e != 0);
+  if (go_token && tid == 0) st_release_u32(ws.go, late ? (go_token | AFD_GO_ABORT) : go_token);
+  // shared_idx must list the entry's shared tokens: row j is token
+  // ffn_rank + j * ffn_size (0..n-1 with one FFN rank: every token is a
+  // shared token; Async GPU Connector, "Data flow" step 3, arange(ffn_rank,
+  // n, ffn_size)).  The rows the fan-in expects of every entry (sprefix)
+  // form one index space, 8 independent loads in flight per thread, read
+  // with the headers; a mismatch counts only for an entry whose header
+  // announces its shared rows (shared_n below).
+  {
+    const int total = f.sprefix[f.n_peers];
+    for (int r0 = tid; r0 < total; r0 += 8 * blockDim.x) {
+      int v[8], want[8], who[8];
+#pragma unroll
+      for (int u = 0; u < 8; u++) {
+        const int r = r0 + u * blockDim.x;
+        who[u] = -1;
+        v[u] = want[u] = 0;
+        if (r < total) {
+          const int lo = entry_of_shared(f, r);
+          const int32_t* sidx = reinterpret_cast<const int32_t*>(
+              slot_ptr(win, g, f.region[lo], f.stage) + g.shared_idx);
+          const int j = r - f.sprefix[lo];
+          want[u] = f.ffn_rank + j * f.ffn_size;
+          who[u] = lo;
+          v[u] = sidx[j];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; u++)
+        if (who[u] >= 0 && v[u] != want[u]) bad_sidx[who[u]] = 1;
+    }
   }
   if (tid < f.n_peers) {
     const int i = tid;
@@ -248,56 +279,12 @@ __device__ bool check_entries(const uint8_t* win, const WinGeom& g, const FanIn&
     ws.cur_seq[i] = fl;
   }
   __syncthreads();
-  // shared_idx must list the entry's shared tokens: row j is token
-  // ffn_rank + j * ffn_size (0..n-1 with one FFN rank: every token is a
-  // shared token; Async GPU Connector, "Data flow" step 3, arange(ffn_rank,
-  // n, ffn_size)).  The rows of all peers form one index space, 8
-  // independent loads in flight per thread.
-  {
-    __shared__ int sh_prefix[AFD_MAX_PEERS + 1];
-    if (tid == 0) {
-      int run = 0;
-      for (int i = 0; i < f.n_peers; i++) {
-        sh_prefix[i] = run;
-        run += err[i] ? 0 : shared_n[i];
-      }
-      sh_prefix[f.n_peers] = run;
-    }
-    __syncthreads();
-    const int total = sh_prefix[f.n_peers];
-    for (int r0 = tid; r0 < total; r0 += 8 * blockDim.x) {
-      int v[8], want[8], who[8];
-#pragma unroll
-      for (int u = 0; u < 8; u++) {
-        const int r = r0 + u * blockDim.x;
-        who[u] = -1;
-        v[u] = want[u] = 0;
-        if (r < total) {
-          int lo = 0, hi = f.n_peers - 1;
-          while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (sh_prefix[mid] <= r) lo = mid; else hi = mid - 1;
-          }
-          const int32_t* sidx = reinterpret_cast<const int32_t*>(
-              slot_ptr(win, g, f.region[lo], f.stage) + g.shared_idx);
-          const int j = r - sh_prefix[lo];
-          want[u] = f.ffn_rank + j * f.ffn_size;
-          who[u] = lo;
-          v[u] = sidx[j];
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 8; u++)
-        if (who[u] >= 0 && v[u] != want[u]) bad_sidx[who[u]] = 1;
-    }
-  }
-  __syncthreads();
   __shared__ int ok_s;
   if (tid == 0) {
     int first = 0;
     for (int i = 0; i < f.n_peers && !first; i++) {
       int e = err[i];
-      if (!e && bad_sidx[i]) e = AFD_ERR_SHAPE;
+      if (!e && shared_n[i] > 0 && bad_sidx[i]) e = AFD_ERR_SHAPE;
       first = e;
     }
     if (!first) first = item_err;

@@ -65,7 +65,7 @@ enum {
 /* Header words.  [RFC-GPU] "Window and slot layout": a fixed 12 int32 words
  * followed by expert_counts[expert_per_rank]; magic "AFDG", a version, and
  * bit 1 of the flags word is the shutdown sentinel.  The page names the
- * fields but not their positions; the order below is this build's reading. */
+ * fields but not their positions; the order below is this implementation's reading. */
 enum {
   H_MAGIC = 0, H_VERSION, H_FLAGS, H_SEQ, H_ECHO_SEQ, H_LAYER, H_STAGE,
   H_NUM_TOKENS, H_ROUTED_TOKENS, H_SHARED_TOKENS, H_NUM_EXPERTS, H_LEN,
@@ -138,7 +138,7 @@ static int64_t orc_round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; 
  *   window = [ flag[num_regions * ring_depth] | slot(0,0) | slot(0,1) | ... ]
  *   slot   = [ header | route_table | routed_x | shared_idx | shared_x ]
  * with every field 256-byte aligned; one layout serves both directions.
- * This build also aligns every field to the activation row pitch (hidden *
+ * This implementation also aligns every field to the activation row pitch (hidden *
  * element size), so the unit is lcm(256, row pitch): any payload row is then
  * a whole row of the window read as a [rows, hidden] matrix.  Field sizes:
  * header (12 + E) int32, route_table [token_cap, topk] int32, routed_x and
@@ -195,7 +195,7 @@ int orc_slot_layout(int num_regions, int ring_depth, int token_cap, int topk,
 /* ------------------------------------------------------------------------ */
 
 /* Experts of FFN rank r among F: a contiguous block; the pages fix no
- * placement, and this build reads it as the balanced linear one -- the
+ * placement, and this implementation reads it as the balanced linear one -- the
  * first E mod F ranks hold one expert more than the others. */
 void orc_expert_range(int E, int F, int r, int* first, int* count) {
   int base = E / F, rem = E % F;
@@ -233,7 +233,7 @@ static uint64_t* orc_flag(uint8_t* win, int region, int ring, int ring_depth) {
  * header, then the flag = seq ([RFC-GPU] "Window and slot layout": the flag
  * is the sender's monotonically increasing seq and is written after the
  * payload).  The dispatch route_table is left untouched: routing happens on
- * the FFN side in this build.  Parity: pinned by the round-trip test. */
+ * the FFN side in this implementation.  Parity: pinned by the round-trip test. */
 int orc_pack_slot(uint8_t* win, const orc_layout* L, int ring_depth, int region,
                   int stage, int layer, const void* x, int n_tokens, int hidden,
                   int act_bytes, int token_cap, int num_experts, int with_shared,
@@ -314,7 +314,7 @@ int orc_split_sizes(int total, int n_peers, const int* seq_lens, int n_lens,
 /* ------------------------------------------------------------------------ */
 
 /* Router logits for one token, l_e = sum_h x_h * Wg[h, e] (+ b_e), in fp32
- * in this build's canonical reduction order (the pages fix none):
+ * in this implementation's canonical reduction order (the pages fix none):
  *   partial_l = fp32 fused multiply-add chain over h = l, l+32, l+64, ...
  *               ascending, starting from +0 (l = 0..31);
  *   then a butterfly: for off = 16, 8, 4, 2, 1: v_l <- v_l + v_(l xor off);

@@ -150,17 +150,21 @@ def stage_work(w, T, nz=None):
     H, I, Is, k, E = w.hidden, w.inter, w.shared_inter, w.topk, w.num_experts
     nz = E if nz is None else nz
     ab = w.act_bytes
+    # the routed partial outputs y and the shared output s stay fp32 up to
+    # the combine (its weighted sum may cancel), so they count 4 bytes each
     return {
         "router": {"flops": 2 * T * H * E, "bytes": T * H * ab + H * E * 4 + T * k * 8},
-        "gather": {"bytes": (T * k + T) * H * ab * 2},
+        # each token row read once from its slot, each routed copy written
+        # once (the shared expert reads its rows in place)
+        "gather": {"bytes": T * H * ab + T * k * H * ab},
         # weights of the experts with rows + the shared expert, rows in, outputs
         "gemm_swiglu": {"flops": 2 * T * H * 2 * (k * I + Is),
                         "bytes": (nz * 2 * I + 2 * Is) * H * 2 + (T * k + T) * H * ab
                         + (T * k * I + T * Is) * ab},
         "gemm_down": {"flops": 2 * T * H * (k * I + Is),
                       "bytes": (nz * I + Is) * H * 2 + (T * k * I + T * Is) * ab
-                      + T * k * H * ab + T * H * 4},
-        "combine_split": {"bytes": T * k * H * ab + T * H * 4 + T * H * ab + T * k * 8},
+                      + T * k * H * 4 + T * H * 4},
+        "combine_split": {"bytes": T * k * H * 4 + T * H * 4 + T * H * ab + T * k * 8},
     }
 
 
@@ -171,7 +175,8 @@ def stage_work_grouped(w, T, Rr, nz=None):
     nz = w.num_experts if nz is None else nz
     ab = w.act_bytes
     return {
-        "gather": {"bytes": (Rr + T) * H * ab * 2},
+        # each received row read once and placed once
+        "gather": {"bytes": Rr * H * ab * 2},
         "gemm_swiglu": {"flops": 2 * H * 2 * (Rr * I + T * Is),
                         "bytes": (nz * 2 * I + 2 * Is) * H * 2 + (Rr + T) * H * ab
                         + (Rr * I + T * Is) * ab},

@@ -83,6 +83,7 @@ SIGNATURES = [
     ("afd_get_window", _I, [_P, _I, C.POINTER(_P), C.POINTER(_I64)]),
     ("afd_get_workspace", _I, [_P, _I, C.POINTER(_P), C.POINTER(_I64)]),
     ("afd_get_stats", _I, [_P, C.POINTER(afd_stats)]),
+    ("afd_last_expert_counts", _I, [_P, C.POINTER(C.c_int32), _I, C.POINTER(C.c_int)]),
     ("afd_launch_count", _I64, [_P]),
     ("afd_strerror", C.c_char_p, [_I]),
     ("afd_profile", _I, [_P, _I]),
@@ -242,6 +243,14 @@ def afd_get_stats(ctx):
     s = afd_stats()
     _check(lib().afd_get_stats(ctx, C.byref(s)), "afd_get_stats")
     return s
+
+
+def afd_last_expert_counts(ctx, n=256):
+    """Per-expert counts of the last step (a list of num_experts ints)."""
+    buf = (C.c_int32 * n)()
+    ne = C.c_int(0)
+    _check(lib().afd_last_expert_counts(ctx, buf, n, C.byref(ne)), "afd_last_expert_counts")
+    return [int(v) for v in buf[:min(n, ne.value)]]
 
 
 def afd_launch_count(ctx):

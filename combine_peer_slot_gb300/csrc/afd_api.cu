@@ -350,7 +350,10 @@ int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out) {
   const int64_t Tm = c->tmax, k = cfg->topk, H = cfg->hidden, E = cfg->num_experts;
   const int64_t I = cfg->inter, Is = cfg->shared_inter;
   const int64_t ab = c->act_f32 ? 4 : 2;
-  const int64_t yb = c->act_f32 ? 4 : 2;
+  // routed expert outputs y: fp32 in the token form (the combine sums them
+  // before the one rounding to the activation type), the activation type in
+  // the grouped form (the rows that go back); sized for the wider
+  const int64_t yb = 4;
   struct Part { int64_t bytes; } parts[] = {
       {4},                                   // status
       {(int64_t)cfg->num_peers * cfg->ring_depth * 8},  // seen
@@ -1014,7 +1017,11 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
       a2.out[0] = ws.y;
       a2.out[1] = ws.s;
       a2.ldo[0] = a2.ldo[1] = c.hidden;
-      a2.out_f32[0] = 0;
+      // token form: y stays fp32 up to the combine, whose weighted sum of a
+      // token's k outputs may cancel to far less than each of them (a bf16
+      // y would be rounded by up to 2^-9 of itself before that sum); the
+      // grouped form returns each row's output in the activation type
+      a2.out_f32[0] = grouped ? 0 : 1;
       a2.out_f32[1] = 1;
       if (in_place) {  // outputs straight into the return slots (rows = window rows)
         a2.out[0] = a2.out[1] = ctx->win[1];
@@ -1073,7 +1080,7 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
       s2.out[0] = ws.y;
       s2.out[1] = ws.s;
       s2.ldo[0] = s2.ldo[1] = c.hidden;
-      s2.out_f32[0] = ctx->act_f32;
+      s2.out_f32[0] = ctx->act_f32 || !grouped;
       s2.out_f32[1] = 1;
       s2.K[0] = c.inter;
       s2.K[1] = c.shared_inter;
@@ -1093,7 +1100,7 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
                                      : launch_scatter_grouped(lc, ctx->geom, ctx->win[1], f, ws,
                                                               c.hidden, ctx->act_f32, has_shared))
                          : launch_combine(lc, ctx->geom, ctx->win[1], f, ws, c.hidden, c.topk,
-                                          ctx->act_f32, has_shared, ctx->act_f32),
+                                          ctx->act_f32, has_shared),
                  grouped ? "scatter" : "combine");
   if (rc) return rc;
   mark(7);
@@ -1196,6 +1203,17 @@ int afd_get_stats(afd_ctx* ctx, afd_stats* out) {
   out->last_total_tokens = ctx->last_T;
   out->num_sms = ctx->num_sms;
   out->forwards = ctx->forwards;
+  return AFD_OK;
+}
+
+int afd_last_expert_counts(afd_ctx* ctx, int32_t* counts, int n, int* n_experts) {
+  if (!ctx || !counts || n < 1) return AFD_ERR_ARG;
+  if (cuda_fail(cudaStreamSynchronize(ctx->stream), "stream sync")) return AFD_ERR_CUDA;
+  const int m = std::min(n, ctx->cfg.num_experts);
+  if (cuda_fail(cudaMemcpy(counts, ctx->ws.counts, (size_t)m * 4, cudaMemcpyDeviceToHost),
+                "expert counts read"))
+    return AFD_ERR_CUDA;
+  if (n_experts) *n_experts = ctx->cfg.num_experts;
   return AFD_OK;
 }
 

@@ -393,7 +393,10 @@ cudaError_t launch_item_head(const LaunchCtx& lc, const WinGeom& g, const uint8_
 int router_blocks(int total_tokens);
 size_t router_min_smem_bytes(int hidden, int E, int act_f32);
 // router: logits [T, E] fp32 (caller's scratch), then top-k / gate weights
-// into ws.ids / ws.w and, if hist is not NULL, the per-16-token histograms
+// into ws.ids / ws.w and, if hist is not NULL, the per-16-token histograms.
+// Without hist (the allocation-free entry point, which has no status poll)
+// an error recorded in ws.status makes the top-k write id -1 and a NaN
+// weight for every token instead of leaving the outputs unwritten.
 cudaError_t launch_router(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                           const FanIn& f, const DevWS& ws, int hidden, int act_f32,
                           const float* WgQ, const float* bias, int E, int k, int renorm,
@@ -414,7 +417,7 @@ cudaError_t launch_gemm_tc2(const LaunchCtx& lc, const GemmArgs& a);
 cudaError_t launch_gemm_simt(const LaunchCtx& lc, const SimtArgs& a, int max_groups);
 cudaError_t launch_combine(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret,
                            const FanIn& f, const DevWS& ws, int hidden, int k, int act_f32,
-                           int has_shared, int y_f32);
+                           int has_shared);
 cudaError_t launch_return_header(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret,
                                  const uint8_t* win, const FanIn& f, const DevWS& ws, int E,
                                  int k);

@@ -1138,7 +1138,9 @@ k_router_logits_tw2(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn
 // a1 router, part 2: top-k on the logits (ties -> lower expert index, NaN
 // below every number) and the gate weights from a softmax over all E
 // (sums carried as float-float); one warp per token, 16 tokens per CTA,
-// whose per-expert histogram (hist[cta][e]) feeds the plan.
+// whose per-expert histogram (hist[cta][e]) feeds the plan.  With no hist
+// (the allocation-free router, whose caller cannot poll a status word) a
+// recorded error leaves id -1 and a NaN weight in every output instead.
 template <bool kDev>
 __global__ void __launch_bounds__(kRtTok * 32)
 k_router_topk(const __grid_constant__ FanIn fp, DevWS ws, const float* __restrict__ logits, int E, int k, int renorm,
@@ -1160,7 +1162,13 @@ k_router_topk(const __grid_constant__ FanIn fp, DevWS ws, const float* __restric
   if (threadIdx.x == 0) skip = read_status(ws.status);
   for (int e = threadIdx.x; e < E; e += blockDim.x) hs[e] = 0;
   __syncthreads();
-  if (skip) return;
+  if (skip) {
+    if (!hist && t < f.total && lane < k) {
+      ws.ids[(int64_t)t * k + lane] = -1;
+      ws.w[(int64_t)t * k + lane] = __int_as_float(0x7fc00000);
+    }
+    return;
+  }
   if (t < f.total) {
     uint32_t taken = 0;  // bit m: expert lane + 32m chosen (E <= 256)
     float top_logit = 0.0f;
@@ -1803,20 +1811,23 @@ __global__ void __launch_bounds__(kThreads) k_gemm_simt(SimtArgs a) {
 // a7 combine + split: out[t] = sum_{j ascending} w[t,j] * y[inv[t,j]] + s[t]
 // in fp32 (fused multiply-add in j order, then + s), rounded to the
 // activation type and written straight into the return slot of t's peer at
-// its local row; the route_table row gets the chosen ids.  Deterministic:
-// each output element is reduced by one thread in a fixed order.
+// its local row; the route_table row gets the chosen ids.  y and s are fp32
+// (the weighted sum may cancel to far less than its terms, so they are
+// rounded only once, here).  Deterministic: each output element is reduced
+// by one thread in a fixed order.
 // ---------------------------------------------------------------------------
-template <bool ACT_F32, bool Y_F32, int kBatch, bool kDev>
+template <bool ACT_F32, int kBatch, bool kDev>
 __global__ void __launch_bounds__(kThreads)
 k_combine(uint8_t* ret, WinGeom g, const __grid_constant__ FanIn fp, DevWS ws, int hidden, int k, int has_shared) {
   grid_dep_wait();
   grid_dep_launch();
   const FanIn& f = step_item<kDev>(fp, ws.item);
   if (read_status(ws.status)) return;
-  // 8 features per lane step: 16-byte loads of bf16 y (two of fp32 y)
+  // 8 features per lane step: two 16-byte loads of a partial's fp32 row
   constexpr int kVec = 8;
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * (blockDim.x >> 5);
+  const float* __restrict__ y = reinterpret_cast<const float*>(ws.y);
   // work item = (token, block of 256 features): a small fan-in still spreads
   // over every SM
   const int nfb = (hidden + 32 * kVec - 1) / (32 * kVec);
@@ -1835,113 +1846,63 @@ k_combine(uint8_t* ret, WinGeom g, const __grid_constant__ FanIn fp, DevWS ws, i
         reinterpret_cast<int32_t*>(slot + g.route_table)[(int64_t)local * k + lane] =
             ws.ids[(int64_t)t * k + lane];
     }
-    {
-      // every lane takes part in the shuffles; lanes past hidden skip memory
-      const int c0 = fb * 32 * kVec + lane * kVec;
-      const bool valid = c0 < hidden;
-      const int c = valid ? c0 : 0;
-      float acc[kVec];
+    // every lane takes part in the shuffles; lanes past hidden skip memory
+    const int c0 = fb * 32 * kVec + lane * kVec;
+    const bool valid = c0 < hidden;
+    const int c = valid ? c0 : 0;
+    float acc[kVec];
 #pragma unroll
-      for (int q = 0; q < kVec; q++) acc[q] = 0.0f;
-      if constexpr (kBatch == 1) {
-        for (int j = 0; j < k; j++) {
-          const int pos = __shfl_sync(0xffffffffu, my_pos, j);
-          const float wj = __shfl_sync(0xffffffffu, my_w, j);
-          float yv[kVec];
-          if constexpr (Y_F32) {
-            const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(ws.y) +
-                                                                (int64_t)pos * hidden + c);
-            const float4 a = valid ? src[0] : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float4 b = valid ? src[1] : make_float4(0.f, 0.f, 0.f, 0.f);
-            yv[0] = a.x; yv[1] = a.y; yv[2] = a.z; yv[3] = a.w;
-            yv[4] = b.x; yv[5] = b.y; yv[6] = b.z; yv[7] = b.w;
-          } else {
-            const uint4 v = valid ? *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(ws.y) +
-                                                                   (int64_t)pos * hidden + c)
-                                  : make_uint4(0, 0, 0, 0);
-            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+    for (int q = 0; q < kVec; q++) acc[q] = 0.0f;
+    // rounds of up to kBatch partials: their rows are all loaded before the
+    // multiply-adds, which still run in ascending j (8 for small fan-ins,
+    // where few warps must keep many loads in flight; 4 for large ones; 1
+    // for fp32 activations)
+    for (int j0 = 0; j0 < k; j0 += kBatch) {
+      float4 raw[kBatch][2];
+      float wj[kBatch];
 #pragma unroll
-            for (int m = 0; m < 4; m++) {
-              yv[2 * m] = __uint_as_float(w4[m] << 16);
-              yv[2 * m + 1] = __uint_as_float(w4[m] & 0xffff0000u);
-            }
-          }
-#pragma unroll
-          for (int q = 0; q < kVec; q++) acc[q] = __fmaf_rn(wj, yv[q], acc[q]);
-        }
-      } else {
-        // rounds of up to kBatch partials: their rows are all loaded before the
-        // multiply-adds, which still run in ascending j (8 for small fan-ins,
-        // where few warps must keep many loads in flight; 4 for large ones,
-        // measured faster than 1, 2, 3, 6 and 8, which trade loads in flight
-        // against registers and resident warps)
-        for (int j0 = 0; j0 < k; j0 += kBatch) {
-          uint4 raw[kBatch][Y_F32 ? 2 : 1];
-          float wj[kBatch];
-  #pragma unroll
-          for (int u = 0; u < kBatch; u++) {
-            const int j = j0 + u;
-            const int pos = __shfl_sync(0xffffffffu, my_pos, j & 31);
-            wj[u] = __shfl_sync(0xffffffffu, my_w, j & 31);
-            const bool ld = valid && j < k;
-            if constexpr (Y_F32) {
-              const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const float*>(ws.y) +
-                                                                (int64_t)pos * hidden + c);
-              raw[u][0] = ld ? src[0] : make_uint4(0, 0, 0, 0);
-              raw[u][1] = ld ? src[1] : make_uint4(0, 0, 0, 0);
-            } else {
-              raw[u][0] = ld ? *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(ws.y) +
-                                                               (int64_t)pos * hidden + c)
-                             : make_uint4(0, 0, 0, 0);
-            }
-          }
-  #pragma unroll
-          for (int u = 0; u < kBatch; u++) {
-            if (j0 + u >= k) break;
-            float yv[kVec];
-            if constexpr (Y_F32) {
-              yv[0] = __uint_as_float(raw[u][0].x); yv[1] = __uint_as_float(raw[u][0].y);
-              yv[2] = __uint_as_float(raw[u][0].z); yv[3] = __uint_as_float(raw[u][0].w);
-              yv[4] = __uint_as_float(raw[u][1].x); yv[5] = __uint_as_float(raw[u][1].y);
-              yv[6] = __uint_as_float(raw[u][1].z); yv[7] = __uint_as_float(raw[u][1].w);
-            } else {
-              const uint32_t w4[4] = {raw[u][0].x, raw[u][0].y, raw[u][0].z, raw[u][0].w};
-  #pragma unroll
-              for (int m = 0; m < 4; m++) {
-                yv[2 * m] = __uint_as_float(w4[m] << 16);
-                yv[2 * m + 1] = __uint_as_float(w4[m] & 0xffff0000u);
-              }
-            }
-  #pragma unroll
-            for (int q = 0; q < kVec; q++) acc[q] = __fmaf_rn(wj[u], yv[q], acc[q]);
-          }
-        }
+      for (int u = 0; u < kBatch; u++) {
+        const int j = j0 + u;
+        const int pos = __shfl_sync(0xffffffffu, my_pos, j & 31);
+        wj[u] = __shfl_sync(0xffffffffu, my_w, j & 31);
+        const bool ld = valid && j < k;
+        const float4* src = reinterpret_cast<const float4*>(y + (int64_t)pos * hidden + c);
+        raw[u][0] = ld ? src[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+        raw[u][1] = ld ? src[1] : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      if (valid) {  // lanes past hidden write nothing
-        if (has_shared) {  // zero rows for peers that sent no shared rows
-          const float4* sp = reinterpret_cast<const float4*>(ws.s + (int64_t)t * hidden + c);
-          const float4 a = sp[0], b = sp[1];
-          acc[0] = __fadd_rn(acc[0], a.x); acc[1] = __fadd_rn(acc[1], a.y);
-          acc[2] = __fadd_rn(acc[2], a.z); acc[3] = __fadd_rn(acc[3], a.w);
-          acc[4] = __fadd_rn(acc[4], b.x); acc[5] = __fadd_rn(acc[5], b.y);
-          acc[6] = __fadd_rn(acc[6], b.z); acc[7] = __fadd_rn(acc[7], b.w);
-        }
-        if constexpr (ACT_F32) {
-          float4* dst = reinterpret_cast<float4*>(slot + g.routed_x + ((int64_t)local * hidden + c) * 4);
-          dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-          dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-        } else {
-          uint4 o;
-          __nv_bfloat162 p0 = __floats2bfloat162_rn(acc[0], acc[1]);
-          __nv_bfloat162 p1 = __floats2bfloat162_rn(acc[2], acc[3]);
-          __nv_bfloat162 p2 = __floats2bfloat162_rn(acc[4], acc[5]);
-          __nv_bfloat162 p3 = __floats2bfloat162_rn(acc[6], acc[7]);
-          o.x = *reinterpret_cast<uint32_t*>(&p0);
-          o.y = *reinterpret_cast<uint32_t*>(&p1);
-          o.z = *reinterpret_cast<uint32_t*>(&p2);
-          o.w = *reinterpret_cast<uint32_t*>(&p3);
-          *reinterpret_cast<uint4*>(slot + g.routed_x + ((int64_t)local * hidden + c) * 2) = o;
-        }
+#pragma unroll
+      for (int u = 0; u < kBatch; u++) {
+        if (j0 + u >= k) break;
+        const float yv[kVec] = {raw[u][0].x, raw[u][0].y, raw[u][0].z, raw[u][0].w,
+                                raw[u][1].x, raw[u][1].y, raw[u][1].z, raw[u][1].w};
+#pragma unroll
+        for (int q = 0; q < kVec; q++) acc[q] = __fmaf_rn(wj[u], yv[q], acc[q]);
+      }
+    }
+    if (valid) {  // lanes past hidden write nothing
+      if (has_shared) {  // zero rows for peers that sent no shared rows
+        const float4* sp = reinterpret_cast<const float4*>(ws.s + (int64_t)t * hidden + c);
+        const float4 a = sp[0], b = sp[1];
+        acc[0] = __fadd_rn(acc[0], a.x); acc[1] = __fadd_rn(acc[1], a.y);
+        acc[2] = __fadd_rn(acc[2], a.z); acc[3] = __fadd_rn(acc[3], a.w);
+        acc[4] = __fadd_rn(acc[4], b.x); acc[5] = __fadd_rn(acc[5], b.y);
+        acc[6] = __fadd_rn(acc[6], b.z); acc[7] = __fadd_rn(acc[7], b.w);
+      }
+      if constexpr (ACT_F32) {
+        float4* dst = reinterpret_cast<float4*>(slot + g.routed_x + ((int64_t)local * hidden + c) * 4);
+        dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      } else {
+        uint4 o;
+        __nv_bfloat162 p0 = __floats2bfloat162_rn(acc[0], acc[1]);
+        __nv_bfloat162 p1 = __floats2bfloat162_rn(acc[2], acc[3]);
+        __nv_bfloat162 p2 = __floats2bfloat162_rn(acc[4], acc[5]);
+        __nv_bfloat162 p3 = __floats2bfloat162_rn(acc[6], acc[7]);
+        o.x = *reinterpret_cast<uint32_t*>(&p0);
+        o.y = *reinterpret_cast<uint32_t*>(&p1);
+        o.z = *reinterpret_cast<uint32_t*>(&p2);
+        o.w = *reinterpret_cast<uint32_t*>(&p3);
+        *reinterpret_cast<uint4*>(slot + g.routed_x + ((int64_t)local * hidden + c) * 2) = o;
       }
     }
   }
@@ -2399,22 +2360,19 @@ cudaError_t launch_gemm_simt(const LaunchCtx& lc, const SimtArgs& a, int max_gro
 }
 
 cudaError_t launch_combine(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret, const FanIn& f,
-                           const DevWS& ws, int hidden, int k, int act_f32, int has_shared,
-                           int y_f32) {
+                           const DevWS& ws, int hidden, int k, int act_f32, int has_shared) {
   if (f.total == 0) return cudaSuccess;
   const int64_t items = (int64_t)f.total * ((hidden + 255) / 256);
   const int grid = grid_for(items, kThreads / 32, lc.num_sms * 8);
   const bool small = items < (int64_t)lc.num_sms * 64;
   const bool d = f.dev != 0;
-  decltype(&k_combine<true, true, 1, false>) kern = nullptr;
-  if (act_f32 && y_f32)
-    kern = d ? k_combine<true, true, 1, true> : k_combine<true, true, 1, false>;
-  else if (!act_f32 && y_f32)
-    kern = d ? k_combine<false, true, 1, true> : k_combine<false, true, 1, false>;
-  else if (!act_f32 && !y_f32)
-    kern = small ? (d ? k_combine<false, false, 8, true> : k_combine<false, false, 8, false>)
-                 : (d ? k_combine<false, false, 4, true> : k_combine<false, false, 4, false>);
-  if (!kern) return cudaErrorInvalidValue;
+  // y is fp32 in the token form
+  decltype(&k_combine<true, 1, false>) kern = nullptr;
+  if (act_f32)
+    kern = d ? k_combine<true, 1, true> : k_combine<true, 1, false>;
+  else
+    kern = small ? (d ? k_combine<false, 8, true> : k_combine<false, 8, false>)
+                 : (d ? k_combine<false, 4, true> : k_combine<false, 4, false>);
   return launch_k(lc, kern, grid, kThreads, 0, ret, g, f, ws, hidden, k, has_shared);
 }
 

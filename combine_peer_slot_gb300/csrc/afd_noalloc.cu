@@ -12,8 +12,12 @@
 // The array is shared by every call: a call rewrites the router weight
 // and clears the status word before the router runs, and calls that overlap
 // on the GPU (different streams, no ordering between them) race on it.
+// Nothing polls the status word: when a bounded wait inside the router
+// gives up, the top-k writes id -1 and a NaN weight for every token, so the
+// failure shows in the caller's own outputs.
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "afd_internal.cuh"
 
@@ -25,28 +29,40 @@ static __device__ __align__(256) float
     g_noalloc_scratch[AFD_NOALLOC_MAX_ROUTER_WEIGHTS + AFD_NOALLOC_MAX_LOGITS + 64];
 
 constexpr int kMaxDevices = 64;
-float* g_scratch_addr[kMaxDevices] = {};
+// per device: the array's device address, looked up once with that device
+// current (two host threads making their first call on one device at once
+// both wait for the one lookup)
+struct ScratchAddr {
+  std::once_flag once;
+  float* ptr = nullptr;
+  cudaError_t err = cudaSuccess;
+};
+ScratchAddr g_scratch[kMaxDevices];
 int64_t g_noalloc_launches = 0;
 
-// Once per device, with that device current: the device address of the
-// array (in host code its name is only a host-side stand-in).
-int scratch_for_current_device(float** out) {
+// In host code the array's name is only a host-side stand-in: its device
+// address must be asked for on each device.
+int scratch_for_current_device(float** out, int* dev_out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
     return AFD_ERR_CUDA;
   }
-  if (!g_scratch_addr[dev]) {
+  ScratchAddr& a = g_scratch[dev];
+  std::call_once(a.once, [&a] {
     void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || !p) {
-      fprintf(stderr, "afd: cudaGetSymbolAddress failed: %s\n", cudaGetErrorString(e));
+    a.err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (a.err == cudaSuccess && !p) a.err = cudaErrorInvalidSymbol;
+    if (a.err != cudaSuccess) {
+      fprintf(stderr, "afd: cudaGetSymbolAddress failed: %s\n", cudaGetErrorString(a.err));
       cudaGetLastError();
-      return AFD_ERR_CUDA;
+    } else {
+      a.ptr = static_cast<float*>(p);
     }
-    g_scratch_addr[dev] = static_cast<float*>(p);
-  }
-  *out = g_scratch_addr[dev];
+  });
+  if (a.err != cudaSuccess) return AFD_ERR_CUDA;
+  *out = a.ptr;
+  *dev_out = dev;
   return AFD_OK;
 }
 
@@ -66,7 +82,8 @@ extern "C" int afd_route_noalloc(const void* x, int n_tokens, int hidden, int ac
   if (n_tokens == 0) return AFD_OK;
   if (!x || !Wg || !ids || !weights || (reinterpret_cast<uintptr_t>(x) & 15)) return AFD_ERR_ARG;
   float* scratch = nullptr;
-  int rc = scratch_for_current_device(&scratch);
+  int dev = 0;
+  int rc = scratch_for_current_device(&scratch, &dev);
   if (rc) return rc;
   float* WgQ = scratch;
   float* logits = scratch + AFD_NOALLOC_MAX_ROUTER_WEIGHTS;
@@ -74,8 +91,6 @@ extern "C" int afd_route_noalloc(const void* x, int n_tokens, int hidden, int ac
       reinterpret_cast<int32_t*>(scratch + AFD_NOALLOC_MAX_ROUTER_WEIGHTS + AFD_NOALLOC_MAX_LOGITS);
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(cuda_stream);
   LaunchCtx lc{stream, 0, &g_noalloc_launches};
-  int dev = 0;
-  cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&lc.num_sms, cudaDevAttrMultiProcessorCount, dev);
   if (cudaMemsetAsync(status, 0, sizeof(int32_t), stream) != cudaSuccess) {
     cudaGetLastError();

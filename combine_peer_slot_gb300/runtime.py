@@ -155,14 +155,6 @@ class Runner:
         d["bias"] = self.host["bias"]
         return d
 
-    def oracle_cfg(self):
-        w = self.w
-        return dict(num_regions=w.num_peers, ring_depth=self.cfg.ring_depth, token_cap=w.token_cap,
-                    hidden=w.hidden,
-                    act_bytes=w.act_bytes, num_experts=w.num_experts, topk=w.topk, inter=w.inter,
-                    shared_inter=w.shared_inter, renorm=w.renorm,
-                    max_total_tokens=self.cfg.max_total_tokens, routed_scaling=w.routed_scaling)
-
     def close(self):
         if self.ctx:
             A.afd_destroy(self.ctx)

@@ -183,7 +183,7 @@ typedef struct afd_layout {
 #define AFD_WS_INV 5        /* int32 [T*topk] flattened index -> position */
 #define AFD_WS_XP 6         /* act [T*topk, hidden] permuted routed rows (shared rows stay in the slots) */
 #define AFD_WS_H 7          /* act [T*topk, inter] routed SwiGLU output */
-#define AFD_WS_Y 8          /* act [T*topk, hidden] routed down projection */
+#define AFD_WS_Y 8          /* fp32 [T*topk, hidden] routed down projection (grouped form: act) */
 #define AFD_WS_HS 9         /* act [T, shared_inter] shared SwiGLU output */
 #define AFD_WS_S 10         /* fp32 [T, hidden] shared expert output */
 #define AFD_WS_STATUS 11    /* int32 device status word */
@@ -483,6 +483,16 @@ int afd_get_workspace(afd_ctx* ctx, int which, void** dev_ptr, int64_t* bytes);
 
 int afd_get_stats(afd_ctx* ctx, afd_stats* out);
 
+/* Synchronise the stream and copy the per-expert counts of the last step
+ * that ran (token form: routed partials per expert; grouped form: received
+ * rows per expert) into counts (host int32 [n]); the first min(n,
+ * num_experts) experts are copied and *n_experts (may be NULL) receives
+ * num_experts.  These are the counts the return headers carry per peer
+ * (Async GPU Connector, "Window and slot layout": expert_counts travel in
+ * band), summed over the step's peers.  Zeros before the first step.
+ * Errors: AFD_ERR_ARG, AFD_ERR_CUDA. */
+int afd_last_expert_counts(afd_ctx* ctx, int32_t* counts, int n, int* n_experts);
+
 /* Kernel launches the library issued on this context since creation. */
 int64_t afd_launch_count(afd_ctx* ctx);
 
@@ -519,14 +529,18 @@ int afd_stage_times(afd_ctx* ctx, float* ms, int n, int64_t* forwards);
  * the router logits and a status word) is a file-scope device array of
  * AFD_NOALLOC_MAX_ROUTER_WEIGHTS + AFD_NOALLOC_MAX_LOGITS + 64 floats
  * (about 5 MiB) that every GPU loading this library holds until exit; the
- * first call on a device looks up that array's device address.  All calls
- * share the array: each call rewrites it and clears the status word first,
- * and calls that overlap on the GPU race on it.
+ * first call on a device looks up that array's device address (once per
+ * device, safe from several host threads).  All calls share the array: each
+ * call rewrites it and clears the status word first, and calls that overlap
+ * on the GPU race on it.
  * 4 * ceil(num_experts / 4) * hidden above
  * AFD_NOALLOC_MAX_ROUTER_WEIGHTS or n_tokens * num_experts above
  * AFD_NOALLOC_MAX_LOGITS returns AFD_ERR_CAPACITY; bad arguments
  * AFD_ERR_ARG; a failing CUDA call AFD_ERR_CUDA.  Asynchronous; allocates
- * nothing. */
+ * nothing.  Device-side failures (a bounded wait inside the router that
+ * gives up) cannot be returned by an asynchronous call and nothing polls
+ * the status word: instead every ids entry of the call is then -1 and every
+ * weight NaN. */
 #define AFD_NOALLOC_MAX_ROUTER_WEIGHTS 262144
 #define AFD_NOALLOC_MAX_LOGITS 1048576
 int afd_route_noalloc(const void* x, int n_tokens, int hidden, int act_dtype, const float* Wg,

@@ -10,6 +10,15 @@ BF16_TOL = 2e-2   # max |err| <= 2e-2 * rms(oracle), bf16 activations
 F32_TOL = 1e-4    # max |err| <= 1e-4 * rms(oracle), fp32 activations
 
 
+def oracle_cfg(run):
+    """The oracle's configuration for a runner's context."""
+    w = run.w
+    return dict(num_regions=w.num_peers, ring_depth=run.cfg.ring_depth, token_cap=w.token_cap,
+                hidden=w.hidden, act_bytes=w.act_bytes, num_experts=w.num_experts, topk=w.topk,
+                inter=w.inter, shared_inter=w.shared_inter, renorm=w.renorm,
+                max_total_tokens=run.cfg.max_total_tokens, routed_scaling=w.routed_scaling)
+
+
 def tol_for(w):
     return BF16_TOL if w.act == "bf16" else F32_TOL
 
@@ -80,7 +89,7 @@ def run_and_compare_full(run, slots=None, layer=0, pack=True):
     assert run.poll() == 0
     win = run.window(A.AFD_DIR_DISPATCH).cpu().numpy()
     ret = run.window(A.AFD_DIR_RETURN).cpu().numpy()
-    c = run.oracle_cfg()
+    c = oracle_cfg(run)
     ret_orc = np.zeros_like(win)
     seen = np.zeros(w.num_peers, np.uint64)
     lens = [w.seq_lens[p] for p in slots]
@@ -89,6 +98,7 @@ def run_and_compare_full(run, slots=None, layer=0, pack=True):
     assert rc == 0
     T, k = sum(lens), w.topk
     check_plan_exact(run, T, r["ids"])
+    assert A.afd_last_expert_counts(run.ctx) == [int(v) for v in r["counts"]]
     wts = ws_array(run, A.AFD_WS_WEIGHTS, T * k, np.float32).reshape(T, k)
     assert np.allclose(wts, r["w"], rtol=1e-6, atol=0), np.abs(wts / r["w"] - 1).max()
     errs = []
@@ -110,60 +120,3 @@ def run_and_compare_full(run, slots=None, layer=0, pack=True):
     e = rel_err(got, ref)
     assert e <= tol_for(w), f"max|err|/rms = {e:.3e} > {tol_for(w)}"
     return e, r
-
-
-def sample_tokens(lens, per_peer=6, seed=0):
-    rng = np.random.default_rng(seed)
-    toks, start = [], 0
-    for n in lens:
-        if n:
-            pick = {start, start + n - 1}
-            pick.update((start + rng.integers(0, n, size=per_peer)).tolist())
-            toks.extend(sorted(pick))
-        start += n
-    return np.array(toks, np.int32)
-
-
-def run_and_compare_sampled(run, layer=0, per_peer=6, nthreads=0, check_routing=True):
-    """Full-size comparison: routing, counts, offsets, permutation bit-exact
-    over every token; outputs on sampled tokens (first, last and random rows
-    of every peer) computed one by one by the oracle."""
-    w = run.w
-    slots = list(range(w.num_peers))
-    lens = [w.seq_lens[p] for p in slots]
-    run.pack_all(layer)
-    rc = run.forward(layer)
-    assert rc == 0, A.strerror(rc)
-    assert run.poll() == 0
-    win = run.window(A.AFD_DIR_DISPATCH).cpu().numpy()
-    ret = run.window(A.AFD_DIR_RETURN).cpu().numpy()
-    T, k = sum(lens), w.topk
-    wts = run.weights_numpy(layer)
-    if check_routing:
-        X = np.concatenate([run.host["x"][p] for p in slots])
-        ids_ref, w_ref, gap = O.route(X, w.act_bytes, wts["Wg"], wts["bias"], k, w.renorm,
-                                      w.routed_scaling, nthreads=nthreads)
-        check_plan_exact(run, T, ids_ref)
-        g = ws_array(run, A.AFD_WS_WEIGHTS, T * k, np.float32).reshape(T, k)
-        assert np.allclose(g, w_ref, rtol=1e-6, atol=0)
-    toks = sample_tokens(lens, per_peer, seed=layer)
-    c = run.oracle_cfg()
-    ids_s, w_s, out_s = O.forward_tokens(c, win, wts, 0, lens, slots, toks, nthreads=nthreads)
-    prefix = np.concatenate([[0], np.cumsum(lens)])
-    got = np.zeros_like(out_s)
-    for q, t in enumerate(toks):
-        p = int(np.searchsorted(prefix, t, side="right") - 1)
-        local = int(t - prefix[p])
-        got[q] = return_rows(ret, run, slots[p], local + 1)[local]
-        assert np.array_equal(route_table(ret, run, slots[p], local + 1)[local], ids_s[q])
-    e = rel_err(got, out_s)
-    assert e <= tol_for(w), f"max|err|/rms = {e:.3e} > {tol_for(w)}"
-    # return headers: per-peer expert counts from the oracle's routing
-    if check_routing:
-        for i, p in enumerate(slots):
-            h = header(ret, run, p)
-            n = lens[i]
-            assert h[7] == n and h[8] == n * k and h[3] == run.last_seq[(p, 0)]
-            cnt = np.bincount(ids_ref[prefix[i]:prefix[i] + n].ravel(), minlength=w.num_experts)
-            assert np.array_equal(h[12:], cnt)
-    return e

@@ -26,8 +26,17 @@ def test_gemm_work_counted_by_hand():
     assert sw["bytes"] == weights + rows_in + rows_out
     dn = bench.stage_work(w, T, E)["gemm_down"]
     assert dn["flops"] == 2 * H * (T * k * I + T * Is)
-    # routed partials in bf16, the shared expert's output in fp32
-    assert dn["bytes"] == (E * I * H + Is * H) * 2 + (T * k * I + T * Is) * 2 + T * k * H * 2 + T * H * 4
+    # routed partials and the shared expert's output in fp32
+    assert dn["bytes"] == (E * I * H + Is * H) * 2 + (T * k * I + T * Is) * 2 + T * k * H * 4 + T * H * 4
+
+
+def test_gather_counts_each_row_once():
+    """The gather reads every token row once from its slot and writes each
+    of its k routed copies once; the shared rows are read in place."""
+    w = W.get("v2lite_prefill")
+    T, H, k = w.total_tokens, w.hidden, w.topk
+    assert bench.stage_work(w, T)["gather"]["bytes"] == T * H * 2 + T * k * H * 2
+    assert bench.stage_work_grouped(w, T, T * k)["gather"]["bytes"] == 2 * T * k * H * 2
 
 
 def test_only_experts_with_rows_count():
@@ -53,6 +62,10 @@ def test_grouped_form_matches_token_form_when_rows_agree():
     T = w.total_tokens
     a = bench.stage_work(w, T, w.num_experts)
     b = bench.stage_work_grouped(w, T, T * w.topk, w.num_experts)
-    for s in ("gemm_swiglu", "gemm_down"):
-        assert a[s]["flops"] == b[s]["flops"]
-        assert a[s]["bytes"] == b[s]["bytes"]
+    assert a["gemm_swiglu"]["flops"] == b["gemm_swiglu"]["flops"]
+    assert a["gemm_swiglu"]["bytes"] == b["gemm_swiglu"]["bytes"]
+    assert a["gemm_down"]["flops"] == b["gemm_down"]["flops"]
+    # the grouped form returns each row's output in the activation type,
+    # the token form keeps it fp32 for its combine
+    T, H, k = w.total_tokens, w.hidden, w.topk
+    assert a["gemm_down"]["bytes"] - b["gemm_down"]["bytes"] == T * k * H * (4 - 2)

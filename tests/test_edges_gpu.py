@@ -39,22 +39,26 @@ def test_all_peers_empty():
 
 @pytest.mark.parametrize("shape", [
     dict(num_experts=256, topk=16, hidden=512, inter=64, shared_inter=64, seq_lens=[40, 7]),
-    # every shape carries a shared expert: alone, a token's routed sum can
-    # cancel to a small rms against which the bf16 rounding of each
-    # expert's output (up to 2^-9 of it) exceeds 2e-2 (up to 2.9e-2 seen)
     dict(num_experts=8, topk=8, hidden=256, inter=96, shared_inter=96, seq_lens=[19, 1, 33]),
+    # without a shared expert a token's weighted sum of its k expert outputs
+    # can cancel to far less than each of them; the expert outputs reach
+    # the combine in fp32, so its one rounding is all the output sees
+    dict(num_experts=8, topk=8, hidden=256, inter=96, shared_inter=0, seq_lens=[19, 1, 33]),
     dict(num_experts=16, topk=2, hidden=4096, inter=128, shared_inter=64, seq_lens=[33, 20]),
     dict(num_experts=64, topk=6, hidden=3072, inter=64, shared_inter=64, seq_lens=[25]),
+    dict(num_experts=64, topk=6, hidden=3072, inter=64, shared_inter=0, seq_lens=[25]),
     # ~128 rows per expert take the 256-row tiles; hidden 320 and inter 176
     # give odd k-block counts (5 and 3, the last one partial), so the pair
     # GEMM's last stage carries a single k-block
     dict(num_experts=8, topk=2, hidden=320, inter=176, shared_inter=80, seq_lens=[300, 212]),
-], ids=["E256_k16", "k_equals_E", "hidden4096", "hidden3072", "wide_odd_k"])
+], ids=["E256_k16", "k_equals_E", "k_equals_E_no_shared", "hidden4096", "hidden3072",
+        "hidden3072_no_shared", "wide_odd_k"])
 def test_shapes_at_the_edges(shape):
     """Routing, plan and outputs against the oracle at the shapes' edges:
     256 experts with top-16 (the largest the router covers), top-k equal to
     the expert count, hidden above 2048 (the router's fallback kernels),
-    wide token tiles over odd and partial k-block counts."""
+    wide token tiles over odd and partial k-block counts, layers with and
+    without a shared expert."""
     w = W.custom("fanin", **shape)
     run = R.Runner(w, max_total_tokens=w.total_tokens)
     e, _ = G.run_and_compare_full(run)

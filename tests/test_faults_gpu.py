@@ -36,7 +36,7 @@ def oracle_code(run, layer=0, lens=None, slots=(0, 1), seen=None):
     ret = np.zeros_like(win)
     seen = np.zeros(run.w.num_peers, np.uint64) if seen is None else seen
     lens = list(run.w.seq_lens) if lens is None else lens
-    rc, _ = O.ffn_forward(run.oracle_cfg(), win, ret, run.weights_numpy(min(layer, run.layers - 1)),
+    rc, _ = O.ffn_forward(G.oracle_cfg(run), win, ret, run.weights_numpy(min(layer, run.layers - 1)),
                           layer, 0, lens, list(slots), seen)
     return rc
 

@@ -85,7 +85,7 @@ def run_grouped(w, seed, with_shared=True, slots=None, zero_rows=(), gemm=A.AFD_
     assert run.poll() == 0
     ret = np.zeros_like(win)
     seen = np.zeros(w.num_peers, np.uint64)
-    rc, y64, s64 = O.grouped_forward(run.oracle_cfg(), win, ret, run.weights_numpy(0), 0, 0,
+    rc, y64, s64 = O.grouped_forward(G.oracle_cfg(run), win, ret, run.weights_numpy(0), 0, 0,
                                      [R_[p] for p in slots], [w.seq_lens[p] for p in slots],
                                      slots, seen)
     assert rc == 0

@@ -73,7 +73,19 @@ def test_serialised_launches(workload):
     if workload == "fanin":
         G.run_and_compare_full(run)
     else:
-        G.run_and_compare_sampled(run, per_peer=2)
+        # the full-size step is compared with the oracle row by row in
+        # test_v2lite_prefill_full_size; here the return window of the
+        # serialised launches must equal the default launches' byte for byte
+        ref = R.Runner(w, max_total_tokens=w.total_tokens)
+        wins = []
+        for r in (run, ref):
+            r.pack_all(0)
+            assert r.forward(0) == 0
+            assert r.poll() == 0
+            wins.append(r.window(A.AFD_DIR_RETURN).cpu().numpy())
+        assert np.array_equal(wins[0], wins[1])
+        ref.close()
+    run.close()
 
 
 def test_fanin_reordered_with_empty_peer():
@@ -99,25 +111,36 @@ def test_single_peer_ragged_tiles():
 
 
 def test_v2lite_prefill_full_size():
+    """Every output row of the 13312-token fan-in against the oracle (which
+    runs the same fan-in on all host cores), with routing, plan, headers and
+    route tables bit-exact."""
     w = W.get("v2lite_prefill")
     run = R.Runner(w, max_total_tokens=w.total_tokens)
-    e = G.run_and_compare_sampled(run, per_peer=8)
+    e, _ = G.run_and_compare_full(run)
     print("v2lite max|err|/rms", e)
+    run.close()
 
 
 def test_skewed_full_size():
     w = W.get("skewed")
     run = R.Runner(w, max_total_tokens=w.total_tokens)
-    e = G.run_and_compare_sampled(run, per_peer=4)
+    e, _ = G.run_and_compare_full(run)
+    print("skewed max|err|/rms", e)
     counts = G.ws_array(run, A.AFD_WS_COUNTS, w.num_experts, np.int32)
     assert (counts == 0).any() and counts.max() > 5 * counts.mean()
+    run.close()
 
 
 def test_decode_26_layers():
+    """All 26 layers, every output row of each, through one context."""
     w = W.get("decode")
     run = R.Runner(w, max_total_tokens=w.total_tokens)
+    worst = 0.0
     for layer in range(w.layers):
-        G.run_and_compare_sampled(run, layer=layer, per_peer=1, check_routing=True)
+        e, _ = G.run_and_compare_full(run, layer=layer)
+        worst = max(worst, e)
+    print("decode 26 layers: worst max|err|/rms", worst)
+    run.close()
 
 
 @pytest.mark.parametrize("gemm", [A.AFD_GEMM_TENSOR, A.AFD_GEMM_SIMT])

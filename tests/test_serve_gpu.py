@@ -68,7 +68,7 @@ def check_item_against_oracle(run, stage, layer, counts):
     ret_orc = np.zeros_like(win)
     seen = np.zeros(w.num_peers * run.cfg.ring_depth, np.uint64)
     slots = list(range(w.num_peers))
-    rc, r = O.ffn_forward(run.oracle_cfg(), win.copy(), ret_orc, run.weights_numpy(layer), layer,
+    rc, r = O.ffn_forward(G.oracle_cfg(run), win.copy(), ret_orc, run.weights_numpy(layer), layer,
                           stage, list(counts), slots, seen)
     assert rc == 0
     start, got, ref = 0, [], []

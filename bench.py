@@ -150,8 +150,9 @@ def stage_work(w, T, nz=None):
     H, I, Is, k, E = w.hidden, w.inter, w.shared_inter, w.topk, w.num_experts
     nz = E if nz is None else nz
     ab = w.act_bytes
-    # the routed partial outputs y and the shared output s stay fp32 up to
-    # the combine (its weighted sum may cancel), so they count 4 bytes each
+    # the routed partial outputs y reach the combine as 24-bit floats (3
+    # bytes: its weighted sum may cancel, so bf16 is too coarse) and the
+    # shared output s as fp32
     return {
         "router": {"flops": 2 * T * H * E, "bytes": T * H * ab + H * E * 4 + T * k * 8},
         # each token row read once from its slot, each routed copy written
@@ -163,8 +164,8 @@ def stage_work(w, T, nz=None):
                         + (T * k * I + T * Is) * ab},
         "gemm_down": {"flops": 2 * T * H * (k * I + Is),
                       "bytes": (nz * I + Is) * H * 2 + (T * k * I + T * Is) * ab
-                      + T * k * H * 4 + T * H * 4},
-        "combine_split": {"bytes": T * k * H * 4 + T * H * 4 + T * H * ab + T * k * 8},
+                      + T * k * H * 3 + T * H * 4},
+        "combine_split": {"bytes": T * k * H * 3 + T * H * 4 + T * H * ab + T * k * 8},
     }
 
 

@@ -401,6 +401,8 @@ int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out) {
   c->ws.xp = b + offs[11];
   c->ws.h = b + offs[12];
   c->ws.y = b + offs[13];
+  // low plane of the 24-bit y after the high plane (2 + 1 of the 4 bytes per element)
+  c->ws.y_lo = b + offs[13] + Tm * k * H * 2;
   c->ws.hs = b + offs[14];
   c->ws.s = reinterpret_cast<float*>(b + offs[15]);
   c->ws.hist = reinterpret_cast<int32_t*>(b + offs[18]);
@@ -987,6 +989,7 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
       a1.tmBs[1] = sh_win ? ctx->tmWin32 : ctx->tmXp32;
       a1.out[0] = ws.h;
       a1.out[1] = ws.hs;
+      a1.out_fmt[0] = a1.out_fmt[1] = OUT_ACT;
       a1.ldo[0] = c.inter;
       a1.ldo[1] = c.shared_inter;
       a1.K[0] = a1.K[1] = c.hidden;
@@ -1017,15 +1020,17 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
       a2.out[0] = ws.y;
       a2.out[1] = ws.s;
       a2.ldo[0] = a2.ldo[1] = c.hidden;
-      // token form: y stays fp32 up to the combine, whose weighted sum of a
-      // token's k outputs may cancel to far less than each of them (a bf16
+      // token form: y keeps 24 bits up to the combine, whose weighted sum of
+      // a token's k outputs may cancel to far less than each of them (a bf16
       // y would be rounded by up to 2^-9 of itself before that sum); the
-      // grouped form returns each row's output in the activation type
-      a2.out_f32[0] = grouped ? 0 : 1;
-      a2.out_f32[1] = 1;
+      // grouped form returns each row's output in the activation type; the
+      // shared output stays fp32
+      a2.out_fmt[0] = grouped ? OUT_ACT : OUT_Y24;
+      a2.out_lo[0] = ws.y_lo;
+      a2.out_fmt[1] = OUT_F32;
       if (in_place) {  // outputs straight into the return slots (rows = window rows)
         a2.out[0] = a2.out[1] = ctx->win[1];
-        a2.out_f32[1] = 0;
+        a2.out_fmt[1] = OUT_ACT;
       }
       a2.K[0] = c.inter;
       a2.K[1] = c.shared_inter;
@@ -1055,7 +1060,7 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
       s1.out[1] = ws.hs;
       s1.ldo[0] = c.inter;
       s1.ldo[1] = c.shared_inter;
-      s1.out_f32[0] = s1.out_f32[1] = ctx->act_f32;
+      s1.out_fmt[0] = s1.out_fmt[1] = ctx->act_f32 ? OUT_F32 : OUT_ACT;
       s1.K[0] = s1.K[1] = c.hidden;
       s1.M[0] = 2 * c.inter;
       s1.M[1] = 2 * c.shared_inter;
@@ -1080,8 +1085,9 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
       s2.out[0] = ws.y;
       s2.out[1] = ws.s;
       s2.ldo[0] = s2.ldo[1] = c.hidden;
-      s2.out_f32[0] = ctx->act_f32 || !grouped;
-      s2.out_f32[1] = 1;
+      s2.out_fmt[0] = ctx->act_f32 ? OUT_F32 : (grouped ? OUT_ACT : OUT_Y24);
+      s2.out_lo[0] = ws.y_lo;
+      s2.out_fmt[1] = OUT_F32;
       s2.K[0] = c.inter;
       s2.K[1] = c.shared_inter;
       s2.M[0] = s2.M[1] = c.hidden;

@@ -448,18 +448,34 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
       } else {
         const int col0 = mt * BM + q * 32;
         const bool cols_ok = col0 + 32 <= args.M[kind];
-        const int out_f32 = args.out_f32[kind];
+        const int fmt = args.out_fmt[kind];
         for (int c0 = half_cols * 32; c0 < t.rows; c0 += 64) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(taddr + (uint32_t)c0, v);
           tmem_ld_wait();
           const int r = c0 + lane;
-          if (out_f32) {
+          if (fmt == OUT_F32) {
             if (cols_ok) {
               float* dst = reinterpret_cast<float*>(args.out[kind]) + (row0 + c0) * ldo + col0 + lane;
 #pragma unroll
               for (int c = 0; c < 32; c++)
                 if (c0 + c < t.rows) dst[(int64_t)c * ldo] = __uint_as_float(v[c]);
+            }
+          } else if (fmt == OUT_Y24) {
+            // lane = feature: each token row gets 64 contiguous bytes of the
+            // high plane and 32 of the low plane per store pair (through
+            // shared memory into 16-byte stores measured 9 % slower over
+            // the down GEMM: its epilogue competes with the operand traffic)
+            if (cols_ok) {
+              uint16_t* dh = reinterpret_cast<uint16_t*>(args.out[kind]) + (row0 + c0) * ldo + col0 + lane;
+              uint8_t* dl = args.out_lo[kind] + (row0 + c0) * ldo + col0 + lane;
+#pragma unroll
+              for (int c = 0; c < 32; c++)
+                if (c0 + c < t.rows) {
+                  const uint32_t b24 = y24_encode(__uint_as_float(v[c]));
+                  dh[(int64_t)c * ldo] = (uint16_t)(b24 >> 8);
+                  dl[(int64_t)c * ldo] = (uint8_t)(b24 & 0xffu);
+                }
             }
           } else {
 #pragma unroll

@@ -105,7 +105,10 @@ struct DevWS {
   int32_t* gbase;         // [2 * MAX_PEERS * E] grouped form: row bases, group-list prefixes
   void* xp;               // act [Tmax * k + Tmax, H]
   void* h;                // act [Tmax * k, I]
-  void* y;                // act [Tmax * k, H]
+  void* y;                // routed down-projection outputs [Tmax * k, H]: token form
+                          // y24 high plane (u16), grouped form act; fp32 with fp32
+                          // activations
+  uint8_t* y_lo;          // token form, bf16 activations: y24 low plane (u8) [Tmax * k, H]
   void* hs;               // act [Tmax, Is]
   float* s;               // f32 [Tmax, H]
   int32_t* hist;          // [E, router CTAs] per-CTA expert histograms
@@ -147,6 +150,18 @@ struct GemmPlan {
   GemmGroup g[AFD_MAX_GROUPS];
 };
 
+// Output formats of the GEMMs.  OUT_Y24 keeps an fp32 result to 24 bits
+// (sign, 8 exponent bits, 15 mantissa bits; the low 8 bits rounded off, half
+// away from zero) as two planes: the high 16 bits (a bf16 bit pattern, the
+// value truncated) and the next 8 bits.  The token form's routed outputs y
+// use it: their weighted sum in the combine may cancel to far less than its
+// terms, against which a bf16 y (relative rounding 2^-9) is too coarse, and
+// 3 bytes per element instead of fp32's 4 cut the combine's reads by a
+// quarter (relative rounding 2^-16).
+#define OUT_ACT 0
+#define OUT_F32 1
+#define OUT_Y24 2
+
 // Arguments of the tensor-core grouped GEMM (one launch = one projection).
 struct GemmArgs {
   CUtensorMap tmA[2];     // weights: [0] routed experts, [1] shared expert
@@ -156,8 +171,9 @@ struct GemmArgs {
   CUtensorMap tmBs[2];    // the same sources with 64 x 32 boxes: the SM-pair
                           // engine uses them for units of <= 64 tokens
   void* out[2];           // outputs per kind
+  uint8_t* out_lo[2];     // OUT_Y24: the low plane (one byte per element, pitch ldo)
   int64_t ldo[2];         // output row pitch in elements
-  int out_f32[2];         // 1 = fp32 output, 0 = bf16
+  int out_fmt[2];         // OUT_ACT (bf16), OUT_F32 or OUT_Y24
   int K[2];               // reduction length per kind
   int M[2];               // weight rows per kind (2I for SwiGLU, H for down)
   const GemmPlan* plan;
@@ -178,8 +194,9 @@ struct SimtArgs {
   const void* B[2];       // token rows per kind: [rows][K]
   int64_t ldb[2];
   void* out[2];
+  uint8_t* out_lo[2];     // OUT_Y24 low plane
   int64_t ldo[2];
-  int out_f32[2];
+  int out_fmt[2];         // OUT_ACT (the activation type), OUT_F32 or OUT_Y24
   int K[2];
   int M[2];               // SwiGLU: 2I (gate rows then up rows); plain: H
   int act_f32;
@@ -197,6 +214,13 @@ struct SimtArgs {
 // device helpers
 // ---------------------------------------------------------------------------
 #ifdef __CUDACC__
+
+// fp32 -> 24-bit y (see OUT_Y24): the value's bits rounded at bit 8
+__device__ __forceinline__ uint32_t y24_encode(float v) { return (__float_as_uint(v) + 0x80u) >> 8; }
+// the two planes back to fp32: high 16 bits, then the low byte, then zero
+__device__ __forceinline__ float y24_decode(uint32_t hi16, uint32_t lo8) {
+  return __uint_as_float((hi16 << 16) | (lo8 << 8));
+}
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
@@ -356,6 +380,28 @@ cudaError_t launch_k(const LaunchCtx& lc, void (*kernel)(KArgs...), dim3 grid, d
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = lc.pdl ? 1 : 0;
+  ++*lc.launches;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// The same with thread-block clusters of cluster_x CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k_cluster(const LaunchCtx& lc, void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                             size_t smem, unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = lc.stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster_x;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = lc.pdl ? 2 : 1;
   ++*lc.launches;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }

@@ -471,6 +471,7 @@ __device__ __forceinline__ float exp_of_diff(float a, float b) {
 }
 
 constexpr int kRtTok = 16;        // tokens per top-k CTA (and per plan histogram)
+constexpr int kPlanSmallMax = 8192;  // partials up to which one CTA plans (no histograms)
 constexpr int kLgTok = 8;         // tokens per logits warp
 constexpr int kLgEpw = 4;         // experts per logits warp
 constexpr int kLgWarps = 4;
@@ -1135,6 +1136,55 @@ k_router_logits_tw2(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn
   }
 }
 
+// Top-k and gate weights of one token, by one warp.  lv[m] is the logit of
+// expert lane + 32 m (-inf past E).  Selection on the logits, ties to the
+// lower expert index, a NaN logit below every number; p_e = softmax over all
+// E relative to the top logit (sums as float-float); the k chosen experts'
+// p (renormalised to sum 1 if asked) times the scale.  Lane j < k returns
+// the j-th choice and its weight.  The same steps for every NL: entries past
+// E are skipped, so NL = 4 and NL = 8 give identical results for E <= 128.
+template <int NL>
+__device__ __forceinline__ void route_token(const float (&lv)[NL], int E, int k, int renorm, float scale,
+                                            int lane, int& my_id, float& my_w) {
+  uint32_t taken = 0;  // bit m: expert lane + 32m chosen
+  float top_logit = 0.0f;
+  my_id = 0;           // lane j keeps the j-th choice
+  float my_logit = 0.0f;
+  for (int j = 0; j < k; j++) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int m = 0; m < NL; m++) {
+      const int e = m * 32 + lane;
+      if (e >= E || (taken & (1u << m))) continue;
+      float v = lv[m];
+      if (v != v) v = -INFINITY;  // a NaN logit ranks below every number
+      if (v > bv || (v == bv && e < bi)) { bv = v; bi = e; }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (j == 0) top_logit = bv;
+    if (lane == j) { my_id = bi; my_logit = bv; }
+  }
+  ffloat den = {0.0f, 0.0f};
+#pragma unroll
+  for (int m = 0; m < NL; m++)
+    if (m * 32 + lane < E) den = ff_add(den, exp_of_diff(lv[m], top_logit));
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) den = ff_add(den, ff_shfl_xor(den, off));
+  const float p = (lane < k) ? ff_div(exp_of_diff(my_logit, top_logit), den) : 0.0f;
+  ffloat psum = {p, 0.0f};
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) psum = ff_add(psum, ff_shfl_xor(psum, off));
+  const float v = renorm ? ff_div(p, psum) : p;
+  my_w = __fmul_rn(v, scale);
+}
+
 // a1 router, part 2: top-k on the logits (ties -> lower expert index, NaN
 // below every number) and the gate weights from a softmax over all E
 // (sums carried as float-float); one warp per token, 16 tokens per CTA,
@@ -1170,51 +1220,415 @@ k_router_topk(const __grid_constant__ FanIn fp, DevWS ws, const float* __restric
     return;
   }
   if (t < f.total) {
-    uint32_t taken = 0;  // bit m: expert lane + 32m chosen (E <= 256)
-    float top_logit = 0.0f;
-    int my_id = 0;       // lane j keeps the j-th choice
-    float my_logit = 0.0f;
-    for (int j = 0; j < k; j++) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-#pragma unroll
-      for (int m = 0; m < 8; m++) {
-        const int e = m * 32 + lane;
-        if (e >= E || (taken & (1u << m))) continue;
-        float v = lv[m];
-        if (v != v) v = -INFINITY;  // a NaN logit ranks below every number
-        if (v > bv || (v == bv && e < bi)) { bv = v; bi = e; }
-      }
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (j == 0) top_logit = bv;
-      if (lane == j) { my_id = bi; my_logit = bv; }
-    }
-    ffloat den = {0.0f, 0.0f};
-#pragma unroll
-    for (int m = 0; m < 8; m++)
-      if (m * 32 + lane < E) den = ff_add(den, exp_of_diff(lv[m], top_logit));
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) den = ff_add(den, ff_shfl_xor(den, off));
-    const float p = (lane < k) ? ff_div(exp_of_diff(my_logit, top_logit), den) : 0.0f;
-    ffloat psum = {p, 0.0f};
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) psum = ff_add(psum, ff_shfl_xor(psum, off));
+    int my_id;
+    float my_w;
+    route_token<8>(lv, E, k, renorm, scale, lane, my_id, my_w);
     if (lane < k) {
-      const float v = renorm ? ff_div(p, psum) : p;
       ws.ids[(int64_t)t * k + lane] = my_id;
-      ws.w[(int64_t)t * k + lane] = __fmul_rn(v, scale);
+      ws.w[(int64_t)t * k + lane] = my_w;
       atomicAdd(&hs[my_id], 1);
     }
   }
   __syncthreads();
   if (hist)  // block-major: hist[cta][e]
     for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(int64_t)blockIdx.x * E + e] = hs[e];
+}
+
+// ---------------------------------------------------------------------------
+// a1 router, fused (bf16 activations, hidden <= 2048, E <= 128): logits and
+// top-k in one kernel on a thread-block cluster of C = ceil(E / 16) CTAs.
+// CTA rank r holds the fp32 gate weights of experts [16 r, 16 r + 16) in
+// shared memory for its whole life; all CTAs of a cluster walk the same
+// 16-token blocks (two 8-token tiles each), so together they produce every
+// logit of a block.  Eight compute warps form teams of 16 / EPW warps; a
+// team takes one tile, warp w of it experts [EPW w, EPW w + EPW) of the
+// CTA's 16 for the tile's 8 tokens, in the canonical fp32 order of
+// k_router_logits (lane l's fused multiply-add chain over h = l, l + 32, ...
+// ascending, a butterfly with xor offsets 16 .. 1, then + bias).  The tile's
+// rows are staged in h-chunks of 256 * (16 / EPW) as transposed 16-byte
+// records (8 tokens of one h), double-buffered, the next chunk loaded into
+// registers while the current one is used.  Each finished logit goes by
+// st.async straight into the shared memory of the block's owner, one CTA of
+// the cluster in rotation, whose mbarrier counts the bytes; the owner's four
+// top-k warps then select, weight and count the block's 16 tokens (ids,
+// gate weights, the block's expert histogram for the plan) and give the
+// buffer back through an mbarrier in every CTA.  The logits never reach
+// global memory and no second kernel runs.  Every wait is bounded; an
+// error stops the arithmetic but not the exchange, so every byte sent is
+// awaited before the cluster's CTAs leave.
+// ---------------------------------------------------------------------------
+constexpr int kFrWarps = 8;                       // compute warps per CTA
+constexpr int kFrSlots = 2;                       // logit buffers per CTA
+constexpr int kFrMaxC = 8;                        // CTAs per cluster (E <= 128)
+constexpr int kFrBlk = 16;                        // tokens per block: two 8-token tiles
+static_assert(kFrBlk == kRtTok, "the plan's histogram rows are router blocks of kRtTok tokens");
+
+struct FrGeom {
+  uint32_t rec_off, rec_bytes;  // record buffers: [teams][2][rec_bytes]
+  uint32_t lb_off;              // logit buffers: [kFrSlots][16][ep] fp32
+  uint32_t hist_off;            // block histograms: [kFrSlots][ep] int
+  uint32_t bar_off;             // weights, full[kFrSlots], empty[kFrMaxC][kFrSlots]
+  uint32_t smem;
+  int C, ep;                    // CTAs per cluster; experts rounded up to 16
+};
+
+__device__ __forceinline__ uint32_t fr_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// this CTA's shared address as seen in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t fr_mapa(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void fr_cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// 4 bytes into a peer's shared memory, counted on the peer's mbarrier
+__device__ __forceinline__ void fr_st_async(uint32_t raddr, float v, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+               ::"r"(raddr), "r"(__float_as_uint(v)), "r"(rbar) : "memory");
+}
+__device__ __forceinline__ void fr_arrive_remote(uint32_t raddr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(raddr) : "memory");
+}
+__device__ __forceinline__ bool fr_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// TK top-k warps.  Each SM sub-partition holds three of the CTA's twelve
+// warps, so a thread gets at most 168 registers (16384 per sub-partition);
+// fewer top-k warps would not give the compute warps more.
+template <int EPW, bool kSpread, bool kDev, int TK = 4>
+__global__ void __launch_bounds__((kFrWarps + TK) * 32, 1)
+k_router_fused(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn fp, DevWS ws, int hidden,
+               const float* __restrict__ WgQ, const float* __restrict__ bias, int E, int k, int renorm,
+               float scale, int32_t* __restrict__ hist, FrGeom geo, uint32_t go_token,
+               int64_t go_timeout_ns) {
+  constexpr int WPT = 16 / EPW;          // warps per team (one tile)
+  // kSpread: row r of every block is routed by CTA r mod C (small fan-ins,
+  // whose plan needs no histograms: every top-k warp takes about one
+  // token); else each block has one owner CTA in rotation, which also
+  // writes the block's expert histogram
+  constexpr int TEAMS = kFrWarps / WPT;  // tiles in flight per CTA
+  constexpr int BPI = TEAMS / 2;         // blocks per cluster iteration
+  constexpr int CHUNK = WPT * 32 * 8;    // h per staged chunk: one 8-h group per team thread
+  static_assert(EPW == 4 || EPW == 8, "4 or 8 experts per warp");
+  // go_token != 0 (host-described steps): started before the header check
+  // ends (see k_router_logits_tw2); the wait on the check moves to the exit
+  struct ExitWait {
+    bool on;
+    __device__ ~ExitWait() {
+      if (on) grid_dep_wait();
+    }
+  } exit_wait{go_token != 0};
+  if (!go_token) grid_dep_wait();
+  // the plan kernel after this one is let in only as this grid's warps
+  // finish: its CTA resident from the start (waiting on this grid)
+  // measured 7 us per decode layer slower, as did starting without the go
+  // token
+  const FanIn& f = step_item<kDev>(fp, ws.item);
+  if (!WgQ) {  // the layer of the step was chosen on the device
+    WgQ = ws.layers[f.layer].WgQ;
+    bias = ws.layers[f.layer].bias;
+  }
+  extern __shared__ __align__(128) uint8_t fr_smem[];
+  __shared__ int skipv[kFrMaxC];
+  __shared__ int skip_s;
+  __shared__ int abort_s;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int C = geo.C, ep = geo.ep;
+  const uint32_t rank = fr_ctarank();
+  const int cid = (int)blockIdx.x / C, ncl = (int)gridDim.x / C;
+  const int e_base = (int)rank * 16;
+  const int ne = min(16, E - e_base);
+  const int T = f.total;
+  const int nblocks = (T + kFrBlk - 1) / kFrBlk;
+  const uint32_t bar0 = smem_u32(fr_smem + geo.bar_off);
+  const uint32_t wbar = bar0;
+  auto full_bar = [&](int s) { return bar0 + 8u * (uint32_t)(1 + s); };
+  auto empty_bar = [&](int q, int s) { return bar0 + 8u * (uint32_t)(1 + kFrSlots + q * kFrSlots + s); };
+  float* lb = reinterpret_cast<float*>(fr_smem + geo.lb_off);  // [kFrSlots][16][ep]
+  // rows of a block this CTA routes, and the bytes its buffer receives per block
+  const int my_rows = kSpread ? (kFrBlk - (int)rank + C - 1) / C : kFrBlk;
+  const uint32_t block_bytes = (uint32_t)(my_rows * E * 4);
+  int* hs = reinterpret_cast<int*>(fr_smem + geo.hist_off);    // [kFrSlots][ep]
+  if (tid == 0) {
+    abort_s = 0;
+    mbar_init(wbar, 1);
+    for (int s = 0; s < kFrSlots; s++) mbar_init(full_bar(s), 1);
+    for (int q = 0; q < C; q++)
+      for (int s = 0; s < kFrSlots; s++) mbar_init(empty_bar(q, s), 1);
+    // each logit buffer is armed (its one arrival and the block's bytes:
+    // 16 tokens x E logits) before any peer may send into it, here for its
+    // first use and by the top-k warps before each later one
+    for (int s = 0; s < kFrSlots; s++) mbar_expect_tx(full_bar(s), block_bytes);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    const uint32_t wbytes = (uint32_t)(((ne + 3) / 4) * hidden * 16);
+    mbar_expect_tx(wbar, wbytes);
+    bulk_load(smem_u32(fr_smem), WgQ + (int64_t)e_base * hidden, wbytes, wbar);
+  }
+  for (int i = tid; i < kFrSlots * ep; i += blockDim.x) hs[i] = 0;
+  __syncthreads();
+  // this CTA has started and its barriers are initialised
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  if (tid == 0) {
+    int ok = 1;
+    if (go_token) {  // the header check hands over the fan-in (bounded)
+      const uint64_t t0 = globaltimer_ns();
+      ok = 0;
+      for (;;) {
+        const uint32_t v = ld_acquire_u32(ws.go);
+        if (v == go_token) { ok = 1; break; }
+        if (v == (go_token | AFD_GO_ABORT)) break;  // the check reports the error
+        if (globaltimer_ns() - t0 > (uint64_t)go_timeout_ns) {
+          set_error(ws.status, AFD_ERR_TIMEOUT);
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    skip_s = !ok || read_status(ws.status);
+  }
+  __syncthreads();
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every peer has started
+  // the skip decision is the cluster's: each CTA's into every CTA
+  if (tid < C)
+    asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(fr_mapa(smem_u32(&skipv[rank]), (uint32_t)tid)),
+                 "r"(skip_s)
+                 : "memory");
+  fr_cluster_sync();
+  int skip = 0;
+  for (int q = 0; q < C; q++) skip |= skipv[q];
+  if (skip) {  // the whole cluster leaves; nothing was exchanged
+    if (tid == 0) {  // the weight copy lands in this CTA's shared memory: wait (bounded)
+      const uint64_t dl = globaltimer_ns() + 100000000ull;
+      while (!mbar_try_wait(wbar, 0) && globaltimer_ns() < dl) {}
+    }
+    return;
+  }
+  // a wait that runs out records the error once; later waits give up fast
+  auto waitb = [&](uint32_t bar, uint32_t parity, uint64_t start) {
+    uint32_t spins = 0;
+    while (!fr_try_wait(bar, parity)) {
+      if ((++spins & 63u) == 0) {
+        const uint64_t lim = *(volatile int*)&abort_s ? 1000000ull : 1000000000ull;
+        if (globaltimer_ns() - start > lim) {
+          if (atomicExch(&abort_s, 1) == 0) set_error(ws.status, AFD_ERR_TIMEOUT);
+          return false;
+        }
+      }
+    }
+    return true;
+  };
+  if (warp < kFrWarps) {
+    // ------------------------------------------------------------ compute
+    const int m = warp / WPT, wt = warp % WPT;
+    const int team_tid = tid - m * WPT * 32;
+    const int bar_id = 2 + m;
+    uint8_t* rec = fr_smem + geo.rec_off + (size_t)m * 2 * geo.rec_bytes;
+    const float4* Wq = reinterpret_cast<const float4*>(fr_smem);  // [4 groups][hidden]
+    const int grp0 = EPW == 8 ? 2 * wt : wt;
+    const int row_bytes = hidden * 2;
+    const int nch = (hidden + CHUNK - 1) / CHUNK;
+    auto block_of = [&](int it) { return (cid + ncl * it) * BPI + m / 2; };
+    const uint8_t* rows[8];
+    uint4 pre[8];
+    auto set_rows = [&](int it) {  // the tile's token rows, straight from the peer slots
+      const int t0 = (2 * block_of(it) + (m & 1)) * 8;
+#pragma unroll
+      for (int r = 0; r < 8; r++) {
+        const int t = t0 + r;
+        rows[r] = nullptr;
+        if (t < T) {
+          const int e = entry_of(f, t);
+          rows[r] = slot_ptr(win, g, f.region[e], f.stage) + g.routed_x + (int64_t)(t - f.prefix[e]) * row_bytes;
+        }
+      }
+    };
+    auto fetch = [&](int c) {  // this thread's 8-h group of chunk c, 8 tokens (zeros past the fan-in)
+      const int h = c * CHUNK + team_tid * 8;
+#pragma unroll
+      for (int r = 0; r < 8; r++)
+        pre[r] = (rows[r] && h < hidden) ? __ldg(reinterpret_cast<const uint4*>(rows[r] + (int64_t)h * 2))
+                                         : make_uint4(0, 0, 0, 0);
+    };
+    if (block_of(0) < nblocks) {  // the first chunk's loads fly while the weights land
+      set_rows(0);
+      fetch(0);
+    }
+    waitb(wbar, 0, globaltimer_ns());
+    int cc = 0;  // chunks consumed by this team
+    for (int it = 0; block_of(it) < nblocks; it++) {
+      float2 acc[4][EPW];  // {token 2p, token 2p + 1} x expert
+#pragma unroll
+      for (int p = 0; p < 4; p++)
+#pragma unroll
+        for (int b = 0; b < EPW; b++) acc[p][b] = make_float2(0.0f, 0.0f);
+      for (int c = 0; c < nch; c++, cc++) {
+        uint8_t* xt = rec + (size_t)(cc & 1) * geo.rec_bytes;
+        if (c * CHUNK + team_tid * 8 < hidden) {  // [t][8 h] -> records [h][8 t]
+          const uint32_t* iw[8];
+#pragma unroll
+          for (int t = 0; t < 8; t++) iw[t] = reinterpret_cast<const uint32_t*>(&pre[t]);
+#pragma unroll
+          for (int j = 0; j < 8; j++) {
+            const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
+            uint4 o;
+            o.x = __byte_perm(iw[0][j >> 1], iw[1][j >> 1], sel);
+            o.y = __byte_perm(iw[2][j >> 1], iw[3][j >> 1], sel);
+            o.z = __byte_perm(iw[4][j >> 1], iw[5][j >> 1], sel);
+            o.w = __byte_perm(iw[6][j >> 1], iw[7][j >> 1], sel);
+            *reinterpret_cast<uint4*>(xt + tw_rec_offset(8 * team_tid + j)) = o;
+          }
+        }
+        // records complete; every warp of the team is past the chunk that
+        // used the other buffer
+        named_bar_sync(bar_id, WPT * 32);
+        if (c + 1 < nch) {
+          fetch(c + 1);
+        } else if (block_of(it + 1) < nblocks) {
+          set_rows(it + 1);
+          fetch(0);
+        }
+        if (!*(volatile int*)&abort_s) {
+          const int h0 = c * CHUNK, len = min(CHUNK, hidden - h0);
+          auto step = [&](int hh) {
+            const uint4 xr = *reinterpret_cast<const uint4*>(xt + tw_rec_offset(hh));
+            float wv[EPW];
+            {
+              const float4 w0 = Wq[(size_t)grp0 * hidden + h0 + hh];
+              wv[0] = w0.x; wv[1] = w0.y; wv[2] = w0.z; wv[3] = w0.w;
+              if constexpr (EPW == 8) {
+                const float4 w1 = Wq[(size_t)(grp0 + 1) * hidden + h0 + hh];
+                wv[4] = w1.x; wv[5] = w1.y; wv[6] = w1.z; wv[7] = w1.w;
+              }
+            }
+            const uint32_t xw[4] = {xr.x, xr.y, xr.z, xr.w};
+#pragma unroll
+            for (int p = 0; p < 4; p++) {
+              const float2 xp = make_float2(__uint_as_float(xw[p] << 16), __uint_as_float(xw[p] & 0xffff0000u));
+#pragma unroll
+              for (int b = 0; b < EPW; b++) acc[p][b] = __ffma2_rn(xp, make_float2(wv[b], wv[b]), acc[p][b]);
+            }
+          };
+          const int nfull = len / 32;
+#pragma unroll 4
+          for (int j = 0; j < nfull; j++) step(32 * j + lane);
+          if (32 * nfull + lane < len) step(32 * nfull + lane);
+        }
+      }
+      // the tile's 8 x EPW logits: lane l ends with one (two) of them
+      float va[32];
+#pragma unroll
+      for (int p = 0; p < 4; p++)
+#pragma unroll
+        for (int b = 0; b < EPW; b++) {
+          if (EPW * 2 * p + b < 32) va[EPW * 2 * p + b] = acc[p][b].x;
+          if (EPW * (2 * p + 1) + b < 32) va[EPW * (2 * p + 1) + b] = acc[p][b].y;
+        }
+      const float sum_a = butterfly_scatter32(va, lane);  // token lane / EPW, expert lane % EPW
+      float sum_b = 0.0f;                                 // EPW 8: token 4 + lane / 8
+      if constexpr (EPW == 8) {
+        float vb[32];
+#pragma unroll
+        for (int p = 2; p < 4; p++)
+#pragma unroll
+          for (int b = 0; b < 8; b++) {
+            vb[8 * (2 * p) + b - 32] = acc[p][b].x;
+            vb[8 * (2 * p + 1) + b - 32] = acc[p][b].y;
+          }
+        sum_b = butterfly_scatter32(vb, lane);
+      }
+      // to the CTA that routes each row: the block's owner, or row mod C
+      const int lblk = it * BPI + m / 2;
+      const int owner = lblk % C;
+      const int s = kSpread ? lblk % kFrSlots : (lblk / C) % kFrSlots;
+      const uint32_t use = (uint32_t)(kSpread ? lblk / kFrSlots : (lblk / C) / kFrSlots);
+      bool ok = true;
+      if (lane == 0) {  // every receiving CTA has given this buffer back
+        if (kSpread) {
+          for (int q = 0; q < C && ok; q++) ok = waitb(empty_bar(q, s), (use & 1u) ^ 1u, globaltimer_ns());
+        } else {
+          ok = waitb(empty_bar(owner, s), (use & 1u) ^ 1u, globaltimer_ns());
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (ok) {
+        const int el = EPW * wt + (lane % EPW);
+        const int e = e_base + el;
+        if (el < ne) {
+          const float bv = bias ? bias[e] : 0.0f;
+          auto send = [&](int row, float sum) {
+            const int q = kSpread ? row % C : owner;
+            const float v = bias ? __fadd_rn(sum, bv) : sum;
+            fr_st_async(fr_mapa(smem_u32(lb + ((size_t)s * 16 + row) * ep + e), (uint32_t)q), v,
+                        fr_mapa(full_bar(s), (uint32_t)q));
+          };
+          const int row_a = (m & 1) * 8 + lane / EPW;
+          send(row_a, sum_a);
+          if constexpr (EPW == 8) send(row_a + 4, sum_b);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ top-k
+    const int tw = warp - kFrWarps;
+    const int ttid = tid - kFrWarps * 32;
+    for (int lblk = kSpread ? 0 : (int)rank;; lblk += kSpread ? 1 : C) {
+      const int it = lblk / BPI, j = lblk % BPI;
+      const int b = (cid + ncl * it) * BPI + j;
+      if (b >= nblocks) break;
+      const int s = kSpread ? lblk % kFrSlots : (lblk / C) % kFrSlots;
+      const uint32_t use = (uint32_t)(kSpread ? lblk / kFrSlots : (lblk / C) / kFrSlots);
+      const bool ok = waitb(full_bar(s), use & 1u, globaltimer_ns()) && !*(volatile int*)&abort_s;
+      if (ok) {
+#pragma unroll 1
+        for (int i = tw; i < my_rows; i += TK) {
+          const int r = kSpread ? (int)rank + C * i : i;
+          const int t = b * kFrBlk + r;
+          if (t >= T) break;
+          float lv[4];
+#pragma unroll
+          for (int mm = 0; mm < 4; mm++) {
+            const int e = lane + 32 * mm;
+            lv[mm] = e < E ? lb[((size_t)s * 16 + r) * ep + e] : -INFINITY;
+          }
+          int my_id;
+          float my_w;
+          route_token<4>(lv, E, k, renorm, scale, lane, my_id, my_w);
+          if (lane < k) {
+            ws.ids[(int64_t)t * k + lane] = my_id;
+            ws.w[(int64_t)t * k + lane] = my_w;
+            atomicAdd(&hs[s * ep + my_id], 1);
+          }
+        }
+      }
+      named_bar_sync(1, TK * 32);  // the buffer is read, the histogram complete
+      for (int e = ttid; e < E; e += TK * 32) {
+        if (!kSpread && hist && !*(volatile int*)&abort_s) hist[(int64_t)b * E + e] = hs[s * ep + e];
+        hs[s * ep + e] = 0;
+      }
+      // armed for its next use, then back to the producers of every CTA
+      if (ttid == 0) mbar_expect_tx(full_bar(s), block_bytes);
+      named_bar_sync(1, TK * 32);
+      if (ttid < C) fr_arrive_remote(fr_mapa(empty_bar((int)rank, s), (uint32_t)ttid));
+    }
+  }
+  // each warp lets the next kernel in once its part is done (the compute
+  // warps before the top-k warps); after the CTA barrier instead measured
+  // 7 us per decode layer slower
+  grid_dep_launch();
+  __syncthreads();
+  fr_cluster_sync();  // no peer sends to or signals this CTA past this point
 }
 
 // ---------------------------------------------------------------------------
@@ -1404,7 +1818,6 @@ k_plan_scan(const __grid_constant__ FanIn fp, DevWS ws, int E, int k, int inter,
 // owns a contiguous chunk of f; per-warp histograms give its cursor per
 // expert; 32-element rounds are ranked with match_any) and the tile tables.
 // ---------------------------------------------------------------------------
-constexpr int kPlanSmallMax = 8192;
 constexpr int kPlanPerLane = kPlanSmallMax / 1024;  // ids per lane: a warp's chunk is <= 256
 
 template <bool kDev>
@@ -1802,8 +2215,15 @@ __global__ void __launch_bounds__(kThreads) k_gemm_simt(SimtArgs a) {
       v = s;
     }
     const int64_t o = (int64_t)(G.out_row0 + r) * a.ldo[kind] + c;
-    if (a.out_f32[kind]) reinterpret_cast<float*>(a.out[kind])[o] = v;
-    else reinterpret_cast<__nv_bfloat16*>(a.out[kind])[o] = __float2bfloat16_rn(v);
+    if (a.out_fmt[kind] == OUT_F32) {
+      reinterpret_cast<float*>(a.out[kind])[o] = v;
+    } else if (a.out_fmt[kind] == OUT_Y24) {
+      const uint32_t b24 = y24_encode(v);
+      reinterpret_cast<uint16_t*>(a.out[kind])[o] = (uint16_t)(b24 >> 8);
+      a.out_lo[kind][o] = (uint8_t)(b24 & 0xffu);
+    } else {
+      reinterpret_cast<__nv_bfloat16*>(a.out[kind])[o] = __float2bfloat16_rn(v);
+    }
   }
 }
 
@@ -1819,15 +2239,19 @@ __global__ void __launch_bounds__(kThreads) k_gemm_simt(SimtArgs a) {
 template <bool ACT_F32, int kBatch, bool kDev>
 __global__ void __launch_bounds__(kThreads)
 k_combine(uint8_t* ret, WinGeom g, const __grid_constant__ FanIn fp, DevWS ws, int hidden, int k, int has_shared) {
+  // y: fp32 with fp32 activations, else the 24-bit planes (OUT_Y24)
   grid_dep_wait();
   grid_dep_launch();
   const FanIn& f = step_item<kDev>(fp, ws.item);
   if (read_status(ws.status)) return;
-  // 8 features per lane step: two 16-byte loads of a partial's fp32 row
+  // 8 features per lane step: two 16-byte loads of a partial's fp32 row,
+  // or 16 bytes of its high plane and 8 of its low plane
   constexpr int kVec = 8;
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * (blockDim.x >> 5);
   const float* __restrict__ y = reinterpret_cast<const float*>(ws.y);
+  const uint16_t* __restrict__ y_hi = reinterpret_cast<const uint16_t*>(ws.y);
+  const uint8_t* __restrict__ y_lo = ws.y_lo;
   // work item = (token, block of 256 features): a small fan-in still spreads
   // over every SM
   const int nfb = (hidden + 32 * kVec - 1) / (32 * kVec);
@@ -1858,7 +2282,7 @@ k_combine(uint8_t* ret, WinGeom g, const __grid_constant__ FanIn fp, DevWS ws, i
     // where few warps must keep many loads in flight; 4 for large ones; 1
     // for fp32 activations)
     for (int j0 = 0; j0 < k; j0 += kBatch) {
-      float4 raw[kBatch][2];
+      uint4 raw[kBatch][2];  // fp32: two 16-byte words; y24: high plane, low plane (8 bytes)
       float wj[kBatch];
 #pragma unroll
       for (int u = 0; u < kBatch; u++) {
@@ -1866,15 +2290,36 @@ k_combine(uint8_t* ret, WinGeom g, const __grid_constant__ FanIn fp, DevWS ws, i
         const int pos = __shfl_sync(0xffffffffu, my_pos, j & 31);
         wj[u] = __shfl_sync(0xffffffffu, my_w, j & 31);
         const bool ld = valid && j < k;
-        const float4* src = reinterpret_cast<const float4*>(y + (int64_t)pos * hidden + c);
-        raw[u][0] = ld ? src[0] : make_float4(0.f, 0.f, 0.f, 0.f);
-        raw[u][1] = ld ? src[1] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const int64_t e0 = (int64_t)pos * hidden + c;
+        if constexpr (ACT_F32) {
+          const uint4* src = reinterpret_cast<const uint4*>(y + e0);
+          raw[u][0] = ld ? src[0] : make_uint4(0, 0, 0, 0);
+          raw[u][1] = ld ? src[1] : make_uint4(0, 0, 0, 0);
+        } else {
+          raw[u][0] = ld ? *reinterpret_cast<const uint4*>(y_hi + e0) : make_uint4(0, 0, 0, 0);
+          const uint2 l = ld ? *reinterpret_cast<const uint2*>(y_lo + e0) : make_uint2(0, 0);
+          raw[u][1] = make_uint4(l.x, l.y, 0, 0);
+        }
       }
 #pragma unroll
       for (int u = 0; u < kBatch; u++) {
         if (j0 + u >= k) break;
-        const float yv[kVec] = {raw[u][0].x, raw[u][0].y, raw[u][0].z, raw[u][0].w,
-                                raw[u][1].x, raw[u][1].y, raw[u][1].z, raw[u][1].w};
+        float yv[kVec];
+        if constexpr (ACT_F32) {
+          const uint32_t w8[kVec] = {raw[u][0].x, raw[u][0].y, raw[u][0].z, raw[u][0].w,
+                                     raw[u][1].x, raw[u][1].y, raw[u][1].z, raw[u][1].w};
+#pragma unroll
+          for (int q = 0; q < kVec; q++) yv[q] = __uint_as_float(w8[q]);
+        } else {
+          const uint32_t hw[4] = {raw[u][0].x, raw[u][0].y, raw[u][0].z, raw[u][0].w};
+          const uint32_t lw[2] = {raw[u][1].x, raw[u][1].y};
+#pragma unroll
+          for (int q = 0; q < kVec; q++) {
+            const uint32_t hi = (q & 1) ? (hw[q >> 1] >> 16) : (hw[q >> 1] & 0xffffu);
+            const uint32_t lo = (lw[q >> 2] >> (8 * (q & 3))) & 0xffu;
+            yv[q] = y24_decode(hi, lo);
+          }
+        }
 #pragma unroll
         for (int q = 0; q < kVec; q++) acc[q] = __fmaf_rn(wj[u], yv[q], acc[q]);
       }
@@ -2285,12 +2730,96 @@ static cudaError_t launch_logits(const LaunchCtx& lc, const WinGeom& g, const ui
   return launch_logits_t<XS, kDev>(lc, g, win, f, ws, hidden, WgQ, bias, E, logits);
 }
 
+static FrGeom fr_geom(int hidden, int E, int epw) {
+  FrGeom g{};
+  g.C = (E + 15) / 16;
+  g.ep = g.C * 16;
+  const int wpt = 16 / epw, teams = kFrWarps / wpt, chunk = wpt * 32 * 8;
+  auto r128 = [](size_t v) { return (uint32_t)((v + 127) / 128 * 128); };
+  g.rec_off = r128((size_t)4 * hidden * 16);  // 4 groups of 4 experts' weights
+  g.rec_bytes = r128(tw_rec_offset(chunk));
+  g.lb_off = g.rec_off + (uint32_t)teams * 2 * g.rec_bytes;
+  g.hist_off = g.lb_off + (uint32_t)(kFrSlots * kFrBlk * g.ep * 4);
+  g.bar_off = g.hist_off + (uint32_t)(kFrSlots * g.ep * 4);
+  g.smem = g.bar_off + 8u * (1 + kFrSlots + kFrMaxC * kFrSlots);
+  return g;
+}
+
+// Clusters of the fused router that fit the GPU at once (queried once per
+// kernel and cluster shape); clusters beyond it would run in a second wave.
+template <int EPW, bool kSpread, bool kDev>
+static int fr_max_clusters(const FrGeom& geo, int num_sms) {
+  static int cached[kFrMaxC + 1] = {};
+  if (cached[geo.C]) return cached[geo.C];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(geo.C * std::max(1, num_sms / geo.C)));
+  cfg.blockDim = dim3((kFrWarps + 4) * 32);
+  cfg.dynamicSmemBytes = geo.smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)geo.C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k_router_fused<EPW, kSpread, kDev>, &cfg) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    n = std::max(1, num_sms / geo.C);
+  }
+  cached[geo.C] = n;
+  return n;
+}
+
+template <int EPW, bool kSpread, bool kDev>
+static cudaError_t launch_router_fused(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
+                                       const FanIn& f, const DevWS& ws, int hidden, const float* WgQ,
+                                       const float* bias, int E, int k, int renorm, float scale,
+                                       int32_t* hist, uint32_t go_token, int64_t go_timeout_ns) {
+  const FrGeom geo = fr_geom(hidden, E, EPW);
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t err = cudaFuncSetAttribute(k_router_fused<EPW, kSpread, kDev>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, 232448 - 2048);
+    if (err != cudaSuccess) return err;
+    attr_done = true;
+  }
+  constexpr int BPI = kFrWarps * EPW / 16 / 2;
+  const int nblocks = (f.total + kFrBlk - 1) / kFrBlk;
+  const int ncl = std::max(1, std::min(fr_max_clusters<EPW, kSpread, kDev>(geo, lc.num_sms), (nblocks + BPI - 1) / BPI));
+  return launch_k_cluster(lc, k_router_fused<EPW, kSpread, kDev>, dim3((unsigned)(ncl * geo.C)),
+                          (kFrWarps + 4) * 32, geo.smem,
+                          (unsigned)geo.C, win, g, f, ws, hidden, WgQ, bias, E, k, renorm, scale, hist, geo,
+                          kDev ? 0u : go_token, go_timeout_ns);
+}
+
+// The fused router covers bf16 activations with hidden <= 2048 and at most
+// 128 experts, when the caller takes the block histograms (the allocation-
+// free entry point keeps the two-kernel router, whose top-k writes its
+// failure sentinel).
+static bool fused_router_fits(int hidden, int E, int act_f32, const int32_t* hist) {
+  return !act_f32 && hist && E <= kFrMaxC * 16 && hidden <= 2048 &&
+         fr_geom(hidden, E, 8).smem <= 232448 - 2048;
+}
+
 template <bool kDev>
 static cudaError_t launch_router_t(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                                    const FanIn& f, const DevWS& ws, int hidden, int act_f32,
                                    const float* WgQ, const float* bias, int E, int k, int renorm,
                                    float scale, float* logits, int32_t* hist, uint32_t go_token,
                                    int64_t go_timeout_ns) {
+  if (fused_router_fits(hidden, E, act_f32, hist)) {
+    // small fan-ins (planned by one CTA, no histograms): 4 experts per warp
+    // and every block's rows routed across the cluster, since the latency
+    // of one tile decides; larger ones: 8 experts per warp (fewer
+    // non-multiply instructions per multiply-add) and a block owner that
+    // writes the block's histogram.  The same test as the plan's choice.
+    if ((int64_t)f.total * k <= kPlanSmallMax)
+      return launch_router_fused<4, true, kDev>(lc, g, win, f, ws, hidden, WgQ, bias, E, k, renorm, scale,
+                                                hist, go_token, go_timeout_ns);
+    return launch_router_fused<8, false, kDev>(lc, g, win, f, ws, hidden, WgQ, bias, E, k, renorm, scale,
+                                               hist, go_token, go_timeout_ns);
+  }
   cudaError_t err =
       act_f32 ? launch_logits<float, kDev>(lc, g, win, f, ws, hidden, WgQ, bias, E, logits, go_token,
                                            go_timeout_ns)
@@ -2366,7 +2895,7 @@ cudaError_t launch_combine(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret, 
   const int grid = grid_for(items, kThreads / 32, lc.num_sms * 8);
   const bool small = items < (int64_t)lc.num_sms * 64;
   const bool d = f.dev != 0;
-  // y is fp32 in the token form
+  // y is fp32 (fp32 activations) or 24-bit (bf16) in the token form
   decltype(&k_combine<true, 1, false>) kern = nullptr;
   if (act_f32)
     kern = d ? k_combine<true, 1, true> : k_combine<true, 1, false>;

@@ -375,7 +375,8 @@ int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out) {
       {(int64_t)sizeof(FanIn)},              // the fan-in of the step in flight
       {AFD_LOOP_WORDS * 4},                  // work-item loop state and log
       {(int64_t)cfg->max_layers * (int64_t)sizeof(DevLayer)},  // per-layer weight table
-      {4}};                                  // go word (header check -> router)
+      {4},                                   // go word (header check -> router)
+      {AFD_MAX_PEERS * 4}};                  // combine items finished per entry
   const int nparts = sizeof(parts) / sizeof(parts[0]);
   int64_t offs[32], total = 0;
   for (int i = 0; i < nparts; i++) {
@@ -414,6 +415,7 @@ int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out) {
   c->dlayers = reinterpret_cast<DevLayer*>(b + offs[24]);
   c->ws.layers = c->dlayers;
   c->ws.go = reinterpret_cast<uint32_t*>(b + offs[25]);
+  c->ws.ret_count = reinterpret_cast<int32_t*>(b + offs[26]);
   c->plan1 = reinterpret_cast<GemmPlan*>(b + offs[16]);
   c->plan2 = reinterpret_cast<GemmPlan*>(b + offs[17]);
   const int ws_map[12] = {4, 5, 6, 7, 8, 9, 11, 12, 13, 14, 15, 0};
@@ -960,9 +962,13 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
                  "plan");
   if (rc) return rc;
   mark(3);
+  // small host-described token-form steps: the gather writes the return
+  // headers and the combine releases the flags (no return-header kernel)
+  const bool flags_in_combine = !grouped && combine_releases_flags(lc, f, c.hidden);
   if (!in_place) {
     rc = cuda_fail(launch_gather(lc, ctx->geom, ctx->win[0], f, ws, c.topk, row_bytes, c.hidden,
-                                 has_shared, sh_in_place),
+                                 has_shared, sh_in_place, flags_in_combine ? ctx->win[1] : nullptr,
+                                 c.num_experts),
                    "gather");
     if (rc) return rc;
   }
@@ -1106,14 +1112,16 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
                                      : launch_scatter_grouped(lc, ctx->geom, ctx->win[1], f, ws,
                                                               c.hidden, ctx->act_f32, has_shared))
                          : launch_combine(lc, ctx->geom, ctx->win[1], f, ws, c.hidden, c.topk,
-                                          ctx->act_f32, has_shared),
+                                          ctx->act_f32, has_shared, flags_in_combine),
                  grouped ? "scatter" : "combine");
   if (rc) return rc;
   mark(7);
-  rc = cuda_fail(launch_return_header(lc, ctx->geom, ctx->win[1], ctx->win[0], f, ws, c.num_experts,
-                                      c.topk),
-                 "return header");
-  if (rc) return rc;
+  if (!flags_in_combine) {
+    rc = cuda_fail(launch_return_header(lc, ctx->geom, ctx->win[1], ctx->win[0], f, ws, c.num_experts,
+                                        c.topk),
+                   "return header");
+    if (rc) return rc;
+  }
   mark(8);
   ctx->last_T = dev ? -1 : (int)T;
   ctx->forwards++;

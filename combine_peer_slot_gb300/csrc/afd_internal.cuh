@@ -118,6 +118,7 @@ struct DevWS {
   const DevLayer* layers; // [max_layers] per-layer weights
   int32_t* loop;          // [AFD_LOOP_WORDS] work-item loop state and log
   uint32_t* go;           // [1] the header check's word for the router (AFD_GO_ABORT)
+  int32_t* ret_count;     // [MAX_PEERS] combine items finished per entry (return flags)
 };
 
 // The header check of a host-described step publishes, once every listed
@@ -455,15 +456,20 @@ cudaError_t launch_plan(const LaunchCtx& lc, const FanIn& f, const DevWS& ws, in
                         int inter, int shared_inter, int hidden, int has_shared, int bn,
                         GemmPlan* plan1, GemmPlan* plan2, const int32_t* hist, int32_t* base,
                         const WinGeom& g, int row_bytes, int sh_in_place);
+// ret_headers (not NULL): also write the step's return headers (every word
+// but the flag) and zero the entries' item counters (see combine_releases_flags)
 cudaError_t launch_gather(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                           const FanIn& f, const DevWS& ws, int k, int row_bytes, int hidden,
-                          int has_shared, int sh_in_place);
+                          int has_shared, int sh_in_place, uint8_t* ret_headers, int E);
 cudaError_t launch_gemm_tc(const LaunchCtx& lc, const GemmArgs& a);
 cudaError_t launch_gemm_tc2(const LaunchCtx& lc, const GemmArgs& a);
 cudaError_t launch_gemm_simt(const LaunchCtx& lc, const SimtArgs& a, int max_groups);
+// flags: the combine releases each entry's return flag after its last item
+// (the gather wrote the headers); only where combine_releases_flags holds
 cudaError_t launch_combine(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret,
                            const FanIn& f, const DevWS& ws, int hidden, int k, int act_f32,
-                           int has_shared);
+                           int has_shared, int flags);
+bool combine_releases_flags(const LaunchCtx& lc, const FanIn& f, int hidden);
 cudaError_t launch_return_header(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret,
                                  const uint8_t* win, const FanIn& f, const DevWS& ws, int E,
                                  int k);

@@ -76,6 +76,39 @@ __device__ __forceinline__ const FanIn& step_item(const FanIn& fp, const FanIn* 
   }
 }
 
+// The return header of list entry i (every word but the flag): magic,
+// version, the dispatch seq echoed, layer, stage, counts and the entry's
+// per-expert partial counts; the threads of a CTA share the words.
+__device__ void write_return_header(uint8_t* ret, const WinGeom& g, const FanIn& f, const DevWS& ws,
+                                    int E, int k, int i) {
+  const int n = f.prefix[i + 1] - f.prefix[i];
+  const uint64_t seq = ws.cur_seq[i];
+  int32_t* h = reinterpret_cast<int32_t*>(slot_ptr(ret, g, f.region[i], f.stage) + g.header);
+  for (int w = threadIdx.x; w < AFD_HEADER_FIXED_WORDS + E; w += blockDim.x) {
+    int32_t v;
+    switch (w) {
+      case 0: v = (int32_t)AFD_HEADER_MAGIC; break;
+      case 1: v = AFD_HEADER_VERSION; break;
+      case 2: v = 0; break;
+      case 3: v = (int32_t)(uint32_t)seq; break;
+      case 4: v = (int32_t)(uint32_t)seq; break;
+      case 5: v = f.layer; break;
+      case 6: v = f.stage; break;
+      case 7: v = n; break;
+      case 8: v = f.grouped ? f.rprefix[i + 1] - f.rprefix[i] : n * k; break;
+      case 9: v = ws.peer_shared[i] ? f.sprefix[i + 1] - f.sprefix[i] : 0; break;
+      case 10: v = E; break;
+      case 11: v = AFD_HEADER_FIXED_WORDS + E; break;
+      default: v = ws.peer_counts[i * E + (w - AFD_HEADER_FIXED_WORDS)];
+    }
+    h[w] = v;
+  }
+}
+
+__device__ __forceinline__ uint64_t* return_flag(uint8_t* ret, const WinGeom& g, const FanIn& f, int i) {
+  return reinterpret_cast<uint64_t*>(ret) + f.region[i] * g.ring_depth + f.stage;
+}
+
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
   return __uint_as_float((uint32_t)b << 16);
 }
@@ -2100,11 +2133,17 @@ k_rank(const __grid_constant__ FanIn fp, DevWS ws, int E, int k, const int32_t* 
 template <bool kDev>
 __global__ void __launch_bounds__(kThreads)
 k_gather(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn fp, DevWS ws, int k, int row_bytes,
-         int hidden, int has_shared, int sh_in_place) {
+         int hidden, int has_shared, int sh_in_place, uint8_t* ret_headers, int E) {
   grid_dep_wait();
   grid_dep_launch();
   const FanIn& f = step_item<kDev>(fp, ws.item);
   if (read_status(ws.status)) return;
+  if (ret_headers) {  // the combine releases the flags: the return headers now, counters zeroed
+    for (int i = blockIdx.x; i < f.n_peers; i += gridDim.x) {
+      write_return_header(ret_headers, g, f, ws, E, k, i);
+      if (threadIdx.x == 0) ws.ret_count[i] = 0;
+    }
+  }
   const int N = f.grouped ? f.rtotal : f.total * k;
   // then the shared rows; when the shared expert reads them in place, only
   // the rows of s of peers that sent none are zeroed here (the combine adds
@@ -2236,10 +2275,14 @@ __global__ void __launch_bounds__(kThreads) k_gemm_simt(SimtArgs a) {
 // rounded only once, here).  Deterministic: each output element is reduced
 // by one thread in a fixed order.
 // ---------------------------------------------------------------------------
-template <bool ACT_F32, int kBatch, bool kDev>
+template <bool ACT_F32, int kBatch, bool kDev, bool kFlags = false>
 __global__ void __launch_bounds__(kThreads)
 k_combine(uint8_t* ret, WinGeom g, const __grid_constant__ FanIn fp, DevWS ws, int hidden, int k, int has_shared) {
-  // y: fp32 with fp32 activations, else the 24-bit planes (OUT_Y24)
+  // y: fp32 with fp32 activations, else the 24-bit planes (OUT_Y24).
+  // kFlags (small fan-ins, one item per warp, every entry with tokens): the
+  // gather wrote the return headers; the warp that finishes an entry's last
+  // item releases its return flag (a counter per entry), so no return-header
+  // kernel follows
   grid_dep_wait();
   grid_dep_launch();
   const FanIn& f = step_item<kDev>(fp, ws.item);
@@ -2350,6 +2393,17 @@ k_combine(uint8_t* ret, WinGeom g, const __grid_constant__ FanIn fp, DevWS ws, i
         *reinterpret_cast<uint4*>(slot + g.routed_x + ((int64_t)local * hidden + c) * 2) = o;
       }
     }
+    if constexpr (kFlags) {
+      __threadfence();  // this item's rows (and route-table row) before its count
+      __syncwarp();
+      if (lane == 0) {
+        const int items_i = (f.prefix[i + 1] - f.prefix[i]) * nfb;
+        if (atomicAdd(&ws.ret_count[i], 1) == items_i - 1) {
+          __threadfence();  // every item of the entry is counted: its payload is out
+          st_release_u64(return_flag(ret, g, f, i), ws.cur_seq[i]);
+        }
+      }
+    }
   }
 }
 
@@ -2415,32 +2469,11 @@ __global__ void k_return_header(uint8_t* ret, WinGeom g, const __grid_constant__
   if (read_status(ws.status)) return;
   const int i = blockIdx.x;
   if (i >= f.n_peers) return;
-  const int n = f.prefix[i + 1] - f.prefix[i];
-  const uint64_t seq = ws.cur_seq[i];
-  int32_t* h = reinterpret_cast<int32_t*>(slot_ptr(ret, g, f.region[i], f.stage) + g.header);
-  for (int w = threadIdx.x; w < AFD_HEADER_FIXED_WORDS + E; w += blockDim.x) {
-    int32_t v;
-    switch (w) {
-      case 0: v = (int32_t)AFD_HEADER_MAGIC; break;
-      case 1: v = AFD_HEADER_VERSION; break;
-      case 2: v = 0; break;
-      case 3: v = (int32_t)(uint32_t)seq; break;
-      case 4: v = (int32_t)(uint32_t)seq; break;
-      case 5: v = f.layer; break;
-      case 6: v = f.stage; break;
-      case 7: v = n; break;
-      case 8: v = f.grouped ? f.rprefix[i + 1] - f.rprefix[i] : n * k; break;
-      case 9: v = ws.peer_shared[i] ? f.sprefix[i + 1] - f.sprefix[i] : 0; break;
-      case 10: v = E; break;
-      case 11: v = AFD_HEADER_FIXED_WORDS + E; break;
-      default: v = ws.peer_counts[i * E + (w - AFD_HEADER_FIXED_WORDS)];
-    }
-    h[w] = v;
-  }
+  write_return_header(ret, g, f, ws, E, k, i);
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    st_release_u64(reinterpret_cast<uint64_t*>(ret) + f.region[i] * g.ring_depth + f.stage, seq);
+    st_release_u64(return_flag(ret, g, f, i), ws.cur_seq[i]);
   }
 }
 
@@ -2875,12 +2908,12 @@ cudaError_t launch_plan(const LaunchCtx& lc, const FanIn& f, const DevWS& ws, in
 
 cudaError_t launch_gather(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                           const FanIn& f, const DevWS& ws, int k, int row_bytes, int hidden,
-                          int has_shared, int sh_in_place) {
+                          int has_shared, int sh_in_place, uint8_t* ret_headers, int E) {
   const int64_t rows = (int64_t)f.total * k + (has_shared ? f.total : 0);
   if (rows == 0) return cudaSuccess;
   return launch_k(lc, f.dev ? k_gather<true> : k_gather<false>,
                   grid_for(rows, kThreads / 32, lc.num_sms * 8), kThreads, 0, win, g, f, ws, k,
-                  row_bytes, hidden, has_shared, sh_in_place);
+                  row_bytes, hidden, has_shared, sh_in_place, ret_headers, E);
 }
 
 cudaError_t launch_gemm_simt(const LaunchCtx& lc, const SimtArgs& a, int max_groups) {
@@ -2889,7 +2922,7 @@ cudaError_t launch_gemm_simt(const LaunchCtx& lc, const SimtArgs& a, int max_gro
 }
 
 cudaError_t launch_combine(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret, const FanIn& f,
-                           const DevWS& ws, int hidden, int k, int act_f32, int has_shared) {
+                           const DevWS& ws, int hidden, int k, int act_f32, int has_shared, int flags) {
   if (f.total == 0) return cudaSuccess;
   const int64_t items = (int64_t)f.total * ((hidden + 255) / 256);
   const int grid = grid_for(items, kThreads / 32, lc.num_sms * 8);
@@ -2897,12 +2930,26 @@ cudaError_t launch_combine(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret, 
   const bool d = f.dev != 0;
   // y is fp32 (fp32 activations) or 24-bit (bf16) in the token form
   decltype(&k_combine<true, 1, false>) kern = nullptr;
-  if (act_f32)
+  if (flags)
+    kern = act_f32 ? k_combine<true, 1, false, true> : k_combine<false, 8, false, true>;
+  else if (act_f32)
     kern = d ? k_combine<true, 1, true> : k_combine<true, 1, false>;
   else
     kern = small ? (d ? k_combine<false, 8, true> : k_combine<false, 8, false>)
                  : (d ? k_combine<false, 4, true> : k_combine<false, 4, false>);
   return launch_k(lc, kern, grid, kThreads, 0, ret, g, f, ws, hidden, k, has_shared);
+}
+
+// The combine can release the return flags itself when every warp gets at
+// most one item (so counting items is cheap) and every entry has tokens
+// (an entry without any would get no item): host-described token-form steps
+// of small fan-ins.
+bool combine_releases_flags(const LaunchCtx& lc, const FanIn& f, int hidden) {
+  if (f.dev || f.grouped || f.total == 0) return false;
+  for (int i = 0; i < f.n_peers; i++)
+    if (f.prefix[i + 1] == f.prefix[i]) return false;
+  const int64_t items = (int64_t)f.total * ((hidden + 255) / 256);
+  return items <= (int64_t)lc.num_sms * 8 * (kThreads / 32);
 }
 
 cudaError_t launch_return_header(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret,

@@ -13,10 +13,11 @@ LIB_PATH = os.path.join(HERE, "libafd_gb300.so")
 AFD_OK = 0
 (AFD_ERR_ARG, AFD_ERR_SHAPE, AFD_ERR_CAPACITY, AFD_ERR_HEADER, AFD_ERR_SEQ, AFD_ERR_LAYER,
  AFD_ERR_STAGE, AFD_ERR_TIMEOUT, AFD_ERR_SHUTDOWN, AFD_ERR_SPLIT_UNEVEN, AFD_ERR_NOT_DEVICE,
- AFD_ERR_CUDA, AFD_ERR_UNSUPPORTED) = range(1, 14)
+ AFD_ERR_CUDA, AFD_ERR_UNSUPPORTED, AFD_ERR_CANARY) = range(1, 15)
 AFD_DTYPE_F32, AFD_DTYPE_BF16 = 0, 1
 AFD_GEMM_TENSOR, AFD_GEMM_SIMT, AFD_GEMM_TENSOR_1CTA = 0, 1, 2
 AFD_CFG_NO_PDL = 1
+AFD_CFG_CANARY = 2
 AFD_DIR_DISPATCH, AFD_DIR_RETURN = 0, 1
 (AFD_WS_IDS, AFD_WS_WEIGHTS, AFD_WS_COUNTS, AFD_WS_OFFSETS, AFD_WS_PERM, AFD_WS_INV, AFD_WS_XP,
  AFD_WS_H, AFD_WS_Y, AFD_WS_HS, AFD_WS_S, AFD_WS_STATUS) = range(12)
@@ -42,7 +43,7 @@ class afd_config(C.Structure):
 class afd_layout(C.Structure):
     _fields_ = [(n, C.c_int64) for n in ("header", "route_table", "routed_x", "shared_idx",
                                          "shared_x", "slot_bytes", "flags_bytes",
-                                         "window_bytes", "align")]
+                                         "window_bytes", "align", "guard")]
 
     def as_dict(self):
         return {n: int(getattr(self, n)) for n, _ in self._fields_}
@@ -85,6 +86,7 @@ SIGNATURES = [
     ("afd_get_stats", _I, [_P, C.POINTER(afd_stats)]),
     ("afd_last_expert_counts", _I, [_P, C.POINTER(C.c_int32), _I, C.POINTER(C.c_int)]),
     ("afd_launch_count", _I64, [_P]),
+    ("afd_check_canaries", _I, [_P, C.POINTER(C.c_int), C.POINTER(_I64)]),
     ("afd_strerror", C.c_char_p, [_I]),
     ("afd_profile", _I, [_P, _I]),
     ("afd_route_noalloc", _I, [_P, _I, _I, _I, _P, _P, _I, _I, _I, _F, _P, _P, _P]),
@@ -251,6 +253,13 @@ def afd_last_expert_counts(ctx, n=256):
     ne = C.c_int(0)
     _check(lib().afd_last_expert_counts(ctx, buf, n, C.byref(ne)), "afd_last_expert_counts")
     return [int(v) for v in buf[:min(n, ne.value)]]
+
+
+def afd_check_canaries(ctx):
+    """(status, window, byte offset of the first changed guard word)."""
+    w, off = C.c_int(-1), C.c_int64(-1)
+    rc = lib().afd_check_canaries(ctx, C.byref(w), C.byref(off))
+    return rc, w.value, off.value
 
 
 def afd_launch_count(ctx):

@@ -116,20 +116,23 @@ int layout_of(const afd_config* c, afd_layout* L) {
   const int64_t rcap = routed_cap_of(c);
   const int64_t rows = std::max<int64_t>(c->token_cap, rcap);
   const int64_t table = std::max<int64_t>((int64_t)c->token_cap * c->topk, c->ffn_size >= 1 ? rcap : 0);
+  // AFD_CFG_CANARY: one alignment unit of guard words after every field
+  const int64_t gd = (c->flags & AFD_CFG_CANARY) ? a : 0;
   int64_t off = 0;
   L->align = a;
+  L->guard = gd;
   L->header = off;
-  off += round_up((int64_t)(AFD_HEADER_FIXED_WORDS + c->num_experts) * 4, a);
+  off += round_up((int64_t)(AFD_HEADER_FIXED_WORDS + c->num_experts) * 4, a) + gd;
   L->route_table = off;
-  off += round_up(table * 4, a);
+  off += round_up(table * 4, a) + gd;
   L->routed_x = off;
-  off += round_up(rows * row, a);
+  off += round_up(rows * row, a) + gd;
   L->shared_idx = off;
-  if (has_shared) off += round_up((int64_t)c->token_cap * 4, a);
+  if (has_shared) off += round_up((int64_t)c->token_cap * 4, a) + gd;
   L->shared_x = off;
-  if (has_shared) off += round_up((int64_t)c->token_cap * row, a);
+  if (has_shared) off += round_up((int64_t)c->token_cap * row, a) + gd;
   L->slot_bytes = off;
-  L->flags_bytes = round_up((int64_t)c->num_peers * c->ring_depth * 8, a);
+  L->flags_bytes = round_up((int64_t)c->num_peers * c->ring_depth * 8, a) + gd;
   L->window_bytes = L->flags_bytes + (int64_t)c->num_peers * c->ring_depth * off;
   return AFD_OK;
 }
@@ -143,7 +146,7 @@ int validate_config(const afd_config* c) {
       c->max_layers < 1 || c->routed_cap_multiplier < 1.0f || c->wait_timeout_ns < 0)
     return AFD_ERR_ARG;
   if (c->act_dtype != AFD_DTYPE_F32 && c->act_dtype != AFD_DTYPE_BF16) return AFD_ERR_ARG;
-  if (c->flags & ~AFD_CFG_NO_PDL) return AFD_ERR_ARG;
+  if (c->flags & ~(AFD_CFG_NO_PDL | AFD_CFG_CANARY)) return AFD_ERR_ARG;
   if (c->ffn_size < 0 || c->ffn_size > AFD_MAX_FFN_RANKS || c->ffn_rank < 0 ||
       c->ffn_rank >= std::max(1, c->ffn_size))
     return AFD_ERR_ARG;
@@ -194,6 +197,7 @@ struct afd_ctx {
   int last_T = 0;
   int64_t forwards = 0;
   uint32_t go_seq = 0;               // tokens for ws.go, one per host-described routed step
+  unsigned long long* canary_result = nullptr;  // AFD_CFG_CANARY: [changed words, first offset]
   int64_t ws_cap[12];
   // stage timing: one set of events per forward, in a ring, so the host
   // reads them after many forwards instead of waiting after each one
@@ -238,10 +242,30 @@ struct afd_ctx {
   int64_t timeout() const { return cfg.wait_timeout_ns ? cfg.wait_timeout_ns : 1000000000ll; }
 };
 
+static CanaryGeom canary_geom(const afd_ctx* c);
+
 static int cuda_fail(cudaError_t e, const char* what) {
   if (e == cudaSuccess) return AFD_OK;
   fprintf(stderr, "afd: %s: %s\n", what, cudaGetErrorString(e));
   return AFD_ERR_CUDA;
+}
+
+// the guard regions of a context's windows (AFD_CFG_CANARY)
+static CanaryGeom canary_geom(const afd_ctx* c) {
+  const afd_layout& L = c->L;
+  CanaryGeom cg;
+  memset(&cg, 0, sizeof cg);
+  cg.flags_bytes = L.flags_bytes;
+  cg.slot_bytes = L.slot_bytes;
+  cg.guard = L.guard;
+  const bool sh = c->cfg.shared_inter > 0;
+  // each field's guard ends where the next field (or the slot) begins
+  const int64_t ends[5] = {L.route_table, L.routed_x, L.shared_idx, sh ? L.shared_x : 0, L.slot_bytes};
+  const int nf = sh ? 5 : 3;
+  for (int i = 0; i < nf; i++) cg.goff[i] = (i == nf - 1 ? L.slot_bytes : ends[i]) - L.guard;
+  cg.n = nf;
+  cg.nslots = c->cfg.num_peers * c->cfg.ring_depth;
+  return cg;
 }
 
 extern "C" {
@@ -262,6 +286,7 @@ const char* afd_strerror(int code) {
     case AFD_ERR_NOT_DEVICE: return "pointer is not device memory";
     case AFD_ERR_CUDA: return "CUDA error";
     case AFD_ERR_UNSUPPORTED: return "unsupported configuration";
+    case AFD_ERR_CANARY: return "guard word after a slot field overwritten";
     default: return "unknown status";
   }
 }
@@ -309,6 +334,7 @@ void afd_destroy(afd_ctx* ctx) {
       if (e) cudaEventDestroy(e);
   cudaFree(ctx->win[0]);
   cudaFree(ctx->win[1]);
+  cudaFree(ctx->canary_result);
   cudaFree(ctx->ws_mem);
   delete ctx;
 }
@@ -344,6 +370,14 @@ int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out) {
   for (int d = 0; d < 2; d++) {
     rc = cuda_fail(cudaMalloc(&c->win[d], c->L.window_bytes), "window allocation");
     if (!rc) rc = cuda_fail(cudaMemset(c->win[d], 0, c->L.window_bytes), "window zero");
+    if (!rc && c->L.guard)
+      rc = cuda_fail(launch_canary(nullptr, c->win[d], canary_geom(c), 1, nullptr, c->num_sms),
+                     "canary fill");
+    if (rc) { afd_destroy(c); return rc; }
+  }
+  if (c->L.guard) {
+    rc = cuda_fail(cudaMalloc(&c->canary_result, 2 * sizeof(unsigned long long)), "canary result");
+    if (!rc) rc = cuda_fail(cudaDeviceSynchronize(), "canary fill");
     if (rc) { afd_destroy(c); return rc; }
   }
   // workspace
@@ -1232,6 +1266,28 @@ int afd_last_expert_counts(afd_ctx* ctx, int32_t* counts, int n, int* n_experts)
 }
 
 int64_t afd_launch_count(afd_ctx* ctx) { return ctx ? ctx->launches : -1; }
+
+int afd_check_canaries(afd_ctx* ctx, int* window, int64_t* offset) {
+  if (!ctx || !ctx->L.guard || !ctx->canary_result) return AFD_ERR_ARG;
+  if (cuda_fail(cudaStreamSynchronize(ctx->stream), "stream sync")) return AFD_ERR_CUDA;
+  const CanaryGeom cg = canary_geom(ctx);
+  for (int d = 0; d < 2; d++) {
+    const unsigned long long init[2] = {0ull, ~0ull};
+    unsigned long long res[2];
+    if (cuda_fail(cudaMemcpy(ctx->canary_result, init, sizeof init, cudaMemcpyHostToDevice), "canary") ||
+        cuda_fail(launch_canary(ctx->stream, ctx->win[d], cg, 0, ctx->canary_result, ctx->num_sms),
+                  "canary check") ||
+        cuda_fail(cudaStreamSynchronize(ctx->stream), "canary check") ||
+        cuda_fail(cudaMemcpy(res, ctx->canary_result, sizeof res, cudaMemcpyDeviceToHost), "canary"))
+      return AFD_ERR_CUDA;
+    if (res[0]) {
+      if (window) *window = d;
+      if (offset) *offset = (int64_t)res[1];
+      return AFD_ERR_CANARY;
+    }
+  }
+  return AFD_OK;
+}
 
 int afd_profile(afd_ctx* ctx, int enable) {
   if (!ctx) return AFD_ERR_ARG;

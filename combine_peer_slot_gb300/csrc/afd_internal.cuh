@@ -89,6 +89,23 @@ struct WinGeom {
   int num_regions;
 };
 
+// Guard regions of a window (AFD_CFG_CANARY): `guard` bytes before
+// flags_bytes, and in every slot `guard` bytes at each of the n offsets in
+// goff (relative to the slot).  The word at byte offset o of the window
+// holds canary_word(o).
+struct CanaryGeom {
+  int64_t flags_bytes, slot_bytes, guard;
+  int64_t goff[5];
+  int n, nslots;
+};
+__host__ __device__ inline uint32_t canary_word(int64_t off) {
+  return 0xCA11AFD0u ^ (uint32_t)(off >> 2) ^ ((uint32_t)(off >> 34) << 16);
+}
+// fill: write the pattern; else count changed words into result[0] and the
+// lowest changed offset into result[1] (initialised by the caller)
+cudaError_t launch_canary(cudaStream_t stream, uint8_t* win, const CanaryGeom& cg, int fill,
+                          unsigned long long* result, int num_sms);
+
 // workspace pointers
 struct DevWS {
   int32_t* status;        // [1] sticky first error

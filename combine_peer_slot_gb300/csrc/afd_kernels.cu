@@ -2151,7 +2151,43 @@ k_gather(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn fp, DevWS 
   const int rows = N + (has_shared ? f.stotal : 0);
   const int nvec = row_bytes / 16;
   const int warps = gridDim.x * (blockDim.x >> 5);
-  for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
+  const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  // token form, large fan-ins: the routed copies in token order, each
+  // token's row read once from its slot and written to its k positions
+  // (walking the positions instead read each row k times, far apart, and L2
+  // kept few of them: 3.2x the rows' bytes came from DRAM at the V2-Lite
+  // prefill shape, 0.081 -> 0.061 ms).  Small fan-ins keep position order:
+  // their rows stay in L2, and a warp per position spreads the copies over
+  // more warps (token order measured 2.4 us per decode layer slower).
+  const bool token_order = !f.grouped && N > kPlanSmallMax;
+  if (token_order) {
+    const int lane = threadIdx.x & 31;
+    for (int t = wid; t < f.total; t += warps) {
+      const int i = entry_of(f, t);
+      const uint4* src = reinterpret_cast<const uint4*>(slot_ptr(win, g, f.region[i], f.stage) + g.routed_x +
+                                                        (int64_t)(t - f.prefix[i]) * row_bytes);
+      const int my_pos = lane < k ? ws.inv[(int64_t)t * k + lane] : 0;
+      for (int v0 = 0; v0 < nvec; v0 += 32 * 8) {
+        uint4 buf[8];
+#pragma unroll
+        for (int u = 0; u < 8; u++) {
+          const int v = v0 + 32 * u + lane;
+          buf[u] = v < nvec ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+        }
+        for (int j = 0; j < k; j++) {
+          const int pos = __shfl_sync(0xffffffffu, my_pos, j);
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(ws.xp) + (int64_t)pos * row_bytes);
+#pragma unroll
+          for (int u = 0; u < 8; u++) {
+            const int v = v0 + 32 * u + lane;
+            if (v < nvec) dst[v] = buf[u];
+          }
+        }
+      }
+    }
+  }
+  // rows by position (grouped, or small token-form fan-ins); then the shared rows
+  for (int r = (token_order ? N : 0) + wid; r < rows; r += warps) {
     uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(ws.xp) + (int64_t)r * row_bytes);
     int i, local;
     int64_t field;
@@ -2629,6 +2665,39 @@ inline int grid_for(int64_t work, int per_block, int cap) {
 // ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
+// Canary words (AFD_CFG_CANARY): write the pattern into every guard word of
+// a window, or count the words that differ from it.
+__global__ void k_canary(uint8_t* win, CanaryGeom cg, int fill, unsigned long long* result) {
+  const int64_t per_slot = (int64_t)cg.n * (cg.guard / 4);
+  const int64_t flag_words = cg.guard / 4;
+  const int64_t total = flag_words + per_slot * cg.nslots;
+  for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < total;
+       w += (int64_t)gridDim.x * blockDim.x) {
+    int64_t off;
+    if (w < flag_words) {
+      off = cg.flags_bytes - cg.guard + 4 * w;
+    } else {
+      const int64_t v = w - flag_words;
+      const int64_t slot = v / per_slot, r = v % per_slot;
+      const int gi = (int)(r / (cg.guard / 4));
+      off = cg.flags_bytes + slot * cg.slot_bytes + cg.goff[gi] + 4 * (r % (cg.guard / 4));
+    }
+    uint32_t* p = reinterpret_cast<uint32_t*>(win + off);
+    if (fill) {
+      *p = canary_word(off);
+    } else if (*p != canary_word(off)) {
+      atomicAdd(&result[0], 1ull);
+      atomicMin(&result[1], (unsigned long long)off);
+    }
+  }
+}
+
+cudaError_t launch_canary(cudaStream_t stream, uint8_t* win, const CanaryGeom& cg, int fill,
+                          unsigned long long* result, int num_sms) {
+  k_canary<<<num_sms * 4, kThreads, 0, stream>>>(win, cg, fill, result);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_pack_payload(const LaunchCtx& lc, const WinGeom& g, uint8_t* win, int region,
                                 int stage, const void* rows, int n_rows, const void* xs, int n_shared,
                                 int row_bytes) {

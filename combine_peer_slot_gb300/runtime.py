@@ -34,7 +34,8 @@ class Runner:
     layer weights registered, and helpers for pack / forward / unpack."""
 
     def __init__(self, w: W.Workload, gemm=A.AFD_GEMM_TENSOR, layers=None, stream=None,
-                 max_total_tokens=0, wait_timeout_ns=0, device="cuda", flags=0, ring_depth=1):
+                 max_total_tokens=0, wait_timeout_ns=0, device="cuda", flags=0, ring_depth=1,
+                 canary=False):
         import torch
         self.w = w
         self.device = device
@@ -44,10 +45,12 @@ class Runner:
                                  w.inter, w.shared_inter, act=w.act, renorm=w.renorm,
                                  routed_scaling=w.routed_scaling, max_layers=self.layers,
                                  max_total_tokens=max_total_tokens, gemm=gemm,
-                                 wait_timeout_ns=wait_timeout_ns, flags=flags,
+                                 wait_timeout_ns=wait_timeout_ns,
+                                 flags=flags | (A.AFD_CFG_CANARY if canary else 0),
                                  ring_depth=ring_depth)
         self.ctx = A.afd_create(self.cfg, self.stream.cuda_stream)
         self.layout = A.afd_slot_layout(self.cfg)
+        self.canary = bool(canary)
         self.host = W.host_inputs(w)
         self.x = [act_tensor(a, w.act, device) for a in self.host["x"]]
         self.Wg = torch.from_numpy(self.host["Wg"]).to(device)

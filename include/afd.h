@@ -61,6 +61,7 @@ extern "C" {
                                   (Data on the wire: CPU tensors are rejected) */
 #define AFD_ERR_CUDA 12        /* a CUDA runtime/driver call failed */
 #define AFD_ERR_UNSUPPORTED 13 /* configuration outside what the kernels cover */
+#define AFD_ERR_CANARY 14      /* a guard word after a slot field was overwritten */
 
 #define AFD_DTYPE_F32 0
 #define AFD_DTYPE_BF16 1
@@ -112,6 +113,13 @@ extern "C" {
  * letting its CTAs be scheduled (and wait on the device) while the previous
  * kernel drains (programmatic dependent launch, the default). */
 #define AFD_CFG_NO_PDL 1
+/* Guard words after the flag array and after every slot field, filled with
+ * a position-dependent pattern when the windows are created and checked by
+ * afd_check_canaries: a write past the end of a field changes them.  Each
+ * guard is one alignment unit (afd_layout.align bytes), so every field
+ * stays aligned; the offsets afd_slot_layout gives include the guards.  A
+ * substitute for a memory checker, for tests. */
+#define AFD_CFG_CANARY 2
 typedef struct afd_config {
   int32_t num_peers;
   int32_t ring_depth;
@@ -151,6 +159,11 @@ typedef struct afd_config {
 typedef struct afd_layout {
   int64_t header, route_table, routed_x, shared_idx, shared_x;
   int64_t slot_bytes, flags_bytes, window_bytes, align;
+  /* AFD_CFG_CANARY: bytes of each guard (align), else 0.  A field's guard is
+   * the `guard` bytes before the next field's offset (before slot_bytes for
+   * the slot's last field); the flag array's, the `guard` bytes before
+   * flags_bytes. */
+  int64_t guard;
 } afd_layout;
 
 /* Header words (int32), Async GPU Connector, "Window and slot layout": a
@@ -495,6 +508,13 @@ int afd_last_expert_counts(afd_ctx* ctx, int32_t* counts, int n, int* n_experts)
 
 /* Kernel launches the library issued on this context since creation. */
 int64_t afd_launch_count(afd_ctx* ctx);
+
+/* Synchronise the stream and check every guard word of both windows of a
+ * context created with AFD_CFG_CANARY.  AFD_OK when all are intact, else
+ * AFD_ERR_CANARY with *window (AFD_DIR_*) and *offset (byte offset within
+ * that window of the first changed word; both may be NULL).  AFD_ERR_ARG for
+ * a context without guards, AFD_ERR_CUDA if the check itself fails. */
+int afd_check_canaries(afd_ctx* ctx, int* window, int64_t* offset);
 
 /* Stage timing.  With enable != 0, every afd_ffn_forward records a CUDA
  * event on the context's stream before and after each stage:

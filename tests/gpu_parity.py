@@ -30,15 +30,16 @@ def ws_array(run, which, count, dtype):
     return run.workspace(which, nbytes).cpu().numpy().view(dtype)
 
 
-def slot_off(run, peer, stage=0):
-    """Byte offset of slot (peer, stage); the runner uses one stage per peer."""
-    L = run.layout
+def slot_off(run, peer, stage=0, L=None):
+    """Byte offset of slot (peer, stage) in layout L (the run's by default)."""
+    L = run.layout if L is None else L
     return L.flags_bytes + (peer * run.cfg.ring_depth + stage) * L.slot_bytes
 
 
-def return_rows(ret, run, peer, n):
-    L, w = run.layout, run.w
-    off = slot_off(run, peer) + L.routed_x
+def return_rows(ret, run, peer, n, L=None):
+    L = run.layout if L is None else L
+    w = run.w
+    off = slot_off(run, peer, L=L) + L.routed_x
     rb = w.hidden * w.act_bytes
     raw = ret[off: off + n * rb]
     if w.act == "bf16":
@@ -46,14 +47,53 @@ def return_rows(ret, run, peer, n):
     return raw.view(np.float32).astype(np.float64).reshape(n, w.hidden)
 
 
-def route_table(ret, run, peer, n):
-    off = slot_off(run, peer) + run.layout.route_table
+def route_table(ret, run, peer, n, L=None):
+    L = run.layout if L is None else L
+    off = slot_off(run, peer, L=L) + L.route_table
     return ret[off: off + n * run.w.topk * 4].view(np.int32).reshape(n, run.w.topk)
 
 
-def header(buf, run, peer):
-    off = slot_off(run, peer) + run.layout.header
+def header(buf, run, peer, L=None):
+    L = run.layout if L is None else L
+    off = slot_off(run, peer, L=L) + L.header
     return buf[off: off + 4 * (12 + run.w.num_experts)].view(np.int32)
+
+
+def plain_layout(run):
+    """The run's slot layout without guard words (the oracle's)."""
+    cfg = A.afd_config.from_buffer_copy(run.cfg)
+    cfg.flags = cfg.flags & ~A.AFD_CFG_CANARY
+    return A.afd_slot_layout(cfg)
+
+
+def plain_window(run, buf):
+    """A window of a run created with canaries, re-laid without the guard
+    words (every field moved to its offset in the plain layout), for the
+    oracle, which knows no guards."""
+    Lg = run.layout
+    if not Lg.guard:
+        return buf
+    Lp = plain_layout(run)
+    out = np.zeros(Lp.window_bytes, np.uint8)
+    nslots = run.cfg.num_peers * run.cfg.ring_depth
+    out[:nslots * 8] = buf[:nslots * 8]
+    names = ["header", "route_table", "routed_x", "shared_idx", "shared_x"]
+    starts = [getattr(Lp, n) for n in names] + [Lp.slot_bytes]
+    for s_ in range(nslots):
+        bg = Lg.flags_bytes + s_ * Lg.slot_bytes
+        bp = Lp.flags_bytes + s_ * Lp.slot_bytes
+        for i, n in enumerate(names):
+            size = starts[i + 1] - starts[i]
+            if size:
+                out[bp + starts[i]: bp + starts[i] + size] = buf[bg + getattr(Lg, n): bg + getattr(Lg, n) + size]
+    return out
+
+
+def check_canaries(run):
+    """Every guard word after the slot fields intact (runs with canaries)."""
+    if run.layout.guard:
+        rc, win, off = A.afd_check_canaries(run.ctx)
+        assert rc == A.AFD_OK, f"guard word changed: window {win}, byte offset {off}"
 
 
 def rel_err(got, ref):
@@ -87,8 +127,11 @@ def run_and_compare_full(run, slots=None, layer=0, pack=True):
     assert rc == 0, A.strerror(rc)
     outs = run.unpack_all(peers=slots)
     assert run.poll() == 0
-    win = run.window(A.AFD_DIR_DISPATCH).cpu().numpy()
-    ret = run.window(A.AFD_DIR_RETURN).cpu().numpy()
+    check_canaries(run)
+    # the oracle reads and writes windows without guard words
+    win = plain_window(run, run.window(A.AFD_DIR_DISPATCH).cpu().numpy())
+    ret = plain_window(run, run.window(A.AFD_DIR_RETURN).cpu().numpy())
+    Lp = plain_layout(run)
     c = oracle_cfg(run)
     ret_orc = np.zeros_like(win)
     seen = np.zeros(w.num_peers, np.uint64)
@@ -103,13 +146,14 @@ def run_and_compare_full(run, slots=None, layer=0, pack=True):
     assert np.allclose(wts, r["w"], rtol=1e-6, atol=0), np.abs(wts / r["w"] - 1).max()
     errs = []
     start = 0
+    nflags = run.cfg.num_peers * run.cfg.ring_depth * 8
     for p in slots:
         n = w.seq_lens[p]
-        assert np.array_equal(header(ret, run, p), header(ret_orc, run, p))
-        assert ret[:run.layout.flags_bytes].view(np.uint64)[p] == ret_orc[:run.layout.flags_bytes].view(np.uint64)[p]
+        assert np.array_equal(header(ret, run, p, Lp), header(ret_orc, run, p, Lp))
+        assert ret[:nflags].view(np.uint64)[p] == ret_orc[:nflags].view(np.uint64)[p]
         if n:
-            assert np.array_equal(route_table(ret, run, p, n), route_table(ret_orc, run, p, n))
-            got = return_rows(ret, run, p, n)
+            assert np.array_equal(route_table(ret, run, p, n, Lp), route_table(ret_orc, run, p, n, Lp))
+            got = return_rows(ret, run, p, n, Lp)
             ref = r["out64"][start:start + n]
             errs.append((got, ref))
             o = outs[p][:n].float().cpu().numpy().astype(np.float64)

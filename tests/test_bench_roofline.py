@@ -69,3 +69,28 @@ def test_grouped_form_matches_token_form_when_rows_agree():
     # the token form keeps 24 bits of it for its combine
     T, H, k = w.total_tokens, w.hidden, w.topk
     assert a["gemm_down"]["bytes"] - b["gemm_down"]["bytes"] == T * k * H * (3 - 2)
+
+
+def test_stage_bytes_never_exceed_the_hbm_peak_at_recorded_times():
+    """The algorithmic bytes bench.py counts for each stage, over that
+    stage's time in a recorded bench line, stay under the measured HBM copy
+    rate: an over-count (a row counted k times that is read once) would show
+    as an impossible bandwidth.  Every expert's weights are counted (an upper
+    bound)."""
+    import json
+    import os
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    for name, fname in (("v2lite_prefill", "bench_v2lite_prefill.json"),
+                        ("decode", "bench_decode_26layers.json")):
+        with open(os.path.join(root, "profiles", fname)) as f:
+            line = json.load(f)
+        w = W.get(name)
+        work = bench.stage_work(w, w.total_tokens)
+        checked = 0
+        for stage, ms in line["stages_ms"].items():
+            nbytes = work.get(stage, {}).get("bytes")
+            if nbytes:
+                gbs = nbytes / (ms * 1e-3) / 1e9
+                assert gbs <= PEAKS["hbm_gbs"] * 1.02, (name, stage, gbs)
+                checked += 1
+        assert checked >= 5, name

@@ -26,7 +26,7 @@ def test_all_peers_empty():
     """Every listed peer sends no tokens: no expert work, and each return
     slot still gets its header (num_tokens 0, no counts) and its flag."""
     w = W.custom("fanin", seq_lens=[0, 0, 0], token_cap=64)
-    run = R.Runner(w, max_total_tokens=64)
+    run = R.Runner(w, max_total_tokens=64, canary=True)
     run.pack_all(0)
     assert run.forward(0) == 0
     assert run.poll() == 0
@@ -60,7 +60,7 @@ def test_shapes_at_the_edges(shape):
     wide token tiles over odd and partial k-block counts, layers with and
     without a shared expert."""
     w = W.custom("fanin", **shape)
-    run = R.Runner(w, max_total_tokens=w.total_tokens)
+    run = R.Runner(w, max_total_tokens=w.total_tokens, canary=True)
     e, _ = G.run_and_compare_full(run)
     print(shape, "max|err|/rms", e)
     run.close()
@@ -72,7 +72,7 @@ def test_sixty_four_peers():
     rng = np.random.default_rng(64)
     lens = [int(v) for v in rng.integers(0, 9, size=A.AFD_MAX_PEERS)]
     w = W.custom("fanin", seq_lens=lens, token_cap=16)
-    run = R.Runner(w, max_total_tokens=w.total_tokens)
+    run = R.Runner(w, max_total_tokens=w.total_tokens, canary=True)
     slots = [int(v) for v in rng.permutation(A.AFD_MAX_PEERS)]
     e, _ = G.run_and_compare_full(run, slots=slots)
     print("64 peers, T =", sum(lens), "max|err|/rms", e)

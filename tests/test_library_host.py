@@ -38,7 +38,7 @@ def test_exports_every_declared_function(lib):
 
 
 def test_strerror(lib):
-    for code in range(0, 14):
+    for code in range(0, 15):
         assert A.strerror(code) and A.strerror(code) != "unknown status"
     assert A.strerror(99) == "unknown status"
 
@@ -50,7 +50,9 @@ def test_layout_matches_oracle(golden, lib):
                             shared_inter=64 if case["has_shared"] else 0,
                             act="f32" if case["act_bytes"] == 4 else "bf16",
                             ring_depth=case["ring_depth"], gemm=A.AFD_GEMM_SIMT)
-        assert A.afd_slot_layout(cfg).as_dict() == case["expect"]
+        got = A.afd_slot_layout(cfg).as_dict()
+        assert got.pop("guard") == 0
+        assert got == case["expect"]
     rng = np.random.default_rng(2)
     for _ in range(300):
         P, D = int(rng.integers(1, 65)), int(rng.integers(1, 9))
@@ -61,8 +63,33 @@ def test_layout_matches_oracle(golden, lib):
         cfg = A.make_config(P, cap, H, E, k, 64, shared_inter=Is, act=act, ring_depth=D,
                             gemm=A.AFD_GEMM_SIMT)
         ours = A.afd_slot_layout(cfg).as_dict()
+        assert ours.pop("guard") == 0
         ref = O.slot_layout(P, D, cap, k, H, 2 if act == "bf16" else 4, E, Is > 0).as_dict()
         assert ours == ref
+
+
+def test_canary_layout_adds_one_guard_after_every_field(lib):
+    """AFD_CFG_CANARY: the flag array and every slot field are followed by one
+    alignment unit of guard words, so each field sits after the guards of
+    the fields before it and stays aligned."""
+    rng = np.random.default_rng(5)
+    for _ in range(200):
+        P, D = int(rng.integers(1, 65)), int(rng.integers(1, 9))
+        cap, k = int(rng.integers(1, 20000)), int(rng.integers(1, 17))
+        H, E = int(rng.integers(1, 293)) * 8, int(rng.integers(k, 257))
+        act = str(rng.choice(["bf16", "f32"]))
+        Is = int(rng.choice([0, 64]))
+        kw = dict(shared_inter=Is, act=act, ring_depth=D, gemm=A.AFD_GEMM_SIMT)
+        plain = A.afd_slot_layout(A.make_config(P, cap, H, E, k, 64, **kw)).as_dict()
+        g = A.afd_slot_layout(A.make_config(P, cap, H, E, k, 64, flags=A.AFD_CFG_CANARY, **kw)).as_dict()
+        a = plain["align"]
+        assert g["guard"] == a and g["align"] == a and plain["guard"] == 0
+        fields = ["header", "route_table", "routed_x"] + (["shared_idx", "shared_x"] if Is else [])
+        for i, f in enumerate(fields):
+            assert g[f] == plain[f] + i * a and g[f] % a == 0
+        assert g["slot_bytes"] == plain["slot_bytes"] + len(fields) * a
+        assert g["flags_bytes"] == plain["flags_bytes"] + a
+        assert g["window_bytes"] == g["flags_bytes"] + P * D * g["slot_bytes"]
 
 
 def test_split_sizes(golden, lib):
@@ -138,6 +165,7 @@ def test_rank_layout_and_experts_match_oracle(lib):
                             gemm=A.AFD_GEMM_SIMT, routed_cap_multiplier=mult, ffn_rank=r,
                             ffn_size=F)
         ours = A.afd_slot_layout(cfg).as_dict()
+        assert ours.pop("guard") == 0
         rcap = O.routed_cap(cap, min(k, cnt), F, mult)
         ref = O.slot_layout_ranks(cfg.num_peers, cfg.ring_depth, cap, min(k, cnt), H,
                                   2 if act == "bf16" else 4, cnt, Is > 0, rcap).as_dict()

@@ -19,7 +19,7 @@ def _cuda():
 
 
 def test_tiny_fp32():
-    run = R.Runner(W.get("tiny"), gemm=A.AFD_GEMM_SIMT)
+    run = R.Runner(W.get("tiny"), gemm=A.AFD_GEMM_SIMT, canary=True)
     e, _ = G.run_and_compare_full(run)
     print("tiny max|err|/rms", e)
 
@@ -27,7 +27,7 @@ def test_tiny_fp32():
 @pytest.mark.parametrize("gemm", [A.AFD_GEMM_TENSOR, A.AFD_GEMM_TENSOR_1CTA, A.AFD_GEMM_SIMT],
                          ids=["tcgen05_pair", "tcgen05_1cta", "simt"])
 def test_fanin_bf16(gemm):
-    run = R.Runner(W.get("fanin"), gemm=gemm)
+    run = R.Runner(W.get("fanin"), gemm=gemm, canary=True)
     e, _ = G.run_and_compare_full(run)
     print("fanin max|err|/rms", e)
 
@@ -41,7 +41,7 @@ def test_weights_copied_at_registration(gemm):
     weights; a second registration of the same layer (same sizes, copies
     reused) then takes the new values."""
     w = W.get("fanin")
-    run = R.Runner(w, gemm=gemm)
+    run = R.Runner(w, gemm=gemm, canary=True)
     snap = run.weights_numpy(0)
     for key in ("W13", "Wd", "W13s", "Wds"):
         if run.weights[0][key] is not None:
@@ -69,14 +69,14 @@ def test_serialised_launches(workload):
     """Every kernel launched after the previous one has finished (no
     programmatic dependent launch): the same results."""
     w = W.get(workload)
-    run = R.Runner(w, max_total_tokens=w.total_tokens, flags=A.AFD_CFG_NO_PDL)
+    run = R.Runner(w, max_total_tokens=w.total_tokens, flags=A.AFD_CFG_NO_PDL, canary=True)
     if workload == "fanin":
         G.run_and_compare_full(run)
     else:
         # the full-size step is compared with the oracle row by row in
         # test_v2lite_prefill_full_size; here the return window of the
         # serialised launches must equal the default launches' byte for byte
-        ref = R.Runner(w, max_total_tokens=w.total_tokens)
+        ref = R.Runner(w, max_total_tokens=w.total_tokens, canary=True)
         wins = []
         for r in (run, ref):
             r.pack_all(0)
@@ -90,7 +90,7 @@ def test_serialised_launches(workload):
 
 def test_fanin_reordered_with_empty_peer():
     w = W.custom("fanin", seq_lens=[37, 0, 91, 5])
-    run = R.Runner(w)
+    run = R.Runner(w, canary=True)
     G.run_and_compare_full(run, slots=[2, 1, 3, 0])
 
 
@@ -98,7 +98,7 @@ def test_fanin_subset_of_peers_and_repeat():
     """Only some peers in the fan-in; then a second round on the same slots
     (the flags must advance) gives the same answer."""
     w = W.custom("fanin", seq_lens=[37, 91, 64])
-    run = R.Runner(w)
+    run = R.Runner(w, canary=True)
     G.run_and_compare_full(run, slots=[2, 0])
     e2, _ = G.run_and_compare_full(run, slots=[2, 0])
 
@@ -106,7 +106,7 @@ def test_fanin_subset_of_peers_and_repeat():
 def test_single_peer_ragged_tiles():
     """One peer, token counts that leave ragged 16/32/256 tails per expert."""
     w = W.custom("fanin", seq_lens=[301], num_experts=8, topk=2)
-    run = R.Runner(w)
+    run = R.Runner(w, canary=True)
     G.run_and_compare_full(run)
 
 
@@ -115,7 +115,7 @@ def test_v2lite_prefill_full_size():
     runs the same fan-in on all host cores), with routing, plan, headers and
     route tables bit-exact."""
     w = W.get("v2lite_prefill")
-    run = R.Runner(w, max_total_tokens=w.total_tokens)
+    run = R.Runner(w, max_total_tokens=w.total_tokens, canary=True)
     e, _ = G.run_and_compare_full(run)
     print("v2lite max|err|/rms", e)
     run.close()
@@ -123,7 +123,7 @@ def test_v2lite_prefill_full_size():
 
 def test_skewed_full_size():
     w = W.get("skewed")
-    run = R.Runner(w, max_total_tokens=w.total_tokens)
+    run = R.Runner(w, max_total_tokens=w.total_tokens, canary=True)
     e, _ = G.run_and_compare_full(run)
     print("skewed max|err|/rms", e)
     counts = G.ws_array(run, A.AFD_WS_COUNTS, w.num_experts, np.int32)
@@ -134,7 +134,7 @@ def test_skewed_full_size():
 def test_decode_26_layers():
     """All 26 layers, every output row of each, through one context."""
     w = W.get("decode")
-    run = R.Runner(w, max_total_tokens=w.total_tokens)
+    run = R.Runner(w, max_total_tokens=w.total_tokens, canary=True)
     worst = 0.0
     for layer in range(w.layers):
         e, _ = G.run_and_compare_full(run, layer=layer)
@@ -149,7 +149,7 @@ def test_fanin_peer_without_shared_rows(gemm):
     do: its tokens get no shared-expert term, while the shared expert reads
     the other peers' rows in place from their slots."""
     w = W.custom("fanin", seq_lens=[37, 20, 91])
-    run = R.Runner(w, max_total_tokens=w.total_tokens, gemm=gemm)
+    run = R.Runner(w, max_total_tokens=w.total_tokens, gemm=gemm, canary=True)
     run.pack_all(peers=[0, 2])
     run.pack_all(peers=[1], with_shared=False)
     e, _ = G.run_and_compare_full(run, pack=False)

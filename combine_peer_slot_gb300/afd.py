@@ -13,11 +13,14 @@ LIB_PATH = os.path.join(HERE, "libafd_gb300.so")
 AFD_OK = 0
 (AFD_ERR_ARG, AFD_ERR_SHAPE, AFD_ERR_CAPACITY, AFD_ERR_HEADER, AFD_ERR_SEQ, AFD_ERR_LAYER,
  AFD_ERR_STAGE, AFD_ERR_TIMEOUT, AFD_ERR_SHUTDOWN, AFD_ERR_SPLIT_UNEVEN, AFD_ERR_NOT_DEVICE,
- AFD_ERR_CUDA, AFD_ERR_UNSUPPORTED, AFD_ERR_CANARY) = range(1, 15)
+ AFD_ERR_CUDA, AFD_ERR_UNSUPPORTED, AFD_ERR_CANARY, AFD_ERR_BOUNDS) = range(1, 16)
 AFD_DTYPE_F32, AFD_DTYPE_BF16 = 0, 1
 AFD_GEMM_TENSOR, AFD_GEMM_SIMT, AFD_GEMM_TENSOR_1CTA = 0, 1, 2
 AFD_CFG_NO_PDL = 1
 AFD_CFG_CANARY = 2
+(AFD_DBG_GATHER_INV, AFD_DBG_GATHER_PERM, AFD_DBG_GATHER_GROUPED, AFD_DBG_COMBINE_INV,
+ AFD_DBG_SCATTER_INV, AFD_DBG_GEMM_OUT) = range(1, 7)
+AFD_DBG_NUM_SITES = 7
 AFD_DIR_DISPATCH, AFD_DIR_RETURN = 0, 1
 (AFD_WS_IDS, AFD_WS_WEIGHTS, AFD_WS_COUNTS, AFD_WS_OFFSETS, AFD_WS_PERM, AFD_WS_INV, AFD_WS_XP,
  AFD_WS_H, AFD_WS_Y, AFD_WS_HS, AFD_WS_S, AFD_WS_STATUS) = range(12)
@@ -87,6 +90,8 @@ SIGNATURES = [
     ("afd_last_expert_counts", _I, [_P, C.POINTER(C.c_int32), _I, C.POINTER(C.c_int)]),
     ("afd_launch_count", _I64, [_P]),
     ("afd_check_canaries", _I, [_P, C.POINTER(C.c_int), C.POINTER(_I64)]),
+    ("afd_debug_bounds", _I, [_P, C.POINTER(C.c_int32), C.POINTER(_I64), C.POINTER(_I64)]),
+    ("afd_debug_plant", _I, [_P, C.c_int32]),
     ("afd_strerror", C.c_char_p, [_I]),
     ("afd_profile", _I, [_P, _I]),
     ("afd_route_noalloc", _I, [_P, _I, _I, _I, _P, _P, _I, _I, _I, _F, _P, _P, _P]),
@@ -115,10 +120,12 @@ STAGE_NAMES = ("header_check", "router", "plan", "gather", "gemm_swiglu", "gemm_
 
 def lib(path=None):
     """Load the library once; raise if it is missing (build it with
-    __graft_entry__.build() or combine_peer_slot_gb300/build.py)."""
+    __graft_entry__.build() or combine_peer_slot_gb300/build.py).  The
+    AFD_LIBRARY environment variable names another build to load instead
+    (e.g. the bounds-checking libafd_gb300_dbg.so)."""
     global _lib
     if _lib is None:
-        path = path or LIB_PATH
+        path = path or os.environ.get("AFD_LIBRARY") or LIB_PATH
         if not os.path.exists(path):
             raise ImportError(f"{path} is not built; run __graft_entry__.build()")
         L = C.CDLL(path)
@@ -260,6 +267,18 @@ def afd_check_canaries(ctx):
     w, off = C.c_int(-1), C.c_int64(-1)
     rc = lib().afd_check_canaries(ctx, C.byref(w), C.byref(off))
     return rc, w.value, off.value
+
+
+def afd_debug_bounds(ctx):
+    """(status, site, index, limit) of the first failed bounds check of the
+    debug build; AFD_ERR_UNSUPPORTED from the release build."""
+    site, idx, lim = C.c_int32(0), C.c_int64(-1), C.c_int64(-1)
+    rc = lib().afd_debug_bounds(ctx, C.byref(site), C.byref(idx), C.byref(lim))
+    return rc, site.value, idx.value, lim.value
+
+
+def afd_debug_plant(ctx, site):
+    return lib().afd_debug_plant(ctx, int(site))
 
 
 def afd_launch_count(ctx):

@@ -287,6 +287,7 @@ const char* afd_strerror(int code) {
     case AFD_ERR_CUDA: return "CUDA error";
     case AFD_ERR_UNSUPPORTED: return "unsupported configuration";
     case AFD_ERR_CANARY: return "guard word after a slot field overwritten";
+    case AFD_ERR_BOUNDS: return "index out of range (debug build bounds check)";
     default: return "unknown status";
   }
 }
@@ -410,7 +411,8 @@ int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out) {
       {AFD_LOOP_WORDS * 4},                  // work-item loop state and log
       {(int64_t)cfg->max_layers * (int64_t)sizeof(DevLayer)},  // per-layer weight table
       {4},                                   // go word (header check -> router)
-      {AFD_MAX_PEERS * 4}};                  // combine items finished per entry
+      {AFD_MAX_PEERS * 4},                   // combine items finished per entry
+      {8 * 8}};                              // debug build's bounds record
   const int nparts = sizeof(parts) / sizeof(parts[0]);
   int64_t offs[32], total = 0;
   for (int i = 0; i < nparts; i++) {
@@ -450,6 +452,7 @@ int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out) {
   c->ws.layers = c->dlayers;
   c->ws.go = reinterpret_cast<uint32_t*>(b + offs[25]);
   c->ws.ret_count = reinterpret_cast<int32_t*>(b + offs[26]);
+  c->ws.dbg = reinterpret_cast<int64_t*>(b + offs[27]);
   c->plan1 = reinterpret_cast<GemmPlan*>(b + offs[16]);
   c->plan2 = reinterpret_cast<GemmPlan*>(b + offs[17]);
   const int ws_map[12] = {4, 5, 6, 7, 8, 9, 11, 12, 13, 14, 15, 0};
@@ -1007,6 +1010,10 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
     if (rc) return rc;
   }
   mark(4);
+  // rows each GEMM output holds: the workspace's (routed, shared) capacity,
+  // or the return window's rows when the outputs go there in place
+  const int64_t Tcap = ctx->tmax;
+  const int64_t win_rows = ctx->L.window_bytes / row_bytes;
   if (N + T > 0) {
     if (c.gemm != AFD_GEMM_SIMT) {
       auto launch = c.gemm == AFD_GEMM_TENSOR ? launch_gemm_tc2 : launch_gemm_tc;
@@ -1037,6 +1044,9 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
       a1.M[1] = 2 * c.shared_inter;
       a1.plan = ctx->plan1;
       a1.status = ws.status;
+      a1.out_rows[0] = Tcap * c.topk;
+      a1.out_rows[1] = Tcap;
+      a1.dbg = ws.dbg;
       a1.swiglu = 1;
       a1.bn = bn;
       a1.timeout_ns = ctx->timeout();
@@ -1077,6 +1087,9 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
       a2.M[0] = a2.M[1] = c.hidden;
       a2.plan = ctx->plan2;
       a2.status = ws.status;
+      a2.out_rows[0] = in_place ? win_rows : Tcap * c.topk;
+      a2.out_rows[1] = in_place ? win_rows : Tcap;
+      a2.dbg = ws.dbg;
       a2.swiglu = 0;
       a2.bn = bn;
       a2.timeout_ns = ctx->timeout();
@@ -1108,6 +1121,9 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
       s1.swiglu = 1;
       s1.plan = ctx->plan1;
       s1.status = ws.status;
+      s1.out_rows[0] = Tcap * c.topk;
+      s1.out_rows[1] = Tcap;
+      s1.dbg = ws.dbg;
       rc = cuda_fail(launch_gemm_simt(lc, s1, c.num_experts + f.n_peers), "simt gemm1");
       if (rc) return rc;
       mark(5);
@@ -1266,6 +1282,38 @@ int afd_last_expert_counts(afd_ctx* ctx, int32_t* counts, int n, int* n_experts)
 }
 
 int64_t afd_launch_count(afd_ctx* ctx) { return ctx ? ctx->launches : -1; }
+
+int afd_debug_bounds(afd_ctx* ctx, int32_t* site, int64_t* index, int64_t* limit) {
+#ifdef AFD_DEBUG_BOUNDS
+  if (!ctx) return AFD_ERR_ARG;
+  int64_t rec[4];
+  if (cuda_fail(cudaStreamSynchronize(ctx->stream), "stream sync") ||
+      cuda_fail(cudaMemcpy(rec, ctx->ws.dbg, sizeof rec, cudaMemcpyDeviceToHost), "bounds record"))
+    return AFD_ERR_CUDA;
+  if (!rec[0]) return AFD_OK;
+  if (site) *site = (int32_t)rec[1];
+  if (index) *index = rec[2];
+  if (limit) *limit = rec[3];
+  return AFD_ERR_BOUNDS;
+#else
+  (void)ctx; (void)site; (void)index; (void)limit;
+  return AFD_ERR_UNSUPPORTED;
+#endif
+}
+
+int afd_debug_plant(afd_ctx* ctx, int32_t site) {
+#ifdef AFD_DEBUG_BOUNDS
+  if (!ctx || site < 0 || site >= AFD_DBG_NUM_SITES) return AFD_ERR_ARG;
+  const int64_t rec[5] = {0, 0, 0, 0, site};
+  if (cuda_fail(cudaStreamSynchronize(ctx->stream), "stream sync") ||
+      cuda_fail(cudaMemcpy(ctx->ws.dbg, rec, sizeof rec, cudaMemcpyHostToDevice), "bounds record"))
+    return AFD_ERR_CUDA;
+  return AFD_OK;
+#else
+  (void)ctx; (void)site;
+  return AFD_ERR_UNSUPPORTED;
+#endif
+}
 
 int afd_check_canaries(afd_ctx* ctx, int* window, int64_t* offset) {
   if (!ctx || !ctx->L.guard || !ctx->canary_result) return AFD_ERR_ARG;

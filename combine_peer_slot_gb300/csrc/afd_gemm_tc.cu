@@ -283,12 +283,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_gemm_tc(const __grid_constan
       const int kind = t.kind;
       const int64_t ldo = args.ldo[kind];
       const int64_t row0 = (int64_t)G.out_row0 + (int64_t)t.nt * plan.bn;
+      const bool rows_ok = dbg_in_range(args.dbg, args.status, AFD_DBG_GEMM_OUT, row0 + t.rows - 1,
+                                        args.out_rows[kind]);
       if (args.swiglu) {
         // lanes 0-15 hold gate rows i = base + lane, lanes 16-31 the up rows
         // of the same i; lane < 16 produces tokens 0-15 of the chunk, lane
         // >= 16 tokens 16-31, after one exchange of 16 values
         const int col0 = t.mt * 64 + q * 16;
-        const bool cols_ok = col0 + 16 <= args.M[kind] / 2;
+        const bool cols_ok = col0 + 16 <= args.M[kind] / 2 && rows_ok;
         for (int c0 = half * 32; c0 < t.rows; c0 += 64) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(taddr + (uint32_t)c0, v);
@@ -319,7 +321,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_gemm_tc(const __grid_constan
         }
       } else {
         const int col0 = t.mt * BM + q * 32;
-        const bool cols_ok = col0 + 32 <= args.M[kind];
+        const bool cols_ok = col0 + 32 <= args.M[kind] && rows_ok;
         const int fmt = args.out_fmt[kind];
         for (int c0 = half * 32; c0 < t.rows; c0 += 64) {
           uint32_t v[32];

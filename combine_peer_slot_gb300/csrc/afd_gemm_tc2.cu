@@ -414,9 +414,11 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
       const int64_t ldo = args.ldo[kind];
       const int64_t row0 = (int64_t)G.out_row0 + (int64_t)t.nt * plan.bn;
       const int mt = 2 * t.mpair + (int)rank;
+      const bool rows_ok = dbg_in_range(args.dbg, args.status, AFD_DBG_GEMM_OUT, row0 + t.rows - 1,
+                                        args.out_rows[kind]);
       if (args.swiglu) {
         const int col0 = mt * 64 + q * 16;
-        const bool cols_ok = col0 + 16 <= args.M[kind] / 2;
+        const bool cols_ok = col0 + 16 <= args.M[kind] / 2 && rows_ok;
         for (int c0 = half_cols * 32; c0 < t.rows; c0 += 64) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(taddr + (uint32_t)c0, v);
@@ -447,7 +449,7 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
         }
       } else {
         const int col0 = mt * BM + q * 32;
-        const bool cols_ok = col0 + 32 <= args.M[kind];
+        const bool cols_ok = col0 + 32 <= args.M[kind] && rows_ok;
         const int fmt = args.out_fmt[kind];
         for (int c0 = half_cols * 32; c0 < t.rows; c0 += 64) {
           uint32_t v[32];

@@ -136,7 +136,31 @@ struct DevWS {
   int32_t* loop;          // [AFD_LOOP_WORDS] work-item loop state and log
   uint32_t* go;           // [1] the header check's word for the router (AFD_GO_ABORT)
   int32_t* ret_count;     // [MAX_PEERS] combine items finished per entry (return flags)
+  int64_t* dbg;           // [8] debug build: failed checks, site, index, limit; [4] planted site
 };
+
+// Debug build (AFD_DEBUG_BOUNDS): index idx, derived from data an earlier
+// kernel wrote, must lie in [0, limit) before it is used.  A failure (or a
+// planted site, whose bound counts as 0) is recorded once, sets the step's
+// status, and returns false: the caller skips the access or uses index 0.
+// The release build compiles the check out.
+__device__ __forceinline__ bool dbg_in_range(int64_t* dbg, int32_t* status, int site, int64_t idx,
+                                             int64_t limit) {
+#ifdef AFD_DEBUG_BOUNDS
+  if (dbg[4] == site) limit = 0;
+  if (idx >= 0 && idx < limit) return true;
+  if (atomicAdd(reinterpret_cast<unsigned long long*>(dbg), 1ull) == 0ull) {
+    dbg[1] = site;
+    dbg[2] = idx;
+    dbg[3] = limit;
+  }
+  atomicCAS(status, 0, AFD_ERR_BOUNDS);
+  return false;
+#else
+  (void)dbg; (void)status; (void)site; (void)idx; (void)limit;
+  return true;
+#endif
+}
 
 // The header check of a host-described step publishes, once every listed
 // flag is acquired, the step's go token in ws.go (release); the router's
@@ -204,6 +228,8 @@ struct GemmArgs {
   const DevLayer* layers;
   const FanIn* item;
   int wsel;
+  int64_t out_rows[2];    // rows each output holds (checked in the debug build)
+  int64_t* dbg;           // the workspace's debug record (DevWS::dbg)
 };
 
 // SIMT GEMM arguments (fp32 activations, cross-check engine)
@@ -226,6 +252,8 @@ struct SimtArgs {
   const DevLayer* layers;
   const FanIn* item;
   int wsel;
+  int64_t out_rows[2];    // rows each output holds (checked in the debug build)
+  int64_t* dbg;           // the workspace's debug record (DevWS::dbg)
 };
 
 // ---------------------------------------------------------------------------

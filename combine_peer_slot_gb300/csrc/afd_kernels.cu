@@ -2166,7 +2166,8 @@ k_gather(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn fp, DevWS 
       const int i = entry_of(f, t);
       const uint4* src = reinterpret_cast<const uint4*>(slot_ptr(win, g, f.region[i], f.stage) + g.routed_x +
                                                         (int64_t)(t - f.prefix[i]) * row_bytes);
-      const int my_pos = lane < k ? ws.inv[(int64_t)t * k + lane] : 0;
+      int my_pos = lane < k ? ws.inv[(int64_t)t * k + lane] : 0;
+      if (lane < k && !dbg_in_range(ws.dbg, ws.status, AFD_DBG_GATHER_INV, my_pos, N)) my_pos = 0;
       for (int v0 = 0; v0 < nvec; v0 += 32 * 8) {
         uint4 buf[8];
 #pragma unroll
@@ -2204,14 +2205,17 @@ k_gather(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn fp, DevWS 
         const int mid = (lo + hi + 1) >> 1;
         if (gp[mid] <= local) lo = mid; else hi = mid - 1;
       }
-      const int pos = ws.gbase[i * E + lo] + (local - gp[lo]);
+      int pos = ws.gbase[i * E + lo] + (local - gp[lo]);
+      if (!dbg_in_range(ws.dbg, ws.status, AFD_DBG_GATHER_GROUPED, pos, N)) pos = 0;
       dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(ws.xp) + (int64_t)pos * row_bytes);
       if ((threadIdx.x & 31) == 0) {
         ws.perm[pos] = r;
         ws.inv[r] = pos;
       }
     } else if (r < N) {
-      const int t = ws.perm[r] / k;
+      int pr = ws.perm[r];
+      if (!dbg_in_range(ws.dbg, ws.status, AFD_DBG_GATHER_PERM, pr, N)) pr = 0;
+      const int t = pr / k;
       i = entry_of(f, t);
       local = t - f.prefix[i];
       field = g.routed_x;
@@ -2289,6 +2293,7 @@ __global__ void __launch_bounds__(kThreads) k_gemm_simt(SimtArgs a) {
       for (int q = 0; q < K; q++) s = fmaf(ld_act(A, ra + q, a.act_f32), ld_act(a.B[kind], brow + q, a.act_f32), s);
       v = s;
     }
+    if (!dbg_in_range(a.dbg, a.status, AFD_DBG_GEMM_OUT, (int64_t)G.out_row0 + r, a.out_rows[kind])) continue;
     const int64_t o = (int64_t)(G.out_row0 + r) * a.ldo[kind] + c;
     if (a.out_fmt[kind] == OUT_F32) {
       reinterpret_cast<float*>(a.out[kind])[o] = v;
@@ -2344,6 +2349,7 @@ k_combine(uint8_t* ret, WinGeom g, const __grid_constant__ FanIn fp, DevWS ws, i
     float my_w = 0.0f;
     if (lane < k) {
       my_pos = ws.inv[(int64_t)t * k + lane];
+      if (!dbg_in_range(ws.dbg, ws.status, AFD_DBG_COMBINE_INV, my_pos, (int64_t)f.total * k)) my_pos = 0;
       my_w = ws.w[(int64_t)t * k + lane];
       if (fb == 0)
         reinterpret_cast<int32_t*>(slot + g.route_table)[(int64_t)local * k + lane] =
@@ -2463,8 +2469,10 @@ k_scatter_grouped(uint8_t* ret, WinGeom g, const __grid_constant__ FanIn fp, Dev
   for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
     if (r < f.rtotal) {
       const int i = entry_of_rows(f, r);
+      int pos = ws.inv[r];
+      if (!dbg_in_range(ws.dbg, ws.status, AFD_DBG_SCATTER_INV, pos, f.rtotal)) pos = 0;
       const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(ws.y) +
-                                                        (int64_t)ws.inv[r] * row_bytes);
+                                                        (int64_t)pos * row_bytes);
       uint4* dst = reinterpret_cast<uint4*>(slot_ptr(ret, g, f.region[i], f.stage) + g.routed_x +
                                             (int64_t)(r - f.rprefix[i]) * row_bytes);
       for (int v = lane; v < row_bytes / 16; v += 32) dst[v] = src[v];

@@ -62,6 +62,7 @@ extern "C" {
 #define AFD_ERR_CUDA 12        /* a CUDA runtime/driver call failed */
 #define AFD_ERR_UNSUPPORTED 13 /* configuration outside what the kernels cover */
 #define AFD_ERR_CANARY 14      /* a guard word after a slot field was overwritten */
+#define AFD_ERR_BOUNDS 15      /* debug build: an index a kernel derived was out of range */
 
 #define AFD_DTYPE_F32 0
 #define AFD_DTYPE_BF16 1
@@ -515,6 +516,35 @@ int64_t afd_launch_count(afd_ctx* ctx);
  * that window of the first changed word; both may be NULL).  AFD_ERR_ARG for
  * a context without guards, AFD_ERR_CUDA if the check itself fails. */
 int afd_check_canaries(afd_ctx* ctx, int* window, int64_t* offset);
+
+/* Bounds checks of the debug build.  The library compiled with
+ * -DAFD_DEBUG_BOUNDS (combine_peer_slot_gb300/build.py, debug=True:
+ * libafd_gb300_dbg.so) checks, before each use, the indices its kernels take
+ * from arrays that earlier kernels of the step wrote: the partial positions
+ * the gather and the combine read through inv / perm (and the grouped form's
+ * row positions), and every output row range of the grouped GEMMs' units
+ * (AFD_DBG_* sites below).  A failed check skips the access (a position is
+ * replaced by 0), sets the step's status to AFD_ERR_BOUNDS and records the
+ * first failure: site, index and the bound it broke.  The release build
+ * compiles the checks out.  (Expert ids and the slot header's counts and
+ * shared indices are checked in both builds.)
+ * afd_debug_bounds synchronises the stream and returns AFD_OK when nothing
+ * failed since the context was created or last planted, else AFD_ERR_BOUNDS
+ * with *site, *index and *limit (each may be NULL).  afd_debug_plant clears
+ * the record and makes every later check at `site` fail (its bound is taken
+ * as 0, so the valid access is skipped; no index out of range is ever
+ * used), site 0 none: a test of the reporting path.  Both return
+ * AFD_ERR_UNSUPPORTED in the release build, AFD_ERR_ARG / AFD_ERR_CUDA on
+ * failure. */
+#define AFD_DBG_GATHER_INV 1     /* k_gather, token order: inv[t, j] < T * k */
+#define AFD_DBG_GATHER_PERM 2    /* k_gather, position order: perm[r] < T * k */
+#define AFD_DBG_GATHER_GROUPED 3 /* k_gather, grouped form: row position < routed rows */
+#define AFD_DBG_COMBINE_INV 4    /* k_combine: inv[t, j] < T * k */
+#define AFD_DBG_SCATTER_INV 5    /* k_scatter_grouped: inv[r] < routed rows */
+#define AFD_DBG_GEMM_OUT 6       /* grouped GEMMs: a unit's last output row < output rows */
+#define AFD_DBG_NUM_SITES 7
+int afd_debug_bounds(afd_ctx* ctx, int32_t* site, int64_t* index, int64_t* limit);
+int afd_debug_plant(afd_ctx* ctx, int32_t site);
 
 /* Stage timing.  With enable != 0, every afd_ffn_forward records a CUDA
  * event on the context's stream before and after each stage:

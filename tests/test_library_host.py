@@ -38,9 +38,16 @@ def test_exports_every_declared_function(lib):
 
 
 def test_strerror(lib):
-    for code in range(0, 15):
+    for code in range(0, 16):
         assert A.strerror(code) and A.strerror(code) != "unknown status"
     assert A.strerror(99) == "unknown status"
+
+
+def test_release_build_has_no_bounds_checks(lib):
+    # the checks are compiled out: the record calls answer UNSUPPORTED
+    # before they look at the context
+    assert A.afd_debug_bounds(None)[0] == A.AFD_ERR_UNSUPPORTED
+    assert A.afd_debug_plant(None, A.AFD_DBG_GEMM_OUT) == A.AFD_ERR_UNSUPPORTED
 
 
 def test_layout_matches_oracle(golden, lib):

@@ -169,6 +169,15 @@ def stage_work(w, T, nz=None):
     }
 
 
+def with_gemm_pair(work):
+    """Work of the one-launch GEMM pair (stage "gemm"): the SwiGLU and down
+    projections' FLOPs and bytes together."""
+    sw, dn = work.get("gemm_swiglu"), work.get("gemm_down")
+    if sw and dn:
+        work["gemm"] = {"flops": sw["flops"] + dn["flops"], "bytes": sw["bytes"] + dn["bytes"]}
+    return work
+
+
 def stage_work_grouped(w, T, Rr, nz=None):
     """Algorithmic work per stage of the grouped form: Rr routed rows arrive
     grouped (no router, no combine: the rows' outputs go back)."""
@@ -248,7 +257,9 @@ def run_ours(args, ws, rank, local):
     w = workload_of(args)
     T = w.total_tokens
     grouped = args.form == "grouped"
-    run = R.Runner(w, max_total_tokens=T)
+    run = R.Runner(w, max_total_tokens=T, flags=A.AFD_CFG_SPLIT_GEMMS if args.split_gemms else 0)
+    # the tensor engine runs both projections as one launch unless split
+    gemm_pair = not args.split_gemms
     if grouped:  # the Attention side routes: grouped rows, no router or combine here
         run.prepare_grouped(seed=w.seed)
     pack = run.pack_grouped_all if grouped else run.pack_all
@@ -322,9 +333,11 @@ def run_ours(args, ws, rank, local):
     else:
         flops, nbytes, t_roof, bound = path_roofline(w, T, int((cnt > 0).sum()), pk)
     stages = {n: stage_sum[i] / (args.steps * w.layers) for i, n in enumerate(A.STAGE_NAMES)}
+    if gemm_pair:  # one launch: its events bracket both projections
+        stages["gemm"] = stages.pop("gemm_swiglu") + stages.pop("gemm_down")
     dom = max(stages, key=stages.get)
     nz = int((cnt > 0).sum())
-    work = (stage_work_grouped(w, T, Rr, nz) if grouped else stage_work(w, T, nz)).get(dom, {})
+    work = with_gemm_pair(stage_work_grouped(w, T, Rr, nz) if grouped else stage_work(w, T, nz)).get(dom, {})
     # a GEMM below the ridge point (peak FLOP/s / peak bytes/s) streams its
     # weights from HBM (decode-sized fan-ins): measured against HBM then
     gemm_tensor = dom.startswith("gemm") and "flops" in work and (
@@ -753,6 +766,8 @@ def main():
     ap.add_argument("--workload", default="v2lite_prefill",
                     choices=["v2lite_prefill", "decode", "skewed", "fanin"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--split-gemms", action="store_true",
+                    help="launch the SwiGLU and down GEMMs as two kernels (AFD_CFG_SPLIT_GEMMS)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=60.0)

@@ -18,6 +18,7 @@ AFD_DTYPE_F32, AFD_DTYPE_BF16 = 0, 1
 AFD_GEMM_TENSOR, AFD_GEMM_SIMT, AFD_GEMM_TENSOR_1CTA = 0, 1, 2
 AFD_CFG_NO_PDL = 1
 AFD_CFG_CANARY = 2
+AFD_CFG_SPLIT_GEMMS = 4
 (AFD_DBG_GATHER_INV, AFD_DBG_GATHER_PERM, AFD_DBG_GATHER_GROUPED, AFD_DBG_COMBINE_INV,
  AFD_DBG_SCATTER_INV, AFD_DBG_GEMM_OUT) = range(1, 7)
 AFD_DBG_NUM_SITES = 7

@@ -146,7 +146,7 @@ int validate_config(const afd_config* c) {
       c->max_layers < 1 || c->routed_cap_multiplier < 1.0f || c->wait_timeout_ns < 0)
     return AFD_ERR_ARG;
   if (c->act_dtype != AFD_DTYPE_F32 && c->act_dtype != AFD_DTYPE_BF16) return AFD_ERR_ARG;
-  if (c->flags & ~(AFD_CFG_NO_PDL | AFD_CFG_CANARY)) return AFD_ERR_ARG;
+  if (c->flags & ~(AFD_CFG_NO_PDL | AFD_CFG_CANARY | AFD_CFG_SPLIT_GEMMS)) return AFD_ERR_ARG;
   if (c->ffn_size < 0 || c->ffn_size > AFD_MAX_FFN_RANKS || c->ffn_rank < 0 ||
       c->ffn_rank >= std::max(1, c->ffn_size))
     return AFD_ERR_ARG;
@@ -412,7 +412,8 @@ int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out) {
       {(int64_t)cfg->max_layers * (int64_t)sizeof(DevLayer)},  // per-layer weight table
       {4},                                   // go word (header check -> router)
       {AFD_MAX_PEERS * 4},                   // combine items finished per entry
-      {8 * 8}};                              // debug build's bounds record
+      {8 * 8},                               // debug build's bounds record
+      {(Tm * k + Tm + AFD_MAX_GROUPS + AFD_MAX_PEERS) * 4}};  // token tiles' SwiGLU counters
   const int nparts = sizeof(parts) / sizeof(parts[0]);
   int64_t offs[32], total = 0;
   for (int i = 0; i < nparts; i++) {
@@ -453,6 +454,7 @@ int afd_create(const afd_config* cfg, void* cuda_stream, afd_ctx** out) {
   c->ws.go = reinterpret_cast<uint32_t*>(b + offs[25]);
   c->ws.ret_count = reinterpret_cast<int32_t*>(b + offs[26]);
   c->ws.dbg = reinterpret_cast<int64_t*>(b + offs[27]);
+  c->ws.dep = reinterpret_cast<int32_t*>(b + offs[28]);
   c->plan1 = reinterpret_cast<GemmPlan*>(b + offs[16]);
   c->plan2 = reinterpret_cast<GemmPlan*>(b + offs[17]);
   const int ws_map[12] = {4, 5, 6, 7, 8, 9, 11, 12, 13, 14, 15, 0};
@@ -1050,9 +1052,6 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
       a1.swiglu = 1;
       a1.bn = bn;
       a1.timeout_ns = ctx->timeout();
-      rc = cuda_fail(launch(lc, a1), "gemm1");
-      if (rc) return rc;
-      mark(5);
       GemmArgs a2;
       memset(&a2, 0, sizeof a2);
       if (L) {
@@ -1093,8 +1092,18 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
       a2.swiglu = 0;
       a2.bn = bn;
       a2.timeout_ns = ctx->timeout();
-      rc = cuda_fail(launch(lc, a2), "gemm2");
-      if (rc) return rc;
+      if (c.gemm == AFD_GEMM_TENSOR && !(c.flags & AFD_CFG_SPLIT_GEMMS)) {
+        // one launch: down units start as soon as their token tile's h rows are stored
+        rc = cuda_fail(launch_gemm_tc2_pair(lc, a1, a2, ws.dep), "gemm");
+        if (rc) return rc;
+        mark(5);
+      } else {
+        rc = cuda_fail(launch(lc, a1), "gemm1");
+        if (rc) return rc;
+        mark(5);
+        rc = cuda_fail(launch(lc, a2), "gemm2");
+        if (rc) return rc;
+      }
     } else {
       SimtArgs s1;
       memset(&s1, 0, sizeof s1);

@@ -72,8 +72,8 @@ struct Ring {
   static constexpr size_t kEpiOffset = ((size_t)STAGES * STAGE_BYTES + sizeof(Tail) + 127) / 128 * 128;
   static constexpr size_t kSmemBytes = 1024 + kEpiOffset + (size_t)EPI_WARPS * EPI_BUF_BYTES;
   static_assert(kEpiOffset % 128 == 0 && EPI_BUF_BYTES % 128 == 0, "epilogue buffers must stay aligned");
-  // (plus the static table of the groups' first units)
-  static_assert(kSmemBytes + AFD_MAX_GROUPS * sizeof(int) <= 232448,
+  // (plus the static tables of both projections' first units)
+  static_assert(kSmemBytes + 2 * AFD_MAX_GROUPS * sizeof(int) <= 232448,
                 "over the per-CTA shared memory limit");
   static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
 };
@@ -221,9 +221,33 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
+// Wait (acquire, bounded by the kernel's deadline) until a token tile's
+// SwiGLU units have all stored their h rows; then order the async proxy (the
+// TMA loads that follow) after those generic-proxy stores.
+__device__ __forceinline__ bool wait_dep(const int32_t* cnt, int target, volatile int* abort_flag,
+                                         uint64_t deadline, int32_t* status) {
+  uint32_t spins = 0;
+  for (;;) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+    if (v >= target) break;
+    if ((++spins & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() > deadline) {
+        *abort_flag = 1;
+        set_error(status, AFD_ERR_TIMEOUT);
+        return false;
+      }
+    }
+    __nanosleep(32);
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
+}
+
 template <bool kNarrow>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
-k_gemm_tc2(const __grid_constant__ GemmArgs args) {
+k_gemm_tc2(const __grid_constant__ GemmPair pargs) {
   using R = Ring<kNarrow>;
   constexpr int STAGES = R::STAGES;
   constexpr int STAGE_BYTES = R::STAGE_BYTES;
@@ -234,7 +258,8 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
   const uint32_t rank = cluster_rank();
   const int cid = (int)cluster_id_x();
   const int ncl = (int)num_clusters_x();
-  const GemmPlan& plan = *args.plan;
+  const int nproj = pargs.nproj;
+  const GemmArgs& args = pargs.p[0];  // status, bn, timeout and layer selection are shared
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; s++) {
@@ -264,15 +289,22 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   grid_dep_wait();
   grid_dep_launch();
-  __shared__ int unit0_s[AFD_MAX_GROUPS];
-  const int ngroups = min(plan.ngroups, AFD_MAX_GROUPS);
-  for (int i = threadIdx.x; i < ngroups; i += blockDim.x) unit0_s[i] = plan.g[i].unit0;
+  // both projections' group tables: the units of p[0], then those of p[1]
+  __shared__ int unit0_s[2][AFD_MAX_GROUPS];
+  int ngroups[2] = {0, 0}, units[2] = {0, 0};
+  for (int ph = 0; ph < nproj; ph++) {
+    const GemmPlan& P = *pargs.p[ph].plan;
+    ngroups[ph] = min(P.ngroups, AFD_MAX_GROUPS);
+    units[ph] = P.total_units;
+    for (int i = threadIdx.x; i < ngroups[ph]; i += blockDim.x) unit0_s[ph][i] = P.g[i].unit0;
+  }
   if (threadIdx.x == 0) {
     int skip = read_status(args.status);
-    if (kNarrow && plan.bn > 2 * R::BN_HALF && !skip) {  // the ring has no room for wider tiles
-      set_error(args.status, AFD_ERR_ARG);
-      skip = 1;
-    }
+    for (int ph = 0; ph < nproj; ph++)
+      if (kNarrow && pargs.p[ph].plan->bn > 2 * R::BN_HALF && !skip) {  // no room for wider tiles
+        set_error(args.status, AFD_ERR_ARG);
+        skip = 1;
+      }
     tail->skip = skip;
   }
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // the peer has started
@@ -286,7 +318,7 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
   tc_fence_before();
   cluster_sync();  // both CTAs' barriers, skip decisions and TMEM columns are in place
   tc_fence_after();
-  const int total = plan.total_units;
+  const int total = units[0] + units[1];
   if (tail->skip || tail->peer_skip || total <= cid) {  // the same decision in both CTAs
     if (warp == 1) {
       __syncwarp();
@@ -296,13 +328,17 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
     return;
   }
 
-  // weight maps: the kernel's own, or the device table's entry for the layer
-  // the device chose for this step (host-written before any launch)
-  const CUtensorMap* tmA = args.tmA;
-  if (args.layers) {
-    const DevLayer& Ld = args.layers[args.item->layer];
-    tmA = args.wsel == 1 ? Ld.tmA1 : Ld.tmA2;
-  }
+  // weight maps per projection: the launch's own, or the device table's
+  // entry for the layer the device chose for this step (host-written before
+  // any launch)
+  const CUtensorMap* tmA_of[2] = {pargs.p[0].tmA, pargs.p[1].tmA};
+  for (int ph = 0; ph < nproj; ph++)
+    if (pargs.p[ph].layers) {
+      const DevLayer& Ld = pargs.p[ph].layers[pargs.p[ph].item->layer];
+      tmA_of[ph] = pargs.p[ph].wsel == 1 ? Ld.tmA1 : Ld.tmA2;
+    }
+  // unit -> (projection, its unit index)
+  auto split_unit = [&](int unit, int& ph) { ph = unit >= units[0]; return ph ? unit - units[0] : unit; };
   const uint32_t tmem_base = tail->tmem_base;
   const uint64_t deadline = globaltimer_ns() + kGemmTimeoutNs;
   volatile int* abort_flag = &tail->abort_flag;
@@ -312,13 +348,21 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
     if (lane == 0) {
       // ------------------------------ TMA producer (both CTAs)
       int s = 0;
-      uint32_t ph = 0;
+      uint32_t sph = 0;
       for (int r = 0;; r++) {
         const int unit = round_unit<kNarrow>(r, cid, ncl);
         if (unit >= total) break;
-        const Unit t = decode_unit<kNarrow>(plan, unit0_s, ngroups, unit);
+        int ph;
+        const int pu = split_unit(unit, ph);
+        const GemmArgs& A = pargs.p[ph];
+        const GemmPlan& plan = *A.plan;
+        const Unit t = decode_unit<kNarrow>(plan, unit0_s[ph], ngroups[ph], pu);
         const GemmGroup& G = plan.g[t.group];
-        const int nkb = (args.K[t.kind] + BK - 1) / BK;
+        const int nkb = (A.K[t.kind] + BK - 1) / BK;
+        // a down unit's token rows: the h rows its token tile's SwiGLU
+        // units store (every epilogue warp of each of those pairs counts)
+        const int32_t* dep = ph == 1 ? pargs.dep + G.nt0 + t.nt : nullptr;
+        const int dep_target = ph == 1 ? ((pargs.p[0].plan->g[t.group].m_tiles + 1) / 2) * 2 * EPI_WARPS : 0;
         // one token box per CTA and k-block: 128 rows, or 32 rows when the
         // unit's half fits (decode-sized groups); rows past the half are read
         // but not used by the MMA, past the buffer they are zero-filled
@@ -327,23 +371,32 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
         const bool small_box = kNarrow || half <= SMALL_BOX_ROWS;
         const uint32_t b_bytes = small_box ? SMALL_BOX_BYTES : R::B_BYTES;
         const int mt = 2 * t.mpair + (int)rank;
-        const CUtensorMap* ta = tmA + t.kind;
-        const CUtensorMap* tb = small_box ? &args.tmBs[t.kind] : &args.tmB[t.kind];
+        const CUtensorMap* ta = tmA_of[ph] + t.kind;
+        const CUtensorMap* tb = small_box ? &A.tmBs[t.kind] : &A.tmB[t.kind];
         bool ok = true;
+        bool dep_ok = dep == nullptr;
+        if (dep) {  // usually long done: check once before the weight loads
+          int v;
+          asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(dep) : "memory");
+          dep_ok = v >= dep_target;
+          if (dep_ok) asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
         for (int kb = 0; kb < nkb; kb += R::KPS) {
           const int cnt = min(R::KPS, nkb - kb);
-          if (!wait_bar(smem_u32(&tail->empty[s]), ph ^ 1, abort_flag, deadline, args.status)) { ok = false; break; }
+          if (!wait_bar(smem_u32(&tail->empty[s]), sph ^ 1, abort_flag, deadline, args.status)) { ok = false; break; }
           const uint32_t full_leader = map_to_rank(smem_u32(&tail->full[s]), 0);
           if (rank == 0) mbar_expect_tx(smem_u32(&tail->full[s]), 2 * cnt * (A_BYTES + b_bytes));
           const uint32_t sa = smem_base + s * STAGE_BYTES;
           const uint32_t sb = sa + R::KPS * A_BYTES;
-          for (int j = 0; j < cnt; j++) {
-            const int kc = (kb + j) * BK;
-            // weights: the tiled copy's 16 KB block (k-block, 128-row tile, expert)
-            tma2_load_5d(sa + j * A_BYTES, ta, 0, 0, kb + j, mt, G.a_idx, full_leader);
-            tma2_load_2d(sb + j * R::B_BYTES, tb, kc, brow, full_leader);
+          // weights: the tiled copy's 16 KB blocks (k-block, 128-row tile, expert);
+          // they need nothing from the SwiGLU units, so they go first
+          for (int j = 0; j < cnt; j++) tma2_load_5d(sa + j * A_BYTES, ta, 0, 0, kb + j, mt, G.a_idx, full_leader);
+          if (!dep_ok) {
+            if (!wait_dep(dep, dep_target, abort_flag, deadline, args.status)) { ok = false; break; }
+            dep_ok = true;
           }
-          if (++s == STAGES) { s = 0; ph ^= 1; }
+          for (int j = 0; j < cnt; j++) tma2_load_2d(sb + j * R::B_BYTES, tb, (kb + j) * BK, brow, full_leader);
+          if (++s == STAGES) { s = 0; sph ^= 1; }
         }
         if (!ok) break;
       }
@@ -359,8 +412,10 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
       for (int r = 0; ok; r++) {
         const int unit = round_unit<kNarrow>(r, cid, ncl);
         if (unit >= total) break;
-        const Unit t = decode_unit<kNarrow>(plan, unit0_s, ngroups, unit);
-        const int nkb = (args.K[t.kind] + BK - 1) / BK;
+        int uph;
+        const int pu = split_unit(unit, uph);
+        const Unit t = decode_unit<kNarrow>(*pargs.p[uph].plan, unit0_s[uph], ngroups[uph], pu);
+        const int nkb = (pargs.p[uph].K[t.kind] + BK - 1) / BK;
         const uint32_t idesc = idesc_pair(t.n_mma);
         if (!wait_bar(smem_u32(&tail->tempty[acc]), acc_ph ^ 1, abort_flag, deadline, args.status)) { ok = false; break; }
         tc_fence_after();
@@ -403,7 +458,11 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
     for (int r = 0;; r++) {
       const int unit = round_unit<kNarrow>(r, cid, ncl);
       if (unit >= total) break;
-      const Unit t = decode_unit<kNarrow>(plan, unit0_s, ngroups, unit);
+      int uph;
+      const int pu = split_unit(unit, uph);
+      const GemmArgs& A = pargs.p[uph];
+      const GemmPlan& plan = *A.plan;
+      const Unit t = decode_unit<kNarrow>(plan, unit0_s[uph], ngroups[uph], pu);
       const GemmGroup& G = plan.g[t.group];
       bool ok = wait_bar(smem_u32(&tail->tfull[acc]), acc_ph, abort_flag, deadline, args.status);
       ok = __all_sync(0xffffffffu, ok);
@@ -411,14 +470,14 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * 256);
       const int kind = t.kind;
-      const int64_t ldo = args.ldo[kind];
+      const int64_t ldo = A.ldo[kind];
       const int64_t row0 = (int64_t)G.out_row0 + (int64_t)t.nt * plan.bn;
       const int mt = 2 * t.mpair + (int)rank;
-      const bool rows_ok = dbg_in_range(args.dbg, args.status, AFD_DBG_GEMM_OUT, row0 + t.rows - 1,
-                                        args.out_rows[kind]);
-      if (args.swiglu) {
+      const bool rows_ok = dbg_in_range(A.dbg, args.status, AFD_DBG_GEMM_OUT, row0 + t.rows - 1,
+                                        A.out_rows[kind]);
+      if (A.swiglu) {
         const int col0 = mt * 64 + q * 16;
-        const bool cols_ok = col0 + 16 <= args.M[kind] / 2 && rows_ok;
+        const bool cols_ok = col0 + 16 <= A.M[kind] / 2 && rows_ok;
         for (int c0 = half_cols * 32; c0 < t.rows; c0 += 64) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(taddr + (uint32_t)c0, v);
@@ -440,7 +499,7 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
           if (r < t.rows && cols_ok) {
             const uint4* src =
                 reinterpret_cast<const uint4*>(ebuf + lane * EPI_PITCH_SWIGLU + (lo ? 0 : 32));
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(args.out[kind]) +
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(A.out[kind]) +
                                                   (row0 + r) * ldo + col0);
             dst[0] = src[0];
             dst[1] = src[1];
@@ -449,8 +508,8 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
         }
       } else {
         const int col0 = mt * BM + q * 32;
-        const bool cols_ok = col0 + 32 <= args.M[kind] && rows_ok;
-        const int fmt = args.out_fmt[kind];
+        const bool cols_ok = col0 + 32 <= A.M[kind] && rows_ok;
+        const int fmt = A.out_fmt[kind];
         for (int c0 = half_cols * 32; c0 < t.rows; c0 += 64) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(taddr + (uint32_t)c0, v);
@@ -458,7 +517,7 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
           const int r = c0 + lane;
           if (fmt == OUT_F32) {
             if (cols_ok) {
-              float* dst = reinterpret_cast<float*>(args.out[kind]) + (row0 + c0) * ldo + col0 + lane;
+              float* dst = reinterpret_cast<float*>(A.out[kind]) + (row0 + c0) * ldo + col0 + lane;
 #pragma unroll
               for (int c = 0; c < 32; c++)
                 if (c0 + c < t.rows) dst[(int64_t)c * ldo] = __uint_as_float(v[c]);
@@ -469,8 +528,8 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
             // shared memory into 16-byte stores measured 9 % slower over
             // the down GEMM: its epilogue competes with the operand traffic)
             if (cols_ok) {
-              uint16_t* dh = reinterpret_cast<uint16_t*>(args.out[kind]) + (row0 + c0) * ldo + col0 + lane;
-              uint8_t* dl = args.out_lo[kind] + (row0 + c0) * ldo + col0 + lane;
+              uint16_t* dh = reinterpret_cast<uint16_t*>(A.out[kind]) + (row0 + c0) * ldo + col0 + lane;
+              uint8_t* dl = A.out_lo[kind] + (row0 + c0) * ldo + col0 + lane;
 #pragma unroll
               for (int c = 0; c < 32; c++)
                 if (c0 + c < t.rows) {
@@ -489,7 +548,7 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
             __syncwarp();
             if (r < t.rows && cols_ok) {
               const uint4* src = reinterpret_cast<const uint4*>(ebuf + lane * EPI_PITCH_BF16);
-              uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(args.out[kind]) +
+              uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(A.out[kind]) +
                                                     (row0 + r) * ldo + col0);
 #pragma unroll
               for (int x = 0; x < 4; x++) dst[x] = src[x];
@@ -497,6 +556,11 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
           }
           __syncwarp();
         }
+      }
+      if (uph == 0 && pargs.dep) {  // this warp's h rows of the tile are stored (release)
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(pargs.dep + G.nt0 + t.nt, 1);
       }
       tc_fence_before();
       __syncwarp();
@@ -515,8 +579,27 @@ k_gemm_tc2(const __grid_constant__ GemmArgs args) {
   }
 }
 
+// Cluster slots the GPU holds at once for this kernel (cached): the pair
+// launch waits across clusters, so every cluster must be resident together.
 template <bool kNarrow>
-cudaError_t launch_variant(const LaunchCtx& lc, const GemmArgs& a) {
+int max_pairs(int num_sms) {
+  static int cached = 0;
+  if (cached) return cached;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((num_sms / 2) * 2));
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = Ring<kNarrow>::kSmemBytes;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tc2<kNarrow>, &cfg) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cached = n > 0 ? n : -1;
+  return cached;
+}
+
+template <bool kNarrow>
+cudaError_t launch_variant(const LaunchCtx& lc, const GemmPair& a) {
   constexpr size_t smem = Ring<kNarrow>::kSmemBytes;
   static bool attr_done = false;
   if (!attr_done) {
@@ -525,12 +608,41 @@ cudaError_t launch_variant(const LaunchCtx& lc, const GemmArgs& a) {
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  const int grid = (lc.num_sms / 2) * 2;  // whole pairs; persistent over the unit table
-  return launch_k(lc, k_gemm_tc2<kNarrow>, grid, NUM_THREADS, smem, a);
+  int pairs = lc.num_sms / 2;  // persistent over the unit table
+  if (a.nproj == 2) {
+    const int m = max_pairs<kNarrow>(lc.num_sms);
+    if (m < 1) {  // residency unknown: the two projections as two launches
+      GemmPair one;
+      memset(&one, 0, sizeof one);
+      one.nproj = 1;
+      for (int ph = 0; ph < 2; ph++) {
+        one.p[0] = a.p[ph];
+        const cudaError_t e = launch_k(lc, k_gemm_tc2<kNarrow>, 2 * pairs, NUM_THREADS, smem, one);
+        if (e != cudaSuccess) return e;
+      }
+      return cudaSuccess;
+    }
+    pairs = std::min(pairs, m);
+  }
+  return launch_k(lc, k_gemm_tc2<kNarrow>, 2 * pairs, NUM_THREADS, smem, a);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_tc2(const LaunchCtx& lc, const GemmArgs& a) {
-  return a.bn <= 2 * Ring<true>::BN_HALF ? launch_variant<true>(lc, a) : launch_variant<false>(lc, a);
+  GemmPair p;
+  memset(&p, 0, sizeof p);
+  p.p[0] = a;
+  p.nproj = 1;
+  return a.bn <= 2 * Ring<true>::BN_HALF ? launch_variant<true>(lc, p) : launch_variant<false>(lc, p);
+}
+
+cudaError_t launch_gemm_tc2_pair(const LaunchCtx& lc, const GemmArgs& a1, const GemmArgs& a2, int32_t* dep) {
+  GemmPair p;
+  memset(&p, 0, sizeof p);
+  p.p[0] = a1;
+  p.p[1] = a2;
+  p.dep = dep;
+  p.nproj = 2;
+  return a1.bn <= 2 * Ring<true>::BN_HALF ? launch_variant<true>(lc, p) : launch_variant<false>(lc, p);
 }

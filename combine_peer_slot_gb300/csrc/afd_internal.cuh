@@ -3,6 +3,8 @@
 #pragma once
 
 #include <cuda.h>
+#include <algorithm>
+#include <cstring>
 #include <utility>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -137,6 +139,7 @@ struct DevWS {
   uint32_t* go;           // [1] the header check's word for the router (AFD_GO_ABORT)
   int32_t* ret_count;     // [MAX_PEERS] combine items finished per entry (return flags)
   int64_t* dbg;           // [8] debug build: failed checks, site, index, limit; [4] planted site
+  int32_t* dep;           // [token tiles] SwiGLU epilogue warps done per token tile (one-launch GEMMs)
 };
 
 // Debug build (AFD_DEBUG_BOUNDS): index idx, derived from data an earlier
@@ -182,6 +185,7 @@ struct GemmGroup {
   int n_tiles;   // token tiles
   int tile0;     // first linear tile index of the group (one CTA per tile)
   int unit0;     // first pair-tile index (two CTAs, 256 weight rows per unit)
+  int nt0;       // first token-tile index over all groups (the same in both plans)
 };
 
 struct GemmPlan {
@@ -189,6 +193,7 @@ struct GemmPlan {
   int total_tiles;
   int bn;        // token tile
   int total_units;
+  int total_ntiles;
   GemmGroup g[AFD_MAX_GROUPS];
 };
 
@@ -230,6 +235,22 @@ struct GemmArgs {
   int wsel;
   int64_t out_rows[2];    // rows each output holds (checked in the debug build)
   int64_t* dbg;           // the workspace's debug record (DevWS::dbg)
+};
+
+// Both projections in one launch of the SM-pair engine: the units of p[0]
+// (SwiGLU), then those of p[1] (down), handed to the pairs in the same
+// rounds.  A down unit reads the h rows of one token tile of one group, which
+// every SwiGLU unit of that tile (one per 256-row weight pair) stores: each of
+// the pair's 16 epilogue warps adds 1 to dep[group's nt0 + tile] after its
+// stores (release), and the down unit's producers issue its weight loads,
+// then wait (acquire, bounded) for m_pairs x 16 before loading the h rows.
+// All SwiGLU units precede all down units in every pair's sequence and every
+// cluster of the grid is resident at once, so the waits always end.
+// nproj 1: p[0] alone, dep unused.
+struct GemmPair {
+  GemmArgs p[2];
+  int32_t* dep;
+  int nproj;
 };
 
 // SIMT GEMM arguments (fp32 activations, cross-check engine)
@@ -508,6 +529,9 @@ cudaError_t launch_gather(const LaunchCtx& lc, const WinGeom& g, const uint8_t* 
                           int has_shared, int sh_in_place, uint8_t* ret_headers, int E);
 cudaError_t launch_gemm_tc(const LaunchCtx& lc, const GemmArgs& a);
 cudaError_t launch_gemm_tc2(const LaunchCtx& lc, const GemmArgs& a);
+// SwiGLU (a1) and down (a2) projections in one launch (GemmPair); dep: the
+// workspace's per-token-tile counters, zeroed by the plan
+cudaError_t launch_gemm_tc2_pair(const LaunchCtx& lc, const GemmArgs& a1, const GemmArgs& a2, int32_t* dep);
 cudaError_t launch_gemm_simt(const LaunchCtx& lc, const SimtArgs& a, int max_groups);
 // flags: the combine releases each entry's return flag after its last item
 // (the gather wrote the headers); only where combine_releases_flags holds

@@ -1701,6 +1701,7 @@ __device__ void write_tile_tables(const FanIn& f, const DevWS& ws, const WinGeom
   const int mt1 = (inter + 63) / 64, mt2 = (hidden + 127) / 128;
   const int u1_per = (mt1 + 1) / 2, u2_per = (mt2 + 1) / 2;
   int tiles1 = 0, tiles2 = 0, units1 = 0, units2 = 0, ng = 0;
+  int ntiles = 0;  // token tiles of the groups so far (dependency counters of the one-launch GEMMs)
   // the shared expert: one group over the gathered shared rows (Xp rows
   // N..), or one group per entry that sent shared rows, read in place from
   // its slot's shared_x (window rows); outputs at the shared-row offsets
@@ -1710,13 +1711,14 @@ __device__ void write_tile_tables(const FanIn& f, const DevWS& ws, const WinGeom
     const int rows = f.stotal;
     const int nt = (rows + bn - 1) / bn;
     if (lane == 0) {
-      plan1->g[0] = GemmGroup{rows, N, 0, 0, 1, mts, nt, 0, 0};
-      plan2->g[0] = GemmGroup{rows, 0, 0, 0, 1, mt2, nt, 0, 0};
+      plan1->g[0] = GemmGroup{rows, N, 0, 0, 1, mts, nt, 0, 0, 0};
+      plan2->g[0] = GemmGroup{rows, 0, 0, 0, 1, mt2, nt, 0, 0, 0};
     }
     tiles1 = mts * nt;
     tiles2 = mt2 * nt;
     units1 = us_per * nt;
     units2 = u2_per * nt;
+    ntiles = nt;
     ng = 1;
   }
   if (has_shared && sh_in_place) {
@@ -1731,15 +1733,16 @@ __device__ void write_tile_tables(const FanIn& f, const DevWS& ws, const WinGeom
         const int gi = ng + __popc(has & lt_mask);
         const int wr = window_row(g, f.region[i], f.stage, g.shared_x, 0, row_bytes);
         plan1->g[gi] = GemmGroup{rows, wr, f.sprefix[i], 0, 1, mts, nt, tiles1 + mts * nt_before,
-                                 units1 + us_per * nt_before};
+                                 units1 + us_per * nt_before, ntiles + nt_before};
         plan2->g[gi] = GemmGroup{rows, f.sprefix[i], f.sprefix[i], 0, 1, mt2, nt,
-                                 tiles2 + mt2 * nt_before, units2 + u2_per * nt_before};
+                                 tiles2 + mt2 * nt_before, units2 + u2_per * nt_before, ntiles + nt_before};
       }
       const int nt_round = __shfl_sync(0xffffffffu, nt_incl, 31);
       tiles1 += mts * nt_round;
       tiles2 += mt2 * nt_round;
       units1 += us_per * nt_round;
       units2 += u2_per * nt_round;
+      ntiles += nt_round;
       ng += __popc(has);
     }
   }
@@ -1754,9 +1757,9 @@ __device__ void write_tile_tables(const FanIn& f, const DevWS& ws, const WinGeom
     const int rows = cnt[e];
     const int nt = (rows + bn - 1) / bn;
     plan1->g[ng + e] = GemmGroup{rows, offs[e], offs[e], e, 0, mt1, nt, tiles1 + mt1 * nt_run,
-                                 units1 + u1_per * nt_run};
+                                 units1 + u1_per * nt_run, ntiles + nt_run};
     plan2->g[ng + e] = GemmGroup{rows, offs[e], offs[e], e, 0, mt2, nt, tiles2 + mt2 * nt_run,
-                                 units2 + u2_per * nt_run};
+                                 units2 + u2_per * nt_run, ntiles + nt_run};
     nt_run += nt;
   }
   const int nt_all = __shfl_sync(0xffffffffu, nts_incl, 31);
@@ -1767,9 +1770,12 @@ __device__ void write_tile_tables(const FanIn& f, const DevWS& ws, const WinGeom
     plan2->total_tiles = tiles2 + mt2 * nt_all;
     plan1->total_units = units1 + u1_per * nt_all;
     plan2->total_units = units2 + u2_per * nt_all;
+    plan1->total_ntiles = plan2->total_ntiles = ntiles + nt_all;
     plan1->bn = bn;
     plan2->bn = bn;
   }
+  // the one-launch GEMMs count each token tile's finished SwiGLU units here
+  for (int i = lane; i < ntiles + nt_all; i += 32) ws.dep[i] = 0;
 }
 
 constexpr int kScanWarps = 32;
@@ -2028,7 +2034,7 @@ k_plan_grouped(const __grid_constant__ FanIn fp, DevWS ws, int E, int inter, int
   // return slot), then one shared group per entry with shared rows (read
   // from its shared_x, outputs into its return shared_x).  h / hs rows
   // follow the groups' order.
-  int tiles1 = 0, tiles2 = 0, units1 = 0, units2 = 0, ng = 0, hrow = 0;
+  int tiles1 = 0, tiles2 = 0, units1 = 0, units2 = 0, ng = 0, hrow = 0, ntiles = 0;
   const int mt1 = (inter + 63) / 64, mt2 = (hidden + 127) / 128;
   for (int i = 0; i < f.n_peers; i++)
     for (int e = 0, lr0 = 0; e < E; lr0 += gl_s[i * E + e], e++) {
@@ -2036,9 +2042,9 @@ k_plan_grouped(const __grid_constant__ FanIn fp, DevWS ws, int E, int inter, int
       if (!rows) continue;
       const int nt = (rows + bn - 1) / bn;
       GemmGroup a{rows, window_row(g, f.region[i], f.stage, g.routed_x, lr0, row_bytes), hrow, e, 0,
-                  mt1, nt, tiles1, units1};
+                  mt1, nt, tiles1, units1, ntiles};
       GemmGroup b{rows, hrow, window_row(g, f.region[i], f.stage, g.routed_x, lr0, row_bytes), e, 0,
-                  mt2, nt, tiles2, units2};
+                  mt2, nt, tiles2, units2, ntiles};
       plan1->g[ng] = a;
       plan2->g[ng] = b;
       tiles1 += mt1 * nt;
@@ -2046,6 +2052,7 @@ k_plan_grouped(const __grid_constant__ FanIn fp, DevWS ws, int E, int inter, int
       units1 += (mt1 + 1) / 2 * nt;
       units2 += (mt2 + 1) / 2 * nt;
       hrow += rows;
+      ntiles += nt;
       ng++;
     }
   if (has_shared)
@@ -2055,14 +2062,15 @@ k_plan_grouped(const __grid_constant__ FanIn fp, DevWS ws, int E, int inter, int
       const int nt = (rows + bn - 1) / bn;
       const int mts = (shared_inter + 63) / 64;
       const int wr = window_row(g, f.region[i], f.stage, g.shared_x, 0, row_bytes);
-      GemmGroup a{rows, wr, f.sprefix[i], 0, 1, mts, nt, tiles1, units1};
-      GemmGroup b{rows, f.sprefix[i], wr, 0, 1, mt2, nt, tiles2, units2};
+      GemmGroup a{rows, wr, f.sprefix[i], 0, 1, mts, nt, tiles1, units1, ntiles};
+      GemmGroup b{rows, f.sprefix[i], wr, 0, 1, mt2, nt, tiles2, units2, ntiles};
       plan1->g[ng] = a;
       plan2->g[ng] = b;
       tiles1 += mts * nt;
       tiles2 += mt2 * nt;
       units1 += (mts + 1) / 2 * nt;
       units2 += (mt2 + 1) / 2 * nt;
+      ntiles += nt;
       ng++;
     }
   plan1->ngroups = plan2->ngroups = ng;
@@ -2070,7 +2078,9 @@ k_plan_grouped(const __grid_constant__ FanIn fp, DevWS ws, int E, int inter, int
   plan2->total_tiles = tiles2;
   plan1->total_units = units1;
   plan2->total_units = units2;
+  plan1->total_ntiles = plan2->total_ntiles = ntiles;
   plan1->bn = plan2->bn = bn;
+  for (int i = 0; i < ntiles; i++) ws.dep[i] = 0;
 }
 
 // ---------------------------------------------------------------------------

@@ -121,6 +121,13 @@ extern "C" {
  * stays aligned; the offsets afd_slot_layout gives include the guards.  A
  * substitute for a memory checker, for tests. */
 #define AFD_CFG_CANARY 2
+/* With the SM-pair engine the SwiGLU and down projections run as one
+ * persistent launch: a pair that has no SwiGLU unit left starts down units
+ * whose token tile's h rows are all stored (per-tile counters in the
+ * workspace), so the down weights stream while the last SwiGLU units finish
+ * and no launch boundary separates the two.  This flag launches them as two
+ * kernels instead (the stage times then split them). */
+#define AFD_CFG_SPLIT_GEMMS 4
 typedef struct afd_config {
   int32_t num_peers;
   int32_t ring_depth;

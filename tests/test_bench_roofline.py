@@ -85,7 +85,7 @@ def test_stage_bytes_never_exceed_the_hbm_peak_at_recorded_times():
         with open(os.path.join(root, "profiles", fname)) as f:
             line = json.load(f)
         w = W.get(name)
-        work = bench.stage_work(w, w.total_tokens)
+        work = bench.with_gemm_pair(bench.stage_work(w, w.total_tokens))
         checked = 0
         for stage, ms in line["stages_ms"].items():
             nbytes = work.get(stage, {}).get("bytes")
@@ -93,4 +93,11 @@ def test_stage_bytes_never_exceed_the_hbm_peak_at_recorded_times():
                 gbs = nbytes / (ms * 1e-3) / 1e9
                 assert gbs <= PEAKS["hbm_gbs"] * 1.02, (name, stage, gbs)
                 checked += 1
-        assert checked >= 5, name
+        assert checked >= 4, name
+
+
+def test_gemm_pair_work_is_both_projections():
+    w = W.get("v2lite_prefill")
+    work = bench.with_gemm_pair(bench.stage_work(w, w.total_tokens))
+    for key in ("flops", "bytes"):
+        assert work["gemm"][key] == work["gemm_swiglu"][key] + work["gemm_down"][key]

@@ -88,6 +88,24 @@ def test_serialised_launches(workload):
     run.close()
 
 
+@pytest.mark.parametrize("workload", ["fanin", "v2lite_prefill", "decode"])
+def test_gemm_pair_equals_split_gemms(workload):
+    """The SwiGLU and down GEMMs as one launch (down units waiting on their
+    token tile's SwiGLU units) and as two launches: the same return window,
+    byte for byte (decode: the first layer)."""
+    w = W.get(workload)
+    wins = []
+    for flags in (0, A.AFD_CFG_SPLIT_GEMMS):
+        run = R.Runner(w, max_total_tokens=w.total_tokens, flags=flags, layers=1)
+        for _ in range(2):  # the counters start from zero again on the second step
+            run.pack_all(0)
+            assert run.forward(0) == 0
+            assert run.poll() == 0
+        wins.append(run.window(A.AFD_DIR_RETURN).cpu().numpy())
+        run.close()
+    assert np.array_equal(wins[0], wins[1])
+
+
 def test_fanin_reordered_with_empty_peer():
     w = W.custom("fanin", seq_lens=[37, 0, 91, 5])
     run = R.Runner(w, canary=True)

@@ -1003,11 +1003,11 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
   mark(3);
   // small host-described token-form steps: the gather writes the return
   // headers and the combine releases the flags (no return-header kernel)
-  const bool flags_in_combine = !grouped && combine_releases_flags(lc, f, c.hidden);
+  const bool flags_in_combine = !grouped && combine_releases_flags(lc, f, c.hidden, c.topk);
   if (!in_place) {
     rc = cuda_fail(launch_gather(lc, ctx->geom, ctx->win[0], f, ws, c.topk, row_bytes, c.hidden,
                                  has_shared, sh_in_place, flags_in_combine ? ctx->win[1] : nullptr,
-                                 c.num_experts),
+                                 c.num_experts, ws.base),
                    "gather");
     if (rc) return rc;
   }
@@ -1076,6 +1076,8 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
       // shared output stays fp32
       a2.out_fmt[0] = grouped ? OUT_ACT : OUT_Y24;
       a2.out_lo[0] = ws.y_lo;
+      // the shared output in fp32 (as 24-bit planes like y it measured 9 us
+      // slower over the V2-Lite prefill GEMMs: two stores per element)
       a2.out_fmt[1] = OUT_F32;
       if (in_place) {  // outputs straight into the return slots (rows = window rows)
         a2.out[0] = a2.out[1] = ctx->win[1];

@@ -282,8 +282,15 @@ struct SimtArgs {
 // ---------------------------------------------------------------------------
 #ifdef __CUDACC__
 
-// fp32 -> 24-bit y (see OUT_Y24): the value's bits rounded at bit 8
-__device__ __forceinline__ uint32_t y24_encode(float v) { return (__float_as_uint(v) + 0x80u) >> 8; }
+// fp32 -> 24-bit y (see OUT_Y24): the value's bits rounded at bit 8 (a
+// finite value of magnitude within half a unit of the largest rounds to
+// infinity, as a bf16 conversion would).  A NaN keeps its quiet bit instead:
+// rounding the all-ones payload the tensor cores produce would carry into
+// the sign bit and leave -0.
+__device__ __forceinline__ uint32_t y24_encode(float v) {
+  const uint32_t b = __float_as_uint(v);
+  return (b & 0x7fffffffu) > 0x7f800000u ? (b >> 8) | 0x4000u : (b + 0x80u) >> 8;
+}
 // the two planes back to fp32: high 16 bits, then the low byte, then zero
 __device__ __forceinline__ float y24_decode(uint32_t hi16, uint32_t lo8) {
   return __uint_as_float((hi16 << 16) | (lo8 << 8));
@@ -524,9 +531,12 @@ cudaError_t launch_plan(const LaunchCtx& lc, const FanIn& f, const DevWS& ws, in
                         const WinGeom& g, int row_bytes, int sh_in_place);
 // ret_headers (not NULL): also write the step's return headers (every word
 // but the flag) and zero the entries' item counters (see combine_releases_flags)
+// large token-form fan-ins: the stable ranks as well (k_rank_gather, from the
+// plan's bases); ret_headers is then unused (the return-header kernel runs)
 cudaError_t launch_gather(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                           const FanIn& f, const DevWS& ws, int k, int row_bytes, int hidden,
-                          int has_shared, int sh_in_place, uint8_t* ret_headers, int E);
+                          int has_shared, int sh_in_place, uint8_t* ret_headers, int E,
+                          const int32_t* base);
 cudaError_t launch_gemm_tc(const LaunchCtx& lc, const GemmArgs& a);
 cudaError_t launch_gemm_tc2(const LaunchCtx& lc, const GemmArgs& a);
 // SwiGLU (a1) and down (a2) projections in one launch (GemmPair); dep: the
@@ -538,7 +548,7 @@ cudaError_t launch_gemm_simt(const LaunchCtx& lc, const SimtArgs& a, int max_gro
 cudaError_t launch_combine(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret,
                            const FanIn& f, const DevWS& ws, int hidden, int k, int act_f32,
                            int has_shared, int flags);
-bool combine_releases_flags(const LaunchCtx& lc, const FanIn& f, int hidden);
+bool combine_releases_flags(const LaunchCtx& lc, const FanIn& f, int hidden, int k);
 cudaError_t launch_return_header(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret,
                                  const uint8_t* win, const FanIn& f, const DevWS& ws, int E,
                                  int k);

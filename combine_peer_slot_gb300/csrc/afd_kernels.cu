@@ -2083,62 +2083,43 @@ k_plan_grouped(const __grid_constant__ FanIn fp, DevWS ws, int E, int inter, int
   for (int i = 0; i < ntiles; i++) ws.dep[i] = 0;
 }
 
-// ---------------------------------------------------------------------------
-// a3 plan, part 2: the stable permutation.  One warp per router CTA's range
-// of partials f (16 tokens x k, contiguous in f): rank among earlier
-// partials of the same expert in the range (match_any per 32-element round
-// plus running per-expert counts), position = offsets[e] + base[b][e] +
-// rank.  Equal to argsort(stable=True) of the flattened ids.  Also the
-// per-peer expert counts of the return headers.
-// ---------------------------------------------------------------------------
-constexpr int kRankWarps = 8;
 
-template <bool kDev>
-__global__ void __launch_bounds__(kRankWarps * 32)
-k_rank(const __grid_constant__ FanIn fp, DevWS ws, int E, int k, const int32_t* __restrict__ base) {
-  grid_dep_wait();
-  grid_dep_launch();
-  const FanIn& f = step_item<kDev>(fp, ws.item);
-  __shared__ int run_s[kRankWarps][256];
-  if (read_status(ws.status)) return;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.x * kRankWarps + warp;
-  if (b >= (f.total + kRtTok - 1) / kRtTok) return;  // past this step's router CTAs
-  // run[e]: next position for expert e in this block = offsets[e] + base[b][e]
-  int* run = run_s[warp];
-  for (int e = lane; e < E; e += 32) run[e] = ws.offsets[e] + base[(int64_t)b * E + e];
-  __syncwarp();
-  const int N = f.total * k;
-  const int f0 = b * kRtTok * k, f1 = min(N, f0 + kRtTok * k);
-  const unsigned lt_mask = (1u << lane) - 1u;
-  for (int g0 = f0; g0 < f1; g0 += 32) {
-    const int fi = g0 + lane;
-    const bool ok = fi < f1;
-    int e = ok ? ws.ids[fi] : -1 - lane;
-    if (ok && (e < 0 || e >= E)) {  // cannot come from the router; keep every index in range
-      set_error(ws.status, AFD_ERR_SHAPE);
-      e = 0;
+// ---------------------------------------------------------------------------
+// Shared row r - N of the step (entries in list order), one warp: copied from
+// its slot's shared_x into Xp row r, or zeros for an entry that sent no
+// shared rows; when the shared expert reads its rows in place, only the s
+// rows of such entries are zeroed here (the combine adds s for every token).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void gather_shared_row(const uint8_t* win, const WinGeom& g, const FanIn& f,
+                                                  const DevWS& ws, int r, int N, int row_bytes, int hidden,
+                                                  int sh_in_place) {
+  const int lane = threadIdx.x & 31;
+  const int t = r - N;
+  const int i = entry_of_shared(f, t);
+  if (sh_in_place) {
+    if (!ws.peer_shared[i]) {
+      float4* srow = reinterpret_cast<float4*>(ws.s + (int64_t)t * hidden);
+      for (int v = lane; v < hidden / 4; v += 32) srow[v] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    const unsigned same = __match_any_sync(0xffffffffu, e);
-    const int rank = __popc(same & lt_mask);
-    int pos = 0;
-    if (ok) pos = run[e] + rank;
-    __syncwarp();
-    if (ok && rank == 0) run[e] += __popc(same);
-    __syncwarp();
-    if (ok) {
-      ws.perm[pos] = fi;
-      ws.inv[fi] = pos;
-      atomicAdd(&ws.peer_counts[entry_of(f, fi / k) * E + e], 1);
-    }
+    return;
   }
+  const int nvec = row_bytes / 16;
+  uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(ws.xp) + (int64_t)r * row_bytes);
+  if (!ws.peer_shared[i]) {
+    for (int v = lane; v < nvec; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(slot_ptr(win, g, f.region[i], f.stage) + g.shared_x +
+                                                    (int64_t)(t - f.sprefix[i]) * row_bytes);
+  for (int v = lane; v < nvec; v += 32) dst[v] = __ldg(src + v);
 }
 
 // ---------------------------------------------------------------------------
 // a3 gather: Xp[pos] = the row of token perm[pos] / k, read straight from its
 // peer slot (the fan-in concatenation is never materialised), then the
-// shared rows in concatenation order -- unless the shared expert reads them
-// in place from the slots' shared_x.  One warp per row, 16-byte vectors.
+// shared rows in concatenation order.  One warp per row, 16-byte vectors:
+// small token-form fan-ins (their rows stay in L2; a warp per position
+// spreads the copies over many warps) and the grouped form.
 // ---------------------------------------------------------------------------
 template <bool kDev>
 __global__ void __launch_bounds__(kThreads)
@@ -2155,59 +2136,22 @@ k_gather(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn fp, DevWS 
     }
   }
   const int N = f.grouped ? f.rtotal : f.total * k;
-  // then the shared rows; when the shared expert reads them in place, only
-  // the rows of s of peers that sent none are zeroed here (the combine adds
-  // s for every token)
   const int rows = N + (has_shared ? f.stotal : 0);
   const int nvec = row_bytes / 16;
   const int warps = gridDim.x * (blockDim.x >> 5);
   const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  // token form, large fan-ins: the routed copies in token order, each
-  // token's row read once from its slot and written to its k positions
-  // (walking the positions instead read each row k times, far apart, and L2
-  // kept few of them: 3.2x the rows' bytes came from DRAM at the V2-Lite
-  // prefill shape, 0.081 -> 0.061 ms).  Small fan-ins keep position order:
-  // their rows stay in L2, and a warp per position spreads the copies over
-  // more warps (token order measured 2.4 us per decode layer slower).
-  const bool token_order = !f.grouped && N > kPlanSmallMax;
-  if (token_order) {
-    const int lane = threadIdx.x & 31;
-    for (int t = wid; t < f.total; t += warps) {
-      const int i = entry_of(f, t);
-      const uint4* src = reinterpret_cast<const uint4*>(slot_ptr(win, g, f.region[i], f.stage) + g.routed_x +
-                                                        (int64_t)(t - f.prefix[i]) * row_bytes);
-      int my_pos = lane < k ? ws.inv[(int64_t)t * k + lane] : 0;
-      if (lane < k && !dbg_in_range(ws.dbg, ws.status, AFD_DBG_GATHER_INV, my_pos, N)) my_pos = 0;
-      for (int v0 = 0; v0 < nvec; v0 += 32 * 8) {
-        uint4 buf[8];
-#pragma unroll
-        for (int u = 0; u < 8; u++) {
-          const int v = v0 + 32 * u + lane;
-          buf[u] = v < nvec ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
-        }
-        for (int j = 0; j < k; j++) {
-          const int pos = __shfl_sync(0xffffffffu, my_pos, j);
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(ws.xp) + (int64_t)pos * row_bytes);
-#pragma unroll
-          for (int u = 0; u < 8; u++) {
-            const int v = v0 + 32 * u + lane;
-            if (v < nvec) dst[v] = buf[u];
-          }
-        }
-      }
+  for (int r = wid; r < rows; r += warps) {
+    if (r >= N) {
+      gather_shared_row(win, g, f, ws, r, N, row_bytes, hidden, sh_in_place);
+      continue;
     }
-  }
-  // rows by position (grouped, or small token-form fan-ins); then the shared rows
-  for (int r = (token_order ? N : 0) + wid; r < rows; r += warps) {
     uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(ws.xp) + (int64_t)r * row_bytes);
     int i, local;
-    int64_t field;
-    if (r < N && f.grouped) {
+    if (f.grouped) {
       // source row r of the entries' concatenation goes to position
       // base[i][e] + (its row within the entry's expert-e group)
       i = entry_of_rows(f, r);
       local = r - f.rprefix[i];
-      field = g.routed_x;
       const int E = f.num_experts;
       const int* gp = ws.gbase + AFD_MAX_PEERS * E + i * E;
       int lo = 0, hi = E - 1;  // the last expert whose first row is <= local (not empty)
@@ -2222,35 +2166,129 @@ k_gather(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn fp, DevWS 
         ws.perm[pos] = r;
         ws.inv[r] = pos;
       }
-    } else if (r < N) {
+    } else {
       int pr = ws.perm[r];
       if (!dbg_in_range(ws.dbg, ws.status, AFD_DBG_GATHER_PERM, pr, N)) pr = 0;
       const int t = pr / k;
       i = entry_of(f, t);
       local = t - f.prefix[i];
-      field = g.routed_x;
-    } else {  // shared rows, entry after entry
-      const int t = r - N;
-      i = entry_of_shared(f, t);
-      local = t - f.sprefix[i];
-      field = g.shared_x;
-      if (sh_in_place) {
-        if (!ws.peer_shared[i]) {
-          float4* srow = reinterpret_cast<float4*>(ws.s + (int64_t)t * hidden);
-          for (int v = threadIdx.x & 31; v < hidden / 4; v += 32)
-            srow[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        continue;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(slot_ptr(win, g, f.region[i], f.stage) + g.routed_x +
+                                                      (int64_t)local * row_bytes);
+    for (int v = (threadIdx.x & 31); v < nvec; v += 32) dst[v] = __ldg(src + v);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// a2 + a3 for large token-form fan-ins: the stable permutation and the
+// gather in one launch, one CTA per 16-token router block.  While every warp
+// loads its two tokens' rows from their slots, the first warp ranks the
+// block's partials: position = offsets[e] + base[b][e] (the plan's exclusive
+// bases from the router's block histograms) + the rank among the block's
+// earlier partials of e (match_any over 32-partial rounds), i.e. a stable
+// argsort of the flattened ids; it records perm / inv and the per-peer
+// counts.  After one barrier each row goes to its k positions, so every
+// token row leaves HBM once (walking the positions instead read each row k
+// times, far apart, and L2 kept few of them: 3.2x the rows' bytes came from
+// DRAM at the V2-Lite prefill shape).  Then the shared rows, as k_gather.
+// ---------------------------------------------------------------------------
+constexpr int kRgWarps = kRtTok / 2;  // two tokens per warp
+
+template <bool kDev>
+__global__ void __launch_bounds__(kRgWarps * 32)
+k_rank_gather(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn fp, DevWS ws, int E, int k,
+              const int32_t* __restrict__ base, int row_bytes, int hidden, int has_shared, int sh_in_place) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const FanIn& f = step_item<kDev>(fp, ws.item);
+  __shared__ int run_s[256];
+  __shared__ int pos_s[kRtTok * 16];  // [token of the block][j], k <= 16
+  __shared__ int skip_s;
+  if (threadIdx.x == 0) skip_s = read_status(ws.status);
+  __syncthreads();  // one decision for the CTA: its loop has barriers
+  if (skip_s) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = f.total, N = T * k;
+  const int nblocks = (T + kRtTok - 1) / kRtTok;
+  const int nvec = row_bytes / 16;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int b = blockIdx.x; b < nblocks; b += gridDim.x) {
+    // this warp's two tokens: the first 8 vectors per lane of each row in flight
+    const uint4* src[2];
+    uint4 buf[2][8];
+#pragma unroll
+    for (int q = 0; q < 2; q++) {
+      const int t = b * kRtTok + 2 * warp + q;
+      src[q] = nullptr;
+      if (t < T) {
+        const int i = entry_of(f, t);
+        src[q] = reinterpret_cast<const uint4*>(slot_ptr(win, g, f.region[i], f.stage) + g.routed_x +
+                                                (int64_t)(t - f.prefix[i]) * row_bytes);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; u++) {
+        const int v = 32 * u + lane;
+        buf[q][u] = (src[q] && v < nvec) ? __ldg(src[q] + v) : make_uint4(0, 0, 0, 0);
       }
     }
-    const int lane = threadIdx.x & 31;
-    if (r >= N && !ws.peer_shared[i]) {
-      for (int v = lane; v < nvec; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
-      continue;
+    if (warp == 0) {
+      for (int e = lane; e < E; e += 32) run_s[e] = ws.offsets[e] + base[(int64_t)b * E + e];
+      __syncwarp();
+      const int f0 = b * kRtTok * k, f1 = min(N, f0 + kRtTok * k);
+      for (int g0 = f0; g0 < f1; g0 += 32) {
+        const int fi = g0 + lane;
+        const bool ok = fi < f1;
+        int e = ok ? ws.ids[fi] : -1 - lane;
+        if (ok && (e < 0 || e >= E)) {  // cannot come from the router; keep every index in range
+          set_error(ws.status, AFD_ERR_SHAPE);
+          e = 0;
+        }
+        const unsigned same = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(same & lt_mask);
+        int pos = 0;
+        if (ok) pos = run_s[e] + rank;
+        __syncwarp();
+        if (ok && rank == 0) run_s[e] += __popc(same);
+        __syncwarp();
+        if (ok) {
+          pos_s[fi - f0] = pos;
+          ws.perm[pos] = fi;
+          ws.inv[fi] = pos;
+          atomicAdd(&ws.peer_counts[entry_of(f, fi / k) * E + e], 1);
+        }
+      }
     }
-    const uint4* src = reinterpret_cast<const uint4*>(slot_ptr(win, g, f.region[i], f.stage) + field +
-                                                      (int64_t)local * row_bytes);
-    for (int v = lane; v < nvec; v += 32) dst[v] = __ldg(src + v);
+    __syncthreads();  // the block's positions
+#pragma unroll
+    for (int q = 0; q < 2; q++) {
+      if (!src[q]) continue;
+      const int tb = 2 * warp + q;
+      for (int v0 = 0; v0 < nvec; v0 += 32 * 8) {
+        if (v0 > 0) {  // rows past 256 vectors: the next pass
+#pragma unroll
+          for (int u = 0; u < 8; u++) {
+            const int v = v0 + 32 * u + lane;
+            buf[q][u] = v < nvec ? __ldg(src[q] + v) : make_uint4(0, 0, 0, 0);
+          }
+        }
+        for (int j = 0; j < k; j++) {
+          int pos = pos_s[tb * k + j];
+          if (!dbg_in_range(ws.dbg, ws.status, AFD_DBG_GATHER_INV, pos, N)) pos = 0;
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(ws.xp) + (int64_t)pos * row_bytes);
+#pragma unroll
+          for (int u = 0; u < 8; u++) {
+            const int v = v0 + 32 * u + lane;
+            if (v < nvec) dst[v] = buf[q][u];
+          }
+        }
+      }
+    }
+    __syncthreads();  // run_s and pos_s are free for the next block
+  }
+  if (has_shared) {
+    const int warps = gridDim.x * kRgWarps, wid = blockIdx.x * kRgWarps + warp;
+    for (int r = N + wid; r < N + f.stotal; r += warps)
+      gather_shared_row(win, g, f, ws, r, N, row_bytes, hidden, sh_in_place);
   }
 }
 
@@ -2970,17 +3008,15 @@ static cudaError_t launch_plan_t(const LaunchCtx& lc, const FanIn& f, const DevW
                                  int k, int inter, int shared_inter, int hidden, int has_shared,
                                  int bn, GemmPlan* plan1, GemmPlan* plan2, const int32_t* hist,
                                  int32_t* base, const WinGeom& g, int row_bytes, int sh_in_place) {
-  const int nblocks = router_blocks(f.total);
   if ((int64_t)f.total * k <= kPlanSmallMax) {
     return launch_k(lc, k_plan_small<kDev>, 1, 1024, 0, f, ws, E, k, inter, shared_inter, hidden,
                     has_shared, bn, plan1, plan2, g, row_bytes, sh_in_place);
   }
-  cudaError_t err = launch_k(lc, k_plan_scan<kDev>, 1, kScanWarps * 32, 0, f, ws, E, k, inter,
-                             shared_inter, hidden, has_shared, bn, hist, base, plan1, plan2, g,
-                             row_bytes, sh_in_place);
-  if (err != cudaSuccess || nblocks == 0) return err;
-  return launch_k(lc, k_rank<kDev>, (nblocks + kRankWarps - 1) / kRankWarps, kRankWarps * 32, 0, f,
-                  ws, E, k, (const int32_t*)base);
+  // larger fan-ins: counts, offsets, bases and tables here; the ranks with
+  // the gather (k_rank_gather)
+  (void)hist;
+  return launch_k(lc, k_plan_scan<kDev>, 1, kScanWarps * 32, 0, f, ws, E, k, inter, shared_inter,
+                  hidden, has_shared, bn, hist, base, plan1, plan2, g, row_bytes, sh_in_place);
 }
 
 cudaError_t launch_plan(const LaunchCtx& lc, const FanIn& f, const DevWS& ws, int E, int k,
@@ -2995,9 +3031,16 @@ cudaError_t launch_plan(const LaunchCtx& lc, const FanIn& f, const DevWS& ws, in
 
 cudaError_t launch_gather(const LaunchCtx& lc, const WinGeom& g, const uint8_t* win,
                           const FanIn& f, const DevWS& ws, int k, int row_bytes, int hidden,
-                          int has_shared, int sh_in_place, uint8_t* ret_headers, int E) {
+                          int has_shared, int sh_in_place, uint8_t* ret_headers, int E,
+                          const int32_t* base) {
   const int64_t rows = (int64_t)f.total * k + (has_shared ? f.total : 0);
   if (rows == 0) return cudaSuccess;
+  if (!f.grouped && (int64_t)f.total * k > kPlanSmallMax) {  // the ranks too (the plan left them)
+    const int nblocks = router_blocks(f.total);
+    return launch_k(lc, f.dev ? k_rank_gather<true> : k_rank_gather<false>,
+                    std::max(1, std::min(nblocks, lc.num_sms * 8)), kRgWarps * 32, 0, win, g, f, ws, E, k,
+                    base, row_bytes, hidden, has_shared, sh_in_place);
+  }
   return launch_k(lc, f.dev ? k_gather<true> : k_gather<false>,
                   grid_for(rows, kThreads / 32, lc.num_sms * 8), kThreads, 0, win, g, f, ws, k,
                   row_bytes, hidden, has_shared, sh_in_place, ret_headers, E);
@@ -3031,8 +3074,12 @@ cudaError_t launch_combine(const LaunchCtx& lc, const WinGeom& g, uint8_t* ret, 
 // most one item (so counting items is cheap) and every entry has tokens
 // (an entry without any would get no item): host-described token-form steps
 // of small fan-ins.
-bool combine_releases_flags(const LaunchCtx& lc, const FanIn& f, int hidden) {
+bool combine_releases_flags(const LaunchCtx& lc, const FanIn& f, int hidden, int k) {
   if (f.dev || f.grouped || f.total == 0) return false;
+  // larger fan-ins rank in the gather (k_rank_gather), so the per-peer
+  // counts the return headers carry are final only after it: the
+  // return-header kernel writes them
+  if ((int64_t)f.total * k > kPlanSmallMax) return false;
   for (int i = 0; i < f.n_peers; i++)
     if (f.prefix[i + 1] == f.prefix[i]) return false;
   const int64_t items = (int64_t)f.total * ((hidden + 255) / 256);

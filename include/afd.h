@@ -204,7 +204,10 @@ typedef struct afd_layout {
 #define AFD_WS_INV 5        /* int32 [T*topk] flattened index -> position */
 #define AFD_WS_XP 6         /* act [T*topk, hidden] permuted routed rows (shared rows stay in the slots) */
 #define AFD_WS_H 7          /* act [T*topk, inter] routed SwiGLU output */
-#define AFD_WS_Y 8          /* fp32 [T*topk, hidden] routed down projection (grouped form: act) */
+#define AFD_WS_Y 8          /* routed down projection [T*topk, hidden]: token form with bf16
+                               activations 24-bit (u16 high plane, then the u8 low plane; value =
+                               bits (hi << 16 | lo << 8) as fp32), fp32 activations fp32;
+                               grouped form: act */
 #define AFD_WS_HS 9         /* act [T, shared_inter] shared SwiGLU output */
 #define AFD_WS_S 10         /* fp32 [T, hidden] shared expert output */
 #define AFD_WS_STATUS 11    /* int32 device status word */

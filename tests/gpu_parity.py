@@ -126,7 +126,8 @@ def run_and_compare_full(run, slots=None, layer=0, pack=True):
     rc = run.forward(layer, slots=slots)
     assert rc == 0, A.strerror(rc)
     outs = run.unpack_all(peers=slots)
-    assert run.poll() == 0
+    st = run.poll()
+    assert st == 0, (A.strerror(st), A.afd_debug_bounds(run.ctx))
     check_canaries(run)
     # the oracle reads and writes windows without guard words
     win = plain_window(run, run.window(A.AFD_DIR_DISPATCH).cpu().numpy())

@@ -128,6 +128,17 @@ def test_single_peer_ragged_tiles():
     G.run_and_compare_full(run)
 
 
+def test_large_fanin_small_rows():
+    """T * k = 9200 partials (ranked inside the gather) while the combine has
+    few enough items to release the flags itself: the return headers must
+    still be written (by the return-header kernel)."""
+    w = W.custom("fanin", seq_lens=[1200, 1100])
+    run = R.Runner(w, max_total_tokens=w.total_tokens, canary=True)
+    e, _ = G.run_and_compare_full(run)
+    print("fanin 2300 tokens max|err|/rms", e)
+    run.close()
+
+
 def test_v2lite_prefill_full_size():
     """Every output row of the 13312-token fan-in against the oracle (which
     runs the same fan-in on all host cores), with routing, plan, headers and

@@ -361,53 +361,97 @@ def run_ours(args, ws, rank, local):
     e2e = None
     if not args.no_e2e:
         dt = torch.bfloat16 if w.act == "bf16" else torch.float32
-        hx = [x.cpu().pin_memory() for x in run.x]
-        hout = [torch.empty((max(n, 1), w.hidden), dtype=dt).pin_memory() for n in w.seq_lens]
-        h2d = sum(x.numel() * x.element_size() for x in hx)
-        d2h = sum(n * w.hidden * w.act_bytes for n in w.seq_lens)
+        # the peers' token rows and outputs in one buffer each (views per
+        # peer), so a forward's inputs go up in one copy and its outputs
+        # come back in one
+        offs = [0]
+        for n in w.seq_lens:
+            offs.append(offs[-1] + n)
+        xall = torch.cat([x[:n] for x, n in zip(run.x, w.seq_lens)]).contiguous()
+        outall = torch.empty((max(T, 1), w.hidden), dtype=dt, device="cuda")
+        run.x = [xall[offs[p]:offs[p + 1]] for p in range(w.num_peers)]
+        run.out = [outall[offs[p]:offs[p + 1]] for p in range(w.num_peers)]
+        hxall = xall.cpu().pin_memory()
+        houtall = torch.empty((max(T, 1), w.hidden), dtype=dt).pin_memory()
+        h2d = T * w.hidden * w.act_bytes
+        d2h = T * w.hidden * w.act_bytes
         if grouped:  # also the routed rows in and their expert outputs back
             hrows = [r.cpu().pin_memory() if r is not None else None for r in run.g_rows]
             hy = [torch.empty_like(y, device="cpu").pin_memory() for y in run.g_y]
             h2d += sum(r.numel() * r.element_size() for r in hrows if r is not None)
             d2h += sum(n * w.hidden * w.act_bytes for n in run.g_n)
 
-        def e2e_step():
-            with torch.cuda.stream(stream):
-                for layer in range(w.layers):
+        # every forward's inputs go up from pinned host memory and its outputs
+        # come back, on a copy stream beside the library's: the next
+        # forward's inputs while this one runs (once its own inputs are
+        # packed), its outputs once they are unpacked (before the next
+        # unpack reuses the buffers)
+        cs = torch.cuda.Stream()
+        ev_in, ev_packed, ev_out, ev_d2h = (torch.cuda.Event() for _ in range(4))
+
+        def copy_inputs():
+            with torch.cuda.stream(cs):
+                cs.wait_event(ev_packed)
+                if T:
+                    xall.copy_(hxall, non_blocking=True)
+                if grouped:
                     for p in range(w.num_peers):
-                        run.x[p].copy_(hx[p], non_blocking=True)
-                        if grouped and hrows[p] is not None:
+                        if hrows[p] is not None:
                             run.g_rows[p].copy_(hrows[p], non_blocking=True)
+                ev_in.record(cs)
+
+        def e2e_step():
+            for layer in range(w.layers):
+                stream.wait_event(ev_in)
+                with torch.cuda.stream(stream):
                     pack(layer)
-                    rc = fwd(layer)
-                    if rc:
-                        raise A.AfdError(rc, "afd_ffn_forward")
+                    ev_packed.record(stream)
+                copy_inputs()  # the next forward's inputs
+                rc = fwd(layer)
+                if rc:
+                    raise A.AfdError(rc, "afd_ffn_forward")
+                stream.wait_event(ev_d2h)
+                with torch.cuda.stream(stream):
                     if grouped:
                         run.unpack_grouped_all()
                     else:
                         run.unpack_all()
-                    for p, n in enumerate(w.seq_lens):
-                        if n:
-                            hout[p][:n].copy_(run.out[p][:n], non_blocking=True)
-                        if grouped and run.g_n[p]:
-                            hy[p][:run.g_n[p]].copy_(run.g_y[p][:run.g_n[p]], non_blocking=True)
-            stream.synchronize()
+                    ev_out.record(stream)
+                with torch.cuda.stream(cs):
+                    cs.wait_event(ev_out)
+                    if T:
+                        houtall[:T].copy_(outall[:T], non_blocking=True)
+                    if grouped:
+                        for p in range(w.num_peers):
+                            if run.g_n[p]:
+                                hy[p][:run.g_n[p]].copy_(run.g_y[p][:run.g_n[p]], non_blocking=True)
+                    ev_d2h.record(cs)
 
+        copy_inputs()  # the first forward's inputs
         for _ in range(max(2, args.warmup)):
             e2e_step()
+        stream.synchronize()
+        cs.synchronize()
         n_e2e = max(5, args.steps // 4)
         barrier(ws)
         t = time.perf_counter()
         for _ in range(n_e2e):
             e2e_step()
+        stream.synchronize()
+        cs.synchronize()
         t = (time.perf_counter() - t) / n_e2e
         t = max_over_ranks(t, ws)
         if run.poll() != 0:
             raise RuntimeError("device error in the end-to-end loop")
+        # the last outputs copied out are the last ones unpacked
+        if T and not torch.equal(houtall[:T], outall[:T].cpu()):
+            raise RuntimeError("end-to-end outputs differ from the device's")
         e2e = {"value": sum_over_ranks(tokens_step, ws) / t, "unit": "tokens/s",
                "ms_per_step": t * 1e3, "h2d_bytes_per_step": h2d * w.layers,
                "d2h_bytes_per_step": d2h * w.layers,
-               "note": "pinned host x -> device, pack, forward, unpack, device -> pinned host"}
+               "note": "pinned host x -> device, pack, forward, unpack, device -> pinned host; every "
+                       "forward's copies inside the timed region, on a copy stream: the next forward's "
+                       "inputs while this one runs, its outputs once unpacked"}
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and not grouped:

@@ -390,13 +390,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_gemm_tc(const __grid_constan
 }  // namespace
 
 cudaError_t launch_gemm_tc(const LaunchCtx& lc, const GemmArgs& a) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<int> attr_done[kMaxCachedDevices];
+  const cudaError_t e = smem_attr_once(k_gemm_tc, (int)kSmemBytes, attr_done);
+  if (e != cudaSuccess) return e;
   return launch_k(lc, k_gemm_tc, lc.num_sms, NUM_THREADS, kSmemBytes, a);
 }
 

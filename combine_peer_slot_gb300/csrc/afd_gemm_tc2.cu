@@ -583,8 +583,12 @@ k_gemm_tc2(const __grid_constant__ GemmPair pargs) {
 // launch waits across clusters, so every cluster must be resident together.
 template <bool kNarrow>
 int max_pairs(int num_sms) {
-  static int cached = 0;
-  if (cached) return cached;
+  static std::atomic<int> cached_dev[kMaxCachedDevices];
+  const int d = current_device();
+  if (d >= 0) {
+    const int c = cached_dev[d].load(std::memory_order_relaxed);
+    if (c) return c;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((num_sms / 2) * 2));
   cfg.blockDim = dim3(NUM_THREADS);
@@ -594,20 +598,17 @@ int max_pairs(int num_sms) {
     cudaGetLastError();
     n = 0;
   }
-  cached = n > 0 ? n : -1;
-  return cached;
+  const int c = n > 0 ? n : -1;
+  if (d >= 0) cached_dev[d].store(c, std::memory_order_relaxed);
+  return c;
 }
 
 template <bool kNarrow>
 cudaError_t launch_variant(const LaunchCtx& lc, const GemmPair& a) {
   constexpr size_t smem = Ring<kNarrow>::kSmemBytes;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc2<kNarrow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<int> attr_done[kMaxCachedDevices];
+  const cudaError_t e = smem_attr_once(k_gemm_tc2<kNarrow>, (int)smem, attr_done);
+  if (e != cudaSuccess) return e;
   int pairs = lc.num_sms / 2;  // persistent over the unit table
   if (a.nproj == 2) {
     const int m = max_pairs<kNarrow>(lc.num_sms);

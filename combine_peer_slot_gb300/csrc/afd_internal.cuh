@@ -12,6 +12,25 @@
 
 #include "../../include/afd.h"
 
+#include <atomic>
+
+// Launch settings the launchers cache (a kernel's shared-memory attribute,
+// occupancy figures) are per device: a process may hold contexts on several.
+constexpr int kMaxCachedDevices = 64;
+inline int current_device() {
+  int d = 0;
+  return cudaGetDevice(&d) == cudaSuccess && d >= 0 && d < kMaxCachedDevices ? d : -1;
+}
+// the kernel's dynamic shared memory limit raised to `bytes`, once per device
+template <typename K>
+cudaError_t smem_attr_once(K kernel, int bytes, std::atomic<int>* done /* [kMaxCachedDevices] */) {
+  const int d = current_device();
+  if (d >= 0 && done[d].load(std::memory_order_acquire)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && d >= 0) done[d].store(1, std::memory_order_release);
+  return e;
+}
+
 #define AFD_MAX_GROUPS 320   // routed experts (<= 256) + one shared group
 
 // ---------------------------------------------------------------------------

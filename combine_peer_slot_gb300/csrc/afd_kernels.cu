@@ -2907,8 +2907,12 @@ static FrGeom fr_geom(int hidden, int E, int epw) {
 // kernel and cluster shape); clusters beyond it would run in a second wave.
 template <int EPW, bool kSpread, bool kDev>
 static int fr_max_clusters(const FrGeom& geo, int num_sms) {
-  static int cached[kFrMaxC + 1] = {};
-  if (cached[geo.C]) return cached[geo.C];
+  static std::atomic<int> cached[kMaxCachedDevices][kFrMaxC + 1];
+  const int d = current_device();
+  if (d >= 0) {
+    const int c = cached[d][geo.C].load(std::memory_order_relaxed);
+    if (c) return c;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(geo.C * std::max(1, num_sms / geo.C)));
   cfg.blockDim = dim3((kFrWarps + 4) * 32);
@@ -2925,7 +2929,7 @@ static int fr_max_clusters(const FrGeom& geo, int num_sms) {
     cudaGetLastError();
     n = std::max(1, num_sms / geo.C);
   }
-  cached[geo.C] = n;
+  if (d >= 0) cached[d][geo.C].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -2935,13 +2939,9 @@ static cudaError_t launch_router_fused(const LaunchCtx& lc, const WinGeom& g, co
                                        const float* bias, int E, int k, int renorm, float scale,
                                        int32_t* hist, uint32_t go_token, int64_t go_timeout_ns) {
   const FrGeom geo = fr_geom(hidden, E, EPW);
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t err = cudaFuncSetAttribute(k_router_fused<EPW, kSpread, kDev>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, 232448 - 2048);
-    if (err != cudaSuccess) return err;
-    attr_done = true;
-  }
+  static std::atomic<int> attr_done[kMaxCachedDevices];
+  const cudaError_t err = smem_attr_once(k_router_fused<EPW, kSpread, kDev>, 232448 - 2048, attr_done);
+  if (err != cudaSuccess) return err;
   constexpr int BPI = kFrWarps * EPW / 16 / 2;
   const int nblocks = (f.total + kFrBlk - 1) / kFrBlk;
   const int ncl = std::max(1, std::min(fr_max_clusters<EPW, kSpread, kDev>(geo, lc.num_sms), (nblocks + BPI - 1) / BPI));

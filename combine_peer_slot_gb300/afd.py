@@ -80,6 +80,10 @@ SIGNATURES = [
     ("afd_announce_shutdown", _I, [_P, _I, _I, _U64]),
     ("afd_ffn_forward", _I, [_P, _I, _I, C.POINTER(C.c_int), C.POINTER(C.c_int), _I]),
     ("afd_unpack_split", _I, [_P, _I, _I, _P, _I, _U64]),
+    ("afd_pack_slots", _I, [_P, _I, C.POINTER(C.c_int32), _I, _I, C.POINTER(_P), C.POINTER(C.c_int32), _I,
+                            C.POINTER(_U64)]),
+    ("afd_unpack_splits", _I, [_P, _I, C.POINTER(C.c_int32), _I, C.POINTER(_P), C.POINTER(C.c_int32),
+                               C.POINTER(_U64)]),
     ("afd_pack_grouped", _I, [_P, _I, _I, _I, _P, _I, C.POINTER(C.c_int), _P, _I, _I, _U64]),
     ("afd_ffn_forward_grouped", _I, [_P, _I, _I, C.POINTER(C.c_int), C.POINTER(C.c_int),
                                      C.POINTER(C.c_int), _I]),
@@ -214,6 +218,20 @@ def afd_ffn_forward(ctx, layer, stage, seq_lens, slots):
 
 def afd_unpack_split(ctx, peer, stage, out_ptr, n_tokens, expect_seq):
     return lib().afd_unpack_split(ctx, peer, stage, out_ptr or None, n_tokens, expect_seq)
+
+
+def afd_pack_slots(ctx, peers, stage, layer, x_ptrs, n_tokens, with_shared, seqs):
+    n = len(peers)
+    return lib().afd_pack_slots(ctx, n, (C.c_int32 * n)(*peers), int(stage), int(layer),
+                                (_P * n)(*[p or None for p in x_ptrs]), (C.c_int32 * n)(*n_tokens),
+                                int(bool(with_shared)), (_U64 * n)(*seqs))
+
+
+def afd_unpack_splits(ctx, peers, stage, out_ptrs, n_tokens, expect_seqs):
+    n = len(peers)
+    return lib().afd_unpack_splits(ctx, n, (C.c_int32 * n)(*peers), int(stage),
+                                   (_P * n)(*[p or None for p in out_ptrs]), (C.c_int32 * n)(*n_tokens),
+                                   (_U64 * n)(*expect_seqs))
 
 
 def afd_pack_grouped(ctx, peer, stage, layer, rows_ptr, n_rows, group_list, x_ptr, n_tokens,

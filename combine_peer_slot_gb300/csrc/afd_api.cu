@@ -1189,6 +1189,73 @@ static int forward_impl(afd_ctx* ctx, int layer, FanIn& f, const PeerList* dev) 
   return AFD_OK;
 }
 
+int afd_pack_slots(afd_ctx* ctx, int n, const int32_t* peers, int stage, int layer,
+                   const void* const* x, const int32_t* n_tokens, int with_shared,
+                   const uint64_t* seq) {
+  if (!ctx || n < 0 || n > AFD_MAX_PEERS || (n > 0 && (!peers || !x || !n_tokens || !seq)))
+    return AFD_ERR_ARG;
+  const afd_config& c = ctx->cfg;
+  if (c.ffn_size >= 1) return AFD_ERR_ARG;  // ranks receive afd_attn_dispatch
+  if (stage < 0 || stage >= c.ring_depth) return AFD_ERR_ARG;
+  if (with_shared && c.shared_inter <= 0) return AFD_ERR_ARG;
+  PackList pl;
+  memset(&pl, 0, sizeof pl);
+  bool seen[AFD_MAX_PEERS] = {};
+  for (int i = 0; i < n; i++) {  // every argument before anything is launched
+    const int p = peers[i];
+    if (p < 0 || p >= c.num_peers || seen[p] || n_tokens[i] < 0) return AFD_ERR_ARG;
+    seen[p] = true;
+    if (n_tokens[i] > c.token_cap) return AFD_ERR_CAPACITY;
+    if (n_tokens[i] > 0) {
+      const int rc = check_dev_ptr(x[i]);
+      if (rc) return rc;
+      if (!aligned16(x[i])) return AFD_ERR_ARG;
+    }
+    if (seq[i] <= ctx->last_seq[(size_t)p * c.ring_depth + stage]) return AFD_ERR_SEQ;
+    pl.region[i] = p;
+    pl.n_rows[i] = n_tokens[i];
+    pl.rows[i] = n_tokens[i] > 0 ? static_cast<const uint4*>(x[i]) : nullptr;
+    pl.seq[i] = seq[i];
+  }
+  pl.n = n;
+  const int row_bytes = c.hidden * (ctx->act_f32 ? 4 : 2);
+  const int rc = cuda_fail(launch_pack_multi(ctx->lc(), ctx->geom, ctx->win[0], stage, layer, pl, with_shared,
+                                             row_bytes, c.num_experts),
+                           "pack");
+  if (!rc)
+    for (int i = 0; i < n; i++) ctx->last_seq[(size_t)peers[i] * c.ring_depth + stage] = seq[i];
+  return rc;
+}
+
+int afd_unpack_splits(afd_ctx* ctx, int n, const int32_t* peers, int stage, void* const* out,
+                      const int32_t* n_tokens, const uint64_t* expect_seq) {
+  if (!ctx || n < 0 || n > AFD_MAX_PEERS || (n > 0 && (!peers || !out || !n_tokens || !expect_seq)))
+    return AFD_ERR_ARG;
+  const afd_config& c = ctx->cfg;
+  if (stage < 0 || stage >= c.ring_depth) return AFD_ERR_ARG;
+  UnpackList ul;
+  memset(&ul, 0, sizeof ul);
+  for (int i = 0; i < n; i++) {
+    const int p = peers[i];
+    if (p < 0 || p >= c.num_peers || n_tokens[i] < 0) return AFD_ERR_ARG;
+    if (n_tokens[i] > c.token_cap) return AFD_ERR_CAPACITY;
+    if (n_tokens[i] > 0) {
+      const int rc = check_dev_ptr(out[i]);
+      if (rc) return rc;
+      if (!aligned16(out[i])) return AFD_ERR_ARG;
+    }
+    ul.region[i] = p;
+    ul.n_rows[i] = n_tokens[i];
+    ul.out[i] = n_tokens[i] > 0 ? static_cast<uint4*>(out[i]) : nullptr;
+    ul.seq[i] = expect_seq[i];
+  }
+  ul.n = n;
+  const int row_bytes = c.hidden * (ctx->act_f32 ? 4 : 2);
+  return cuda_fail(launch_unpack_multi(ctx->lc(), ctx->geom, ctx->win[1], stage, ul, row_bytes, c.num_experts,
+                                       ctx->ws.status, ctx->timeout()),
+                   "unpack");
+}
+
 int afd_unpack_split(afd_ctx* ctx, int peer, int stage, void* out, int n_tokens,
                      uint64_t expect_seq) {
   if (!ctx) return AFD_ERR_ARG;

@@ -102,6 +102,22 @@ struct GroupList {
   int32_t n[256];
 };
 
+// several peers' slots packed or unpacked in one launch (by value)
+struct PackList {
+  int n;
+  int region[AFD_MAX_PEERS];
+  int n_rows[AFD_MAX_PEERS];
+  const uint4* rows[AFD_MAX_PEERS];
+  uint64_t seq[AFD_MAX_PEERS];
+};
+struct UnpackList {
+  int n;
+  int region[AFD_MAX_PEERS];
+  int n_rows[AFD_MAX_PEERS];
+  uint4* out[AFD_MAX_PEERS];
+  uint64_t seq[AFD_MAX_PEERS];  // the flag value each expects
+};
+
 // window geometry (both windows share it)
 struct WinGeom {
   int64_t flags_bytes, slot_bytes;
@@ -573,6 +589,11 @@ cudaError_t launch_return_header(const LaunchCtx& lc, const WinGeom& g, uint8_t*
                                  int k);
 // n rows of the return slot's field; the header must carry expect_tokens
 // tokens (and expect_routed routed rows unless it is -1)
+cudaError_t launch_pack_multi(const LaunchCtx& lc, const WinGeom& g, uint8_t* win, int stage, int layer,
+                              const PackList& pl, int with_shared, int row_bytes, int num_experts);
+cudaError_t launch_unpack_multi(const LaunchCtx& lc, const WinGeom& g, const uint8_t* ret, int stage,
+                                const UnpackList& ul, int row_bytes, int num_experts, int32_t* status,
+                                int64_t timeout_ns);
 cudaError_t launch_unpack(const LaunchCtx& lc, const WinGeom& g, const uint8_t* ret, int region,
                           int stage, void* out, int n, int row_bytes, int num_experts,
                           uint64_t expect_seq, int32_t* status, int64_t timeout_ns, int64_t field,

@@ -137,11 +137,11 @@ __global__ void k_pack_payload(uint8_t* win, WinGeom g, int region, int stage,
   }
 }
 
-__global__ void k_pack_header(uint8_t* win, WinGeom g, int region, int stage, int layer, int n,
-                              int with_shared, int num_experts, uint64_t seq, int shutdown,
-                              int routed_tokens, GroupList gl) {
-  grid_dep_wait();
-  grid_dep_launch();
+// the header of slot (region, stage), then (after the CTA's stores) its
+// flag = seq; one CTA
+__device__ void write_dispatch_header(uint8_t* win, const WinGeom& g, int region, int stage, int layer, int n,
+                                      int with_shared, int num_experts, uint64_t seq, int shutdown,
+                                      int routed_tokens, const GroupList* gl) {
   uint8_t* slot = slot_ptr(win, g, region, stage);
   int32_t* h = reinterpret_cast<int32_t*>(slot + g.header);
   for (int i = threadIdx.x; i < AFD_HEADER_FIXED_WORDS + num_experts; i += blockDim.x) {
@@ -159,7 +159,7 @@ __global__ void k_pack_header(uint8_t* win, WinGeom g, int region, int stage, in
       case 9: v = with_shared ? n : 0; break;
       case 10: v = num_experts; break;
       case 11: v = AFD_HEADER_FIXED_WORDS + num_experts; break;
-      default: v = gl.n[i - AFD_HEADER_FIXED_WORDS];
+      default: v = gl ? gl->n[i - AFD_HEADER_FIXED_WORDS] : 0;
     }
     h[i] = v;
   }
@@ -169,6 +169,52 @@ __global__ void k_pack_header(uint8_t* win, WinGeom g, int region, int stage, in
     uint64_t* flag = reinterpret_cast<uint64_t*>(win) + (int64_t)region * g.ring_depth + stage;
     st_release_u64(flag, seq);
   }
+}
+
+__global__ void k_pack_header(uint8_t* win, WinGeom g, int region, int stage, int layer, int n,
+                              int with_shared, int num_experts, uint64_t seq, int shutdown,
+                              int routed_tokens, const __grid_constant__ GroupList gl) {
+  grid_dep_wait();
+  grid_dep_launch();
+  write_dispatch_header(win, g, region, stage, layer, n, with_shared, num_experts, seq, shutdown,
+                        routed_tokens, &gl);
+}
+
+// Several peers' packs (afd_pack_slots): CTA row y = entry y of the list,
+// its CTAs striding over that peer's vectors; then a CTA per entry writes
+// its header and releases its flag.
+__global__ void k_pack_payload_multi(uint8_t* win, WinGeom g, int stage, const __grid_constant__ PackList pl,
+                                     int with_shared, int row_bytes) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int e = blockIdx.y;
+  if (e >= pl.n) return;
+  uint8_t* slot = slot_ptr(win, g, pl.region[e], stage);
+  uint4* rx = reinterpret_cast<uint4*>(slot + g.routed_x);
+  uint4* sx = reinterpret_cast<uint4*>(slot + g.shared_x);
+  int32_t* sidx = reinterpret_cast<int32_t*>(slot + g.shared_idx);
+  const uint4* __restrict__ rows = pl.rows[e];
+  const int n = pl.n_rows[e];
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t nvec = (int64_t)n * row_bytes / 16;
+  for (int64_t i = i0; i < nvec; i += stride) {
+    const uint4 v = rows[i];
+    rx[i] = v;
+    if (with_shared) sx[i] = v;
+  }
+  if (with_shared)
+    for (int64_t i = i0; i < n; i += stride) sidx[i] = (int32_t)i;
+}
+
+__global__ void k_pack_header_multi(uint8_t* win, WinGeom g, int stage, int layer,
+                                    const __grid_constant__ PackList pl, int with_shared, int num_experts) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int e = blockIdx.x;
+  if (e >= pl.n) return;
+  write_dispatch_header(win, g, pl.region[e], stage, layer, pl.n_rows[e], with_shared, num_experts,
+                        pl.seq[e], 0, 0, nullptr);
 }
 
 // ---------------------------------------------------------------------------
@@ -2571,13 +2617,11 @@ __global__ void k_return_header(uint8_t* ret, WinGeom g, const __grid_constant__
 
 // Unpack: block-local bounded wait on the return flag and header check by
 // thread 0, then the block copies its share of the rows.
-__global__ void __launch_bounds__(kThreads)
-k_unpack(const uint8_t* ret, WinGeom g, int region, int stage, uint4* out, int n, int row_bytes,
-         int E, uint64_t expect_seq, int32_t* status, int64_t timeout_ns, int64_t field,
-         int expect_tokens, int expect_routed) {
-  grid_dep_wait();
-  grid_dep_launch();
-  __shared__ int ok;
+// thread 0 of the CTA: bounded wait for the return flag of (region, stage)
+// to reach expect_seq, then the header checks; the CTA's verdict in *ok
+__device__ void unpack_check(const uint8_t* ret, const WinGeom& g, int region, int stage, int E,
+                             uint64_t expect_seq, int32_t* status, int64_t timeout_ns,
+                             int expect_tokens, int expect_routed, int* ok) {
   if (threadIdx.x == 0) {
     int e = read_status(status) ? -1 : 0;
     if (!e) {
@@ -2605,12 +2649,42 @@ k_unpack(const uint8_t* ret, WinGeom g, int region, int stage, uint4* out, int n
       }
       if (e > 0) set_error(status, e);
     }
-    ok = (e == 0);
+    *ok = (e == 0);
   }
   __syncthreads();
+}
+
+__global__ void __launch_bounds__(kThreads)
+k_unpack(const uint8_t* ret, WinGeom g, int region, int stage, uint4* out, int n, int row_bytes,
+         int E, uint64_t expect_seq, int32_t* status, int64_t timeout_ns, int64_t field,
+         int expect_tokens, int expect_routed) {
+  grid_dep_wait();
+  grid_dep_launch();
+  __shared__ int ok;
+  unpack_check(ret, g, region, stage, E, expect_seq, status, timeout_ns, expect_tokens, expect_routed, &ok);
   if (!ok) return;
   const uint4* src = reinterpret_cast<const uint4*>(slot_ptr(ret, g, region, stage) + field);
   const int64_t nvec = (int64_t)n * row_bytes / 16;
+  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec;
+       v += (int64_t)gridDim.x * blockDim.x)
+    out[v] = src[v];
+}
+
+// Several peers' unpacks (afd_unpack_splits): CTA row y = entry y, each CTA
+// checks its entry's flag and header, then copies its share of the rows.
+__global__ void __launch_bounds__(kThreads)
+k_unpack_multi(const uint8_t* ret, WinGeom g, int stage, const __grid_constant__ UnpackList ul, int row_bytes,
+               int E, int32_t* status, int64_t timeout_ns) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int e = blockIdx.y;
+  if (e >= ul.n) return;
+  __shared__ int ok;
+  unpack_check(ret, g, ul.region[e], stage, E, ul.seq[e], status, timeout_ns, ul.n_rows[e], -1, &ok);
+  if (!ok) return;
+  const uint4* src = reinterpret_cast<const uint4*>(slot_ptr(ret, g, ul.region[e], stage) + g.routed_x);
+  uint4* out = ul.out[e];
+  const int64_t nvec = (int64_t)ul.n_rows[e] * row_bytes / 16;
   for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec;
        v += (int64_t)gridDim.x * blockDim.x)
     out[v] = src[v];
@@ -3090,6 +3164,29 @@ cudaError_t launch_return_header(const LaunchCtx& lc, const WinGeom& g, uint8_t*
                                  const uint8_t*, const FanIn& f, const DevWS& ws, int E, int k) {
   return launch_k(lc, f.dev ? k_return_header<true> : k_return_header<false>, f.n_peers, 128, 0,
                   ret, g, f, ws, E, k);
+}
+
+cudaError_t launch_pack_multi(const LaunchCtx& lc, const WinGeom& g, uint8_t* win, int stage, int layer,
+                              const PackList& pl, int with_shared, int row_bytes, int num_experts) {
+  if (pl.n == 0) return cudaSuccess;
+  int64_t most = 0;
+  for (int e = 0; e < pl.n; e++) most = std::max<int64_t>(most, (int64_t)pl.n_rows[e] * row_bytes / 16);
+  const int gx = std::max(1, grid_for(most, kThreads * 4, lc.num_sms * 4));
+  cudaError_t err = launch_k(lc, k_pack_payload_multi, dim3((unsigned)gx, (unsigned)pl.n), kThreads, 0, win, g,
+                             stage, pl, with_shared, row_bytes);
+  if (err != cudaSuccess) return err;
+  return launch_k(lc, k_pack_header_multi, pl.n, 128, 0, win, g, stage, layer, pl, with_shared, num_experts);
+}
+
+cudaError_t launch_unpack_multi(const LaunchCtx& lc, const WinGeom& g, const uint8_t* ret, int stage,
+                                const UnpackList& ul, int row_bytes, int num_experts, int32_t* status,
+                                int64_t timeout_ns) {
+  if (ul.n == 0) return cudaSuccess;
+  int64_t most = 0;
+  for (int e = 0; e < ul.n; e++) most = std::max<int64_t>(most, (int64_t)ul.n_rows[e] * row_bytes / 16);
+  const int gx = std::max(1, grid_for(most, kThreads * 4, lc.num_sms * 4));
+  return launch_k(lc, k_unpack_multi, dim3((unsigned)gx, (unsigned)ul.n), kThreads, 0, ret, g, stage, ul,
+                  row_bytes, num_experts, status, timeout_ns);
 }
 
 cudaError_t launch_unpack(const LaunchCtx& lc, const WinGeom& g, const uint8_t* ret, int region,

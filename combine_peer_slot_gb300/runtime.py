@@ -68,11 +68,24 @@ class Runner:
         self.last_seq = {}
         dt = torch.bfloat16 if w.act == "bf16" else torch.float32
         self.out = [torch.empty((max(n, 1), w.hidden), dtype=dt, device=device) for n in w.seq_lens]
+        self.batched = True  # pack / unpack all listed peers in one call (afd_pack_slots / afd_unpack_splits)
 
     # -- attention side, simulated ------------------------------------------------
     def pack_all(self, layer=0, stage=0, peers=None, with_shared=None):
         ws = (self.w.shared_inter > 0) if with_shared is None else with_shared
-        for p in (range(self.w.num_peers) if peers is None else peers):
+        peers = list(range(self.w.num_peers)) if peers is None else list(peers)
+        if self.batched:
+            seqs = [self.seq + 1 + i for i in range(len(peers))]
+            ns = [self.w.seq_lens[p] for p in peers]
+            rc = A.afd_pack_slots(self.ctx, peers, stage, layer,
+                                  [self.x[p].data_ptr() if n else 0 for p, n in zip(peers, ns)], ns, ws, seqs)
+            if rc:
+                raise A.AfdError(rc, "afd_pack_slots")
+            self.seq += len(peers)
+            for p, s in zip(peers, seqs):
+                self.last_seq[(p, stage)] = s
+            return
+        for p in peers:
             self.seq += 1
             n = self.w.seq_lens[p]
             rc = A.afd_pack_slot(self.ctx, p, stage, layer, self.x[p].data_ptr() if n else 0, n,
@@ -87,7 +100,16 @@ class Runner:
         return A.afd_ffn_forward(self.ctx, layer, stage, lens, slots)
 
     def unpack_all(self, stage=0, peers=None):
-        for p in (range(self.w.num_peers) if peers is None else peers):
+        peers = list(range(self.w.num_peers)) if peers is None else list(peers)
+        if self.batched:
+            ns = [self.w.seq_lens[p] for p in peers]
+            rc = A.afd_unpack_splits(self.ctx, peers, stage,
+                                     [self.out[p].data_ptr() if n else 0 for p, n in zip(peers, ns)], ns,
+                                     [self.last_seq[(p, stage)] for p in peers])
+            if rc:
+                raise A.AfdError(rc, "afd_unpack_splits")
+            return self.out
+        for p in peers:
             n = self.w.seq_lens[p]
             rc = A.afd_unpack_split(self.ctx, p, stage, self.out[p].data_ptr() if n else 0, n,
                                     self.last_seq[(p, stage)])

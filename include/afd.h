@@ -318,6 +318,24 @@ int afd_ffn_forward(afd_ctx* ctx, int layer, int stage, const int* seq_lens, con
 int afd_unpack_split(afd_ctx* ctx, int peer, int stage, void* out, int n_tokens,
                      uint64_t expect_seq);
 
+/* afd_pack_slot for n peers of one stage in one call: peers[i] (distinct),
+ * x[i] (host array of device pointers, 16-byte aligned; NULL for 0 tokens),
+ * n_tokens[i] and seq[i] (host arrays), with_shared for all.  Two launches
+ * whatever n: every payload, then every header with its flag released after
+ * that peer's payload.  Every argument is checked before anything is
+ * launched; the errors are afd_pack_slot's.  A process that hosts several
+ * attention peers (or the peers' emulation) packs a step in one call. */
+int afd_pack_slots(afd_ctx* ctx, int n, const int32_t* peers, int stage, int layer,
+                   const void* const* x, const int32_t* n_tokens, int with_shared,
+                   const uint64_t* seq);
+
+/* afd_unpack_split for n peers of one stage in one call (host arrays of
+ * peers, device output pointers, token counts and expected seqs); one
+ * launch, each peer's rows copied after its own flag and header check.
+ * Errors as afd_unpack_split. */
+int afd_unpack_splits(afd_ctx* ctx, int n, const int32_t* peers, int stage, void* const* out,
+                      const int32_t* n_tokens, const uint64_t* expect_seq);
+
 /* ---- grouped form: the Attention side routes ------------------------------
  * [RFC]: Async GPU Connector, "Data flow" steps 1-4 and "Attention gate and
  * FFN expert compute": the Attention side computes the gate, sorts the

@@ -137,6 +137,30 @@ def test_host_side_errors():
     assert run.poll() == 0
 
 
+def test_batched_pack_unpack_host_side_errors():
+    """afd_pack_slots / afd_unpack_splits check every entry before launching
+    anything: a refused call leaves the slots and the seqs as they were."""
+    run = make_run()
+    cap, H = run.w.token_cap, run.w.hidden
+    x0, x1 = run.x[0].data_ptr(), run.x[1].data_ptr()
+    host = torch.zeros((5, H), dtype=torch.bfloat16)
+    assert A.afd_pack_slots(run.ctx, [0, 0], 0, 0, [x0, x0], [5, 5], 1, [10, 11]) == A.AFD_ERR_ARG
+    assert A.afd_pack_slots(run.ctx, [0, 1], 0, 0, [x0, host.data_ptr()], [5, 5], 1, [10, 11]) == \
+        A.AFD_ERR_NOT_DEVICE
+    assert A.afd_pack_slots(run.ctx, [0, 1], 0, 0, [x0, x1], [5, cap + 1], 1, [10, 11]) == A.AFD_ERR_CAPACITY
+    assert A.afd_pack_slots(run.ctx, [0, 1], 1, 0, [x0, x1], [5, 5], 1, [10, 11]) == A.AFD_ERR_ARG
+    run.pack_all(0)
+    s0 = run.last_seq[(0, 0)]
+    assert A.afd_pack_slots(run.ctx, [1, 0], 0, 0, [x1, x0], [5, 5], 1, [10**6, s0]) == A.AFD_ERR_SEQ
+    out = torch.empty((5, H), dtype=torch.bfloat16, device="cuda")
+    assert A.afd_unpack_splits(run.ctx, [0], 0, [host.data_ptr()], [5], [s0]) == A.AFD_ERR_NOT_DEVICE
+    assert A.afd_unpack_splits(run.ctx, [0], 0, [out.data_ptr()], [cap + 1], [s0]) == A.AFD_ERR_CAPACITY
+    # the refused packs left the slots alone: the step packed above still runs
+    assert run.forward(0) == 0
+    run.unpack_all()
+    assert run.poll() == 0
+
+
 def test_unpack_wrong_seq():
     run = make_run()
     run.pack_all(0)

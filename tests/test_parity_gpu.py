@@ -106,6 +106,27 @@ def test_gemm_pair_equals_split_gemms(workload):
     assert np.array_equal(wins[0], wins[1])
 
 
+def test_batched_pack_unpack_equal_per_peer_calls():
+    """afd_pack_slots / afd_unpack_splits (all peers in one call, an empty
+    peer among them) leave the same dispatch and return windows and the same
+    unpacked rows as afd_pack_slot / afd_unpack_split per peer."""
+    w = W.custom("fanin", seq_lens=[37, 0, 91, 5])
+    got = []
+    for batched in (True, False):
+        run = R.Runner(w, max_total_tokens=w.total_tokens, layers=1)
+        run.batched = batched
+        run.pack_all(0)
+        disp = run.window(A.AFD_DIR_DISPATCH).cpu().numpy()
+        assert run.forward(0) == 0
+        outs = [o[:n].cpu() for o, n in zip(run.unpack_all(), w.seq_lens)]
+        assert run.poll() == 0
+        got.append((disp, run.window(A.AFD_DIR_RETURN).cpu().numpy(), outs))
+        run.close()
+    assert np.array_equal(got[0][0], got[1][0])
+    assert np.array_equal(got[0][1], got[1][1])
+    assert all(torch.equal(a, b) for a, b in zip(got[0][2], got[1][2]))
+
+
 def test_fanin_reordered_with_empty_peer():
     w = W.custom("fanin", seq_lens=[37, 0, 91, 5])
     run = R.Runner(w, canary=True)

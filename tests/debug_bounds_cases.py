@@ -4,7 +4,8 @@ tests/test_debug_bounds_gpu.py; prints one JSON line.
 
 Clean runs: the debug build gives the oracle's results on the token form
 (both gather orders, the three GEMM engines) and the grouped form, and no
-check fails.  Planted runs: for each check site, afd_debug_plant makes every
+check fails; nor on the full-size V2-Lite prefill fan-in and all 26 layers of
+the decode-shaped pass.  Planted runs: for each check site, afd_debug_plant makes every
 check there fail on valid indices (the bound is taken as 0, so the access is
 skipped and no index out of range is used); the step must then report
 AFD_ERR_BOUNDS and the record must name the site, after which a clean step
@@ -54,6 +55,22 @@ def clean_grouped():
     return {"err": err, "bounds": rc[0]}
 
 
+def clean_full_size(name):
+    """A full-size workload through the debug build (every layer of it): no
+    check fails and every step ends without error (its outputs are compared
+    with the oracle by the release build's parity tests)."""
+    w = W.get(name)
+    run = R.Runner(w, max_total_tokens=w.total_tokens)
+    for layer in range(w.layers):
+        run.pack_all(layer)
+        assert run.forward(layer) == A.AFD_OK
+        run.unpack_all()
+    st = run.poll()
+    rc = A.afd_debug_bounds(run.ctx)
+    run.close()
+    return {"step": st, "bounds": rc[0], "layers": w.layers}
+
+
 def planted(site, name, gemm=A.AFD_GEMM_TENSOR):
     """One step with `site` planted, then a clean step on the same context."""
     w = workload(name)
@@ -90,6 +107,8 @@ def main():
         "clean_fanin_simt": clean_token_form("fanin", A.AFD_GEMM_SIMT),
         "clean_token_order": clean_token_form("token_order", A.AFD_GEMM_TENSOR),
         "clean_grouped": clean_grouped(),
+        "full_v2lite_prefill": clean_full_size("v2lite_prefill"),
+        "full_decode": clean_full_size("decode"),
         "planted": {
             "gather_inv": planted(A.AFD_DBG_GATHER_INV, "token_order"),
             "gather_perm": planted(A.AFD_DBG_GATHER_PERM, "fanin"),

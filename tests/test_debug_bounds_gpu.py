@@ -40,6 +40,13 @@ def test_debug_build_matches_oracle_without_failed_checks(debug_results, case):
     assert r["err"] <= 2e-2
 
 
+@pytest.mark.parametrize("case", ["full_v2lite_prefill", "full_decode"])
+def test_debug_build_full_size_without_failed_checks(debug_results, case):
+    r = debug_results[case]
+    assert r["step"] == A.AFD_OK
+    assert r["bounds"] == A.AFD_OK
+
+
 SITES = {"gather_inv": A.AFD_DBG_GATHER_INV, "gather_perm": A.AFD_DBG_GATHER_PERM,
          "gather_grouped": A.AFD_DBG_GATHER_GROUPED, "combine_inv": A.AFD_DBG_COMBINE_INV,
          "scatter_inv": A.AFD_DBG_SCATTER_INV, "gemm_out_tc2": A.AFD_DBG_GEMM_OUT,

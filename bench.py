@@ -564,8 +564,9 @@ def run_serve(args, ws, rank, local):
         raise RuntimeError(f"device error in the timed region: {A.strerror(status)}")
     log, served = A.afd_serve_log(run.ctx, 64)
     assert [r[1] for r in log[-L:]] == list(range(L)), "items served out of layer order"
-    # the pack kernels are the Attention side's, not the step's
-    pack_launches = L * w.num_peers * 2
+    # the pack kernels are the Attention side's, not the step's: two launches
+    # per stage with the batched packs, two per peer and stage without
+    pack_launches = L * 2 * (1 if run.batched else w.num_peers)
     launches = {m: v - pack_launches * args.steps for m, v in launches.items()}
     launches["graph"] = graph_kernels * args.steps
     per = {m: max_over_ranks(v / args.steps, ws) for m, v in ms.items()}

@@ -1711,11 +1711,12 @@ k_router_fused(const uint8_t* win, WinGeom g, const __grid_constant__ FanIn fp, 
 }
 
 // ---------------------------------------------------------------------------
-// a2 plan, part 1 (one CTA): per-expert counts and exclusive offsets from the
-// router CTAs' histograms (bincount + cumsum, Async GPU Connector, "Data
-// flow" step 1), each router CTA's base position within each expert's
-// segment (base[b][e] = sum of hist[b'][e] for b' < b), the zeroed per-peer
-// counts, and the tile tables of both grouped GEMMs.
+// a2 plan for larger fan-ins (one CTA): per-expert counts and exclusive
+// offsets from the router blocks' histograms (bincount + cumsum, Async GPU
+// Connector, "Data flow" step 1), each router block's base position within
+// each expert's segment (base[b][e] = sum of hist[b'][e] for b' < b), the
+// zeroed per-peer counts, and the tile tables of both grouped GEMMs; the
+// stable ranks follow in k_rank_gather.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
 #pragma unroll

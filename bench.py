@@ -92,19 +92,19 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
 
 class ClockSampler:
     def __init__(self, device_index):
-        self.path = tempfile.mktemp(prefix="afd_clocks_", suffix=".csv")
+        fd, self.path = tempfile.mkstemp(prefix="afd_clocks_", suffix=".csv")
+        self.f = os.fdopen(fd, "w")
         self.proc = None
         self.dev = device_index
 
     def __enter__(self):
         try:
-            self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={CLOCK_FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
-        except (OSError, FileNotFoundError):
+        except OSError:
             self.proc = None
         return self
 
@@ -115,10 +115,12 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-            self.f.close()
+                self.proc.wait()
+        self.f.close()
 
     def summary(self):
-        if not self.proc or not os.path.exists(self.path):
+        if not self.proc:
+            os.unlink(self.path)
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]

@@ -42,7 +42,8 @@ def test_all_peers_empty():
     dict(num_experts=8, topk=8, hidden=256, inter=96, shared_inter=96, seq_lens=[19, 1, 33]),
     # without a shared expert a token's weighted sum of its k expert outputs
     # can cancel to far less than each of them; the expert outputs reach
-    # the combine in fp32, so its one rounding is all the output sees
+    # the combine as 24-bit floats (16 significant bits, 2^-16 relative
+    # rounding), far finer than the output's bf16 rounding
     dict(num_experts=8, topk=8, hidden=256, inter=96, shared_inter=0, seq_lens=[19, 1, 33]),
     dict(num_experts=16, topk=2, hidden=4096, inter=128, shared_inter=64, seq_lens=[33, 20]),
     dict(num_experts=64, topk=6, hidden=3072, inter=64, shared_inter=64, seq_lens=[25]),

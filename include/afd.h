@@ -564,7 +564,7 @@ int afd_check_canaries(afd_ctx* ctx, int* window, int64_t* offset);
  * used), site 0 none: a test of the reporting path.  Both return
  * AFD_ERR_UNSUPPORTED in the release build, AFD_ERR_ARG / AFD_ERR_CUDA on
  * failure. */
-#define AFD_DBG_GATHER_INV 1     /* k_gather, token order: inv[t, j] < T * k */
+#define AFD_DBG_GATHER_INV 1     /* k_rank_gather (token order): inv[t, j] < T * k */
 #define AFD_DBG_GATHER_PERM 2    /* k_gather, position order: perm[r] < T * k */
 #define AFD_DBG_GATHER_GROUPED 3 /* k_gather, grouped form: row position < routed rows */
 #define AFD_DBG_COMBINE_INV 4    /* k_combine: inv[t, j] < T * k */

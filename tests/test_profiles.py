@@ -73,3 +73,27 @@ def test_bench_traffic_from_current_summaries():
     for workload in ("v2lite_prefill", "decode"):
         t = bench.traffic_from_profile("gemm", workload)
         assert t is not None and t > 1e9, workload
+
+
+def test_tracked_bench_lines_meet_the_targets():
+    """The tracked bench lines: V2-Lite prefill at >= 60 % of its tensor
+    roofline, the 26-layer decode pass at >= 70 % of its HBM roofline, each
+    with clocks sampled under load and no slowdown reason, an end-to-end
+    figure through host buffers and the dominant kernel's DRAM traffic."""
+    import json
+    for fname, bound, target in (("bench_v2lite_prefill.json", "tensor", 0.60),
+                                 ("bench_decode_26layers.json", "hbm", 0.70)):
+        with open(os.path.join(ROOT, "profiles", fname)) as f:
+            line = json.load(f)
+        pr = line["path_roofline"]
+        assert pr["bound"] == bound and pr["frac"] >= target, (fname, pr["frac"])
+        assert abs(pr["roofline_ms"] / line["ms_per_step"] - pr["frac"]) < 1e-9
+        clk = line["clocks"]
+        assert clk["samples"] >= 1 and clk["sm_mhz"] >= 0.95 * clk["sm_max_mhz"], clk
+        assert not set(clk["reasons"]) & {"hw_slowdown", "hw_thermal_slowdown",
+                                          "sw_thermal_slowdown"}, clk
+        assert line["warmup"] >= 3 and line["gpu_launches"] > 0
+        e2e = line["e2e"]
+        assert e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
+        assert e2e["ms_per_step"] >= line["ms_per_step"]
+        assert line["roofline"]["traffic"] and 0 < line["roofline"]["frac"] <= 1.05
